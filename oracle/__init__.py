@@ -1,0 +1,167 @@
+"""fp64 CPU oracle for exact softmax attention (forward).
+
+TEST INFRASTRUCTURE ONLY.  Callers allowed: the tests, the package smoke check
+and the benchmark's CPU-baseline leg.  The CUDA path never imports this package
+and this package never imports the CUDA path; the two share only the seeded
+input generators.
+
+Every routine wraps ``oracle.c``, plain C in fp64.  See that file for the
+definition it computes and the passages of the pages it follows.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+
+from . import build as _build
+
+_c_i64p = ctypes.POINTER(ctypes.c_int64)
+_c_dp = ctypes.POINTER(ctypes.c_double)
+_c_u16p = ctypes.POINTER(ctypes.c_uint16)
+
+
+def _u16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError("oracle inputs are bf16 bit patterns (uint16)")
+    return a
+
+
+def _ptr(a, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+class Oracle:
+    """The oracle library at ``path`` (the built ``oracle.c``)."""
+
+    def __init__(self, path: str):
+        L = ctypes.CDLL(path)
+        L.oracle_cpu_count.restype = ctypes.c_int
+        L.oracle_attn_rows.restype = ctypes.c_int
+        L.oracle_attn_rows.argtypes = [_c_u16p, _c_u16p, _c_u16p, _c_i64p, ctypes.c_int64,
+                                       ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
+                                       _c_i64p, ctypes.c_int64, _c_dp, _c_dp, ctypes.c_int,
+                                       ctypes.POINTER(ctypes.c_int)]
+        L.oracle_attn_probs.restype = ctypes.c_int64
+        L.oracle_attn_probs.argtypes = [_c_u16p, _c_u16p, _c_i64p, ctypes.c_int64, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_double, ctypes.c_int,
+                                        ctypes.c_int64, ctypes.c_int, ctypes.c_int64, _c_dp]
+        L.oracle_softmax_merge.restype = ctypes.c_int
+        L.oracle_softmax_merge.argtypes = [_c_dp, ctypes.c_int64, _c_i64p, ctypes.c_int64,
+                                           _c_dp, _c_dp, _c_dp]
+        L.oracle_attn_online.restype = ctypes.c_int
+        L.oracle_attn_online.argtypes = [_c_u16p, _c_u16p, _c_u16p, _c_i64p, ctypes.c_int64,
+                                         ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
+                                         _c_i64p, ctypes.c_int64, ctypes.c_int64, _c_dp, _c_dp]
+        self.lib = L
+        self.path = path
+
+    def cpu_count(self) -> int:
+        return int(self.lib.oracle_cpu_count())
+
+    def attn_rows(self, q, k, v, cu_seqlens, rows, scale: float, causal: bool,
+                  nthreads: int = 0):
+        """O (fp64 [n, d]) and LSE (fp64 [n]) of the given (seq, head, row) triples.
+
+        q, k, v: uint16 bf16 bits, [tokens, H, d].  Returns (o, lse, threads_used).
+        """
+        q, k, v = _u16(q), _u16(k), _u16(v)
+        tokens, H, d = q.shape
+        cu = np.ascontiguousarray(cu_seqlens, dtype=np.int64)
+        rows = np.ascontiguousarray(rows, dtype=np.int64).reshape(-1, 3)
+        n = rows.shape[0]
+        o = np.zeros((n, d), dtype=np.float64)
+        lse = np.zeros(n, dtype=np.float64)
+        used = ctypes.c_int(0)
+        st = self.lib.oracle_attn_rows(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16),
+                                       _ptr(v, ctypes.c_uint16), _ptr(cu, ctypes.c_int64),
+                                       len(cu) - 1, H, d, float(scale), int(bool(causal)),
+                                       _ptr(rows, ctypes.c_int64), n, _ptr(o, ctypes.c_double),
+                                       _ptr(lse, ctypes.c_double), int(nthreads),
+                                       ctypes.byref(used))
+        if st != 0:
+            raise ValueError(f"oracle_attn_rows failed with status {st}")
+        return o, lse, used.value
+
+    def attn_probs(self, q, k, cu_seqlens, seq: int, h: int, i: int, scale: float,
+                   causal: bool):
+        """The probability row P_i (fp64) of one query row."""
+        q, k = _u16(q), _u16(k)
+        tokens, H, d = q.shape
+        cu = np.ascontiguousarray(cu_seqlens, dtype=np.int64)
+        L = int(cu[seq + 1] - cu[seq])
+        p = np.zeros(max(L, 1), dtype=np.float64)
+        n = self.lib.oracle_attn_probs(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16),
+                                       _ptr(cu, ctypes.c_int64), len(cu) - 1, H, d,
+                                       float(scale), int(bool(causal)), int(seq), int(h),
+                                       int(i), _ptr(p, ctypes.c_double))
+        if n < 0:
+            raise ValueError(f"oracle_attn_probs failed with status {n}")
+        return p[:n]
+
+    def softmax_merge(self, x, cuts):
+        """softmax(x) by segment-wise (m, l, f) merging at the given cut points.
+
+        Returns (softmax, m, l)."""
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        cuts = np.ascontiguousarray(cuts, dtype=np.int64)
+        out = np.zeros_like(x)
+        m = ctypes.c_double(0)
+        l = ctypes.c_double(0)
+        st = self.lib.oracle_softmax_merge(_ptr(x, ctypes.c_double), x.size,
+                                           _ptr(cuts, ctypes.c_int64) if cuts.size else None,
+                                           cuts.size, _ptr(out, ctypes.c_double),
+                                           ctypes.byref(m), ctypes.byref(l))
+        if st != 0:
+            raise ValueError(f"oracle_softmax_merge failed with status {st}")
+        return out, m.value, l.value
+
+    def attn_online(self, q, k, v, cu_seqlens, rows, scale: float, causal: bool, bc: int):
+        """O and LSE of the given rows by the block-wise online loop (block size bc)."""
+        q, k, v = _u16(q), _u16(k), _u16(v)
+        tokens, H, d = q.shape
+        cu = np.ascontiguousarray(cu_seqlens, dtype=np.int64)
+        rows = np.ascontiguousarray(rows, dtype=np.int64).reshape(-1, 3)
+        n = rows.shape[0]
+        o = np.zeros((n, d), dtype=np.float64)
+        lse = np.zeros(n, dtype=np.float64)
+        st = self.lib.oracle_attn_online(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16),
+                                         _ptr(v, ctypes.c_uint16), _ptr(cu, ctypes.c_int64),
+                                         len(cu) - 1, H, d, float(scale), int(bool(causal)),
+                                         _ptr(rows, ctypes.c_int64), n, int(bc),
+                                         _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double))
+        if st != 0:
+            raise ValueError(f"oracle_attn_online failed with status {st}")
+        return o, lse
+
+
+_default = None
+
+
+def default() -> Oracle:
+    """The oracle built from this package's ``oracle.c``."""
+    global _default
+    if _default is None:
+        _default = Oracle(_build.build())
+    return _default
+
+
+def cpu_count() -> int:
+    return default().cpu_count()
+
+
+def attn_rows(*a, **kw):
+    return default().attn_rows(*a, **kw)
+
+
+def attn_probs(*a, **kw):
+    return default().attn_probs(*a, **kw)
+
+
+def softmax_merge(*a, **kw):
+    return default().softmax_merge(*a, **kw)
+
+
+def attn_online(*a, **kw):
+    return default().attn_online(*a, **kw)

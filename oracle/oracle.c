@@ -1,0 +1,414 @@
+/*
+ * fp64 CPU oracle for exact softmax attention, forward pass.
+ *
+ * TEST INFRASTRUCTURE.  Only the tests, the package smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  It shares no code,
+ * header, table or helper with the CUDA path, and nothing in the CUDA path may
+ * call it.
+ *
+ * What it computes (the plain definition, for one sequence s, head h, row i):
+ *
+ *   S_ij  = scale * sum_k q_ik k_jk        for every visible key j
+ *   m_i   = max_j S_ij
+ *   l_i   = sum_j exp(S_ij - m_i)
+ *   P_ij  = exp(S_ij - m_i) / l_i
+ *   O_i   = sum_j P_ij v_j
+ *   LSE_i = m_i + log(l_i)                 (natural log, scaled-logit units)
+ *
+ * Sources on the pages:
+ *   - the attention formula softmax(Q K^T / sqrt(d)) V: "flash-attention-evolution"
+ *     (letsgetai), section "为什么 attention 慢", display equation;
+ *   - materialise S, then P = softmax(S), then O = P V: "FlashAttention"
+ *     (compassingai), section 3 "技術原理", the three-step listing of standard
+ *     attention (read for what it computes);
+ *   - normalise by l once at the end: "flash-attention-evolution", section
+ *     FlashAttention "核心机制", the two-segment merge equations (softmax = f / l).
+ *
+ * Readings where the pages are silent: "visible" is every key j < L_s, or
+ * j <= i when causal (lower-triangular mask within each sequence); the LSE is
+ * the natural log of sum_j exp(S_ij) in units of the scaled logits.
+ *
+ * Inputs are bf16 bit patterns (uint16) in the packed layout
+ * [tokens, H, d]; sequence s occupies tokens cu_seqlens[s] .. cu_seqlens[s+1]-1.
+ * Every bf16 value widens exactly to fp64 here; nothing is rounded afterwards.
+ *
+ * Besides the definition, two more routines restate the pages' own incremental
+ * formulations so the tests can pin one against the other:
+ *   - oracle_softmax_merge: the two-segment (m, l, f) merge identity;
+ *   - oracle_attn_online:   the block-by-block running-max / running-sum loop
+ *     ("FlashAttention", compassingai, section 3, online softmax listing),
+ *     finished with the division by l that the merge equations add.
+ */
+#define _GNU_SOURCE
+#include <math.h>
+#include <pthread.h>
+#include <sched.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+#define ORACLE_OK 0
+#define ORACLE_EINVAL -1
+#define ORACLE_ENOMEM -2
+
+static double widen_bf16(uint16_t bits)
+{
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Number of CPUs in this process's affinity mask (at least 1). */
+int oracle_cpu_count(void)
+{
+    cpu_set_t set;
+    CPU_ZERO(&set);
+    if (sched_getaffinity(0, sizeof set, &set) == 0) {
+        int n = CPU_COUNT(&set);
+        if (n > 0)
+            return n;
+    }
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    return n > 0 ? (int)n : 1;
+}
+
+typedef struct {
+    const uint16_t *q, *k, *v;
+    const int64_t *cu;
+    int64_t nseq;
+    int H, d;
+    double scale;
+    int causal;
+    const int64_t *rows; /* [nrows][3] = (seq, head, row) */
+    int64_t nrows;
+    double *o;   /* [nrows][d] */
+    double *lse; /* [nrows] */
+    int64_t begin, end;
+    int status;
+} rows_job;
+
+/* Checks one requested row and returns its sequence bounds. */
+static int row_bounds(const rows_job *jb, int64_t r, int64_t *base, int64_t *L,
+                      int64_t *i, int *h)
+{
+    int64_t s = jb->rows[3 * r + 0];
+    int64_t hh = jb->rows[3 * r + 1];
+    int64_t ii = jb->rows[3 * r + 2];
+    if (s < 0 || s >= jb->nseq || hh < 0 || hh >= jb->H)
+        return ORACLE_EINVAL;
+    *base = jb->cu[s];
+    *L = jb->cu[s + 1] - jb->cu[s];
+    if (ii < 0 || ii >= *L)
+        return ORACLE_EINVAL;
+    *i = ii;
+    *h = (int)hh;
+    return ORACLE_OK;
+}
+
+static void *rows_worker(void *arg)
+{
+    rows_job *jb = (rows_job *)arg;
+    const int H = jb->H, d = jb->d;
+    int64_t maxL = 0;
+    for (int64_t s = 0; s < jb->nseq; ++s)
+        if (jb->cu[s + 1] - jb->cu[s] > maxL)
+            maxL = jb->cu[s + 1] - jb->cu[s];
+    double *srow = (double *)malloc(sizeof(double) * (size_t)(maxL > 0 ? maxL : 1));
+    double *qrow = (double *)malloc(sizeof(double) * (size_t)d);
+    if (!srow || !qrow) {
+        free(srow);
+        free(qrow);
+        jb->status = ORACLE_ENOMEM;
+        return NULL;
+    }
+    for (int64_t r = jb->begin; r < jb->end; ++r) {
+        int64_t base, L, i;
+        int h;
+        if (row_bounds(jb, r, &base, &L, &i, &h) != ORACLE_OK) {
+            jb->status = ORACLE_EINVAL;
+            break;
+        }
+        const int64_t nvis = jb->causal ? i + 1 : L;
+        const uint16_t *qi = jb->q + ((base + i) * H + h) * (int64_t)d;
+        for (int c = 0; c < d; ++c)
+            qrow[c] = widen_bf16(qi[c]);
+        /* S_ij = scale * <q_i, k_j> for every visible key, materialised */
+        for (int64_t j = 0; j < nvis; ++j) {
+            const uint16_t *kj = jb->k + ((base + j) * H + h) * (int64_t)d;
+            double dot = 0.0;
+            for (int c = 0; c < d; ++c)
+                dot += qrow[c] * widen_bf16(kj[c]);
+            srow[j] = jb->scale * dot;
+        }
+        /* m_i = max_j S_ij */
+        double m = -INFINITY;
+        for (int64_t j = 0; j < nvis; ++j)
+            if (srow[j] > m)
+                m = srow[j];
+        /* l_i = sum_j exp(S_ij - m_i) */
+        double l = 0.0;
+        for (int64_t j = 0; j < nvis; ++j)
+            l += exp(srow[j] - m);
+        /* P_ij = exp(S_ij - m_i) / l_i ;  O_i = sum_j P_ij v_j */
+        double *oi = jb->o + r * (int64_t)d;
+        for (int c = 0; c < d; ++c)
+            oi[c] = 0.0;
+        for (int64_t j = 0; j < nvis; ++j) {
+            const double p = exp(srow[j] - m) / l;
+            const uint16_t *vj = jb->v + ((base + j) * H + h) * (int64_t)d;
+            for (int c = 0; c < d; ++c)
+                oi[c] += p * widen_bf16(vj[c]);
+        }
+        /* LSE_i = m_i + log(l_i) */
+        jb->lse[r] = nvis > 0 ? m + log(l) : -INFINITY;
+    }
+    free(srow);
+    free(qrow);
+    return NULL;
+}
+
+static int check_common(const void *q, const void *k, const void *v, const int64_t *cu,
+                        int64_t nseq, int H, int d, double scale)
+{
+    if (!q || !k || !v || !cu || nseq < 0 || H <= 0 || d <= 0 || !isfinite(scale))
+        return ORACLE_EINVAL;
+    if (cu[0] != 0)
+        return ORACLE_EINVAL;
+    for (int64_t s = 0; s < nseq; ++s)
+        if (cu[s + 1] < cu[s])
+            return ORACLE_EINVAL;
+    return ORACLE_OK;
+}
+
+/*
+ * O and LSE of the requested rows, by the plain definition above.
+ * nthreads <= 0 uses every CPU of the affinity mask; *threads_used (if not
+ * NULL) receives the number of threads that ran.  Returns 0, or a negative
+ * code for a bad argument (row outside its sequence, decreasing cu_seqlens...).
+ */
+int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                     const int64_t *cu_seqlens, int64_t nseq, int H, int d,
+                     double scale, int causal, const int64_t *rows, int64_t nrows,
+                     double *o, double *lse, int nthreads, int *threads_used)
+{
+    int st = check_common(q, k, v, cu_seqlens, nseq, H, d, scale);
+    if (st != ORACLE_OK || nrows < 0 || (nrows > 0 && (!rows || !o || !lse)))
+        return ORACLE_EINVAL;
+    int nt = nthreads > 0 ? nthreads : oracle_cpu_count();
+    if (nt > nrows)
+        nt = nrows > 0 ? (int)nrows : 1;
+    rows_job *jobs = (rows_job *)calloc((size_t)nt, sizeof(rows_job));
+    pthread_t *tid = (pthread_t *)calloc((size_t)nt, sizeof(pthread_t));
+    if (!jobs || !tid) {
+        free(jobs);
+        free(tid);
+        return ORACLE_ENOMEM;
+    }
+    int started = 0;
+    for (int t = 0; t < nt; ++t) {
+        rows_job *jb = &jobs[t];
+        jb->q = q; jb->k = k; jb->v = v;
+        jb->cu = cu_seqlens; jb->nseq = nseq;
+        jb->H = H; jb->d = d; jb->scale = scale; jb->causal = causal;
+        jb->rows = rows; jb->nrows = nrows; jb->o = o; jb->lse = lse;
+        jb->begin = nrows * t / nt;
+        jb->end = nrows * (t + 1) / nt;
+        jb->status = ORACLE_OK;
+    }
+    if (nt == 1) {
+        rows_worker(&jobs[0]);
+        started = 1;
+    } else {
+        for (int t = 0; t < nt; ++t) {
+            if (pthread_create(&tid[t], NULL, rows_worker, &jobs[t]) != 0)
+                break;
+            ++started;
+        }
+        /* rows of threads that failed to start run on this thread */
+        for (int t = started; t < nt; ++t)
+            rows_worker(&jobs[t]);
+        for (int t = 0; t < started; ++t)
+            pthread_join(tid[t], NULL);
+    }
+    for (int t = 0; t < nt; ++t)
+        if (jobs[t].status != ORACLE_OK)
+            st = jobs[t].status;
+    if (threads_used)
+        *threads_used = nt == 1 ? 1 : (started > 0 ? started : 1);
+    free(jobs);
+    free(tid);
+    return st;
+}
+
+/*
+ * The probability row P_i (length nvis: L_s, or i+1 when causal) of one query
+ * row, by the plain definition.  p must hold L_s doubles.  Returns the number
+ * of visible keys written, or a negative code.
+ */
+int64_t oracle_attn_probs(const uint16_t *q, const uint16_t *k,
+                          const int64_t *cu_seqlens, int64_t nseq, int H, int d,
+                          double scale, int causal, int64_t seq, int h, int64_t i,
+                          double *p)
+{
+    static const uint16_t dummy = 0;
+    int st = check_common(q, k, &dummy, cu_seqlens, nseq, H, d, scale);
+    if (st != ORACLE_OK || !p || seq < 0 || seq >= nseq || h < 0 || h >= H)
+        return ORACLE_EINVAL;
+    const int64_t base = cu_seqlens[seq];
+    const int64_t L = cu_seqlens[seq + 1] - base;
+    if (i < 0 || i >= L)
+        return ORACLE_EINVAL;
+    const int64_t nvis = causal ? i + 1 : L;
+    const uint16_t *qi = q + ((base + i) * H + h) * (int64_t)d;
+    double m = -INFINITY;
+    for (int64_t j = 0; j < nvis; ++j) {
+        const uint16_t *kj = k + ((base + j) * H + h) * (int64_t)d;
+        double dot = 0.0;
+        for (int c = 0; c < d; ++c)
+            dot += widen_bf16(qi[c]) * widen_bf16(kj[c]);
+        p[j] = scale * dot;
+        if (p[j] > m)
+            m = p[j];
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j < nvis; ++j)
+        l += exp(p[j] - m);
+    for (int64_t j = 0; j < nvis; ++j)
+        p[j] = exp(p[j] - m) / l;
+    return nvis;
+}
+
+/*
+ * Softmax of x[0..n) computed segment by segment with the two-segment merge
+ * identity ("flash-attention-evolution", section FlashAttention "核心机制"):
+ * for x = (x1, x2),
+ *   m(x) = max(m(x1), m(x2)),
+ *   l(x) = e^{m(x1)-m(x)} l(x1) + e^{m(x2)-m(x)} l(x2),
+ *   f(x) = [e^{m(x1)-m(x)} f(x1), e^{m(x2)-m(x)} f(x2)],
+ *   softmax(x) = f(x) / l(x),
+ * where for one segment m is its max, f = exp(x - m) and l = sum f.
+ * The segment boundaries are cuts[0..ncuts) (strictly increasing, inside
+ * (0, n)).  Segments are merged left to right into a running (m, l, f).
+ * Writes softmax(x) to out and returns 0; *m_out and *l_out get the merged
+ * statistics.
+ */
+int oracle_softmax_merge(const double *x, int64_t n, const int64_t *cuts, int64_t ncuts,
+                         double *out, double *m_out, double *l_out)
+{
+    if (!x || !out || n <= 0 || ncuts < 0 || (ncuts > 0 && !cuts))
+        return ORACLE_EINVAL;
+    for (int64_t c = 0; c < ncuts; ++c)
+        if (cuts[c] <= 0 || cuts[c] >= n || (c > 0 && cuts[c] <= cuts[c - 1]))
+            return ORACLE_EINVAL;
+    double m_run = -INFINITY, l_run = 0.0;
+    int64_t lo = 0;
+    for (int64_t seg = 0; seg <= ncuts; ++seg) {
+        const int64_t hi = seg < ncuts ? cuts[seg] : n;
+        /* statistics of the new segment x2 = x[lo, hi) */
+        double m2 = -INFINITY;
+        for (int64_t j = lo; j < hi; ++j)
+            if (x[j] > m2)
+                m2 = x[j];
+        double l2 = 0.0;
+        for (int64_t j = lo; j < hi; ++j) {
+            out[j] = exp(x[j] - m2); /* f(x2) */
+            l2 += out[j];
+        }
+        /* merge (m_run, l_run, f_run = out[0, lo)) with (m2, l2, f2 = out[lo, hi)) */
+        const double m = m_run > m2 ? m_run : m2;
+        const double a1 = lo > 0 ? exp(m_run - m) : 0.0;
+        const double a2 = exp(m2 - m);
+        for (int64_t j = 0; j < lo; ++j)
+            out[j] *= a1;
+        for (int64_t j = lo; j < hi; ++j)
+            out[j] *= a2;
+        l_run = a1 * l_run + a2 * l2;
+        m_run = m;
+        lo = hi;
+    }
+    for (int64_t j = 0; j < n; ++j)
+        out[j] /= l_run;
+    if (m_out)
+        *m_out = m_run;
+    if (l_out)
+        *l_out = l_run;
+    return ORACLE_OK;
+}
+
+/*
+ * O and LSE of the requested rows by the block-wise online loop
+ * ("FlashAttention", compassingai, section 3, online softmax listing): keys
+ * are visited in blocks of bc; per block
+ *   S = scores of the block, m_new = max(m, rowmax S), P = exp(S - m_new),
+ *   l = exp(m - m_new) l + rowsum P, O = exp(m - m_new) O + P V, m = m_new,
+ * and at the end O / l (the merge equations' final normalisation) and
+ * LSE = m + log l.  Single-threaded; used only to pin the definition.
+ */
+int oracle_attn_online(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                       const int64_t *cu_seqlens, int64_t nseq, int H, int d,
+                       double scale, int causal, const int64_t *rows, int64_t nrows,
+                       int64_t bc, double *o, double *lse)
+{
+    int st = check_common(q, k, v, cu_seqlens, nseq, H, d, scale);
+    if (st != ORACLE_OK || bc <= 0 || nrows < 0 || (nrows > 0 && (!rows || !o || !lse)))
+        return ORACLE_EINVAL;
+    double *sblk = (double *)malloc(sizeof(double) * (size_t)bc);
+    double *acc = (double *)malloc(sizeof(double) * (size_t)d);
+    if (!sblk || !acc) {
+        free(sblk);
+        free(acc);
+        return ORACLE_ENOMEM;
+    }
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t s = rows[3 * r], hh = rows[3 * r + 1], i = rows[3 * r + 2];
+        if (s < 0 || s >= nseq || hh < 0 || hh >= H) {
+            st = ORACLE_EINVAL;
+            break;
+        }
+        const int64_t base = cu_seqlens[s], L = cu_seqlens[s + 1] - base;
+        if (i < 0 || i >= L) {
+            st = ORACLE_EINVAL;
+            break;
+        }
+        const int64_t nvis = causal ? i + 1 : L;
+        const uint16_t *qi = q + ((base + i) * H + hh) * (int64_t)d;
+        double m = -INFINITY, l = 0.0;
+        for (int c = 0; c < d; ++c)
+            acc[c] = 0.0;
+        for (int64_t j0 = 0; j0 < nvis; j0 += bc) {
+            const int64_t nb = nvis - j0 < bc ? nvis - j0 : bc;
+            double bmax = -INFINITY;
+            for (int64_t jj = 0; jj < nb; ++jj) {
+                const uint16_t *kj = k + ((base + j0 + jj) * H + hh) * (int64_t)d;
+                double dot = 0.0;
+                for (int c = 0; c < d; ++c)
+                    dot += widen_bf16(qi[c]) * widen_bf16(kj[c]);
+                sblk[jj] = scale * dot;
+                if (sblk[jj] > bmax)
+                    bmax = sblk[jj];
+            }
+            const double m_new = m > bmax ? m : bmax;
+            const double alpha = exp(m - m_new); /* 0 on the first block (m = -inf) */
+            double rowsum = 0.0;
+            for (int c = 0; c < d; ++c)
+                acc[c] *= alpha;
+            for (int64_t jj = 0; jj < nb; ++jj) {
+                const double p = exp(sblk[jj] - m_new);
+                rowsum += p;
+                const uint16_t *vj = v + ((base + j0 + jj) * H + hh) * (int64_t)d;
+                for (int c = 0; c < d; ++c)
+                    acc[c] += p * widen_bf16(vj[c]);
+            }
+            l = alpha * l + rowsum;
+            m = m_new;
+        }
+        for (int c = 0; c < d; ++c)
+            o[r * d + c] = acc[c] / l;
+        lse[r] = m + log(l);
+    }
+    free(sblk);
+    free(acc);
+    return st;
+}

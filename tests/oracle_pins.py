@@ -1,0 +1,247 @@
+"""Checks that pin the fp64 oracle to facts fixed outside the oracle itself.
+
+Each check takes an ``oracle.Oracle`` and raises AssertionError when the oracle
+disagrees with:
+  - a brute-force high-precision (50-digit Decimal) evaluation of the
+    definition on tiny inputs, without max subtraction;
+  - a hand closed form on two keys;
+  - rows of P summing to one;
+  - constant V giving constant O;
+  - Q = 0 (or K = 0) giving the column mean of V (causal: the prefix mean)
+    with LSE = log(#visible keys);
+  - a large-scale one-hot limit where O tends to one chosen value row;
+  - torch's scaled_dot_product_attention and logsumexp in fp64 on CPU;
+  - the two-segment merge identity of the online softmax;
+  - the block-wise online loop, for several block sizes;
+  - packing: a sequence inside a packed batch equals that sequence alone;
+  - causal masking: the last row of a causal sequence sees every key.
+The mutation tests run the same checks against deliberately broken copies of
+the oracle and require each copy to fail at least one of them.
+"""
+from __future__ import annotations
+
+import math
+from decimal import Decimal, getcontext
+
+import numpy as np
+
+from io_aware_exact_06_gb300 import inputs
+
+
+def _rand_workload(seed, seqlens, H, d, std=1.0):
+    return inputs.make_workload("pin", seed, seqlens, H, d, causal=False, qk_std=std, v_std=std)
+
+
+def _close(a, b, tol, what):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    err = np.max(np.abs(a - b) / np.maximum(1.0, np.abs(b))) if a.size else 0.0
+    assert err <= tol, f"{what}: max rel/abs error {err:.3e} > {tol:.1e}"
+
+
+def check_brute_force_decimal(orc):
+    """Tiny inputs, definition evaluated in 50-digit decimal arithmetic."""
+    getcontext().prec = 50
+    wl = _rand_workload(101, [3, 5, 1], H=2, d=4)
+    rows = inputs.all_rows(wl.cu_seqlens, wl.H)
+    qf = inputs.bf16_bits_to_f64(wl.q)
+    kf = inputs.bf16_bits_to_f64(wl.k)
+    vf = inputs.bf16_bits_to_f64(wl.v)
+    for causal in (False, True):
+        for scale in (0.5, 1.0 / math.sqrt(4), 1.7):
+            o, lse, _ = orc.attn_rows(wl.q, wl.k, wl.v, wl.cu_seqlens, rows, scale, causal, 1)
+            for n, (s, h, i) in enumerate(rows):
+                base = int(wl.cu_seqlens[s])
+                L = int(wl.cu_seqlens[s + 1]) - base
+                nvis = i + 1 if causal else L
+                ds = Decimal(scale)
+                e = []
+                for j in range(nvis):
+                    dot = sum(Decimal(qf[base + i, h, c]) * Decimal(kf[base + j, h, c])
+                              for c in range(wl.d))
+                    e.append((ds * dot).exp())
+                z = sum(e)
+                ref_o = [float(sum(e[j] * Decimal(vf[base + j, h, c]) for j in range(nvis)) / z)
+                         for c in range(wl.d)]
+                _close(o[n], ref_o, 1e-13, f"O brute force row {(s, h, i)} causal={causal}")
+                _close(lse[n], float(z.ln()), 1e-13, f"LSE brute force row {(s, h, i)}")
+
+
+def check_two_key_closed_form(orc):
+    """N=2, d=1: O_0 = (e^{s00} v0 + e^{s01} v1) / (e^{s00} + e^{s01})."""
+    bits = inputs.f64_to_bf16_bits
+    qv = np.array([1.5, -0.75]); kv = np.array([0.5, 2.0]); vv = np.array([3.0, -1.0])
+    q = bits(qv).reshape(2, 1, 1); k = bits(kv).reshape(2, 1, 1); v = bits(vv).reshape(2, 1, 1)
+    cu = np.array([0, 2])
+    scale = 0.8
+    rows = np.array([[0, 0, 0], [0, 0, 1]])
+    o, lse, _ = orc.attn_rows(q, k, v, cu, rows, scale, False, 1)
+    for i in range(2):
+        s0 = scale * qv[i] * kv[0]
+        s1 = scale * qv[i] * kv[1]
+        ref = (math.exp(s0) * vv[0] + math.exp(s1) * vv[1]) / (math.exp(s0) + math.exp(s1))
+        _close(o[i, 0], ref, 1e-15, f"two-key O row {i}")
+        _close(lse[i], math.log(math.exp(s0) + math.exp(s1)), 1e-15, f"two-key LSE row {i}")
+    o, lse, _ = orc.attn_rows(q, k, v, cu, rows, scale, True, 1)
+    _close(o[0, 0], vv[0], 0.0, "causal row 0 sees only key 0")
+    _close(lse[0], scale * qv[0] * kv[0], 1e-15, "causal row 0 LSE = its single logit")
+
+
+def check_probs_sum_to_one(orc):
+    wl = _rand_workload(202, [37, 64], H=3, d=16, std=2.0)
+    for causal in (False, True):
+        for (s, h, i) in [(0, 0, 0), (0, 2, 36), (1, 1, 17), (1, 2, 63)]:
+            p = orc.attn_probs(wl.q, wl.k, wl.cu_seqlens, s, h, i, 0.25, causal)
+            L = int(wl.cu_seqlens[s + 1] - wl.cu_seqlens[s])
+            assert p.size == (i + 1 if causal else L), "visible key count"
+            assert np.all(p >= 0)
+            _close(math.fsum(p), 1.0, 1e-14, "sum of P row")
+
+
+def check_constant_v(orc):
+    wl = _rand_workload(303, [50, 20], H=2, d=8, std=1.5)
+    c = inputs.f64_to_bf16_bits(np.array([-2.625]))[0]
+    v = np.full_like(wl.v, c)
+    rows = inputs.all_rows(wl.cu_seqlens, wl.H)
+    for causal in (False, True):
+        o, _, _ = orc.attn_rows(wl.q, wl.k, v, wl.cu_seqlens, rows, 0.3, causal, 2)
+        _close(o, np.full_like(o, -2.625), 1e-14, "constant V gives constant O")
+
+
+def check_zero_q_or_k(orc):
+    wl = _rand_workload(404, [33, 7], H=2, d=8)
+    zero = np.zeros_like(wl.q)
+    rows = inputs.all_rows(wl.cu_seqlens, wl.H)
+    vf = inputs.bf16_bits_to_f64(wl.v)
+    for which in ("q", "k"):
+        q = zero if which == "q" else wl.q
+        k = zero if which == "k" else wl.k
+        for causal in (False, True):
+            o, lse, _ = orc.attn_rows(q, k, wl.v, wl.cu_seqlens, rows, 0.7, causal, 2)
+            for n, (s, h, i) in enumerate(rows):
+                base = int(wl.cu_seqlens[s]); L = int(wl.cu_seqlens[s + 1]) - base
+                nvis = i + 1 if causal else L
+                ref = vf[base:base + nvis, h, :].mean(axis=0)
+                _close(o[n], ref, 1e-14, f"{which}=0 mean of visible V")
+                _close(lse[n], math.log(nvis), 1e-14, f"{which}=0 LSE = log(#visible)")
+
+
+def check_one_hot_limit(orc):
+    """K rows are distinct one-hot vectors, q_i = e_r: S_ij = scale * [j == r].
+
+    With scale t >= 60 the softmax puts all but ~L*e^-t of its mass on key r, so
+    O_i = v_r and LSE_i = t + log(1 + (L-1) e^-t) to fp64 precision."""
+    L, d, H = 12, 16, 2
+    k = np.zeros((L, H, d)); q = np.zeros((L, H, d))
+    for j in range(L):
+        k[j, :, j] = 1.0
+    targets = [(i * 5 + 3) % L for i in range(L)]
+    for i, r in enumerate(targets):
+        q[i, :, r] = 1.0
+    wl = _rand_workload(505, [L], H=H, d=d)
+    bits = inputs.f64_to_bf16_bits
+    qb, kb = bits(q.ravel()).reshape(q.shape), bits(k.ravel()).reshape(k.shape)
+    rows = inputs.all_rows(wl.cu_seqlens, H)
+    vf = inputs.bf16_bits_to_f64(wl.v)
+    # scale 800: exp(800) overflows fp64, so this also needs a true max subtraction
+    for scale in (60.0, 800.0):
+        o, lse, _ = orc.attn_rows(qb, kb, wl.v, wl.cu_seqlens, rows, scale, False, 1)
+        for n, (s, h, i) in enumerate(rows):
+            r = targets[i]
+            _close(o[n], vf[r, h], 1e-14, f"one-hot limit picks v_r (scale {scale})")
+            _close(lse[n], scale + math.log1p((L - 1) * math.exp(-scale)), 1e-14,
+                   f"one-hot LSE (scale {scale})")
+
+
+def check_torch_sdpa(orc):
+    """Library cross-check: torch SDPA (fp64, CPU) and logsumexp of the masked logits."""
+    import torch
+    B, H, N, d = 2, 3, 45, 16
+    wl = _rand_workload(606, [N] * B, H=H, d=d, std=1.3)
+    rows = inputs.all_rows(wl.cu_seqlens, H)
+    to_t = lambda a: torch.from_numpy(inputs.bf16_bits_to_f64(a).reshape(B, N, H, d)).permute(0, 2, 1, 3)
+    qt, kt, vt = to_t(wl.q), to_t(wl.k), to_t(wl.v)
+    for causal in (False, True):
+        scale = 1.0 / math.sqrt(d)
+        ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, is_causal=causal, scale=scale)
+        logits = (qt @ kt.transpose(-1, -2)) * scale
+        if causal:
+            mask = torch.ones(N, N, dtype=torch.bool).tril()
+            logits = logits.masked_fill(~mask, float("-inf"))
+        ref_lse = torch.logsumexp(logits, dim=-1)
+        o, lse, _ = orc.attn_rows(wl.q, wl.k, wl.v, wl.cu_seqlens, rows, scale, causal, 2)
+        for n, (s, h, i) in enumerate(rows):
+            _close(o[n], ref[s, h, i].numpy(), 1e-12, f"SDPA O causal={causal}")
+            _close(lse[n], float(ref_lse[s, h, i]), 1e-12, f"logsumexp causal={causal}")
+
+
+def check_merge_identity(orc):
+    rng_bits = inputs.splitmix64(707, 0, 4096)
+    x = ((rng_bits >> np.uint64(11)).astype(np.float64) * 2.0 ** -53 - 0.5) * 40.0
+    for n, cuts in [(1, []), (2, [1]), (10, [3]), (100, [10, 11, 50, 99]),
+                    (1000, list(range(128, 1000, 128))), (777, [5, 400])]:
+        xs = x[:n]
+        sm, m, l = orc.softmax_merge(xs, cuts)
+        e = np.exp(xs - xs.max())
+        _close(sm, e / e.sum(), 1e-14, f"merged softmax n={n} cuts={len(cuts)}")
+        _close(m, xs.max(), 0.0, "merged max")
+        _close(l, math.fsum(e), 1e-13, "merged sum")
+    # the merge must not depend on where the row is cut
+    a, _, _ = orc.softmax_merge(x[:500], [7, 300])
+    b, _, _ = orc.softmax_merge(x[:500], [250])
+    _close(a, b, 1e-14, "merge independent of cut points")
+
+
+def check_online_loop(orc):
+    wl = _rand_workload(808, [200, 129], H=2, d=16, std=2.5)
+    rows = inputs.all_rows(wl.cu_seqlens, wl.H)
+    for causal in (False, True):
+        o, lse, _ = orc.attn_rows(wl.q, wl.k, wl.v, wl.cu_seqlens, rows, 0.4, causal, 2)
+        for bc in (1, 7, 64, 128, 1000):
+            o2, lse2 = orc.attn_online(wl.q, wl.k, wl.v, wl.cu_seqlens, rows, 0.4, causal, bc)
+            _close(o2, o, 1e-12, f"online loop O bc={bc} causal={causal}")
+            _close(lse2, lse, 1e-12, f"online loop LSE bc={bc}")
+
+
+def check_packing(orc):
+    wl = _rand_workload(909, [17, 40, 3], H=2, d=8)
+    for causal in (False, True):
+        rows = inputs.all_rows(wl.cu_seqlens, wl.H)
+        o, lse, _ = orc.attn_rows(wl.q, wl.k, wl.v, wl.cu_seqlens, rows, 0.35, causal, 2)
+        for s in range(wl.nseq):
+            a, b = int(wl.cu_seqlens[s]), int(wl.cu_seqlens[s + 1])
+            cu1 = np.array([0, b - a])
+            rows1 = inputs.all_rows(cu1, wl.H)
+            o1, lse1, _ = orc.attn_rows(wl.q[a:b], wl.k[a:b], wl.v[a:b], cu1, rows1, 0.35, causal, 1)
+            sel = rows[:, 0] == s
+            _close(o[sel], o1, 0.0, "packed sequence equals the sequence alone")
+            _close(lse[sel], lse1, 0.0, "packed LSE equals the sequence alone")
+
+
+def check_causal_last_row(orc):
+    wl = _rand_workload(1010, [31, 64], H=2, d=8)
+    rows = np.array([[0, 0, 30], [0, 1, 30], [1, 0, 63], [1, 1, 63]])
+    o1, l1, _ = orc.attn_rows(wl.q, wl.k, wl.v, wl.cu_seqlens, rows, 0.5, True, 1)
+    o2, l2, _ = orc.attn_rows(wl.q, wl.k, wl.v, wl.cu_seqlens, rows, 0.5, False, 1)
+    _close(o1, o2, 0.0, "last causal row sees every key")
+    _close(l1, l2, 0.0, "last causal row LSE")
+    # and a middle row does not: causal row 10 must differ from the full row 10
+    rows = np.array([[1, 0, 10]])
+    o1, _, _ = orc.attn_rows(wl.q, wl.k, wl.v, wl.cu_seqlens, rows, 0.5, True, 1)
+    o2, _, _ = orc.attn_rows(wl.q, wl.k, wl.v, wl.cu_seqlens, rows, 0.5, False, 1)
+    assert np.max(np.abs(o1 - o2)) > 1e-3, "causal mask has no effect on a middle row"
+
+
+ALL_CHECKS = [
+    check_brute_force_decimal,
+    check_two_key_closed_form,
+    check_probs_sum_to_one,
+    check_constant_v,
+    check_zero_q_or_k,
+    check_one_hot_limit,
+    check_torch_sdpa,
+    check_merge_identity,
+    check_online_loop,
+    check_packing,
+    check_causal_last_row,
+]

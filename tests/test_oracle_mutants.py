@@ -1,0 +1,63 @@
+"""Each planted mistake in a copy of the oracle must fail at least one pin.
+
+The copies are built on the CPU in a temporary folder from ``oracle/oracle.c``
+with one textual change each; the committed oracle is never modified.  This
+shows the pins in tests/oracle_pins.py are strong enough to catch a dropped
+term, a wrong sign or index, a transposed operand, a misread layout.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from tests import oracle_pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+MUTANTS = {
+    "drop_scale": [("srow[j] = jb->scale * dot;", "srow[j] = dot;")],
+    "no_normalise": [("const double p = exp(srow[j] - m) / l;", "const double p = exp(srow[j] - m);")],
+    "lse_without_max": [("jb->lse[r] = nvis > 0 ? m + log(l)", "jb->lse[r] = nvis > 0 ? log(l)")],
+    "lse_sign": [("jb->lse[r] = nvis > 0 ? m + log(l)", "jb->lse[r] = nvis > 0 ? m - log(l)")],
+    "v_read_from_k": [("const uint16_t *vj = jb->v + ", "const uint16_t *vj = jb->k + ")],
+    "causal_ignored": [("const int64_t nvis = jb->causal ? i + 1 : L;\n        const uint16_t *qi = jb->q",
+                        "const int64_t nvis = L;\n        const uint16_t *qi = jb->q")],
+    "causal_excludes_diagonal": [("const int64_t nvis = jb->causal ? i + 1 : L;\n        const uint16_t *qi = jb->q",
+                                  "const int64_t nvis = jb->causal ? (i > 0 ? i : 1) : L;\n        const uint16_t *qi = jb->q")],
+    "k_wrong_head": [("const uint16_t *kj = jb->k + ((base + j) * H + h)",
+                      "const uint16_t *kj = jb->k + ((base + j) * H + 0)")],
+    "transposed_scores": [("const uint16_t *qi = jb->q + ((base + i) * H + h) * (int64_t)d;",
+                           "const uint16_t *qi = jb->k + ((base + i) * H + h) * (int64_t)d;"),
+                          ("const uint16_t *kj = jb->k + ((base + j) * H + h) * (int64_t)d;\n            double dot",
+                           "const uint16_t *kj = jb->q + ((base + j) * H + h) * (int64_t)d;\n            double dot")],
+    "sequence_base_ignored": [("const uint16_t *vj = jb->v + ((base + j)", "const uint16_t *vj = jb->v + ((0 + j)")],
+    "short_dot": [("for (int c = 0; c < d; ++c)\n                dot += qrow[c]",
+                   "for (int c = 0; c < d - 1; ++c)\n                dot += qrow[c]")],
+    "exp_sign": [("l += exp(srow[j] - m);", "l += exp(m - srow[j]);")],
+    "bad_widening": [("uint32_t u = (uint32_t)bits << 16;", "uint32_t u = (uint32_t)bits << 15;")],
+    "max_over_first_key_only": [("if (srow[j] > m)\n                m = srow[j];",
+                                 "if (j == 0)\n                m = srow[j];")],
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    src = open(SRC).read()
+    for old, new in MUTANTS[name]:
+        assert src.count(old) == 1, f"mutation anchor not unique or missing: {old!r}"
+        src = src.replace(old, new)
+    path = tmp_path / "oracle_mutant.c"
+    path.write_text(src)
+    lib = tmp_path / "liboracle_mutant.so"
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+                    "-pthread", str(path), "-o", str(lib), "-lm"], check=True)
+    mutant = oracle.Oracle(str(lib))
+    caught = []
+    for check in oracle_pins.ALL_CHECKS:
+        try:
+            check(mutant)
+        except (AssertionError, ValueError) as e:
+            caught.append((check.__name__, str(e)[:80]))
+            break
+    assert caught, f"mutant {name} passed every pin"
