@@ -1,0 +1,356 @@
+"""Benchmark of the GB300 fused exact attention forward.
+
+One step = one forward pass (attn_fwd: every kernel of the path) over the
+long-context causal workload B=2, H=16, N=8192, d=128 (bf16, fp32 accumulate),
+with inputs resident in device memory.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Metric: attention forward TFLOP/s, FLOPs = 4*B*H*N^2*d halved for causal,
+whole job (all ranks) / the slowest rank's time.  N > 1 runs one independent
+replica per GPU (launched by torch.distributed.run); the path needs no
+exchange between GPUs.
+
+`--impl reference` times the fp64 CPU oracle (the only other implementation
+of this path) on the host cores, one bounded sample of the workload's rows
+per step, and reports it in the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from io_aware_exact_06_gb300 import inputs  # noqa: E402
+
+WORKLOAD = "long_causal"
+METRIC = "attention fwd TFLOP/s on 1 GB300 (bf16) and fraction of dense BF16 peak"
+UNIT = "TFLOP/s"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def workload_config(wl):
+    c = inputs.CONFIGS[WORKLOAD]
+    io_bytes = 4 * wl.tokens * wl.H * wl.d * 2
+    return {"workload": f"{WORKLOAD}: B={c['B']} H={c['H']} N={c['N']} d={c['d']} causal",
+            "B": c["B"], "H": c["H"], "N": c["N"], "d": c["d"], "causal": c["causal"],
+            "scale": "1/sqrt(d)", "inputs": "Q,K,V iid N(0,1) bf16, seeded (SplitMix64 + Box-Muller)",
+            "l2": f"Q,K,V,O = {io_bytes / 1e6:.0f} MB > 129 MB L2 (no flush between steps)"}
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]), float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])), \
+            float(pk["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, 1700.0, FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = ""
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+        return False
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_sample(wl, budget_s: float, seed: int):
+    """Rows of the workload for a bounded oracle run of about budget_s seconds
+    (calibrated on a small batch of the same rows)."""
+    import oracle
+    rows = inputs.sample_rows(wl.cu_seqlens, wl.H, 1 << 18, seed=seed)
+    rows = rows[np.argsort(inputs.splitmix64(seed + 1, 0, len(rows)))]
+    calib = rows[:256]
+    t0 = time.perf_counter()
+    oracle.attn_rows(wl.q, wl.k, wl.v, wl.cu_seqlens, calib, wl.scale, wl.causal)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    n = int(min(len(rows), max(256, 256 * budget_s / dt)))
+    return rows[:n]
+
+
+def row_flops(wl, rows) -> float:
+    """4*d FLOPs per visible key of each row (QK^T and PV), the metric's count."""
+    L = (wl.cu_seqlens[rows[:, 0] + 1] - wl.cu_seqlens[rows[:, 0]]).astype(np.float64)
+    vis = rows[:, 2] + 1.0 if wl.causal else L
+    return float(np.sum(4.0 * wl.d * vis))
+
+
+def cpu_baseline(wl, budget_s: float = 15.0):
+    import oracle
+    rows = oracle_sample(wl, budget_s, seed=0xBA5E)
+    t0 = time.perf_counter()
+    _, _, used = oracle.attn_rows(wl.q, wl.k, wl.v, wl.cu_seqlens, rows, wl.scale, wl.causal)
+    dt = time.perf_counter() - t0
+    return {"value": row_flops(wl, rows) / dt / 1e12, "unit": UNIT, "cores": int(used),
+            "kind": "oracle",
+            "sample": f"{len(rows)} seeded rows of {WORKLOAD} (fp64, materialised score rows), "
+                      f"{dt:.1f} s; FLOPs = 4*d per visible key"}
+
+
+def exp_unit_bound(sm_mhz, d: int, per_gpu_tflops: float):
+    """The exp-unit roofline: each score element costs 4*d flops of the metric
+    and one exp2, so the bound is SMs * f_SM * (ex2 per clock per SM) * 4d.
+    Also the clock-based tensor peak SMs * f_SM * (MMA flop per clock per SM).
+    Rates are measured on this GPU; f_SM is the median clock of the run."""
+    try:
+        from io_aware_exact_06_gb300 import unit_rates
+        r = unit_rates.measure()
+    except Exception as e:  # noqa: BLE001 - reported, not fatal
+        return {"error": str(e)[:200]}
+    f = (sm_mhz or r["max_clock_mhz"]) * 1e6
+    exp_tf = r["sm_count"] * f * r["ex2_per_clk_per_sm"] * 4 * d / 1e12
+    mma_tf = r["sm_count"] * f * r["mma_bf16_flop_per_clk_per_sm"] / 1e12
+    return {"ex2_per_clk_per_sm": r["ex2_per_clk_per_sm"],
+            "mma_flop_per_clk_per_sm": r["mma_bf16_flop_per_clk_per_sm"],
+            "sm_count": r["sm_count"], "sm_mhz": f / 1e6,
+            "exp_bound_tflops": exp_tf, "frac_of_exp_bound": per_gpu_tflops / exp_tf,
+            "tensor_peak_at_clock_tflops": mma_tf,
+            "frac_of_tensor_peak_at_clock": per_gpu_tflops / mma_tf}
+
+
+def run_reference(args, world, rank):
+    """The oracle on the host cores, one bounded sample of rows per step."""
+    if rank != 0:
+        return
+    import oracle
+    wl = inputs.config_workload(WORKLOAD)
+    per_step_s = args.ref_step_s or max(1.0, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
+    rows = oracle_sample(wl, per_step_s, seed=0x5EED)
+    fl = row_flops(wl, rows)
+    for _ in range(args.warmup):
+        oracle.attn_rows(wl.q, wl.k, wl.v, wl.cu_seqlens, rows, wl.scale, wl.causal)
+    times, used = [], 1
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        _, _, used = oracle.attn_rows(wl.q, wl.k, wl.v, wl.cu_seqlens, rows, wl.scale, wl.causal)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = fl * args.steps / total / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(wl),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": int(used), "kind": "oracle",
+                             "sample": f"{len(rows)} seeded rows of {WORKLOAD} per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_cuda(args, world, rank, local):
+    import torch
+    import __graft_entry__
+    import io_aware_exact_06_gb300 as fa
+    __graft_entry__.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = inputs.config_workload(WORKLOAD)
+    B, H, N, d = wl.nseq, wl.H, int(wl.seqlens()[0]), wl.d
+    host = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    q_h, k_h, v_h = host(wl.q).pin_memory(), host(wl.k).pin_memory(), host(wl.v).pin_memory()
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    o_h = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream(dev)
+    flops_step = wl.flops()
+
+    def step():
+        fa.attn_fwd(q, k, v, o, lse, B, H, N, d, wl.scale, True, None, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if fa.attn_last_device_error(stream) != 0:
+        raise RuntimeError("device error during warm-up")
+
+    # device-timed region: inputs resident in HBM
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    status = fa.attn_last_device_error(stream)
+    if status != 0:
+        raise RuntimeError(f"device error status {status}")
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
+    kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    # end to end through the C ABI with host buffers: H2D of Q, K, V from
+    # pinned memory, the forward, D2H of O and LSE, every step
+    def e2e_step():
+        q.copy_(q_h, non_blocking=True)
+        k.copy_(k_h, non_blocking=True)
+        v.copy_(v_h, non_blocking=True)
+        step()
+        o_h.copy_(o, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 10))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    h2d = 3 * q.numel() * 2
+    d2h = o.numel() * 2 + lse.numel() * 4
+
+    if rank != 0:
+        return
+    peak, _, _, src = peaks()
+    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+    achieved = flops_step / (kernel_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(wl),
+        "frac_of_dense_bf16_peak": value / world / peak,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                     "frac": achieved / peak, "peak_source": f"{src} bf16_tflops (burst)",
+                     "kernel": "attn_fwd_kernel<128>", "traffic": args.traffic},
+        "clocks": clk.summary(),
+        "e2e": {"value": world * flops_step * e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+    }
+    line["exp_unit_bound"] = exp_unit_bound(line["clocks"].get("sm_mhz"), d, value / world)
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    print(json.dumps(line), flush=True)
+
+
+# DRAM bytes (read + write) of one attn_fwd_kernel<128> launch of this
+# workload, from the ncu capture summarised under profiles/ (None until taken
+# for the current kernel).
+TRAFFIC_BYTES = None
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-step-s", type=float, default=0.0,
+                    help="reference arm: oracle seconds per step (default: fit the run in ~2.5 min)")
+    args = ap.parse_args()
+    args.traffic = TRAFFIC_BYTES
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_cuda(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

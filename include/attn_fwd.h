@@ -1,0 +1,111 @@
+/*
+ * C ABI of the GB300 (sm_103a) fused exact attention forward.
+ *
+ * Computes, for every sequence s, head h and query row i,
+ *     O_i   = sum_j softmax_j(scale * q_i . k_j) v_j
+ *     LSE_i = log sum_j exp(scale * q_i . k_j)        (natural log)
+ * over the visible keys j (all keys of the sequence, or j <= i when causal),
+ * in one kernel that never writes the score or probability matrices to device
+ * memory: tiles of Q, K and V with a running row max and running row sum
+ * ("flash-attention-evolution" (letsgetai), FlashAttention section "核心机制";
+ * "FlashAttention" (compassingai), section 3 "技術原理").
+ *
+ * Numerics: bf16 inputs, fp32 accumulation, P rounded to bf16 before the PV
+ * product, O written as bf16 (round to nearest even), LSE as fp32.
+ *
+ * Only sm_103 devices are supported (the kernels are built for sm_103a only).
+ * All pointers are device pointers unless stated otherwise.  Every call is
+ * asynchronous on `stream` like any CUDA kernel launch; argument errors are
+ * reported synchronously, before anything is launched.
+ */
+#ifndef IO_AWARE_EXACT_06_ATTN_FWD_H
+#define IO_AWARE_EXACT_06_ATTN_FWD_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *attn_stream_t;
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_NULL = -1,           /* a required pointer is NULL */
+    ATTN_ERR_SHAPE = -2,          /* B, H or N negative or too large */
+    ATTN_ERR_HEADDIM = -3,        /* d is not 64 or 128 */
+    ATTN_ERR_ALIGN = -4,          /* q/k/v/o not 16-byte or lse not 4-byte aligned */
+    ATTN_ERR_SCALE = -5,          /* scale is not finite */
+    ATTN_ERR_CUDA = -6,           /* a CUDA runtime call or launch failed */
+    ATTN_ERR_DEVICE_TIMEOUT = -7, /* a bounded device-side wait expired */
+    ATTN_ERR_SEQLENS = -8,        /* cu_seqlens not increasing from 0, or a length > N */
+    ATTN_ERR_ARCH = -9            /* current device is not sm_103 */
+} attn_status;
+
+/*
+ * attn_fwd: O = softmax(scale * Q K^T) V and the per-row LSE.
+ *
+ * Layout, dense (cu_seqlens == NULL): q, k, v, o are contiguous [B, N, H, d]
+ *   bf16 (token-major, heads interleaved); lse is [B, H, N] fp32.
+ * Layout, packed variable length (cu_seqlens != NULL): q, k, v, o are
+ *   [total, H, d] with total = cu_seqlens[B]; sequence s occupies tokens
+ *   cu_seqlens[s] .. cu_seqlens[s+1]-1; lse is [H, total].  N must be >= every
+ *   sequence length (it bounds the work list); cu_seqlens is int32[B+1] in
+ *   device memory and is validated on the device (see attn_last_device_error).
+ *   Zero-length sequences are allowed.
+ * q, k, v: read only.  o, lse: written for every valid row, nothing else.
+ * d: 64 or 128.  scale: any finite value (1/sqrt(d) for the usual attention).
+ * causal: nonzero means key j is visible to query i iff j <= i (within each
+ *   sequence); zero means every key of the sequence is visible.
+ * Alignment: q, k, v, o 16-byte aligned; lse 4-byte aligned.
+ * Ownership: the caller owns every buffer and keeps it alive until the stream
+ *   work has finished.  The library keeps a small cached device workspace per
+ *   (device, stream) pair (the scheduling list) and an error word per device,
+ *   allocated on first use.  Calls on one stream are ordered; calls on
+ *   different streams may run concurrently.
+ * B == 0, N == 0 or H == 0 is a no-op returning ATTN_OK.
+ * Returns ATTN_OK or a negative attn_status; nothing is launched on error.
+ */
+int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+             int B, int H, int N, int d, float scale, int causal,
+             const int32_t *cu_seqlens, attn_stream_t stream);
+
+/* Options of attn_fwd_ex.  Zero-initialise and set what is needed. */
+typedef struct {
+    uint64_t wait_timeout_ns; /* bound on each device-side wait; 0 = 2 s */
+    int fault_inject;         /* 0 = none; 1 = CTA 0 never issues its first K copy,
+                                 so a bounded wait must expire (tests only) */
+    int max_ctas;             /* 0 = one persistent CTA per SM; else at most this many */
+} attn_fwd_options;
+
+/* attn_fwd with options (opts may be NULL).  Same arguments and errors. */
+int attn_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse,
+                int B, int H, int N, int d, float scale, int causal,
+                const int32_t *cu_seqlens, attn_stream_t stream,
+                const attn_fwd_options *opts);
+
+/*
+ * Synchronises `stream`, then returns and clears the device-side error word
+ * of the current device: ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT (a bounded wait
+ * expired; the kernel stopped early and its outputs are incomplete) or
+ * ATTN_ERR_SEQLENS (invalid cu_seqlens; nothing was computed).  Returns
+ * ATTN_ERR_CUDA if the synchronisation itself fails.
+ */
+int attn_last_device_error(attn_stream_t stream);
+
+/* Identifier of the wait that expired, as read by the last
+ * attn_last_device_error call (0 if none); for diagnostics. */
+int attn_last_error_site(void);
+
+/* The cudaError_t behind the last ATTN_ERR_CUDA of this thread (0 if none). */
+int attn_last_cuda_error(void);
+
+/* A static, human-readable name of a status code. */
+const char *attn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IO_AWARE_EXACT_06_ATTN_FWD_H */

@@ -1,0 +1,154 @@
+"""GB300 (sm_103a) fused exact attention forward.
+
+A thin ctypes binding of the C ABI in ``include/attn_fwd.h`` (the library
+``_build/libattn_fwd.so``, built by ``build.py``).  The functions here only
+marshal arguments: every step of the computation runs in the library's CUDA
+kernels.  There is no CPU path: calling the library without it built, or on a
+device other than sm_103, raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+__all__ = ["attn_fwd", "attn_fwd_ex", "attn_last_device_error", "attn_last_error_site",
+           "attn_status_string", "AttnError", "AttnFwdOptions", "lib", "forward",
+           "EXPORTED_SYMBOLS"]
+
+# Every symbol include/attn_fwd.h declares.
+EXPORTED_SYMBOLS = ("attn_fwd", "attn_fwd_ex", "attn_last_device_error", "attn_last_error_site",
+                    "attn_last_cuda_error", "attn_status_string")
+
+ATTN_OK = 0
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str = "attn_fwd"):
+        self.status = status
+        extra = f" (cudaError {lib().attn_last_cuda_error()})" if status == -6 else ""
+        super().__init__(f"{what} failed: {attn_status_string(status)} [{status}]{extra}")
+
+
+class AttnFwdOptions(ctypes.Structure):
+    _fields_ = [("wait_timeout_ns", ctypes.c_uint64),
+                ("fault_inject", ctypes.c_int),
+                ("max_ctas", ctypes.c_int)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"CUDA library not built: {path} is missing "
+                               "(run `python -m io_aware_exact_06_gb300.build`)")
+        L = ctypes.CDLL(path)
+        vp, i = ctypes.c_void_p, ctypes.c_int
+        sig = [vp, vp, vp, vp, vp, i, i, i, i, ctypes.c_float, i, vp, vp]
+        L.attn_fwd.argtypes = sig
+        L.attn_fwd.restype = i
+        L.attn_fwd_ex.argtypes = sig + [ctypes.POINTER(AttnFwdOptions)]
+        L.attn_fwd_ex.restype = i
+        L.attn_last_device_error.argtypes = [vp]
+        L.attn_last_device_error.restype = i
+        L.attn_last_error_site.restype = i
+        L.attn_last_cuda_error.restype = i
+        L.attn_status_string.argtypes = [i]
+        L.attn_status_string.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def _ptr(x) -> int | None:
+    """A device pointer from a torch tensor, an int address or None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None or isinstance(stream, int):
+        return stream
+    return stream.cuda_stream  # torch.cuda.Stream
+
+
+def attn_status_string(status: int) -> str:
+    return lib().attn_status_string(int(status)).decode()
+
+
+def attn_fwd(q, k, v, o, lse, B: int, H: int, N: int, d: int, scale: float, causal: bool,
+             cu_seqlens=None, stream=None) -> int:
+    """The C call ``attn_fwd`` with the same arguments (tensors or addresses).
+
+    Raises AttnError on a non-zero status; returns 0."""
+    st = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(N),
+                        int(d), float(scale), int(bool(causal)), _ptr(cu_seqlens), _stream(stream))
+    if st != ATTN_OK:
+        raise AttnError(st)
+    return st
+
+
+def attn_fwd_ex(q, k, v, o, lse, B: int, H: int, N: int, d: int, scale: float, causal: bool,
+                cu_seqlens=None, stream=None, wait_timeout_ns: int = 0, fault_inject: int = 0,
+                max_ctas: int = 0) -> int:
+    """The C call ``attn_fwd_ex``; options as keyword arguments."""
+    opts = AttnFwdOptions(int(wait_timeout_ns), int(fault_inject), int(max_ctas))
+    st = lib().attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(N),
+                           int(d), float(scale), int(bool(causal)), _ptr(cu_seqlens),
+                           _stream(stream), ctypes.byref(opts))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_ex")
+    return st
+
+
+def attn_last_device_error(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device error status."""
+    return lib().attn_last_device_error(_stream(stream))
+
+
+def attn_last_error_site() -> int:
+    return lib().attn_last_error_site()
+
+
+def forward(q, k, v, causal: bool, scale: float | None = None, cu_seqlens=None,
+            max_seqlen: int | None = None, out=None, lse=None, stream=None):
+    """Convenience call on torch CUDA tensors.
+
+    Dense: q, k, v are [B, N, H, d] bf16.  Packed: [total, H, d] with
+    cu_seqlens (int32 [B+1], on the device) and max_seqlen.  Returns (o, lse):
+    o like q; lse [B, H, N] (dense) or [H, total] (packed), fp32.
+    Output tensors are allocated by torch when not given.
+    """
+    import torch
+    if q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+        raise TypeError("q, k, v must be bf16")
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous CUDA tensors")
+    d = q.shape[-1]
+    if cu_seqlens is None:
+        B, N, H, _ = q.shape
+        lse_shape = (B, H, N)
+    else:
+        total, H, _ = q.shape
+        B = cu_seqlens.numel() - 1
+        N = int(max_seqlen)
+        lse_shape = (H, total)
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(lse_shape, dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    attn_fwd(q, k, v, out, lse, B, H, N, d, scale, causal, cu_seqlens, stream)
+    return out, lse

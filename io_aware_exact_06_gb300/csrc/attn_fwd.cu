@@ -1,0 +1,259 @@
+// Host side of the C ABI declared in include/attn_fwd.h: argument checks,
+// TMA descriptors, the per-stream scheduling workspace, and the launches of
+// the scheduler kernel (packed variable-length batches) and the persistent
+// fused attention kernel.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "../../include/attn_fwd.h"
+#include "attn_fwd_kernel.cuh"
+
+namespace {
+
+using attn::FwdCfg;
+using attn::FwdParams;
+
+thread_local int g_last_cuda_error = 0;
+int g_last_error_site = 0;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct DeviceState {
+  bool ready = false;
+  int sms = 0;
+  int major = 0, minor = 0;
+  int* err = nullptr;  // [0] error bits, [1] site of an expired wait
+};
+
+struct StreamWorkspace {
+  int* buf = nullptr;       // [0] entry count, [1..3] unused, [4..] (seq, q-block) pairs
+  int64_t capacity = 0;     // entries
+};
+
+std::mutex g_mu;
+std::map<int, DeviceState> g_dev;
+std::map<std::pair<int, attn_stream_t>, StreamWorkspace> g_ws;
+EncodeTiledFn g_encode = nullptr;
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return ATTN_ERR_CUDA;
+}
+
+int get_encode(EncodeTiledFn* out) {
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                      cudaEnableDefault, &q);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (q != cudaDriverEntryPointSuccess || !fn) return cuda_fail(cudaErrorSymbolNotFound);
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  *out = g_encode;
+  return ATTN_OK;
+}
+
+int device_state(int dev, DeviceState** out) {
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    cudaError_t e;
+    if ((e = cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((e = cudaDeviceGetAttribute(&st.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((e = cudaDeviceGetAttribute(&st.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return cuda_fail(e);
+    if (st.major != 10 || st.minor != 3) return ATTN_ERR_ARCH;
+    if ((e = cudaFuncSetAttribute(attn::attn_fwd_kernel<64>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  FwdCfg<64>::kSmemBytes)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((e = cudaFuncSetAttribute(attn::attn_fwd_kernel<128>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  FwdCfg<128>::kSmemBytes)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((e = cudaMalloc(&st.err, 4 * sizeof(int))) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaMemset(st.err, 0, 4 * sizeof(int))) != cudaSuccess) return cuda_fail(e);
+    st.ready = true;
+  }
+  *out = &st;
+  return ATTN_OK;
+}
+
+int stream_workspace(int dev, attn_stream_t stream, int64_t entries, int** out) {
+  StreamWorkspace& ws = g_ws[std::make_pair(dev, stream)];
+  if (ws.capacity < entries || !ws.buf) {
+    cudaError_t e;
+    if (ws.buf) {
+      // the old list may still be read by work queued on this stream
+      if ((e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream))) != cudaSuccess)
+        return cuda_fail(e);
+      cudaFree(ws.buf);
+      ws.buf = nullptr;
+      ws.capacity = 0;
+    }
+    const int64_t cap = entries < 1024 ? 1024 : entries;
+    if ((e = cudaMalloc(&ws.buf, (size_t)(4 + 2 * cap) * sizeof(int))) != cudaSuccess)
+      return cuda_fail(e);
+    ws.capacity = cap;
+  }
+  *out = ws.buf;
+  return ATTN_OK;
+}
+
+// 3-D view [tokens, H, d] of a bf16 tensor; box = 128 tokens x 1 head x 64
+// elements (128 bytes, the 128-byte swizzle span).
+int make_map(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int64_t tokens, int H, int d) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)tokens};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)attn::kBM};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+  return ATTN_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+template <int D>
+int launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                const FwdParams& p, int grid, cudaStream_t s) {
+  attn::attn_fwd_kernel<D><<<grid, attn::kThreads, FwdCfg<D>::kSmemBytes, s>>>(mq, mk, mv, p);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int H, int N, int d, float scale, int causal,
+                           const int32_t* cu_seqlens, attn_stream_t stream,
+                           const attn_fwd_options* opts) {
+  if (B < 0 || H < 0 || N < 0) return ATTN_ERR_SHAPE;
+  if (d != 64 && d != 128) return ATTN_ERR_HEADDIM;
+  if (!std::isfinite(scale)) return ATTN_ERR_SCALE;
+  if (B == 0 || H == 0 || N == 0) return ATTN_OK;
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return ATTN_ERR_ALIGN;
+  // token indices and the TMA outer extent stay within int32
+  const int64_t tokens_bound = (int64_t)B * N;
+  if (tokens_bound > INT32_MAX - 2 * attn::kBN || (int64_t)H * d > (1 << 20) || H > 65535)
+    return ATTN_ERR_SHAPE;
+  const int64_t nqb = (N + attn::kUnitRows - 1) / attn::kUnitRows;
+  const int64_t units = (int64_t)B * nqb * H;
+  if (units > INT32_MAX) return ATTN_ERR_SHAPE;
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  DeviceState* ds = nullptr;
+  int st = device_state(dev, &ds);
+  if (st != ATTN_OK) return st;
+  EncodeTiledFn enc = nullptr;
+  if ((st = get_encode(&enc)) != ATTN_OK) return st;
+
+  // The token extent of the TMA view is B*N.  Dense: exact.  Packed: an upper
+  // bound of cu_seqlens[B] (every length <= N, checked on the device before
+  // any load); the kernel never asks for a token at or past the end of its
+  // sequence, so no copy reads beyond the caller's buffer.
+  CUtensorMap mq, mk, mv;
+  if ((st = make_map(enc, &mq, q, tokens_bound, H, d)) != ATTN_OK) return st;
+  if ((st = make_map(enc, &mk, k, tokens_bound, H, d)) != ATTN_OK) return st;
+  if ((st = make_map(enc, &mv, v, tokens_bound, H, d)) != ATTN_OK) return st;
+
+  FwdParams p{};
+  p.o = reinterpret_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.cu_seqlens = cu_seqlens;
+  p.err = ds->err;
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.causal = causal ? 1 : 0;
+  p.scale = scale;
+  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p.timeout_ns = (opts && opts->wait_timeout_ns) ? opts->wait_timeout_ns : 2000000000ull;
+  p.fault_inject = opts ? opts->fault_inject : 0;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int grid = ds->sms;
+  if (cu_seqlens) {
+    int* ws = nullptr;
+    const int64_t max_entries = (int64_t)B * nqb;
+    if ((st = stream_workspace(dev, stream, max_entries, &ws)) != ATTN_OK) return st;
+    p.num_entries = ws;
+    p.work = ws + 4;
+    const int ncost = (int)std::min<int64_t>((N + attn::kBN - 1) / attn::kBN,
+                                             attn::kMaxCostBuckets - 1);
+    attn::build_worklist_kernel<<<1, 1024, (ncost + 1) * sizeof(int), s>>>(
+        cu_seqlens, B, N, p.causal, ws + 4, ws, ds->err, (int)max_entries);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+  } else if (units < grid) {
+    grid = (int)units;
+  }
+  if (opts && opts->max_ctas > 0 && opts->max_ctas < grid) grid = opts->max_ctas;
+  return d == 64 ? launch_attn<64>(mq, mk, mv, p, grid, s) : launch_attn<128>(mq, mk, mv, p, grid, s);
+}
+
+extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int H, int N, int d, float scale, int causal, const int32_t* cu_seqlens,
+                        attn_stream_t stream) {
+  return attn_fwd_ex(q, k, v, o, lse, B, H, N, d, scale, causal, cu_seqlens, stream, nullptr);
+}
+
+extern "C" int attn_last_device_error(attn_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e);
+  auto it = g_dev.find(dev);
+  if (it == g_dev.end() || !it->second.ready) {
+    g_last_error_site = 0;
+    return ATTN_OK;
+  }
+  int h[2] = {0, 0};
+  if ((e = cudaMemcpy(h, it->second.err, sizeof h, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e);
+  if ((e = cudaMemset(it->second.err, 0, sizeof h)) != cudaSuccess) return cuda_fail(e);
+  g_last_error_site = h[1];
+  if (h[0] & attn::kErrTimeout) return ATTN_ERR_DEVICE_TIMEOUT;
+  if (h[0] & attn::kErrSeqlens) return ATTN_ERR_SEQLENS;
+  if (h[0] & attn::kErrWorklist) return ATTN_ERR_SHAPE;
+  return ATTN_OK;
+}
+
+extern "C" int attn_last_error_site(void) { return g_last_error_site; }
+
+extern "C" int attn_last_cuda_error(void) { return g_last_cuda_error; }
+
+extern "C" const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_NULL: return "null pointer";
+    case ATTN_ERR_SHAPE: return "bad shape";
+    case ATTN_ERR_HEADDIM: return "head dim must be 64 or 128";
+    case ATTN_ERR_ALIGN: return "misaligned pointer";
+    case ATTN_ERR_SCALE: return "scale is not finite";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case ATTN_ERR_SEQLENS: return "invalid cu_seqlens";
+    case ATTN_ERR_ARCH: return "device is not sm_103";
+    default: return "unknown status";
+  }
+}

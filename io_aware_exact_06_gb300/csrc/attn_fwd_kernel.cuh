@@ -1,0 +1,663 @@
+// Fused exact softmax-attention forward for sm_103a (GB300).
+//
+// O = softmax(scale * Q K^T) V and LSE = log(sum exp(scale * Q K^T)) per row,
+// computed tile by tile with a running row max m and running row sum l, so the
+// N x N score (S) and probability (P) matrices never reach HBM.
+//   - tiling + online softmax + one fused kernel: "flash-attention-evolution"
+//     (letsgetai), FlashAttention section "核心机制" (items 1-2 and the
+//     two-segment merge equations); "FlashAttention" (compassingai), section 3;
+//   - query-tile-outer / KV-tile-inner loop, query tiles spread over CTAs:
+//     "FlashAttention 1-4 演进速查" (argus-lessons), FlashAttention-2 items;
+//   - producer warp + MMA warp + softmax warps (warp specialisation) and the
+//     softmax of one tile overlapping the MMAs of another (ping-pong), with
+//     registers moved between warp roles (setmaxnreg): same page,
+//     FlashAttention-3 items;
+//   - accumulators in tensor memory (TMEM), asynchronous MMA pipeline,
+//     conditional rescaling of O, longest-processing-time-first scheduling:
+//     same page, FlashAttention-4 items.
+//
+// CTA layout (384 threads = 3 warpgroups, one CTA per SM, persistent):
+//   warps 0-3   softmax group 0: query tile 0 of the unit, one thread per row
+//   warps 4-7   softmax group 1: query tile 1 of the unit
+//   warp  8     TMA producer (lane 0): Q tiles, then K_j, V_j into a ring
+//   warp  9     MMA issuer (lane 0) and TMEM owner
+//   warps 10-11 idle
+// Registers are moved from the third warpgroup to the softmax warpgroups with
+// setmaxnreg (launch: 384 x 168; after: 256 x 216 + 128 x 72 <= 384 x 168).
+// A work unit is (sequence, head, 256 query rows) = two 128-row query tiles.
+// Per KV tile j the tensor core runs, in order,
+//   O0 += P0 V_{j-1};  S0 = Q0 K_j^T;  O1 += P1 V_{j-1};  S1 = Q1 K_j^T
+// so softmax group 0 works on S0 while the tensor core runs group 1's MMAs
+// and the other way round.  P_g is written back into the TMEM columns of S_g
+// (bf16 pairs) and read from there as the A operand of the PV product.
+//
+// TMEM (512 columns x 128 lanes x 32 bit): S0 [0,128), S1 [128,256),
+// O0 [256, 256+D), O1 [256+D, 256+2D).
+//
+// Every wait is bounded; on a timeout the kernel records an error word, stops
+// issuing work, lets copies in flight land, frees TMEM and returns.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "sm100_ptx.cuh"
+
+namespace attn {
+
+constexpr int kBM = 128;               // query rows per tile (= TMEM lanes)
+constexpr int kBN = 128;               // keys per KV tile
+constexpr int kQTiles = 2;             // query tiles per work unit
+constexpr int kUnitRows = kBM * kQTiles;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 384;
+constexpr int kLaunchRegs = 168;        // 65536 / 384, rounded down to 8
+constexpr int kSoftmaxRegs = 216;
+constexpr int kControlRegs = 72;
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * kLaunchRegs,
+              "register split exceeds the launch allotment");
+constexpr int kChunkBytes = kBM * 128; // 128 rows x 64 bf16 (one 128-byte swizzle span)
+constexpr float kRescaleLog2 = 8.0f;   // rescale O only if the row max grew by > 2^8
+
+// Device error word bits.
+constexpr int kErrTimeout = 1;
+constexpr int kErrSeqlens = 2;
+constexpr int kErrWorklist = 4;
+
+struct FwdParams {
+  __nv_bfloat16* o;        // [tokens, H, D]
+  float* lse;              // dense [B, H, N]; varlen [H, tokens]
+  const int* cu_seqlens;   // null: dense batch of B sequences of length N
+  const int* work;         // varlen: LPT-ordered (seq, q-block) pairs
+  const int* num_entries;  // varlen: number of pairs in `work`
+  int* err;                // err[0]: error bits; err[1]: where a wait gave up
+  int B, H, N;
+  int causal;
+  float scale;             // softmax scale on the logits
+  float scale_log2;        // scale * log2(e)
+  unsigned long long timeout_ns;
+  int fault_inject;        // 1: CTA 0 never issues its first K copy (test hook)
+};
+
+template <int D>
+struct FwdCfg {
+  static_assert(D == 64 || D == 128, "head dim 64 or 128");
+  static constexpr int kChunks = D / 64;
+  static constexpr int kTileBytes = kChunks * kChunkBytes;   // one 128 x D bf16 tile
+  static constexpr int kStages = D == 128 ? 4 : 8;           // K/V ring slots
+  static constexpr int kSmemQ = kQTiles * kTileBytes;
+  static constexpr int kSmemRing = kStages * kTileBytes;
+  static constexpr int kSmemBytes = kSmemQ + kSmemRing + 1024;  // + alignment slack
+  // TMEM column of S_g (P_g aliases its first 64 columns) and of O_g
+  __host__ __device__ static constexpr uint32_t col_s(int g) { return (uint32_t)g * 128u; }
+  __host__ __device__ static constexpr uint32_t col_o(int g) { return 256u + (uint32_t)g * D; }
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kIdescS = make_idesc_bf16(kBM, kBN, false);
+  static constexpr uint32_t kIdescPV = make_idesc_bf16(kBM, D, true);
+};
+
+// Barrier slots in shared memory.
+enum : int {
+  kBarQFull = 0,
+  kBarQEmpty = 1,
+  kBarSFull = 2,   // +g
+  kBarPFull = 4,   // +g
+  kBarOFull = 6,   // +g
+  kBarDrain = 8,
+  kBarKV = 9,      // kv_full[s] = kBarKV + s, kv_empty[s] = kBarKV + kStages + s
+};
+constexpr int kMaxBars = kBarKV + 2 * 8;
+
+// One work unit: rows [256 qb, 256 qb + 256) of head h of one sequence.
+struct Unit {
+  int seq, h, qb;
+  int tok0;  // first token of the sequence in the packed tensors
+  int L;     // sequence length
+  int nkv;   // KV tiles visited
+};
+
+__device__ __forceinline__ int num_units(const FwdParams& p) {
+  if (p.cu_seqlens) return *p.num_entries * p.H;
+  const int nqb = (p.N + kUnitRows - 1) / kUnitRows;
+  return p.B * p.H * nqb;
+}
+
+// Unit u of the longest-first order.  Dense: q-blocks in decreasing cost
+// (causal cost grows with the q-block index), then batch, then head.  Varlen:
+// the scheduler kernel's sorted (seq, q-block) list, then head.
+__device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
+  Unit un;
+  const int e = u / p.H;
+  un.h = u - e * p.H;
+  if (p.cu_seqlens) {
+    un.seq = p.work[2 * e];
+    un.qb = p.work[2 * e + 1];
+    un.tok0 = p.cu_seqlens[un.seq];
+    un.L = p.cu_seqlens[un.seq + 1] - un.tok0;
+  } else {
+    const int nqb = (p.N + kUnitRows - 1) / kUnitRows;
+    const int rank = e / p.B;
+    un.seq = e - rank * p.B;
+    un.qb = nqb - 1 - rank;
+    un.tok0 = un.seq * p.N;
+    un.L = p.N;
+  }
+  const int row_end = p.causal ? min(un.L, (un.qb + 1) * kUnitRows) : un.L;
+  un.nkv = (row_end + kBN - 1) / kBN;
+  return un;
+}
+
+// First row (sequence-relative) actually loaded for query tile g: the nominal
+// start, pulled back so the 128-row tile ends at the sequence end at the
+// latest.  Rows before the nominal start are recomputed but never stored.
+__device__ __forceinline__ int q_tile_start(const Unit& un, int g) {
+  return min(un.qb * kUnitRows + g * kBM, un.L - kBM);
+}
+// First key actually loaded for KV tile j (same pull-back at the sequence end;
+// keys before 128*j were already visited and are masked out).
+__device__ __forceinline__ int kv_tile_start(const Unit& un, int j) {
+  return min(j * kBN, un.L - kBN);
+}
+
+struct SharedState {
+  uint64_t bars[kMaxBars];
+  uint32_t tmem_base;
+  volatile int abort_flag;
+};
+
+// Bounded wait on an mbarrier phase; gives up on timeout or when another warp
+// has aborted.  `where` identifies the wait in the error record.
+__device__ __forceinline__ bool wait_bar(SharedState& ss, int bar, uint32_t parity,
+                                         const FwdParams& p, int where) {
+  const uint32_t a = smem_u32(&ss.bars[bar]);
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (mbar_try_wait(a, parity)) return true;
+    if (ss.abort_flag) return false;
+    if (globaltimer_ns() - t0 > p.timeout_ns) {
+      ss.abort_flag = 1;
+      atomicOr(p.err, kErrTimeout);
+      atomicCAS(p.err + 1, 0, where);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t bar_addr(SharedState& ss, int bar) {
+  return smem_u32(&ss.bars[bar]);
+}
+
+// ------------------------------------------------------------ producer --
+template <int D>
+__device__ __forceinline__ void producer_loop(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                                              const CUtensorMap* tm_v, const FwdParams& p,
+                                              SharedState& ss, uint8_t* sQ, uint8_t* sRing,
+                                              int n_units) {
+  using C = FwdCfg<D>;
+  uint32_t ring = 0;
+  int units_done = 0;
+  bool injected = false;
+  for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+    const Unit un = decode_unit(p, u);
+    if (units_done > 0 && !wait_bar(ss, kBarQEmpty, (units_done - 1) & 1, p, 1)) return;
+    mbar_arrive_expect_tx(bar_addr(ss, kBarQFull), kQTiles * C::kTileBytes);
+    for (int g = 0; g < kQTiles; ++g) {
+      const int r0 = un.tok0 + q_tile_start(un, g);
+      for (int c = 0; c < C::kChunks; ++c)
+        tma_load_3d(smem_u32(sQ + g * C::kTileBytes + c * kChunkBytes), tm_q,
+                    bar_addr(ss, kBarQFull), c * 64, un.h, r0);
+    }
+    for (int j = 0; j < un.nkv; ++j) {
+      const int k0 = un.tok0 + kv_tile_start(un, j);
+      for (int kind = 0; kind < 2; ++kind) {
+        const int slot = ring % C::kStages;
+        const uint32_t n = ring / C::kStages;
+        if (n > 0 && !wait_bar(ss, kBarKV + C::kStages + slot, (n - 1) & 1, p, 2)) return;
+        const uint32_t full = bar_addr(ss, kBarKV + slot);
+        mbar_arrive_expect_tx(full, C::kTileBytes);
+        if (p.fault_inject == 1 && blockIdx.x == 0 && !injected && kind == 0) {
+          injected = true;  // test hook: the bytes this barrier waits for never come
+        } else {
+          const CUtensorMap* tm = kind == 0 ? tm_k : tm_v;
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(smem_u32(sRing + slot * C::kTileBytes + c * kChunkBytes), tm, full,
+                        c * 64, un.h, k0);
+        }
+        ++ring;
+      }
+    }
+    ++units_done;
+  }
+}
+
+// ----------------------------------------------------------------- MMA --
+// S = Q K^T over D/16 MMAs of K-depth 16.  Both operands K-major, 128-byte
+// swizzle: 64-element chunks of 128 rows each (16 KB apart), 8-row groups
+// 1024 bytes apart; a 16-element step inside a chunk advances the start
+// address by 32 bytes.
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+  using C = FwdCfg<D>;
+  const uint64_t a0 = make_sdesc(q_smem, 16, 1024, kSwizzle128B);
+  const uint64_t b0 = make_sdesc(k_smem, 16, 1024, kSwizzle128B);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t off = (uint64_t)(((kk / 4) * kChunkBytes + (kk % 4) * 32) >> 4);
+    mma_ss(d_tmem, a0 + off, b0 + off, C::kIdescS, kk > 0 ? 1u : 0u);
+  }
+}
+
+// O (+)= P V over 128/16 MMAs.  P: bf16 pairs in TMEM (8 columns per 16
+// keys).  V: MN-major (d contiguous), 128-byte swizzle: 64-element d chunks
+// 16 KB apart (leading offset), 8-key groups 1024 bytes apart (stride
+// offset); 16 keys advance the start address by 2048 bytes.
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
+                                         bool accumulate) {
+  using C = FwdCfg<D>;
+  const uint64_t b0 = make_sdesc(v_smem, kChunkBytes, 1024, kSwizzle128B);
+  const uint32_t acc0 = accumulate ? 1u : 0u;
+#pragma unroll
+  for (int kk = 0; kk < kBN / 16; ++kk)
+    mma_ts(d_tmem, p_tmem + kk * 8, b0 + (uint64_t)((kk * 2048) >> 4), C::kIdescPV,
+           kk > 0 ? 1u : acc0);
+}
+
+template <int D>
+__device__ __forceinline__ void mma_loop(const FwdParams& p, SharedState& ss, uint8_t* sQ,
+                                         uint8_t* sRing, uint32_t tmem, int n_units) {
+  using C = FwdCfg<D>;
+  uint32_t ring = 0;
+  uint32_t pcount[2] = {0, 0};
+  int units_done = 0;
+  const uint32_t q_smem[2] = {smem_u32(sQ), smem_u32(sQ + C::kTileBytes)};
+  auto slot_smem = [&](uint32_t pos) { return smem_u32(sRing + (pos % C::kStages) * C::kTileBytes); };
+  auto wait_full = [&](uint32_t pos) {
+    return wait_bar(ss, kBarKV + pos % C::kStages, (pos / C::kStages) & 1, p, 10);
+  };
+  auto release = [&](uint32_t pos) { mma_commit(bar_addr(ss, kBarKV + C::kStages + pos % C::kStages)); };
+
+  for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+    const Unit un = decode_unit(p, u);
+    if (!wait_bar(ss, kBarQFull, units_done & 1, p, 11)) return;
+    tc_fence_after();
+    uint32_t posK = ring, posV = ring + 1;
+    ring += 2;
+    if (!wait_full(posK)) return;
+    tc_fence_after();
+    for (int g = 0; g < kQTiles; ++g) {
+      issue_qk<D>(tmem + C::col_s(g), q_smem[g], slot_smem(posK));
+      mma_commit(bar_addr(ss, kBarSFull + g));
+    }
+    release(posK);
+    // Q is free for the next unit's copy once the unit's last S product is done
+    if (un.nkv == 1) mma_commit(bar_addr(ss, kBarQEmpty));
+    for (int j = 1; j <= un.nkv; ++j) {
+      const bool more = j < un.nkv;
+      uint32_t nextK = 0, nextV = 0;
+      if (more) {
+        nextK = ring;
+        nextV = ring + 1;
+        ring += 2;
+      }
+      if (!wait_full(posV)) return;
+      for (int g = 0; g < kQTiles; ++g) {
+        // P_g of tile j-1 is in TMEM (and O_g rescaled if needed)
+        if (!wait_bar(ss, kBarPFull + g, pcount[g] & 1, p, 12 + g)) return;
+        ++pcount[g];
+        tc_fence_after();
+        issue_pv<D>(tmem + C::col_o(g), tmem + C::col_s(g), slot_smem(posV), j > 1);
+        if (g == kQTiles - 1) release(posV);
+        if (more) {
+          if (g == 0) {
+            if (!wait_full(nextK)) return;
+            tc_fence_after();
+          }
+          issue_qk<D>(tmem + C::col_s(g), q_smem[g], slot_smem(nextK));
+          mma_commit(bar_addr(ss, kBarSFull + g));
+        } else {
+          mma_commit(bar_addr(ss, kBarOFull + g));
+        }
+      }
+      if (more) {
+        release(nextK);
+        if (j == un.nkv - 1) mma_commit(bar_addr(ss, kBarQEmpty));
+        posV = nextV;
+      }
+    }
+    ++units_done;
+  }
+}
+
+// ------------------------------------------------------------- softmax --
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// The two bf16 halves of a packed pair, widened exactly to fp32.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+template <int D>
+__device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss, uint32_t tmem,
+                                             int g, int n_units) {
+  using C = FwdCfg<D>;
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int trow = (warp % 4) * 32 + lane;  // row within the tile = TMEM lane
+  const uint32_t lane_addr = tmem + ((uint32_t)((warp % 4) * 32) << 16);
+  const uint32_t colS = C::col_s(g), colO = C::col_o(g);
+  const float c2 = p.scale_log2;
+  uint32_t scount = 0;
+  int units_done = 0;
+  int tokens_total = 0;
+  if (p.cu_seqlens) tokens_total = p.cu_seqlens[p.B];
+
+  for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+    const Unit un = decode_unit(p, u);
+    const int a0 = q_tile_start(un, g);
+    const int row = a0 + trow;                       // sequence-relative row of this thread
+    const int nominal0 = un.qb * kUnitRows + g * kBM;
+    float m_used = -INFINITY;
+    float l = 0.f;    // sum of the fp32 probabilities: the LSE
+    float l_r = 0.f;  // sum of the bf16-rounded probabilities the PV product used: O's divisor
+    for (int j = 0; j < un.nkv; ++j) {
+      if (!__all_sync(0xffffffffu, wait_bar(ss, kBarSFull + g, scount & 1, p, 20 + g))) return;
+      ++scount;
+      tc_fence_after();
+      float s[kBN];
+      {
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        tmem_ld_x32(lane_addr + colS + 0, r0);
+        tmem_ld_x32(lane_addr + colS + 32, r1);
+        tmem_ld_x32(lane_addr + colS + 64, r2);
+        tmem_ld_x32(lane_addr + colS + 96, r3);
+        tmem_ld_wait_x32(r0);
+        tmem_ld_wait_x32(r1);
+        tmem_ld_wait_x32(r2);
+        tmem_ld_wait_x32(r3);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          s[i] = __uint_as_float(r0[i]);
+          s[32 + i] = __uint_as_float(r1[i]);
+          s[64 + i] = __uint_as_float(r2[i]);
+          s[96 + i] = __uint_as_float(r3[i]);
+        }
+      }
+      // Mask: keys already visited by the previous tile (pulled-back last
+      // tile) and, when causal, keys after this row.  The pull-back keeps
+      // every loaded key inside the sequence.  Decided per group, applied
+      // per row.
+      const int b0 = kv_tile_start(un, j);
+      const int lo = j * kBN - b0;
+      const bool need_mask = lo > 0 || (p.causal && b0 + kBN - 1 > a0);
+      if (need_mask) {
+        const int hi = p.causal ? min(row - b0, kBN - 1) : kBN - 1;
+#pragma unroll
+        for (int c = 0; c < kBN; ++c)
+          if (c < lo || c > hi) s[c] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+      const float m_new = fmaxf(m_used, mx);
+      if (j == 0) {
+        m_used = m_new;
+      } else {
+        const bool resc = (m_new - m_used) * c2 > kRescaleLog2;
+        if (__any_sync(0xffffffffu, resc)) {
+          const float alpha = resc ? ex2_approx((m_used - m_new) * c2) : 1.0f;
+#pragma unroll
+          for (int cc = 0; cc < D; cc += 32) {
+            uint32_t r[32];
+            tmem_ld_x32(lane_addr + colO + cc, r);
+            tmem_ld_wait_x32(r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st_x32(lane_addr + colO + cc, r);
+          }
+          tmem_st_wait();
+          l *= alpha;
+          l_r *= alpha;
+          if (resc) m_used = m_new;
+        }
+      }
+      const float neg = m_used == -INFINITY ? 0.f : -m_used * c2;
+      float sum = 0.f, sum_r = 0.f;
+      uint32_t pa[32], pb[32];
+#pragma unroll
+      for (int c = 0; c < kBN / 2; c += 2) {
+        const float p0 = ex2_approx(fmaf(s[c], c2, neg));
+        const float p1 = ex2_approx(fmaf(s[c + 1], c2, neg));
+        sum += p0 + p1;
+        pa[c / 2] = pack_bf16x2(p0, p1);
+        sum_r += bf16_lo(pa[c / 2]) + bf16_hi(pa[c / 2]);
+      }
+#pragma unroll
+      for (int c = kBN / 2; c < kBN; c += 2) {
+        const float p0 = ex2_approx(fmaf(s[c], c2, neg));
+        const float p1 = ex2_approx(fmaf(s[c + 1], c2, neg));
+        sum += p0 + p1;
+        const int i = (c - kBN / 2) / 2;
+        pb[i] = pack_bf16x2(p0, p1);
+        sum_r += bf16_lo(pb[i]) + bf16_hi(pb[i]);
+      }
+      l += sum;
+      l_r += sum_r;
+      tmem_st_x32(lane_addr + colS, pa);
+      tmem_st_x32(lane_addr + colS + 32, pb);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar_addr(ss, kBarPFull + g));
+    }
+    // Epilogue: O / l_r -> bf16, LSE = scale * m + ln(l).  Rows before the
+    // nominal tile start (recomputed) and rows past the sequence are skipped.
+    if (!__all_sync(0xffffffffu, wait_bar(ss, kBarOFull + g, units_done & 1, p, 22 + g))) return;
+    tc_fence_after();
+    const bool store = row >= nominal0 && row < un.L && row >= 0;
+    // Dividing by the sum of the weights actually multiplied into V keeps a
+    // dominant term exact (its bf16 rounding cancels); the LSE uses the fp32 sum.
+    const float inv_l = l_r > 0.f ? 1.0f / l_r : 0.f;
+    __nv_bfloat16* orow = p.o + ((size_t)(store ? un.tok0 + row : 0) * p.H + un.h) * D;
+#pragma unroll
+    for (int cc = 0; cc < D; cc += 32) {
+      uint32_t r[32];
+      tmem_ld_x32(lane_addr + colO + cc, r);
+      tmem_ld_wait_x32(r);
+      if (store) {
+        uint4* dst = reinterpret_cast<uint4*>(orow + cc);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(r[8 * i + 0]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l);
+          w.y = pack_bf16x2(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l);
+          w.z = pack_bf16x2(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l);
+          w.w = pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l);
+          dst[i] = w;
+        }
+      }
+    }
+    if (store) {
+      const float lse = l > 0.f ? m_used * p.scale + __log2f(l) * 0.69314718055994531f : -INFINITY;
+      size_t idx;
+      if (p.cu_seqlens)
+        idx = (size_t)un.h * tokens_total + un.tok0 + row;
+      else
+        idx = ((size_t)un.seq * p.H + un.h) * p.N + row;
+      p.lse[idx] = lse;
+    }
+    tc_fence_before();
+    ++units_done;
+  }
+}
+
+// -------------------------------------------------------------- kernel --
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ SharedState ss;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sRing = smem + C::kSmemQ;
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_addr(ss, kBarQFull), 1);
+    mbar_init(bar_addr(ss, kBarQEmpty), 1);
+    for (int g = 0; g < kQTiles; ++g) {
+      mbar_init(bar_addr(ss, kBarSFull + g), 1);
+      mbar_init(bar_addr(ss, kBarPFull + g), kBM);
+      mbar_init(bar_addr(ss, kBarOFull + g), 1);
+    }
+    mbar_init(bar_addr(ss, kBarDrain), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar_addr(ss, kBarKV + s), 1);
+      mbar_init(bar_addr(ss, kBarKV + C::kStages + s), 1);
+    }
+    ss.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(&ss.tmem_base), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ss.tmem_base;
+  const int n_units = num_units(p);
+
+  if (warp >= 8) {
+    setmaxnreg_dec<kControlRegs>();
+    if (warp == kProducerWarp) {
+      if (lane == 0) producer_loop<D>(&tm_q, &tm_k, &tm_v, p, ss, sQ, sRing, n_units);
+    } else if (warp == kMmaWarp) {
+      if (lane == 0) {
+        mma_loop<D>(p, ss, sQ, sRing, tmem, n_units);
+        // every MMA issued by this thread has finished before TMEM is freed
+        mma_commit(bar_addr(ss, kBarDrain));
+        mbar_wait(bar_addr(ss, kBarDrain), 0, 100000000ull);
+      }
+    }
+    __syncwarp();
+  } else {
+    setmaxnreg_inc<kSoftmaxRegs>();
+    softmax_loop<D>(p, ss, tmem, warp / 4, n_units);
+    __syncwarp();
+  }
+
+  if (ss.abort_flag) {
+    // copies issued before the abort may still be landing: give them 1 ms
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 1000000ull) {
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ----------------------------------------------------------- scheduler --
+// Builds the longest-first list of (sequence, q-block) pairs of a packed
+// variable-length batch and validates cu_seqlens.  One CTA.  Cost of a pair =
+// KV tiles it visits; a counting sort over cost in descending order.
+constexpr int kMaxCostBuckets = 8192;
+
+__global__ void __launch_bounds__(1024)
+build_worklist_kernel(const int* cu_seqlens, int nseq, int max_len, int causal, int* work,
+                      int* num_entries, int* err, int max_entries) {
+  extern __shared__ int hist[];  // [ncost + 1]
+  __shared__ int bad;
+  __shared__ int total;
+  const int ncost = min((max_len + kBN - 1) / kBN, kMaxCostBuckets - 1);
+  for (int i = threadIdx.x; i <= ncost; i += blockDim.x) hist[i] = 0;
+  if (threadIdx.x == 0) {
+    bad = cu_seqlens[0] != 0;
+    total = 0;
+  }
+  __syncthreads();
+  for (int s = threadIdx.x; s < nseq; s += blockDim.x) {
+    const int L = cu_seqlens[s + 1] - cu_seqlens[s];
+    if (L < 0 || L > max_len) bad = 1;
+  }
+  __syncthreads();
+  if (bad) {
+    if (threadIdx.x == 0) {
+      *num_entries = 0;
+      atomicOr(err, kErrSeqlens);
+    }
+    return;
+  }
+  auto cost_of = [&](int L, int qb) {
+    const int row_end = causal ? min(L, (qb + 1) * kUnitRows) : L;
+    return min((row_end + kBN - 1) / kBN, ncost);
+  };
+  for (int s = threadIdx.x; s < nseq; s += blockDim.x) {
+    const int L = cu_seqlens[s + 1] - cu_seqlens[s];
+    const int nqb = (L + kUnitRows - 1) / kUnitRows;
+    for (int qb = 0; qb < nqb; ++qb) atomicAdd(&hist[cost_of(L, qb)], 1);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int off = 0;
+    for (int c = ncost; c >= 0; --c) {
+      const int t = hist[c];
+      hist[c] = off;
+      off += t;
+    }
+    total = off;
+  }
+  __syncthreads();
+  if (total > max_entries) {
+    if (threadIdx.x == 0) {
+      *num_entries = 0;
+      atomicOr(err, kErrWorklist);
+    }
+    return;
+  }
+  for (int s = threadIdx.x; s < nseq; s += blockDim.x) {
+    const int L = cu_seqlens[s + 1] - cu_seqlens[s];
+    const int nqb = (L + kUnitRows - 1) / kUnitRows;
+    for (int qb = 0; qb < nqb; ++qb) {
+      const int pos = atomicAdd(&hist[cost_of(L, qb)], 1);
+      work[2 * pos] = s;
+      work[2 * pos + 1] = qb;
+    }
+  }
+  if (threadIdx.x == 0) *num_entries = total;
+}
+
+}  // namespace attn

@@ -1,0 +1,133 @@
+// Per-SM unit rates of the running GPU, for the rooflines of the attention
+// forward: MUFU exp2 (ex2.approx.ftz.f32) results per clock per SM, and
+// tcgen05 bf16 MMA flops per clock per SM.  Standalone program; prints one
+// JSON object.  Every wait is bounded.
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <vector>
+
+#include "sm100_ptx.cuh"
+
+using namespace attn;
+
+namespace {
+
+constexpr int kChains = 8;
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 1024 threads per SM, kChains independent ex2 chains per thread.
+__global__ void __launch_bounds__(1024, 1) ex2_rate(float* out, long long* cycles, int iters) {
+  float x[kChains];
+  for (int j = 0; j < kChains; ++j) x[j] = (threadIdx.x & 7) * 0.01f - 0.3f * j;
+  __syncthreads();
+  const long long t0 = clock64();
+  for (int i = 0; i < iters; ++i) {
+#pragma unroll
+    for (int j = 0; j < kChains; ++j) x[j] = fmaf(ex2(x[j]), -0.5f, 0.25f);
+  }
+  __syncthreads();
+  const long long t1 = clock64();
+  float s = 0.f;
+  for (int j = 0; j < kChains; ++j) s += x[j];
+  out[blockIdx.x * blockDim.x + threadIdx.x] = s;
+  if (threadIdx.x == 0) cycles[blockIdx.x] = t1 - t0;
+}
+
+// One thread per SM issues n back-to-back 128x256x16 bf16 MMAs into TMEM.
+__global__ void __launch_bounds__(128, 1) mma_rate(long long* cycles, int n, int* err) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tmem_base;
+  const int tid = threadIdx.x, warp = tid / 32;
+  for (int i = tid; i < 65536 / 4; i += 128) reinterpret_cast<uint32_t*>(smem)[i] = 0;
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&tmem_base), 256);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  if (tid == 0) {
+    const uint32_t id = make_idesc_bf16(128, 256, false);
+    const uint64_t a = make_sdesc(smem_u32(smem), 16, 1024, kSwizzle128B);
+    const uint64_t b = make_sdesc(smem_u32(smem + 16384), 16, 1024, kSwizzle128B);
+    const long long t0 = clock64();
+    for (int i = 0; i < n; ++i) mma_ss(tmem, a, b, id, i > 0);
+    mma_commit(smem_u32(&bar));
+    if (!mbar_wait(smem_u32(&bar), 0, 1000000000ull)) atomicOr(err, 1);
+    cycles[blockIdx.x] = clock64() - t0;
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+bool check(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) {
+    printf("{\"error\": \"%s: %s\"}\n", what, cudaGetErrorString(e));
+    return false;
+  }
+  return true;
+}
+
+}  // namespace
+
+int main() {
+  int sms = 0, clk_khz = 0, major = 0, minor = 0;
+  if (!check(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0), "attr")) return 1;
+  cudaDeviceGetAttribute(&clk_khz, cudaDevAttrClockRate, 0);
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, 0);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, 0);
+  float* out = nullptr;
+  long long* cyc = nullptr;
+  int* err = nullptr;
+  if (!check(cudaMalloc(&out, (size_t)sms * 1024 * sizeof(float)), "malloc")) return 1;
+  if (!check(cudaMalloc(&cyc, sms * sizeof(long long)), "malloc")) return 1;
+  if (!check(cudaMalloc(&err, sizeof(int)), "malloc")) return 1;
+  cudaMemset(err, 0, sizeof(int));
+  std::vector<long long> h(sms);
+
+  const int iters = 4096;
+  ex2_rate<<<sms, 1024>>>(out, cyc, 64);
+  ex2_rate<<<sms, 1024>>>(out, cyc, iters);
+  if (!check(cudaDeviceSynchronize(), "ex2_rate")) return 1;
+  cudaMemcpy(h.data(), cyc, sms * sizeof(long long), cudaMemcpyDeviceToHost);
+  double mean = 0;
+  for (long long c : h) mean += (double)c / sms;
+  const double ex2_per_clk = 1024.0 * kChains * iters / mean;
+
+  const int n = 4096;
+  const size_t smem = 65536 + 1024;
+  cudaFuncSetAttribute(mma_rate, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  mma_rate<<<sms, 128, smem>>>(cyc, 64, err);
+  mma_rate<<<sms, 128, smem>>>(cyc, n, err);
+  if (!check(cudaDeviceSynchronize(), "mma_rate")) return 1;
+  cudaMemcpy(h.data(), cyc, sms * sizeof(long long), cudaMemcpyDeviceToHost);
+  int herr = 0;
+  cudaMemcpy(&herr, err, sizeof(int), cudaMemcpyDeviceToHost);
+  mean = 0;
+  for (long long c : h) mean += (double)c / sms;
+  const double mma_flop_per_clk = 2.0 * 128 * 256 * 16 * n / mean;
+  printf("{\"sm_count\": %d, \"sm\": \"%d.%d\", \"max_clock_mhz\": %.0f, \"ex2_per_clk_per_sm\": %.2f, "
+         "\"mma_bf16_flop_per_clk_per_sm\": %.1f, \"mma_wait_error\": %d}\n",
+         sms, major, minor, clk_khz / 1000.0, ex2_per_clk, mma_flop_per_clk, herr);
+  return herr ? 2 : 0;
+}

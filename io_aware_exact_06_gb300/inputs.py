@@ -206,31 +206,37 @@ def sample_rows(cu_seqlens, H: int, count: int, seed: int) -> np.ndarray:
     every row) are held.  The result is sorted.
     """
     cu = np.asarray(cu_seqlens, dtype=np.int64)
-    rows = []
+    lens = np.diff(cu)
+    fixed = []
     for s in range(len(cu) - 1):
-        L = int(cu[s + 1] - cu[s])
+        L = int(lens[s])
         if L == 0:
             continue
-        fixed = sorted({0, L - 1} | {r for r in (127, 128, 255, 256) if r < L})
-        for h in range(H):
-            for r in fixed:
-                rows.append((s, h, r))
-    chosen = set(rows)
-    lens = np.diff(cu)
+        rr = sorted({0, L - 1} | {r for r in (127, 128, 255, 256) if r < L})
+        fixed.extend(int(cu[s]) + r for r in rr)
+    fixed = np.asarray(fixed, dtype=np.int64)
+    # key = token * H + head over the packed (token, head) grid
+    fixed_keys = np.unique((fixed[:, None] * H + np.arange(H, dtype=np.int64)[None, :]).ravel())
     total = int(lens.sum()) * H
-    target = min(count, total)
-    drawn = 0
-    while len(chosen) < target:
-        need = target - len(chosen)
-        draws = splitmix64(seed, drawn, need)
-        drawn += need
-        flat = (draws % np.uint64(total)).astype(np.int64)  # index over (token, head)
-        tok = flat // H
-        hh = flat % H
-        seq = np.searchsorted(cu, tok, side="right") - 1
-        r = tok - cu[seq]
-        chosen.update(zip(seq.tolist(), hh.tolist(), r.tolist()))
-    return np.array(sorted(chosen), dtype=np.int64).reshape(-1, 3)
+    target = min(max(count, fixed_keys.size), total)
+    if target >= total:
+        keys = np.arange(total, dtype=np.int64)
+    else:
+        # the rest: the keys with the smallest SplitMix64 hash (a seeded
+        # sample without repeats, no rejection loop)
+        prio = splitmix64(seed, 0, total)
+        prio[fixed_keys] = 0
+        extra = target - fixed_keys.size
+        free = np.ones(total, dtype=bool)
+        free[fixed_keys] = False
+        cand = np.flatnonzero(free)
+        pick = cand[np.argpartition(prio[cand], extra - 1)[:extra]] if extra > 0 else cand[:0]
+        keys = np.concatenate([fixed_keys, pick])
+    tok = keys // H
+    hh = keys % H
+    seq = np.searchsorted(cu, tok, side="right") - 1
+    out = np.stack([seq, hh, tok - cu[seq]], axis=1).astype(np.int64)
+    return out[np.lexsort((out[:, 2], out[:, 1], out[:, 0]))]
 
 
 def all_rows(cu_seqlens, H: int) -> np.ndarray:

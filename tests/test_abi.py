@@ -1,0 +1,86 @@
+"""The C-ABI library: it loads without a GPU, exports every declared symbol,
+and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import io_aware_exact_06_gb300 as fa
+from io_aware_exact_06_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return fa.lib()
+
+
+def declared_functions():
+    names = []
+    for f in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if f.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(attn_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_binding_symbols():
+    assert declared_functions() == sorted(fa.EXPORTED_SYMBOLS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    assert fa.attn_status_string(0) == "ok"
+    assert "timed out" in fa.attn_status_string(-7)
+    assert fa.attn_status_string(12345) == "unknown status"
+
+
+BUF = 1 << 20  # fake, 16-byte aligned addresses: validation fails before any use
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(B=-1), -2),
+    (dict(H=-3), -2),
+    (dict(d=96), -3),
+    (dict(d=0), -3),
+    (dict(scale=float("nan")), -5),
+    (dict(scale=float("inf")), -5),
+    (dict(q=None), -1),
+    (dict(lse=None), -1),
+    (dict(q=BUF + 8), -4),
+    (dict(o=BUF + 4), -4),
+    (dict(lse=BUF + 2), -4),
+    (dict(B=70000, N=1 << 16), -2),
+    (dict(H=70000), -2),
+])
+def test_argument_errors(lib, args, status):
+    a = dict(q=BUF, k=BUF, v=BUF, o=BUF, lse=BUF, B=2, H=4, N=256, d=128, scale=0.1,
+             causal=1, cu=None, stream=None)
+    a.update(args)
+    st = lib.attn_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"], a["d"],
+                      a["scale"], a["causal"], a["cu"], a["stream"])
+    assert st == status
+
+
+@pytest.mark.parametrize("zero", ["B", "H", "N"])
+def test_empty_problem_is_a_noop(lib, zero):
+    a = dict(B=2, H=4, N=256)
+    a[zero] = 0
+    # null pointers are fine when there is nothing to do
+    assert lib.attn_fwd(None, None, None, None, None, a["B"], a["H"], a["N"], 64, 0.125, 0,
+                        None, None) == 0
+
+
+def test_binding_raises_on_error(lib):
+    with pytest.raises(fa.AttnError) as e:
+        fa.attn_fwd(BUF, BUF, BUF, BUF, BUF, 1, 1, 128, 80, 0.1, False)
+    assert e.value.status == -3

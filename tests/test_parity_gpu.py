@@ -1,0 +1,149 @@
+"""CUDA path against the fp64 oracle, element by element, through the C ABI.
+
+Tolerances: O max-abs <= 1.5e-2 and relative L2 <= 5e-3 (bf16 output, fp32
+accumulation, bf16 P); LSE max-abs <= 2e-3.  Full-size workloads compare a
+seeded sample of >= 4096 rows that always holds the first, last and
+tile-edge rows of every sequence and head."""
+import numpy as np
+import pytest
+
+from io_aware_exact_06_gb300 import inputs
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import torch
+    import __graft_entry__
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    __graft_entry__.build()
+    return torch.device("cuda:0")
+
+
+_cache = {}
+
+
+def workload(name):
+    if name not in _cache:
+        _cache[name] = inputs.config_workload(name)
+    return _cache[name]
+
+
+@pytest.mark.parametrize("name", ["tiny", "gpt2_causal"])
+def test_small_configs_every_row(dev, name):
+    wl = workload(name)
+    o, lse, st = parity.run_cuda(wl, dev)
+    assert st == 0
+    parity.compare(o, lse, wl, inputs.all_rows(wl.cu_seqlens, wl.H), name)
+
+
+@pytest.mark.parametrize("name", ["long_causal", "long_full", "stress", "varlen"])
+def test_large_configs_sampled_rows(dev, name):
+    wl = workload(name)
+    o, lse, st = parity.run_cuda(wl, dev)
+    assert st == 0
+    rows = inputs.sample_rows(wl.cu_seqlens, wl.H, 4096, seed=inputs.CONFIG_SEED_BASE + 7)
+    assert len(rows) >= 4096
+    parity.compare(o, lse, wl, rows, name)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ragged_packed_lengths(dev, d, causal):
+    lens = [1, 127, 128, 129, 0, 255, 256, 257, 300, 2, 513]
+    wl = inputs.make_workload("ragged", 4242 + d, lens, 3, d, causal, qk_std=1.5, varlen=True)
+    o, lse, st = parity.run_cuda(wl, dev, packed=True)
+    assert st == 0
+    parity.compare(o, lse, wl, inputs.all_rows(wl.cu_seqlens, wl.H), "ragged")
+
+
+@pytest.mark.parametrize("N", [50, 200, 384, 640])
+@pytest.mark.parametrize("causal", [False, True])
+def test_dense_lengths_not_multiple_of_tile(dev, N, causal):
+    wl = inputs.make_workload("dense", 77 + N, [N] * 3, 2, 128, causal)
+    o, lse, st = parity.run_cuda(wl, dev)
+    assert st == 0
+    parity.compare(o, lse, wl, inputs.all_rows(wl.cu_seqlens, wl.H), f"dense N={N}")
+
+
+def test_zero_q_gives_mean_of_visible_v_at_full_size(dev):
+    """Q = 0: every logit is 0, so O_i is the mean of the visible V rows and
+    LSE_i = log(#visible).  Checked on every row of the long causal workload."""
+    import torch
+    wl = workload("long_causal")
+    wl0 = inputs.Workload("zeroq", np.zeros_like(wl.q), wl.k, wl.v, wl.cu_seqlens, wl.H, wl.d,
+                          wl.scale, True, False, wl.max_seqlen)
+    o, lse, st = parity.run_cuda(wl0, dev)
+    assert st == 0
+    B, N = wl.nseq, int(wl.seqlens()[0])
+    v = parity.to_device(wl, dev)[2].double().reshape(B, N, wl.H, wl.d)
+    prefix = torch.cumsum(v, dim=1) / torch.arange(1, N + 1, device=dev, dtype=torch.float64).view(1, N, 1, 1)
+    got = o.double().reshape(B, N, wl.H, wl.d)
+    err = (got - prefix).abs().max().item()
+    rel = ((got - prefix).norm() / prefix.norm()).item()
+    assert err <= parity.O_MAX_ABS and rel <= parity.O_REL_L2, (err, rel)
+    ref_lse = torch.log(torch.arange(1, N + 1, device=dev, dtype=torch.float64))
+    lse_err = (lse.double().reshape(wl.H, B, N) - ref_lse).abs().max().item()
+    assert lse_err <= parity.LSE_MAX_ABS
+
+
+def test_constant_v_gives_constant_o_varlen(dev):
+    wl = workload("varlen")
+    c = inputs.f64_to_bf16_bits(np.array([0.8125]))[0]
+    wlc = inputs.Workload("constv", wl.q, wl.k, np.full_like(wl.v, c), wl.cu_seqlens, wl.H, wl.d,
+                          wl.scale, True, True, wl.max_seqlen)
+    o, lse, st = parity.run_cuda(wlc, dev)
+    assert st == 0
+    assert (o.float() - 0.8125).abs().max().item() <= 4e-3
+
+
+def test_deterministic(dev):
+    import torch
+    wl = workload("varlen")
+    o1, l1, _ = parity.run_cuda(wl, dev)
+    o2, l2, _ = parity.run_cuda(wl, dev)
+    assert torch.equal(o1, o2)
+    assert torch.equal(l1, l2)
+
+
+def test_non_default_stream(dev):
+    import torch
+    wl = workload("tiny")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o, lse, st = parity.run_cuda(wl, dev, stream=s)
+    assert st == 0
+    parity.compare(o, lse, wl, inputs.all_rows(wl.cu_seqlens, wl.H), "stream")
+
+
+def test_bounded_wait_expires_with_error_status(dev):
+    """A host flag makes CTA 0 skip one copy, so its MMA warp's bounded wait
+    expires: the call reports ATTN_ERR_DEVICE_TIMEOUT and the context stays
+    usable for the next call."""
+    import io_aware_exact_06_gb300 as fa
+    wl = workload("tiny")
+    _, _, st = parity.run_cuda(wl, dev, wait_timeout_ns=50_000_000, fault_inject=1)
+    assert st == -7
+    assert fa.attn_last_error_site() != 0
+    o, lse, st = parity.run_cuda(wl, dev)
+    assert st == 0
+    parity.compare(o, lse, wl, inputs.all_rows(wl.cu_seqlens, wl.H), "after timeout")
+
+
+@pytest.mark.parametrize("bad", ["decreasing", "too_long", "nonzero_start"])
+def test_invalid_cu_seqlens_reported(dev, bad):
+    import torch
+    import io_aware_exact_06_gb300 as fa
+    wl = inputs.make_workload("bad", 5, [100, 100, 100], 2, 64, True, varlen=True)
+    q, k, v, cu = parity.to_device(wl, dev)
+    cu_bad = {"decreasing": [0, 150, 120, 300], "too_long": [0, 100, 300, 300],
+              "nonzero_start": [8, 100, 200, 300]}[bad]
+    cu = torch.tensor(cu_bad, dtype=torch.int32, device=dev)
+    o = torch.full_like(q, 7.0)
+    lse = torch.full((2, 300), 7.0, device=dev)
+    fa.attn_fwd(q, k, v, o, lse, 3, 2, 128, 64, wl.scale, True, cu, None)
+    assert fa.attn_last_device_error() == -8
+    assert (o.float() == 7.0).all() and (lse == 7.0).all(), "nothing is written"
