@@ -40,7 +40,8 @@ typedef enum {
     ATTN_ERR_CUDA = -6,           /* a CUDA runtime call or launch failed */
     ATTN_ERR_DEVICE_TIMEOUT = -7, /* a bounded device-side wait expired */
     ATTN_ERR_SEQLENS = -8,        /* cu_seqlens not increasing from 0, or a length > N */
-    ATTN_ERR_ARCH = -9            /* current device is not sm_103 */
+    ATTN_ERR_ARCH = -9,           /* current device is not sm_103 */
+    ATTN_ERR_SCRATCH = -10        /* attn_fwd_noalloc: problem larger than its fixed scratch */
 } attn_status;
 
 /*
@@ -100,6 +101,40 @@ int attn_last_error_site(void);
 
 /* The cudaError_t behind the last ATTN_ERR_CUDA of this thread (0 if none). */
 int attn_last_cuda_error(void);
+
+/*
+ * attn_fwd_noalloc: attn_fwd for callers that must not allocate device memory.
+ *
+ * The pages have no counterpart to this entry point.  It exists for callers
+ * that cannot call cudaMalloc: code that runs inside another framework whose
+ * memory pool owns all device memory, or a runtime that forbids device
+ * allocation after start-up because an allocation may synchronise the device
+ * or fail at an arbitrary point of a latency-critical loop.  attn_fwd
+ * allocates a small workspace on its first call per device and stream; this
+ * variant allocates nothing: its scratch (the error word and
+ * the scheduling list of packed batches) is a fixed array of 8 + 2 * 65536
+ * int32 (about 512 KB) in the library's own device memory, which every GPU
+ * that loads the library holds until the process exits.
+ *
+ * Same arguments, layouts and results as attn_fwd.  Differences:
+ *   - B * ceil(N / 256) must not exceed 65536 (the number of (sequence,
+ *     256-row block) pairs the scratch holds); larger problems return
+ *     ATTN_ERR_SCRATCH before anything is launched.
+ *   - The first call on a device does the set-up for that device (kernel
+ *     attributes and the device address of the scratch array); make that
+ *     first call before any stream capture.  No call allocates device memory.
+ *   - Every call clears the words that must start at zero (with an
+ *     asynchronous memset on `stream`) and then shares the same scratch:
+ *     calls whose work overlaps on the GPU (different streams, or different
+ *     host threads without ordering) race on it and must be serialised by
+ *     the caller.  The array keeps the last call's contents.
+ *   - Device-side errors of this variant (an expired bounded wait, invalid
+ *     cu_seqlens) are recorded in its scratch, not in the error word read by
+ *     attn_last_device_error; the outputs of such a call are incomplete.
+ */
+int attn_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
+                     int B, int H, int N, int d, float scale, int causal,
+                     const int32_t *cu_seqlens, attn_stream_t stream);
 
 /* A static, human-readable name of a status code. */
 const char *attn_status_string(int status);

@@ -254,6 +254,130 @@ extern "C" const char* attn_status_string(int status) {
     case ATTN_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
     case ATTN_ERR_SEQLENS: return "invalid cu_seqlens";
     case ATTN_ERR_ARCH: return "device is not sm_103";
+    case ATTN_ERR_SCRATCH: return "problem larger than the fixed scratch of attn_fwd_noalloc";
     default: return "unknown status";
   }
+}
+
+// ---------------------------------------------------------------------------
+// attn_fwd_noalloc: the same forward pass without any device allocation, for
+// callers that cannot call cudaMalloc.  Its scratch is the file-scope array
+// below: error bits, error site, entry count, then the (sequence, q-block)
+// pairs of a packed batch.  Every call shares it.
+namespace {
+
+constexpr int kNoAllocMaxEntries = 1 << 16;
+constexpr int kNoAllocHeader = 8;  // [0] error bits, [1] error site, [2] entry count
+constexpr int kNoAllocScratchInts = kNoAllocHeader + 2 * kNoAllocMaxEntries;
+
+static __device__ __align__(256) int g_noalloc_scratch[kNoAllocScratchInts];
+
+struct NoAllocDevice {
+  bool ready = false;
+  int sms = 0;
+  int* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+};
+
+std::map<int, NoAllocDevice> g_noalloc_dev;
+
+// Once per device, with that device current: kernel attributes and the device
+// address of the scratch array (the host-side name is only a stand-in).
+int noalloc_setup(int dev, NoAllocDevice** out) {
+  NoAllocDevice& st = g_noalloc_dev[dev];
+  if (!st.ready) {
+    int major = 0, minor = 0;
+    cudaError_t e;
+    if ((e = cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return cuda_fail(e);
+    if (major != 10 || minor != 3) return ATTN_ERR_ARCH;
+    if ((e = cudaFuncSetAttribute(attn::attn_fwd_kernel<64>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  FwdCfg<64>::kSmemBytes)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((e = cudaFuncSetAttribute(attn::attn_fwd_kernel<128>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  FwdCfg<128>::kSmemBytes)) != cudaSuccess)
+      return cuda_fail(e);
+    void* ptr = nullptr;
+    if ((e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch)) != cudaSuccess) return cuda_fail(e);
+    st.scratch = static_cast<int*>(ptr);
+    st.ready = true;
+  }
+  *out = &st;
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                                int B, int H, int N, int d, float scale, int causal,
+                                const int32_t* cu_seqlens, attn_stream_t stream) {
+  if (B < 0 || H < 0 || N < 0) return ATTN_ERR_SHAPE;
+  if (d != 64 && d != 128) return ATTN_ERR_HEADDIM;
+  if (!std::isfinite(scale)) return ATTN_ERR_SCALE;
+  if (B == 0 || H == 0 || N == 0) return ATTN_OK;
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return ATTN_ERR_ALIGN;
+  const int64_t tokens_bound = (int64_t)B * N;
+  if (tokens_bound > INT32_MAX - 2 * attn::kBN || (int64_t)H * d > (1 << 20) || H > 65535)
+    return ATTN_ERR_SHAPE;
+  const int64_t nqb = (N + attn::kUnitRows - 1) / attn::kUnitRows;
+  const int64_t entries = (int64_t)B * nqb;
+  if (entries > kNoAllocMaxEntries) return ATTN_ERR_SCRATCH;
+  const int64_t units = entries * H;
+  if (units > INT32_MAX) return ATTN_ERR_SHAPE;
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  NoAllocDevice* nd = nullptr;
+  int st = noalloc_setup(dev, &nd);
+  if (st != ATTN_OK) return st;
+  EncodeTiledFn enc = nullptr;
+  if ((st = get_encode(&enc)) != ATTN_OK) return st;
+  CUtensorMap mq, mk, mv;
+  if ((st = make_map(enc, &mq, q, tokens_bound, H, d)) != ATTN_OK) return st;
+  if ((st = make_map(enc, &mk, k, tokens_bound, H, d)) != ATTN_OK) return st;
+  if ((st = make_map(enc, &mv, v, tokens_bound, H, d)) != ATTN_OK) return st;
+
+  int* scratch = nd->scratch;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // the error word and the entry count must start at zero on every call
+  if ((e = cudaMemsetAsync(scratch, 0, kNoAllocHeader * sizeof(int), s)) != cudaSuccess)
+    return cuda_fail(e);
+
+  FwdParams p{};
+  p.o = reinterpret_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.cu_seqlens = cu_seqlens;
+  p.err = scratch;
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.causal = causal ? 1 : 0;
+  p.scale = scale;
+  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p.timeout_ns = 2000000000ull;
+  p.fault_inject = 0;
+
+  int grid = nd->sms;
+  if (cu_seqlens) {
+    p.num_entries = scratch + 2;
+    p.work = scratch + kNoAllocHeader;
+    const int ncost = (int)std::min<int64_t>((N + attn::kBN - 1) / attn::kBN,
+                                             attn::kMaxCostBuckets - 1);
+    attn::build_worklist_kernel<<<1, 1024, (ncost + 1) * sizeof(int), s>>>(
+        cu_seqlens, B, N, p.causal, scratch + kNoAllocHeader, scratch + 2, scratch,
+        (int)entries);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+  } else if (units < grid) {
+    grid = (int)units;
+  }
+  return d == 64 ? launch_attn<64>(mq, mk, mv, p, grid, s) : launch_attn<128>(mq, mk, mv, p, grid, s);
 }
