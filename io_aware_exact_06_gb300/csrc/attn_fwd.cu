@@ -36,7 +36,8 @@ struct DeviceState {
 };
 
 struct StreamWorkspace {
-  int* buf = nullptr;       // [0] entry count, [1..3] unused, [4..] (seq, q-block) pairs
+  int* buf = nullptr;       // [0] entry count, [1] next-unit counter, [2] finished CTAs,
+                            // [3] unused, [4..] (seq, q-block) pairs
   int64_t capacity = 0;     // entries
 };
 
@@ -106,6 +107,7 @@ int stream_workspace(int dev, attn_stream_t stream, int64_t entries, int** out) 
     const int64_t cap = entries < 1024 ? 1024 : entries;
     if ((e = cudaMalloc(&ws.buf, (size_t)(4 + 2 * cap) * sizeof(int))) != cudaSuccess)
       return cuda_fail(e);
+    if ((e = cudaMemset(ws.buf, 0, 4 * sizeof(int))) != cudaSuccess) return cuda_fail(e);
     ws.capacity = cap;
   }
   *out = ws.buf;
@@ -192,16 +194,17 @@ extern "C" int attn_fwd_ex(const void* q, const void* k, const void* v, void* o,
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int grid = ds->sms;
+  int* ws = nullptr;
+  const int64_t max_entries = cu_seqlens ? (int64_t)B * nqb : 0;
+  if ((st = stream_workspace(dev, stream, max_entries, &ws)) != ATTN_OK) return st;
+  p.sched = ws + 1;
   if (cu_seqlens) {
-    int* ws = nullptr;
-    const int64_t max_entries = (int64_t)B * nqb;
-    if ((st = stream_workspace(dev, stream, max_entries, &ws)) != ATTN_OK) return st;
     p.num_entries = ws;
     p.work = ws + 4;
     const int ncost = (int)std::min<int64_t>((N + attn::kBN - 1) / attn::kBN,
                                              attn::kMaxCostBuckets - 1);
     attn::build_worklist_kernel<<<1, 1024, (ncost + 1) * sizeof(int), s>>>(
-        cu_seqlens, B, N, p.causal, ws + 4, ws, ds->err, (int)max_entries);
+        cu_seqlens, B, N, p.causal, ws + 4, ws, ds->err, (int)max_entries, ws + 1);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
   } else if (units < grid) {
     grid = (int)units;
@@ -267,7 +270,8 @@ extern "C" const char* attn_status_string(int status) {
 namespace {
 
 constexpr int kNoAllocMaxEntries = 1 << 16;
-constexpr int kNoAllocHeader = 8;  // [0] error bits, [1] error site, [2] entry count
+constexpr int kNoAllocHeader = 8;  // [0] error bits, [1] error site, [2] entry count,
+                                   // [3] next-unit counter, [4] finished CTAs
 constexpr int kNoAllocScratchInts = kNoAllocHeader + 2 * kNoAllocMaxEntries;
 
 static __device__ __align__(256) int g_noalloc_scratch[kNoAllocScratchInts];
@@ -357,6 +361,7 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
   p.lse = lse;
   p.cu_seqlens = cu_seqlens;
   p.err = scratch;
+  p.sched = scratch + 3;
   p.B = B;
   p.H = H;
   p.N = N;
@@ -374,7 +379,7 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
                                              attn::kMaxCostBuckets - 1);
     attn::build_worklist_kernel<<<1, 1024, (ncost + 1) * sizeof(int), s>>>(
         cu_seqlens, B, N, p.causal, scratch + kNoAllocHeader, scratch + 2, scratch,
-        (int)entries);
+        (int)entries, scratch + 3);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
   } else if (units < grid) {
     grid = (int)units;

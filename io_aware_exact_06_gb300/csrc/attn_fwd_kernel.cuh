@@ -16,6 +16,11 @@
 //     conditional rescaling of O, longest-processing-time-first scheduling:
 //     same page, FlashAttention-4 items.
 //
+// Scheduling: a persistent CTA takes units in longest-first order: its first
+// unit is blockIdx.x, every further one comes from an atomic counter (the
+// producer pops it and publishes it to the MMA and softmax warps through a
+// two-slot ring in shared memory), so CTAs that drew short units take more.
+//
 // CTA layout (384 threads = 3 warpgroups, one CTA per SM, persistent):
 //   warps 0-3   softmax group 0: query tile 0 of the unit, one thread per row
 //   warps 4-7   softmax group 1: query tile 1 of the unit
@@ -72,6 +77,8 @@ struct FwdParams {
   const int* work;         // varlen: LPT-ordered (seq, q-block) pairs
   const int* num_entries;  // varlen: number of pairs in `work`
   int* err;                // err[0]: error bits; err[1]: where a wait gave up
+  int* sched;              // [0] next-unit counter, [1] finished CTAs; zero at launch,
+                           // reset to zero by the last CTA to finish
   int B, H, N;
   int causal;
   float scale;             // softmax scale on the logits
@@ -105,9 +112,13 @@ enum : int {
   kBarPFull = 4,   // +g
   kBarOFull = 6,   // +g
   kBarDrain = 8,
-  kBarKV = 9,      // kv_full[s] = kBarKV + s, kv_empty[s] = kBarKV + kStages + s
+  kBarUnitFull = 9,    // +slot
+  kBarUnitEmpty = 11,  // +slot
+  kBarKV = 13,     // kv_full[s] = kBarKV + s, kv_empty[s] = kBarKV + kStages + s
 };
 constexpr int kMaxBars = kBarKV + 2 * 8;
+constexpr int kUnitSlots = 2;            // unit indices published by the producer
+constexpr int kUnitConsumers = 1 + 8;    // the MMA thread and the 8 softmax warps
 
 // One work unit: rows [256 qb, 256 qb + 256) of head h of one sequence.
 struct Unit {
@@ -164,6 +175,7 @@ struct SharedState {
   uint64_t bars[kMaxBars];
   uint32_t tmem_base;
   volatile int abort_flag;
+  volatile int unit_ring[kUnitSlots];
 };
 
 // Bounded wait on an mbarrier phase; gives up on timeout or when another warp
@@ -201,7 +213,21 @@ __device__ __forceinline__ void producer_loop(const CUtensorMap* tm_q, const CUt
   uint32_t ring = 0;
   int units_done = 0;
   bool injected = false;
-  for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+  uint32_t uslot = 0;
+  int u = blockIdx.x;  // first unit static, then longest-first order by atomic pop
+  for (;;) {
+    if (u >= n_units) u = -1;
+    {
+      const int slot = uslot % kUnitSlots;
+      const uint32_t n = uslot / kUnitSlots;
+      if (n > 0 && !wait_bar(ss, kBarUnitEmpty + slot, (n - 1) & 1, p, 3)) return;
+      ss.unit_ring[slot] = u;
+      mbar_arrive(bar_addr(ss, kBarUnitFull + slot));
+      ++uslot;
+    }
+    if (u < 0) return;
+    // next unit index, fetched while this unit's copies are issued
+    const int next_u = (int)gridDim.x + atomicAdd(p.sched, 1);
     const Unit un = decode_unit(p, u);
     if (units_done > 0 && !wait_bar(ss, kBarQEmpty, (units_done - 1) & 1, p, 1)) return;
     mbar_arrive_expect_tx(bar_addr(ss, kBarQFull), kQTiles * C::kTileBytes);
@@ -231,7 +257,28 @@ __device__ __forceinline__ void producer_loop(const CUtensorMap* tm_q, const CUt
       }
     }
     ++units_done;
+    u = next_u;
   }
+}
+
+// Unit index published by the producer for the consumer's next unit
+// (-1: no more work).  `lane0_arrives`: the arrive on the slot's empty
+// barrier comes from lane 0 of a warp after every lane has read it.
+__device__ __forceinline__ bool next_unit(SharedState& ss, const FwdParams& p, uint32_t& uslot,
+                                          bool whole_warp, int& u) {
+  const int slot = uslot % kUnitSlots;
+  bool ok = wait_bar(ss, kBarUnitFull + slot, (uslot / kUnitSlots) & 1, p, 30);
+  if (whole_warp) ok = __all_sync(0xffffffffu, ok);
+  if (!ok) return false;
+  u = ss.unit_ring[slot];
+  if (whole_warp) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar_addr(ss, kBarUnitEmpty + slot));
+  } else {
+    mbar_arrive(bar_addr(ss, kBarUnitEmpty + slot));
+  }
+  ++uslot;
+  return true;
 }
 
 // ----------------------------------------------------------------- MMA --
@@ -281,7 +328,10 @@ __device__ __forceinline__ void mma_loop(const FwdParams& p, SharedState& ss, ui
   };
   auto release = [&](uint32_t pos) { mma_commit(bar_addr(ss, kBarKV + C::kStages + pos % C::kStages)); };
 
-  for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+  uint32_t uslot = 0;
+  for (;;) {
+    int u;
+    if (!next_unit(ss, p, uslot, false, u) || u < 0) return;
     const Unit un = decode_unit(p, u);
     if (!wait_bar(ss, kBarQFull, units_done & 1, p, 11)) return;
     tc_fence_after();
@@ -345,9 +395,35 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// The two bf16 halves of a packed pair, widened exactly to fp32.
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// (d0, d1) = (a0, a1) * b + c, one packed fp32x2 instruction.
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b, float c) {
+  asm("{\n .reg .b64 x, y, z, r;\n mov.b64 x, {%2, %3};\n mov.b64 y, {%4, %4};\n"
+      " mov.b64 z, {%5, %5};\n fma.rn.f32x2 r, x, y, z;\n mov.b64 {%0, %1}, r;\n}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+
+// (a0, a1) += (b0, b1), one packed fp32x2 instruction.
+__device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
+  asm("{\n .reg .b64 x, y, r;\n mov.b64 x, {%0, %1};\n mov.b64 y, {%2, %3};\n"
+      " add.rn.f32x2 r, x, y;\n mov.b64 {%0, %1}, r;\n}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b0), "f"(b1));
+}
+
+// acc_lo += bf16 low half of w, acc_hi += bf16 high half (exact widening).
+__device__ __forceinline__ void add_bf16x2_to_f32(float& acc_lo, float& acc_hi, uint32_t w) {
+  asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n add.rn.f32.bf16 %0, lo, %0;\n"
+      " add.rn.f32.bf16 %1, hi, %1;\n}"
+      : "+f"(acc_lo), "+f"(acc_hi)
+      : "r"(w));
+}
 
 template <int D>
 __device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss, uint32_t tmem,
@@ -364,7 +440,10 @@ __device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss
   int tokens_total = 0;
   if (p.cu_seqlens) tokens_total = p.cu_seqlens[p.B];
 
-  for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+  uint32_t uslot = 0;
+  for (;;) {
+    int u;
+    if (!next_unit(ss, p, uslot, true, u) || u < 0) return;
     const Unit un = decode_unit(p, u);
     const int a0 = q_tile_start(un, g);
     const int row = a0 + trow;                       // sequence-relative row of this thread
@@ -408,9 +487,17 @@ __device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss
         for (int c = 0; c < kBN; ++c)
           if (c < lo || c > hi) s[c] = -INFINITY;
       }
-      float mx = s[0];
+      // row max: four independent 3-input max chains
+      float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]);
+      float mx2 = fmaxf(s[4], s[5]), mx3 = fmaxf(s[6], s[7]);
 #pragma unroll
-      for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+      for (int c = 8; c < kBN; c += 8) {
+        mx0 = max3(mx0, s[c], s[c + 1]);
+        mx1 = max3(mx1, s[c + 2], s[c + 3]);
+        mx2 = max3(mx2, s[c + 4], s[c + 5]);
+        mx3 = max3(mx3, s[c + 6], s[c + 7]);
+      }
+      const float mx = fmaxf(max3(mx0, mx1, mx2), mx3);
       const float m_new = fmaxf(m_used, mx);
       if (j == 0) {
         m_used = m_new;
@@ -434,27 +521,33 @@ __device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss
         }
       }
       const float neg = m_used == -INFINITY ? 0.f : -m_used * c2;
-      float sum = 0.f, sum_r = 0.f;
+      // p = 2^(c2 * s - c2 * m): packed fp32x2 FMA, MUFU ex2, packed sums;
+      // sum of the bf16-rounded values with mixed-precision adds.
+      float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;  // fp32 sum (two pairs)
+      float ra0 = 0.f, ra1 = 0.f;                        // rounded sum
       uint32_t pa[32], pb[32];
 #pragma unroll
-      for (int c = 0; c < kBN / 2; c += 2) {
-        const float p0 = ex2_approx(fmaf(s[c], c2, neg));
-        const float p1 = ex2_approx(fmaf(s[c + 1], c2, neg));
-        sum += p0 + p1;
-        pa[c / 2] = pack_bf16x2(p0, p1);
-        sum_r += bf16_lo(pa[c / 2]) + bf16_hi(pa[c / 2]);
+      for (int c = 0; c < kBN; c += 4) {
+        float x0, x1, x2, x3;
+        fma2(x0, x1, s[c], s[c + 1], c2, neg);
+        fma2(x2, x3, s[c + 2], s[c + 3], c2, neg);
+        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+        const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+        add2(sa0, sa1, p0, p1);
+        add2(sb0, sb1, p2, p3);
+        const uint32_t w0 = pack_bf16x2(p0, p1), w1 = pack_bf16x2(p2, p3);
+        add_bf16x2_to_f32(ra0, ra1, w0);
+        add_bf16x2_to_f32(ra0, ra1, w1);
+        if (c < kBN / 2) {
+          pa[c / 2] = w0;
+          pa[c / 2 + 1] = w1;
+        } else {
+          pb[(c - kBN / 2) / 2] = w0;
+          pb[(c - kBN / 2) / 2 + 1] = w1;
+        }
       }
-#pragma unroll
-      for (int c = kBN / 2; c < kBN; c += 2) {
-        const float p0 = ex2_approx(fmaf(s[c], c2, neg));
-        const float p1 = ex2_approx(fmaf(s[c + 1], c2, neg));
-        sum += p0 + p1;
-        const int i = (c - kBN / 2) / 2;
-        pb[i] = pack_bf16x2(p0, p1);
-        sum_r += bf16_lo(pb[i]) + bf16_hi(pb[i]);
-      }
-      l += sum;
-      l_r += sum_r;
+      l += (sa0 + sa1) + (sb0 + sb1);
+      l_r += ra0 + ra1;
       tmem_st_x32(lane_addr + colS, pa);
       tmem_st_x32(lane_addr + colS + 32, pb);
       tmem_st_wait();
@@ -535,6 +628,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       mbar_init(bar_addr(ss, kBarOFull + g), 1);
     }
     mbar_init(bar_addr(ss, kBarDrain), 1);
+    for (int i = 0; i < kUnitSlots; ++i) {
+      mbar_init(bar_addr(ss, kBarUnitFull + i), 1);
+      mbar_init(bar_addr(ss, kBarUnitEmpty + i), kUnitConsumers);
+    }
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(bar_addr(ss, kBarKV + s), 1);
       mbar_init(bar_addr(ss, kBarKV + C::kStages + s), 1);
@@ -588,17 +685,28 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+  if (threadIdx.x == 0) {
+    // every CTA has taken its last unit once all have arrived here: the last
+    // one leaves the counters at zero for the next launch on this workspace
+    __threadfence();
+    if (atomicAdd(p.sched + 1, 1) == (int)gridDim.x - 1) {
+      atomicExch(p.sched, 0);
+      atomicExch(p.sched + 1, 0);
+      __threadfence();
+    }
+  }
 }
 
 // ----------------------------------------------------------- scheduler --
 // Builds the longest-first list of (sequence, q-block) pairs of a packed
-// variable-length batch and validates cu_seqlens.  One CTA.  Cost of a pair =
+// variable-length batch, validates cu_seqlens and zeroes the unit counters of
+// the attention kernel that follows.  One CTA.  Cost of a pair =
 // KV tiles it visits; a counting sort over cost in descending order.
 constexpr int kMaxCostBuckets = 8192;
 
 __global__ void __launch_bounds__(1024)
 build_worklist_kernel(const int* cu_seqlens, int nseq, int max_len, int causal, int* work,
-                      int* num_entries, int* err, int max_entries) {
+                      int* num_entries, int* err, int max_entries, int* sched) {
   extern __shared__ int hist[];  // [ncost + 1]
   __shared__ int bad;
   __shared__ int total;
@@ -607,6 +715,8 @@ build_worklist_kernel(const int* cu_seqlens, int nseq, int max_len, int causal, 
   if (threadIdx.x == 0) {
     bad = cu_seqlens[0] != 0;
     total = 0;
+    sched[0] = 0;
+    sched[1] = 0;
   }
   __syncthreads();
   for (int s = threadIdx.x; s < nseq; s += blockDim.x) {
