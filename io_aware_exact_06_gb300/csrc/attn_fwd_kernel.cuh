@@ -21,14 +21,17 @@
 // producer pops it and publishes it to the MMA and softmax warps through a
 // two-slot ring in shared memory), so CTAs that drew short units take more.
 //
-// CTA layout (384 threads = 3 warpgroups, one CTA per SM, persistent):
-//   warps 0-3   softmax group 0: query tile 0 of the unit, one thread per row
-//   warps 4-7   softmax group 1: query tile 1 of the unit
-//   warp  8     TMA producer (lane 0): Q tiles, then K_j, V_j into a ring
-//   warp  9     MMA issuer (lane 0) and TMEM owner
-//   warps 10-11 idle
-// Registers are moved from the third warpgroup to the softmax warpgroups with
-// setmaxnreg (launch: 384 x 168; after: 256 x 216 + 128 x 72 <= 384 x 168).
+// CTA layout (640 threads = 5 warpgroups, one CTA per SM, persistent):
+//   warps 0-7   softmax group 0 (query tile 0 of the unit), warps 8-15 group 1:
+//               warp w reads TMEM lanes 32*(w%4).. (its 32 rows) and handles
+//               key columns [64*h, 64*h+64) with h = (w%8)/4, so two warps
+//               share each row; they combine row maxima and sums through
+//               shared memory under a named barrier
+//   warp  16    TMA producer (lane 0): Q tiles, then K_j, V_j into a ring
+//   warp  17    MMA issuer (lane 0) and TMEM owner
+//   warps 18-19 idle
+// Registers are moved from the control warpgroup to the softmax warpgroups
+// with setmaxnreg (launch: 640 x 96; after: 512 x 104 + 128 x 64).
 // A work unit is (sequence, head, 256 query rows) = two 128-row query tiles.
 // Per KV tile j the tensor core runs, in order,
 //   O0 += P0 V_{j-1};  S0 = Q0 K_j^T;  O1 += P1 V_{j-1};  S1 = Q1 K_j^T
@@ -54,14 +57,19 @@ constexpr int kBM = 128;               // query rows per tile (= TMEM lanes)
 constexpr int kBN = 128;               // keys per KV tile
 constexpr int kQTiles = 2;             // query tiles per work unit
 constexpr int kUnitRows = kBM * kQTiles;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 384;
-constexpr int kLaunchRegs = 168;        // 65536 / 384, rounded down to 8
-constexpr int kSoftmaxRegs = 216;
-constexpr int kControlRegs = 72;
-static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * kLaunchRegs,
+constexpr int kGroupWarps = 8;           // softmax warps per query tile
+constexpr int kGroupThreads = 32 * kGroupWarps;
+constexpr int kSoftmaxWarps = kQTiles * kGroupWarps;
+constexpr int kProducerWarp = kSoftmaxWarps;
+constexpr int kMmaWarp = kSoftmaxWarps + 1;
+constexpr int kThreads = 32 * (kSoftmaxWarps + 4);
+constexpr int kLaunchRegs = 96;          // 65536 / 640, rounded down to 8
+constexpr int kSoftmaxRegs = 104;
+constexpr int kControlRegs = 64;
+static_assert(kThreads == 640, "five warpgroups");
+static_assert(kSoftmaxWarps * 32 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * kLaunchRegs,
               "register split exceeds the launch allotment");
+constexpr int kHalfCols = kBN / 2;       // key columns per softmax thread
 constexpr int kChunkBytes = kBM * 128; // 128 rows x 64 bf16 (one 128-byte swizzle span)
 constexpr float kRescaleLog2 = 8.0f;   // rescale O only if the row max grew by > 2^8
 
@@ -118,7 +126,7 @@ enum : int {
 };
 constexpr int kMaxBars = kBarKV + 2 * 8;
 constexpr int kUnitSlots = 2;            // unit indices published by the producer
-constexpr int kUnitConsumers = 1 + 8;    // the MMA thread and the 8 softmax warps
+constexpr int kUnitConsumers = 1 + kSoftmaxWarps;  // the MMA thread and every softmax warp
 
 // One work unit: rows [256 qb, 256 qb + 256) of head h of one sequence.
 struct Unit {
@@ -176,6 +184,8 @@ struct SharedState {
   uint32_t tmem_base;
   volatile int abort_flag;
   volatile int unit_ring[kUnitSlots];
+  float row_max[2][kQTiles][2][kBM];   // [tile parity][group][column half][row]
+  float row_sum[kQTiles][2][2][kBM];   // [group][column half][l, l_r][row]
 };
 
 // Bounded wait on an mbarrier phase; gives up on timeout or when another warp
@@ -425,15 +435,25 @@ __device__ __forceinline__ void add_bf16x2_to_f32(float& acc_lo, float& acc_hi, 
       : "r"(w));
 }
 
+// Named barrier of the two warps that share a 32-row quadrant of a group.
+__device__ __forceinline__ void pair_sync(int g, int quadrant) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + g * 4 + quadrant), "r"(64) : "memory");
+}
+
 template <int D>
 __device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss, uint32_t tmem,
                                              int g, int n_units) {
   using C = FwdCfg<D>;
+  constexpr int kOCols = D / 2;             // O columns rescaled / stored by this thread
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const int trow = (warp % 4) * 32 + lane;  // row within the tile = TMEM lane
-  const uint32_t lane_addr = tmem + ((uint32_t)((warp % 4) * 32) << 16);
-  const uint32_t colS = C::col_s(g), colO = C::col_o(g);
+  const int quadrant = warp % 4;
+  const int half = (warp % kGroupWarps) / 4;   // which 64 key columns
+  const int trow = quadrant * 32 + lane;       // row within the tile = TMEM lane
+  const uint32_t lane_addr = tmem + ((uint32_t)(quadrant * 32) << 16);
+  const uint32_t colS = C::col_s(g) + half * kHalfCols;     // this thread's S columns
+  const uint32_t colP = C::col_s(g) + half * (kHalfCols / 2);  // its packed P columns
+  const uint32_t colO = C::col_o(g) + half * kOCols;
   const float c2 = p.scale_log2;
   uint32_t scount = 0;
   int units_done = 0;
@@ -449,85 +469,76 @@ __device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss
     const int row = a0 + trow;                       // sequence-relative row of this thread
     const int nominal0 = un.qb * kUnitRows + g * kBM;
     float m_used = -INFINITY;
-    float l = 0.f;    // sum of the fp32 probabilities: the LSE
-    float l_r = 0.f;  // sum of the bf16-rounded probabilities the PV product used: O's divisor
+    float l = 0.f;    // sum of the fp32 probabilities (this half): the LSE
+    float l_r = 0.f;  // sum of the bf16-rounded probabilities (this half): O's divisor
     for (int j = 0; j < un.nkv; ++j) {
       if (!__all_sync(0xffffffffu, wait_bar(ss, kBarSFull + g, scount & 1, p, 20 + g))) return;
       ++scount;
       tc_fence_after();
-      float s[kBN];
+      float s[kHalfCols];
       {
-        uint32_t r0[32], r1[32], r2[32], r3[32];
-        tmem_ld_x32(lane_addr + colS + 0, r0);
+        uint32_t r0[32], r1[32];
+        tmem_ld_x32(lane_addr + colS, r0);
         tmem_ld_x32(lane_addr + colS + 32, r1);
-        tmem_ld_x32(lane_addr + colS + 64, r2);
-        tmem_ld_x32(lane_addr + colS + 96, r3);
         tmem_ld_wait_x32(r0);
         tmem_ld_wait_x32(r1);
-        tmem_ld_wait_x32(r2);
-        tmem_ld_wait_x32(r3);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           s[i] = __uint_as_float(r0[i]);
           s[32 + i] = __uint_as_float(r1[i]);
-          s[64 + i] = __uint_as_float(r2[i]);
-          s[96 + i] = __uint_as_float(r3[i]);
         }
       }
       // Mask: keys already visited by the previous tile (pulled-back last
       // tile) and, when causal, keys after this row.  The pull-back keeps
       // every loaded key inside the sequence.  Decided per group, applied
-      // per row.
+      // per row; column c of this thread is key column half*64 + c.
       const int b0 = kv_tile_start(un, j);
-      const int lo = j * kBN - b0;
-      const bool need_mask = lo > 0 || (p.causal && b0 + kBN - 1 > a0);
+      const int lo = j * kBN - b0 - half * kHalfCols;
+      const bool need_mask = j * kBN > b0 || (p.causal && b0 + kBN - 1 > a0);
       if (need_mask) {
-        const int hi = p.causal ? min(row - b0, kBN - 1) : kBN - 1;
+        const int hi = (p.causal ? min(row - b0, kBN - 1) : kBN - 1) - half * kHalfCols;
 #pragma unroll
-        for (int c = 0; c < kBN; ++c)
+        for (int c = 0; c < kHalfCols; ++c)
           if (c < lo || c > hi) s[c] = -INFINITY;
       }
-      // row max: four independent 3-input max chains
+      // row max: partial over this half (four 3-input max chains), then the
+      // partner's half through shared memory
       float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]);
       float mx2 = fmaxf(s[4], s[5]), mx3 = fmaxf(s[6], s[7]);
 #pragma unroll
-      for (int c = 8; c < kBN; c += 8) {
+      for (int c = 8; c < kHalfCols; c += 8) {
         mx0 = max3(mx0, s[c], s[c + 1]);
         mx1 = max3(mx1, s[c + 2], s[c + 3]);
         mx2 = max3(mx2, s[c + 4], s[c + 5]);
         mx3 = max3(mx3, s[c + 6], s[c + 7]);
       }
-      const float mx = fmaxf(max3(mx0, mx1, mx2), mx3);
+      const float mine = fmaxf(max3(mx0, mx1, mx2), mx3);
+      ss.row_max[j & 1][g][half][trow] = mine;
+      pair_sync(g, quadrant);  // also orders both halves' S loads before any P store
+      const float mx = fmaxf(mine, ss.row_max[j & 1][g][half ^ 1][trow]);
       const float m_new = fmaxf(m_used, mx);
+      // O correction decision: only when the row max grew by more than 2^8
+      // (warp-uniform; the partner warp holds the same rows and decides alike)
+      float alpha = 1.0f;
+      bool rescale_warp = false;
       if (j == 0) {
         m_used = m_new;
       } else {
         const bool resc = (m_new - m_used) * c2 > kRescaleLog2;
-        if (__any_sync(0xffffffffu, resc)) {
-          const float alpha = resc ? ex2_approx((m_used - m_new) * c2) : 1.0f;
-#pragma unroll
-          for (int cc = 0; cc < D; cc += 32) {
-            uint32_t r[32];
-            tmem_ld_x32(lane_addr + colO + cc, r);
-            tmem_ld_wait_x32(r);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            tmem_st_x32(lane_addr + colO + cc, r);
-          }
-          tmem_st_wait();
-          l *= alpha;
-          l_r *= alpha;
-          if (resc) m_used = m_new;
+        rescale_warp = __any_sync(0xffffffffu, resc);
+        if (resc) {
+          alpha = ex2_approx((m_used - m_new) * c2);
+          m_used = m_new;
         }
       }
       const float neg = m_used == -INFINITY ? 0.f : -m_used * c2;
       // p = 2^(c2 * s - c2 * m): packed fp32x2 FMA, MUFU ex2, packed sums;
       // sum of the bf16-rounded values with mixed-precision adds.
-      float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;  // fp32 sum (two pairs)
-      float ra0 = 0.f, ra1 = 0.f;                        // rounded sum
-      uint32_t pa[32], pb[32];
+      float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
+      float ra0 = 0.f, ra1 = 0.f;
+      uint32_t pw[32];
 #pragma unroll
-      for (int c = 0; c < kBN; c += 4) {
+      for (int c = 0; c < kHalfCols; c += 4) {
         float x0, x1, x2, x3;
         fma2(x0, x1, s[c], s[c + 1], c2, neg);
         fma2(x2, x3, s[c + 2], s[c + 3], c2, neg);
@@ -535,36 +546,50 @@ __device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss
         const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
         add2(sa0, sa1, p0, p1);
         add2(sb0, sb1, p2, p3);
-        const uint32_t w0 = pack_bf16x2(p0, p1), w1 = pack_bf16x2(p2, p3);
-        add_bf16x2_to_f32(ra0, ra1, w0);
-        add_bf16x2_to_f32(ra0, ra1, w1);
-        if (c < kBN / 2) {
-          pa[c / 2] = w0;
-          pa[c / 2 + 1] = w1;
-        } else {
-          pb[(c - kBN / 2) / 2] = w0;
-          pb[(c - kBN / 2) / 2 + 1] = w1;
+        pw[c / 2] = pack_bf16x2(p0, p1);
+        pw[c / 2 + 1] = pack_bf16x2(p2, p3);
+        add_bf16x2_to_f32(ra0, ra1, pw[c / 2]);
+        add_bf16x2_to_f32(ra0, ra1, pw[c / 2 + 1]);
+      }
+      l = l * alpha + ((sa0 + sa1) + (sb0 + sb1));
+      l_r = l_r * alpha + (ra0 + ra1);
+      // O *= alpha before this tile's PV product (after the exps, when the
+      // scores no longer occupy registers)
+      if (rescale_warp) {
+#pragma unroll
+        for (int cc = 0; cc < kOCols; cc += 32) {
+          uint32_t r[32];
+          tmem_ld_x32(lane_addr + colO + cc, r);
+          tmem_ld_wait_x32(r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          tmem_st_x32(lane_addr + colO + cc, r);
         }
       }
-      l += (sa0 + sa1) + (sb0 + sb1);
-      l_r += ra0 + ra1;
-      tmem_st_x32(lane_addr + colS, pa);
-      tmem_st_x32(lane_addr + colS + 32, pb);
+      tmem_st_x32(lane_addr + colP, pw);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar_addr(ss, kBarPFull + g));
     }
-    // Epilogue: O / l_r -> bf16, LSE = scale * m + ln(l).  Rows before the
+    // Epilogue: the two halves' sums are combined; O / l_r -> bf16 (each
+    // thread its D/2 columns), LSE = scale * m + ln(l).  Rows before the
     // nominal tile start (recomputed) and rows past the sequence are skipped.
+    ss.row_sum[g][half][0][trow] = l;
+    ss.row_sum[g][half][1][trow] = l_r;
+    pair_sync(g, quadrant);
+    l += ss.row_sum[g][half ^ 1][0][trow];
+    l_r += ss.row_sum[g][half ^ 1][1][trow];
+    pair_sync(g, quadrant);  // both read before the next unit writes again
     if (!__all_sync(0xffffffffu, wait_bar(ss, kBarOFull + g, units_done & 1, p, 22 + g))) return;
     tc_fence_after();
     const bool store = row >= nominal0 && row < un.L && row >= 0;
     // Dividing by the sum of the weights actually multiplied into V keeps a
     // dominant term exact (its bf16 rounding cancels); the LSE uses the fp32 sum.
     const float inv_l = l_r > 0.f ? 1.0f / l_r : 0.f;
-    __nv_bfloat16* orow = p.o + ((size_t)(store ? un.tok0 + row : 0) * p.H + un.h) * D;
+    __nv_bfloat16* orow =
+        p.o + ((size_t)(store ? un.tok0 + row : 0) * p.H + un.h) * D + half * kOCols;
 #pragma unroll
-    for (int cc = 0; cc < D; cc += 32) {
+    for (int cc = 0; cc < kOCols; cc += 32) {
       uint32_t r[32];
       tmem_ld_x32(lane_addr + colO + cc, r);
       tmem_ld_wait_x32(r);
@@ -581,7 +606,7 @@ __device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss
         }
       }
     }
-    if (store) {
+    if (store && half == 0) {
       const float lse = l > 0.f ? m_used * p.scale + __log2f(l) * 0.69314718055994531f : -INFINITY;
       size_t idx;
       if (p.cu_seqlens)
@@ -624,7 +649,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     mbar_init(bar_addr(ss, kBarQEmpty), 1);
     for (int g = 0; g < kQTiles; ++g) {
       mbar_init(bar_addr(ss, kBarSFull + g), 1);
-      mbar_init(bar_addr(ss, kBarPFull + g), kBM);
+      mbar_init(bar_addr(ss, kBarPFull + g), kGroupThreads);
       mbar_init(bar_addr(ss, kBarOFull + g), 1);
     }
     mbar_init(bar_addr(ss, kBarDrain), 1);
@@ -654,7 +679,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const uint32_t tmem = ss.tmem_base;
   const int n_units = num_units(p);
 
-  if (warp >= 8) {
+  if (warp >= kSoftmaxWarps) {
     setmaxnreg_dec<kControlRegs>();
     if (warp == kProducerWarp) {
       if (lane == 0) producer_loop<D>(&tm_q, &tm_k, &tm_v, p, ss, sQ, sRing, n_units);
@@ -669,7 +694,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __syncwarp();
   } else {
     setmaxnreg_inc<kSoftmaxRegs>();
-    softmax_loop<D>(p, ss, tmem, warp / 4, n_units);
+    softmax_loop<D>(p, ss, tmem, warp / kGroupWarps, n_units);
     __syncwarp();
   }
 
