@@ -71,7 +71,9 @@ static_assert(kSoftmaxWarps * 32 * kSoftmaxRegs + 128 * kControlRegs <= kThreads
               "register split exceeds the launch allotment");
 constexpr int kHalfCols = kBN / 2;       // key columns per softmax thread
 constexpr int kChunkBytes = kBM * 128; // 128 rows x 64 bf16 (one 128-byte swizzle span)
-constexpr float kRescaleLog2 = 8.0f;   // rescale O only if the row max grew by > 2^8
+// Rescale O only if the row max grew by more than 2^16: a stale-max probability
+// stays below 2^16, far inside the bf16 (P) and fp32 (O, l) exponent range.
+constexpr float kRescaleLog2 = 16.0f;
 
 // Device error word bits.
 constexpr int kErrTimeout = 1;
@@ -185,7 +187,7 @@ struct SharedState {
   volatile int abort_flag;
   volatile int unit_ring[kUnitSlots];
   float row_max[2][kQTiles][2][kBM];   // [tile parity][group][column half][row]
-  float row_sum[kQTiles][2][2][kBM];   // [group][column half][l, l_r][row]
+  float row_sum[kQTiles][2][2][kBM];   // [group][column half][l, l_fix][row]
 };
 
 // Bounded wait on an mbarrier phase; gives up on timeout or when another warp
@@ -405,6 +407,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// x rounded to the nearest bf16 (ties to even), as fp32.
+__device__ __forceinline__ float bf16_round_f32(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
+
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -425,14 +432,6 @@ __device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
       " add.rn.f32x2 r, x, y;\n mov.b64 {%0, %1}, r;\n}"
       : "+f"(a0), "+f"(a1)
       : "f"(b0), "f"(b1));
-}
-
-// acc_lo += bf16 low half of w, acc_hi += bf16 high half (exact widening).
-__device__ __forceinline__ void add_bf16x2_to_f32(float& acc_lo, float& acc_hi, uint32_t w) {
-  asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n add.rn.f32.bf16 %0, lo, %0;\n"
-      " add.rn.f32.bf16 %1, hi, %1;\n}"
-      : "+f"(acc_lo), "+f"(acc_hi)
-      : "r"(w));
 }
 
 // Named barrier of the two warps that share a 32-row quadrant of a group.
@@ -469,8 +468,8 @@ __device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss
     const int row = a0 + trow;                       // sequence-relative row of this thread
     const int nominal0 = un.qb * kUnitRows + g * kBM;
     float m_used = -INFINITY;
-    float l = 0.f;    // sum of the fp32 probabilities (this half): the LSE
-    float l_r = 0.f;  // sum of the bf16-rounded probabilities (this half): O's divisor
+    float l = 0.f;     // sum of the fp32 probabilities (this half): the LSE
+    float l_fix = 0.f; // rounding change of each tile's largest probability (this half)
     for (int j = 0; j < un.nkv; ++j) {
       if (!__all_sync(0xffffffffu, wait_bar(ss, kBarSFull + g, scount & 1, p, 20 + g))) return;
       ++scount;
@@ -532,10 +531,15 @@ __device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss
         }
       }
       const float neg = m_used == -INFINITY ? 0.f : -m_used * c2;
-      // p = 2^(c2 * s - c2 * m): packed fp32x2 FMA, MUFU ex2, packed sums;
-      // sum of the bf16-rounded values with mixed-precision adds.
+      // O is divided by l plus the bf16 rounding change of the largest
+      // probability of every 64-key half tile: when one key dominates a row,
+      // its rounding then cancels between O and the divisor (the other terms'
+      // rounding errors are small and of both signs).  Same arithmetic as the
+      // loop below, so this p_max is bit-identical to the one written to P.
+      const float p_max = ex2_approx(fmaf(mine, c2, neg));
+      const float fix = bf16_round_f32(p_max) - p_max;
+      // p = 2^(c2 * s - c2 * m): packed fp32x2 FMA, MUFU ex2, packed sums
       float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
-      float ra0 = 0.f, ra1 = 0.f;
       uint32_t pw[32];
 #pragma unroll
       for (int c = 0; c < kHalfCols; c += 4) {
@@ -548,11 +552,9 @@ __device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss
         add2(sb0, sb1, p2, p3);
         pw[c / 2] = pack_bf16x2(p0, p1);
         pw[c / 2 + 1] = pack_bf16x2(p2, p3);
-        add_bf16x2_to_f32(ra0, ra1, pw[c / 2]);
-        add_bf16x2_to_f32(ra0, ra1, pw[c / 2 + 1]);
       }
       l = l * alpha + ((sa0 + sa1) + (sb0 + sb1));
-      l_r = l_r * alpha + (ra0 + ra1);
+      l_fix = l_fix * alpha + fix;
       // O *= alpha before this tile's PV product (after the exps, when the
       // scores no longer occupy registers)
       if (rescale_warp) {
@@ -575,16 +577,16 @@ __device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss
     // thread its D/2 columns), LSE = scale * m + ln(l).  Rows before the
     // nominal tile start (recomputed) and rows past the sequence are skipped.
     ss.row_sum[g][half][0][trow] = l;
-    ss.row_sum[g][half][1][trow] = l_r;
+    ss.row_sum[g][half][1][trow] = l_fix;
     pair_sync(g, quadrant);
     l += ss.row_sum[g][half ^ 1][0][trow];
-    l_r += ss.row_sum[g][half ^ 1][1][trow];
+    const float l_r = l + l_fix + ss.row_sum[g][half ^ 1][1][trow];
     pair_sync(g, quadrant);  // both read before the next unit writes again
     if (!__all_sync(0xffffffffu, wait_bar(ss, kBarOFull + g, units_done & 1, p, 22 + g))) return;
     tc_fence_after();
     const bool store = row >= nominal0 && row < un.L && row >= 0;
-    // Dividing by the sum of the weights actually multiplied into V keeps a
-    // dominant term exact (its bf16 rounding cancels); the LSE uses the fp32 sum.
+    // O's divisor carries the rounding of each tile's dominant probability;
+    // the LSE uses the fp32 sum.
     const float inv_l = l_r > 0.f ? 1.0f / l_r : 0.f;
     __nv_bfloat16* orow =
         p.o + ((size_t)(store ? un.tok0 + row : 0) * p.H + un.h) * D + half * kOCols;
