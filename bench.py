@@ -328,7 +328,7 @@ def run_cuda(args, world, rank, local):
 # DRAM bytes (read + write) of one attn_fwd_kernel<128> launch of this
 # workload, from the ncu capture summarised under profiles/ (None until taken
 # for the current kernel).
-TRAFFIC_BYTES = None
+TRAFFIC_BYTES = 608_546_048  # 549.29 MB read + 59.25 MB written (profiles/attn_fwd_kernel_long_causal.md)
 
 
 def main():

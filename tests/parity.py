@@ -2,6 +2,9 @@
 path through the C ABI, compare chosen rows with the fp64 oracle."""
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 
 import oracle
@@ -63,6 +66,10 @@ def compare(o, lse_ht, wl, rows, what=""):
     ref_o, ref_lse, _ = oracle.attn_rows(wl.q, wl.k, wl.v, wl.cu_seqlens, rows, wl.scale, wl.causal)
     got_o, got_lse = gather(o, lse_ht, wl, rows)
     stats = error_stats(got_o, got_lse, ref_o, ref_lse)
+    log = os.environ.get("PARITY_LOG")
+    if log:
+        with open(log, "a") as f:
+            f.write(json.dumps({"case": what, **stats}) + "\n")
     assert np.isfinite(got_o).all() and np.isfinite(got_lse).all(), f"{what}: non-finite output"
     assert stats["o_max_abs"] <= O_MAX_ABS, f"{what}: {stats}"
     assert stats["o_rel_l2"] <= O_REL_L2, f"{what}: {stats}"
