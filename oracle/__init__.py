@@ -43,6 +43,12 @@ class Oracle:
                                        ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
                                        _c_i64p, ctypes.c_int64, _c_dp, _c_dp, ctypes.c_int,
                                        ctypes.POINTER(ctypes.c_int)]
+        L.oracle_attn_rows_window.restype = ctypes.c_int
+        L.oracle_attn_rows_window.argtypes = [_c_u16p, _c_u16p, _c_u16p, _c_i64p, ctypes.c_int64,
+                                              ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                              ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                              _c_i64p, ctypes.c_int64, _c_dp, _c_dp, ctypes.c_int,
+                                              ctypes.POINTER(ctypes.c_int)]
         L.oracle_attn_probs.restype = ctypes.c_int64
         L.oracle_attn_probs.argtypes = [_c_u16p, _c_u16p, _c_i64p, ctypes.c_int64, ctypes.c_int,
                                         ctypes.c_int, ctypes.c_double, ctypes.c_int,
@@ -61,10 +67,12 @@ class Oracle:
         return int(self.lib.oracle_cpu_count())
 
     def attn_rows(self, q, k, v, cu_seqlens, rows, scale: float, causal: bool,
-                  nthreads: int = 0):
+                  nthreads: int = 0, window=(-1, -1)):
         """O (fp64 [n, d]) and LSE (fp64 [n]) of the given (seq, head, row) triples.
 
-        q, k, v: uint16 bf16 bits, [tokens, H, d].  Returns (o, lse, threads_used).
+        q, k, v: uint16 bf16 bits, [tokens, H, d].  window = (wl, wr): keys
+        i - wl <= j <= i + wr only (negative: unbounded).  Returns (o, lse,
+        threads_used).
         """
         q, k, v = _u16(q), _u16(k), _u16(v)
         tokens, H, d = q.shape
@@ -74,12 +82,13 @@ class Oracle:
         o = np.zeros((n, d), dtype=np.float64)
         lse = np.zeros(n, dtype=np.float64)
         used = ctypes.c_int(0)
-        st = self.lib.oracle_attn_rows(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16),
-                                       _ptr(v, ctypes.c_uint16), _ptr(cu, ctypes.c_int64),
-                                       len(cu) - 1, H, d, float(scale), int(bool(causal)),
-                                       _ptr(rows, ctypes.c_int64), n, _ptr(o, ctypes.c_double),
-                                       _ptr(lse, ctypes.c_double), int(nthreads),
-                                       ctypes.byref(used))
+        wl, wr = (int(window[0]), int(window[1]))
+        st = self.lib.oracle_attn_rows_window(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16),
+                                              _ptr(v, ctypes.c_uint16), _ptr(cu, ctypes.c_int64),
+                                              len(cu) - 1, H, d, float(scale), int(bool(causal)),
+                                              wl, wr, _ptr(rows, ctypes.c_int64), n,
+                                              _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double),
+                                              int(nthreads), ctypes.byref(used))
         if st != 0:
             raise ValueError(f"oracle_attn_rows failed with status {st}")
         return o, lse, used.value

@@ -27,6 +27,9 @@
  * Readings where the pages are silent: "visible" is every key j < L_s, or
  * j <= i when causal (lower-triangular mask within each sequence); the LSE is
  * the natural log of sum_j exp(S_ij) in units of the scaled logits.
+ * Sliding windows ("FlashAttention" (compassingai), section 5, FlexAttention
+ * item: sliding-window masks over the same tiled kernel) narrow the visible
+ * keys further to i - wl <= j <= i + wr (wl, wr < 0: no bound on that side).
  *
  * Inputs are bf16 bit patterns (uint16) in the packed layout
  * [tokens, H, d]; sequence s occupies tokens cu_seqlens[s] .. cu_seqlens[s+1]-1.
@@ -81,6 +84,7 @@ typedef struct {
     int H, d;
     double scale;
     int causal;
+    int64_t wl, wr;      /* window: i - wl <= j <= i + wr; negative = unbounded */
     const int64_t *rows; /* [nrows][3] = (seq, head, row) */
     int64_t nrows;
     double *o;   /* [nrows][d] */
@@ -130,17 +134,24 @@ static void *rows_worker(void *arg)
             jb->status = ORACLE_EINVAL;
             break;
         }
-        const int64_t nvis = jb->causal ? i + 1 : L;
+        /* visible keys [jlo, jhi): the whole sequence, or j <= i when causal,
+           narrowed by the window to i - wl <= j <= i + wr */
+        int64_t jlo = 0, jhi = jb->causal ? i + 1 : L;
+        if (jb->wl >= 0 && i - jb->wl > jlo)
+            jlo = i - jb->wl;
+        if (jb->wr >= 0 && i + jb->wr + 1 < jhi)
+            jhi = i + jb->wr + 1;
+        const int64_t nvis = jhi > jlo ? jhi - jlo : 0;
         const uint16_t *qi = jb->q + ((base + i) * H + h) * (int64_t)d;
         for (int c = 0; c < d; ++c)
             qrow[c] = widen_bf16(qi[c]);
         /* S_ij = scale * <q_i, k_j> for every visible key, materialised */
-        for (int64_t j = 0; j < nvis; ++j) {
+        for (int64_t j = jlo; j < jhi; ++j) {
             const uint16_t *kj = jb->k + ((base + j) * H + h) * (int64_t)d;
             double dot = 0.0;
             for (int c = 0; c < d; ++c)
                 dot += qrow[c] * widen_bf16(kj[c]);
-            srow[j] = jb->scale * dot;
+            srow[j - jlo] = jb->scale * dot;
         }
         /* m_i = max_j S_ij */
         double m = -INFINITY;
@@ -157,7 +168,7 @@ static void *rows_worker(void *arg)
             oi[c] = 0.0;
         for (int64_t j = 0; j < nvis; ++j) {
             const double p = exp(srow[j] - m) / l;
-            const uint16_t *vj = jb->v + ((base + j) * H + h) * (int64_t)d;
+            const uint16_t *vj = jb->v + ((base + jlo + j) * H + h) * (int64_t)d;
             for (int c = 0; c < d; ++c)
                 oi[c] += p * widen_bf16(vj[c]);
         }
@@ -183,15 +194,17 @@ static int check_common(const void *q, const void *k, const void *v, const int64
 }
 
 /*
- * O and LSE of the requested rows, by the plain definition above.
- * nthreads <= 0 uses every CPU of the affinity mask; *threads_used (if not
+ * O and LSE of the requested rows, by the plain definition above, with the
+ * visible keys of row i narrowed to i - wl <= j <= i + wr (wl, wr < 0: no
+ * bound on that side).  nthreads <= 0 uses every CPU of the affinity mask; *threads_used (if not
  * NULL) receives the number of threads that ran.  Returns 0, or a negative
  * code for a bad argument (row outside its sequence, decreasing cu_seqlens...).
  */
-int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                     const int64_t *cu_seqlens, int64_t nseq, int H, int d,
-                     double scale, int causal, const int64_t *rows, int64_t nrows,
-                     double *o, double *lse, int nthreads, int *threads_used)
+int oracle_attn_rows_window(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                            const int64_t *cu_seqlens, int64_t nseq, int H, int d,
+                            double scale, int causal, int64_t wl, int64_t wr,
+                            const int64_t *rows, int64_t nrows, double *o, double *lse,
+                            int nthreads, int *threads_used)
 {
     int st = check_common(q, k, v, cu_seqlens, nseq, H, d, scale);
     if (st != ORACLE_OK || nrows < 0 || (nrows > 0 && (!rows || !o || !lse)))
@@ -212,6 +225,7 @@ int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
         jb->q = q; jb->k = k; jb->v = v;
         jb->cu = cu_seqlens; jb->nseq = nseq;
         jb->H = H; jb->d = d; jb->scale = scale; jb->causal = causal;
+        jb->wl = wl; jb->wr = wr;
         jb->rows = rows; jb->nrows = nrows; jb->o = o; jb->lse = lse;
         jb->begin = nrows * t / nt;
         jb->end = nrows * (t + 1) / nt;
@@ -240,6 +254,16 @@ int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     free(jobs);
     free(tid);
     return st;
+}
+
+/* O and LSE of the requested rows without a window (every visible key). */
+int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                     const int64_t *cu_seqlens, int64_t nseq, int H, int d,
+                     double scale, int causal, const int64_t *rows, int64_t nrows,
+                     double *o, double *lse, int nthreads, int *threads_used)
+{
+    return oracle_attn_rows_window(q, k, v, cu_seqlens, nseq, H, d, scale, causal, -1, -1, rows,
+                                   nrows, o, lse, nthreads, threads_used);
 }
 
 /*

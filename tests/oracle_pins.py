@@ -232,6 +232,94 @@ def check_causal_last_row(orc):
     assert np.max(np.abs(o1 - o2)) > 1e-3, "causal mask has no effect on a middle row"
 
 
+def _visible(i, L, causal, wl, wr):
+    """Visible keys of row i written out directly from the window definition."""
+    return [j for j in range(L)
+            if (not causal or j <= i) and (wl < 0 or j >= i - wl) and (wr < 0 or j <= i + wr)]
+
+
+WINDOWS = [(0, 0), (1, -1), (2, 1), (-1, 2), (3, 0), (0, 5), (-1, -1)]
+
+
+def check_window_brute_force_decimal(orc):
+    """Sliding windows on tiny inputs against 50-digit decimal evaluation."""
+    getcontext().prec = 50
+    wl_ = _rand_workload(111, [6, 9], H=2, d=4, std=1.2)
+    rows = inputs.all_rows(wl_.cu_seqlens, wl_.H)
+    qf, kf, vf = (inputs.bf16_bits_to_f64(a) for a in (wl_.q, wl_.k, wl_.v))
+    for causal in (False, True):
+        for (a, b) in WINDOWS:
+            o, lse, _ = orc.attn_rows(wl_.q, wl_.k, wl_.v, wl_.cu_seqlens, rows, 0.6, causal, 1,
+                                      window=(a, b))
+            for n, (s, h, i) in enumerate(rows):
+                base = int(wl_.cu_seqlens[s]); L = int(wl_.cu_seqlens[s + 1]) - base
+                vis = _visible(i, L, causal, a, b)
+                e = [(Decimal(0.6) * sum(Decimal(qf[base + i, h, c]) * Decimal(kf[base + j, h, c])
+                                         for c in range(wl_.d))).exp() for j in vis]
+                z = sum(e)
+                ref = [float(sum(e[t] * Decimal(vf[base + j, h, c]) for t, j in enumerate(vis)) / z)
+                       for c in range(wl_.d)]
+                _close(o[n], ref, 1e-13, f"window {(a, b)} causal={causal} row {(s, h, i)}")
+                _close(lse[n], float(z.ln()), 1e-13, f"window LSE {(a, b)}")
+
+
+def check_window_closed_forms(orc):
+    """A zero-width window sees only its own key: O_i = v_i, LSE_i = scale q_i.k_i.
+    Q = 0 gives the mean of V over the window; a window wider than the
+    sequence is no window."""
+    wl_ = _rand_workload(112, [20, 7], H=2, d=8)
+    rows = inputs.all_rows(wl_.cu_seqlens, wl_.H)
+    qf, kf, vf = (inputs.bf16_bits_to_f64(a) for a in (wl_.q, wl_.k, wl_.v))
+    for causal, win in ((True, (0, -1)), (False, (0, 0))):
+        o, lse, _ = orc.attn_rows(wl_.q, wl_.k, wl_.v, wl_.cu_seqlens, rows, 0.4, causal, 1,
+                                  window=win)
+        for n, (s, h, i) in enumerate(rows):
+            t = int(wl_.cu_seqlens[s]) + i
+            _close(o[n], vf[t, h], 0.0, "zero window picks v_i")
+            _close(lse[n], 0.4 * float(np.dot(qf[t, h], kf[t, h])), 1e-14, "zero window LSE")
+    zero = np.zeros_like(wl_.q)
+    for causal in (False, True):
+        for (a, b) in WINDOWS:
+            o, lse, _ = orc.attn_rows(zero, wl_.k, wl_.v, wl_.cu_seqlens, rows, 0.4, causal, 1,
+                                      window=(a, b))
+            for n, (s, h, i) in enumerate(rows):
+                base = int(wl_.cu_seqlens[s]); L = int(wl_.cu_seqlens[s + 1]) - base
+                vis = _visible(i, L, causal, a, b)
+                _close(o[n], vf[[base + j for j in vis], h].mean(axis=0), 1e-14, "Q=0 window mean")
+                _close(lse[n], math.log(len(vis)), 1e-14, "Q=0 window LSE")
+        o1, l1, _ = orc.attn_rows(wl_.q, wl_.k, wl_.v, wl_.cu_seqlens, rows, 0.4, causal, 1,
+                                  window=(100, 100))
+        o2, l2, _ = orc.attn_rows(wl_.q, wl_.k, wl_.v, wl_.cu_seqlens, rows, 0.4, causal, 1)
+        _close(o1, o2, 0.0, "wide window is no window")
+        _close(l1, l2, 0.0, "wide window LSE")
+
+
+def check_window_torch_sdpa(orc):
+    """torch scaled_dot_product_attention (fp64, CPU) with the window as a boolean mask."""
+    import torch
+    B, H, N, d = 2, 2, 37, 8
+    wl_ = _rand_workload(113, [N] * B, H=H, d=d, std=1.3)
+    rows = inputs.all_rows(wl_.cu_seqlens, H)
+    to_t = lambda a: torch.from_numpy(inputs.bf16_bits_to_f64(a).reshape(B, N, H, d)).permute(0, 2, 1, 3)
+    qt, kt, vt = to_t(wl_.q), to_t(wl_.k), to_t(wl_.v)
+    ii = torch.arange(N).view(N, 1)
+    jj = torch.arange(N).view(1, N)
+    for causal in (False, True):
+        for (a, b) in [(4, 0), (2, 3), (10, -1), (-1, 1)]:
+            mask = torch.ones(N, N, dtype=torch.bool)
+            if causal:
+                mask &= jj <= ii
+            if a >= 0:
+                mask &= jj >= ii - a
+            if b >= 0:
+                mask &= jj <= ii + b
+            ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=0.3)
+            o, _, _ = orc.attn_rows(wl_.q, wl_.k, wl_.v, wl_.cu_seqlens, rows, 0.3, causal, 2,
+                                    window=(a, b))
+            for n, (s, h, i) in enumerate(rows):
+                _close(o[n], ref[s, h, i].numpy(), 1e-12, f"SDPA window {(a, b)} causal={causal}")
+
+
 ALL_CHECKS = [
     check_brute_force_decimal,
     check_two_key_closed_form,
@@ -244,4 +332,7 @@ ALL_CHECKS = [
     check_online_loop,
     check_packing,
     check_causal_last_row,
+    check_window_brute_force_decimal,
+    check_window_closed_forms,
+    check_window_torch_sdpa,
 ]

@@ -16,22 +16,25 @@ from tests import oracle_pins
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
 MUTANTS = {
-    "drop_scale": [("srow[j] = jb->scale * dot;", "srow[j] = dot;")],
+    "drop_scale": [("srow[j - jlo] = jb->scale * dot;", "srow[j - jlo] = dot;")],
     "no_normalise": [("const double p = exp(srow[j] - m) / l;", "const double p = exp(srow[j] - m);")],
     "lse_without_max": [("jb->lse[r] = nvis > 0 ? m + log(l)", "jb->lse[r] = nvis > 0 ? log(l)")],
     "lse_sign": [("jb->lse[r] = nvis > 0 ? m + log(l)", "jb->lse[r] = nvis > 0 ? m - log(l)")],
     "v_read_from_k": [("const uint16_t *vj = jb->v + ", "const uint16_t *vj = jb->k + ")],
-    "causal_ignored": [("const int64_t nvis = jb->causal ? i + 1 : L;\n        const uint16_t *qi = jb->q",
-                        "const int64_t nvis = L;\n        const uint16_t *qi = jb->q")],
-    "causal_excludes_diagonal": [("const int64_t nvis = jb->causal ? i + 1 : L;\n        const uint16_t *qi = jb->q",
-                                  "const int64_t nvis = jb->causal ? (i > 0 ? i : 1) : L;\n        const uint16_t *qi = jb->q")],
+    "causal_ignored": [("int64_t jlo = 0, jhi = jb->causal ? i + 1 : L;",
+                        "int64_t jlo = 0, jhi = L;")],
+    "causal_excludes_diagonal": [("int64_t jlo = 0, jhi = jb->causal ? i + 1 : L;",
+                                  "int64_t jlo = 0, jhi = jb->causal ? (i > 0 ? i : 1) : L;")],
+    "window_left_off_by_one": [("            jlo = i - jb->wl;", "            jlo = i - jb->wl + 1;")],
+    "window_right_ignored": [("            jhi = i + jb->wr + 1;", "            jhi = jhi;")],
+    "window_v_not_shifted": [("((base + jlo + j) * H + h)", "((base + j) * H + h)")],
     "k_wrong_head": [("const uint16_t *kj = jb->k + ((base + j) * H + h)",
                       "const uint16_t *kj = jb->k + ((base + j) * H + 0)")],
     "transposed_scores": [("const uint16_t *qi = jb->q + ((base + i) * H + h) * (int64_t)d;",
                            "const uint16_t *qi = jb->k + ((base + i) * H + h) * (int64_t)d;"),
                           ("const uint16_t *kj = jb->k + ((base + j) * H + h) * (int64_t)d;\n            double dot",
                            "const uint16_t *kj = jb->q + ((base + j) * H + h) * (int64_t)d;\n            double dot")],
-    "sequence_base_ignored": [("const uint16_t *vj = jb->v + ((base + j)", "const uint16_t *vj = jb->v + ((0 + j)")],
+    "sequence_base_ignored": [("const uint16_t *vj = jb->v + ((base + jlo + j)", "const uint16_t *vj = jb->v + ((jlo + j)")],
     "short_dot": [("for (int c = 0; c < d; ++c)\n                dot += qrow[c]",
                    "for (int c = 0; c < d - 1; ++c)\n                dot += qrow[c]")],
     "exp_sign": [("l += exp(srow[j] - m);", "l += exp(m - srow[j]);")],
