@@ -72,6 +72,21 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
              int B, int H, int N, int d, float scale, int causal,
              const int32_t *cu_seqlens, attn_stream_t stream);
 
+/*
+ * attn_fwd_window: attn_fwd with a sliding window.  Key j is visible to query
+ * i iff i - window_left <= j <= i + window_right (within the sequence, and
+ * j <= i when causal); -1 leaves that side unbounded, so (-1, -1) is attn_fwd.
+ * Tiles outside every row's window are skipped, so the cost grows with the
+ * window, not with the sequence.  Sliding-window masks over the same tiled
+ * kernel: "FlashAttention" (compassingai), section 5, FlexAttention item.
+ * Same layouts, ownership and errors as attn_fwd; a window value below -1
+ * returns ATTN_ERR_SHAPE.
+ */
+int attn_fwd_window(const void *q, const void *k, const void *v, void *o, float *lse,
+                    int B, int H, int N, int d, float scale, int causal,
+                    int window_left, int window_right, const int32_t *cu_seqlens,
+                    attn_stream_t stream);
+
 /* Options of attn_fwd_ex.  Zero-initialise and set what is needed. */
 typedef struct {
     uint64_t wait_timeout_ns; /* bound on each device-side wait; 0 = 2 s */

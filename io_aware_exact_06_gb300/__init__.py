@@ -13,13 +13,14 @@ import os
 
 from . import build as _build
 
-__all__ = ["attn_fwd", "attn_fwd_ex", "attn_fwd_noalloc", "attn_last_device_error", "attn_last_error_site",
+__all__ = ["attn_fwd", "attn_fwd_ex", "attn_fwd_noalloc", "attn_fwd_window", "attn_last_device_error", "attn_last_error_site",
            "attn_status_string", "AttnError", "AttnFwdOptions", "lib", "forward",
            "EXPORTED_SYMBOLS"]
 
 # Every symbol include/attn_fwd.h declares.
 EXPORTED_SYMBOLS = ("attn_fwd", "attn_fwd_ex", "attn_last_device_error", "attn_last_error_site",
-                    "attn_last_cuda_error", "attn_status_string", "attn_fwd_noalloc")
+                    "attn_last_cuda_error", "attn_status_string", "attn_fwd_noalloc",
+                    "attn_fwd_window")
 
 ATTN_OK = 0
 
@@ -55,6 +56,8 @@ def lib() -> ctypes.CDLL:
         L.attn_fwd.restype = i
         L.attn_fwd_ex.argtypes = sig + [ctypes.POINTER(AttnFwdOptions)]
         L.attn_fwd_ex.restype = i
+        L.attn_fwd_window.argtypes = sig[:11] + [i, i] + sig[11:]
+        L.attn_fwd_window.restype = i
         L.attn_fwd_noalloc.argtypes = sig
         L.attn_fwd_noalloc.restype = i
         L.attn_last_device_error.argtypes = [vp]
@@ -108,6 +111,18 @@ def attn_fwd_ex(q, k, v, o, lse, B: int, H: int, N: int, d: int, scale: float, c
                            _stream(stream), ctypes.byref(opts))
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_ex")
+    return st
+
+
+def attn_fwd_window(q, k, v, o, lse, B: int, H: int, N: int, d: int, scale: float, causal: bool,
+                    window_left: int, window_right: int, cu_seqlens=None, stream=None) -> int:
+    """The C call ``attn_fwd_window``: keys i - window_left <= j <= i + window_right
+    (-1: unbounded side)."""
+    st = lib().attn_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H),
+                               int(N), int(d), float(scale), int(bool(causal)), int(window_left),
+                               int(window_right), _ptr(cu_seqlens), _stream(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_window")
     return st
 
 

@@ -65,6 +65,26 @@ int get_encode(EncodeTiledFn* out) {
   return ATTN_OK;
 }
 
+// Dynamic shared memory limits of every attention kernel instantiation.
+cudaError_t set_smem_attributes() {
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(attn::attn_fwd_kernel<64, false>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                FwdCfg<64>::kSmemBytes)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(attn::attn_fwd_kernel<128, false>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                FwdCfg<128>::kSmemBytes)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(attn::attn_fwd_kernel<64, true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                FwdCfg<64>::kSmemBytes)) != cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(attn::attn_fwd_kernel<128, true>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              FwdCfg<128>::kSmemBytes);
+}
+
 int device_state(int dev, DeviceState** out) {
   DeviceState& st = g_dev[dev];
   if (!st.ready) {
@@ -76,14 +96,7 @@ int device_state(int dev, DeviceState** out) {
     if ((e = cudaDeviceGetAttribute(&st.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
       return cuda_fail(e);
     if (st.major != 10 || st.minor != 3) return ATTN_ERR_ARCH;
-    if ((e = cudaFuncSetAttribute(attn::attn_fwd_kernel<64>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  FwdCfg<64>::kSmemBytes)) != cudaSuccess)
-      return cuda_fail(e);
-    if ((e = cudaFuncSetAttribute(attn::attn_fwd_kernel<128>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  FwdCfg<128>::kSmemBytes)) != cudaSuccess)
-      return cuda_fail(e);
+    if ((e = set_smem_attributes()) != cudaSuccess) return cuda_fail(e);
     if ((e = cudaMalloc(&st.err, 4 * sizeof(int))) != cudaSuccess) return cuda_fail(e);
     if ((e = cudaMemset(st.err, 0, 4 * sizeof(int))) != cudaSuccess) return cuda_fail(e);
     st.ready = true;
@@ -133,18 +146,23 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 template <int D>
 int launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                 const FwdParams& p, int grid, cudaStream_t s) {
-  attn::attn_fwd_kernel<D><<<grid, attn::kThreads, FwdCfg<D>::kSmemBytes, s>>>(mq, mk, mv, p);
+  if (p.wl >= 0 || p.wr >= 0)
+    attn::attn_fwd_kernel<D, true><<<grid, attn::kThreads, FwdCfg<D>::kSmemBytes, s>>>(mq, mk, mv, p);
+  else
+    attn::attn_fwd_kernel<D, false><<<grid, attn::kThreads, FwdCfg<D>::kSmemBytes, s>>>(mq, mk, mv, p);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 
 }  // namespace
 
-extern "C" int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
-                           int B, int H, int N, int d, float scale, int causal,
-                           const int32_t* cu_seqlens, attn_stream_t stream,
-                           const attn_fwd_options* opts) {
+namespace {
+
+int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                  int N, int d, float scale, int causal, int window_left, int window_right,
+                  const int32_t* cu_seqlens, attn_stream_t stream, const attn_fwd_options* opts) {
   if (B < 0 || H < 0 || N < 0) return ATTN_ERR_SHAPE;
+  if (window_left < -1 || window_right < -1) return ATTN_ERR_SHAPE;
   if (d != 64 && d != 128) return ATTN_ERR_HEADDIM;
   if (!std::isfinite(scale)) return ATTN_ERR_SCALE;
   if (B == 0 || H == 0 || N == 0) return ATTN_OK;
@@ -187,6 +205,8 @@ extern "C" int attn_fwd_ex(const void* q, const void* k, const void* v, void* o,
   p.H = H;
   p.N = N;
   p.causal = causal ? 1 : 0;
+  p.wl = window_left;
+  p.wr = window_right;
   p.scale = scale;
   p.scale_log2 = (float)((double)scale * 1.4426950408889634);
   p.timeout_ns = (opts && opts->wait_timeout_ns) ? opts->wait_timeout_ns : 2000000000ull;
@@ -204,7 +224,7 @@ extern "C" int attn_fwd_ex(const void* q, const void* k, const void* v, void* o,
     const int ncost = (int)std::min<int64_t>((N + attn::kBN - 1) / attn::kBN,
                                              attn::kMaxCostBuckets - 1);
     attn::build_worklist_kernel<<<1, 1024, (ncost + 1) * sizeof(int), s>>>(
-        cu_seqlens, B, N, p.causal, ws + 4, ws, ds->err, (int)max_entries, ws + 1);
+        cu_seqlens, B, N, p.causal, p.wl, p.wr, ws + 4, ws, ds->err, (int)max_entries, ws + 1);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
   } else if (units < grid) {
     grid = (int)units;
@@ -213,10 +233,29 @@ extern "C" int attn_fwd_ex(const void* q, const void* k, const void* v, void* o,
   return d == 64 ? launch_attn<64>(mq, mk, mv, p, grid, s) : launch_attn<128>(mq, mk, mv, p, grid, s);
 }
 
+}  // namespace
+
+extern "C" int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int H, int N, int d, float scale, int causal,
+                           const int32_t* cu_seqlens, attn_stream_t stream,
+                           const attn_fwd_options* opts) {
+  return attn_fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, -1, -1, cu_seqlens, stream,
+                       opts);
+}
+
 extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                         int H, int N, int d, float scale, int causal, const int32_t* cu_seqlens,
                         attn_stream_t stream) {
-  return attn_fwd_ex(q, k, v, o, lse, B, H, N, d, scale, causal, cu_seqlens, stream, nullptr);
+  return attn_fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, -1, -1, cu_seqlens, stream,
+                       nullptr);
+}
+
+extern "C" int attn_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse,
+                               int B, int H, int N, int d, float scale, int causal,
+                               int window_left, int window_right, const int32_t* cu_seqlens,
+                               attn_stream_t stream) {
+  return attn_fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, window_left, window_right,
+                       cu_seqlens, stream, nullptr);
 }
 
 extern "C" int attn_last_device_error(attn_stream_t stream) {
@@ -298,14 +337,7 @@ int noalloc_setup(int dev, NoAllocDevice** out) {
     if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
       return cuda_fail(e);
     if (major != 10 || minor != 3) return ATTN_ERR_ARCH;
-    if ((e = cudaFuncSetAttribute(attn::attn_fwd_kernel<64>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  FwdCfg<64>::kSmemBytes)) != cudaSuccess)
-      return cuda_fail(e);
-    if ((e = cudaFuncSetAttribute(attn::attn_fwd_kernel<128>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  FwdCfg<128>::kSmemBytes)) != cudaSuccess)
-      return cuda_fail(e);
+    if ((e = set_smem_attributes()) != cudaSuccess) return cuda_fail(e);
     void* ptr = nullptr;
     if ((e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch)) != cudaSuccess) return cuda_fail(e);
     st.scratch = static_cast<int*>(ptr);
@@ -366,6 +398,8 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
   p.H = H;
   p.N = N;
   p.causal = causal ? 1 : 0;
+  p.wl = -1;
+  p.wr = -1;
   p.scale = scale;
   p.scale_log2 = (float)((double)scale * 1.4426950408889634);
   p.timeout_ns = 2000000000ull;
@@ -378,7 +412,7 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
     const int ncost = (int)std::min<int64_t>((N + attn::kBN - 1) / attn::kBN,
                                              attn::kMaxCostBuckets - 1);
     attn::build_worklist_kernel<<<1, 1024, (ncost + 1) * sizeof(int), s>>>(
-        cu_seqlens, B, N, p.causal, scratch + kNoAllocHeader, scratch + 2, scratch,
+        cu_seqlens, B, N, p.causal, p.wl, p.wr, scratch + kNoAllocHeader, scratch + 2, scratch,
         (int)entries, scratch + 3);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
   } else if (units < grid) {

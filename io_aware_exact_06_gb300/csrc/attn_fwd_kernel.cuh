@@ -91,6 +91,7 @@ struct FwdParams {
                            // reset to zero by the last CTA to finish
   int B, H, N;
   int causal;
+  int wl, wr;              // sliding window: keys i - wl <= j <= i + wr (-1: unbounded)
   float scale;             // softmax scale on the logits
   float scale_log2;        // scale * log2(e)
   unsigned long long timeout_ns;
@@ -135,8 +136,24 @@ struct Unit {
   int seq, h, qb;
   int tok0;  // first token of the sequence in the packed tensors
   int L;     // sequence length
+  int kv0;   // first KV tile visited
   int nkv;   // KV tiles visited
 };
+
+// KV tiles [kv0, kv0 + nkv) that hold a key visible to some row of q-block qb
+// (rows [256 qb, 256 qb + 256) of a sequence of length L): every key, or keys
+// up to the row when causal, narrowed by the sliding window.  Tiles outside
+// are skipped; the cost of the unit is nkv.
+__host__ __device__ __forceinline__ void unit_kv_range(int L, int qb, int causal, int wl, int wr,
+                                                       int& kv0, int& nkv) {
+  const int r_lo = qb * kUnitRows;
+  const int r_hi = min(qb * kUnitRows + kUnitRows, L) - 1;
+  int k_lo = 0, k_hi = causal ? r_hi : L - 1;
+  if (wl >= 0) k_lo = max(0, r_lo - wl);
+  if (wr >= 0) k_hi = min(k_hi, r_hi + wr);
+  kv0 = k_lo / kBN;
+  nkv = k_hi / kBN + 1 - kv0;
+}
 
 __device__ __forceinline__ int num_units(const FwdParams& p) {
   if (p.cu_seqlens) return *p.num_entries * p.H;
@@ -164,8 +181,7 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
     un.tok0 = un.seq * p.N;
     un.L = p.N;
   }
-  const int row_end = p.causal ? min(un.L, (un.qb + 1) * kUnitRows) : un.L;
-  un.nkv = (row_end + kBN - 1) / kBN;
+  unit_kv_range(un.L, un.qb, p.causal, p.wl, p.wr, un.kv0, un.nkv);
   return un;
 }
 
@@ -250,7 +266,7 @@ __device__ __forceinline__ void producer_loop(const CUtensorMap* tm_q, const CUt
                     bar_addr(ss, kBarQFull), c * 64, un.h, r0);
     }
     for (int j = 0; j < un.nkv; ++j) {
-      const int k0 = un.tok0 + kv_tile_start(un, j);
+      const int k0 = un.tok0 + kv_tile_start(un, un.kv0 + j);
       for (int kind = 0; kind < 2; ++kind) {
         const int slot = ring % C::kStages;
         const uint32_t n = ring / C::kStages;
@@ -439,7 +455,7 @@ __device__ __forceinline__ void pair_sync(int g, int quadrant) {
   asm volatile("bar.sync %0, %1;" ::"r"(1 + g * 4 + quadrant), "r"(64) : "memory");
 }
 
-template <int D>
+template <int D, bool kWindow>
 __device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss, uint32_t tmem,
                                              int g, int n_units) {
   using C = FwdCfg<D>;
@@ -488,14 +504,26 @@ __device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss
         }
       }
       // Mask: keys already visited by the previous tile (pulled-back last
-      // tile) and, when causal, keys after this row.  The pull-back keeps
-      // every loaded key inside the sequence.  Decided per group, applied
-      // per row; column c of this thread is key column half*64 + c.
-      const int b0 = kv_tile_start(un, j);
-      const int lo = j * kBN - b0 - half * kHalfCols;
-      const bool need_mask = j * kBN > b0 || (p.causal && b0 + kBN - 1 > a0);
+      // tile), keys after this row when causal, keys outside the sliding
+      // window.  The pull-back keeps every loaded key inside the sequence.
+      // Decided per group, applied per row; column c of this thread is key
+      // column half*64 + c.
+      const int jt = un.kv0 + j;  // tile index within the sequence
+      const int b0 = kv_tile_start(un, jt);
+      // keys every row of the group may see: [max_klo, min_khi]
+      const int max_klo = (kWindow && p.wl >= 0) ? max(0, a0 + kBM - 1 - p.wl) : 0;
+      int min_khi = p.causal ? a0 : un.L - 1;
+      if (kWindow && p.wr >= 0) min_khi = min(min_khi, a0 + p.wr);
+      const bool need_mask = jt * kBN > b0 || b0 < max_klo || b0 + kBN - 1 > min_khi;
       if (need_mask) {
-        const int hi = (p.causal ? min(row - b0, kBN - 1) : kBN - 1) - half * kHalfCols;
+        // this row's keys [klo, khi]; keys below jt*128 were visited by the
+        // previous tile (pulled-back last tile)
+        int klo = (kWindow && p.wl >= 0) ? max(0, row - p.wl) : 0;
+        int khi = p.causal ? row : un.L - 1;
+        if (kWindow && p.wr >= 0) khi = min(khi, row + p.wr);
+        klo = max(klo, jt * kBN);
+        const int lo = klo - b0 - half * kHalfCols;
+        const int hi = min(khi - b0, kBN - 1) - half * kHalfCols;
 #pragma unroll
         for (int c = 0; c < kHalfCols; ++c)
           if (c < lo || c > hi) s[c] = -INFINITY;
@@ -518,18 +546,18 @@ __device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss
       const float m_new = fmaxf(m_used, mx);
       // O correction decision: only when the row max grew by more than 2^8
       // (warp-uniform; the partner warp holds the same rows and decides alike)
+      // (a row whose keys so far were all hidden has O = 0 and l = 0: its
+      // first visible key sets the reference without a rescale)
       float alpha = 1.0f;
-      bool rescale_warp = false;
-      if (j == 0) {
+      bool resc = false;
+      if (m_used == -INFINITY) {
         m_used = m_new;
-      } else {
-        const bool resc = (m_new - m_used) * c2 > kRescaleLog2;
-        rescale_warp = __any_sync(0xffffffffu, resc);
-        if (resc) {
-          alpha = ex2_approx((m_used - m_new) * c2);
-          m_used = m_new;
-        }
+      } else if ((m_new - m_used) * c2 > kRescaleLog2) {
+        resc = true;
+        alpha = ex2_approx((m_used - m_new) * c2);
+        m_used = m_new;
       }
+      const bool rescale_warp = __any_sync(0xffffffffu, resc);
       const float neg = m_used == -INFINITY ? 0.f : -m_used * c2;
       // O is divided by l plus the bf16 rounding change of the largest
       // probability of every 64-key half tile: when one key dominates a row,
@@ -632,7 +660,9 @@ __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-template <int D>
+// kWindow: the sliding-window bounds p.wl / p.wr are applied (a separate
+// instantiation, so plain attention carries none of that arithmetic).
+template <int D, bool kWindow>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -696,7 +726,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __syncwarp();
   } else {
     setmaxnreg_inc<kSoftmaxRegs>();
-    softmax_loop<D>(p, ss, tmem, warp / kGroupWarps, n_units);
+    softmax_loop<D, kWindow>(p, ss, tmem, warp / kGroupWarps, n_units);
     __syncwarp();
   }
 
@@ -732,8 +762,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 constexpr int kMaxCostBuckets = 8192;
 
 __global__ void __launch_bounds__(1024)
-build_worklist_kernel(const int* cu_seqlens, int nseq, int max_len, int causal, int* work,
-                      int* num_entries, int* err, int max_entries, int* sched) {
+build_worklist_kernel(const int* cu_seqlens, int nseq, int max_len, int causal, int wl, int wr,
+                      int* work, int* num_entries, int* err, int max_entries, int* sched) {
   extern __shared__ int hist[];  // [ncost + 1]
   __shared__ int bad;
   __shared__ int total;
@@ -759,8 +789,9 @@ build_worklist_kernel(const int* cu_seqlens, int nseq, int max_len, int causal, 
     return;
   }
   auto cost_of = [&](int L, int qb) {
-    const int row_end = causal ? min(L, (qb + 1) * kUnitRows) : L;
-    return min((row_end + kBN - 1) / kBN, ncost);
+    int kv0, nkv;
+    unit_kv_range(L, qb, causal, wl, wr, kv0, nkv);
+    return min(nkv, ncost);
   };
   for (int s = threadIdx.x; s < nseq; s += blockDim.x) {
     const int L = cu_seqlens[s + 1] - cu_seqlens[s];

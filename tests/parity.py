@@ -21,7 +21,7 @@ def to_device(wl, dev):
     return t(wl.q), t(wl.k), t(wl.v), torch.from_numpy(wl.cu_seqlens).to(dev)
 
 
-def run_cuda(wl, dev, packed: bool | None = None, stream=None, **opts):
+def run_cuda(wl, dev, packed: bool | None = None, stream=None, window=None, **opts):
     """Runs the CUDA path on workload wl.  Dense layout when every sequence has
     the same length and packed is not forced; returns (o [tokens,H,d] bf16,
     lse [H, tokens] fp32) on the device, plus the device error status."""
@@ -34,12 +34,21 @@ def run_cuda(wl, dev, packed: bool | None = None, stream=None, **opts):
     if dense:
         B, N = wl.nseq, int(lens[0])
         lse = torch.empty((B, wl.H, N), dtype=torch.float32, device=dev)
-        fa.attn_fwd_ex(q, k, v, o, lse, B, wl.H, N, wl.d, wl.scale, wl.causal, None, stream, **opts)
+        if window is None:
+            fa.attn_fwd_ex(q, k, v, o, lse, B, wl.H, N, wl.d, wl.scale, wl.causal, None, stream, **opts)
+        else:
+            fa.attn_fwd_window(q, k, v, o, lse, B, wl.H, N, wl.d, wl.scale, wl.causal, window[0],
+                               window[1], None, stream)
         lse_ht = lse.permute(1, 0, 2).reshape(wl.H, B * N)
     else:
         lse = torch.empty((wl.H, wl.tokens), dtype=torch.float32, device=dev)
-        fa.attn_fwd_ex(q, k, v, o, lse, wl.nseq, wl.H, int(lens.max()) if len(lens) else 0, wl.d,
-                       wl.scale, wl.causal, cu, stream, **opts)
+        N = int(lens.max()) if len(lens) else 0
+        if window is None:
+            fa.attn_fwd_ex(q, k, v, o, lse, wl.nseq, wl.H, N, wl.d, wl.scale, wl.causal, cu, stream,
+                           **opts)
+        else:
+            fa.attn_fwd_window(q, k, v, o, lse, wl.nseq, wl.H, N, wl.d, wl.scale, wl.causal,
+                               window[0], window[1], cu, stream)
         lse_ht = lse
     status = fa.attn_last_device_error(stream)
     return o, lse_ht, status
@@ -62,8 +71,9 @@ def error_stats(got_o, got_lse, ref_o, ref_lse):
     }
 
 
-def compare(o, lse_ht, wl, rows, what=""):
-    ref_o, ref_lse, _ = oracle.attn_rows(wl.q, wl.k, wl.v, wl.cu_seqlens, rows, wl.scale, wl.causal)
+def compare(o, lse_ht, wl, rows, what="", window=(-1, -1)):
+    ref_o, ref_lse, _ = oracle.attn_rows(wl.q, wl.k, wl.v, wl.cu_seqlens, rows, wl.scale, wl.causal,
+                                         window=window)
     got_o, got_lse = gather(o, lse_ht, wl, rows)
     stats = error_stats(got_o, got_lse, ref_o, ref_lse)
     log = os.environ.get("PARITY_LOG")

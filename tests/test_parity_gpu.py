@@ -147,3 +147,55 @@ def test_invalid_cu_seqlens_reported(dev, bad):
     fa.attn_fwd(q, k, v, o, lse, 3, 2, 128, 64, wl.scale, True, cu, None)
     assert fa.attn_last_device_error() == -8
     assert (o.float() == 7.0).all() and (lse == 7.0).all(), "nothing is written"
+
+
+# ---------------------------------------------------------------- windows --
+# Sliding windows: key j visible to query i iff i - wl <= j <= i + wr (-1:
+# unbounded), on top of the causal mask.
+
+def test_window_long_causal_sampled(dev):
+    """The long causal workload with a 1024-key window (keys i-1023 .. i)."""
+    wl = workload("long_causal")
+    o, lse, st = parity.run_cuda(wl, dev, window=(1023, -1))
+    assert st == 0
+    rows = inputs.sample_rows(wl.cu_seqlens, wl.H, 4096, seed=inputs.CONFIG_SEED_BASE + 8)
+    parity.compare(o, lse, wl, rows, "window 1023 causal", window=(1023, -1))
+
+
+WINDOWS = [(0, 0), (5, -1), (127, 3), (128, 128), (300, -1), (-1, 64), (0, -1), (1000, 1000)]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_window_ragged_packed(dev, d, causal):
+    lens = [1, 127, 128, 129, 0, 255, 256, 257, 300, 2, 513]
+    wl = inputs.make_workload("ragged", 4343 + d, lens, 2, d, causal, qk_std=1.5, varlen=True)
+    rows = inputs.all_rows(wl.cu_seqlens, wl.H)
+    for win in WINDOWS:
+        o, lse, st = parity.run_cuda(wl, dev, packed=True, window=win)
+        assert st == 0
+        parity.compare(o, lse, wl, rows, f"window {win} ragged", window=win)
+
+
+def test_window_dense_odd_length(dev):
+    wl = inputs.make_workload("dense_win", 99, [1000, 1000], 2, 128, False)
+    for win in [(100, 37), (0, 200), (513, 0)]:
+        o, lse, st = parity.run_cuda(wl, dev, window=win)
+        assert st == 0
+        parity.compare(o, lse, wl, inputs.all_rows(wl.cu_seqlens, wl.H), f"window {win} dense",
+                       window=win)
+
+
+def test_window_unbounded_equals_plain(dev):
+    import torch
+    wl = workload("gpt2_causal")
+    o1, l1, _ = parity.run_cuda(wl, dev)
+    o2, l2, _ = parity.run_cuda(wl, dev, window=(-1, -1))
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_window_rejects_bad_values(dev):
+    import io_aware_exact_06_gb300 as fa
+    with pytest.raises(fa.AttnError):
+        fa.attn_fwd_window(1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 1, 1, 128, 64, 0.1, True,
+                           -2, 0)
