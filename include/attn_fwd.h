@@ -87,6 +87,29 @@ int attn_fwd_window(const void *q, const void *k, const void *v, void *o, float 
                     int window_left, int window_right, const int32_t *cu_seqlens,
                     attn_stream_t stream);
 
+/*
+ * attn_fwd_kvsplit: queries and keys of different lengths, the keys of every
+ * query block processed in num_splits ranges by separate work units whose
+ * partial results (O / l and LSE per range, fp32) are merged afterwards by
+ * the two-segment merge identity ("flash-attention-evolution" (letsgetai),
+ * FlashAttention "核心机制"); parallelising over the key sequence for
+ * inference is the pages' FlashDecoding item ("FlashAttention" (compassingai),
+ * section 5).
+ * Layout (dense): q, o [B, Nq, H, d]; k, v [B, Nk, H, d]; lse [B, H, Nq].
+ * causal: query row r sits at key position Nk - Nq + r (the queries are the
+ *   last Nq positions of the key sequence) and sees keys j <= Nk - Nq + r;
+ *   requires Nq <= Nk.  Non-causal: every key is visible.
+ * num_splits: 1..256 ranges, or 0 to choose (the count with the shortest
+ *   estimated makespan over the SMs, at most 64).
+ * Ownership: like attn_fwd; in addition the library keeps a per-(device,
+ *   stream) fp32 workspace for the partial results, grown on demand.
+ * Errors: like attn_fwd; Nk == 0, num_splits outside [0, 256] or causal with
+ *   Nq > Nk return ATTN_ERR_SHAPE.
+ */
+int attn_fwd_kvsplit(const void *q, const void *k, const void *v, void *o, float *lse,
+                     int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                     int num_splits, attn_stream_t stream);
+
 /* Options of attn_fwd_ex.  Zero-initialise and set what is needed. */
 typedef struct {
     uint64_t wait_timeout_ns; /* bound on each device-side wait; 0 = 2 s */

@@ -13,14 +13,14 @@ import os
 
 from . import build as _build
 
-__all__ = ["attn_fwd", "attn_fwd_ex", "attn_fwd_noalloc", "attn_fwd_window", "attn_last_device_error", "attn_last_error_site",
+__all__ = ["attn_fwd", "attn_fwd_ex", "attn_fwd_noalloc", "attn_fwd_window", "attn_fwd_kvsplit", "attn_last_device_error", "attn_last_error_site",
            "attn_status_string", "AttnError", "AttnFwdOptions", "lib", "forward",
            "EXPORTED_SYMBOLS"]
 
 # Every symbol include/attn_fwd.h declares.
 EXPORTED_SYMBOLS = ("attn_fwd", "attn_fwd_ex", "attn_last_device_error", "attn_last_error_site",
                     "attn_last_cuda_error", "attn_status_string", "attn_fwd_noalloc",
-                    "attn_fwd_window")
+                    "attn_fwd_window", "attn_fwd_kvsplit")
 
 ATTN_OK = 0
 
@@ -58,6 +58,8 @@ def lib() -> ctypes.CDLL:
         L.attn_fwd_ex.restype = i
         L.attn_fwd_window.argtypes = sig[:11] + [i, i] + sig[11:]
         L.attn_fwd_window.restype = i
+        L.attn_fwd_kvsplit.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_float, i, i, vp]
+        L.attn_fwd_kvsplit.restype = i
         L.attn_fwd_noalloc.argtypes = sig
         L.attn_fwd_noalloc.restype = i
         L.attn_last_device_error.argtypes = [vp]
@@ -123,6 +125,18 @@ def attn_fwd_window(q, k, v, o, lse, B: int, H: int, N: int, d: int, scale: floa
                                int(window_right), _ptr(cu_seqlens), _stream(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_window")
+    return st
+
+
+def attn_fwd_kvsplit(q, k, v, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, scale: float,
+                     causal: bool, num_splits: int = 0, stream=None) -> int:
+    """The C call ``attn_fwd_kvsplit``: Nq queries against Nk keys, the keys cut
+    into num_splits ranges (0: automatic) merged afterwards."""
+    st = lib().attn_fwd_kvsplit(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H),
+                                int(Nq), int(Nk), int(d), float(scale), int(bool(causal)),
+                                int(num_splits), _stream(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_kvsplit")
     return st
 
 

@@ -44,6 +44,12 @@ struct StreamWorkspace {
 std::mutex g_mu;
 std::map<int, DeviceState> g_dev;
 std::map<std::pair<int, attn_stream_t>, StreamWorkspace> g_ws;
+
+struct PartialWorkspace {
+  float* buf = nullptr;  // split-KV partial O then LSE
+  size_t capacity = 0;   // floats
+};
+std::map<std::pair<int, attn_stream_t>, PartialWorkspace> g_part;
 EncodeTiledFn g_encode = nullptr;
 
 int cuda_fail(cudaError_t e) {
@@ -68,19 +74,27 @@ int get_encode(EncodeTiledFn* out) {
 // Dynamic shared memory limits of every attention kernel instantiation.
 cudaError_t set_smem_attributes() {
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(attn::attn_fwd_kernel<64, false>,
+  if ((e = cudaFuncSetAttribute(attn::attn_fwd_kernel<64, attn::kModePlain>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 FwdCfg<64>::kSmemBytes)) != cudaSuccess)
     return e;
-  if ((e = cudaFuncSetAttribute(attn::attn_fwd_kernel<128, false>,
+  if ((e = cudaFuncSetAttribute(attn::attn_fwd_kernel<128, attn::kModePlain>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 FwdCfg<128>::kSmemBytes)) != cudaSuccess)
     return e;
-  if ((e = cudaFuncSetAttribute(attn::attn_fwd_kernel<64, true>,
+  if ((e = cudaFuncSetAttribute(attn::attn_fwd_kernel<64, attn::kModeWindow>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 FwdCfg<64>::kSmemBytes)) != cudaSuccess)
     return e;
-  return cudaFuncSetAttribute(attn::attn_fwd_kernel<128, true>,
+  if ((e = cudaFuncSetAttribute(attn::attn_fwd_kernel<64, attn::kModeSplit>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                FwdCfg<64>::kSmemBytes)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(attn::attn_fwd_kernel<128, attn::kModeSplit>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                FwdCfg<128>::kSmemBytes)) != cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(attn::attn_fwd_kernel<128, attn::kModeWindow>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               FwdCfg<128>::kSmemBytes);
 }
@@ -127,6 +141,24 @@ int stream_workspace(int dev, attn_stream_t stream, int64_t entries, int** out) 
   return ATTN_OK;
 }
 
+int partial_workspace(int dev, attn_stream_t stream, size_t floats, float** out) {
+  PartialWorkspace& ws = g_part[std::make_pair(dev, stream)];
+  if (ws.capacity < floats || !ws.buf) {
+    cudaError_t e;
+    if (ws.buf) {
+      if ((e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream))) != cudaSuccess)
+        return cuda_fail(e);
+      cudaFree(ws.buf);
+      ws.buf = nullptr;
+      ws.capacity = 0;
+    }
+    if ((e = cudaMalloc(&ws.buf, floats * sizeof(float))) != cudaSuccess) return cuda_fail(e);
+    ws.capacity = floats;
+  }
+  *out = ws.buf;
+  return ATTN_OK;
+}
+
 // 3-D view [tokens, H, d] of a bf16 tensor; box = 128 tokens x 1 head x 64
 // elements (128 bytes, the 128-byte swizzle span).
 int make_map(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int64_t tokens, int H, int d) {
@@ -147,9 +179,9 @@ template <int D>
 int launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                 const FwdParams& p, int grid, cudaStream_t s) {
   if (p.wl >= 0 || p.wr >= 0)
-    attn::attn_fwd_kernel<D, true><<<grid, attn::kThreads, FwdCfg<D>::kSmemBytes, s>>>(mq, mk, mv, p);
+    attn::attn_fwd_kernel<D, attn::kModeWindow><<<grid, attn::kThreads, FwdCfg<D>::kSmemBytes, s>>>(mq, mk, mv, p);
   else
-    attn::attn_fwd_kernel<D, false><<<grid, attn::kThreads, FwdCfg<D>::kSmemBytes, s>>>(mq, mk, mv, p);
+    attn::attn_fwd_kernel<D, attn::kModePlain><<<grid, attn::kThreads, FwdCfg<D>::kSmemBytes, s>>>(mq, mk, mv, p);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
@@ -419,4 +451,112 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
     grid = (int)units;
   }
   return d == 64 ? launch_attn<64>(mq, mk, mv, p, grid, s) : launch_attn<128>(mq, mk, mv, p, grid, s);
+}
+
+// ---------------------------------------------------------------------------
+// attn_fwd_kvsplit: queries and keys of different lengths (bottom-right
+// causal alignment), the visible KV tiles of every query block cut into
+// ranges processed by separate units, then merged by the combine kernel.
+extern "C" int attn_fwd_kvsplit(const void* q, const void* k, const void* v, void* o, float* lse,
+                                int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                                int num_splits, attn_stream_t stream) {
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || num_splits < 0 || num_splits > 256)
+    return ATTN_ERR_SHAPE;
+  if (d != 64 && d != 128) return ATTN_ERR_HEADDIM;
+  if (!std::isfinite(scale)) return ATTN_ERR_SCALE;
+  if (B == 0 || H == 0 || Nq == 0) return ATTN_OK;
+  if (Nk == 0 || (causal && Nq > Nk)) return ATTN_ERR_SHAPE;
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return ATTN_ERR_ALIGN;
+  const int64_t q_tokens = (int64_t)B * Nq, k_tokens = (int64_t)B * Nk;
+  if (q_tokens > INT32_MAX - 2 * attn::kBN || k_tokens > INT32_MAX - 2 * attn::kBN ||
+      (int64_t)H * d > (1 << 20) || H > 65535)
+    return ATTN_ERR_SHAPE;
+  const int64_t nqb = (Nq + attn::kUnitRows - 1) / attn::kUnitRows;
+  const int64_t base_units = (int64_t)B * nqb * H;
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  DeviceState* ds = nullptr;
+  int st = device_state(dev, &ds);
+  if (st != ATTN_OK) return st;
+  EncodeTiledFn enc = nullptr;
+  if ((st = get_encode(&enc)) != ATTN_OK) return st;
+
+  int S = num_splits;
+  if (S == 0) {
+    // The number of ranges with the shortest estimated makespan: units of
+    // equal cost run in ceil(units / SMs) rounds of ceil(tiles / S) KV tiles
+    // each; every extra range adds about a quarter tile of partial-result
+    // traffic and merge work.  At most one range per KV tile, at most 64.
+    const int64_t tiles = (Nk + attn::kBN - 1) / attn::kBN;
+    double best = 0.0;
+    for (int64_t c = 1; c <= std::min<int64_t>(tiles, 64); ++c) {
+      const int64_t rounds = (base_units * c + ds->sms - 1) / ds->sms;
+      const double t = (double)rounds * (double)((tiles + c - 1) / c) + 0.25 * (double)(c - 1);
+      if (c == 1 || t < best) {
+        best = t;
+        S = (int)c;
+      }
+    }
+  }
+  const int64_t units = base_units * S;
+  const int64_t combine_blocks = (q_tokens * H * 32 + 255) / 256;
+  if (units > INT32_MAX || combine_blocks > INT32_MAX) return ATTN_ERR_SHAPE;
+
+  CUtensorMap mq, mk, mv;
+  if ((st = make_map(enc, &mq, q, q_tokens, H, d)) != ATTN_OK) return st;
+  if ((st = make_map(enc, &mk, k, k_tokens, H, d)) != ATTN_OK) return st;
+  if ((st = make_map(enc, &mv, v, k_tokens, H, d)) != ATTN_OK) return st;
+
+  int* ws = nullptr;
+  if ((st = stream_workspace(dev, stream, 0, &ws)) != ATTN_OK) return st;
+  float* part = nullptr;
+  const size_t o_floats = (size_t)S * q_tokens * H * d;
+  const size_t lse_floats = (size_t)S * B * H * Nq;
+  if ((st = partial_workspace(dev, stream, o_floats + lse_floats, &part)) != ATTN_OK) return st;
+
+  FwdParams p{};
+  p.o = reinterpret_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.err = ds->err;
+  p.sched = ws + 1;
+  p.B = B;
+  p.H = H;
+  p.N = Nq;
+  p.Nk = Nk;
+  p.q_off = causal ? Nk - Nq : 0;
+  p.num_splits = S;
+  p.o_part = part;
+  p.lse_part = part + o_floats;
+  p.causal = causal ? 1 : 0;
+  p.wl = -1;
+  p.wr = -1;
+  p.scale = scale;
+  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p.timeout_ns = 2000000000ull;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int grid = (int)std::min<int64_t>(units, ds->sms);
+  if (d == 64)
+    attn::attn_fwd_kernel<64, attn::kModeSplit><<<grid, attn::kThreads, FwdCfg<64>::kSmemBytes, s>>>(
+        mq, mk, mv, p);
+  else
+    attn::attn_fwd_kernel<128, attn::kModeSplit><<<grid, attn::kThreads, FwdCfg<128>::kSmemBytes, s>>>(
+        mq, mk, mv, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+  const int blocks = (int)combine_blocks;
+  if (d == 64)
+    attn::attn_combine_kernel<64><<<blocks, 256, 0, s>>>(p.o_part, p.lse_part,
+                                                         reinterpret_cast<__nv_bfloat16*>(o), lse, B, H,
+                                                         Nq, S);
+  else
+    attn::attn_combine_kernel<128><<<blocks, 256, 0, s>>>(p.o_part, p.lse_part,
+                                                          reinterpret_cast<__nv_bfloat16*>(o), lse, B, H,
+                                                          Nq, S);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+  return ATTN_OK;
 }

@@ -92,6 +92,13 @@ struct FwdParams {
   int B, H, N;
   int causal;
   int wl, wr;              // sliding window: keys i - wl <= j <= i + wr (-1: unbounded)
+  // split-KV mode (dense only): queries [B, Nq = N, H, D], keys [B, Nk, H, D];
+  // query row r sits at key position q_off + r (q_off = Nk - Nq when causal);
+  // the visible KV tiles of a q-block are cut into num_splits ranges whose
+  // partial results (O / l in fp32, LSE) go to o_part / lse_part.
+  int Nk, q_off, num_splits;
+  float* o_part;           // [num_splits][B * Nq][H][D]
+  float* lse_part;         // [num_splits][B][H][Nq]
   float scale;             // softmax scale on the logits
   float scale_log2;        // scale * log2(e)
   unsigned long long timeout_ns;
@@ -131,13 +138,21 @@ constexpr int kMaxBars = kBarKV + 2 * 8;
 constexpr int kUnitSlots = 2;            // unit indices published by the producer
 constexpr int kUnitConsumers = 1 + kSoftmaxWarps;  // the MMA thread and every softmax warp
 
-// One work unit: rows [256 qb, 256 qb + 256) of head h of one sequence.
+// Kernel modes (separate instantiations): plain attention, sliding window,
+// split-KV with separate query and key lengths.
+enum : int { kModePlain = 0, kModeWindow = 1, kModeSplit = 2 };
+
+// One work unit: rows [256 qb, 256 qb + 256) of head h of one sequence
+// (split-KV: and one range of its KV tiles).
 struct Unit {
   int seq, h, qb;
-  int tok0;  // first token of the sequence in the packed tensors
-  int L;     // sequence length
-  int kv0;   // first KV tile visited
-  int nkv;   // KV tiles visited
+  int tok0;   // first query token of the sequence in the packed tensors
+  int L;      // query length of the sequence
+  int k_tok0; // first key token (split-KV; else tok0)
+  int Lk;     // key length (split-KV; else L)
+  int kv0;    // first KV tile visited
+  int nkv;    // KV tiles visited
+  int split;  // KV range index (split-KV; else 0)
 };
 
 // KV tiles [kv0, kv0 + nkv) that hold a key visible to some row of q-block qb
@@ -158,30 +173,54 @@ __host__ __device__ __forceinline__ void unit_kv_range(int L, int qb, int causal
 __device__ __forceinline__ int num_units(const FwdParams& p) {
   if (p.cu_seqlens) return *p.num_entries * p.H;
   const int nqb = (p.N + kUnitRows - 1) / kUnitRows;
-  return p.B * p.H * nqb;
+  return p.B * p.H * nqb * (p.num_splits > 1 ? p.num_splits : 1);
 }
 
 // Unit u of the longest-first order.  Dense: q-blocks in decreasing cost
 // (causal cost grows with the q-block index), then batch, then head.  Varlen:
-// the scheduler kernel's sorted (seq, q-block) list, then head.
+// the scheduler kernel's sorted (seq, q-block) list, then head.  Split-KV:
+// q-blocks in decreasing cost, then KV range, then batch, then head.
+template <int kMode>
 __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
   Unit un;
   const int e = u / p.H;
   un.h = u - e * p.H;
-  if (p.cu_seqlens) {
+  un.split = 0;
+  if (kMode != kModeSplit && p.cu_seqlens) {
     un.seq = p.work[2 * e];
     un.qb = p.work[2 * e + 1];
     un.tok0 = p.cu_seqlens[un.seq];
     un.L = p.cu_seqlens[un.seq + 1] - un.tok0;
   } else {
     const int nqb = (p.N + kUnitRows - 1) / kUnitRows;
-    const int rank = e / p.B;
-    un.seq = e - rank * p.B;
+    int rank;
+    if (kMode == kModeSplit) {
+      rank = e / (p.B * p.num_splits);
+      const int rem = e - rank * p.B * p.num_splits;
+      un.split = rem / p.B;
+      un.seq = rem - un.split * p.B;
+    } else {
+      rank = e / p.B;
+      un.seq = e - rank * p.B;
+    }
     un.qb = nqb - 1 - rank;
     un.tok0 = un.seq * p.N;
     un.L = p.N;
   }
-  unit_kv_range(un.L, un.qb, p.causal, p.wl, p.wr, un.kv0, un.nkv);
+  if (kMode == kModeSplit) {
+    // visible KV tiles of the q-block, cut into num_splits near-equal ranges
+    un.k_tok0 = un.seq * p.Nk;
+    un.Lk = p.Nk;
+    const int r_hi = min(un.qb * kUnitRows + kUnitRows, un.L) - 1;
+    const int k_hi = p.causal ? min(p.Nk - 1, p.q_off + r_hi) : p.Nk - 1;
+    const int n = k_hi / kBN + 1;
+    un.kv0 = (int)((long long)n * un.split / p.num_splits);
+    un.nkv = (int)((long long)n * (un.split + 1) / p.num_splits) - un.kv0;
+  } else {
+    un.k_tok0 = un.tok0;
+    un.Lk = un.L;
+    unit_kv_range(un.L, un.qb, p.causal, p.wl, p.wr, un.kv0, un.nkv);
+  }
   return un;
 }
 
@@ -194,7 +233,7 @@ __device__ __forceinline__ int q_tile_start(const Unit& un, int g) {
 // First key actually loaded for KV tile j (same pull-back at the sequence end;
 // keys before 128*j were already visited and are masked out).
 __device__ __forceinline__ int kv_tile_start(const Unit& un, int j) {
-  return min(j * kBN, un.L - kBN);
+  return min(j * kBN, un.Lk - kBN);
 }
 
 struct SharedState {
@@ -232,7 +271,7 @@ __device__ __forceinline__ uint32_t bar_addr(SharedState& ss, int bar) {
 }
 
 // ------------------------------------------------------------ producer --
-template <int D>
+template <int D, int kMode>
 __device__ __forceinline__ void producer_loop(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                               const CUtensorMap* tm_v, const FwdParams& p,
                                               SharedState& ss, uint8_t* sQ, uint8_t* sRing,
@@ -256,7 +295,11 @@ __device__ __forceinline__ void producer_loop(const CUtensorMap* tm_q, const CUt
     if (u < 0) return;
     // next unit index, fetched while this unit's copies are issued
     const int next_u = (int)gridDim.x + atomicAdd(p.sched, 1);
-    const Unit un = decode_unit(p, u);
+    const Unit un = decode_unit<kMode>(p, u);
+    if (kMode == kModeSplit && un.nkv <= 0) {  // empty KV range: nothing to copy
+      u = next_u;
+      continue;
+    }
     if (units_done > 0 && !wait_bar(ss, kBarQEmpty, (units_done - 1) & 1, p, 1)) return;
     mbar_arrive_expect_tx(bar_addr(ss, kBarQFull), kQTiles * C::kTileBytes);
     for (int g = 0; g < kQTiles; ++g) {
@@ -266,7 +309,7 @@ __device__ __forceinline__ void producer_loop(const CUtensorMap* tm_q, const CUt
                     bar_addr(ss, kBarQFull), c * 64, un.h, r0);
     }
     for (int j = 0; j < un.nkv; ++j) {
-      const int k0 = un.tok0 + kv_tile_start(un, un.kv0 + j);
+      const int k0 = un.k_tok0 + kv_tile_start(un, un.kv0 + j);
       for (int kind = 0; kind < 2; ++kind) {
         const int slot = ring % C::kStages;
         const uint32_t n = ring / C::kStages;
@@ -342,7 +385,7 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
            kk > 0 ? 1u : acc0);
 }
 
-template <int D>
+template <int D, int kMode>
 __device__ __forceinline__ void mma_loop(const FwdParams& p, SharedState& ss, uint8_t* sQ,
                                          uint8_t* sRing, uint32_t tmem, int n_units) {
   using C = FwdCfg<D>;
@@ -360,7 +403,10 @@ __device__ __forceinline__ void mma_loop(const FwdParams& p, SharedState& ss, ui
   for (;;) {
     int u;
     if (!next_unit(ss, p, uslot, false, u) || u < 0) return;
-    const Unit un = decode_unit(p, u);
+    const Unit un = decode_unit<kMode>(p, u);
+    // an empty KV range (split-KV with more ranges than tiles) has no copy,
+    // no MMA and no barrier traffic: the softmax warps write its empty result
+    if (kMode == kModeSplit && un.nkv <= 0) continue;
     if (!wait_bar(ss, kBarQFull, units_done & 1, p, 11)) return;
     tc_fence_after();
     uint32_t posK = ring, posV = ring + 1;
@@ -450,12 +496,30 @@ __device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
       : "f"(b0), "f"(b1));
 }
 
-// Named barrier of the two warps that share a 32-row quadrant of a group.
+// Barriers of the two warps that share a 32-row quadrant of a group: a named
+// hardware barrier of 64 threads.  Both warps pass the same sequence of these
+// barriers, also after a wait has given up: a warp whose wait failed goes on
+// through the rest of its unit with the values it has (they are not a
+// result; the kernel is stopping).  After every unit hand-off the pair passes
+// one checking barrier, which leaves both warps with the OR of their failure
+// flags; then both leave together if either failed, so neither is ever left
+// waiting for a partner that has gone.
 __device__ __forceinline__ void pair_sync(int g, int quadrant) {
-  asm volatile("bar.sync %0, %1;" ::"r"(1 + g * 4 + quadrant), "r"(64) : "memory");
+  asm volatile("bar.sync %0, 64;" ::"r"(1 + g * 4 + quadrant) : "memory");
 }
 
-template <int D, bool kWindow>
+__device__ __forceinline__ bool pair_sync_check(int g, int quadrant, bool fail) {
+  uint32_t any;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
+      " bar.red.or.pred q, %2, 64, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(any)
+      : "r"(fail ? 1u : 0u), "r"(1 + g * 4 + quadrant)
+      : "memory");
+  return any != 0;
+}
+
+template <int D, int kMode>
 __device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss, uint32_t tmem,
                                              int g, int n_units) {
   using C = FwdCfg<D>;
@@ -471,15 +535,23 @@ __device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss
   const uint32_t colO = C::col_o(g) + half * kOCols;
   const float c2 = p.scale_log2;
   uint32_t scount = 0;
-  int units_done = 0;
+  int units_done = 0;  // units with an O result (every unit but empty split-KV ranges)
   int tokens_total = 0;
   if (p.cu_seqlens) tokens_total = p.cu_seqlens[p.B];
 
   uint32_t uslot = 0;
+  // A wait of this warp gave up: the pair leaves at the next checking barrier.
+  // The next unit's index is taken in the epilogue of the current one, before
+  // the checking barrier that ends it.
+  int u = -1;
+  bool fail = !next_unit(ss, p, uslot, true, u);
+  if (pair_sync_check(g, quadrant, fail)) return;
   for (;;) {
-    int u;
-    if (!next_unit(ss, p, uslot, true, u) || u < 0) return;
-    const Unit un = decode_unit(p, u);
+    if (u < 0) return;
+    const Unit un = decode_unit<kMode>(p, u);
+    constexpr bool kWindow = kMode == kModeWindow;
+    const int Lk = kMode == kModeSplit ? un.Lk : un.L;
+    const int q_off = kMode == kModeSplit ? p.q_off : 0;  // key position of query row 0
     const int a0 = q_tile_start(un, g);
     const int row = a0 + trow;                       // sequence-relative row of this thread
     const int nominal0 = un.qb * kUnitRows + g * kBM;
@@ -487,9 +559,11 @@ __device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss
     float l = 0.f;     // sum of the fp32 probabilities (this half): the LSE
     float l_fix = 0.f; // rounding change of each tile's largest probability (this half)
     for (int j = 0; j < un.nkv; ++j) {
-      if (!__all_sync(0xffffffffu, wait_bar(ss, kBarSFull + g, scount & 1, p, 20 + g))) return;
+      fail |= !__all_sync(0xffffffffu, wait_bar(ss, kBarSFull + g, scount & 1, p, 20 + g));
       ++scount;
       tc_fence_after();
+      // (after a failed wait the loads read stale columns; the unit goes on
+      // with them, its results are dropped and the warp leaves after it)
       float s[kHalfCols];
       {
         uint32_t r0[32], r1[32];
@@ -512,14 +586,14 @@ __device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss
       const int b0 = kv_tile_start(un, jt);
       // keys every row of the group may see: [max_klo, min_khi]
       const int max_klo = (kWindow && p.wl >= 0) ? max(0, a0 + kBM - 1 - p.wl) : 0;
-      int min_khi = p.causal ? a0 : un.L - 1;
+      int min_khi = p.causal ? q_off + a0 : Lk - 1;
       if (kWindow && p.wr >= 0) min_khi = min(min_khi, a0 + p.wr);
       const bool need_mask = jt * kBN > b0 || b0 < max_klo || b0 + kBN - 1 > min_khi;
       if (need_mask) {
         // this row's keys [klo, khi]; keys below jt*128 were visited by the
         // previous tile (pulled-back last tile)
         int klo = (kWindow && p.wl >= 0) ? max(0, row - p.wl) : 0;
-        int khi = p.causal ? row : un.L - 1;
+        int khi = p.causal ? q_off + row : Lk - 1;
         if (kWindow && p.wr >= 0) khi = min(khi, row + p.wr);
         klo = max(klo, jt * kBN);
         const int lo = klo - b0 - half * kHalfCols;
@@ -541,7 +615,8 @@ __device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss
       }
       const float mine = fmaxf(max3(mx0, mx1, mx2), mx3);
       ss.row_max[j & 1][g][half][trow] = mine;
-      pair_sync(g, quadrant);  // also orders both halves' S loads before any P store
+      // (also orders both halves' S loads before any P store)
+      pair_sync(g, quadrant);
       const float mx = fmaxf(mine, ss.row_max[j & 1][g][half ^ 1][trow]);
       const float m_new = fmaxf(m_used, mx);
       // O correction decision: only when the row max grew by more than 2^8
@@ -609,10 +684,50 @@ __device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss
     pair_sync(g, quadrant);
     l += ss.row_sum[g][half ^ 1][0][trow];
     const float l_r = l + l_fix + ss.row_sum[g][half ^ 1][1][trow];
-    pair_sync(g, quadrant);  // both read before the next unit writes again
-    if (!__all_sync(0xffffffffu, wait_bar(ss, kBarOFull + g, units_done & 1, p, 22 + g))) return;
-    tc_fence_after();
+    u = -1;
+    if (!fail) fail = !next_unit(ss, p, uslot, true, u);
+    // (also: both halves have read row_sum before the next unit writes it)
+    if (pair_sync_check(g, quadrant, fail)) return;
+    // (an empty KV range of split-KV has no MMA work and no O-done signal;
+    // after a failed wait the kernel is stopping and what is stored below is
+    // not a result)
+    const bool has_o = kMode != kModeSplit || un.nkv > 0;
+    if (has_o) {
+      fail |= !__all_sync(0xffffffffu, wait_bar(ss, kBarOFull + g, units_done & 1, p, 22 + g));
+      tc_fence_after();
+    }
     const bool store = row >= nominal0 && row < un.L && row >= 0;
+    if (kMode == kModeSplit) {
+      // partial result of this KV range: O / l_r (fp32) and its LSE; the
+      // combine kernel merges the ranges
+      const float inv = l_r > 0.f ? 1.0f / l_r : 0.f;
+      float* prow = p.o_part + (((size_t)un.split * p.B * p.N + (store ? un.tok0 + row : 0)) * p.H + un.h) * D +
+                    half * kOCols;
+#pragma unroll
+      for (int cc = 0; cc < kOCols; cc += 32) {
+        uint32_t r[32];
+        if (has_o) {
+          tmem_ld_x32(lane_addr + colO + cc, r);
+          tmem_ld_wait_x32(r);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = 0u;
+        }
+        if (store) {
+          float4* dst = reinterpret_cast<float4*>(prow + cc);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
+                                 __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
+        }
+      }
+      if (store && half == 0)
+        p.lse_part[(((size_t)un.split * p.B + un.seq) * p.H + un.h) * p.N + row] =
+            l > 0.f ? m_used * p.scale + __log2f(l) * 0.69314718055994531f : -INFINITY;
+      tc_fence_before();
+      if (has_o) ++units_done;
+      continue;
+    }
     // O's divisor carries the rounding of each tile's dominant probability;
     // the LSE uses the fp32 sum.
     const float inv_l = l_r > 0.f ? 1.0f / l_r : 0.f;
@@ -660,9 +775,10 @@ __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-// kWindow: the sliding-window bounds p.wl / p.wr are applied (a separate
-// instantiation, so plain attention carries none of that arithmetic).
-template <int D, bool kWindow>
+// kMode: kModeWindow applies the sliding-window bounds p.wl / p.wr;
+// kModeSplit runs split-KV units and writes partial results.  Separate
+// instantiations, so plain attention carries none of that arithmetic.
+template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -714,10 +830,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   if (warp >= kSoftmaxWarps) {
     setmaxnreg_dec<kControlRegs>();
     if (warp == kProducerWarp) {
-      if (lane == 0) producer_loop<D>(&tm_q, &tm_k, &tm_v, p, ss, sQ, sRing, n_units);
+      if (lane == 0) producer_loop<D, kMode>(&tm_q, &tm_k, &tm_v, p, ss, sQ, sRing, n_units);
     } else if (warp == kMmaWarp) {
       if (lane == 0) {
-        mma_loop<D>(p, ss, sQ, sRing, tmem, n_units);
+        mma_loop<D, kMode>(p, ss, sQ, sRing, tmem, n_units);
         // every MMA issued by this thread has finished before TMEM is freed
         mma_commit(bar_addr(ss, kBarDrain));
         mbar_wait(bar_addr(ss, kBarDrain), 0, 100000000ull);
@@ -726,7 +842,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __syncwarp();
   } else {
     setmaxnreg_inc<kSoftmaxRegs>();
-    softmax_loop<D, kWindow>(p, ss, tmem, warp / kGroupWarps, n_units);
+    softmax_loop<D, kMode>(p, ss, tmem, warp / kGroupWarps, n_units);
     __syncwarp();
   }
 
@@ -826,6 +942,50 @@ build_worklist_kernel(const int* cu_seqlens, int nseq, int max_len, int causal, 
     }
   }
   if (threadIdx.x == 0) *num_entries = total;
+}
+
+// ------------------------------------------------------------- combine --
+// Merges the split-KV partial results of every query row with the pages'
+// two-segment merge identity applied across the KV ranges
+// ("flash-attention-evolution" (letsgetai), FlashAttention "核心机制"): with
+// LSE_s = m_s + ln l_s and O_s = f_s / l_s of range s,
+//   m = max_s LSE_s,  w_s = e^{LSE_s - m},  LSE = m + ln sum_s w_s,
+//   O = sum_s w_s O_s / sum_s w_s.
+// One warp per (token, head) row; lane c holds columns c, c+32, ...
+template <int D>
+__global__ void __launch_bounds__(256)
+attn_combine_kernel(const float* o_part, const float* lse_part, __nv_bfloat16* o, float* lse,
+                    int B, int H, int Nq, int S) {
+  constexpr int kPer = D / 32;
+  const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / 32;
+  const int lane = threadIdx.x % 32;
+  const long long rows = (long long)B * Nq * H;
+  if (warp >= rows) return;
+  const long long tok = warp / H;
+  const int h = (int)(warp - tok * H);
+  const int b = (int)(tok / Nq);
+  const int r = (int)(tok - (long long)b * Nq);
+  float m = -INFINITY;
+  for (int s = 0; s < S; ++s) m = fmaxf(m, lse_part[(((size_t)s * B + b) * H + h) * Nq + r]);
+  float acc[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
+  float wsum = 0.f;
+  if (m != -INFINITY) {
+    for (int s = 0; s < S; ++s) {
+      const float ls = lse_part[(((size_t)s * B + b) * H + h) * Nq + r];
+      const float w = ls == -INFINITY ? 0.f : __expf(ls - m);
+      wsum += w;
+      const float* src = o_part + (((size_t)s * B * Nq + tok) * H + h) * D;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) acc[i] = fmaf(w, src[lane + 32 * i], acc[i]);
+    }
+  }
+  const float inv = wsum > 0.f ? 1.0f / wsum : 0.f;
+  __nv_bfloat16* dst = o + (tok * H + h) * D;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) dst[lane + 32 * i] = __float2bfloat16_rn(acc[i] * inv);
+  if (lane == 0) lse[((size_t)b * H + h) * Nq + r] = wsum > 0.f ? m + __logf(wsum) : -INFINITY;
 }
 
 }  // namespace attn
