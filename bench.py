@@ -5,6 +5,7 @@ long-context causal workload B=2, H=16, N=8192, d=128 (bf16, fp32 accumulate),
 with inputs resident in device memory.  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+  python bench.py --workload decode   # split-KV decode line (attn_fwd_kvsplit)
 
 Metric: attention forward TFLOP/s, FLOPs = 4*B*H*N^2*d halved for causal,
 whole job (all ranks) / the slowest rank's time.  N > 1 runs one independent
@@ -325,10 +326,155 @@ def run_cuda(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+DECODE = {"B": 8, "H": 16, "Nq": 1, "Nk": 32768, "d": 128}
+# DRAM bytes (read + write) of one decode call (split kernel + combine), from
+# the ncu capture summarised under profiles/ (None once either kernel changes).
+DECODE_TRAFFIC_BYTES = 2_217_673_728 + 875_008
+DECODE_METRIC = "split-KV decode: algorithmic HBM GB/s on 1 GB300 (bf16 K/V cache)"
+
+
+def decode_config(S):
+    c = DECODE
+    return {"workload": f"decode (split-KV): B={c['B']} H={c['H']} Nq={c['Nq']} Nk={c['Nk']} "
+                        f"d={c['d']} causal (bottom-right)",
+            "B": c["B"], "H": c["H"], "Nq": c["Nq"], "Nk": c["Nk"], "d": c["d"], "causal": True,
+            "num_splits": S, "scale": "1/sqrt(d)",
+            "inputs": "Q,K,V iid N(0,1) bf16, seeded (SplitMix64 + Box-Muller)",
+            "l2": "K,V = 2.1 GB > 129 MB L2 (no flush between steps)"}
+
+
+def run_decode(args, world, rank, local):
+    """One step = one attn_fwd_kvsplit call (split kernel + combine kernel) of a
+    batch of single-token queries against a resident 32768-token K/V cache.
+    Metric: algorithmic bytes (K and V read once, Q read, O and LSE written)
+    per second; the path is bound by HBM bandwidth."""
+    import torch
+    import __graft_entry__
+    import io_aware_exact_06_gb300 as fa
+    __graft_entry__.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    c = DECODE
+    B, H, Nq, Nk, d = c["B"], c["H"], c["Nq"], c["Nk"], c["d"]
+    seed = 0xA77E0100
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    q_h = bf(inputs.normal_bf16(4 * seed + 1, B * Nq * H * d)).reshape(B, Nq, H, d).pin_memory()
+    k = bf(inputs.normal_bf16(4 * seed + 2, B * Nk * H * d)).reshape(B, Nk, H, d).to(dev)
+    v = bf(inputs.normal_bf16(4 * seed + 3, B * Nk * H * d)).reshape(B, Nk, H, d).to(dev)
+    q = q_h.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+    o_h = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream(dev)
+    scale = d ** -0.5
+    bytes_step = 2 * B * Nk * H * d * 2 + 2 * B * Nq * H * d * 2 + B * H * Nq * 4
+
+    def step():
+        fa.attn_fwd_kvsplit(q, k, v, o, lse, B, H, Nq, Nk, d, scale, True, 0, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if fa.attn_last_device_error(stream) != 0:
+        raise RuntimeError("device error during warm-up")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    if fa.attn_last_device_error(stream) != 0:
+        raise RuntimeError("device error in the timed region")
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    call_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    def e2e_step():  # a new query batch from the host, the result back
+        q.copy_(q_h, non_blocking=True)
+        step()
+        o_h.copy_(o, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    n_e2e = max(3, min(args.steps, 10))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    if rank != 0:
+        return
+    _, _, hbm, src = peaks()
+    achieved = bytes_step / (call_ms * 1e-3) / 1e9
+    line = {
+        "metric": DECODE_METRIC, "value": world * bytes_step * args.steps / (total_ms * 1e-3) / 1e9,
+        "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": decode_config("auto"),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "peak_source": f"{src} hbm_gbs",
+                     "kernel": "attn_fwd_kernel<128, split> + attn_combine_kernel<128> (one call)",
+                     "traffic": DECODE_TRAFFIC_BYTES},
+        "clocks": clk.summary(),
+        "e2e": {"value": world * bytes_step * n_e2e / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": q.numel() * 2,
+                "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4},
+        "gpu_launches": 2 * args.steps,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = decode_cpu_baseline(q_h, k, v, scale)
+    print(json.dumps(line), flush=True)
+
+
+def decode_cpu_baseline(q_h, k, v, scale):
+    """The oracle on the decode rows of sequence 0 (every head): the query is
+    the last key position of a self-attention problem whose other query rows
+    are zero (they change no other row)."""
+    import oracle
+    B, Nq, H, d = q_h.shape
+    Nk = k.shape[1]
+    k0 = k[0].cpu().view(torch_int16()).numpy().view(np.uint16).reshape(Nk, H, d)
+    v0 = v[0].cpu().view(torch_int16()).numpy().view(np.uint16).reshape(Nk, H, d)
+    qf = np.zeros((Nk, H, d), dtype=np.uint16)
+    qf[Nk - Nq:] = q_h[0].view(torch_int16()).numpy().view(np.uint16)
+    cu = np.array([0, Nk], dtype=np.int64)
+    rows = np.array([(0, h, Nk - Nq + r) for h in range(H) for r in range(Nq)], dtype=np.int64)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        _, _, used = oracle.attn_rows(qf, k0, v0, cu, rows, scale, True)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt > 5.0:
+            break
+    per_row_bytes = 2 * Nk * d * 2 + 2 * d * 2 + 4
+    return {"value": reps * len(rows) * per_row_bytes / dt / 1e9, "unit": "GB/s", "cores": int(used),
+            "kind": "oracle",
+            "sample": f"{len(rows)} decode rows (sequence 0, every head) x {reps} repetitions, "
+                      f"{dt:.1f} s; bytes = K and V of the row's head once + q, o, lse"}
+
+
+def torch_int16():
+    import torch
+    return torch.int16
+
+
 # DRAM bytes (read + write) of one attn_fwd_kernel<128> launch of this
 # workload, from the ncu capture summarised under profiles/ (None until taken
 # for the current kernel).
-TRAFFIC_BYTES = 608_546_048  # 549.29 MB read + 59.25 MB written (profiles/attn_fwd_kernel_long_causal.md)
+TRAFFIC_BYTES = 607_184_640  # 549.02 MB read + 58.17 MB written (profiles/attn_fwd_kernel_long_causal.md)
 
 
 def main():
@@ -338,6 +484,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD, choices=[WORKLOAD, "decode"])
     ap.add_argument("--ref-step-s", type=float, default=0.0,
                     help="reference arm: oracle seconds per step (default: fit the run in ~2.5 min)")
     args = ap.parse_args()
@@ -345,6 +492,8 @@ def main():
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.workload == "decode":
+        run_decode(args, world, rank, local)
     else:
         run_cuda(args, world, rank, local)
     if world > 1:
