@@ -1,4 +1,4 @@
-"""fp64 CPU oracle for exact softmax attention (forward).
+"""fp64 CPU oracle for exact softmax attention (forward and gradients).
 
 TEST INFRASTRUCTURE ONLY.  Callers allowed: the tests, the package smoke check
 and the benchmark's CPU-baseline leg.  The CUDA path never imports this package
@@ -60,6 +60,11 @@ class Oracle:
         L.oracle_attn_online.argtypes = [_c_u16p, _c_u16p, _c_u16p, _c_i64p, ctypes.c_int64,
                                          ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
                                          _c_i64p, ctypes.c_int64, ctypes.c_int64, _c_dp, _c_dp]
+        L.oracle_attn_bwd.restype = ctypes.c_int
+        L.oracle_attn_bwd.argtypes = [_c_u16p, _c_u16p, _c_u16p, _c_u16p, _c_i64p, ctypes.c_int64,
+                                      ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
+                                      _c_i64p, ctypes.c_int64, _c_dp, _c_dp, _c_dp, ctypes.c_int,
+                                      ctypes.POINTER(ctypes.c_int)]
         self.lib = L
         self.path = path
 
@@ -92,6 +97,36 @@ class Oracle:
         if st != 0:
             raise ValueError(f"oracle_attn_rows failed with status {st}")
         return o, lse, used.value
+
+    def attn_bwd(self, q, k, v, dout, cu_seqlens, pairs, scale: float, causal: bool,
+                 nthreads: int = 0):
+        """dQ, dK, dV (fp64) of the given (seq, head) pairs.
+
+        q, k, v, dout: uint16 bf16 bits, [tokens, H, d] (dout = dO, the
+        gradient of the loss with respect to O).  Returns (dq, dk, dv,
+        threads_used); each gradient is a list with one [L_s, d] array per
+        pair.
+        """
+        q, k, v, dout = _u16(q), _u16(k), _u16(v), _u16(dout)
+        tokens, H, d = q.shape
+        cu = np.ascontiguousarray(cu_seqlens, dtype=np.int64)
+        pairs = np.ascontiguousarray(pairs, dtype=np.int64).reshape(-1, 2)
+        lens = [int(cu[s + 1] - cu[s]) for s in pairs[:, 0]]
+        n = sum(lens)
+        dq = np.zeros((max(n, 1), d), dtype=np.float64)
+        dk = np.zeros_like(dq)
+        dv = np.zeros_like(dq)
+        used = ctypes.c_int(0)
+        st = self.lib.oracle_attn_bwd(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16),
+                                      _ptr(v, ctypes.c_uint16), _ptr(dout, ctypes.c_uint16),
+                                      _ptr(cu, ctypes.c_int64), len(cu) - 1, H, d, float(scale),
+                                      int(bool(causal)), _ptr(pairs, ctypes.c_int64), len(pairs),
+                                      _ptr(dq, ctypes.c_double), _ptr(dk, ctypes.c_double),
+                                      _ptr(dv, ctypes.c_double), int(nthreads), ctypes.byref(used))
+        if st != 0:
+            raise ValueError(f"oracle_attn_bwd failed with status {st}")
+        split = np.cumsum(lens)[:-1]
+        return np.split(dq[:n], split), np.split(dk[:n], split), np.split(dv[:n], split), used.value
 
     def attn_probs(self, q, k, cu_seqlens, seq: int, h: int, i: int, scale: float,
                    causal: bool):
@@ -166,6 +201,10 @@ def attn_rows(*a, **kw):
 
 def attn_probs(*a, **kw):
     return default().attn_probs(*a, **kw)
+
+
+def attn_bwd(*a, **kw):
+    return default().attn_bwd(*a, **kw)
 
 
 def softmax_merge(*a, **kw):

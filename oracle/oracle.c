@@ -1,5 +1,5 @@
 /*
- * fp64 CPU oracle for exact softmax attention, forward pass.
+ * fp64 CPU oracle for exact softmax attention: forward pass and its gradients.
  *
  * TEST INFRASTRUCTURE.  Only the tests, the package smoke check and the
  * benchmark's CPU-baseline leg may load this library.  It shares no code,
@@ -34,6 +34,24 @@
  * Inputs are bf16 bit patterns (uint16) in the packed layout
  * [tokens, H, d]; sequence s occupies tokens cu_seqlens[s] .. cu_seqlens[s+1]-1.
  * Every bf16 value widens exactly to fp64 here; nothing is rounded afterwards.
+ *
+ * Backward (oracle_attn_bwd).  The pages say only that the backward pass
+ * rebuilds S and P from Q, K, V (and the saved row statistics) instead of
+ * storing them ("flash-attention-evolution" (letsgetai), FlashAttention
+ * "核心机制", the recomputation paragraph; "FlashAttention 1-4 演进速查"
+ * (argus-lessons), FlashAttention-1 items).  What the backward computes is
+ * then the derivative of the definition above, given the gradient dO of a
+ * scalar loss with respect to O (and none with respect to the LSE): by the
+ * chain rule through O_i = sum_j P_ij v_j and the row softmax,
+ *
+ *   dV_j   = sum_i P_ij dO_i
+ *   dP_ij  = <dO_i, v_j>
+ *   D_i    = sum_j P_ij dP_ij
+ *   dS_ij  = P_ij (dP_ij - D_i)
+ *   dQ_i   = scale * sum_j dS_ij k_j
+ *   dK_j   = scale * sum_i dS_ij q_i
+ *
+ * over the same visible (i, j) pairs as the forward.
  *
  * Besides the definition, two more routines restate the pages' own incremental
  * formulations so the tests can pin one against the other:
@@ -434,5 +452,193 @@ int oracle_attn_online(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     }
     free(sblk);
     free(acc);
+    return st;
+}
+
+/* ------------------------------------------------------------- backward -- */
+
+typedef struct {
+    const uint16_t *q, *k, *v, *dout;
+    int64_t base, L;
+    int H, h, d;
+    double scale;
+    int causal;
+    int64_t begin, end; /* query rows of this worker */
+    double *dq;         /* [L][d], rows begin..end-1 written */
+    double *dk, *dv;    /* [L][d] private accumulators of this worker */
+    int status;
+} bwd_job;
+
+static void *bwd_worker(void *arg)
+{
+    bwd_job *jb = (bwd_job *)arg;
+    const int H = jb->H, h = jb->h, d = jb->d;
+    const int64_t L = jb->L, base = jb->base;
+    double *p = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+    double *dp = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+    double *qf = (double *)malloc(sizeof(double) * (size_t)d);
+    double *dorow = (double *)malloc(sizeof(double) * (size_t)d);
+    if (!p || !dp || !qf || !dorow) {
+        free(p);
+        free(dp);
+        free(qf);
+        free(dorow);
+        jb->status = ORACLE_ENOMEM;
+        return NULL;
+    }
+    for (int64_t i = jb->begin; i < jb->end; ++i) {
+        const int64_t nvis = jb->causal ? i + 1 : L;
+        const uint16_t *qsrc = jb->q + ((base + i) * H + h) * (int64_t)d;
+        const uint16_t *doi = jb->dout + ((base + i) * H + h) * (int64_t)d;
+        for (int c = 0; c < d; ++c) {
+            qf[c] = widen_bf16(qsrc[c]);
+            dorow[c] = widen_bf16(doi[c]);
+        }
+        /* the forward's row: S_ij, m_i, l_i, P_ij */
+        double m = -INFINITY;
+        for (int64_t j = 0; j < nvis; ++j) {
+            const uint16_t *kr = jb->k + ((base + j) * H + h) * (int64_t)d;
+            double acc = 0.0;
+            for (int c = 0; c < d; ++c)
+                acc += qf[c] * widen_bf16(kr[c]);
+            p[j] = jb->scale * acc;
+            if (p[j] > m)
+                m = p[j];
+        }
+        double l = 0.0;
+        for (int64_t j = 0; j < nvis; ++j)
+            l += exp(p[j] - m);
+        for (int64_t j = 0; j < nvis; ++j)
+            p[j] = exp(p[j] - m) / l;
+        /* dP_ij = <dO_i, v_j>;  D_i = sum_j P_ij dP_ij */
+        double D = 0.0;
+        for (int64_t j = 0; j < nvis; ++j) {
+            const uint16_t *vr = jb->v + ((base + j) * H + h) * (int64_t)d;
+            double acc = 0.0;
+            for (int c = 0; c < d; ++c)
+                acc += dorow[c] * widen_bf16(vr[c]);
+            dp[j] = acc;
+            D += p[j] * dp[j];
+        }
+        /* dS_ij = P_ij (dP_ij - D_i); dQ_i, and this row's share of dK_j, dV_j */
+        double *dqi = jb->dq + i * (int64_t)d;
+        for (int c = 0; c < d; ++c)
+            dqi[c] = 0.0;
+        for (int64_t j = 0; j < nvis; ++j) {
+            const double ds = p[j] * (dp[j] - D);
+            const uint16_t *kr = jb->k + ((base + j) * H + h) * (int64_t)d;
+            double *dkr = jb->dk + j * (int64_t)d;
+            double *dvr = jb->dv + j * (int64_t)d;
+            for (int c = 0; c < d; ++c) {
+                dqi[c] += jb->scale * ds * widen_bf16(kr[c]);
+                dkr[c] += jb->scale * ds * qf[c];
+                dvr[c] += p[j] * dorow[c];
+            }
+        }
+    }
+    free(p);
+    free(dp);
+    free(qf);
+    free(dorow);
+    return NULL;
+}
+
+/*
+ * dQ, dK, dV of the listed (sequence, head) pairs, by the chain rule written
+ * out above.  pairs is [npairs][2] = (seq, head); the outputs hold, pair after
+ * pair, the L_s rows of that pair ([sum_p L_{s_p}][d] each, fp64).  dout is
+ * the upstream gradient dO in the layout of q.  nthreads <= 0 uses every CPU
+ * of the affinity mask (the query rows of a pair are split among the threads;
+ * each keeps its own dK, dV sums, added up at the end).  Returns 0 or a
+ * negative code.
+ */
+int oracle_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                    const uint16_t *dout, const int64_t *cu_seqlens, int64_t nseq, int H,
+                    int d, double scale, int causal, const int64_t *pairs, int64_t npairs,
+                    double *dq, double *dk, double *dv, int nthreads, int *threads_used)
+{
+    int st = check_common(q, k, v, cu_seqlens, nseq, H, d, scale);
+    if (st != ORACLE_OK || !dout || npairs < 0 || (npairs > 0 && (!pairs || !dq || !dk || !dv)))
+        return ORACLE_EINVAL;
+    for (int64_t pp = 0; pp < npairs; ++pp)
+        if (pairs[2 * pp] < 0 || pairs[2 * pp] >= nseq || pairs[2 * pp + 1] < 0 ||
+            pairs[2 * pp + 1] >= H)
+            return ORACLE_EINVAL;
+    const int ncpu = nthreads > 0 ? nthreads : oracle_cpu_count();
+    int used_max = 1;
+    int64_t out_row = 0;
+    for (int64_t pp = 0; pp < npairs && st == ORACLE_OK; ++pp) {
+        const int64_t s = pairs[2 * pp];
+        const int h = (int)pairs[2 * pp + 1];
+        const int64_t base = cu_seqlens[s], L = cu_seqlens[s + 1] - base;
+        int nt = ncpu;
+        if (nt > L)
+            nt = L > 0 ? (int)L : 1;
+        bwd_job *jobs = (bwd_job *)calloc((size_t)nt, sizeof(bwd_job));
+        pthread_t *tid = (pthread_t *)calloc((size_t)nt, sizeof(pthread_t));
+        double *acc = (double *)calloc((size_t)nt * 2 * (size_t)(L > 0 ? L : 1) * (size_t)d,
+                                       sizeof(double));
+        if (!jobs || !tid || !acc) {
+            free(jobs);
+            free(tid);
+            free(acc);
+            return ORACLE_ENOMEM;
+        }
+        /* equal work per thread: causal row i costs i + 1 keys, so the split
+           points of the rows go as L * sqrt(t / nt) */
+        for (int t = 0; t < nt; ++t) {
+            bwd_job *jb = &jobs[t];
+            jb->q = q; jb->k = k; jb->v = v; jb->dout = dout;
+            jb->base = base; jb->L = L;
+            jb->H = H; jb->h = h; jb->d = d; jb->scale = scale; jb->causal = causal;
+            if (causal) {
+                jb->begin = t == 0 ? 0 : (int64_t)((double)L * sqrt((double)t / nt));
+                jb->end = t == nt - 1 ? L : (int64_t)((double)L * sqrt((double)(t + 1) / nt));
+            } else {
+                jb->begin = L * t / nt;
+                jb->end = L * (t + 1) / nt;
+            }
+            jb->dq = dq + out_row * (int64_t)d;
+            jb->dk = acc + (size_t)t * 2 * (size_t)L * (size_t)d;
+            jb->dv = jb->dk + (size_t)L * (size_t)d;
+            jb->status = ORACLE_OK;
+        }
+        int started = 0;
+        if (nt == 1) {
+            bwd_worker(&jobs[0]);
+            started = 1;
+        } else {
+            for (int t = 0; t < nt; ++t) {
+                if (pthread_create(&tid[t], NULL, bwd_worker, &jobs[t]) != 0)
+                    break;
+                ++started;
+            }
+            for (int t = started; t < nt; ++t)
+                bwd_worker(&jobs[t]);
+            for (int t = 0; t < started; ++t)
+                pthread_join(tid[t], NULL);
+        }
+        /* dK_j, dV_j = the sums over every worker's rows */
+        for (int64_t x = 0; x < L * (int64_t)d; ++x) {
+            double sk = 0.0, sv = 0.0;
+            for (int t = 0; t < nt; ++t) {
+                sk += jobs[t].dk[x];
+                sv += jobs[t].dv[x];
+            }
+            dk[out_row * (int64_t)d + x] = sk;
+            dv[out_row * (int64_t)d + x] = sv;
+        }
+        for (int t = 0; t < nt; ++t)
+            if (jobs[t].status != ORACLE_OK)
+                st = jobs[t].status;
+        if (nt > 1 && started > used_max)
+            used_max = started;
+        out_row += L;
+        free(jobs);
+        free(tid);
+        free(acc);
+    }
+    if (threads_used)
+        *threads_used = used_max;
     return st;
 }

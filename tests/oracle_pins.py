@@ -14,7 +14,10 @@ disagrees with:
   - the two-segment merge identity of the online softmax;
   - the block-wise online loop, for several block sizes;
   - packing: a sequence inside a packed batch equals that sequence alone;
-  - causal masking: the last row of a causal sequence sees every key.
+  - causal masking: the last row of a causal sequence sees every key;
+  - gradients (dQ, dK, dV): central finite differences of sum(dO * O), torch
+    autograd through SDPA in fp64, the sum rules (sum of dV = sum of dO, sum
+    of dK = 0), constant V (no dQ, dK), dO = 0, and packing.
 The mutation tests run the same checks against deliberately broken copies of
 the oracle and require each copy to fail at least one of them.
 """
@@ -320,6 +323,118 @@ def check_window_torch_sdpa(orc):
                 _close(o[n], ref[s, h, i].numpy(), 1e-12, f"SDPA window {(a, b)} causal={causal}")
 
 
+# ------------------------------------------------------------ backward --
+
+def _all_pairs(wl):
+    return [(s, h) for s in range(wl.nseq) for h in range(wl.H)]
+
+
+def _np_forward(qf, kf, vf, scale, causal):
+    """O of one (sequence, head) from fp64 arrays [L, d] (for finite differences)."""
+    S = scale * (qf @ kf.T)
+    if causal:
+        S = np.where(np.tril(np.ones(S.shape, dtype=bool)), S, -np.inf)
+    S = S - S.max(axis=1, keepdims=True)
+    P = np.exp(S)
+    P /= P.sum(axis=1, keepdims=True)
+    return P @ vf
+
+
+def check_bwd_finite_differences(orc):
+    """Central differences of loss = sum(dO * O) agree with the oracle's dQ, dK,
+    dV; the fp64 forward used for the differences is first tied to the pinned
+    forward oracle."""
+    wl = _rand_workload(1111, [3, 6], H=2, d=4)
+    dout = inputs.normal_bf16(1112, wl.q.size).reshape(wl.q.shape)
+    qf, kf, vf = (inputs.bf16_bits_to_f64(a) for a in (wl.q, wl.k, wl.v))
+    dof = inputs.bf16_bits_to_f64(dout)
+    scale = 0.6
+    for causal in (False, True):
+        pairs = _all_pairs(wl)
+        dq, dk, dv, _ = orc.attn_bwd(wl.q, wl.k, wl.v, dout, wl.cu_seqlens, pairs, scale, causal)
+        o_or, _, _ = orc.attn_rows(wl.q, wl.k, wl.v, wl.cu_seqlens,
+                                   inputs.all_rows(wl.cu_seqlens, wl.H), scale, causal, 1)
+        for n, (s, h) in enumerate(pairs):
+            a, b = int(wl.cu_seqlens[s]), int(wl.cu_seqlens[s + 1])
+            X = [qf[a:b, h].copy(), kf[a:b, h].copy(), vf[a:b, h].copy()]
+            G = dof[a:b, h]
+            sel = [r for r, (ss, hh, _) in enumerate(inputs.all_rows(wl.cu_seqlens, wl.H))
+                   if ss == s and hh == h]
+            _close(_np_forward(*X, scale, causal), o_or[sel], 1e-13, "fp64 forward = oracle forward")
+            eps = 1e-6
+            for t, grad in enumerate((dq[n], dk[n], dv[n])):
+                num = np.zeros_like(X[t])
+                for idx in np.ndindex(*X[t].shape):
+                    keep = X[t][idx]
+                    X[t][idx] = keep + eps
+                    up = float(np.sum(G * _np_forward(*X, scale, causal)))
+                    X[t][idx] = keep - eps
+                    dn = float(np.sum(G * _np_forward(*X, scale, causal)))
+                    X[t][idx] = keep
+                    num[idx] = (up - dn) / (2 * eps)
+                _close(grad, num, 1e-7, f"finite differences of {'QKV'[t]} causal={causal}")
+
+
+def check_bwd_torch_autograd(orc):
+    """Library cross-check: torch autograd through SDPA, fp64 on CPU."""
+    import torch
+    B, H, N, d = 2, 3, 37, 16
+    wl = _rand_workload(1212, [N] * B, H=H, d=d, std=1.2)
+    dout = inputs.normal_bf16(1213, wl.q.size).reshape(wl.q.shape)
+    to_t = lambda a: torch.from_numpy(inputs.bf16_bits_to_f64(a).reshape(B, N, H, d)).permute(0, 2, 1, 3)
+    for causal in (False, True):
+        qt, kt, vt = (to_t(a).clone().requires_grad_(True) for a in (wl.q, wl.k, wl.v))
+        scale = 1.0 / math.sqrt(d)
+        out = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, is_causal=causal, scale=scale)
+        out.backward(to_t(dout))
+        pairs = _all_pairs(wl)
+        dq, dk, dv, _ = orc.attn_bwd(wl.q, wl.k, wl.v, dout, wl.cu_seqlens, pairs, scale, causal, 2)
+        for n, (s, h) in enumerate(pairs):
+            _close(dq[n], qt.grad[s, h].numpy(), 1e-11, f"autograd dQ causal={causal}")
+            _close(dk[n], kt.grad[s, h].numpy(), 1e-11, f"autograd dK causal={causal}")
+            _close(dv[n], vt.grad[s, h].numpy(), 1e-11, f"autograd dV causal={causal}")
+
+
+def check_bwd_invariants(orc):
+    """Rows of P sum to one, so sum_j dV_j = sum_i dO_i and sum_j dS_ij = 0,
+    so sum_j dK_j = 0; constant V rows make dP constant along a row, so
+    dS = 0 and dQ = dK = 0; dO = 0 gives no gradient at all."""
+    wl = _rand_workload(1313, [9, 30, 1], H=2, d=8)
+    dout = inputs.normal_bf16(1314, wl.q.size).reshape(wl.q.shape)
+    dof = inputs.bf16_bits_to_f64(dout)
+    pairs = _all_pairs(wl)
+    for causal in (False, True):
+        dq, dk, dv, _ = orc.attn_bwd(wl.q, wl.k, wl.v, dout, wl.cu_seqlens, pairs, 0.45, causal)
+        for n, (s, h) in enumerate(pairs):
+            a, b = int(wl.cu_seqlens[s]), int(wl.cu_seqlens[s + 1])
+            _close(dv[n].sum(axis=0), dof[a:b, h].sum(axis=0), 1e-12, "sum of dV = sum of dO")
+            _close(dk[n].sum(axis=0), np.zeros(wl.d), 1e-12, "sum of dK = 0")
+        vconst = np.tile(inputs.f64_to_bf16_bits(np.linspace(-2, 2, wl.d)), (wl.q.shape[0], wl.H, 1))
+        dq, dk, dv, _ = orc.attn_bwd(wl.q, wl.k, vconst, dout, wl.cu_seqlens, pairs, 0.45, causal)
+        for n in range(len(pairs)):
+            _close(dq[n], 0 * dq[n], 1e-12, "constant V: dQ = 0")
+            _close(dk[n], 0 * dk[n], 1e-12, "constant V: dK = 0")
+        zero = np.zeros_like(dout)
+        dq, dk, dv, _ = orc.attn_bwd(wl.q, wl.k, wl.v, zero, wl.cu_seqlens, pairs, 0.45, causal)
+        for n in range(len(pairs)):
+            assert not dq[n].any() and not dk[n].any() and not dv[n].any(), "dO = 0: no gradient"
+
+
+def check_bwd_packing(orc):
+    """A sequence inside a packed batch has the gradients it has alone."""
+    wl = _rand_workload(1414, [13, 21, 2], H=2, d=8)
+    dout = inputs.normal_bf16(1415, wl.q.size).reshape(wl.q.shape)
+    pairs = _all_pairs(wl)
+    for causal in (False, True):
+        dq, dk, dv, _ = orc.attn_bwd(wl.q, wl.k, wl.v, dout, wl.cu_seqlens, pairs, 0.3, causal, 3)
+        for n, (s, h) in enumerate(pairs):
+            a, b = int(wl.cu_seqlens[s]), int(wl.cu_seqlens[s + 1])
+            g = orc.attn_bwd(wl.q[a:b], wl.k[a:b], wl.v[a:b], dout[a:b], np.array([0, b - a]),
+                             [(0, h)], 0.3, causal, 1)
+            for t in range(3):
+                _close((dq, dk, dv)[t][n], g[t][0], 1e-13, f"packed gradient {'QKV'[t]}")
+
+
 ALL_CHECKS = [
     check_brute_force_decimal,
     check_two_key_closed_form,
@@ -335,4 +450,8 @@ ALL_CHECKS = [
     check_window_brute_force_decimal,
     check_window_closed_forms,
     check_window_torch_sdpa,
+    check_bwd_finite_differences,
+    check_bwd_torch_autograd,
+    check_bwd_invariants,
+    check_bwd_packing,
 ]

@@ -41,6 +41,18 @@ MUTANTS = {
     "bad_widening": [("uint32_t u = (uint32_t)bits << 16;", "uint32_t u = (uint32_t)bits << 15;")],
     "max_over_first_key_only": [("if (srow[j] > m)\n                m = srow[j];",
                                  "if (j == 0)\n                m = srow[j];")],
+    # gradients
+    "bwd_dq_drops_scale": [("dqi[c] += jb->scale * ds * widen_bf16(kr[c]);",
+                            "dqi[c] += ds * widen_bf16(kr[c]);")],
+    "bwd_no_rowsum_term": [("const double ds = p[j] * (dp[j] - D);", "const double ds = p[j] * dp[j];")],
+    "bwd_dk_from_k": [("dkr[c] += jb->scale * ds * qf[c];",
+                       "dkr[c] += jb->scale * ds * widen_bf16(kr[c]);")],
+    "bwd_dv_from_ds": [("dvr[c] += p[j] * dorow[c];", "dvr[c] += ds * dorow[c];")],
+    "bwd_causal_ignored": [("const int64_t nvis = jb->causal ? i + 1 : L;", "const int64_t nvis = L;")],
+    "bwd_dp_from_k": [("acc += dorow[c] * widen_bf16(vr[c]);",
+                       "acc += dorow[c] * widen_bf16(jb->k[((base + j) * H + h) * (int64_t)d + c]);")],
+    "bwd_unnormalised_p": [("p[j] = exp(p[j] - m) / l;\n        /* dP_ij", "p[j] = exp(p[j] - m);\n        /* dP_ij")],
+    "bwd_one_worker_summed": [("sk += jobs[t].dk[x];", "sk = jobs[t].dk[x];")],
 }
 
 
