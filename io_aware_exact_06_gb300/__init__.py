@@ -1,6 +1,7 @@
-"""GB300 (sm_103a) fused exact attention forward.
+"""GB300 (sm_103a) fused exact attention: forward and backward.
 
-A thin ctypes binding of the C ABI in ``include/attn_fwd.h`` (the library
+A thin ctypes binding of the C ABI in ``include/attn_fwd.h`` and
+``include/attn_bwd.h`` (the library
 ``_build/libattn_fwd.so``, built by ``build.py``).  The functions here only
 marshal arguments: every step of the computation runs in the library's CUDA
 kernels.  There is no CPU path: calling the library without it built, or on a
@@ -13,14 +14,14 @@ import os
 
 from . import build as _build
 
-__all__ = ["attn_fwd", "attn_fwd_ex", "attn_fwd_noalloc", "attn_fwd_window", "attn_fwd_kvsplit", "attn_last_device_error", "attn_last_error_site",
+__all__ = ["attn_fwd", "attn_bwd", "attn_fwd_ex", "attn_fwd_noalloc", "attn_fwd_window", "attn_fwd_kvsplit", "attn_last_device_error", "attn_last_error_site",
            "attn_status_string", "AttnError", "AttnFwdOptions", "lib", "forward",
            "EXPORTED_SYMBOLS"]
 
-# Every symbol include/attn_fwd.h declares.
+# Every symbol the headers under include/ declare.
 EXPORTED_SYMBOLS = ("attn_fwd", "attn_fwd_ex", "attn_last_device_error", "attn_last_error_site",
                     "attn_last_cuda_error", "attn_status_string", "attn_fwd_noalloc",
-                    "attn_fwd_window", "attn_fwd_kvsplit")
+                    "attn_fwd_window", "attn_fwd_kvsplit", "attn_bwd")
 
 ATTN_OK = 0
 
@@ -60,6 +61,8 @@ def lib() -> ctypes.CDLL:
         L.attn_fwd_window.restype = i
         L.attn_fwd_kvsplit.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_float, i, i, vp]
         L.attn_fwd_kvsplit.restype = i
+        L.attn_bwd.argtypes = [vp] * 9 + [i, i, i, i, ctypes.c_float, i, vp, vp]
+        L.attn_bwd.restype = i
         L.attn_fwd_noalloc.argtypes = sig
         L.attn_fwd_noalloc.restype = i
         L.attn_last_device_error.argtypes = [vp]
@@ -149,6 +152,17 @@ def attn_fwd_noalloc(q, k, v, o, lse, B: int, H: int, N: int, d: int, scale: flo
                                 _ptr(cu_seqlens), _stream(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_noalloc")
+    return st
+
+
+def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B: int, H: int, N: int, d: int, scale: float,
+             causal: bool, cu_seqlens=None, stream=None) -> int:
+    """The C call ``attn_bwd``: dQ, dK, dV of attn_fwd for the upstream gradient dout."""
+    st = lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
+                        _ptr(dk), _ptr(dv), int(B), int(H), int(N), int(d), float(scale),
+                        int(bool(causal)), _ptr(cu_seqlens), _stream(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd")
     return st
 
 

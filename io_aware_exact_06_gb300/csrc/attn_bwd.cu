@@ -1,0 +1,163 @@
+// Host side of the C ABI declared in include/attn_bwd.h: argument checks, the
+// per-stream workspace (per-row D and LSE * log2 e, unit counters), TMA
+// descriptors and the three launches (row prologue, dK/dV kernel, dQ kernel).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <map>
+#include <set>
+#include <utility>
+
+#include "../../include/attn_bwd.h"
+#include "attn_bwd_kernel.cuh"
+#include "attn_host.h"
+
+namespace {
+
+using bwd::BwdCfg;
+using bwd::BwdParams;
+
+struct BwdWorkspace {
+  void* buf = nullptr;   // [0, 256): unit counters (int), then lse2 and D (float)
+  size_t floats = 0;     // capacity of each of the two float arrays
+};
+
+std::map<std::pair<int, attn_stream_t>, BwdWorkspace> g_bwd_ws;
+std::set<int> g_bwd_ready;
+
+constexpr size_t kCounterBytes = 256;
+
+cudaError_t set_bwd_attributes() {
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(bwd::bwd_tile_kernel<64, true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                BwdCfg<64>::kKvSmemBytes)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(bwd::bwd_tile_kernel<128, true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                BwdCfg<128>::kKvSmemBytes)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(bwd::bwd_tile_kernel<64, false>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                BwdCfg<64>::kQSmemBytes)) != cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(bwd::bwd_tile_kernel<128, false>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              BwdCfg<128>::kQSmemBytes);
+}
+
+int bwd_workspace(int dev, attn_stream_t stream, size_t floats, int** counters, float** lse2,
+                  float** dd) {
+  BwdWorkspace& ws = g_bwd_ws[std::make_pair(dev, stream)];
+  if (ws.floats < floats || !ws.buf) {
+    cudaError_t e;
+    if (ws.buf) {
+      // the old buffers may still be read by work queued on this stream
+      if ((e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream))) != cudaSuccess)
+        return attn_host::lib_cuda_fail(e);
+      cudaFree(ws.buf);
+      ws.buf = nullptr;
+      ws.floats = 0;
+    }
+    const size_t cap = std::max<size_t>(floats, 1 << 16);
+    if ((e = cudaMalloc(&ws.buf, kCounterBytes + 2 * cap * sizeof(float))) != cudaSuccess)
+      return attn_host::lib_cuda_fail(e);
+    if ((e = cudaMemset(ws.buf, 0, kCounterBytes)) != cudaSuccess) return attn_host::lib_cuda_fail(e);
+    ws.floats = cap;
+  }
+  *counters = static_cast<int*>(ws.buf);
+  *lse2 = reinterpret_cast<float*>(static_cast<char*>(ws.buf) + kCounterBytes);
+  *dd = *lse2 + ws.floats;
+  return ATTN_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+template <int D>
+int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+               const CUtensorMap& mdo, const void* o, const void* dout, const float* lse,
+               BwdParams p, int* counters, int grid, cudaStream_t s) {
+  const long long rows = (long long)p.B * p.H * p.T * bwd::kTile;
+  const long long blocks = (rows * 32 + 255) / 256;
+  bwd::bwd_prep_kernel<D><<<(unsigned)blocks, 256, 0, s>>>(
+      reinterpret_cast<const __nv_bfloat16*>(o), reinterpret_cast<const __nv_bfloat16*>(dout), lse,
+      const_cast<float*>(p.lse2), const_cast<float*>(p.dd), p.B, p.H, p.N, p.T);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return attn_host::lib_cuda_fail(e);
+  p.sched = counters;
+  bwd::bwd_tile_kernel<D, true><<<grid, bwd::kThreads, BwdCfg<D>::kKvSmemBytes, s>>>(
+      mq, mk, mv, mdo, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return attn_host::lib_cuda_fail(e);
+  p.sched = counters + 4;
+  bwd::bwd_tile_kernel<D, false><<<grid, bwd::kThreads, BwdCfg<D>::kQSmemBytes, s>>>(
+      mq, mk, mv, mdo, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return attn_host::lib_cuda_fail(e);
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                        const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                        int H, int N, int d, float scale, int causal, const int32_t* cu_seqlens,
+                        attn_stream_t stream) {
+  if (B < 0 || H < 0 || N < 0) return ATTN_ERR_SHAPE;
+  if (d != 64 && d != 128) return ATTN_ERR_HEADDIM;
+  if (!std::isfinite(scale)) return ATTN_ERR_SCALE;
+  if (cu_seqlens) return ATTN_ERR_SHAPE;
+  if (B == 0 || H == 0 || N == 0) return ATTN_OK;
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return ATTN_ERR_NULL;
+  for (const void* ptr : {q, k, v, o, dout, (const void*)dq, (const void*)dk, (const void*)dv})
+    if (!aligned(ptr, 16)) return ATTN_ERR_ALIGN;
+  if (!aligned(lse, 4)) return ATTN_ERR_ALIGN;
+  const int64_t tokens = (int64_t)B * N;
+  if (tokens > INT32_MAX - 2 * bwd::kTile || (int64_t)H * d > (1 << 20) || H > 65535)
+    return ATTN_ERR_SHAPE;
+  const int64_t T = (N + bwd::kTile - 1) / bwd::kTile;
+  const int64_t units = (int64_t)B * H * T;
+  if (units > INT32_MAX / bwd::kTile) return ATTN_ERR_SHAPE;
+
+  std::lock_guard<std::mutex> lock(attn_host::lib_mutex());
+  int dev = 0, sms = 0;
+  int* err = nullptr;
+  int st = attn_host::lib_device(&dev, &sms, &err);
+  if (st != ATTN_OK) return st;
+  if (!g_bwd_ready.count(dev)) {
+    cudaError_t e = set_bwd_attributes();
+    if (e != cudaSuccess) return attn_host::lib_cuda_fail(e);
+    g_bwd_ready.insert(dev);
+  }
+  CUtensorMap mq, mk, mv, mdo;
+  if ((st = attn_host::lib_make_map(&mq, q, tokens, H, d)) != ATTN_OK) return st;
+  if ((st = attn_host::lib_make_map(&mk, k, tokens, H, d)) != ATTN_OK) return st;
+  if ((st = attn_host::lib_make_map(&mv, v, tokens, H, d)) != ATTN_OK) return st;
+  if ((st = attn_host::lib_make_map(&mdo, dout, tokens, H, d)) != ATTN_OK) return st;
+  int* counters = nullptr;
+  float *lse2 = nullptr, *dd = nullptr;
+  if ((st = bwd_workspace(dev, stream, (size_t)units * bwd::kTile, &counters, &lse2, &dd)) !=
+      ATTN_OK)
+    return st;
+
+  BwdParams p{};
+  p.dq = reinterpret_cast<__nv_bfloat16*>(dq);
+  p.dk = reinterpret_cast<__nv_bfloat16*>(dk);
+  p.dv = reinterpret_cast<__nv_bfloat16*>(dv);
+  p.lse2 = lse2;
+  p.dd = dd;
+  p.err = err;
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.T = (int)T;
+  p.causal = causal ? 1 : 0;
+  p.scale = scale;
+  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p.timeout_ns = 2000000000ull;
+  const int grid = (int)std::min<int64_t>(units, sms);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return d == 64 ? launch_bwd<64>(mq, mk, mv, mdo, o, dout, lse, p, counters, grid, s)
+                 : launch_bwd<128>(mq, mk, mv, mdo, o, dout, lse, p, counters, grid, s);
+}

@@ -14,6 +14,7 @@
 
 #include "../../include/attn_fwd.h"
 #include "attn_fwd_kernel.cuh"
+#include "attn_host.h"
 
 namespace {
 
@@ -560,3 +561,31 @@ extern "C" int attn_fwd_kvsplit(const void* q, const void* k, const void* v, voi
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
   return ATTN_OK;
 }
+
+// ---------------------------------------------------------------------------
+// Services shared with the backward's host code (attn_host.h).
+namespace attn_host {
+
+std::mutex& lib_mutex() { return g_mu; }
+
+int lib_cuda_fail(cudaError_t e) { return cuda_fail(e); }
+
+int lib_device(int* dev, int* sms, int** err) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  DeviceState* ds = nullptr;
+  const int st = device_state(*dev, &ds);
+  if (st != ATTN_OK) return st;
+  *sms = ds->sms;
+  *err = ds->err;
+  return ATTN_OK;
+}
+
+int lib_make_map(CUtensorMap* map, const void* ptr, int64_t tokens, int H, int d) {
+  EncodeTiledFn enc = nullptr;
+  const int st = get_encode(&enc);
+  if (st != ATTN_OK) return st;
+  return make_map(enc, map, ptr, tokens, H, d);
+}
+
+}  // namespace attn_host

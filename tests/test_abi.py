@@ -84,3 +84,30 @@ def test_binding_raises_on_error(lib):
     with pytest.raises(fa.AttnError) as e:
         fa.attn_fwd(BUF, BUF, BUF, BUF, BUF, 1, 1, 128, 80, 0.1, False)
     assert e.value.status == -3
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(B=-1), -2),
+    (dict(d=96), -3),
+    (dict(scale=float("nan")), -5),
+    (dict(cu=BUF), -2),
+    (dict(dout=None), -1),
+    (dict(dq=None), -1),
+    (dict(lse=None), -1),
+    (dict(dk=BUF + 8), -4),
+    (dict(dout=BUF + 2), -4),
+    (dict(lse=BUF + 2), -4),
+    (dict(B=70000, N=1 << 16), -2),
+])
+def test_backward_argument_errors(lib, args, status):
+    a = dict(q=BUF, k=BUF, v=BUF, o=BUF, dout=BUF, lse=BUF, dq=BUF, dk=BUF, dv=BUF, B=2, H=4,
+             N=256, d=128, scale=0.1, causal=1, cu=None, stream=None)
+    a.update(args)
+    st = lib.attn_bwd(a["q"], a["k"], a["v"], a["o"], a["dout"], a["lse"], a["dq"], a["dk"],
+                      a["dv"], a["B"], a["H"], a["N"], a["d"], a["scale"], a["causal"], a["cu"],
+                      a["stream"])
+    assert st == status
+
+
+def test_backward_empty_problem_is_a_noop(lib):
+    assert lib.attn_bwd(*([None] * 9), 0, 4, 256, 64, 0.125, 0, None, None) == 0
