@@ -65,6 +65,23 @@ class Oracle:
                                       ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
                                       _c_i64p, ctypes.c_int64, _c_dp, _c_dp, _c_dp, ctypes.c_int,
                                       ctypes.POINTER(ctypes.c_int)]
+        L.oracle_e4m3_encode.restype = ctypes.c_uint8
+        L.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        L.oracle_e4m3_decode.restype = ctypes.c_double
+        L.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        L.oracle_fwht_f32.restype = None
+        L.oracle_fwht_f32.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_int,
+                                      ctypes.POINTER(ctypes.c_int8)]
+        L.oracle_fp8_quantize.restype = ctypes.c_int
+        L.oracle_fp8_quantize.argtypes = [_c_u16p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          ctypes.POINTER(ctypes.c_int8),
+                                          ctypes.POINTER(ctypes.c_uint8),
+                                          ctypes.POINTER(ctypes.c_float)]
+        L.oracle_attn_rows_f64.restype = ctypes.c_int
+        L.oracle_attn_rows_f64.argtypes = [_c_dp, _c_dp, _c_dp, _c_i64p, ctypes.c_int64,
+                                           ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                           ctypes.c_int, _c_i64p, ctypes.c_int64, _c_dp, _c_dp]
         self.lib = L
         self.path = path
 
@@ -127,6 +144,64 @@ class Oracle:
             raise ValueError(f"oracle_attn_bwd failed with status {st}")
         split = np.cumsum(lens)[:-1]
         return np.split(dq[:n], split), np.split(dk[:n], split), np.split(dv[:n], split), used.value
+
+    def e4m3_encode(self, x) -> np.ndarray:
+        """e4m3 codes (uint8) of fp32 values: nearest, ties to even, saturating."""
+        x = np.ascontiguousarray(x, dtype=np.float32).ravel()
+        return np.array([self.lib.oracle_e4m3_encode(float(v)) for v in x], dtype=np.uint8)
+
+    def e4m3_decode(self, c) -> np.ndarray:
+        c = np.ascontiguousarray(c, dtype=np.uint8).ravel()
+        return np.array([self.lib.oracle_e4m3_decode(int(v)) for v in c], dtype=np.float64)
+
+    def fwht_f32(self, x, signs=None) -> np.ndarray:
+        """(x * signs) H_d in fp32 butterflies, for each row of x [..., d]."""
+        x = np.array(x, dtype=np.float32)
+        d = x.shape[-1]
+        flat = x.reshape(-1, d)
+        sg = None if signs is None else np.ascontiguousarray(signs, dtype=np.int8)
+        for r in range(flat.shape[0]):
+            row = np.ascontiguousarray(flat[r])
+            self.lib.oracle_fwht_f32(_ptr(row, ctypes.c_float), d,
+                                     None if sg is None else _ptr(sg, ctypes.c_int8))
+            flat[r] = row
+        return flat.reshape(x.shape)
+
+    def fp8_quantize(self, x, B: int, N: int, block_rows: int, rotate: bool, signs=None):
+        """Block e4m3 quantisation of bf16 bits x [B*N, H, d] (see oracle.c).
+
+        Returns (codes uint8 [B*N, H, d], scales fp32 [B, H, nblocks])."""
+        x = _u16(x)
+        tokens, H, d = x.shape
+        nblk = 1 if block_rows == 0 else -(-N // block_rows)
+        codes = np.zeros(x.shape, dtype=np.uint8)
+        scales = np.zeros((B, H, nblk), dtype=np.float32)
+        sg = None if signs is None else np.ascontiguousarray(signs, dtype=np.int8)
+        st = self.lib.oracle_fp8_quantize(_ptr(x, ctypes.c_uint16), int(B), int(N), H, d,
+                                          int(block_rows), int(bool(rotate)),
+                                          None if sg is None else _ptr(sg, ctypes.c_int8),
+                                          _ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_float))
+        if st != 0:
+            raise ValueError(f"oracle_fp8_quantize failed with status {st}")
+        return codes, scales
+
+    def attn_rows_f64(self, q, k, v, cu_seqlens, rows, scale: float, causal: bool):
+        """O and LSE of the given rows for fp64 inputs [tokens, H, d]."""
+        q, k, v = (np.ascontiguousarray(a, dtype=np.float64) for a in (q, k, v))
+        tokens, H, d = q.shape
+        cu = np.ascontiguousarray(cu_seqlens, dtype=np.int64)
+        rows = np.ascontiguousarray(rows, dtype=np.int64).reshape(-1, 3)
+        n = rows.shape[0]
+        o = np.zeros((n, d), dtype=np.float64)
+        lse = np.zeros(n, dtype=np.float64)
+        st = self.lib.oracle_attn_rows_f64(_ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double),
+                                           _ptr(v, ctypes.c_double), _ptr(cu, ctypes.c_int64),
+                                           len(cu) - 1, H, d, float(scale), int(bool(causal)),
+                                           _ptr(rows, ctypes.c_int64), n,
+                                           _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double))
+        if st != 0:
+            raise ValueError(f"oracle_attn_rows_f64 failed with status {st}")
+        return o, lse
 
     def attn_probs(self, q, k, cu_seqlens, seq: int, h: int, i: int, scale: float,
                    causal: bool):
@@ -205,6 +280,26 @@ def attn_probs(*a, **kw):
 
 def attn_bwd(*a, **kw):
     return default().attn_bwd(*a, **kw)
+
+
+def e4m3_encode(*a, **kw):
+    return default().e4m3_encode(*a, **kw)
+
+
+def e4m3_decode(*a, **kw):
+    return default().e4m3_decode(*a, **kw)
+
+
+def fwht_f32(*a, **kw):
+    return default().fwht_f32(*a, **kw)
+
+
+def fp8_quantize(*a, **kw):
+    return default().fp8_quantize(*a, **kw)
+
+
+def attn_rows_f64(*a, **kw):
+    return default().attn_rows_f64(*a, **kw)
 
 
 def softmax_merge(*a, **kw):

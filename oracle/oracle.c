@@ -53,6 +53,25 @@
  *
  * over the same visible (i, j) pairs as the forward.
  *
+ * FP8 (oracle_fp8_quantize, oracle_attn_rows_f64).  The pages name the FP8
+ * forward's two devices without formulas: block quantisation and incoherent
+ * processing ("flash-attention-evolution" (letsgetai), FlashAttention-3
+ * section, item 3; "FlashAttention 1-4 演进速查" (argus-lessons),
+ * FlashAttention-3 items).  Readings taken here:
+ *   - incoherent processing multiplies Q and K along d by the same orthogonal
+ *     matrix, diag(signs) H_d / sqrt(d) with H_d the Sylvester-Hadamard
+ *     matrix, so Q K^T is unchanged; the transform is computed unnormalised
+ *     (butterflies in fp32) and the 1/d it leaves in Q K^T goes into the
+ *     logit scale;
+ *   - block quantisation gives every block its own scale: the block's largest
+ *     |x| maps to 448, the largest finite e4m3 value; codes are e4m3, rounded
+ *     to nearest even, saturating.
+ * Because a quantised code is an integer decided by floating point, this
+ * oracle takes each step in fp32 in the kernel's order (the butterfly
+ * stages, the max, 448 / amax, x * (448 / amax), the rounding), so codes and
+ * scales are reproduced bit for bit.  The attention of the dequantised values
+ * is then the plain definition again, in fp64 (oracle_attn_rows_f64).
+ *
  * Besides the definition, two more routines restate the pages' own incremental
  * formulations so the tests can pin one against the other:
  *   - oracle_softmax_merge: the two-segment (m, l, f) merge identity;
@@ -640,5 +659,205 @@ int oracle_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     }
     if (threads_used)
         *threads_used = used_max;
+    return st;
+}
+
+/* ----------------------------------------------------------------- FP8 -- */
+
+/*
+ * e4m3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; no infinity,
+ * the all-ones magnitude is NaN): the code of x rounded to nearest, ties to
+ * even, with finite overflow saturating to +-448.  x is fp32; NaN maps to the
+ * NaN code 0x7f.
+ */
+uint8_t oracle_e4m3_encode(float x)
+{
+    if (isnan(x))
+        return 0x7f;
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a >= 448.0)
+        return sign | 0x7e; /* largest finite: 1.75 * 2^8 */
+    /* the value grid: subnormals m * 2^-9 (m < 8), normals (8 + m) * 2^(e - 10)
+       for e in 1..15; find the spacing of the binade of a */
+    int e;
+    double spacing;
+    if (a < 0.015625) { /* 2^-6: subnormal range */
+        e = 0;
+        spacing = 0.001953125; /* 2^-9 */
+    } else {
+        e = (int)floor(log2(a)) + 7; /* biased exponent of a's binade */
+        if (ldexp(1.0, e - 7) > a)
+            --e; /* guard the log2 rounding */
+        else if (ldexp(1.0, e - 6) <= a)
+            ++e;
+        spacing = ldexp(1.0, e - 10);
+    }
+    const double q = a / spacing; /* exact: spacing is a power of two */
+    double n = floor(q);
+    const double frac = q - n;
+    if (frac > 0.5 || (frac == 0.5 && fmod(n, 2.0) == 1.0))
+        n += 1.0;
+    /* n counts spacings from 0: subnormal n in 0..8, normal n in 8..16 */
+    if (e == 0) {
+        if (n >= 8.0)
+            return sign | 0x08; /* rounded up to the smallest normal 2^-6 */
+        return sign | (uint8_t)n;
+    }
+    if (n >= 16.0) { /* rounded up into the next binade */
+        ++e;
+        n = 8.0;
+        if (e > 15 || (e == 15 && n - 8.0 > 6.0))
+            return sign | 0x7e;
+    }
+    if (e == 15 && n - 8.0 > 6.0)
+        return sign | 0x7e;
+    return sign | (uint8_t)((e << 3) | ((int)n - 8));
+}
+
+/* The value of an e4m3 code (NaN for 0x7f / 0xff). */
+double oracle_e4m3_decode(uint8_t c)
+{
+    const int sign = c & 0x80, e = (c >> 3) & 0xf, m = c & 7;
+    if (e == 15 && m == 7)
+        return NAN;
+    double v = e == 0 ? ldexp((double)m, -9) : ldexp(8.0 + m, e - 10);
+    return sign ? -v : v;
+}
+
+/*
+ * The unnormalised Hadamard transform of x[0..d) (d a power of two) times the
+ * signs, in fp32: y = (x * signs) H_d, computed by butterflies over strides
+ * 1, 2, 4, ..., d/2 (pairs (i, i + h) with bit h of i clear become
+ * (a + b, a - b)).  signs may be NULL (all +1).
+ */
+void oracle_fwht_f32(float *x, int d, const int8_t *signs)
+{
+    if (signs)
+        for (int c = 0; c < d; ++c)
+            x[c] = signs[c] < 0 ? -x[c] : x[c];
+    for (int h = 1; h < d; h <<= 1)
+        for (int i = 0; i < d; ++i)
+            if (!(i & h)) {
+                const float a = x[i], b = x[i + h];
+                x[i] = a + b;
+                x[i + h] = a - b;
+            }
+}
+
+/*
+ * Block quantisation of a [tokens, H, d] bf16 tensor of B dense sequences of
+ * length N: blocks of block_rows rows per sequence and head (the last block
+ * pulled back to end at the sequence end, the rows it shares with the block
+ * before it taking that block's codes; block_rows = 0: one block per
+ * sequence and head), each row optionally rotated by oracle_fwht_f32 with
+ * the given signs first (rotate != 0).  codes: [tokens, H, d] e4m3;
+ * scales: [B][H][nblocks] fp32 = amax / 448 (1 when the block is all zero).
+ */
+int oracle_fp8_quantize(const uint16_t *x, int64_t B, int64_t N, int H, int d, int block_rows,
+                        int rotate, const int8_t *signs, uint8_t *codes, float *scales)
+{
+    if (!x || !codes || !scales || B < 0 || N <= 0 || H <= 0 || d <= 0 || block_rows < 0 ||
+        (d & (d - 1)))
+        return ORACLE_EINVAL;
+    const int64_t rows_per = block_rows > 0 ? block_rows : N;
+    const int64_t nblk = (N + rows_per - 1) / rows_per;
+    float *blk = (float *)malloc(sizeof(float) * (size_t)rows_per * (size_t)d);
+    if (!blk)
+        return ORACLE_ENOMEM;
+    for (int64_t b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h)
+            for (int64_t t = 0; t < nblk; ++t) {
+                /* rows [r0, r0 + rows_per) of the block, pulled back at the end */
+                int64_t r0 = t * rows_per;
+                if (r0 + rows_per > N)
+                    r0 = N - rows_per;
+                const int64_t nominal = t * rows_per;
+                float amax = 0.0f;
+                for (int64_t r = 0; r < rows_per; ++r) {
+                    float *y = blk + r * d;
+                    const int64_t row = r0 + r;
+                    for (int c = 0; c < d; ++c)
+                        y[c] = row >= 0 ? (float)widen_bf16(x[((b * N + row) * H + h) * (int64_t)d + c])
+                                        : 0.0f;
+                    if (rotate)
+                        oracle_fwht_f32(y, d, signs);
+                    for (int c = 0; c < d; ++c)
+                        if (fabsf(y[c]) > amax)
+                            amax = fabsf(y[c]);
+                }
+                const float inv = amax > 0.0f ? 448.0f / amax : 1.0f;
+                scales[(b * H + h) * nblk + t] = amax > 0.0f ? amax / 448.0f : 1.0f;
+                for (int64_t r = 0; r < rows_per; ++r) {
+                    const int64_t row = r0 + r;
+                    if (row < nominal || row < 0)
+                        continue; /* the previous block's row */
+                    for (int c = 0; c < d; ++c)
+                        codes[((b * N + row) * H + h) * (int64_t)d + c] =
+                            oracle_e4m3_encode(blk[r * d + c] * inv);
+                }
+            }
+    free(blk);
+    return ORACLE_OK;
+}
+
+/*
+ * O and LSE of the requested rows, by the plain definition, for fp64 inputs
+ * in the packed layout [tokens, H, d] (e.g. dequantised FP8 values).
+ * Single-threaded.
+ */
+int oracle_attn_rows_f64(const double *q, const double *k, const double *v,
+                         const int64_t *cu_seqlens, int64_t nseq, int H, int d, double scale,
+                         int causal, const int64_t *rows, int64_t nrows, double *o, double *lse)
+{
+    if (!q || !k || !v || !cu_seqlens || nseq < 0 || H <= 0 || d <= 0 || !isfinite(scale) ||
+        nrows < 0 || (nrows > 0 && (!rows || !o || !lse)))
+        return ORACLE_EINVAL;
+    int64_t maxL = 0;
+    for (int64_t s = 0; s < nseq; ++s)
+        if (cu_seqlens[s + 1] - cu_seqlens[s] > maxL)
+            maxL = cu_seqlens[s + 1] - cu_seqlens[s];
+    double *sc = (double *)malloc(sizeof(double) * (size_t)(maxL > 0 ? maxL : 1));
+    if (!sc)
+        return ORACLE_ENOMEM;
+    int st = ORACLE_OK;
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t s = rows[3 * r], hh = rows[3 * r + 1], i = rows[3 * r + 2];
+        if (s < 0 || s >= nseq || hh < 0 || hh >= H) {
+            st = ORACLE_EINVAL;
+            break;
+        }
+        const int64_t base = cu_seqlens[s], L = cu_seqlens[s + 1] - base;
+        if (i < 0 || i >= L) {
+            st = ORACLE_EINVAL;
+            break;
+        }
+        const int64_t nv = causal ? i + 1 : L;
+        const double *qi = q + ((base + i) * H + hh) * (int64_t)d;
+        double mx = -INFINITY;
+        for (int64_t j = 0; j < nv; ++j) {
+            const double *kk = k + ((base + j) * H + hh) * (int64_t)d;
+            double acc = 0.0;
+            for (int c = 0; c < d; ++c)
+                acc += qi[c] * kk[c];
+            sc[j] = scale * acc;
+            if (sc[j] > mx)
+                mx = sc[j];
+        }
+        double z = 0.0;
+        for (int64_t j = 0; j < nv; ++j)
+            z += exp(sc[j] - mx);
+        double *orow = o + r * (int64_t)d;
+        for (int c = 0; c < d; ++c)
+            orow[c] = 0.0;
+        for (int64_t j = 0; j < nv; ++j) {
+            const double w = exp(sc[j] - mx) / z;
+            const double *vv = v + ((base + j) * H + hh) * (int64_t)d;
+            for (int c = 0; c < d; ++c)
+                orow[c] += w * vv[c];
+        }
+        lse[r] = mx + log(z);
+    }
+    free(sc);
     return st;
 }

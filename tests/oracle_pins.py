@@ -17,7 +17,11 @@ disagrees with:
   - causal masking: the last row of a causal sequence sees every key;
   - gradients (dQ, dK, dV): central finite differences of sum(dO * O), torch
     autograd through SDPA in fp64, the sum rules (sum of dV = sum of dO, sum
-    of dK = 0), constant V (no dQ, dK), dO = 0, and packing.
+    of dK = 0), constant V (no dQ, dK), dO = 0, and packing;
+  - FP8: e4m3 decoding from the bit fields and encoding by exhaustive
+    nearest search, the fp32 Hadamard butterflies against scipy's Hadamard
+    matrix, block scales and codes against the exhaustive encoder, and the
+    fp64-input attention against the bf16-input one.
 The mutation tests run the same checks against deliberately broken copies of
 the oracle and require each copy to fail at least one of them.
 """
@@ -435,6 +439,128 @@ def check_bwd_packing(orc):
                 _close((dq, dk, dv)[t][n], g[t][0], 1e-13, f"packed gradient {'QKV'[t]}")
 
 
+# ---------------------------------------------------------------- FP8 --
+
+def _e4m3_table():
+    """Every finite e4m3 value from its bit fields (sign, 4-bit exponent with
+    bias 7, 3-bit mantissa; exponent 15 with mantissa 7 is NaN)."""
+    vals = {}
+    for c in range(256):
+        sgn = -1.0 if c & 0x80 else 1.0
+        e, m = (c >> 3) & 15, c & 7
+        if e == 15 and m == 7:
+            continue
+        vals[c] = sgn * (m * 2.0 ** -9 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7))
+    return vals
+
+
+def check_e4m3_brute_force(orc):
+    """Decoding matches the bit fields; encoding is the nearest finite value
+    by exhaustive search (ties to the even code, beyond 448 saturating)."""
+    table = _e4m3_table()
+    codes = np.array(sorted(table), dtype=np.uint8)
+    _close(orc.e4m3_decode(codes), [table[c] for c in codes], 0.0, "e4m3 decode")
+    assert math.isnan(orc.e4m3_decode([0x7f])[0]) and math.isnan(orc.e4m3_decode([0xff])[0])
+    assert table[0x7e] == 448.0 and table[0x08] == 2.0 ** -6 and table[0x01] == 2.0 ** -9
+    pos = sorted((v, c) for c, v in table.items() if v >= 0 and c != 0x80)
+    bits = inputs.splitmix64(1515, 0, 4000)
+    xs = list(((bits >> np.uint64(40)).astype(np.float64) / 2.0 ** 24 - 0.5) * 1100.0)
+    xs += [v for v, _ in pos] + [(pos[i][0] + pos[i + 1][0]) / 2 for i in range(len(pos) - 1)]
+    xs += [1e-12, 2.0 ** -10, 447.9, 448.0, 463.9, 464.0, 1e6]
+    xs = np.array([np.float32(x) for x in xs] + [-np.float32(x) for x in xs], dtype=np.float32)
+    got = orc.e4m3_encode(xs)
+    for x, c in zip(xs, got):
+        a = abs(float(x))
+        best = min(pos, key=lambda vc: (abs(vc[0] - a), vc[1] & 1))  # nearest, then even code
+        want = best[1] if a < 448.0 else 0x7e
+        if x < 0 and not (want == 0 and a < 2.0 ** -10 + 0.0):
+            want |= 0x80
+        if want & 0x7f == 0:  # +-0: either sign bit
+            assert c & 0x7f == 0, f"e4m3({x}) = {c:#x}, want zero"
+            continue
+        assert c == want, f"e4m3({x}) = {c:#x}, want {want:#x}"
+
+
+def check_fwht(orc):
+    """The fp32 butterflies equal (x * signs) H_d with H_d from scipy (the
+    Sylvester construction): exactly on small integers (every partial sum is
+    exact in fp32), within fp32 rounding on normal draws; H_d H_d = d I."""
+    from scipy.linalg import hadamard
+    for d in (8, 64, 128):
+        Hd = hadamard(d).astype(np.float64)
+        signs = np.where(inputs.splitmix64(1616 + d, 0, d) & np.uint64(1), -1, 1).astype(np.int8)
+        ints = ((inputs.splitmix64(1617 + d, 0, 4 * d) % np.uint64(201)).astype(np.float64) - 100).reshape(4, d)
+        got = orc.fwht_f32(ints, signs)
+        _close(got, (ints * signs) @ Hd, 0.0, f"integer Hadamard d={d}")
+        x = inputs.bf16_bits_to_f64(inputs.normal_bf16(1618 + d, 8 * d)).reshape(8, d)
+        got = orc.fwht_f32(x, signs).astype(np.float64)
+        ref = (x * signs) @ Hd
+        assert np.max(np.abs(got - ref)) <= 1e-5 * np.max(np.abs(ref)), f"fp32 Hadamard d={d}"
+        twice = orc.fwht_f32(orc.fwht_f32(x, None), None).astype(np.float64)
+        assert np.max(np.abs(twice - d * x)) <= 1e-4 * d * np.max(np.abs(x)), "H H = d I"
+
+
+def check_fp8_block_quantize(orc):
+    """Per-block scale = max|x| / 448 and codes = nearest e4m3 of x * (448 /
+    max|x|) (fp32), by exhaustive search; the last block of a ragged sequence
+    is pulled back and leaves the rows it shares to the block before it; with
+    rotation the block is that of the Hadamard-rotated rows."""
+    table = _e4m3_table()
+    pos = sorted((v, c) for c, v in table.items() if v >= 0 and c != 0x80)
+    grid = np.array([v for v, _ in pos])
+
+    def nearest(y):
+        a = np.abs(y.astype(np.float64))
+        idx = np.abs(a[..., None] - grid[None, :]).argmin(axis=-1)
+        # ties to the even code: if the next code is equally near and even, take it
+        nxt = np.minimum(idx + 1, len(grid) - 1)
+        tie = np.abs(a - grid[nxt]) == np.abs(a - grid[idx])
+        odd = np.array([pos[i][1] & 1 for i in range(len(pos))])[idx] == 1
+        idx = np.where(tie & odd & (nxt != idx), nxt, idx)
+        c = np.array([pos[i][1] for i in range(len(pos))], dtype=np.uint8)[idx]
+        return np.where((y < 0) & (c != 0), c | 0x80, c).astype(np.uint8)
+
+    B, N, H, d, rows = 2, 300, 2, 8, 128
+    x = inputs.normal_bf16(1717, B * N * H * d, 2.0).reshape(B * N, H, d)
+    xf = inputs.bf16_bits_to_f64(x).astype(np.float32)
+    for rotate in (False, True):
+        signs = np.array([1, -1, 1, 1, -1, -1, 1, -1], dtype=np.int8)
+        codes, scales = orc.fp8_quantize(x, B, N, rows, rotate, signs)
+        nblk = -(-N // rows)
+        assert scales.shape == (B, H, nblk)
+        for b in range(B):
+            for h in range(H):
+                for t in range(nblk):
+                    r0 = min(t * rows, N - rows)
+                    blk = xf[b * N + r0:b * N + r0 + rows, h]
+                    if rotate:
+                        blk = orc.fwht_f32(blk, signs)
+                    amax = np.float32(np.max(np.abs(blk)))
+                    assert scales[b, h, t] == np.float32(amax / np.float32(448.0)), "block scale"
+                    inv = np.float32(np.float32(448.0) / amax)
+                    want = nearest((blk * inv).astype(np.float32))
+                    keep = np.arange(r0, r0 + rows) >= t * rows
+                    got = codes[b * N + r0:b * N + r0 + rows, h][keep]
+                    assert np.array_equal(got, want[keep]), f"codes b={b} h={h} t={t} rotate={rotate}"
+
+
+def check_attn_rows_f64(orc):
+    """The fp64-input definition equals the bf16-input one on bf16 values."""
+    wl = _rand_workload(1818, [37, 5], H=2, d=8, std=1.5)
+    rows = inputs.all_rows(wl.cu_seqlens, wl.H)
+    f = lambda a: inputs.bf16_bits_to_f64(a)
+    for causal in (False, True):
+        o1, l1, _ = orc.attn_rows(wl.q, wl.k, wl.v, wl.cu_seqlens, rows, 0.4, causal, 1)
+        o2, l2 = orc.attn_rows_f64(f(wl.q), f(wl.k), f(wl.v), wl.cu_seqlens, rows, 0.4, causal)
+        _close(o2, o1, 1e-14, f"f64-input O causal={causal}")
+        _close(l2, l1, 1e-14, f"f64-input LSE causal={causal}")
+    # logits of several hundred: exp overflows fp64 without the true row max
+    o1, l1, _ = orc.attn_rows(wl.q, wl.k, wl.v, wl.cu_seqlens, rows, 400.0, False, 1)
+    o2, l2 = orc.attn_rows_f64(f(wl.q), f(wl.k), f(wl.v), wl.cu_seqlens, rows, 400.0, False)
+    _close(o2, o1, 1e-12, "f64-input O, large logits")
+    _close(l2, l1, 1e-12, "f64-input LSE, large logits")
+
+
 ALL_CHECKS = [
     check_brute_force_decimal,
     check_two_key_closed_form,
@@ -454,4 +580,8 @@ ALL_CHECKS = [
     check_bwd_torch_autograd,
     check_bwd_invariants,
     check_bwd_packing,
+    check_e4m3_brute_force,
+    check_fwht,
+    check_fp8_block_quantize,
+    check_attn_rows_f64,
 ]

@@ -53,6 +53,19 @@ MUTANTS = {
                        "acc += dorow[c] * widen_bf16(jb->k[((base + j) * H + h) * (int64_t)d + c]);")],
     "bwd_unnormalised_p": [("p[j] = exp(p[j] - m) / l;\n        /* dP_ij", "p[j] = exp(p[j] - m);\n        /* dP_ij")],
     "bwd_one_worker_summed": [("sk += jobs[t].dk[x];", "sk = jobs[t].dk[x];")],
+    # FP8
+    "e4m3_ties_away": [("if (frac > 0.5 || (frac == 0.5 && fmod(n, 2.0) == 1.0))",
+                        "if (frac >= 0.5)")],
+    "e4m3_no_saturation": [("    if (a >= 448.0)\n        return sign | 0x7e;", "    if (a >= 480.0)\n        return sign | 0x7f;")],
+    "e4m3_bias_off_by_one": [("double v = e == 0 ? ldexp((double)m, -9) : ldexp(8.0 + m, e - 10);",
+                              "double v = e == 0 ? ldexp((double)m, -9) : ldexp(8.0 + m, e - 9);")],
+    "fwht_last_stage_skipped": [("for (int h = 1; h < d; h <<= 1)", "for (int h = 1; h < d / 2; h <<= 1)")],
+    "fwht_signs_ignored": [("x[c] = signs[c] < 0 ? -x[c] : x[c];", "x[c] = x[c];")],
+    "quant_scale_inverted": [("const float inv = amax > 0.0f ? 448.0f / amax : 1.0f;",
+                              "const float inv = amax > 0.0f ? amax / 448.0f : 1.0f;")],
+    "quant_tail_overwrites_shared_rows": [("if (row < nominal || row < 0)", "if (row < 0)")],
+    "attn_f64_no_max": [("            if (sc[j] > mx)\n                mx = sc[j];\n        }\n        double z",
+                         "            if (j == 0)\n                mx = sc[j];\n        }\n        double z")],
 }
 
 
