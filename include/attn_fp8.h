@@ -1,0 +1,68 @@
+/*
+ * C ABI of the GB300 (sm_103a) FP8 attention forward (e4m3, d = 128).
+ *
+ * The FP8 path of the pages ("flash-attention-evolution" (letsgetai),
+ * FlashAttention-3 section, item 3; "FlashAttention 1-4 演进速查"
+ * (argus-lessons), FlashAttention-3 items) quantises the operands to 8-bit
+ * floats and controls the error with block quantisation and incoherent
+ * processing.  Read here as:
+ *   - incoherent processing: Q and K are multiplied along d by the same
+ *     orthogonal matrix diag(signs) H_d / sqrt(d) (H_d Sylvester-Hadamard,
+ *     signs a caller-supplied +-1 vector), which leaves Q K^T unchanged;
+ *   - block quantisation: e4m3 codes (round to nearest even, saturating at
+ *     448), one fp32 scale per block: per 128-row tile and head for Q and K,
+ *     per sequence and head for V; a block's max |x| maps to 448.
+ * P is quantised as e4m3(256 P) before the P V product; fp32 accumulation.
+ * This is an approximation of the exact attention of attn_fwd.h.
+ *
+ * Dense batches only: q, k, v, o [B, N, H, 128] bf16, lse [B, H, N] fp32.
+ * Same conventions as attn_fwd.h (device pointers, asynchronous on stream,
+ * status codes, error word); d other than 128 returns ATTN_ERR_HEADDIM.
+ */
+#ifndef IO_AWARE_EXACT_06_ATTN_FP8_H
+#define IO_AWARE_EXACT_06_ATTN_FP8_H
+
+#include <stdint.h>
+
+#include "attn_fwd.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * attn_fp8_quantize_qk: the Q or K quantisation step.  x [B, N, H, 128] bf16
+ * (device); codes [B, N, H, 128] e4m3 (uint8, device); scales [B, H, T] fp32
+ * (device), T = ceil(N / 128): block t holds rows [128 t, 128 t + 128) of a
+ * sequence and head, the last block pulled back to end at N (the rows it
+ * shares with block t - 1 keep that block's codes).  signs: host array of 128
+ * int8 (+1 / -1) for the rotation, or NULL for no rotation.  N >= 1.
+ */
+int attn_fp8_quantize_qk(const void *x, uint8_t *codes, float *scales, int B, int H, int N,
+                         int d, const int8_t *signs, attn_stream_t stream);
+
+/*
+ * attn_fp8_quantize_v: the V quantisation step.  v [B, N, H, 128] bf16;
+ * codes_t [B, H, 128, Np] e4m3 with Np = 128 * ceil(N / 128): the codes
+ * transposed per sequence and head (keys contiguous), keys >= N zero; scale
+ * [B, H] fp32 (max |V| / 448 of the sequence and head).  N >= 1.
+ */
+int attn_fp8_quantize_v(const void *v, uint8_t *codes_t, float *scale, int B, int H, int N,
+                        int d, attn_stream_t stream);
+
+/*
+ * attn_fwd_fp8: O = softmax(scale * Q K^T) V and the LSE through the FP8 path
+ * above (quantisation kernels, then the FP8 attention kernel).  scale: finite
+ * and >= 0; causal as in attn_fwd.  signs: as for attn_fp8_quantize_qk.  The
+ * library keeps a per-(device, stream) workspace for the codes and scales
+ * (about 4 * B * N * H * 128 bytes), grown on demand.
+ */
+int attn_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                 int N, int d, float scale, int causal, const int8_t *signs,
+                 attn_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IO_AWARE_EXACT_06_ATTN_FP8_H */

@@ -36,7 +36,7 @@ typedef enum {
     ATTN_ERR_SHAPE = -2,          /* B, H or N negative or too large */
     ATTN_ERR_HEADDIM = -3,        /* d is not 64 or 128 */
     ATTN_ERR_ALIGN = -4,          /* q/k/v/o not 16-byte or lse not 4-byte aligned */
-    ATTN_ERR_SCALE = -5,          /* scale is not finite */
+    ATTN_ERR_SCALE = -5,          /* scale is negative or not finite */
     ATTN_ERR_CUDA = -6,           /* a CUDA runtime call or launch failed */
     ATTN_ERR_DEVICE_TIMEOUT = -7, /* a bounded device-side wait expired */
     ATTN_ERR_SEQLENS = -8,        /* cu_seqlens not increasing from 0, or a length > N */
@@ -56,7 +56,7 @@ typedef enum {
  *   device memory and is validated on the device (see attn_last_device_error).
  *   Zero-length sequences are allowed.
  * q, k, v: read only.  o, lse: written for every valid row, nothing else.
- * d: 64 or 128.  scale: any finite value (1/sqrt(d) for the usual attention).
+ * d: 64 or 128.  scale: finite and >= 0 (1/sqrt(d) for the usual attention).
  * causal: nonzero means key j is visible to query i iff j <= i (within each
  *   sequence); zero means every key of the sequence is visible.
  * Alignment: q, k, v, o 16-byte aligned; lse 4-byte aligned.

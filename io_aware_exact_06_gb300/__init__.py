@@ -1,7 +1,7 @@
 """GB300 (sm_103a) fused exact attention: forward and backward.
 
-A thin ctypes binding of the C ABI in ``include/attn_fwd.h`` and
-``include/attn_bwd.h`` (the library
+A thin ctypes binding of the C ABI in ``include/attn_fwd.h``,
+``include/attn_bwd.h`` and ``include/attn_fp8.h`` (the library
 ``_build/libattn_fwd.so``, built by ``build.py``).  The functions here only
 marshal arguments: every step of the computation runs in the library's CUDA
 kernels.  There is no CPU path: calling the library without it built, or on a
@@ -14,14 +14,16 @@ import os
 
 from . import build as _build
 
-__all__ = ["attn_fwd", "attn_bwd", "attn_fwd_ex", "attn_fwd_noalloc", "attn_fwd_window", "attn_fwd_kvsplit", "attn_last_device_error", "attn_last_error_site",
+__all__ = ["attn_fwd", "attn_bwd", "attn_fwd_fp8", "attn_fp8_quantize_qk", "attn_fp8_quantize_v",
+           "attn_fwd_ex", "attn_fwd_noalloc", "attn_fwd_window", "attn_fwd_kvsplit", "attn_last_device_error", "attn_last_error_site",
            "attn_status_string", "AttnError", "AttnFwdOptions", "lib", "forward",
            "EXPORTED_SYMBOLS"]
 
 # Every symbol the headers under include/ declare.
 EXPORTED_SYMBOLS = ("attn_fwd", "attn_fwd_ex", "attn_last_device_error", "attn_last_error_site",
                     "attn_last_cuda_error", "attn_status_string", "attn_fwd_noalloc",
-                    "attn_fwd_window", "attn_fwd_kvsplit", "attn_bwd")
+                    "attn_fwd_window", "attn_fwd_kvsplit", "attn_bwd", "attn_fwd_fp8",
+                    "attn_fp8_quantize_qk", "attn_fp8_quantize_v")
 
 ATTN_OK = 0
 
@@ -63,6 +65,12 @@ def lib() -> ctypes.CDLL:
         L.attn_fwd_kvsplit.restype = i
         L.attn_bwd.argtypes = [vp] * 9 + [i, i, i, i, ctypes.c_float, i, vp, vp]
         L.attn_bwd.restype = i
+        L.attn_fwd_fp8.argtypes = sig[:11] + [vp, vp]
+        L.attn_fwd_fp8.restype = i
+        L.attn_fp8_quantize_qk.argtypes = [vp, vp, vp, i, i, i, i, vp, vp]
+        L.attn_fp8_quantize_qk.restype = i
+        L.attn_fp8_quantize_v.argtypes = [vp, vp, vp, i, i, i, i, vp]
+        L.attn_fp8_quantize_v.restype = i
         L.attn_fwd_noalloc.argtypes = sig
         L.attn_fwd_noalloc.restype = i
         L.attn_last_device_error.argtypes = [vp]
@@ -163,6 +171,50 @@ def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B: int, H: int, N: int, d: int, 
                         int(bool(causal)), _ptr(cu_seqlens), _stream(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_bwd")
+    return st
+
+
+def _signs(signs):
+    """A host int8[128] sign vector (kept alive by the caller) or None."""
+    if signs is None:
+        return None, None
+    import numpy as np
+    arr = np.ascontiguousarray(signs, dtype=np.int8)
+    if arr.shape != (128,):
+        raise ValueError("signs must hold 128 entries of +1 / -1")
+    return arr, arr.ctypes.data
+
+
+def attn_fwd_fp8(q, k, v, o, lse, B: int, H: int, N: int, d: int, scale: float, causal: bool,
+                 signs=None, stream=None) -> int:
+    """The C call ``attn_fwd_fp8`` (e4m3 path; signs: 128 x +-1 or None)."""
+    keep, sp = _signs(signs)
+    st = lib().attn_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(N),
+                            int(d), float(scale), int(bool(causal)), sp, _stream(stream))
+    del keep
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_fp8")
+    return st
+
+
+def attn_fp8_quantize_qk(x, codes, scales, B: int, H: int, N: int, d: int, signs=None,
+                         stream=None) -> int:
+    """The C call ``attn_fp8_quantize_qk``."""
+    keep, sp = _signs(signs)
+    st = lib().attn_fp8_quantize_qk(_ptr(x), _ptr(codes), _ptr(scales), int(B), int(H), int(N),
+                                    int(d), sp, _stream(stream))
+    del keep
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fp8_quantize_qk")
+    return st
+
+
+def attn_fp8_quantize_v(v, codes_t, scale, B: int, H: int, N: int, d: int, stream=None) -> int:
+    """The C call ``attn_fp8_quantize_v``."""
+    st = lib().attn_fp8_quantize_v(_ptr(v), _ptr(codes_t), _ptr(scale), int(B), int(H), int(N),
+                                   int(d), _stream(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fp8_quantize_v")
     return st
 
 

@@ -106,7 +106,7 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
                         attn_stream_t stream) {
   if (B < 0 || H < 0 || N < 0) return ATTN_ERR_SHAPE;
   if (d != 64 && d != 128) return ATTN_ERR_HEADDIM;
-  if (!std::isfinite(scale)) return ATTN_ERR_SCALE;
+  if (!std::isfinite(scale) || scale < 0.0f) return ATTN_ERR_SCALE;
   if (cu_seqlens) return ATTN_ERR_SHAPE;
   if (B == 0 || H == 0 || N == 0) return ATTN_OK;
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return ATTN_ERR_NULL;

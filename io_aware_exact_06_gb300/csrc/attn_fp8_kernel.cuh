@@ -1,0 +1,694 @@
+// FP8 (e4m3) fused attention forward for sm_103a, d = 128, dense batches.
+//
+// The pages name the FP8 path's two devices without formulas: block
+// quantisation and incoherent processing ("flash-attention-evolution"
+// (letsgetai), FlashAttention-3 section, item 3; "FlashAttention 1-4 演进速查"
+// (argus-lessons), FlashAttention-3 items).  This build reads them as:
+//   - incoherent processing: Q and K are multiplied along d by the same
+//     orthogonal matrix diag(signs) H_d / sqrt(d) (H_d Sylvester-Hadamard), so
+//     Q K^T is unchanged while outliers of single channels spread over all d;
+//     the transform is applied unnormalised (fp32 butterflies) and its 1/d
+//     goes into the logit scale;
+//   - block quantisation: one scale per 128-row tile and head for Q and K (the
+//     tiles the tensor core multiplies), one per sequence and head for V (its
+//     scale then factors out of the P V sum); a block's max |x| maps to 448,
+//     the largest finite e4m3 value.
+// P = 2^(x - m) <= 2^0.5 is stored as e4m3 of 256 P (the normal e4m3 range then
+// reaches 2^-14), the running max moving whenever it grows by more than 0.5
+// (log2 units), so 256 P stays below 448.
+//
+// Kernels:
+//   fp8_quant_qk_kernel   rotation + block quantisation of Q or K, one CTA per
+//                         (sequence, head, 128-row block), two passes (the
+//                         block max, then the codes)
+//   fp8_amax_v_kernel     max |V| per (sequence, head) (atomic max of the
+//                         non-negative fp32 bit patterns)
+//   fp8_quant_v_kernel    V codes, stored transposed per (sequence, head):
+//                         [d][keys padded to 128] (keys contiguous), so both
+//                         products of the attention kernel take K-major
+//                         operands
+//   attn_fp8_kernel       the forward pass: the bf16 kernel's schedule and warp
+//                         roles (persistent CTAs, longest-first units of two
+//                         128-row query tiles, producer / MMA / 16 softmax
+//                         warps, P in TMEM over its S), tcgen05.mma of
+//                         kind::f8f6f4, K tiles not pulled back (keys past the
+//                         sequence are masked).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cstdint>
+
+#include "attn_fwd_kernel.cuh"
+
+namespace attn {
+
+constexpr int kFp8D = 128;
+constexpr int kFp8TileBytes = kBM * kFp8D;   // 128 rows x 128 e4m3 = one 128-byte swizzle span
+constexpr int kFp8Stages = 8;                // K / V ring slots
+constexpr int kFp8SmemBytes = kQTiles * kFp8TileBytes + kFp8Stages * kFp8TileBytes + 1024;
+constexpr float kFp8Max = 448.0f;
+constexpr float kFp8PScale = 256.0f;         // P is stored as e4m3(256 P)
+constexpr float kFp8RescaleLog2 = 0.5f;
+
+// Instruction descriptor of tcgen05.mma kind::f8f6f4, e4m3 A and B, fp32 D,
+// both operands K-major: [4,6) D format (1 = f32), [7,10) A format (0 =
+// e4m3), [10,13) B format (0 = e4m3), [17,23) N >> 3, [24,29) M >> 4.
+__host__ __device__ constexpr uint32_t make_idesc_e4m3(uint32_t M, uint32_t N) {
+  return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+constexpr uint32_t kIdescFp8 = make_idesc_e4m3(kBM, kBN);
+
+__device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      "  .reg .pred p;\n"
+      "  setp.ne.b32 p, %4, 0;\n"
+      "  tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      "  .reg .pred p;\n"
+      "  setp.ne.b32 p, %4, 0;\n"
+      "  tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+struct Fp8Params {
+  __nv_bfloat16* o;     // [B*N, H, 128]
+  float* lse;           // [B, H, N]
+  const float* sq;      // [B*H][T]: Q block scales
+  const float* sk;      // [B*H][T]: K block scales
+  const float* sv;      // [B*H]: V scale
+  int* err;
+  int* sched;
+  int B, H, N, T;
+  int causal;
+  float logit_log2;     // scale * log2(e) / d (the transform's 1/d folded in)
+  float scale;
+  unsigned long long timeout_ns;
+};
+
+// Sign vector of the transform, one bit per channel (1: negate).
+struct Fp8Signs {
+  uint32_t bits[4];
+};
+
+// ----------------------------------------------------------- quantisers --
+// (x * signs) H_128 of the 128 values held 4 per lane (lane l: channels
+// 4l..4l+3), fp32 butterflies over strides 1, 2 (in the lane) and 4..64
+// (across lanes): the lower element of a pair becomes a + b, the upper a - b.
+__device__ __forceinline__ void fwht128_warp(float (&v)[4], int lane) {
+  float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
+  v[0] = a0 + a2;
+  v[1] = a1 + a3;
+  v[2] = a0 - a2;
+  v[3] = a1 - a3;
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const bool upper = lane & m;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float other = __shfl_xor_sync(0xffffffffu, v[j], m);
+      v[j] = upper ? other - v[j] : v[j] + other;
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return lo | (hi << 16);
+}
+
+// One CTA (8 warps) per (sequence, head, 128-row block); the last block of a
+// sequence is pulled back to end at N and leaves the rows it shares with the
+// block before it to that block.
+__global__ void __launch_bounds__(256)
+fp8_quant_qk_kernel(const __nv_bfloat16* x, uint8_t* codes, float* scales, int B, int H, int N,
+                    int T, Fp8Signs signs, int rotate) {
+  __shared__ float warp_max[8];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int t = blockIdx.x % T;
+  const int bh = blockIdx.x / T;
+  const int b = bh / H, h = bh % H;
+  const int r0 = min(t * kBM, N - kBM);
+  float sgn[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int c = 4 * lane + j;
+    sgn[j] = rotate && ((signs.bits[c / 32] >> (c % 32)) & 1u) ? -1.0f : 1.0f;
+  }
+  auto load_row = [&](int row, float (&v)[4]) {
+    if (row >= 0) {
+      const uint2 w = *reinterpret_cast<const uint2*>(x + (((size_t)b * N + row) * H + h) * kFp8D +
+                                                      4 * lane);
+      const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&w.x);
+      const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&w.y);
+      v[0] = __bfloat162float(p0.x) * sgn[0];
+      v[1] = __bfloat162float(p0.y) * sgn[1];
+      v[2] = __bfloat162float(p1.x) * sgn[2];
+      v[3] = __bfloat162float(p1.y) * sgn[3];
+      if (rotate) fwht128_warp(v, lane);
+    } else {
+      v[0] = v[1] = v[2] = v[3] = 0.f;
+    }
+  };
+  float amax = 0.f;
+  for (int r = warp; r < kBM; r += 8) {
+    float v[4];
+    load_row(r0 + r, v);
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))));
+  }
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+  if (lane == 0) warp_max[warp] = amax;
+  __syncthreads();
+  amax = warp_max[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) amax = fmaxf(amax, warp_max[w]);
+  const float inv = amax > 0.f ? __fdiv_rn(kFp8Max, amax) : 1.0f;
+  if (threadIdx.x == 0) scales[blockIdx.x] = amax > 0.f ? __fdiv_rn(amax, kFp8Max) : 1.0f;
+  for (int r = warp; r < kBM; r += 8) {
+    const int row = r0 + r;
+    if (row < t * kBM) continue;  // the previous block's row (or before the sequence)
+    float v[4];
+    load_row(row, v);
+    *reinterpret_cast<uint32_t*>(codes + (((size_t)b * N + row) * H + h) * kFp8D + 4 * lane) =
+        e4m3x4(__fmul_rn(v[0], inv), __fmul_rn(v[1], inv), __fmul_rn(v[2], inv),
+               __fmul_rn(v[3], inv));
+  }
+}
+
+// amax[b*H + h] = max |V| over the sequence (bit patterns of non-negative
+// floats order like the floats).  One CTA per (sequence, head, 128 rows).
+__global__ void __launch_bounds__(256)
+fp8_amax_v_kernel(const __nv_bfloat16* v, unsigned int* amax_bits, int B, int H, int N, int T) {
+  __shared__ float warp_max[8];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int t = blockIdx.x % T;
+  const int bh = blockIdx.x / T;
+  const int b = bh / H, h = bh % H;
+  float m = 0.f;
+  for (int r = warp; r < kBM; r += 8) {
+    const int row = t * kBM + r;
+    if (row >= N) break;
+    const uint2 w = *reinterpret_cast<const uint2*>(v + (((size_t)b * N + row) * H + h) * kFp8D +
+                                                    4 * lane);
+    const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&w.x);
+    const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&w.y);
+    m = fmaxf(m, fmaxf(fmaxf(fabsf(__bfloat162float(p0.x)), fabsf(__bfloat162float(p0.y))),
+                       fmaxf(fabsf(__bfloat162float(p1.x)), fabsf(__bfloat162float(p1.y)))));
+  }
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
+  if (lane == 0) warp_max[warp] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int w = 1; w < 8; ++w) m = fmaxf(m, warp_max[w]);
+    atomicMax(amax_bits + bh, __float_as_uint(m));
+  }
+}
+
+// V codes, transposed: vt[(b*H + h) * 128 + c][key] for keys padded to Np
+// (a multiple of 128; padding keys get code 0).  Also writes the V scale.
+// One CTA per (sequence, head, 128 keys).
+__global__ void __launch_bounds__(256)
+fp8_quant_v_kernel(const __nv_bfloat16* v, const unsigned int* amax_bits, float* sv, uint8_t* vt,
+                   int B, int H, int N, int Np) {
+  __shared__ uint8_t tile[kFp8D][kBN + 16];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int T = Np / kBN;
+  const int t = blockIdx.x % T;
+  const int bh = blockIdx.x / T;
+  const int b = bh / H, h = bh % H;
+  const float amax = __uint_as_float(amax_bits[bh]);
+  const float inv = amax > 0.f ? __fdiv_rn(kFp8Max, amax) : 1.0f;
+  if (t == 0 && threadIdx.x == 0) sv[bh] = amax > 0.f ? __fdiv_rn(amax, kFp8Max) : 1.0f;
+  for (int r = warp; r < kBN; r += 8) {
+    const int key = t * kBN + r;
+    float f[4] = {0.f, 0.f, 0.f, 0.f};
+    if (key < N) {
+      const uint2 w = *reinterpret_cast<const uint2*>(v + (((size_t)b * N + key) * H + h) * kFp8D +
+                                                      4 * lane);
+      const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&w.x);
+      const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&w.y);
+      f[0] = __bfloat162float(p0.x);
+      f[1] = __bfloat162float(p0.y);
+      f[2] = __bfloat162float(p1.x);
+      f[3] = __bfloat162float(p1.y);
+    }
+    const uint32_t c4 = e4m3x4(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv), __fmul_rn(f[2], inv),
+                               __fmul_rn(f[3], inv));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) tile[4 * lane + j][r] = (uint8_t)(c4 >> (8 * j));
+  }
+  __syncthreads();
+  // 128 rows (channels) x 128 keys, 16 bytes per thread-store
+  for (int i = threadIdx.x; i < kFp8D * (kBN / 16); i += 256) {
+    const int c = i / (kBN / 16), q = i % (kBN / 16);
+    uint4 w;
+    uint8_t* src = &tile[c][q * 16];
+    w.x = src[0] | (src[1] << 8) | (src[2] << 16) | ((uint32_t)src[3] << 24);
+    w.y = src[4] | (src[5] << 8) | (src[6] << 16) | ((uint32_t)src[7] << 24);
+    w.z = src[8] | (src[9] << 8) | (src[10] << 16) | ((uint32_t)src[11] << 24);
+    w.w = src[12] | (src[13] << 8) | (src[14] << 16) | ((uint32_t)src[15] << 24);
+    *reinterpret_cast<uint4*>(vt + ((size_t)bh * kFp8D + c) * Np + t * kBN + q * 16) = w;
+  }
+}
+
+// ------------------------------------------------------------ attention --
+// S = Q K^T over 4 k-steps of 32 e4m3: both operands K-major, 128-byte
+// swizzle, one 128-byte span per row; a k-step advances the start by 32 bytes.
+__device__ __forceinline__ void issue_qk_fp8(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+  const uint64_t a0 = make_sdesc(q_smem, 16, 1024, kSwizzle128B);
+  const uint64_t b0 = make_sdesc(k_smem, 16, 1024, kSwizzle128B);
+#pragma unroll
+  for (int kk = 0; kk < kFp8D / 32; ++kk)
+    mma_f8_ss(d_tmem, a0 + (uint64_t)(kk * 2), b0 + (uint64_t)(kk * 2), kIdescFp8, kk > 0 ? 1u : 0u);
+}
+
+// O (+)= P V over 4 k-steps of 32 keys: P (e4m3, four per TMEM column, keys
+// 32 kk.. in columns 8 kk..) and V^T (128 channels x 128 keys, K-major).
+__device__ __forceinline__ void issue_pv_fp8(uint32_t d_tmem, uint32_t p_tmem, uint32_t vt_smem,
+                                             bool accumulate) {
+  const uint64_t b0 = make_sdesc(vt_smem, 16, 1024, kSwizzle128B);
+  const uint32_t acc0 = accumulate ? 1u : 0u;
+#pragma unroll
+  for (int kk = 0; kk < kBN / 32; ++kk)
+    mma_f8_ts(d_tmem, p_tmem + 8 * kk, b0 + (uint64_t)(kk * 2), kIdescFp8, kk > 0 ? 1u : acc0);
+}
+
+__device__ __forceinline__ bool fp8_wait(SharedState& ss, int bar, uint32_t parity,
+                                         const Fp8Params& p, int where) {
+  const uint32_t a = bar_addr(ss, bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (mbar_try_wait(a, parity)) return true;
+    if (ss.abort_flag) return false;
+    if (globaltimer_ns() - t0 > p.timeout_ns) {
+      ss.abort_flag = 1;
+      atomicOr(p.err, kErrTimeout);
+      atomicCAS(p.err + 1, 0, where);
+      return false;
+    }
+  }
+}
+
+// Unit u: rows [256 qb, +256) of head h of sequence b; KV tiles [0, nkv).
+struct Fp8Unit {
+  int b, h, qb, nkv;
+};
+
+__device__ __forceinline__ Fp8Unit fp8_unit(const Fp8Params& p, int u) {
+  Fp8Unit un;
+  const int e = u / p.H;
+  un.h = u - e * p.H;
+  const int nqb = (p.N + kUnitRows - 1) / kUnitRows;
+  const int rank = e / p.B;
+  un.b = e - rank * p.B;
+  un.qb = nqb - 1 - rank;
+  const int r_hi = min(un.qb * kUnitRows + kUnitRows, p.N) - 1;
+  un.nkv = (p.causal ? r_hi : p.N - 1) / kBN + 1;
+  return un;
+}
+
+__device__ __forceinline__ int fp8_q_start(const Fp8Params& p, const Fp8Unit& un, int g) {
+  return min(un.qb * kUnitRows + g * kBM, p.N - kBM);
+}
+
+__device__ __forceinline__ void fp8_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                                             const CUtensorMap* tm_vt, const Fp8Params& p,
+                                             SharedState& ss, uint8_t* sQ, uint8_t* sRing,
+                                             int n_units) {
+  uint32_t ring = 0, uslot = 0;
+  int units_done = 0;
+  int u = blockIdx.x;
+  for (;;) {
+    if (u >= n_units) u = -1;
+    {
+      const int slot = uslot % kUnitSlots;
+      const uint32_t n = uslot / kUnitSlots;
+      if (n > 0 && !fp8_wait(ss, kBarUnitEmpty + slot, (n - 1) & 1, p, 203)) return;
+      ss.unit_ring[slot] = u;
+      mbar_arrive(bar_addr(ss, kBarUnitFull + slot));
+      ++uslot;
+    }
+    if (u < 0) return;
+    const int next_u = (int)gridDim.x + atomicAdd(p.sched, 1);
+    const Fp8Unit un = fp8_unit(p, u);
+    if (units_done > 0 && !fp8_wait(ss, kBarQEmpty, (units_done - 1) & 1, p, 201)) return;
+    mbar_arrive_expect_tx(bar_addr(ss, kBarQFull), kQTiles * kFp8TileBytes);
+    for (int g = 0; g < kQTiles; ++g)
+      tma_load_3d(smem_u32(sQ + g * kFp8TileBytes), tm_q, bar_addr(ss, kBarQFull), 0, un.h,
+                  un.b * p.N + fp8_q_start(p, un, g));
+    for (int j = 0; j < un.nkv; ++j) {
+      for (int kind = 0; kind < 2; ++kind) {
+        const int slot = ring % kFp8Stages;
+        const uint32_t n = ring / kFp8Stages;
+        if (n > 0 && !fp8_wait(ss, kBarKV + kFp8Stages + slot, (n - 1) & 1, p, 202)) return;
+        const uint32_t full = bar_addr(ss, kBarKV + slot);
+        mbar_arrive_expect_tx(full, kFp8TileBytes);
+        const uint32_t dst = smem_u32(sRing + slot * kFp8TileBytes);
+        if (kind == 0)
+          tma_load_3d(dst, tm_k, full, 0, un.h, un.b * p.N + j * kBN);
+        else
+          tma_load_3d(dst, tm_vt, full, j * kBN, 0, un.b * p.H + un.h);
+        ++ring;
+      }
+    }
+    ++units_done;
+    u = next_u;
+  }
+}
+
+__device__ __forceinline__ bool fp8_next_unit(SharedState& ss, const Fp8Params& p,
+                                              uint32_t& uslot, bool whole_warp, int& u) {
+  const int slot = uslot % kUnitSlots;
+  bool ok = fp8_wait(ss, kBarUnitFull + slot, (uslot / kUnitSlots) & 1, p, 230);
+  if (whole_warp) ok = __all_sync(0xffffffffu, ok);
+  if (!ok) return false;
+  u = ss.unit_ring[slot];
+  if (whole_warp) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar_addr(ss, kBarUnitEmpty + slot));
+  } else {
+    mbar_arrive(bar_addr(ss, kBarUnitEmpty + slot));
+  }
+  ++uslot;
+  return true;
+}
+
+__device__ __forceinline__ void fp8_mma_loop(const Fp8Params& p, SharedState& ss, uint8_t* sQ,
+                                             uint8_t* sRing, uint32_t tmem) {
+  uint32_t ring = 0;
+  uint32_t pcount[2] = {0, 0};
+  int units_done = 0;
+  const uint32_t q_smem[2] = {smem_u32(sQ), smem_u32(sQ + kFp8TileBytes)};
+  auto slot_smem = [&](uint32_t pos) { return smem_u32(sRing + (pos % kFp8Stages) * kFp8TileBytes); };
+  auto wait_full = [&](uint32_t pos) {
+    return fp8_wait(ss, kBarKV + pos % kFp8Stages, (pos / kFp8Stages) & 1, p, 210);
+  };
+  auto release = [&](uint32_t pos) { mma_commit(bar_addr(ss, kBarKV + kFp8Stages + pos % kFp8Stages)); };
+  // TMEM: S_g at 128 g (P_g over its first 32 columns), O_g at 256 + 128 g
+  uint32_t uslot = 0;
+  for (;;) {
+    int u;
+    if (!fp8_next_unit(ss, p, uslot, false, u) || u < 0) return;
+    const Fp8Unit un = fp8_unit(p, u);
+    if (!fp8_wait(ss, kBarQFull, units_done & 1, p, 211)) return;
+    tc_fence_after();
+    uint32_t posK = ring, posV = ring + 1;
+    ring += 2;
+    if (!wait_full(posK)) return;
+    tc_fence_after();
+    for (int g = 0; g < kQTiles; ++g) {
+      issue_qk_fp8(tmem + 128u * g, q_smem[g], slot_smem(posK));
+      mma_commit(bar_addr(ss, kBarSFull + g));
+    }
+    release(posK);
+    if (un.nkv == 1) mma_commit(bar_addr(ss, kBarQEmpty));
+    for (int j = 1; j <= un.nkv; ++j) {
+      const bool more = j < un.nkv;
+      uint32_t nextK = 0, nextV = 0;
+      if (more) {
+        nextK = ring;
+        nextV = ring + 1;
+        ring += 2;
+      }
+      if (!wait_full(posV)) return;
+      for (int g = 0; g < kQTiles; ++g) {
+        if (!fp8_wait(ss, kBarPFull + g, pcount[g] & 1, p, 212 + g)) return;
+        ++pcount[g];
+        tc_fence_after();
+        issue_pv_fp8(tmem + 256u + 128u * g, tmem + 128u * g, slot_smem(posV), j > 1);
+        if (g == kQTiles - 1) release(posV);
+        if (more) {
+          if (g == 0) {
+            if (!wait_full(nextK)) return;
+            tc_fence_after();
+          }
+          issue_qk_fp8(tmem + 128u * g, q_smem[g], slot_smem(nextK));
+          mma_commit(bar_addr(ss, kBarSFull + g));
+        } else {
+          mma_commit(bar_addr(ss, kBarOFull + g));
+        }
+      }
+      if (more) {
+        release(nextK);
+        if (j == un.nkv - 1) mma_commit(bar_addr(ss, kBarQEmpty));
+        posV = nextV;
+      }
+    }
+    ++units_done;
+  }
+}
+
+__device__ __forceinline__ void fp8_softmax_loop(const Fp8Params& p, SharedState& ss,
+                                                 uint32_t tmem, int g) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int quadrant = warp % 4;
+  const int half = (warp % kGroupWarps) / 4;         // which 64 key columns
+  const int trow = quadrant * 32 + lane;              // row of the tile = TMEM lane
+  const uint32_t lane_addr = tmem + ((uint32_t)(quadrant * 32) << 16);
+  const uint32_t colS = 128u * g + half * kHalfCols;
+  const uint32_t colP = 128u * g + half * 16u;        // 64 e4m3 = 16 columns
+  const uint32_t colO = 256u + 128u * g + half * 64u; // this thread's 64 O columns
+  uint32_t scount = 0, uslot = 0;
+  int units_done = 0;
+  int u = -1;
+  bool fail = !fp8_next_unit(ss, p, uslot, true, u);
+  if (pair_sync_check(g, quadrant, fail)) return;
+  for (;;) {
+    if (u < 0) return;
+    const Fp8Unit un = fp8_unit(p, u);
+    const int bh = un.b * p.H + un.h;
+    const int a0 = fp8_q_start(p, un, g);
+    const int row = a0 + trow;
+    const int nominal0 = un.qb * kUnitRows + g * kBM;
+    // the quantisation block of this query tile (the pulled-back last block
+    // when the tile is pulled back; rows it shares with the block before it
+    // are recomputed with the wrong scale here but never stored)
+    const float qfac = p.logit_log2 * p.sq[(size_t)bh * p.T + min(nominal0 / kBM, p.T - 1)];
+    const int khi = p.causal ? min(row, p.N - 1) : p.N - 1;  // this row's last visible key
+    float m_used = -INFINITY;  // running max of the log2-scaled logits (moved by > 0.5 only)
+    float l = 0.f;             // sum of the fp32 probabilities (this half)
+    for (int j = 0; j < un.nkv; ++j) {
+      fail |= !__all_sync(0xffffffffu, fp8_wait(ss, kBarSFull + g, scount & 1, p, 220 + g));
+      ++scount;
+      tc_fence_after();
+      float s[kHalfCols];
+      {
+        uint32_t r0[32], r1[32];
+        tmem_ld_x32(lane_addr + colS, r0);
+        tmem_ld_x32(lane_addr + colS + 32, r1);
+        tmem_ld_wait_x32(r0);
+        tmem_ld_wait_x32(r1);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          s[i] = __uint_as_float(r0[i]);
+          s[32 + i] = __uint_as_float(r1[i]);
+        }
+      }
+      // keys past the sequence (the tile is not pulled back) and, when
+      // causal, after the row
+      const int hi = khi - (j * kBN + half * kHalfCols);  // last visible column of this thread
+      if (__any_sync(0xffffffffu, hi < kHalfCols - 1)) {
+#pragma unroll
+        for (int c = 0; c < kHalfCols; ++c)
+          if (c > hi) s[c] = -INFINITY;
+      }
+      float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]);
+      float mx2 = fmaxf(s[4], s[5]), mx3 = fmaxf(s[6], s[7]);
+#pragma unroll
+      for (int c = 8; c < kHalfCols; c += 8) {
+        mx0 = max3(mx0, s[c], s[c + 1]);
+        mx1 = max3(mx1, s[c + 2], s[c + 3]);
+        mx2 = max3(mx2, s[c + 4], s[c + 5]);
+        mx3 = max3(mx3, s[c + 6], s[c + 7]);
+      }
+      const float mine = fmaxf(max3(mx0, mx1, mx2), mx3);
+      ss.row_max[j & 1][g][half][trow] = mine;
+      pair_sync(g, quadrant);  // (also orders both halves' S loads before any P store)
+      const float c2t = qfac * p.sk[(size_t)bh * p.T + j];  // log2 units per raw S unit
+      const float raw = fmaxf(mine, ss.row_max[j & 1][g][half ^ 1][trow]);
+      const float m_new = fmaxf(m_used, raw == -INFINITY ? -INFINITY : raw * c2t);
+      float alpha = 1.0f;
+      bool resc = false;
+      if (m_used == -INFINITY) {
+        m_used = m_new;
+      } else if (m_new - m_used > kFp8RescaleLog2) {
+        resc = true;
+        alpha = ex2_approx(m_used - m_new);
+        m_used = m_new;
+      }
+      const bool rescale_warp = __any_sync(0xffffffffu, resc);
+      const float neg = m_used == -INFINITY ? 0.f : -m_used;
+      float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
+      uint32_t pw[16];
+#pragma unroll
+      for (int c = 0; c < kHalfCols; c += 4) {
+        float x0, x1, x2, x3;
+        fma2(x0, x1, s[c], s[c + 1], c2t, neg);
+        fma2(x2, x3, s[c + 2], s[c + 3], c2t, neg);
+        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+        const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+        add2(sa0, sa1, p0, p1);
+        add2(sb0, sb1, p2, p3);
+        pw[c / 4] = e4m3x4(p0 * kFp8PScale, p1 * kFp8PScale, p2 * kFp8PScale, p3 * kFp8PScale);
+      }
+      l = l * alpha + ((sa0 + sa1) + (sb0 + sb1));
+      if (rescale_warp) {
+#pragma unroll
+        for (int cc = 0; cc < 64; cc += 32) {
+          uint32_t r[32];
+          tmem_ld_x32(lane_addr + colO + cc, r);
+          tmem_ld_wait_x32(r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          tmem_st_x32(lane_addr + colO + cc, r);
+        }
+      }
+      tmem_st_x16(lane_addr + colP, pw);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar_addr(ss, kBarPFull + g));
+    }
+    // epilogue: O = O_acc * s_v / (256 l) -> bf16; LSE = ln 2 (m + log2 l)
+    ss.row_sum[g][half][0][trow] = l;
+    pair_sync(g, quadrant);
+    l += ss.row_sum[g][half ^ 1][0][trow];
+    u = -1;
+    if (!fail) fail = !fp8_next_unit(ss, p, uslot, true, u);
+    if (pair_sync_check(g, quadrant, fail)) return;
+    fail |= !__all_sync(0xffffffffu, fp8_wait(ss, kBarOFull + g, units_done & 1, p, 222 + g));
+    tc_fence_after();
+    const bool store = row >= nominal0 && row < p.N && row >= 0;
+    const float ofac = l > 0.f ? p.sv[bh] / (kFp8PScale * l) : 0.f;
+    __nv_bfloat16* orow =
+        p.o + ((size_t)(store ? un.b * p.N + row : 0) * p.H + un.h) * kFp8D + half * 64;
+#pragma unroll
+    for (int cc = 0; cc < 64; cc += 32) {
+      uint32_t r[32];
+      tmem_ld_x32(lane_addr + colO + cc, r);
+      tmem_ld_wait_x32(r);
+      if (store) {
+        uint4* dst = reinterpret_cast<uint4*>(orow + cc);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(r[8 * i + 0]) * ofac, __uint_as_float(r[8 * i + 1]) * ofac);
+          w.y = pack_bf16x2(__uint_as_float(r[8 * i + 2]) * ofac, __uint_as_float(r[8 * i + 3]) * ofac);
+          w.z = pack_bf16x2(__uint_as_float(r[8 * i + 4]) * ofac, __uint_as_float(r[8 * i + 5]) * ofac);
+          w.w = pack_bf16x2(__uint_as_float(r[8 * i + 6]) * ofac, __uint_as_float(r[8 * i + 7]) * ofac);
+          dst[i] = w;
+        }
+      }
+    }
+    if (store && half == 0)
+      p.lse[(size_t)bh * p.N + row] =
+          l > 0.f ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+    tc_fence_before();
+    ++units_done;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+attn_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_vt, const Fp8Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ SharedState ss;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sRing = smem + kQTiles * kFp8TileBytes;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int n_units = p.B * p.H * ((p.N + kUnitRows - 1) / kUnitRows);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_addr(ss, kBarQFull), 1);
+    mbar_init(bar_addr(ss, kBarQEmpty), 1);
+    for (int g = 0; g < kQTiles; ++g) {
+      mbar_init(bar_addr(ss, kBarSFull + g), 1);
+      mbar_init(bar_addr(ss, kBarPFull + g), kGroupThreads);
+      mbar_init(bar_addr(ss, kBarOFull + g), 1);
+    }
+    mbar_init(bar_addr(ss, kBarDrain), 1);
+    for (int i = 0; i < kUnitSlots; ++i) {
+      mbar_init(bar_addr(ss, kBarUnitFull + i), 1);
+      mbar_init(bar_addr(ss, kBarUnitEmpty + i), kUnitConsumers);
+    }
+    for (int s = 0; s < kFp8Stages; ++s) {
+      mbar_init(bar_addr(ss, kBarKV + s), 1);
+      mbar_init(bar_addr(ss, kBarKV + kFp8Stages + s), 1);
+    }
+    ss.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_vt);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(&ss.tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ss.tmem_base;
+
+  if (warp >= kSoftmaxWarps) {
+    setmaxnreg_dec<kControlRegs>();
+    if (warp == kProducerWarp) {
+      if (lane == 0) fp8_producer(&tm_q, &tm_k, &tm_vt, p, ss, sQ, sRing, n_units);
+    } else if (warp == kMmaWarp) {
+      if (lane == 0) {
+        fp8_mma_loop(p, ss, sQ, sRing, tmem);
+        mma_commit(bar_addr(ss, kBarDrain));
+        mbar_wait(bar_addr(ss, kBarDrain), 0, 100000000ull);
+      }
+    }
+    __syncwarp();
+  } else {
+    setmaxnreg_inc<kSoftmaxRegs>();
+    fp8_softmax_loop(p, ss, tmem, warp / kGroupWarps);
+    __syncwarp();
+  }
+
+  if (ss.abort_flag) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 1000000ull) {
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(p.sched + 1, 1) == (int)gridDim.x - 1) {
+      atomicExch(p.sched, 0);
+      atomicExch(p.sched + 1, 0);
+      __threadfence();
+    }
+  }
+}
+
+}  // namespace attn

@@ -12,7 +12,9 @@
 #include <mutex>
 #include <utility>
 
+#include "../../include/attn_fp8.h"
 #include "../../include/attn_fwd.h"
+#include "attn_fp8_kernel.cuh"
 #include "attn_fwd_kernel.cuh"
 #include "attn_host.h"
 
@@ -94,6 +96,9 @@ cudaError_t set_smem_attributes() {
   if ((e = cudaFuncSetAttribute(attn::attn_fwd_kernel<128, attn::kModeSplit>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 FwdCfg<128>::kSmemBytes)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(attn::attn_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                attn::kFp8SmemBytes)) != cudaSuccess)
     return e;
   return cudaFuncSetAttribute(attn::attn_fwd_kernel<128, attn::kModeWindow>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -197,7 +202,7 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* l
   if (B < 0 || H < 0 || N < 0) return ATTN_ERR_SHAPE;
   if (window_left < -1 || window_right < -1) return ATTN_ERR_SHAPE;
   if (d != 64 && d != 128) return ATTN_ERR_HEADDIM;
-  if (!std::isfinite(scale)) return ATTN_ERR_SCALE;
+  if (!std::isfinite(scale) || scale < 0.0f) return ATTN_ERR_SCALE;
   if (B == 0 || H == 0 || N == 0) return ATTN_OK;
   if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
@@ -324,7 +329,7 @@ extern "C" const char* attn_status_string(int status) {
     case ATTN_ERR_SHAPE: return "bad shape";
     case ATTN_ERR_HEADDIM: return "head dim must be 64 or 128";
     case ATTN_ERR_ALIGN: return "misaligned pointer";
-    case ATTN_ERR_SCALE: return "scale is not finite";
+    case ATTN_ERR_SCALE: return "scale is negative or not finite";
     case ATTN_ERR_CUDA: return "CUDA error";
     case ATTN_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
     case ATTN_ERR_SEQLENS: return "invalid cu_seqlens";
@@ -387,7 +392,7 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
                                 const int32_t* cu_seqlens, attn_stream_t stream) {
   if (B < 0 || H < 0 || N < 0) return ATTN_ERR_SHAPE;
   if (d != 64 && d != 128) return ATTN_ERR_HEADDIM;
-  if (!std::isfinite(scale)) return ATTN_ERR_SCALE;
+  if (!std::isfinite(scale) || scale < 0.0f) return ATTN_ERR_SCALE;
   if (B == 0 || H == 0 || N == 0) return ATTN_OK;
   if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
@@ -464,7 +469,7 @@ extern "C" int attn_fwd_kvsplit(const void* q, const void* k, const void* v, voi
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || num_splits < 0 || num_splits > 256)
     return ATTN_ERR_SHAPE;
   if (d != 64 && d != 128) return ATTN_ERR_HEADDIM;
-  if (!std::isfinite(scale)) return ATTN_ERR_SCALE;
+  if (!std::isfinite(scale) || scale < 0.0f) return ATTN_ERR_SCALE;
   if (B == 0 || H == 0 || Nq == 0) return ATTN_OK;
   if (Nk == 0 || (causal && Nq > Nk)) return ATTN_ERR_SHAPE;
   if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL;
@@ -589,3 +594,212 @@ int lib_make_map(CUtensorMap* map, const void* ptr, int64_t tokens, int H, int d
 }
 
 }  // namespace attn_host
+
+// ---------------------------------------------------------------------------
+// FP8 path (include/attn_fp8.h).
+namespace {
+
+struct Fp8Workspace {
+  void* buf = nullptr;
+  size_t bytes = 0;
+};
+std::map<std::pair<int, attn_stream_t>, Fp8Workspace> g_fp8_ws;
+
+int fp8_workspace(int dev, attn_stream_t stream, size_t bytes, uint8_t** out) {
+  Fp8Workspace& ws = g_fp8_ws[std::make_pair(dev, stream)];
+  if (ws.bytes < bytes || !ws.buf) {
+    cudaError_t e;
+    if (ws.buf) {
+      if ((e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream))) != cudaSuccess)
+        return cuda_fail(e);
+      cudaFree(ws.buf);
+      ws.buf = nullptr;
+      ws.bytes = 0;
+    }
+    if ((e = cudaMalloc(&ws.buf, bytes)) != cudaSuccess) return cuda_fail(e);
+    ws.bytes = bytes;
+  }
+  *out = static_cast<uint8_t*>(ws.buf);
+  return ATTN_OK;
+}
+
+// e4m3 rows [tokens, H, 128]: box 128 bytes x 1 head x 128 rows.
+int make_map_fp8_rows(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int64_t tokens, int H) {
+  cuuint64_t dims[3] = {(cuuint64_t)attn::kFp8D, (cuuint64_t)H, (cuuint64_t)tokens};
+  cuuint64_t strides[2] = {(cuuint64_t)attn::kFp8D, (cuuint64_t)H * attn::kFp8D};
+  cuuint32_t box[3] = {(cuuint32_t)attn::kFp8D, 1, (cuuint32_t)attn::kBM};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : cuda_fail(cudaErrorInvalidValue);
+}
+
+// transposed e4m3 V [B*H][128][Np]: box 128 keys x 128 channels x 1.
+int make_map_fp8_vt(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int64_t bh, int64_t np) {
+  cuuint64_t dims[3] = {(cuuint64_t)np, (cuuint64_t)attn::kFp8D, (cuuint64_t)bh};
+  cuuint64_t strides[2] = {(cuuint64_t)np, (cuuint64_t)np * attn::kFp8D};
+  cuuint32_t box[3] = {(cuuint32_t)attn::kBN, (cuuint32_t)attn::kFp8D, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : cuda_fail(cudaErrorInvalidValue);
+}
+
+int fp8_check(int B, int H, int N, int d) {
+  if (B < 0 || H < 0 || N < 0) return ATTN_ERR_SHAPE;
+  if (d != attn::kFp8D) return ATTN_ERR_HEADDIM;
+  const int64_t tokens = (int64_t)B * N;
+  if (tokens > INT32_MAX - 2 * attn::kBN || H > 65535 ||
+      (int64_t)B * H * ((N + attn::kBN - 1) / attn::kBN) > INT32_MAX / 2)
+    return ATTN_ERR_SHAPE;
+  return ATTN_OK;
+}
+
+attn::Fp8Signs pack_signs(const int8_t* signs) {
+  attn::Fp8Signs sg{};
+  if (signs)
+    for (int c = 0; c < attn::kFp8D; ++c)
+      if (signs[c] < 0) sg.bits[c / 32] |= 1u << (c % 32);
+  return sg;
+}
+
+int launch_quant_qk(const void* x, uint8_t* codes, float* scales, int B, int H, int N,
+                    const int8_t* signs, cudaStream_t s) {
+  const int T = (N + attn::kBM - 1) / attn::kBM;
+  attn::fp8_quant_qk_kernel<<<B * H * T, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(x),
+                                                      codes, scales, B, H, N, T, pack_signs(signs),
+                                                      signs ? 1 : 0);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+int launch_quant_v(const void* v, uint8_t* codes_t, float* scale, unsigned int* amax_bits, int B,
+                   int H, int N, cudaStream_t s) {
+  const int T = (N + attn::kBN - 1) / attn::kBN;
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(amax_bits, 0, (size_t)B * H * sizeof(unsigned int), s)) != cudaSuccess)
+    return cuda_fail(e);
+  attn::fp8_amax_v_kernel<<<B * H * T, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(v),
+                                                    amax_bits, B, H, N, T);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+  attn::fp8_quant_v_kernel<<<B * H * T, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(v),
+                                                     amax_bits, scale, codes_t, B, H, N,
+                                                     T * attn::kBN);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" int attn_fp8_quantize_qk(const void* x, uint8_t* codes, float* scales, int B, int H,
+                                    int N, int d, const int8_t* signs, attn_stream_t stream) {
+  int st = fp8_check(B, H, N, d);
+  if (st != ATTN_OK) return st;
+  if (B == 0 || H == 0 || N == 0) return ATTN_OK;
+  if (!x || !codes || !scales) return ATTN_ERR_NULL;
+  if (!aligned(x, 16) || !aligned(codes, 16) || !aligned(scales, 4)) return ATTN_ERR_ALIGN;
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  DeviceState* ds = nullptr;
+  if ((st = device_state(dev, &ds)) != ATTN_OK) return st;
+  return launch_quant_qk(x, codes, scales, B, H, N, signs, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int attn_fp8_quantize_v(const void* v, uint8_t* codes_t, float* scale, int B, int H,
+                                   int N, int d, attn_stream_t stream) {
+  int st = fp8_check(B, H, N, d);
+  if (st != ATTN_OK) return st;
+  if (B == 0 || H == 0 || N == 0) return ATTN_OK;
+  if (!v || !codes_t || !scale) return ATTN_ERR_NULL;
+  if (!aligned(v, 16) || !aligned(codes_t, 16) || !aligned(scale, 4)) return ATTN_ERR_ALIGN;
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  DeviceState* ds = nullptr;
+  if ((st = device_state(dev, &ds)) != ATTN_OK) return st;
+  uint8_t* ws = nullptr;
+  if ((st = fp8_workspace(dev, stream, (size_t)B * H * sizeof(unsigned int) + 256, &ws)) != ATTN_OK)
+    return st;
+  return launch_quant_v(v, codes_t, scale, reinterpret_cast<unsigned int*>(ws), B, H, N,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int H, int N, int d, float scale, int causal,
+                            const int8_t* signs, attn_stream_t stream) {
+  int st = fp8_check(B, H, N, d);
+  if (st != ATTN_OK) return st;
+  if (!std::isfinite(scale) || scale < 0.0f) return ATTN_ERR_SCALE;
+  if (B == 0 || H == 0 || N == 0) return ATTN_OK;
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return ATTN_ERR_ALIGN;
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  DeviceState* ds = nullptr;
+  if ((st = device_state(dev, &ds)) != ATTN_OK) return st;
+  EncodeTiledFn enc = nullptr;
+  if ((st = get_encode(&enc)) != ATTN_OK) return st;
+
+  const int64_t tokens = (int64_t)B * N;
+  const int64_t T = (N + attn::kBM - 1) / attn::kBM;
+  const int64_t np = T * attn::kBN;
+  const int64_t bh = (int64_t)B * H;
+  // workspace: Q codes, K codes, V codes (transposed, padded), Q and K block
+  // scales, V scales, V max bits; each part 256-byte aligned
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  const size_t b_q = up((size_t)tokens * H * attn::kFp8D), b_vt = up((size_t)bh * attn::kFp8D * np);
+  const size_t b_s = up((size_t)bh * T * sizeof(float)), b_v = up((size_t)bh * sizeof(float));
+  uint8_t* ws = nullptr;
+  if ((st = fp8_workspace(dev, stream, 2 * b_q + b_vt + 2 * b_s + 2 * b_v + 256, &ws)) != ATTN_OK)
+    return st;
+  uint8_t* q8 = ws;
+  uint8_t* k8 = q8 + b_q;
+  uint8_t* vt = k8 + b_q;
+  float* sq = reinterpret_cast<float*>(vt + b_vt);
+  float* sk = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(sq) + b_s);
+  float* sv = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(sk) + b_s);
+  unsigned int* amax = reinterpret_cast<unsigned int*>(reinterpret_cast<uint8_t*>(sv) + b_v);
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = launch_quant_qk(q, q8, sq, B, H, N, signs, s)) != ATTN_OK) return st;
+  if ((st = launch_quant_qk(k, k8, sk, B, H, N, signs, s)) != ATTN_OK) return st;
+  if ((st = launch_quant_v(v, vt, sv, amax, B, H, N, s)) != ATTN_OK) return st;
+
+  CUtensorMap mq, mk, mvt;
+  if ((st = make_map_fp8_rows(enc, &mq, q8, tokens, H)) != ATTN_OK) return st;
+  if ((st = make_map_fp8_rows(enc, &mk, k8, tokens, H)) != ATTN_OK) return st;
+  if ((st = make_map_fp8_vt(enc, &mvt, vt, bh, np)) != ATTN_OK) return st;
+  int* sched = nullptr;
+  if ((st = stream_workspace(dev, stream, 0, &sched)) != ATTN_OK) return st;
+
+  attn::Fp8Params p{};
+  p.o = reinterpret_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.sq = sq;
+  p.sk = sk;
+  p.sv = sv;
+  p.err = ds->err;
+  p.sched = sched + 1;
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.T = (int)T;
+  p.causal = causal ? 1 : 0;
+  p.scale = scale;
+  // the unnormalised rotation multiplies Q K^T by d
+  p.logit_log2 = (float)((double)scale * 1.4426950408889634 / (signs ? (double)attn::kFp8D : 1.0));
+  p.timeout_ns = 2000000000ull;
+  const int64_t units = bh * ((N + attn::kUnitRows - 1) / attn::kUnitRows);
+  const int grid = (int)std::min<int64_t>(units, ds->sms);
+  attn::attn_fp8_kernel<<<grid, attn::kThreads, attn::kFp8SmemBytes, s>>>(mq, mk, mvt, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+  return ATTN_OK;
+}

@@ -54,6 +54,7 @@ BUF = 1 << 20  # fake, 16-byte aligned addresses: validation fails before any us
     (dict(d=0), -3),
     (dict(scale=float("nan")), -5),
     (dict(scale=float("inf")), -5),
+    (dict(scale=-0.5), -5),
     (dict(q=None), -1),
     (dict(lse=None), -1),
     (dict(q=BUF + 8), -4),
@@ -111,3 +112,21 @@ def test_backward_argument_errors(lib, args, status):
 
 def test_backward_empty_problem_is_a_noop(lib):
     assert lib.attn_bwd(*([None] * 9), 0, 4, 256, 64, 0.125, 0, None, None) == 0
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(d=64), -3),
+    (dict(B=-1), -2),
+    (dict(scale=-1.0), -5),
+    (dict(scale=float("nan")), -5),
+    (dict(q=None), -1),
+    (dict(o=BUF + 8), -4),
+])
+def test_fp8_argument_errors(lib, args, status):
+    a = dict(q=BUF, k=BUF, v=BUF, o=BUF, lse=BUF, B=2, H=4, N=256, d=128, scale=0.1, causal=1)
+    a.update(args)
+    st = lib.attn_fwd_fp8(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"], a["d"],
+                          a["scale"], a["causal"], None, None)
+    assert st == status
+    assert lib.attn_fp8_quantize_qk(BUF, BUF, BUF, 1, 1, 128, 64, None, None) == -3
+    assert lib.attn_fp8_quantize_v(None, BUF, BUF, 1, 1, 128, 128, None) == -1

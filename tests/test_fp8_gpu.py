@@ -1,0 +1,178 @@
+"""FP8 forward (attn_fwd_fp8) against the oracle.
+
+The quantisation step decides integers (e4m3 codes) from floating point, so
+the CUDA codes and scales must equal the oracle's bit for bit (both take the
+steps in fp32 in the same order).  The attention is compared with two fp64
+references: the exact attention of the dequantised Q, K, V (what is left is
+the quantisation of P and the fp32 / bf16 arithmetic), and the exact attention
+of the original bf16 inputs (the whole FP8 error).
+
+Tolerances, from the e4m3 format (3 mantissa bits: a rounded value is within
+2^-4 of the exact one, relative, uniformly spread, rms 2^-4 / sqrt(3) ~ 0.036):
+  - against the dequantised reference, only P carries that error; O is a
+    P-weighted sum of V rows, so its relative L2 error is about 0.036 (the
+    errors of different keys have independent signs): bound 0.08, twice that;
+    the LSE comes from the unquantised fp32 row sum: bound 2e-3;
+  - against the exact attention, Q, K and V add their own e4m3 rounding.  A
+    logit scale * sum_c q_c k_c then carries an error of standard deviation
+    sqrt(2) * 0.036 * (logit standard deviation) ~ 0.05 for unit-variance
+    inputs; a row with one visible key has that error in its LSE, and the
+    largest of a few hundred compared rows reaches about 5 sigma: bound 0.3 on
+    the LSE; O adds V's 0.036 to P's: bound 0.15 on its relative L2.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from io_aware_exact_06_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+REL_DEQ, LSE_DEQ = 0.08, 2e-3
+REL_EXACT, LSE_EXACT = 0.15, 0.3
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import torch
+    import __graft_entry__
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    __graft_entry__.build()
+    return torch.device("cuda:0")
+
+
+def signs_of(seed):
+    return np.where(inputs.splitmix64(seed, 0, 128) & np.uint64(1), -1, 1).astype(np.int8)
+
+
+def with_outliers(bits, seed, factor=20.0, nch=3):
+    """bf16 bits with a few channels scaled up (the case incoherent processing is for)."""
+    x = inputs.bf16_bits_to_f64(bits).copy()
+    ch = (inputs.splitmix64(seed, 0, nch) % np.uint64(x.shape[-1])).astype(np.int64)
+    x[..., ch] *= factor
+    return inputs.f64_to_bf16_bits(x)
+
+
+def to_dev(dev, bits):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+
+@pytest.mark.parametrize("N", [1, 300, 1024])
+@pytest.mark.parametrize("rotate", [False, True])
+def test_quantize_qk_bit_exact(dev, N, rotate):
+    import torch
+    import io_aware_exact_06_gb300 as fa
+    B, H = 2, 3
+    x = with_outliers(inputs.normal_bf16(3100 + N, B * N * H * 128).reshape(B * N, H, 128), 3101)
+    sg = signs_of(3102) if rotate else None
+    T = -(-N // 128)
+    codes = torch.zeros((B * N, H, 128), dtype=torch.uint8, device=dev)
+    scales = torch.zeros((B, H, T), dtype=torch.float32, device=dev)
+    fa.attn_fp8_quantize_qk(to_dev(dev, x), codes, scales, B, H, N, 128, sg)
+    assert fa.attn_last_device_error() == 0
+    ref_codes, ref_scales = oracle.fp8_quantize(x, B, N, 128, rotate, sg)
+    assert np.array_equal(scales.cpu().numpy(), ref_scales)
+    assert np.array_equal(codes.cpu().numpy(), ref_codes)
+
+
+@pytest.mark.parametrize("N", [1, 300, 1024])
+def test_quantize_v_bit_exact(dev, N):
+    import torch
+    import io_aware_exact_06_gb300 as fa
+    B, H = 2, 3
+    v = inputs.normal_bf16(3200 + N, B * N * H * 128, 1.5).reshape(B * N, H, 128)
+    Np = 128 * (-(-N // 128))
+    codes_t = torch.full((B, H, 128, Np), 0x55, dtype=torch.uint8, device=dev)
+    scale = torch.zeros((B, H), dtype=torch.float32, device=dev)
+    fa.attn_fp8_quantize_v(to_dev(dev, v), codes_t, scale, B, H, N, 128)
+    assert fa.attn_last_device_error() == 0
+    ref_codes, ref_scale = oracle.fp8_quantize(v, B, N, 0, False)
+    got = codes_t.cpu().numpy()
+    assert np.array_equal(scale.cpu().numpy(), ref_scale[:, :, 0])
+    back = got[:, :, :, :N].transpose(0, 3, 1, 2).reshape(B * N, H, 128)
+    assert np.array_equal(back, ref_codes)
+    assert not got[:, :, :, N:].any(), "padding keys are zero"
+
+
+def dequantised(x, B, N, block_rows, rotate, sg):
+    """fp64 values of the oracle's codes times their block scales."""
+    codes, scales = oracle.fp8_quantize(x, B, N, block_rows, rotate, sg)
+    H = x.shape[1]
+    vals = oracle.e4m3_decode(codes.ravel()).reshape(codes.shape)
+    rows = np.arange(N)
+    blk = np.zeros(N, dtype=np.int64) if block_rows == 0 else np.minimum(rows // block_rows, scales.shape[2] - 1)
+    s = scales[:, :, blk].transpose(0, 2, 1).reshape(B * N, H, 1).astype(np.float64)
+    return vals * s
+
+
+def run_fp8(dev, q, k, v, B, N, H, causal, sg, scale):
+    import torch
+    import io_aware_exact_06_gb300 as fa
+    o = torch.empty((B * N, H, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    fa.attn_fwd_fp8(to_dev(dev, q), to_dev(dev, k), to_dev(dev, v), o, lse, B, H, N, 128, scale,
+                    causal, sg)
+    assert fa.attn_last_device_error() == 0
+    return o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+
+
+def errors(got_o, got_lse, ref_o, ref_lse):
+    rel = np.linalg.norm(got_o - ref_o) / np.linalg.norm(ref_o)
+    return float(rel), float(np.abs(got_lse - ref_lse).max())
+
+
+def check_case(dev, B, N, H, causal, rotate, seed, outliers):
+    q = inputs.normal_bf16(seed, B * N * H * 128).reshape(B * N, H, 128)
+    k = inputs.normal_bf16(seed + 1, B * N * H * 128).reshape(B * N, H, 128)
+    v = inputs.normal_bf16(seed + 2, B * N * H * 128).reshape(B * N, H, 128)
+    if outliers:
+        q, k = with_outliers(q, seed + 3), with_outliers(k, seed + 4)
+    scale = 128 ** -0.5
+    sg = signs_of(seed + 5) if rotate else None
+    got_o, got_lse = run_fp8(dev, q, k, v, B, N, H, causal, sg, scale)
+    cu = np.arange(B + 1) * N
+    rows = inputs.sample_rows(cu, H, 512, seed=seed + 6)
+    tok = cu[rows[:, 0]] + rows[:, 2]
+    go, gl = got_o[tok, rows[:, 1]], got_lse[rows[:, 0], rows[:, 1], rows[:, 2]]
+    qd = dequantised(q, B, N, 128, rotate, sg)
+    kd = dequantised(k, B, N, 128, rotate, sg)
+    vd = dequantised(v, B, N, 0, False, None)
+    ref_o, ref_l = oracle.attn_rows_f64(qd, kd, vd, cu, rows, scale / (128 if rotate else 1), causal)
+    deq = errors(go, gl, ref_o, ref_l)
+    ex_o, ex_l, _ = oracle.attn_rows(q, k, v, cu, rows, scale, causal)
+    exact = errors(go, gl, ex_o, ex_l)
+    log = os.environ.get("PARITY_LOG")
+    if log:
+        with open(log, "a") as f:
+            f.write(json.dumps({"test": "fp8", "B": B, "N": N, "H": H, "causal": causal,
+                                "rotate": rotate, "outliers": outliers, "vs_dequantised": deq,
+                                "vs_exact": exact}) + "\n")
+    return deq, exact
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("rotate", [False, True])
+def test_fp8_attention(dev, causal, rotate):
+    for (B, N, H) in [(1, 256, 2), (2, 1000, 3)]:
+        (rel_d, lse_d), (rel_e, lse_e) = check_case(dev, B, N, H, causal, rotate, 3300 + N, False)
+        assert rel_d <= REL_DEQ and lse_d <= LSE_DEQ, (N, causal, rotate, rel_d, lse_d)
+        assert rel_e <= REL_EXACT and lse_e <= LSE_EXACT, (N, causal, rotate, rel_e, lse_e)
+
+
+def test_fp8_short_sequence(dev):
+    (rel_d, lse_d), (rel_e, lse_e) = check_case(dev, 3, 77, 2, True, True, 3400, False)
+    assert rel_d <= REL_DEQ and lse_d <= LSE_DEQ
+    assert rel_e <= REL_EXACT and lse_e <= LSE_EXACT
+
+
+def test_incoherent_processing_helps_with_outliers(dev):
+    # channels of Q and K 20x larger than the rest: block scales are set by
+    # them, the other channels lose precision; the rotation spreads them
+    (_, _), (rel_plain, _) = check_case(dev, 1, 1024, 4, False, False, 3500, True)
+    (_, _), (rel_rot, _) = check_case(dev, 1, 1024, 4, False, True, 3500, True)
+    assert rel_rot < rel_plain, (rel_rot, rel_plain)
