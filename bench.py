@@ -6,6 +6,8 @@ with inputs resident in device memory.  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
   python bench.py --workload decode   # split-KV decode line (attn_fwd_kvsplit)
+  python bench.py --workload bwd      # backward line (attn_bwd)
+  python bench.py --workload fp8      # FP8 forward line (attn_fwd_fp8)
 
 Metric: attention forward TFLOP/s, FLOPs = 4*B*H*N^2*d halved for causal,
 whole job (all ranks) / the slowest rank's time.  N > 1 runs one independent
@@ -471,6 +473,267 @@ def torch_int16():
     return torch.int16
 
 
+BWD_METRIC = "attention bwd TFLOP/s on 1 GB300 (bf16; 2.5x the forward's FLOPs)"
+
+
+def run_bwd(args, world, rank, local):
+    """One step = one attn_bwd call (row prologue, dK/dV kernel, dQ kernel) on
+    the long causal workload with a seeded upstream gradient dO; O and the LSE
+    come from one attn_fwd call before the timed region.  FLOPs = 2.5x the
+    forward's (five matrix products per visible tile pair against two)."""
+    import torch
+    import __graft_entry__
+    import io_aware_exact_06_gb300 as fa
+    __graft_entry__.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = inputs.config_workload(WORKLOAD)
+    B, H, N, d = wl.nseq, wl.H, int(wl.seqlens()[0]), wl.d
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    dout_bits = inputs.normal_bf16(0xD0D0, wl.q.size).reshape(wl.q.shape)
+    host = [bf(a).pin_memory() for a in (wl.q, wl.k, wl.v, dout_bits)]
+    q, k, v, do = (t.to(dev) for t in host)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    fa.attn_fwd(q, k, v, o, lse, B, H, N, d, wl.scale, True, None, stream)
+    o_h = o.cpu().pin_memory()
+    lse_h = lse.cpu().pin_memory()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    grads_h = [torch.empty(q.shape, dtype=torch.bfloat16).pin_memory() for _ in range(3)]
+    flops_step = 2.5 * wl.flops()
+
+    def step():
+        fa.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, B, H, N, d, wl.scale, True, None, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if fa.attn_last_device_error(stream) != 0:
+        raise RuntimeError("device error during warm-up")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    if fa.attn_last_device_error(stream) != 0:
+        raise RuntimeError("device error in the timed region")
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    call_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    def e2e_step():  # Q, K, V, O, dO and LSE from the host, the three gradients back
+        for dst, src in zip((q, k, v, do), host):
+            dst.copy_(src, non_blocking=True)
+        o.copy_(o_h, non_blocking=True)
+        lse.copy_(lse_h, non_blocking=True)
+        step()
+        for dst, src in zip(grads_h, (dq, dk, dv)):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    n_e2e = max(3, min(args.steps, 10))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    if rank != 0:
+        return
+    peak, _, _, src = peaks()
+    achieved = flops_step / (call_ms * 1e-3) / 1e12
+    cfg = workload_config(wl)
+    cfg["workload"] = cfg["workload"] + ", backward (dO ~ N(0,1) bf16, seeded)"
+    line = {
+        "metric": BWD_METRIC, "value": world * flops_step * args.steps / (total_ms * 1e-3) / 1e12,
+        "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                     "frac": achieved / peak, "peak_source": f"{src} bf16_tflops (burst)",
+                     "kernel": "bwd_prep_kernel<128> + bwd_tile_kernel<128, dK/dV> + "
+                               "bwd_tile_kernel<128, dQ> (one call)",
+                     "tensor_work_tflops": achieved * 7.0 / 5.0,
+                     "traffic": BWD_TRAFFIC_BYTES},
+        "clocks": clk.summary(),
+        "e2e": {"value": world * flops_step * n_e2e / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": 5 * q.numel() * 2 + lse.numel() * 4,
+                "d2h_bytes_per_step": 3 * q.numel() * 2},
+        "gpu_launches": 3 * args.steps,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = bwd_cpu_baseline(wl, dout_bits)
+    print(json.dumps(line), flush=True)
+
+
+def bwd_cpu_baseline(wl, dout_bits, budget_s: float = 10.0):
+    """The oracle's gradients of whole (sequence, head) pairs of the workload,
+    pair after pair until about budget_s seconds have passed."""
+    import oracle
+    t0 = time.perf_counter()
+    done, used = 0, 1
+    L = float(wl.seqlens()[0])
+    pairs = [(s, h) for h in range(wl.H) for s in range(wl.nseq)]
+    while done < len(pairs) and time.perf_counter() - t0 < budget_s:
+        _, _, _, used = oracle.attn_bwd(wl.q, wl.k, wl.v, dout_bits, wl.cu_seqlens, [pairs[done]],
+                                        wl.scale, True)
+        done += 1
+    dt = time.perf_counter() - t0
+    flops = done * 2.5 * 4.0 * L * L * wl.d / 2
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": int(used), "kind": "oracle",
+            "sample": f"{done} whole (sequence, head) pairs of {WORKLOAD} (fp64 chain rule), "
+                      f"{dt:.1f} s; FLOPs = 2.5x the forward's"}
+
+
+FP8_METRIC = "attention fwd TFLOP/s on 1 GB300 (FP8 e4m3 path: block quantisation + incoherent processing)"
+
+
+def run_fp8(args, world, rank, local):
+    """One step = one attn_fwd_fp8 call (Q and K quantisers, V max and
+    quantiser, FP8 attention kernel) on the long causal workload; same FLOP
+    convention as the bf16 line.  Peak: the measured bf16 burst peak times 2
+    (the nominal FP8 : BF16 dense ratio)."""
+    import torch
+    import __graft_entry__
+    import io_aware_exact_06_gb300 as fa
+    __graft_entry__.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = inputs.config_workload(WORKLOAD)
+    B, H, N, d = wl.nseq, wl.H, int(wl.seqlens()[0]), wl.d
+    signs = np.where(inputs.splitmix64(0x51635, 0, d) & np.uint64(1), -1, 1).astype(np.int8)
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    host = [bf(a).pin_memory() for a in (wl.q, wl.k, wl.v)]
+    q, k, v = (t.to(dev) for t in host)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    o_h = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream(dev)
+    flops_step = wl.flops()
+
+    def step():
+        fa.attn_fwd_fp8(q, k, v, o, lse, B, H, N, d, wl.scale, True, signs, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if fa.attn_last_device_error(stream) != 0:
+        raise RuntimeError("device error during warm-up")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    if fa.attn_last_device_error(stream) != 0:
+        raise RuntimeError("device error in the timed region")
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    call_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    def e2e_step():
+        for dst, src in zip((q, k, v), host):
+            dst.copy_(src, non_blocking=True)
+        step()
+        o_h.copy_(o, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    n_e2e = max(3, min(args.steps, 10))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    if rank != 0:
+        return
+    peak_bf16, _, _, src = peaks()
+    peak = 2.0 * peak_bf16
+    achieved = flops_step / (call_ms * 1e-3) / 1e12
+    cfg = workload_config(wl)
+    cfg["workload"] = cfg["workload"] + ", FP8 e4m3 (128-row blocks, Hadamard rotation)"
+    line = {
+        "metric": FP8_METRIC, "value": world * flops_step * args.steps / (total_ms * 1e-3) / 1e12,
+        "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp8_e4m3", "data": "synthetic", "config": cfg,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                     "frac": achieved / peak,
+                     "peak_source": f"{src} bf16_tflops (burst) x 2, the nominal FP8:BF16 dense ratio",
+                     "kernel": "fp8 quantisers + attn_fp8_kernel (one call)",
+                     "traffic": None},
+        "clocks": clk.summary(),
+        "e2e": {"value": world * flops_step * n_e2e / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": 3 * q.numel() * 2,
+                "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4},
+        "gpu_launches": 5 * args.steps,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = fp8_cpu_baseline(wl, signs)
+    print(json.dumps(line), flush=True)
+
+
+def fp8_cpu_baseline(wl, signs, budget_s: float = 10.0):
+    """The oracle's FP8 path (quantisation of one sequence and head, then the
+    fp64 attention of the dequantised values) on a bounded sample of rows."""
+    import oracle
+    N, H, d = int(wl.seqlens()[0]), wl.H, wl.d
+    t0 = time.perf_counter()
+    sl = slice(0, N)  # sequence 0
+    pick = lambda a: np.ascontiguousarray(a[sl, :1])  # head 0
+    qc, qs = oracle.fp8_quantize(pick(wl.q), 1, N, 128, True, signs)
+    kc, ks = oracle.fp8_quantize(pick(wl.k), 1, N, 128, True, signs)
+    vc, vs = oracle.fp8_quantize(pick(wl.v), 1, N, 0, False)
+    blk = np.minimum(np.arange(N) // 128, qs.shape[2] - 1)
+    deq = lambda c, s: oracle.e4m3_decode(c.ravel()).reshape(c.shape) * s[0, 0][blk][:, None, None]
+    qd, kd = deq(qc, qs), deq(kc, ks)
+    vd = oracle.e4m3_decode(vc.ravel()).reshape(vc.shape) * float(vs[0, 0, 0])
+    cu = np.array([0, N])
+    rows_all = np.stack([np.zeros(N, np.int64), np.zeros(N, np.int64), np.arange(N)], axis=1)
+    rows_all = rows_all[np.argsort(inputs.splitmix64(0xF8, 0, N))]
+    done, flops = 0, 0.0
+    while done < N and time.perf_counter() - t0 < budget_s:
+        batch = rows_all[done:done + 256]
+        oracle.attn_rows_f64(qd, kd, vd, cu, batch, wl.scale / d, True)
+        flops += float(np.sum(4.0 * d * (batch[:, 2] + 1)))
+        done += len(batch)
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"quantisation of sequence 0, head 0 and the fp64 attention of {done} of its "
+                      f"dequantised rows, {dt:.1f} s (single-threaded)"}
+
+
+# DRAM bytes (read + write) of one backward call on this workload (all three
+# kernels), from the ncu capture summarised under profiles/ (None until taken).
+BWD_TRAFFIC_BYTES = None
+
+
 # DRAM bytes (read + write) of one attn_fwd_kernel<128> launch of this
 # workload, from the ncu capture summarised under profiles/ (None until taken
 # for the current kernel).
@@ -484,7 +747,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default=WORKLOAD, choices=[WORKLOAD, "decode"])
+    ap.add_argument("--workload", default=WORKLOAD, choices=[WORKLOAD, "decode", "bwd", "fp8"])
     ap.add_argument("--ref-step-s", type=float, default=0.0,
                     help="reference arm: oracle seconds per step (default: fit the run in ~2.5 min)")
     args = ap.parse_args()
@@ -494,6 +757,10 @@ def main():
         run_reference(args, world, rank)
     elif args.workload == "decode":
         run_decode(args, world, rank, local)
+    elif args.workload == "bwd":
+        run_bwd(args, world, rank, local)
+    elif args.workload == "fp8":
+        run_fp8(args, world, rank, local)
     else:
         run_cuda(args, world, rank, local)
     if world > 1:
