@@ -18,10 +18,10 @@
 // (log2 units), so 256 P stays below 448.
 //
 // Kernels:
-//   fp8_quant_qk_kernel   rotation + block quantisation of Q or K, one CTA per
-//                         (sequence, head, 128-row block), two passes (the
-//                         block max, then the codes)
-//   fp8_amax_v_kernel     max |V| per (sequence, head) (atomic max of the
+//   fp8_quant_stage1_kernel  rotation + block quantisation of Q and of K, one
+//                         CTA per (sequence, head, 128-row block) holding its
+//                         rotated rows in registers; and in the same launch the
+//                         max |V| per (sequence, head) (atomic max of the
 //                         non-negative fp32 bit patterns)
 //   fp8_quant_v_kernel    V codes, stored transposed per (sequence, head):
 //                         [d][keys padded to 128] (keys contiguous), so both
@@ -130,17 +130,15 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
   return lo | (hi << 16);
 }
 
-// One CTA (8 warps) per (sequence, head, 128-row block); the last block of a
-// sequence is pulled back to end at N and leaves the rows it shares with the
-// block before it to that block.
-__global__ void __launch_bounds__(256)
-fp8_quant_qk_kernel(const __nv_bfloat16* x, uint8_t* codes, float* scales, int B, int H, int N,
-                    int T, Fp8Signs signs, int rotate) {
-  __shared__ float warp_max[8];
+// Quantises one 128-row block of Q or K (rotation, block max, codes) with one
+// CTA of 8 warps; the last block of a sequence is pulled back to end at N and
+// leaves the rows it shares with the block before it to that block.  Each
+// warp holds its 16 rotated rows in registers between the max and the codes.
+__device__ __forceinline__ void fp8_quant_block(const __nv_bfloat16* x, uint8_t* codes,
+                                                float* scale_out, int b, int h, int t, int H,
+                                                int N, const Fp8Signs& signs, int rotate,
+                                                float* warp_max) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int t = blockIdx.x % T;
-  const int bh = blockIdx.x / T;
-  const int b = bh / H, h = bh % H;
   const int r0 = min(t * kBM, N - kBM);
   float sgn[4];
 #pragma unroll
@@ -148,26 +146,28 @@ fp8_quant_qk_kernel(const __nv_bfloat16* x, uint8_t* codes, float* scales, int B
     const int c = 4 * lane + j;
     sgn[j] = rotate && ((signs.bits[c / 32] >> (c % 32)) & 1u) ? -1.0f : 1.0f;
   }
-  auto load_row = [&](int row, float (&v)[4]) {
-    if (row >= 0) {
-      const uint2 w = *reinterpret_cast<const uint2*>(x + (((size_t)b * N + row) * H + h) * kFp8D +
-                                                      4 * lane);
-      const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&w.x);
-      const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&w.y);
-      v[0] = __bfloat162float(p0.x) * sgn[0];
-      v[1] = __bfloat162float(p0.y) * sgn[1];
-      v[2] = __bfloat162float(p1.x) * sgn[2];
-      v[3] = __bfloat162float(p1.y) * sgn[3];
-      if (rotate) fwht128_warp(v, lane);
-    } else {
-      v[0] = v[1] = v[2] = v[3] = 0.f;
-    }
-  };
+  constexpr int kRows = kBM / 8;  // rows per warp: warp + 8 i
+  uint2 raw[kRows];
+#pragma unroll
+  for (int i = 0; i < kRows; ++i) {
+    const int row = r0 + warp + 8 * i;
+    raw[i] = row >= 0 ? *reinterpret_cast<const uint2*>(x + (((size_t)b * N + row) * H + h) * kFp8D +
+                                                         4 * lane)
+                      : make_uint2(0u, 0u);
+  }
+  float v[kRows][4];
   float amax = 0.f;
-  for (int r = warp; r < kBM; r += 8) {
-    float v[4];
-    load_row(r0 + r, v);
-    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))));
+#pragma unroll
+  for (int i = 0; i < kRows; ++i) {
+    const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw[i].x);
+    const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw[i].y);
+    v[i][0] = __bfloat162float(p0.x) * sgn[0];
+    v[i][1] = __bfloat162float(p0.y) * sgn[1];
+    v[i][2] = __bfloat162float(p1.x) * sgn[2];
+    v[i][3] = __bfloat162float(p1.y) * sgn[3];
+    if (rotate) fwht128_warp(v[i], lane);
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[i][0]), fabsf(v[i][1])),
+                             fmaxf(fabsf(v[i][2]), fabsf(v[i][3]))));
   }
 #pragma unroll
   for (int m = 16; m > 0; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
@@ -177,28 +177,25 @@ fp8_quant_qk_kernel(const __nv_bfloat16* x, uint8_t* codes, float* scales, int B
 #pragma unroll
   for (int w = 1; w < 8; ++w) amax = fmaxf(amax, warp_max[w]);
   const float inv = amax > 0.f ? __fdiv_rn(kFp8Max, amax) : 1.0f;
-  if (threadIdx.x == 0) scales[blockIdx.x] = amax > 0.f ? __fdiv_rn(amax, kFp8Max) : 1.0f;
-  for (int r = warp; r < kBM; r += 8) {
-    const int row = r0 + r;
+  if (threadIdx.x == 0) *scale_out = amax > 0.f ? __fdiv_rn(amax, kFp8Max) : 1.0f;
+#pragma unroll
+  for (int i = 0; i < kRows; ++i) {
+    const int row = r0 + warp + 8 * i;
     if (row < t * kBM) continue;  // the previous block's row (or before the sequence)
-    float v[4];
-    load_row(row, v);
     *reinterpret_cast<uint32_t*>(codes + (((size_t)b * N + row) * H + h) * kFp8D + 4 * lane) =
-        e4m3x4(__fmul_rn(v[0], inv), __fmul_rn(v[1], inv), __fmul_rn(v[2], inv),
-               __fmul_rn(v[3], inv));
+        e4m3x4(__fmul_rn(v[i][0], inv), __fmul_rn(v[i][1], inv), __fmul_rn(v[i][2], inv),
+               __fmul_rn(v[i][3], inv));
   }
 }
 
-// amax[b*H + h] = max |V| over the sequence (bit patterns of non-negative
-// floats order like the floats).  One CTA per (sequence, head, 128 rows).
-__global__ void __launch_bounds__(256)
-fp8_amax_v_kernel(const __nv_bfloat16* v, unsigned int* amax_bits, int B, int H, int N, int T) {
-  __shared__ float warp_max[8];
+// max |V| of rows [128 t, 128 t + 128) of one (sequence, head), folded into
+// amax_bits[b*H + h] (bit patterns of non-negative floats order like the
+// floats).
+__device__ __forceinline__ void fp8_amax_block(const __nv_bfloat16* v, unsigned int* amax_bits,
+                                               int b, int h, int t, int H, int N, float* warp_max) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int t = blockIdx.x % T;
-  const int bh = blockIdx.x / T;
-  const int b = bh / H, h = bh % H;
   float m = 0.f;
+#pragma unroll 4
   for (int r = warp; r < kBM; r += 8) {
     const int row = t * kBM + r;
     if (row >= N) break;
@@ -216,17 +213,41 @@ fp8_amax_v_kernel(const __nv_bfloat16* v, unsigned int* amax_bits, int B, int H,
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int w = 1; w < 8; ++w) m = fmaxf(m, warp_max[w]);
-    atomicMax(amax_bits + bh, __float_as_uint(m));
+    atomicMax(amax_bits + b * H + h, __float_as_uint(m));
   }
+}
+
+// One launch for the first quantisation stage: blocks [0, nb) quantise Q
+// (when q is given), [nb, 2 nb) quantise K (when k is given), [2 nb, 3 nb)
+// take the max |V| (when v is given); nb = B * H * T, block = (b * H + h) * T + t.
+__global__ void __launch_bounds__(256)
+fp8_quant_stage1_kernel(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv_bfloat16* v,
+                        uint8_t* q8, uint8_t* k8, float* sq, float* sk, unsigned int* amax_v,
+                        int B, int H, int N, int T, Fp8Signs signs, int rotate, int block0) {
+  __shared__ float warp_max[8];
+  const int nb = B * H * T;
+  const int gidx = (int)blockIdx.x + block0;  // block0 skips absent leading segments
+  const int seg = gidx / nb, idx = gidx % nb;
+  const int t = idx % T, bh = idx / T;
+  const int b = bh / H, h = bh % H;
+  if (seg == 0)
+    fp8_quant_block(q, q8, sq + idx, b, h, t, H, N, signs, rotate, warp_max);
+  else if (seg == 1)
+    fp8_quant_block(k, k8, sk + idx, b, h, t, H, N, signs, rotate, warp_max);
+  else
+    fp8_amax_block(v, amax_v, b, h, t, H, N, warp_max);
 }
 
 // V codes, transposed: vt[(b*H + h) * 128 + c][key] for keys padded to Np
 // (a multiple of 128; padding keys get code 0).  Also writes the V scale.
-// One CTA per (sequence, head, 128 keys).
+// One CTA per (sequence, head, 128 keys): codes go to shared memory key-major
+// (a warp writes one key's 128 bytes), then each thread gathers 16 keys of one
+// channel (the bytes a warp reads at once lie in 8 words: no bank conflict)
+// and writes them as one 16-byte store.
 __global__ void __launch_bounds__(256)
 fp8_quant_v_kernel(const __nv_bfloat16* v, const unsigned int* amax_bits, float* sv, uint8_t* vt,
                    int B, int H, int N, int Np) {
-  __shared__ uint8_t tile[kFp8D][kBN + 16];
+  __shared__ __align__(16) uint8_t tile[kBN][kFp8D];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int T = Np / kBN;
   const int t = blockIdx.x % T;
@@ -235,6 +256,7 @@ fp8_quant_v_kernel(const __nv_bfloat16* v, const unsigned int* amax_bits, float*
   const float amax = __uint_as_float(amax_bits[bh]);
   const float inv = amax > 0.f ? __fdiv_rn(kFp8Max, amax) : 1.0f;
   if (t == 0 && threadIdx.x == 0) sv[bh] = amax > 0.f ? __fdiv_rn(amax, kFp8Max) : 1.0f;
+#pragma unroll 4
   for (int r = warp; r < kBN; r += 8) {
     const int key = t * kBN + r;
     float f[4] = {0.f, 0.f, 0.f, 0.f};
@@ -248,22 +270,23 @@ fp8_quant_v_kernel(const __nv_bfloat16* v, const unsigned int* amax_bits, float*
       f[2] = __bfloat162float(p1.x);
       f[3] = __bfloat162float(p1.y);
     }
-    const uint32_t c4 = e4m3x4(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv), __fmul_rn(f[2], inv),
-                               __fmul_rn(f[3], inv));
-#pragma unroll
-    for (int j = 0; j < 4; ++j) tile[4 * lane + j][r] = (uint8_t)(c4 >> (8 * j));
+    *reinterpret_cast<uint32_t*>(&tile[r][4 * lane]) =
+        e4m3x4(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv), __fmul_rn(f[2], inv),
+               __fmul_rn(f[3], inv));
   }
   __syncthreads();
-  // 128 rows (channels) x 128 keys, 16 bytes per thread-store
+  // output chunk i: channel c = i % 128, keys 16 q .. 16 q + 15 with q = i / 128
+#pragma unroll
   for (int i = threadIdx.x; i < kFp8D * (kBN / 16); i += 256) {
-    const int c = i / (kBN / 16), q = i % (kBN / 16);
-    uint4 w;
-    uint8_t* src = &tile[c][q * 16];
-    w.x = src[0] | (src[1] << 8) | (src[2] << 16) | ((uint32_t)src[3] << 24);
-    w.y = src[4] | (src[5] << 8) | (src[6] << 16) | ((uint32_t)src[7] << 24);
-    w.z = src[8] | (src[9] << 8) | (src[10] << 16) | ((uint32_t)src[11] << 24);
-    w.w = src[12] | (src[13] << 8) | (src[14] << 16) | ((uint32_t)src[15] << 24);
-    *reinterpret_cast<uint4*>(vt + ((size_t)bh * kFp8D + c) * Np + t * kBN + q * 16) = w;
+    const int c = i % kFp8D, q = i / kFp8D;
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      w[j] = (uint32_t)tile[16 * q + 4 * j][c] | ((uint32_t)tile[16 * q + 4 * j + 1][c] << 8) |
+             ((uint32_t)tile[16 * q + 4 * j + 2][c] << 16) |
+             ((uint32_t)tile[16 * q + 4 * j + 3][c] << 24);
+    *reinterpret_cast<uint4*>(vt + ((size_t)bh * kFp8D + c) * Np + t * kBN + q * 16) =
+        make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 

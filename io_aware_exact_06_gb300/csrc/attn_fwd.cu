@@ -665,30 +665,35 @@ attn::Fp8Signs pack_signs(const int8_t* signs) {
   return sg;
 }
 
-int launch_quant_qk(const void* x, uint8_t* codes, float* scales, int B, int H, int N,
-                    const int8_t* signs, cudaStream_t s) {
+// First stage: Q and / or K codes and block scales, and / or max |V| per
+// (sequence, head) (amax_v zeroed here first).  Null inputs are skipped.
+int launch_quant_stage1(const void* q, const void* k, const void* v, uint8_t* q8, uint8_t* k8,
+                        float* sq, float* sk, unsigned int* amax_v, int B, int H, int N,
+                        const int8_t* signs, cudaStream_t s) {
   const int T = (N + attn::kBM - 1) / attn::kBM;
-  attn::fp8_quant_qk_kernel<<<B * H * T, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(x),
-                                                      codes, scales, B, H, N, T, pack_signs(signs),
-                                                      signs ? 1 : 0);
-  cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+  const int nb = B * H * T;
+  cudaError_t e;
+  if (v && (e = cudaMemsetAsync(amax_v, 0, (size_t)B * H * sizeof(unsigned int), s)) != cudaSuccess)
+    return cuda_fail(e);
+  // segments: Q, K, V (the grid covers the last segment that is present)
+  const int nseg = v ? 3 : (k ? 2 : 1);
+  const int first = q ? 0 : (k ? 1 : 2);
+  attn::fp8_quant_stage1_kernel<<<(nseg - first) * nb, 256, 0, s>>>(
+      reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k),
+      reinterpret_cast<const __nv_bfloat16*>(v), q8, k8, sq, sk, amax_v, B, H, N, T,
+      pack_signs(signs), signs ? 1 : 0, first * nb);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+  return ATTN_OK;
 }
 
 int launch_quant_v(const void* v, uint8_t* codes_t, float* scale, unsigned int* amax_bits, int B,
                    int H, int N, cudaStream_t s) {
   const int T = (N + attn::kBN - 1) / attn::kBN;
-  cudaError_t e;
-  if ((e = cudaMemsetAsync(amax_bits, 0, (size_t)B * H * sizeof(unsigned int), s)) != cudaSuccess)
-    return cuda_fail(e);
-  attn::fp8_amax_v_kernel<<<B * H * T, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(v),
-                                                    amax_bits, B, H, N, T);
-  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
   attn::fp8_quant_v_kernel<<<B * H * T, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(v),
                                                      amax_bits, scale, codes_t, B, H, N,
                                                      T * attn::kBN);
-  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
-  return ATTN_OK;
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 
 }  // namespace
@@ -706,7 +711,8 @@ extern "C" int attn_fp8_quantize_qk(const void* x, uint8_t* codes, float* scales
   if (e != cudaSuccess) return cuda_fail(e);
   DeviceState* ds = nullptr;
   if ((st = device_state(dev, &ds)) != ATTN_OK) return st;
-  return launch_quant_qk(x, codes, scales, B, H, N, signs, reinterpret_cast<cudaStream_t>(stream));
+  return launch_quant_stage1(x, nullptr, nullptr, codes, nullptr, scales, nullptr, nullptr, B, H, N,
+                             signs, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int attn_fp8_quantize_v(const void* v, uint8_t* codes_t, float* scale, int B, int H,
@@ -725,8 +731,12 @@ extern "C" int attn_fp8_quantize_v(const void* v, uint8_t* codes_t, float* scale
   uint8_t* ws = nullptr;
   if ((st = fp8_workspace(dev, stream, (size_t)B * H * sizeof(unsigned int) + 256, &ws)) != ATTN_OK)
     return st;
-  return launch_quant_v(v, codes_t, scale, reinterpret_cast<unsigned int*>(ws), B, H, N,
-                        reinterpret_cast<cudaStream_t>(stream));
+  unsigned int* amax = reinterpret_cast<unsigned int*>(ws);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = launch_quant_stage1(nullptr, nullptr, v, nullptr, nullptr, nullptr, nullptr, amax, B, H,
+                                N, nullptr, s)) != ATTN_OK)
+    return st;
+  return launch_quant_v(v, codes_t, scale, amax, B, H, N, s);
 }
 
 extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -769,8 +779,8 @@ extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o
   unsigned int* amax = reinterpret_cast<unsigned int*>(reinterpret_cast<uint8_t*>(sv) + b_v);
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if ((st = launch_quant_qk(q, q8, sq, B, H, N, signs, s)) != ATTN_OK) return st;
-  if ((st = launch_quant_qk(k, k8, sk, B, H, N, signs, s)) != ATTN_OK) return st;
+  if ((st = launch_quant_stage1(q, k, v, q8, k8, sq, sk, amax, B, H, N, signs, s)) != ATTN_OK)
+    return st;
   if ((st = launch_quant_v(v, vt, sv, amax, B, H, N, s)) != ATTN_OK) return st;
 
   CUtensorMap mq, mk, mvt;
