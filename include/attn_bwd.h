@@ -33,21 +33,24 @@ extern "C" {
 #endif
 
 /*
- * attn_bwd: dQ, dK, dV of attn_fwd (dense batches).
+ * attn_bwd: dQ, dK, dV of attn_fwd.
  *
- * Layout: q, k, v, o, dout, dq, dk, dv are contiguous [B, N, H, d] bf16;
- *   lse is [B, H, N] fp32, as written by attn_fwd for the same q, k, v,
- *   scale and causal flag.
- * q, k, v, o, dout, lse: read only.  dq, dk, dv: every element written.
+ * Layouts as for attn_fwd, with dout, dq, dk, dv laid out like q:
+ *   dense (cu_seqlens == NULL): q, k, v, o, dout, dq, dk, dv [B, N, H, d]
+ *   bf16, lse [B, H, N] fp32; packed (cu_seqlens != NULL, device int32
+ *   [B+1], validated on the device): [total, H, d] and lse [H, total], N >=
+ *   every length, at most 8192 tiles of 128 rows per sequence.  lse is the
+ *   one attn_fwd wrote for the same q, k, v, scale and causal flag.
+ * q, k, v, o, dout, lse: read only.  dq, dk, dv: every element of every
+ *   sequence written.
  * d: 64 or 128.  scale and causal: those of the forward call.
- * cu_seqlens: must be NULL (packed batches are not supported by the backward;
- *   ATTN_ERR_SHAPE otherwise).
  * Alignment: the bf16 tensors 16-byte aligned; lse 4-byte aligned.
  * Ownership: the caller owns every buffer.  The library keeps a cached
  *   per-(device, stream) workspace of 2 * B * H * ceil(N / 128) * 128 floats
- *   (each row's D = <dO, O> and LSE * log2(e)), grown on demand; device-side
- *   errors (an expired bounded wait) are latched in the same error word as
- *   the forward's and read by attn_last_device_error.
+ *   (each row's D = <dO, O> and LSE * log2(e)) and, for packed batches, its
+ *   scheduling lists, grown on demand; device-side errors (an expired bounded
+ *   wait, invalid cu_seqlens) are latched in the same error word as the
+ *   forward's and read by attn_last_device_error.
  * B == 0, N == 0 or H == 0 is a no-op returning ATTN_OK.
  * Returns ATTN_OK or a negative attn_status; nothing is launched on error.
  */

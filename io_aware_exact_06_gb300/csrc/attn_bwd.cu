@@ -21,8 +21,10 @@ using bwd::BwdCfg;
 using bwd::BwdParams;
 
 struct BwdWorkspace {
-  void* buf = nullptr;   // [0, 256): unit counters (int), then lse2 and D (float)
+  void* buf = nullptr;   // [0, 256): unit counters (int), then lse2 and D (float), then the
+                         // packed-batch lists (int)
   size_t floats = 0;     // capacity of each of the two float arrays
+  size_t ints = 0;       // capacity of the list area
 };
 
 std::map<std::pair<int, attn_stream_t>, BwdWorkspace> g_bwd_ws;
@@ -49,10 +51,10 @@ cudaError_t set_bwd_attributes() {
                               BwdCfg<128>::kQSmemBytes);
 }
 
-int bwd_workspace(int dev, attn_stream_t stream, size_t floats, int** counters, float** lse2,
-                  float** dd) {
+int bwd_workspace(int dev, attn_stream_t stream, size_t floats, size_t ints, int** counters,
+                  float** lse2, float** dd, int** lists) {
   BwdWorkspace& ws = g_bwd_ws[std::make_pair(dev, stream)];
-  if (ws.floats < floats || !ws.buf) {
+  if (ws.floats < floats || ws.ints < ints || !ws.buf) {
     cudaError_t e;
     if (ws.buf) {
       // the old buffers may still be read by work queued on this stream
@@ -63,14 +65,18 @@ int bwd_workspace(int dev, attn_stream_t stream, size_t floats, int** counters, 
       ws.floats = 0;
     }
     const size_t cap = std::max<size_t>(floats, 1 << 16);
-    if ((e = cudaMalloc(&ws.buf, kCounterBytes + 2 * cap * sizeof(float))) != cudaSuccess)
+    const size_t icap = std::max<size_t>(ints, 1024);
+    if ((e = cudaMalloc(&ws.buf, kCounterBytes + 2 * cap * sizeof(float) + icap * sizeof(int))) !=
+        cudaSuccess)
       return attn_host::lib_cuda_fail(e);
     if ((e = cudaMemset(ws.buf, 0, kCounterBytes)) != cudaSuccess) return attn_host::lib_cuda_fail(e);
     ws.floats = cap;
+    ws.ints = icap;
   }
   *counters = static_cast<int*>(ws.buf);
   *lse2 = reinterpret_cast<float*>(static_cast<char*>(ws.buf) + kCounterBytes);
   *dd = *lse2 + ws.floats;
+  *lists = reinterpret_cast<int*>(*dd + ws.floats);
   return ATTN_OK;
 }
 
@@ -79,12 +85,13 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 template <int D>
 int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                const CUtensorMap& mdo, const void* o, const void* dout, const float* lse,
-               BwdParams p, int* counters, int grid, cudaStream_t s) {
-  const long long rows = (long long)p.B * p.H * p.T * bwd::kTile;
-  const long long blocks = (rows * 32 + 255) / 256;
+               BwdParams p, int* counters, int64_t max_tiles, int grid, cudaStream_t s) {
+  // one warp per row slot of every tile and head (packed: an upper bound of the tiles)
+  const long long slots = (long long)p.H * max_tiles * bwd::kTile;
+  const long long blocks = (slots * 32 + 255) / 256;
   bwd::bwd_prep_kernel<D><<<(unsigned)blocks, 256, 0, s>>>(
       reinterpret_cast<const __nv_bfloat16*>(o), reinterpret_cast<const __nv_bfloat16*>(dout), lse,
-      const_cast<float*>(p.lse2), const_cast<float*>(p.dd), p.B, p.H, p.N, p.T);
+      p, slots);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return attn_host::lib_cuda_fail(e);
   p.sched = counters;
@@ -107,7 +114,6 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   if (B < 0 || H < 0 || N < 0) return ATTN_ERR_SHAPE;
   if (d != 64 && d != 128) return ATTN_ERR_HEADDIM;
   if (!std::isfinite(scale) || scale < 0.0f) return ATTN_ERR_SCALE;
-  if (cu_seqlens) return ATTN_ERR_SHAPE;
   if (B == 0 || H == 0 || N == 0) return ATTN_OK;
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return ATTN_ERR_NULL;
   for (const void* ptr : {q, k, v, o, dout, (const void*)dq, (const void*)dk, (const void*)dv})
@@ -117,8 +123,9 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   if (tokens > INT32_MAX - 2 * bwd::kTile || (int64_t)H * d > (1 << 20) || H > 65535)
     return ATTN_ERR_SHAPE;
   const int64_t T = (N + bwd::kTile - 1) / bwd::kTile;
-  const int64_t units = (int64_t)B * H * T;
-  if (units > INT32_MAX / bwd::kTile) return ATTN_ERR_SHAPE;
+  const int64_t max_tiles = (int64_t)B * T;  // packed: every length <= N
+  const int64_t units = max_tiles * H;
+  if (units > INT32_MAX / bwd::kTile || (cu_seqlens && T > bwd::kMaxCostBuckets)) return ATTN_ERR_SHAPE;
 
   std::lock_guard<std::mutex> lock(attn_host::lib_mutex());
   int dev = 0, sms = 0;
@@ -127,6 +134,9 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   if (st != ATTN_OK) return st;
   if (!g_bwd_ready.count(dev)) {
     cudaError_t e = set_bwd_attributes();
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(bwd::bwd_worklist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               2 * (bwd::kMaxCostBuckets + 1) * (int)sizeof(int));
     if (e != cudaSuccess) return attn_host::lib_cuda_fail(e);
     g_bwd_ready.insert(dev);
   }
@@ -137,8 +147,12 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   if ((st = attn_host::lib_make_map(&mdo, dout, tokens, H, d)) != ATTN_OK) return st;
   int* counters = nullptr;
   float *lse2 = nullptr, *dd = nullptr;
-  if ((st = bwd_workspace(dev, stream, (size_t)units * bwd::kTile, &counters, &lse2, &dd)) !=
-      ATTN_OK)
+  int* lists = nullptr;
+  // lists: [0] tile count, tile_off [B + 1] (at 8), then three (sequence, tile) lists
+  const size_t off_lists = 8 + (size_t)B + 1;
+  const size_t ints = cu_seqlens ? off_lists + 6 * (size_t)max_tiles : 0;
+  if ((st = bwd_workspace(dev, stream, (size_t)units * bwd::kTile, ints, &counters, &lse2, &dd,
+                          &lists)) != ATTN_OK)
     return st;
 
   BwdParams p{};
@@ -148,6 +162,23 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   p.lse2 = lse2;
   p.dd = dd;
   p.err = err;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cu_seqlens) {
+    int* tile_list = lists + off_lists;
+    int* kv_list = tile_list + 2 * max_tiles;
+    int* q_list = kv_list + 2 * max_tiles;
+    p.cu_seqlens = cu_seqlens;
+    p.num_tiles = lists;
+    p.tile_off = lists + 8;
+    p.tile_list = tile_list;
+    p.kv_list = kv_list;
+    p.q_list = q_list;
+    bwd::bwd_worklist_kernel<<<1, 1024, 2 * (T + 1) * sizeof(int), s>>>(
+        cu_seqlens, B, N, causal ? 1 : 0, lists, lists + 8, tile_list, kv_list, q_list, err,
+        (int)max_tiles, counters, counters + 4);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return attn_host::lib_cuda_fail(e);
+  }
   p.B = B;
   p.H = H;
   p.N = N;
@@ -157,7 +188,6 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   p.scale_log2 = (float)((double)scale * 1.4426950408889634);
   p.timeout_ns = 2000000000ull;
   const int grid = (int)std::min<int64_t>(units, sms);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return d == 64 ? launch_bwd<64>(mq, mk, mv, mdo, o, dout, lse, p, counters, grid, s)
-                 : launch_bwd<128>(mq, mk, mv, mdo, o, dout, lse, p, counters, grid, s);
+  return d == 64 ? launch_bwd<64>(mq, mk, mv, mdo, o, dout, lse, p, counters, max_tiles, grid, s)
+                 : launch_bwd<128>(mq, mk, mv, mdo, o, dout, lse, p, counters, max_tiles, grid, s);
 }

@@ -80,17 +80,28 @@ static_assert(kComputeWarps * 32 * kComputeRegs + 128 * kControlRegs <= kThreads
 constexpr int kChunkBytes = kTile * 128;   // 128 rows x 64 bf16 (one 128-byte swizzle span)
 constexpr int kUnitSlots = 2;
 
+constexpr int kMaxCostBuckets = 8192;  // packed batches: at most this many tiles per sequence
+
 constexpr int kErrTimeout = 1;
+constexpr int kErrSeqlens = 2;
+constexpr int kErrWorklist = 4;
 
 struct BwdParams {
   __nv_bfloat16* dq;   // [tokens, H, D]
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  const float* lse2;   // [B*H][T][128]: LSE * log2(e) per row of each query tile (+inf: none)
-  const float* dd;     // [B*H][T][128]: D_i = <dO_i, O_i>
+  const float* lse2;   // [H][tiles][128]: LSE * log2(e) per row of each 128-row tile (+inf: none)
+  const float* dd;     // [H][tiles][128]: D_i = <dO_i, O_i>
   int* err;            // [0] error bits, [1] where a wait gave up
   int* sched;          // [0] next-unit counter, [1] finished CTAs (zero at launch, reset at exit)
-  int B, H, N, T;
+  // packed batches (cu_seqlens != null): the scheduler kernel's lists
+  const int* cu_seqlens;
+  const int* num_tiles;  // tiles of all sequences (one 128-row tile = one unit per head)
+  const int* tile_off;   // [nseq + 1]: first tile of each sequence
+  const int* tile_list;  // [tiles] (sequence, tile) in sequence order
+  const int* kv_list;    // [tiles] (sequence, tile), longest dK/dV unit first
+  const int* q_list;     // [tiles] (sequence, tile), longest dQ unit first
+  int B, H, N, T;        // dense: B sequences of length N, T = ceil(N / 128) tiles each
   int causal;
   float scale;         // softmax scale on the logits
   float scale_log2;    // scale * log2(e)
@@ -246,36 +257,73 @@ __device__ __forceinline__ bool publish_unit(Shared& ss, const BwdParams& p, uin
   return true;
 }
 
-// One unit: (batch b, head h, tile t of 128 rows) and the range of tiles of
-// the other operand it visits, [o0, o0 + n).  Longest first: the dK/dV
-// kernel's causal cost T - t grows as t falls, the dQ kernel's t + 1 as t
-// rises.
+// One unit: (sequence b, head h, tile t of 128 rows) and the range of tiles
+// of the other operand it visits, [o0, o0 + n); tok0 and L place the
+// sequence in the packed tensors, tile0 its first tile in the per-row vectors.
+// Longest first: the dK/dV kernel's causal cost T - t grows as t falls, the
+// dQ kernel's t + 1 as t rises (dense: closed form; packed: the scheduler
+// kernel's sorted lists).
 struct Unit {
   int b, h, t, o0, n;
+  int tok0, L, tile0;
 };
+
+__device__ __forceinline__ int total_tiles(const BwdParams& p) {
+  return p.cu_seqlens ? *p.num_tiles : p.B * p.T;
+}
+
+__device__ __forceinline__ void place(const BwdParams& p, Unit& un) {
+  if (p.cu_seqlens) {
+    un.tok0 = p.cu_seqlens[un.b];
+    un.L = p.cu_seqlens[un.b + 1] - un.tok0;
+    un.tile0 = p.tile_off[un.b];
+  } else {
+    un.tok0 = un.b * p.N;
+    un.L = p.N;
+    un.tile0 = un.b * p.T;
+  }
+}
 
 __device__ __forceinline__ Unit kv_unit(const BwdParams& p, int u) {
   Unit un;
-  const int rank = u / (p.B * p.H);
-  const int rem = u - rank * p.B * p.H;
-  un.b = rem / p.H;
-  un.h = rem - un.b * p.H;
-  un.t = rank;
+  const int e = u / p.H;
+  un.h = u - e * p.H;
+  if (p.cu_seqlens) {
+    un.b = p.kv_list[2 * e];
+    un.t = p.kv_list[2 * e + 1];
+  } else {
+    un.t = e / p.B;
+    un.b = e - un.t * p.B;
+  }
+  place(p, un);
+  const int T = (un.L + kTile - 1) / kTile;
   un.o0 = p.causal ? un.t : 0;
-  un.n = p.T - un.o0;
+  un.n = T - un.o0;
   return un;
 }
 
 __device__ __forceinline__ Unit q_unit(const BwdParams& p, int u) {
   Unit un;
-  const int rank = u / (p.B * p.H);
-  const int rem = u - rank * p.B * p.H;
-  un.b = rem / p.H;
-  un.h = rem - un.b * p.H;
-  un.t = p.T - 1 - rank;
+  const int e = u / p.H;
+  un.h = u - e * p.H;
+  if (p.cu_seqlens) {
+    un.b = p.q_list[2 * e];
+    un.t = p.q_list[2 * e + 1];
+  } else {
+    const int rank = e / p.B;
+    un.b = e - rank * p.B;
+    un.t = p.T - 1 - rank;
+  }
+  place(p, un);
+  const int T = (un.L + kTile - 1) / kTile;
   un.o0 = 0;
-  un.n = p.causal ? un.t + 1 : p.T;
+  un.n = p.causal ? un.t + 1 : T;
   return un;
+}
+
+// Index of row slot 0 of tile t of the unit's sequence in the per-row vectors.
+__device__ __forceinline__ size_t vec_index(const BwdParams& p, const Unit& un, int t) {
+  return ((size_t)un.h * total_tiles(p) + un.tile0 + t) * kTile;
 }
 
 // ------------------------------------------------------------ prologue --
@@ -283,23 +331,35 @@ __device__ __forceinline__ Unit q_unit(const BwdParams& p, int u) {
 // for every row slot of every query tile.  One warp per row slot.
 template <int D>
 __global__ void __launch_bounds__(256)
-bwd_prep_kernel(const __nv_bfloat16* o, const __nv_bfloat16* dout, const float* lse,
-                float* lse2, float* dd, int B, int H, int N, int T) {
+bwd_prep_kernel(const __nv_bfloat16* o, const __nv_bfloat16* dout, const float* lse, BwdParams p,
+                long long slots) {
   const long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / 32;
   const int lane = threadIdx.x % 32;
-  const long long total = (long long)B * H * T * kTile;
-  if (w >= total) return;
+  if (w >= slots) return;
+  const int tiles = total_tiles(p);
+  if (tiles <= 0) return;
   const int r = (int)(w % kTile);
-  const long long bt = w / kTile;
-  const int t = (int)(bt % T);
-  const long long bh = bt / T;
-  const int b = (int)(bh / H), h = (int)(bh % H);
-  const int row = tile_start(t, N) + r;
-  const bool valid = row >= t * kTile;  // (and row < N: the tile ends at N)
+  const long long gt = w / kTile;
+  const int g = (int)(gt % tiles);
+  const int h = (int)(gt / tiles);
+  if (h >= p.H) return;  // (packed: the grid covers an upper bound of the tiles)
+  Unit un;
+  un.h = h;
+  int t;
+  if (p.cu_seqlens) {
+    un.b = p.tile_list[2 * g];
+    t = p.tile_list[2 * g + 1];
+  } else {
+    un.b = g / p.T;
+    t = g - un.b * p.T;
+  }
+  place(p, un);
+  const int row = tile_start(t, un.L) + r;
+  const bool valid = row >= t * kTile;  // (and row < L: the tile ends at L)
   float acc = 0.f;
   if (valid) {
     constexpr int kPer = D / 32;
-    const size_t base = (((size_t)b * N + row) * H + h) * D + lane * kPer;
+    const size_t base = ((size_t)(un.tok0 + row) * p.H + h) * D + lane * kPer;
 #pragma unroll
     for (int c = 0; c < kPer; c += 2) {
       const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(o + base + c);
@@ -311,9 +371,101 @@ bwd_prep_kernel(const __nv_bfloat16* o, const __nv_bfloat16* dout, const float* 
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (lane == 0) {
-    dd[w] = acc;
-    lse2[w] = valid ? lse[((size_t)b * H + h) * N + row] * 1.4426950408889634f : INFINITY;
+    const size_t idx = vec_index(p, un, t) + r;
+    float* dd = const_cast<float*>(p.dd);
+    float* lse2 = const_cast<float*>(p.lse2);
+    dd[idx] = acc;
+    size_t li = 0;
+    if (valid)
+      li = p.cu_seqlens ? (size_t)h * p.cu_seqlens[p.B] + un.tok0 + row
+                        : ((size_t)un.b * p.H + h) * p.N + row;
+    lse2[idx] = valid ? lse[li] * 1.4426950408889634f : INFINITY;
   }
+}
+
+// Packed batches: validates cu_seqlens, lays out the 128-row tiles of every
+// sequence (tile_off, tile_list) and sorts them longest first for each tile
+// kernel (a counting sort over the cost in tiles), and zeroes both kernels'
+// unit counters.  One CTA.  base: [0] tile count, then tile_off [nseq + 1],
+// tile_list, kv_list, q_list (2 ints per entry, max_entries entries each).
+__global__ void __launch_bounds__(1024)
+bwd_worklist_kernel(const int* cu_seqlens, int nseq, int max_len, int causal, int* count,
+                    int* tile_off, int* tile_list, int* kv_list, int* q_list, int* err,
+                    int max_entries, int* sched_kv, int* sched_q) {
+  extern __shared__ int hist[];  // [2][ncost + 1]
+  __shared__ int bad, total;
+  const int ncost = (max_len + kTile - 1) / kTile;
+  int* hkv = hist;
+  int* hq = hist + ncost + 1;
+  for (int i = threadIdx.x; i <= ncost; i += blockDim.x) hkv[i] = hq[i] = 0;
+  if (threadIdx.x == 0) {
+    bad = cu_seqlens[0] != 0;
+    sched_kv[0] = sched_kv[1] = 0;
+    sched_q[0] = sched_q[1] = 0;
+  }
+  __syncthreads();
+  for (int s = threadIdx.x; s < nseq; s += blockDim.x) {
+    const int L = cu_seqlens[s + 1] - cu_seqlens[s];
+    if (L < 0 || L > max_len) bad = 1;
+  }
+  __syncthreads();
+  if (bad) {
+    if (threadIdx.x == 0) {
+      *count = 0;
+      atomicOr(err, kErrSeqlens);
+    }
+    return;
+  }
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int s = 0; s < nseq; ++s) {
+      tile_off[s] = acc;
+      acc += (cu_seqlens[s + 1] - cu_seqlens[s] + kTile - 1) / kTile;
+    }
+    tile_off[nseq] = acc;
+    total = acc;
+  }
+  __syncthreads();
+  if (total > max_entries) {
+    if (threadIdx.x == 0) {
+      *count = 0;
+      atomicOr(err, kErrWorklist);
+    }
+    return;
+  }
+  for (int s = threadIdx.x; s < nseq; s += blockDim.x) {
+    const int T = (cu_seqlens[s + 1] - cu_seqlens[s] + kTile - 1) / kTile;
+    for (int t = 0; t < T; ++t) {
+      tile_list[2 * (tile_off[s] + t)] = s;
+      tile_list[2 * (tile_off[s] + t) + 1] = t;
+      atomicAdd(&hkv[causal ? T - t : T], 1);
+      atomicAdd(&hq[causal ? t + 1 : T], 1);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int okv = 0, oq = 0;
+    for (int c = ncost; c >= 0; --c) {
+      const int a = hkv[c], b = hq[c];
+      hkv[c] = okv;
+      hq[c] = oq;
+      okv += a;
+      oq += b;
+    }
+  }
+  __syncthreads();
+  for (int s = threadIdx.x; s < nseq; s += blockDim.x) {
+    const int T = (cu_seqlens[s + 1] - cu_seqlens[s] + kTile - 1) / kTile;
+    for (int t = 0; t < T; ++t) {
+      const int a = atomicAdd(&hkv[causal ? T - t : T], 1);
+      const int b = atomicAdd(&hq[causal ? t + 1 : T], 1);
+      kv_list[2 * a] = s;
+      kv_list[2 * a + 1] = t;
+      q_list[2 * b] = s;
+      q_list[2 * b + 1] = t;
+    }
+  }
+  if (threadIdx.x == 0) *count = total;
 }
 
 // -------------------------------------------------------- dK/dV kernel --
@@ -331,10 +483,9 @@ __device__ __forceinline__ void kv_producer(const CUtensorMap* tm_q, const CUten
     if (!publish_unit(ss, p, uslot, u) || u < 0) return;
     const int next_u = (int)gridDim.x + atomicAdd(p.sched, 1);
     const Unit un = kv_unit(p, u);
-    const int bh = un.b * p.H + un.h;
     if (units_done > 0 && !wait_bar(ss, kBarResEmpty, (units_done - 1) & 1, p, 102)) return;
     mbar_arrive_expect_tx(bar_addr(ss, kBarResFull), 2 * C::kTileBytes);
-    const int k0 = un.b * p.N + tile_start(un.t, p.N);
+    const int k0 = un.tok0 + tile_start(un.t, un.L);
     for (int c = 0; c < D / 64; ++c) {
       tma_load_3d(smem_u32(sK + c * kChunkBytes), tm_k, bar_addr(ss, kBarResFull), c * 64, un.h, k0);
       tma_load_3d(smem_u32(sV + c * kChunkBytes), tm_v, bar_addr(ss, kBarResFull), c * 64, un.h, k0);
@@ -346,12 +497,12 @@ __device__ __forceinline__ void kv_producer(const CUtensorMap* tm_q, const CUten
       const uint32_t full = bar_addr(ss, kBarStage + slot);
       uint8_t* st = sStage + slot * C::kKvStageBytes;
       mbar_arrive_expect_tx(full, C::kKvStageBytes);
-      const int q0 = un.b * p.N + tile_start(i, p.N);
+      const int q0 = un.tok0 + tile_start(i, un.L);
       for (int c = 0; c < D / 64; ++c) {
         tma_load_3d(smem_u32(st + c * kChunkBytes), tm_q, full, c * 64, un.h, q0);
         tma_load_3d(smem_u32(st + C::kTileBytes + c * kChunkBytes), tm_do, full, c * 64, un.h, q0);
       }
-      const size_t vec = ((size_t)bh * p.T + i) * kTile;
+      const size_t vec = vec_index(p, un, i);
       bulk_load(smem_u32(st + 2 * C::kTileBytes), p.lse2 + vec, 512, full);
       bulk_load(smem_u32(st + 2 * C::kTileBytes + 512), p.dd + vec, 512, full);
       ++ring;
@@ -432,13 +583,13 @@ __device__ __forceinline__ void kv_compute(const BwdParams& p, Shared& ss, uint8
     int u = -1;
     if (!next_unit(ss, p, uslot, true, u) || u < 0) return;
     const Unit un = kv_unit(p, u);
-    const int ks = tile_start(un.t, p.N);
+    const int ks = tile_start(un.t, un.L);
     const int key = ks + kr;
     for (int i = 0; i < un.n; ++i) {
       const uint32_t pos = ring + i;
       const float* sl = reinterpret_cast<const float*>(sStage + (pos % C::kStages) * C::kKvStageBytes +
                                                        2 * C::kTileBytes);
-      const int q0 = tile_start(un.o0 + i, p.N) + 32 * cg;  // query of this warp's column 0
+      const int q0 = tile_start(un.o0 + i, un.L) + 32 * cg;  // query of this warp's column 0
       // the stage's LSE and D vectors are read below: wait for its copies too
       if (!__all_sync(0xffffffffu, wait_bar(ss, kBarStage + pos % C::kStages,
                                             (pos / C::kStages) & 1, p, 123)))
@@ -449,7 +600,7 @@ __device__ __forceinline__ void kv_compute(const BwdParams& p, Shared& ss, uint8
       attn::tmem_ld_x32(lane_addr + kColS + 32 * cg, r);
       attn::tmem_ld_wait_x32(r);
       // P^T = 2^(c s - LSE log2 e); causal: 0 where the key is after the query
-      const bool diag = p.causal && ks + kTile - 1 > tile_start(un.o0 + i, p.N);
+      const bool diag = p.causal && ks + kTile - 1 > tile_start(un.o0 + i, un.L);
       float pf[32];
 #pragma unroll
       for (int c = 0; c < 32; c += 4) {
@@ -499,7 +650,7 @@ __device__ __forceinline__ void kv_compute(const BwdParams& p, Shared& ss, uint8
     if (!__all_sync(0xffffffffu, wait_bar(ss, kBarAccFull, units_done & 1, p, 122))) return;
     tc_fence_after();
     const bool store = key >= un.t * kTile;  // (key < N: the tile ends at N)
-    const size_t row_off = (((size_t)un.b * p.N + (store ? key : 0)) * p.H + un.h) * D + cg * kAccCols;
+    const size_t row_off = ((size_t)(store ? un.tok0 + key : 0) * p.H + un.h) * D + cg * kAccCols;
 #pragma unroll
     for (int which = 0; which < 2; ++which) {
       const uint32_t col = (which == 0 ? kColDV : kColDK) + cg * kAccCols;
@@ -549,7 +700,7 @@ __device__ __forceinline__ void q_producer(const CUtensorMap* tm_q, const CUtens
     const Unit un = q_unit(p, u);
     if (units_done > 0 && !wait_bar(ss, kBarResEmpty, (units_done - 1) & 1, p, 104)) return;
     mbar_arrive_expect_tx(bar_addr(ss, kBarResFull), 2 * C::kTileBytes);
-    const int q0 = un.b * p.N + tile_start(un.t, p.N);
+    const int q0 = un.tok0 + tile_start(un.t, un.L);
     for (int c = 0; c < D / 64; ++c) {
       tma_load_3d(smem_u32(sQ + c * kChunkBytes), tm_q, bar_addr(ss, kBarResFull), c * 64, un.h, q0);
       tma_load_3d(smem_u32(sDO + c * kChunkBytes), tm_do, bar_addr(ss, kBarResFull), c * 64, un.h, q0);
@@ -561,7 +712,7 @@ __device__ __forceinline__ void q_producer(const CUtensorMap* tm_q, const CUtens
       const uint32_t full = bar_addr(ss, kBarStage + slot);
       uint8_t* st = sStage + slot * C::kQStageBytes;
       mbar_arrive_expect_tx(full, C::kQStageBytes);
-      const int k0 = un.b * p.N + tile_start(j, p.N);
+      const int k0 = un.tok0 + tile_start(j, un.L);
       for (int c = 0; c < D / 64; ++c) {
         tma_load_3d(smem_u32(st + c * kChunkBytes), tm_k, full, c * 64, un.h, k0);
         tma_load_3d(smem_u32(st + C::kTileBytes + c * kChunkBytes), tm_v, full, c * 64, un.h, k0);
@@ -641,13 +792,13 @@ __device__ __forceinline__ void q_compute(const BwdParams& p, Shared& ss, uint32
     int u = -1;
     if (!next_unit(ss, p, uslot, true, u) || u < 0) return;
     const Unit un = q_unit(p, u);
-    const int row = tile_start(un.t, p.N) + qr;
-    const size_t vec = ((size_t)(un.b * p.H + un.h) * p.T + un.t) * kTile + qr;
+    const int row = tile_start(un.t, un.L) + qr;
+    const size_t vec = vec_index(p, un, un.t) + qr;
     const float neg_lse2 = -p.lse2[vec];
     const float d_row = p.dd[vec];
     for (int j = 0; j < un.n; ++j) {
       const int jt = un.o0 + j;
-      const int k0 = tile_start(jt, p.N) + 32 * cg;  // key of this warp's column 0
+      const int k0 = tile_start(jt, un.L) + 32 * cg;  // key of this warp's column 0
       if (!__all_sync(0xffffffffu, wait_bar(ss, kBarSFull, scount & 1, p, 150))) return;
       tc_fence_after();
       uint32_t s[32];
@@ -697,7 +848,7 @@ __device__ __forceinline__ void q_compute(const BwdParams& p, Shared& ss, uint32
       attn::tmem_ld_wait_x16(a);
     }
     if (store) {
-      __nv_bfloat16* dst = p.dq + (((size_t)un.b * p.N + row) * p.H + un.h) * D + cg * kAccCols;
+      __nv_bfloat16* dst = p.dq + ((size_t)(un.tok0 + row) * p.H + un.h) * D + cg * kAccCols;
 #pragma unroll
       for (int c = 0; c < kAccCols; c += 8) {
         uint4 v;
@@ -732,7 +883,7 @@ bwd_tile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   uint8_t* sRes1 = smem + C::kTileBytes;     // V or dO
   uint8_t* sStage = smem + 2 * C::kTileBytes;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int n_units = p.B * p.H * p.T;
+  const int n_units = total_tiles(p) * p.H;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kUnitSlots; ++i) {

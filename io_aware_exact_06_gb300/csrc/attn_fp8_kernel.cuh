@@ -104,6 +104,7 @@ struct Fp8Signs {
 };
 
 // ----------------------------------------------------------- quantisers --
+constexpr int kQuantWarps = 16;  // warps per quantiser CTA (one 128-row block)
 // (x * signs) H_128 of the 128 values held 4 per lane (lane l: channels
 // 4l..4l+3), fp32 butterflies over strides 1, 2 (in the lane) and 4..64
 // (across lanes): the lower element of a pair becomes a + b, the upper a - b.
@@ -131,9 +132,9 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
 }
 
 // Quantises one 128-row block of Q or K (rotation, block max, codes) with one
-// CTA of 8 warps; the last block of a sequence is pulled back to end at N and
-// leaves the rows it shares with the block before it to that block.  Each
-// warp holds its 16 rotated rows in registers between the max and the codes.
+// CTA of 16 warps; the last block of a sequence is pulled back to end at N
+// and leaves the rows it shares with the block before it to that block.  Each
+// warp holds its 8 rotated rows in registers between the max and the codes.
 __device__ __forceinline__ void fp8_quant_block(const __nv_bfloat16* x, uint8_t* codes,
                                                 float* scale_out, int b, int h, int t, int H,
                                                 int N, const Fp8Signs& signs, int rotate,
@@ -146,11 +147,11 @@ __device__ __forceinline__ void fp8_quant_block(const __nv_bfloat16* x, uint8_t*
     const int c = 4 * lane + j;
     sgn[j] = rotate && ((signs.bits[c / 32] >> (c % 32)) & 1u) ? -1.0f : 1.0f;
   }
-  constexpr int kRows = kBM / 8;  // rows per warp: warp + 8 i
+  constexpr int kRows = kBM / kQuantWarps;  // rows per warp: warp + kQuantWarps i
   uint2 raw[kRows];
 #pragma unroll
   for (int i = 0; i < kRows; ++i) {
-    const int row = r0 + warp + 8 * i;
+    const int row = r0 + warp + kQuantWarps * i;
     raw[i] = row >= 0 ? *reinterpret_cast<const uint2*>(x + (((size_t)b * N + row) * H + h) * kFp8D +
                                                          4 * lane)
                       : make_uint2(0u, 0u);
@@ -175,12 +176,12 @@ __device__ __forceinline__ void fp8_quant_block(const __nv_bfloat16* x, uint8_t*
   __syncthreads();
   amax = warp_max[0];
 #pragma unroll
-  for (int w = 1; w < 8; ++w) amax = fmaxf(amax, warp_max[w]);
+  for (int w = 1; w < kQuantWarps; ++w) amax = fmaxf(amax, warp_max[w]);
   const float inv = amax > 0.f ? __fdiv_rn(kFp8Max, amax) : 1.0f;
   if (threadIdx.x == 0) *scale_out = amax > 0.f ? __fdiv_rn(amax, kFp8Max) : 1.0f;
 #pragma unroll
   for (int i = 0; i < kRows; ++i) {
-    const int row = r0 + warp + 8 * i;
+    const int row = r0 + warp + kQuantWarps * i;
     if (row < t * kBM) continue;  // the previous block's row (or before the sequence)
     *reinterpret_cast<uint32_t*>(codes + (((size_t)b * N + row) * H + h) * kFp8D + 4 * lane) =
         e4m3x4(__fmul_rn(v[i][0], inv), __fmul_rn(v[i][1], inv), __fmul_rn(v[i][2], inv),
@@ -196,7 +197,7 @@ __device__ __forceinline__ void fp8_amax_block(const __nv_bfloat16* v, unsigned 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   float m = 0.f;
 #pragma unroll 4
-  for (int r = warp; r < kBM; r += 8) {
+  for (int r = warp; r < kBM; r += kQuantWarps) {
     const int row = t * kBM + r;
     if (row >= N) break;
     const uint2 w = *reinterpret_cast<const uint2*>(v + (((size_t)b * N + row) * H + h) * kFp8D +
@@ -212,7 +213,7 @@ __device__ __forceinline__ void fp8_amax_block(const __nv_bfloat16* v, unsigned 
   __syncthreads();
   if (threadIdx.x == 0) {
 #pragma unroll
-    for (int w = 1; w < 8; ++w) m = fmaxf(m, warp_max[w]);
+    for (int w = 1; w < kQuantWarps; ++w) m = fmaxf(m, warp_max[w]);
     atomicMax(amax_bits + b * H + h, __float_as_uint(m));
   }
 }
@@ -220,11 +221,11 @@ __device__ __forceinline__ void fp8_amax_block(const __nv_bfloat16* v, unsigned 
 // One launch for the first quantisation stage: blocks [0, nb) quantise Q
 // (when q is given), [nb, 2 nb) quantise K (when k is given), [2 nb, 3 nb)
 // take the max |V| (when v is given); nb = B * H * T, block = (b * H + h) * T + t.
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(32 * kQuantWarps)
 fp8_quant_stage1_kernel(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv_bfloat16* v,
                         uint8_t* q8, uint8_t* k8, float* sq, float* sk, unsigned int* amax_v,
                         int B, int H, int N, int T, Fp8Signs signs, int rotate, int block0) {
-  __shared__ float warp_max[8];
+  __shared__ float warp_max[kQuantWarps];
   const int nb = B * H * T;
   const int gidx = (int)blockIdx.x + block0;  // block0 skips absent leading segments
   const int seg = gidx / nb, idx = gidx % nb;

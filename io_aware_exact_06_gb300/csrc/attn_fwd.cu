@@ -678,7 +678,7 @@ int launch_quant_stage1(const void* q, const void* k, const void* v, uint8_t* q8
   // segments: Q, K, V (the grid covers the last segment that is present)
   const int nseg = v ? 3 : (k ? 2 : 1);
   const int first = q ? 0 : (k ? 1 : 2);
-  attn::fp8_quant_stage1_kernel<<<(nseg - first) * nb, 256, 0, s>>>(
+  attn::fp8_quant_stage1_kernel<<<(nseg - first) * nb, 32 * attn::kQuantWarps, 0, s>>>(
       reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k),
       reinterpret_cast<const __nv_bfloat16*>(v), q8, k8, sq, sk, amax_v, B, H, N, T,
       pack_signs(signs), signs ? 1 : 0, first * nb);

@@ -91,7 +91,7 @@ def test_binding_raises_on_error(lib):
     (dict(B=-1), -2),
     (dict(d=96), -3),
     (dict(scale=float("nan")), -5),
-    (dict(cu=BUF), -2),
+    (dict(cu=BUF, N=(8193 * 128)), -2),
     (dict(dout=None), -1),
     (dict(dq=None), -1),
     (dict(lse=None), -1),
