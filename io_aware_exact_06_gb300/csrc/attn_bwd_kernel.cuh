@@ -160,6 +160,40 @@ __device__ __forceinline__ void mma_tmem_rows(uint32_t d_tmem, uint32_t a_tmem, 
            BwdCfg<D>::kIdescAcc, kk > 0 ? 1u : acc0);
 }
 
+// D = A B^T over D/16 k-steps with A (128 rows x D bf16, two elements per
+// column, k-step kk in columns 8 kk..) in TMEM and B (128 rows x D) K-major in
+// shared memory as for mma_rows_rows: the dQ kernel's S and dP products with
+// Q and dO kept in TMEM, so that only K and V are read from shared memory.
+template <int D>
+__device__ __forceinline__ void mma_cols_rows(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem) {
+  const uint64_t b0 = make_sdesc(b_smem, 16, 1024, attn::kSwizzle128B);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t off = (uint64_t)(((kk / 4) * kChunkBytes + (kk % 4) * 32) >> 4);
+    mma_ts(d_tmem, a_tmem + 8 * kk, b0 + off, BwdCfg<D>::kIdescS, kk > 0 ? 1u : 0u);
+  }
+}
+
+// Row r of a 128 x D bf16 tile in the 128-byte-swizzled layout of the TMA
+// copies (64-element chunks 16 KB apart, row r's 16-byte unit u at
+// (u ^ (r % 8)) * 16), elements [32 cg, 32 cg + 32), to 16 TMEM columns of
+// this thread's lane (two elements per column).
+template <int D>
+__device__ __forceinline__ void tile_row_to_tmem(const uint8_t* tile, uint32_t taddr, int r, int cg) {
+  const uint8_t* row = tile + (cg / 2) * kChunkBytes + r * 128;
+  uint32_t w[16];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int u = 4 * (cg % 2) + k;
+    const uint4 v = *reinterpret_cast<const uint4*>(row + ((u ^ (r & 7)) << 4));
+    w[4 * k + 0] = v.x;
+    w[4 * k + 1] = v.y;
+    w[4 * k + 2] = v.z;
+    w[4 * k + 3] = v.w;
+  }
+  attn::tmem_st_x16(taddr, w);
+}
+
 // ----------------------------------------------------- shared utilities --
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
@@ -197,7 +231,9 @@ enum : int {
   kBarAccEmpty = 12,  // the compute warps have read them
   kBarDrain = 13,
   kBarStage = 14,     // full[s] = kBarStage + s, empty[s] = kBarStage + 4 + s
-  kMaxBars = kBarStage + 8,
+  kBarQTmemFull = 22, // dQ kernel: the unit's Q and dO are in TMEM
+  kBarQTmemEmpty = 23,// dQ kernel: the unit's products no longer read them
+  kMaxBars = 24,
 };
 
 struct Shared {
@@ -728,8 +764,7 @@ template <int D>
 __device__ __forceinline__ void q_mma(const BwdParams& p, Shared& ss, uint8_t* sQ, uint8_t* sDO,
                                       uint8_t* sStage, uint32_t tmem) {
   using C = BwdCfg<D>;
-  constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
-  const uint32_t q_smem = smem_u32(sQ), do_smem = smem_u32(sDO);
+  constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColQ = 256 + D, kColDO = 256 + D + D / 2;
   auto k_smem = [&](uint32_t pos) { return smem_u32(sStage + (pos % C::kStages) * C::kQStageBytes); };
   auto v_smem = [&](uint32_t pos) { return k_smem(pos) + C::kTileBytes; };
   auto stage_full = [&](uint32_t pos) {
@@ -741,12 +776,13 @@ __device__ __forceinline__ void q_mma(const BwdParams& p, Shared& ss, uint8_t* s
     int u;
     if (!next_unit(ss, p, uslot, false, u) || u < 0) return;
     const Unit un = q_unit(p, u);
-    if (!wait_bar(ss, kBarResFull, units_done & 1, p, 141)) return;
+    // Q and dO of the unit, copied into TMEM by the compute warps
+    if (!wait_bar(ss, kBarQTmemFull, units_done & 1, p, 141)) return;
     if (!stage_full(ring)) return;
     tc_fence_after();
-    mma_rows_rows<D>(tmem + kColS, q_smem, k_smem(ring));     // S = Q K^T
+    mma_cols_rows<D>(tmem + kColS, tmem + kColQ, k_smem(ring));     // S = Q K^T
     mma_commit(bar_addr(ss, kBarSFull));
-    mma_rows_rows<D>(tmem + kColDP, do_smem, v_smem(ring));   // dP = dO V^T
+    mma_cols_rows<D>(tmem + kColDP, tmem + kColDO, v_smem(ring));   // dP = dO V^T
     mma_commit(bar_addr(ss, kBarDPFull));
     for (int j = 0; j < un.n; ++j) {
       const uint32_t pos = ring + j;
@@ -756,7 +792,7 @@ __device__ __forceinline__ void q_mma(const BwdParams& p, Shared& ss, uint8_t* s
       if (more) {
         if (!stage_full(pos + 1)) return;
         tc_fence_after();
-        mma_rows_rows<D>(tmem + kColS, q_smem, k_smem(pos + 1));
+        mma_cols_rows<D>(tmem + kColS, tmem + kColQ, k_smem(pos + 1));
         mma_commit(bar_addr(ss, kBarSFull));
       }
       if (!wait_bar(ss, kBarDSFull, dscount++ & 1, p, 143)) return;
@@ -766,20 +802,21 @@ __device__ __forceinline__ void q_mma(const BwdParams& p, Shared& ss, uint8_t* s
       mma_tmem_rows<D>(tmem + kColDQ, tmem + kColDP, k_smem(pos), j > 0);   // dQ += dS K
       mma_commit(bar_addr(ss, kBarStage + 4 + pos % C::kStages));
       if (more) {
-        mma_rows_rows<D>(tmem + kColDP, do_smem, v_smem(pos + 1));
+        mma_cols_rows<D>(tmem + kColDP, tmem + kColDO, v_smem(pos + 1));
         mma_commit(bar_addr(ss, kBarDPFull));
       }
     }
     ring += un.n;
     mma_commit(bar_addr(ss, kBarAccFull));
-    mma_commit(bar_addr(ss, kBarResEmpty));
+    mma_commit(bar_addr(ss, kBarQTmemEmpty));
     ++units_done;
   }
 }
 
 template <int D>
-__device__ __forceinline__ void q_compute(const BwdParams& p, Shared& ss, uint32_t tmem) {
-  constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+__device__ __forceinline__ void q_compute(const BwdParams& p, Shared& ss, const uint8_t* sQ,
+                                          const uint8_t* sDO, uint32_t tmem) {
+  constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColQ = 256 + D, kColDO = 256 + D + D / 2;
   constexpr int kAccCols = D / 4;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int quadrant = warp % 4, cg = warp / 4;
@@ -796,6 +833,24 @@ __device__ __forceinline__ void q_compute(const BwdParams& p, Shared& ss, uint32
     const size_t vec = vec_index(p, un, un.t) + qr;
     const float neg_lse2 = -p.lse2[vec];
     const float d_row = p.dd[vec];
+    // Q and dO from the producer's tiles into TMEM (once the previous unit's
+    // products are done with it); the tiles are then free for the next unit
+    if (!__all_sync(0xffffffffu, wait_bar(ss, kBarResFull, units_done & 1, p, 153))) return;
+    if (units_done > 0 &&
+        !__all_sync(0xffffffffu, wait_bar(ss, kBarQTmemEmpty, (units_done - 1) & 1, p, 154)))
+      return;
+    tc_fence_after();
+    if (cg < D / 32) {
+      tile_row_to_tmem<D>(sQ, lane_addr + kColQ + 16 * cg, qr, cg);
+      tile_row_to_tmem<D>(sDO, lane_addr + kColDO + 16 * cg, qr, cg);
+    }
+    attn::tmem_st_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(bar_addr(ss, kBarResEmpty));
+      mbar_arrive(bar_addr(ss, kBarQTmemFull));
+    }
     for (int j = 0; j < un.n; ++j) {
       const int jt = un.o0 + j;
       const int k0 = tile_start(jt, un.L) + 32 * cg;  // key of this warp's column 0
@@ -891,7 +946,11 @@ bwd_tile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       mbar_init(bar_addr(ss, kBarUnitEmpty + i), 1 + kComputeWarps);
     }
     mbar_init(bar_addr(ss, kBarResFull), 1);
-    mbar_init(bar_addr(ss, kBarResEmpty), 1);
+    // (dK/dV kernel: released by the MMA thread; dQ kernel: by the compute
+    // warps once they have copied Q and dO into TMEM)
+    mbar_init(bar_addr(ss, kBarResEmpty), kKv ? 1 : kComputeWarps);
+    mbar_init(bar_addr(ss, kBarQTmemFull), kComputeWarps);
+    mbar_init(bar_addr(ss, kBarQTmemEmpty), 1);
     mbar_init(bar_addr(ss, kBarSFull), 1);
     mbar_init(bar_addr(ss, kBarDPFull), 1);
     mbar_init(bar_addr(ss, kBarSCons), kComputeWarps);
@@ -948,7 +1007,7 @@ bwd_tile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (kKv)
       kv_compute<D>(p, ss, sStage, tmem);
     else
-      q_compute<D>(p, ss, tmem);
+      q_compute<D>(p, ss, sRes0, sRes1, tmem);
     __syncwarp();
   }
 
