@@ -60,6 +60,12 @@ class Oracle:
         L.oracle_attn_online.argtypes = [_c_u16p, _c_u16p, _c_u16p, _c_i64p, ctypes.c_int64,
                                          ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
                                          _c_i64p, ctypes.c_int64, ctypes.c_int64, _c_dp, _c_dp]
+        L.oracle_attn_bwd_window.restype = ctypes.c_int
+        L.oracle_attn_bwd_window.argtypes = [_c_u16p, _c_u16p, _c_u16p, _c_u16p, _c_i64p,
+                                             ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_double, ctypes.c_int, ctypes.c_int64,
+                                             ctypes.c_int64, _c_i64p, ctypes.c_int64, _c_dp, _c_dp,
+                                             _c_dp, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
         L.oracle_attn_bwd.restype = ctypes.c_int
         L.oracle_attn_bwd.argtypes = [_c_u16p, _c_u16p, _c_u16p, _c_u16p, _c_i64p, ctypes.c_int64,
                                       ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
@@ -116,11 +122,12 @@ class Oracle:
         return o, lse, used.value
 
     def attn_bwd(self, q, k, v, dout, cu_seqlens, pairs, scale: float, causal: bool,
-                 nthreads: int = 0):
+                 nthreads: int = 0, window=(-1, -1)):
         """dQ, dK, dV (fp64) of the given (seq, head) pairs.
 
         q, k, v, dout: uint16 bf16 bits, [tokens, H, d] (dout = dO, the
-        gradient of the loss with respect to O).  Returns (dq, dk, dv,
+        gradient of the loss with respect to O).  window = (wl, wr): keys
+        i - wl <= j <= i + wr only (negative: unbounded).  Returns (dq, dk, dv,
         threads_used); each gradient is a list with one [L_s, d] array per
         pair.
         """
@@ -134,10 +141,11 @@ class Oracle:
         dk = np.zeros_like(dq)
         dv = np.zeros_like(dq)
         used = ctypes.c_int(0)
-        st = self.lib.oracle_attn_bwd(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16),
+        st = self.lib.oracle_attn_bwd_window(_ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16),
                                       _ptr(v, ctypes.c_uint16), _ptr(dout, ctypes.c_uint16),
                                       _ptr(cu, ctypes.c_int64), len(cu) - 1, H, d, float(scale),
-                                      int(bool(causal)), _ptr(pairs, ctypes.c_int64), len(pairs),
+                                      int(bool(causal)), int(window[0]), int(window[1]),
+                                      _ptr(pairs, ctypes.c_int64), len(pairs),
                                       _ptr(dq, ctypes.c_double), _ptr(dk, ctypes.c_double),
                                       _ptr(dv, ctypes.c_double), int(nthreads), ctypes.byref(used))
         if st != 0:

@@ -51,7 +51,8 @@
  *   dQ_i   = scale * sum_j dS_ij k_j
  *   dK_j   = scale * sum_i dS_ij q_i
  *
- * over the same visible (i, j) pairs as the forward.
+ * over the same visible (i, j) pairs as the forward (with a sliding window:
+ * oracle_attn_bwd_window).
  *
  * FP8 (oracle_fp8_quantize, oracle_attn_rows_f64).  The pages name the FP8
  * forward's two devices without formulas: block quantisation and incoherent
@@ -482,6 +483,7 @@ typedef struct {
     int H, h, d;
     double scale;
     int causal;
+    int64_t wl, wr; /* window: i - wl <= j <= i + wr; negative = unbounded */
     int64_t begin, end; /* query rows of this worker */
     double *dq;         /* [L][d], rows begin..end-1 written */
     double *dk, *dv;    /* [L][d] private accumulators of this worker */
@@ -506,7 +508,13 @@ static void *bwd_worker(void *arg)
         return NULL;
     }
     for (int64_t i = jb->begin; i < jb->end; ++i) {
-        const int64_t nvis = jb->causal ? i + 1 : L;
+        /* visible keys [klo, khi), as in the forward */
+        int64_t klo = 0, khi = jb->causal ? i + 1 : L;
+        if (jb->wl >= 0 && i - jb->wl > klo)
+            klo = i - jb->wl;
+        if (jb->wr >= 0 && i + jb->wr + 1 < khi)
+            khi = i + jb->wr + 1;
+        const int64_t nvis = khi > klo ? khi - klo : 0;
         const uint16_t *qsrc = jb->q + ((base + i) * H + h) * (int64_t)d;
         const uint16_t *doi = jb->dout + ((base + i) * H + h) * (int64_t)d;
         for (int c = 0; c < d; ++c) {
@@ -516,7 +524,7 @@ static void *bwd_worker(void *arg)
         /* the forward's row: S_ij, m_i, l_i, P_ij */
         double m = -INFINITY;
         for (int64_t j = 0; j < nvis; ++j) {
-            const uint16_t *kr = jb->k + ((base + j) * H + h) * (int64_t)d;
+            const uint16_t *kr = jb->k + ((base + klo + j) * H + h) * (int64_t)d;
             double acc = 0.0;
             for (int c = 0; c < d; ++c)
                 acc += qf[c] * widen_bf16(kr[c]);
@@ -532,7 +540,7 @@ static void *bwd_worker(void *arg)
         /* dP_ij = <dO_i, v_j>;  D_i = sum_j P_ij dP_ij */
         double D = 0.0;
         for (int64_t j = 0; j < nvis; ++j) {
-            const uint16_t *vr = jb->v + ((base + j) * H + h) * (int64_t)d;
+            const uint16_t *vr = jb->v + ((base + klo + j) * H + h) * (int64_t)d;
             double acc = 0.0;
             for (int c = 0; c < d; ++c)
                 acc += dorow[c] * widen_bf16(vr[c]);
@@ -545,9 +553,9 @@ static void *bwd_worker(void *arg)
             dqi[c] = 0.0;
         for (int64_t j = 0; j < nvis; ++j) {
             const double ds = p[j] * (dp[j] - D);
-            const uint16_t *kr = jb->k + ((base + j) * H + h) * (int64_t)d;
-            double *dkr = jb->dk + j * (int64_t)d;
-            double *dvr = jb->dv + j * (int64_t)d;
+            const uint16_t *kr = jb->k + ((base + klo + j) * H + h) * (int64_t)d;
+            double *dkr = jb->dk + (klo + j) * (int64_t)d;
+            double *dvr = jb->dv + (klo + j) * (int64_t)d;
             for (int c = 0; c < d; ++c) {
                 dqi[c] += jb->scale * ds * widen_bf16(kr[c]);
                 dkr[c] += jb->scale * ds * qf[c];
@@ -571,10 +579,11 @@ static void *bwd_worker(void *arg)
  * each keeps its own dK, dV sums, added up at the end).  Returns 0 or a
  * negative code.
  */
-int oracle_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                    const uint16_t *dout, const int64_t *cu_seqlens, int64_t nseq, int H,
-                    int d, double scale, int causal, const int64_t *pairs, int64_t npairs,
-                    double *dq, double *dk, double *dv, int nthreads, int *threads_used)
+int oracle_attn_bwd_window(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                           const uint16_t *dout, const int64_t *cu_seqlens, int64_t nseq, int H,
+                           int d, double scale, int causal, int64_t wl, int64_t wr,
+                           const int64_t *pairs, int64_t npairs, double *dq, double *dk,
+                           double *dv, int nthreads, int *threads_used)
 {
     int st = check_common(q, k, v, cu_seqlens, nseq, H, d, scale);
     if (st != ORACLE_OK || !dout || npairs < 0 || (npairs > 0 && (!pairs || !dq || !dk || !dv)))
@@ -610,6 +619,7 @@ int oracle_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
             jb->q = q; jb->k = k; jb->v = v; jb->dout = dout;
             jb->base = base; jb->L = L;
             jb->H = H; jb->h = h; jb->d = d; jb->scale = scale; jb->causal = causal;
+            jb->wl = wl; jb->wr = wr;
             if (causal) {
                 jb->begin = t == 0 ? 0 : (int64_t)((double)L * sqrt((double)t / nt));
                 jb->end = t == nt - 1 ? L : (int64_t)((double)L * sqrt((double)(t + 1) / nt));
@@ -860,4 +870,14 @@ int oracle_attn_rows_f64(const double *q, const double *k, const double *v,
     }
     free(sc);
     return st;
+}
+
+/* The gradients without a window (every visible key). */
+int oracle_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                    const uint16_t *dout, const int64_t *cu_seqlens, int64_t nseq, int H,
+                    int d, double scale, int causal, const int64_t *pairs, int64_t npairs,
+                    double *dq, double *dk, double *dv, int nthreads, int *threads_used)
+{
+    return oracle_attn_bwd_window(q, k, v, dout, cu_seqlens, nseq, H, d, scale, causal, -1, -1,
+                                  pairs, npairs, dq, dk, dv, nthreads, threads_used);
 }

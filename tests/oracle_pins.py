@@ -379,6 +379,65 @@ def check_bwd_finite_differences(orc):
                 _close(grad, num, 1e-7, f"finite differences of {'QKV'[t]} causal={causal}")
 
 
+def check_bwd_window(orc):
+    """Sliding-window gradients: central finite differences of a windowed fp64
+    forward (tied to the pinned windowed forward oracle) and torch autograd
+    through an attention with the window as an explicit boolean mask."""
+    import torch
+    wl_, H, d = [7, 12], 2, 4
+    wlk = _rand_workload(1919, wl_, H=H, d=d)
+    dout = inputs.normal_bf16(1920, wlk.q.size).reshape(wlk.q.shape)
+    qf, kf, vf = (inputs.bf16_bits_to_f64(a) for a in (wlk.q, wlk.k, wlk.v))
+    dof = inputs.bf16_bits_to_f64(dout)
+    scale = 0.55
+    for causal, (a, b) in [(False, (2, 1)), (True, (3, -1)), (False, (0, 0)), (True, (1, 5))]:
+        pairs = _all_pairs(wlk)
+        dq, dk, dv, _ = orc.attn_bwd(wlk.q, wlk.k, wlk.v, dout, wlk.cu_seqlens, pairs, scale, causal,
+                                     window=(a, b))
+        rows = inputs.all_rows(wlk.cu_seqlens, wlk.H)
+        o_or, _, _ = orc.attn_rows(wlk.q, wlk.k, wlk.v, wlk.cu_seqlens, rows, scale, causal, 1,
+                                   window=(a, b))
+        for n, (sq, h) in enumerate(pairs):
+            lo, hi = int(wlk.cu_seqlens[sq]), int(wlk.cu_seqlens[sq + 1])
+            L = hi - lo
+            vis = np.zeros((L, L), dtype=bool)
+            for i in range(L):
+                vis[i, _visible(i, L, causal, a, b)] = True
+
+            def fwd(X):
+                S = scale * (X[0] @ X[1].T)
+                S = np.where(vis, S, -np.inf)
+                S = S - S.max(axis=1, keepdims=True)
+                P = np.exp(S)
+                P /= P.sum(axis=1, keepdims=True)
+                return P @ X[2]
+
+            X = [qf[lo:hi, h].copy(), kf[lo:hi, h].copy(), vf[lo:hi, h].copy()]
+            sel = [r for r, (s2, h2, _) in enumerate(rows) if s2 == sq and h2 == h]
+            _close(fwd(X), o_or[sel], 1e-13, "windowed fp64 forward = oracle forward")
+            G = dof[lo:hi, h]
+            eps = 1e-6
+            for t, grad in enumerate((dq[n], dk[n], dv[n])):
+                num = np.zeros_like(X[t])
+                for idx in np.ndindex(*X[t].shape):
+                    keep = X[t][idx]
+                    X[t][idx] = keep + eps
+                    up = float(np.sum(G * fwd(X)))
+                    X[t][idx] = keep - eps
+                    dn = float(np.sum(G * fwd(X)))
+                    X[t][idx] = keep
+                    num[idx] = (up - dn) / (2 * eps)
+                _close(grad, num, 1e-7, f"window {(a, b)} finite differences of {'QKV'[t]}")
+            # torch autograd with the mask
+            qt, kt, vt = (torch.from_numpy(x.copy()).requires_grad_(True) for x in X)
+            out = torch.nn.functional.scaled_dot_product_attention(
+                qt[None], kt[None], vt[None], attn_mask=torch.from_numpy(vis)[None], scale=scale)[0]
+            out.backward(torch.from_numpy(G.copy()))
+            _close(dq[n], qt.grad.numpy(), 1e-11, f"window {(a, b)} autograd dQ")
+            _close(dk[n], kt.grad.numpy(), 1e-11, f"window {(a, b)} autograd dK")
+            _close(dv[n], vt.grad.numpy(), 1e-11, f"window {(a, b)} autograd dV")
+
+
 def check_bwd_torch_autograd(orc):
     """Library cross-check: torch autograd through SDPA, fp64 on CPU."""
     import torch
@@ -580,6 +639,7 @@ ALL_CHECKS = [
     check_bwd_torch_autograd,
     check_bwd_invariants,
     check_bwd_packing,
+    check_bwd_window,
     check_e4m3_brute_force,
     check_fwht,
     check_fp8_block_quantize,

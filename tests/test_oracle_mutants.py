@@ -48,7 +48,9 @@ MUTANTS = {
     "bwd_dk_from_k": [("dkr[c] += jb->scale * ds * qf[c];",
                        "dkr[c] += jb->scale * ds * widen_bf16(kr[c]);")],
     "bwd_dv_from_ds": [("dvr[c] += p[j] * dorow[c];", "dvr[c] += ds * dorow[c];")],
-    "bwd_causal_ignored": [("const int64_t nvis = jb->causal ? i + 1 : L;", "const int64_t nvis = L;")],
+    "bwd_causal_ignored": [("int64_t klo = 0, khi = jb->causal ? i + 1 : L;", "int64_t klo = 0, khi = L;")],
+    "bwd_window_dk_not_shifted": [("double *dkr = jb->dk + (klo + j) * (int64_t)d;", "double *dkr = jb->dk + j * (int64_t)d;")],
+    "bwd_window_right_ignored": [("            khi = i + jb->wr + 1;", "            khi = khi;")],
     "bwd_dp_from_k": [("acc += dorow[c] * widen_bf16(vr[c]);",
                        "acc += dorow[c] * widen_bf16(jb->k[((base + j) * H + h) * (int64_t)d + c]);")],
     "bwd_unnormalised_p": [("p[j] = exp(p[j] - m) / l;\n        /* dP_ij", "p[j] = exp(p[j] - m);\n        /* dP_ij")],
