@@ -58,6 +58,19 @@ int attn_bwd(const void *q, const void *k, const void *v, const void *o, const v
              const float *lse, void *dq, void *dk, void *dv, int B, int H, int N, int d,
              float scale, int causal, const int32_t *cu_seqlens, attn_stream_t stream);
 
+/*
+ * attn_bwd_window: attn_bwd for attn_fwd_window's sliding window: key j is
+ * visible to query i iff i - window_left <= j <= i + window_right (-1: no
+ * bound on that side), within the sequence and j <= i when causal; the
+ * window and lse must be those of the forward call.  Tiles no query and key
+ * of the window pair up in are skipped.  A window value below -1 returns
+ * ATTN_ERR_SHAPE; otherwise as attn_bwd ((-1, -1) is attn_bwd).
+ */
+int attn_bwd_window(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                    const float *lse, void *dq, void *dk, void *dv, int B, int H, int N, int d,
+                    float scale, int causal, int window_left, int window_right,
+                    const int32_t *cu_seqlens, attn_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

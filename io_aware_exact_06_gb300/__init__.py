@@ -14,7 +14,7 @@ import os
 
 from . import build as _build
 
-__all__ = ["attn_fwd", "attn_bwd", "attn_fwd_fp8", "attn_fp8_quantize_qk", "attn_fp8_quantize_v",
+__all__ = ["attn_fwd", "attn_bwd", "attn_bwd_window", "attn_fwd_fp8", "attn_fp8_quantize_qk", "attn_fp8_quantize_v",
            "attn_fwd_ex", "attn_fwd_noalloc", "attn_fwd_window", "attn_fwd_kvsplit", "attn_last_device_error", "attn_last_error_site",
            "attn_status_string", "AttnError", "AttnFwdOptions", "lib", "forward",
            "EXPORTED_SYMBOLS"]
@@ -22,7 +22,8 @@ __all__ = ["attn_fwd", "attn_bwd", "attn_fwd_fp8", "attn_fp8_quantize_qk", "attn
 # Every symbol the headers under include/ declare.
 EXPORTED_SYMBOLS = ("attn_fwd", "attn_fwd_ex", "attn_last_device_error", "attn_last_error_site",
                     "attn_last_cuda_error", "attn_status_string", "attn_fwd_noalloc",
-                    "attn_fwd_window", "attn_fwd_kvsplit", "attn_bwd", "attn_fwd_fp8",
+                    "attn_fwd_window", "attn_fwd_kvsplit", "attn_bwd", "attn_bwd_window",
+                    "attn_fwd_fp8",
                     "attn_fp8_quantize_qk", "attn_fp8_quantize_v")
 
 ATTN_OK = 0
@@ -65,6 +66,8 @@ def lib() -> ctypes.CDLL:
         L.attn_fwd_kvsplit.restype = i
         L.attn_bwd.argtypes = [vp] * 9 + [i, i, i, i, ctypes.c_float, i, vp, vp]
         L.attn_bwd.restype = i
+        L.attn_bwd_window.argtypes = [vp] * 9 + [i, i, i, i, ctypes.c_float, i, i, i, vp, vp]
+        L.attn_bwd_window.restype = i
         L.attn_fwd_fp8.argtypes = sig[:11] + [vp, vp]
         L.attn_fwd_fp8.restype = i
         L.attn_fp8_quantize_qk.argtypes = [vp, vp, vp, i, i, i, i, vp, vp]
@@ -171,6 +174,19 @@ def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B: int, H: int, N: int, d: int, 
                         int(bool(causal)), _ptr(cu_seqlens), _stream(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_bwd")
+    return st
+
+
+def attn_bwd_window(q, k, v, o, dout, lse, dq, dk, dv, B: int, H: int, N: int, d: int,
+                    scale: float, causal: bool, window_left: int, window_right: int,
+                    cu_seqlens=None, stream=None) -> int:
+    """The C call ``attn_bwd_window`` (the sliding window of attn_fwd_window)."""
+    st = lib().attn_bwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
+                               _ptr(dq), _ptr(dk), _ptr(dv), int(B), int(H), int(N), int(d),
+                               float(scale), int(bool(causal)), int(window_left),
+                               int(window_right), _ptr(cu_seqlens), _stream(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd_window")
     return st
 
 

@@ -107,11 +107,13 @@ int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
 
 }  // namespace
 
-extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o,
-                        const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
-                        int H, int N, int d, float scale, int causal, const int32_t* cu_seqlens,
-                        attn_stream_t stream) {
-  if (B < 0 || H < 0 || N < 0) return ATTN_ERR_SHAPE;
+namespace {
+
+int attn_bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                  const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                  float scale, int causal, int window_left, int window_right,
+                  const int32_t* cu_seqlens, attn_stream_t stream) {
+  if (B < 0 || H < 0 || N < 0 || window_left < -1 || window_right < -1) return ATTN_ERR_SHAPE;
   if (d != 64 && d != 128) return ATTN_ERR_HEADDIM;
   if (!std::isfinite(scale) || scale < 0.0f) return ATTN_ERR_SCALE;
   if (B == 0 || H == 0 || N == 0) return ATTN_OK;
@@ -174,7 +176,8 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
     p.kv_list = kv_list;
     p.q_list = q_list;
     bwd::bwd_worklist_kernel<<<1, 1024, 2 * (T + 1) * sizeof(int), s>>>(
-        cu_seqlens, B, N, causal ? 1 : 0, lists, lists + 8, tile_list, kv_list, q_list, err,
+        cu_seqlens, B, N, causal ? 1 : 0, window_left, window_right, lists, lists + 8, tile_list,
+        kv_list, q_list, err,
         (int)max_tiles, counters, counters + 4);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return attn_host::lib_cuda_fail(e);
@@ -184,10 +187,31 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   p.N = N;
   p.T = (int)T;
   p.causal = causal ? 1 : 0;
+  p.wl = window_left;
+  p.wr = window_right;
   p.scale = scale;
   p.scale_log2 = (float)((double)scale * 1.4426950408889634);
   p.timeout_ns = 2000000000ull;
   const int grid = (int)std::min<int64_t>(units, sms);
   return d == 64 ? launch_bwd<64>(mq, mk, mv, mdo, o, dout, lse, p, counters, max_tiles, grid, s)
                  : launch_bwd<128>(mq, mk, mv, mdo, o, dout, lse, p, counters, max_tiles, grid, s);
+}
+
+}  // namespace
+
+extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                        const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                        int H, int N, int d, float scale, int causal, const int32_t* cu_seqlens,
+                        attn_stream_t stream) {
+  return attn_bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, -1, -1,
+                       cu_seqlens, stream);
+}
+
+extern "C" int attn_bwd_window(const void* q, const void* k, const void* v, const void* o,
+                               const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                               int B, int H, int N, int d, float scale, int causal,
+                               int window_left, int window_right, const int32_t* cu_seqlens,
+                               attn_stream_t stream) {
+  return attn_bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, window_left,
+                       window_right, cu_seqlens, stream);
 }

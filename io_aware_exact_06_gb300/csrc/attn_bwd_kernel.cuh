@@ -103,6 +103,7 @@ struct BwdParams {
   const int* q_list;     // [tiles] (sequence, tile), longest dQ unit first
   int B, H, N, T;        // dense: B sequences of length N, T = ceil(N / 128) tiles each
   int causal;
+  int wl, wr;            // sliding window: keys i - wl <= j <= i + wr visible (-1: unbounded)
   float scale;         // softmax scale on the logits
   float scale_log2;    // scale * log2(e)
   unsigned long long timeout_ns;
@@ -293,6 +294,36 @@ __device__ __forceinline__ bool publish_unit(Shared& ss, const BwdParams& p, uin
   return true;
 }
 
+// Query tiles [o0, o0 + n) holding a query that sees some key of key tile t
+// (nominal keys [128 t, min(128 t + 127, L - 1)]) of a sequence of length L.
+__host__ __device__ __forceinline__ void kv_range(int L, int t, int causal, int wl, int wr, int& o0,
+                                                  int& n) {
+  const int kh = min(t * kTile + kTile - 1, L - 1);
+  int lo = causal ? t * kTile : 0;
+  if (wr >= 0) lo = max(lo, t * kTile - wr);
+  int hi = L - 1;
+  if (wl >= 0) hi = min(hi, kh + wl);
+  lo = max(lo, 0);
+  o0 = lo / kTile;
+  n = hi / kTile + 1 - o0;
+}
+
+// Key tiles [o0, o0 + n) holding a key some row of query tile t sees.
+__host__ __device__ __forceinline__ void q_range(int L, int t, int causal, int wl, int wr, int& o0,
+                                                 int& n) {
+  const int rh = min(t * kTile + kTile - 1, L - 1);
+  const int lo = wl >= 0 ? max(0, t * kTile - wl) : 0;
+  int hi = causal ? rh : L - 1;
+  if (wr >= 0) hi = min(hi, rh + wr);
+  o0 = lo / kTile;
+  n = hi / kTile + 1 - o0;
+}
+
+// Key j visible to query i (both sequence-relative).
+__device__ __forceinline__ bool visible(const BwdParams& p, int i, int j) {
+  return (!p.causal || j <= i) && (p.wl < 0 || j >= i - p.wl) && (p.wr < 0 || j <= i + p.wr);
+}
+
 // One unit: (sequence b, head h, tile t of 128 rows) and the range of tiles
 // of the other operand it visits, [o0, o0 + n); tok0 and L place the
 // sequence in the packed tensors, tile0 its first tile in the per-row vectors.
@@ -332,9 +363,7 @@ __device__ __forceinline__ Unit kv_unit(const BwdParams& p, int u) {
     un.b = e - un.t * p.B;
   }
   place(p, un);
-  const int T = (un.L + kTile - 1) / kTile;
-  un.o0 = p.causal ? un.t : 0;
-  un.n = T - un.o0;
+  kv_range(un.L, un.t, p.causal, p.wl, p.wr, un.o0, un.n);
   return un;
 }
 
@@ -351,9 +380,7 @@ __device__ __forceinline__ Unit q_unit(const BwdParams& p, int u) {
     un.t = p.T - 1 - rank;
   }
   place(p, un);
-  const int T = (un.L + kTile - 1) / kTile;
-  un.o0 = 0;
-  un.n = p.causal ? un.t + 1 : T;
+  q_range(un.L, un.t, p.causal, p.wl, p.wr, un.o0, un.n);
   return un;
 }
 
@@ -425,8 +452,8 @@ bwd_prep_kernel(const __nv_bfloat16* o, const __nv_bfloat16* dout, const float* 
 // unit counters.  One CTA.  base: [0] tile count, then tile_off [nseq + 1],
 // tile_list, kv_list, q_list (2 ints per entry, max_entries entries each).
 __global__ void __launch_bounds__(1024)
-bwd_worklist_kernel(const int* cu_seqlens, int nseq, int max_len, int causal, int* count,
-                    int* tile_off, int* tile_list, int* kv_list, int* q_list, int* err,
+bwd_worklist_kernel(const int* cu_seqlens, int nseq, int max_len, int causal, int wl, int wr,
+                    int* count, int* tile_off, int* tile_list, int* kv_list, int* q_list, int* err,
                     int max_entries, int* sched_kv, int* sched_q) {
   extern __shared__ int hist[];  // [2][ncost + 1]
   __shared__ int bad, total;
@@ -470,12 +497,16 @@ bwd_worklist_kernel(const int* cu_seqlens, int nseq, int max_len, int causal, in
     return;
   }
   for (int s = threadIdx.x; s < nseq; s += blockDim.x) {
-    const int T = (cu_seqlens[s + 1] - cu_seqlens[s] + kTile - 1) / kTile;
+    const int L = cu_seqlens[s + 1] - cu_seqlens[s];
+    const int T = (L + kTile - 1) / kTile;
     for (int t = 0; t < T; ++t) {
       tile_list[2 * (tile_off[s] + t)] = s;
       tile_list[2 * (tile_off[s] + t) + 1] = t;
-      atomicAdd(&hkv[causal ? T - t : T], 1);
-      atomicAdd(&hq[causal ? t + 1 : T], 1);
+      int o0, nkv, nq;
+      kv_range(L, t, causal, wl, wr, o0, nkv);
+      q_range(L, t, causal, wl, wr, o0, nq);
+      atomicAdd(&hkv[nkv], 1);
+      atomicAdd(&hq[nq], 1);
     }
   }
   __syncthreads();
@@ -491,10 +522,14 @@ bwd_worklist_kernel(const int* cu_seqlens, int nseq, int max_len, int causal, in
   }
   __syncthreads();
   for (int s = threadIdx.x; s < nseq; s += blockDim.x) {
-    const int T = (cu_seqlens[s + 1] - cu_seqlens[s] + kTile - 1) / kTile;
+    const int L = cu_seqlens[s + 1] - cu_seqlens[s];
+    const int T = (L + kTile - 1) / kTile;
     for (int t = 0; t < T; ++t) {
-      const int a = atomicAdd(&hkv[causal ? T - t : T], 1);
-      const int b = atomicAdd(&hq[causal ? t + 1 : T], 1);
+      int o0, nkv, nq;
+      kv_range(L, t, causal, wl, wr, o0, nkv);
+      q_range(L, t, causal, wl, wr, o0, nq);
+      const int a = atomicAdd(&hkv[nkv], 1);
+      const int b = atomicAdd(&hq[nq], 1);
       kv_list[2 * a] = s;
       kv_list[2 * a + 1] = t;
       q_list[2 * b] = s;
@@ -635,8 +670,12 @@ __device__ __forceinline__ void kv_compute(const BwdParams& p, Shared& ss, uint8
       uint32_t r[32];
       attn::tmem_ld_x32(lane_addr + kColS + 32 * cg, r);
       attn::tmem_ld_wait_x32(r);
-      // P^T = 2^(c s - LSE log2 e); causal: 0 where the key is after the query
-      const bool diag = p.causal && ks + kTile - 1 > tile_start(un.o0 + i, un.L);
+      // P^T = 2^(c s - LSE log2 e); 0 where the query does not see the key
+      // (causal, sliding window); decided per tile pair, applied per element
+      const int qs = tile_start(un.o0 + i, un.L);
+      const bool diag = (p.causal && ks + kTile - 1 > qs) ||
+                        (p.wl >= 0 && ks < qs + kTile - 1 - p.wl) ||
+                        (p.wr >= 0 && ks + kTile - 1 > qs + p.wr);
       float pf[32];
 #pragma unroll
       for (int c = 0; c < 32; c += 4) {
@@ -649,7 +688,7 @@ __device__ __forceinline__ void kv_compute(const BwdParams& p, Shared& ss, uint8
       if (diag) {
 #pragma unroll
         for (int c = 0; c < 32; ++c)
-          if (key > q0 + c) pf[c] = 0.f;
+          if (!visible(p, q0 + c, key)) pf[c] = 0.f;
       }
       uint32_t w[16];
 #pragma unroll
@@ -868,11 +907,12 @@ __device__ __forceinline__ void q_compute(const BwdParams& p, Shared& ss, const 
       // keys of the previous tile (pulled-back tail) or before the sequence,
       // and keys after the query when causal, contribute nothing
       const int klo = jt * kTile;
-      const bool edge = k0 < klo || (p.causal && k0 + 31 > row);
+      const bool edge = k0 < klo || (p.causal && k0 + 31 > row) ||
+                        (p.wl >= 0 && k0 < row - p.wl) || (p.wr >= 0 && k0 + 31 > row + p.wr);
       if (__any_sync(0xffffffffu, edge)) {
 #pragma unroll
         for (int c = 0; c < 32; ++c)
-          if (k0 + c < klo || (p.causal && k0 + c > row)) pf[c] = 0.f;
+          if (k0 + c < klo || !visible(p, row, k0 + c)) pf[c] = 0.f;
       }
       if (!__all_sync(0xffffffffu, wait_bar(ss, kBarDPFull, scount & 1, p, 151))) return;
       ++scount;

@@ -130,3 +130,8 @@ def test_fp8_argument_errors(lib, args, status):
     assert st == status
     assert lib.attn_fp8_quantize_qk(BUF, BUF, BUF, 1, 1, 128, 64, None, None) == -3
     assert lib.attn_fp8_quantize_v(None, BUF, BUF, 1, 1, 128, 128, None) == -1
+
+
+def test_backward_window_below_minus_one(lib):
+    assert lib.attn_bwd_window(*([BUF] * 9), 1, 1, 128, 64, 0.1, 1, -2, 0, None, None) == -2
+    assert lib.attn_bwd_window(*([BUF] * 9), 1, 1, 128, 64, 0.1, 1, 0, -3, None, None) == -2

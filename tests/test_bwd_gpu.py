@@ -171,6 +171,69 @@ def test_packed_equals_dense(dev):
         assert np.array_equal(x, y)
 
 
+def run_bwd_window(dev, wl, dout_bits, window, packed=False):
+    """CUDA windowed forward then windowed backward (dense or packed)."""
+    import torch
+    import io_aware_exact_06_gb300 as fa
+    H, d = wl.H, wl.d
+    lens = wl.seqlens()
+    N = int(lens.max())
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+    q, k, v, do = t(wl.q), t(wl.k), t(wl.v), t(dout_bits)
+    cu = torch.from_numpy(wl.cu_seqlens.astype(np.int32)).to(dev) if packed else None
+    B = wl.nseq
+    o = torch.empty_like(q)
+    lse = (torch.empty((H, wl.tokens), dtype=torch.float32, device=dev) if packed
+           else torch.empty((B, H, N), dtype=torch.float32, device=dev))
+    fa.attn_fwd_window(q, k, v, o, lse, B, H, N, d, wl.scale, wl.causal, window[0], window[1], cu)
+    grads = [torch.full_like(q, float("nan")) for _ in range(3)]
+    fa.attn_bwd_window(q, k, v, o, do, lse, *grads, B, H, N, d, wl.scale, wl.causal, window[0],
+                       window[1], cu)
+    assert fa.attn_last_device_error() == 0
+    return tuple(x.float().cpu().numpy().astype(np.float64) for x in grads)
+
+
+def compare_window(wl, dout_bits, got, pairs, window, what):
+    ref = oracle.attn_bwd(wl.q, wl.k, wl.v, dout_bits, wl.cu_seqlens, pairs, wl.scale, wl.causal,
+                          window=window)
+    for t, name in enumerate(("dq", "dk", "dv")):
+        r = np.concatenate(ref[t])
+        g = np.concatenate([got[t][int(wl.cu_seqlens[s]):int(wl.cu_seqlens[s + 1]), h]
+                            for s, h in pairs])
+        assert np.isfinite(g).all(), (what, name)
+        rel = np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-300)
+        mx = np.abs(g - r).max()
+        if np.abs(r).max() > 0:
+            assert rel <= REL_L2, (what, name, rel)
+        assert mx <= MAX_ABS_REL * np.abs(r).max() + ABS_FLOOR, (what, name, mx)
+
+
+@pytest.mark.parametrize("window,causal", [((100, 0), True), ((64, 64), False), ((0, 300), False),
+                                           ((200, -1), True), ((-1, 130), False), ((0, 0), False)])
+@pytest.mark.parametrize("d", [64, 128])
+def test_window_dense(dev, window, causal, d):
+    wl, dout = make(2800 + d + window[0] + 3 * window[1], 2, 1000, 2, d, causal)
+    compare_window(wl, dout, run_bwd_window(dev, wl, dout, window), all_pairs(wl), window,
+                   f"window {window} causal={causal} d={d}")
+
+
+def test_window_packed(dev):
+    lens = [0, 1, 77, 300, 1000, 513]
+    wl = inputs.make_workload("bwd_win_packed", 2900, lens, 2, 128, True, varlen=True)
+    dout = inputs.normal_bf16(2901, wl.q.size).reshape(wl.q.shape)
+    pairs = [(s, h) for s in range(wl.nseq) for h in range(wl.H) if lens[s] > 0]
+    compare_window(wl, dout, run_bwd_window(dev, wl, dout, (150, -1), packed=True), pairs,
+                   (150, -1), "packed window (150, -1)")
+
+
+def test_unbounded_window_is_attn_bwd(dev):
+    wl, dout = make(2950, 2, 700, 2, 128, True)
+    a = run_bwd(dev, wl, dout)
+    b = run_bwd_window(dev, wl, dout, (-1, -1))
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+
+
 def test_zero_upstream_gradient(dev):
     wl, _ = make(2401, 2, 300, 2, 64, True)
     zero = np.zeros_like(wl.q)
