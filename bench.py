@@ -626,7 +626,7 @@ def run_fp8(args, world, rank, local):
     flops_step = wl.flops()
 
     def step():
-        fa.attn_fwd_fp8(q, k, v, o, lse, B, H, N, d, wl.scale, True, signs, stream)
+        fa.attn_fwd_fp8(q, k, v, o, lse, B, H, N, d, wl.scale, True, signs, stream=stream)
 
     for _ in range(max(3, args.warmup)):
         step()

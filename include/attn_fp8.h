@@ -15,9 +15,15 @@
  * P is quantised as e4m3(256 P) before the P V product; fp32 accumulation.
  * This is an approximation of the exact attention of attn_fwd.h.
  *
- * Dense batches only: q, k, v, o [B, N, H, 128] bf16, lse [B, H, N] fp32.
- * Same conventions as attn_fwd.h (device pointers, asynchronous on stream,
- * status codes, error word); d other than 128 returns ATTN_ERR_HEADDIM.
+ * Layouts as in attn_fwd.h.  Dense (cu_seqlens == NULL): q, k, v, o
+ * [B, N, H, 128] bf16, lse [B, H, N] fp32.  Packed (cu_seqlens int32[B+1] on
+ * the device, lengths <= N, checked on the device like attn_fwd's): q, k, v, o
+ * [total, H, 128], lse [H, total], total = cu_seqlens[B].  The per-sequence
+ * outputs of the quantisers keep their dense shapes with N as the length
+ * bound: a sequence of length L has blocks [0, ceil(L / 128)) written, the
+ * rest of its rows untouched.  Same conventions as attn_fwd.h (device
+ * pointers, asynchronous on stream, status codes, error word); d other than
+ * 128 returns ATTN_ERR_HEADDIM.
  */
 #ifndef IO_AWARE_EXACT_06_ATTN_FP8_H
 #define IO_AWARE_EXACT_06_ATTN_FP8_H
@@ -32,34 +38,39 @@ extern "C" {
 
 /*
  * attn_fp8_quantize_qk: the Q or K quantisation step.  x [B, N, H, 128] bf16
- * (device); codes [B, N, H, 128] e4m3 (uint8, device); scales [B, H, T] fp32
- * (device), T = ceil(N / 128): block t holds rows [128 t, 128 t + 128) of a
- * sequence and head, the last block pulled back to end at N (the rows it
- * shares with block t - 1 keep that block's codes).  signs: host array of 128
- * int8 (+1 / -1) for the rotation, or NULL for no rotation.  N >= 1.
+ * (packed: [total, H, 128]); codes e4m3 (uint8) of the same shape; scales
+ * [B, H, T] fp32, T = ceil(N / 128): block t holds rows [128 t, 128 t + 128)
+ * of a sequence (of length L) and head, the last block pulled back to end at L
+ * (the rows it shares with block t - 1 keep that block's codes; rows before
+ * the sequence count as zero).  cu_seqlens: NULL (dense) or as above.  signs:
+ * host array of 128 int8 (+1 / -1) for the rotation, or NULL for no rotation.
  */
 int attn_fp8_quantize_qk(const void *x, uint8_t *codes, float *scales, int B, int H, int N,
-                         int d, const int8_t *signs, attn_stream_t stream);
+                         int d, const int32_t *cu_seqlens, const int8_t *signs,
+                         attn_stream_t stream);
 
 /*
- * attn_fp8_quantize_v: the V quantisation step.  v [B, N, H, 128] bf16;
- * codes_t [B, H, 128, Np] e4m3 with Np = 128 * ceil(N / 128): the codes
- * transposed per sequence and head (keys contiguous), keys >= N zero; scale
- * [B, H] fp32 (max |V| / 448 of the sequence and head).  N >= 1.
+ * attn_fp8_quantize_v: the V quantisation step.  v [B, N, H, 128] bf16
+ * (packed: [total, H, 128]); codes_t [B, H, 128, Np] e4m3 with
+ * Np = 128 * ceil(N / 128): the codes transposed per sequence and head (keys
+ * contiguous), keys L .. 128 ceil(L / 128) - 1 zero for a sequence of length
+ * L; scale [B, H] fp32 (max |V| / 448 of the sequence and head; 1 when that
+ * max is 0; not written for an empty sequence).  cu_seqlens: NULL or as above.
  */
 int attn_fp8_quantize_v(const void *v, uint8_t *codes_t, float *scale, int B, int H, int N,
-                        int d, attn_stream_t stream);
+                        int d, const int32_t *cu_seqlens, attn_stream_t stream);
 
 /*
  * attn_fwd_fp8: O = softmax(scale * Q K^T) V and the LSE through the FP8 path
  * above (quantisation kernels, then the FP8 attention kernel).  scale: finite
- * and >= 0; causal as in attn_fwd.  signs: as for attn_fp8_quantize_qk.  The
- * library keeps a per-(device, stream) workspace for the codes and scales
- * (about 4 * B * N * H * 128 bytes), grown on demand.
+ * and >= 0; causal and cu_seqlens as in attn_fwd (an invalid cu_seqlens sets
+ * ATTN_ERR_SEQLENS in the error word and nothing is computed).  signs: as for
+ * attn_fp8_quantize_qk.  The library keeps a per-(device, stream) workspace
+ * for the codes and scales (about 4 * B * N * H * 128 bytes), grown on demand.
  */
 int attn_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
-                 int N, int d, float scale, int causal, const int8_t *signs,
-                 attn_stream_t stream);
+                 int N, int d, float scale, int causal, const int32_t *cu_seqlens,
+                 const int8_t *signs, attn_stream_t stream);
 
 #ifdef __cplusplus
 }

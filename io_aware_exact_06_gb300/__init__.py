@@ -68,11 +68,11 @@ def lib() -> ctypes.CDLL:
         L.attn_bwd.restype = i
         L.attn_bwd_window.argtypes = [vp] * 9 + [i, i, i, i, ctypes.c_float, i, i, i, vp, vp]
         L.attn_bwd_window.restype = i
-        L.attn_fwd_fp8.argtypes = sig[:11] + [vp, vp]
+        L.attn_fwd_fp8.argtypes = sig[:11] + [vp, vp, vp]
         L.attn_fwd_fp8.restype = i
-        L.attn_fp8_quantize_qk.argtypes = [vp, vp, vp, i, i, i, i, vp, vp]
+        L.attn_fp8_quantize_qk.argtypes = [vp, vp, vp, i, i, i, i, vp, vp, vp]
         L.attn_fp8_quantize_qk.restype = i
-        L.attn_fp8_quantize_v.argtypes = [vp, vp, vp, i, i, i, i, vp]
+        L.attn_fp8_quantize_v.argtypes = [vp, vp, vp, i, i, i, i, vp, vp]
         L.attn_fp8_quantize_v.restype = i
         L.attn_fwd_noalloc.argtypes = sig
         L.attn_fwd_noalloc.restype = i
@@ -202,11 +202,12 @@ def _signs(signs):
 
 
 def attn_fwd_fp8(q, k, v, o, lse, B: int, H: int, N: int, d: int, scale: float, causal: bool,
-                 signs=None, stream=None) -> int:
+                 signs=None, cu_seqlens=None, stream=None) -> int:
     """The C call ``attn_fwd_fp8`` (e4m3 path; signs: 128 x +-1 or None)."""
     keep, sp = _signs(signs)
     st = lib().attn_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(N),
-                            int(d), float(scale), int(bool(causal)), sp, _stream(stream))
+                            int(d), float(scale), int(bool(causal)), _ptr(cu_seqlens), sp,
+                            _stream(stream))
     del keep
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_fp8")
@@ -214,21 +215,22 @@ def attn_fwd_fp8(q, k, v, o, lse, B: int, H: int, N: int, d: int, scale: float, 
 
 
 def attn_fp8_quantize_qk(x, codes, scales, B: int, H: int, N: int, d: int, signs=None,
-                         stream=None) -> int:
+                         cu_seqlens=None, stream=None) -> int:
     """The C call ``attn_fp8_quantize_qk``."""
     keep, sp = _signs(signs)
     st = lib().attn_fp8_quantize_qk(_ptr(x), _ptr(codes), _ptr(scales), int(B), int(H), int(N),
-                                    int(d), sp, _stream(stream))
+                                    int(d), _ptr(cu_seqlens), sp, _stream(stream))
     del keep
     if st != ATTN_OK:
         raise AttnError(st, "attn_fp8_quantize_qk")
     return st
 
 
-def attn_fp8_quantize_v(v, codes_t, scale, B: int, H: int, N: int, d: int, stream=None) -> int:
+def attn_fp8_quantize_v(v, codes_t, scale, B: int, H: int, N: int, d: int, cu_seqlens=None,
+                        stream=None) -> int:
     """The C call ``attn_fp8_quantize_v``."""
     st = lib().attn_fp8_quantize_v(_ptr(v), _ptr(codes_t), _ptr(scale), int(B), int(H), int(N),
-                                   int(d), _stream(stream))
+                                   int(d), _ptr(cu_seqlens), _stream(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_fp8_quantize_v")
     return st

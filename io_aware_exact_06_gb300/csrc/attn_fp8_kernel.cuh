@@ -1,4 +1,5 @@
-// FP8 (e4m3) fused attention forward for sm_103a, d = 128, dense batches.
+// FP8 (e4m3) fused attention forward for sm_103a, d = 128, dense or packed
+// variable-length batches.
 //
 // The pages name the FP8 path's two devices without formulas: block
 // quantisation and incoherent processing ("flash-attention-evolution"
@@ -33,10 +34,17 @@
 //                         warps, P in TMEM over its S), tcgen05.mma of
 //                         kind::f8f6f4, K tiles not pulled back (keys past the
 //                         sequence are masked).
+// Packed batches (cu_seqlens, every length <= N) keep the dense layouts of the
+// scales and of the transposed V codes, indexed by sequence with N the length
+// bound: blocks and key tiles past a sequence's end are neither written nor
+// read.  The quantisers run after the bf16 path's worklist kernel, which
+// validates cu_seqlens; they do nothing when it found no work (an invalid
+// cu_seqlens among the reasons), so no block reads outside [0, cu_seqlens[B]).
 #pragma once
 
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
+#include <cfloat>
 #include <cstdint>
 
 #include "attn_fwd_kernel.cuh"
@@ -84,14 +92,17 @@ __device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint
 }
 
 struct Fp8Params {
-  __nv_bfloat16* o;     // [B*N, H, 128]
-  float* lse;           // [B, H, N]
+  __nv_bfloat16* o;     // [tokens, H, 128]
+  float* lse;           // dense [B, H, N]; packed [H, cu_seqlens[B]]
   const float* sq;      // [B*H][T]: Q block scales
   const float* sk;      // [B*H][T]: K block scales
   const float* sv;      // [B*H]: V scale
+  const int* cu_seqlens;   // null: dense batch of B sequences of length N
+  const int* work;         // packed: longest-first (sequence, q-block) pairs
+  const int* num_entries;  // packed: number of pairs in `work`
   int* err;
   int* sched;
-  int B, H, N, T;
+  int B, H, N, T;          // N: the length (packed: the length bound); T = ceil(N / 128)
   int causal;
   float logit_log2;     // scale * log2(e) / d (the transform's 1/d folded in)
   float scale;
@@ -132,15 +143,16 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
 }
 
 // Quantises one 128-row block of Q or K (rotation, block max, codes) with one
-// CTA of 16 warps; the last block of a sequence is pulled back to end at N
-// and leaves the rows it shares with the block before it to that block.  Each
-// warp holds its 8 rotated rows in registers between the max and the codes.
+// CTA of 16 warps; the last block of a sequence (tokens [tok0, tok0 + L)) is
+// pulled back to end at L and leaves the rows it shares with the block before
+// it to that block; rows before the sequence count as zero.  Each warp holds
+// its 8 rotated rows in registers between the max and the codes.
 __device__ __forceinline__ void fp8_quant_block(const __nv_bfloat16* x, uint8_t* codes,
-                                                float* scale_out, int b, int h, int t, int H,
-                                                int N, const Fp8Signs& signs, int rotate,
+                                                float* scale_out, int tok0, int L, int h, int t,
+                                                int H, const Fp8Signs& signs, int rotate,
                                                 float* warp_max) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int r0 = min(t * kBM, N - kBM);
+  const int r0 = min(t * kBM, L - kBM);
   float sgn[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -152,7 +164,7 @@ __device__ __forceinline__ void fp8_quant_block(const __nv_bfloat16* x, uint8_t*
 #pragma unroll
   for (int i = 0; i < kRows; ++i) {
     const int row = r0 + warp + kQuantWarps * i;
-    raw[i] = row >= 0 ? *reinterpret_cast<const uint2*>(x + (((size_t)b * N + row) * H + h) * kFp8D +
+    raw[i] = row >= 0 ? *reinterpret_cast<const uint2*>(x + ((size_t)(tok0 + row) * H + h) * kFp8D +
                                                          4 * lane)
                       : make_uint2(0u, 0u);
   }
@@ -183,24 +195,25 @@ __device__ __forceinline__ void fp8_quant_block(const __nv_bfloat16* x, uint8_t*
   for (int i = 0; i < kRows; ++i) {
     const int row = r0 + warp + kQuantWarps * i;
     if (row < t * kBM) continue;  // the previous block's row (or before the sequence)
-    *reinterpret_cast<uint32_t*>(codes + (((size_t)b * N + row) * H + h) * kFp8D + 4 * lane) =
+    *reinterpret_cast<uint32_t*>(codes + ((size_t)(tok0 + row) * H + h) * kFp8D + 4 * lane) =
         e4m3x4(__fmul_rn(v[i][0], inv), __fmul_rn(v[i][1], inv), __fmul_rn(v[i][2], inv),
                __fmul_rn(v[i][3], inv));
   }
 }
 
-// max |V| of rows [128 t, 128 t + 128) of one (sequence, head), folded into
-// amax_bits[b*H + h] (bit patterns of non-negative floats order like the
-// floats).
+// max |V| of rows [128 t, 128 t + 128) of one (sequence, head) (tokens
+// [tok0, tok0 + L)), folded into *amax_bits (bit patterns of non-negative
+// floats order like the floats).
 __device__ __forceinline__ void fp8_amax_block(const __nv_bfloat16* v, unsigned int* amax_bits,
-                                               int b, int h, int t, int H, int N, float* warp_max) {
+                                               int tok0, int L, int h, int t, int H,
+                                               float* warp_max) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   float m = 0.f;
 #pragma unroll 4
   for (int r = warp; r < kBM; r += kQuantWarps) {
     const int row = t * kBM + r;
-    if (row >= N) break;
-    const uint2 w = *reinterpret_cast<const uint2*>(v + (((size_t)b * N + row) * H + h) * kFp8D +
+    if (row >= L) break;
+    const uint2 w = *reinterpret_cast<const uint2*>(v + ((size_t)(tok0 + row) * H + h) * kFp8D +
                                                     4 * lane);
     const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&w.x);
     const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&w.y);
@@ -214,8 +227,23 @@ __device__ __forceinline__ void fp8_amax_block(const __nv_bfloat16* v, unsigned 
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int w = 1; w < kQuantWarps; ++w) m = fmaxf(m, warp_max[w]);
-    atomicMax(amax_bits + b * H + h, __float_as_uint(m));
+    atomicMax(amax_bits, __float_as_uint(m));
   }
+}
+
+// Tokens [tok0, tok0 + L) of sequence b; false when block t lies past its end
+// or when the worklist kernel found no work (packed only).
+__device__ __forceinline__ bool fp8_seq_block(const int* cu_seqlens, const int* num_entries,
+                                              int b, int t, int N, int& tok0, int& L) {
+  if (!cu_seqlens) {
+    tok0 = b * N;
+    L = N;
+    return true;
+  }
+  if (*num_entries == 0) return false;
+  tok0 = cu_seqlens[b];
+  L = cu_seqlens[b + 1] - tok0;
+  return t * kBM < L;
 }
 
 // One launch for the first quantisation stage: blocks [0, nb) quantise Q
@@ -224,36 +252,42 @@ __device__ __forceinline__ void fp8_amax_block(const __nv_bfloat16* v, unsigned 
 __global__ void __launch_bounds__(32 * kQuantWarps)
 fp8_quant_stage1_kernel(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv_bfloat16* v,
                         uint8_t* q8, uint8_t* k8, float* sq, float* sk, unsigned int* amax_v,
-                        int B, int H, int N, int T, Fp8Signs signs, int rotate, int block0) {
+                        int B, int H, int N, int T, Fp8Signs signs, int rotate, int block0,
+                        const int* cu_seqlens, const int* num_entries) {
   __shared__ float warp_max[kQuantWarps];
   const int nb = B * H * T;
   const int gidx = (int)blockIdx.x + block0;  // block0 skips absent leading segments
   const int seg = gidx / nb, idx = gidx % nb;
   const int t = idx % T, bh = idx / T;
   const int b = bh / H, h = bh % H;
+  int tok0, L;
+  if (!fp8_seq_block(cu_seqlens, num_entries, b, t, N, tok0, L)) return;  // uniform in the CTA
   if (seg == 0)
-    fp8_quant_block(q, q8, sq + idx, b, h, t, H, N, signs, rotate, warp_max);
+    fp8_quant_block(q, q8, sq + idx, tok0, L, h, t, H, signs, rotate, warp_max);
   else if (seg == 1)
-    fp8_quant_block(k, k8, sk + idx, b, h, t, H, N, signs, rotate, warp_max);
+    fp8_quant_block(k, k8, sk + idx, tok0, L, h, t, H, signs, rotate, warp_max);
   else
-    fp8_amax_block(v, amax_v, b, h, t, H, N, warp_max);
+    fp8_amax_block(v, amax_v + bh, tok0, L, h, t, H, warp_max);
 }
 
 // V codes, transposed: vt[(b*H + h) * 128 + c][key] for keys padded to Np
-// (a multiple of 128; padding keys get code 0).  Also writes the V scale.
+// (a multiple of 128; padding keys of the sequence's last tile get code 0,
+// tiles past its end are not written).  Also writes the V scale.
 // One CTA per (sequence, head, 128 keys): codes go to shared memory key-major
 // (a warp writes one key's 128 bytes), then each thread gathers 16 keys of one
 // channel (the bytes a warp reads at once lie in 8 words: no bank conflict)
 // and writes them as one 16-byte store.
 __global__ void __launch_bounds__(256)
 fp8_quant_v_kernel(const __nv_bfloat16* v, const unsigned int* amax_bits, float* sv, uint8_t* vt,
-                   int B, int H, int N, int Np) {
+                   int B, int H, int N, int Np, const int* cu_seqlens, const int* num_entries) {
   __shared__ __align__(16) uint8_t tile[kBN][kFp8D];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int T = Np / kBN;
   const int t = blockIdx.x % T;
   const int bh = blockIdx.x / T;
   const int b = bh / H, h = bh % H;
+  int tok0, L;
+  if (!fp8_seq_block(cu_seqlens, num_entries, b, t, N, tok0, L)) return;  // uniform in the CTA
   const float amax = __uint_as_float(amax_bits[bh]);
   const float inv = amax > 0.f ? __fdiv_rn(kFp8Max, amax) : 1.0f;
   if (t == 0 && threadIdx.x == 0) sv[bh] = amax > 0.f ? __fdiv_rn(amax, kFp8Max) : 1.0f;
@@ -261,8 +295,8 @@ fp8_quant_v_kernel(const __nv_bfloat16* v, const unsigned int* amax_bits, float*
   for (int r = warp; r < kBN; r += 8) {
     const int key = t * kBN + r;
     float f[4] = {0.f, 0.f, 0.f, 0.f};
-    if (key < N) {
-      const uint2 w = *reinterpret_cast<const uint2*>(v + (((size_t)b * N + key) * H + h) * kFp8D +
+    if (key < L) {
+      const uint2 w = *reinterpret_cast<const uint2*>(v + ((size_t)(tok0 + key) * H + h) * kFp8D +
                                                       4 * lane);
       const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&w.x);
       const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&w.y);
@@ -332,26 +366,44 @@ __device__ __forceinline__ bool fp8_wait(SharedState& ss, int bar, uint32_t pari
   }
 }
 
-// Unit u: rows [256 qb, +256) of head h of sequence b; KV tiles [0, nkv).
+// Unit u: rows [256 qb, +256) of head h of sequence b (tokens [tok0, tok0 +
+// L)); KV tiles [0, nkv).  Dense: q-blocks in decreasing cost, then batch,
+// then head; packed: the worklist kernel's longest-first pairs, then head.
 struct Fp8Unit {
-  int b, h, qb, nkv;
+  int b, h, qb, nkv, tok0, L;
 };
+
+__device__ __forceinline__ int fp8_num_units(const Fp8Params& p) {
+  if (p.cu_seqlens) return *p.num_entries * p.H;
+  return p.B * p.H * ((p.N + kUnitRows - 1) / kUnitRows);
+}
 
 __device__ __forceinline__ Fp8Unit fp8_unit(const Fp8Params& p, int u) {
   Fp8Unit un;
   const int e = u / p.H;
   un.h = u - e * p.H;
-  const int nqb = (p.N + kUnitRows - 1) / kUnitRows;
-  const int rank = e / p.B;
-  un.b = e - rank * p.B;
-  un.qb = nqb - 1 - rank;
-  const int r_hi = min(un.qb * kUnitRows + kUnitRows, p.N) - 1;
-  un.nkv = (p.causal ? r_hi : p.N - 1) / kBN + 1;
+  if (p.cu_seqlens) {
+    un.b = p.work[2 * e];
+    un.qb = p.work[2 * e + 1];
+    un.tok0 = p.cu_seqlens[un.b];
+    un.L = p.cu_seqlens[un.b + 1] - un.tok0;
+  } else {
+    const int nqb = (p.N + kUnitRows - 1) / kUnitRows;
+    const int rank = e / p.B;
+    un.b = e - rank * p.B;
+    un.qb = nqb - 1 - rank;
+    un.tok0 = un.b * p.N;
+    un.L = p.N;
+  }
+  const int r_hi = min(un.qb * kUnitRows + kUnitRows, un.L) - 1;
+  un.nkv = (p.causal ? r_hi : un.L - 1) / kBN + 1;
   return un;
 }
 
-__device__ __forceinline__ int fp8_q_start(const Fp8Params& p, const Fp8Unit& un, int g) {
-  return min(un.qb * kUnitRows + g * kBM, p.N - kBM);
+// First row (sequence-relative) loaded for query tile g, pulled back so the
+// tile ends at the sequence end at the latest.
+__device__ __forceinline__ int fp8_q_start(const Fp8Unit& un, int g) {
+  return min(un.qb * kUnitRows + g * kBM, un.L - kBM);
 }
 
 __device__ __forceinline__ void fp8_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
@@ -378,7 +430,7 @@ __device__ __forceinline__ void fp8_producer(const CUtensorMap* tm_q, const CUte
     mbar_arrive_expect_tx(bar_addr(ss, kBarQFull), kQTiles * kFp8TileBytes);
     for (int g = 0; g < kQTiles; ++g)
       tma_load_3d(smem_u32(sQ + g * kFp8TileBytes), tm_q, bar_addr(ss, kBarQFull), 0, un.h,
-                  un.b * p.N + fp8_q_start(p, un, g));
+                  un.tok0 + fp8_q_start(un, g));
     for (int j = 0; j < un.nkv; ++j) {
       for (int kind = 0; kind < 2; ++kind) {
         const int slot = ring % kFp8Stages;
@@ -388,7 +440,7 @@ __device__ __forceinline__ void fp8_producer(const CUtensorMap* tm_q, const CUte
         mbar_arrive_expect_tx(full, kFp8TileBytes);
         const uint32_t dst = smem_u32(sRing + slot * kFp8TileBytes);
         if (kind == 0)
-          tma_load_3d(dst, tm_k, full, 0, un.h, un.b * p.N + j * kBN);
+          tma_load_3d(dst, tm_k, full, 0, un.h, un.tok0 + j * kBN);
         else
           tma_load_3d(dst, tm_vt, full, j * kBN, 0, un.b * p.H + un.h);
         ++ring;
@@ -500,14 +552,15 @@ __device__ __forceinline__ void fp8_softmax_loop(const Fp8Params& p, SharedState
     if (u < 0) return;
     const Fp8Unit un = fp8_unit(p, u);
     const int bh = un.b * p.H + un.h;
-    const int a0 = fp8_q_start(p, un, g);
+    const int a0 = fp8_q_start(un, g);
     const int row = a0 + trow;
     const int nominal0 = un.qb * kUnitRows + g * kBM;
     // the quantisation block of this query tile (the pulled-back last block
     // when the tile is pulled back; rows it shares with the block before it
     // are recomputed with the wrong scale here but never stored)
-    const float qfac = p.logit_log2 * p.sq[(size_t)bh * p.T + min(nominal0 / kBM, p.T - 1)];
-    const int khi = p.causal ? min(row, p.N - 1) : p.N - 1;  // this row's last visible key
+    const int t_last = (un.L + kBM - 1) / kBM - 1;
+    const float qfac = p.logit_log2 * p.sq[(size_t)bh * p.T + min(nominal0 / kBM, t_last)];
+    const int khi = p.causal ? min(row, un.L - 1) : un.L - 1;  // this row's last visible key
     float m_used = -INFINITY;  // running max of the log2-scaled logits (moved by > 0.5 only)
     float l = 0.f;             // sum of the fp32 probabilities (this half)
     for (int j = 0; j < un.nkv; ++j) {
@@ -547,7 +600,10 @@ __device__ __forceinline__ void fp8_softmax_loop(const Fp8Params& p, SharedState
       const float mine = fmaxf(max3(mx0, mx1, mx2), mx3);
       ss.row_max[j & 1][g][half][trow] = mine;
       pair_sync(g, quadrant);  // (also orders both halves' S loads before any P store)
-      const float c2t = qfac * p.sk[(size_t)bh * p.T + j];  // log2 units per raw S unit
+      // log2 units per raw S unit, at least the smallest normal float so that a
+      // masked (-inf) logit stays -inf (a zero scale, or tiny block scales,
+      // would give -inf * 0 = NaN)
+      const float c2t = fmaxf(qfac * p.sk[(size_t)bh * p.T + j], FLT_MIN);
       const float raw = fmaxf(mine, ss.row_max[j & 1][g][half ^ 1][trow]);
       const float m_new = fmaxf(m_used, raw == -INFINITY ? -INFINITY : raw * c2t);
       float alpha = 1.0f;
@@ -600,10 +656,10 @@ __device__ __forceinline__ void fp8_softmax_loop(const Fp8Params& p, SharedState
     if (pair_sync_check(g, quadrant, fail)) return;
     fail |= !__all_sync(0xffffffffu, fp8_wait(ss, kBarOFull + g, units_done & 1, p, 222 + g));
     tc_fence_after();
-    const bool store = row >= nominal0 && row < p.N && row >= 0;
+    const bool store = row >= nominal0 && row < un.L && row >= 0;
     const float ofac = l > 0.f ? p.sv[bh] / (kFp8PScale * l) : 0.f;
     __nv_bfloat16* orow =
-        p.o + ((size_t)(store ? un.b * p.N + row : 0) * p.H + un.h) * kFp8D + half * 64;
+        p.o + ((size_t)(store ? un.tok0 + row : 0) * p.H + un.h) * kFp8D + half * 64;
 #pragma unroll
     for (int cc = 0; cc < 64; cc += 32) {
       uint32_t r[32];
@@ -623,7 +679,7 @@ __device__ __forceinline__ void fp8_softmax_loop(const Fp8Params& p, SharedState
       }
     }
     if (store && half == 0)
-      p.lse[(size_t)bh * p.N + row] =
+      p.lse[p.cu_seqlens ? (size_t)un.h * p.cu_seqlens[p.B] + un.tok0 + row : (size_t)bh * p.N + row] =
           l > 0.f ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
     tc_fence_before();
     ++units_done;
@@ -640,7 +696,7 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   uint8_t* sQ = smem;
   uint8_t* sRing = smem + kQTiles * kFp8TileBytes;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int n_units = p.B * p.H * ((p.N + kUnitRows - 1) / kUnitRows);
+  const int n_units = fp8_num_units(p);
 
   if (threadIdx.x == 0) {
     mbar_init(bar_addr(ss, kBarQFull), 1);

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cfloat>
 #include <cmath>
 #include <cstdint>
 #include <map>
@@ -181,6 +182,16 @@ int make_map(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int64_t token
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// The forward kernels' exponent scale c = scale * log2 e, at least the
+// smallest normal float.  They form 2^(c s - c m) with masked logits s = -inf,
+// and c = 0 (scale 0, or a scale whose product underflows) would make that
+// NaN.  With c = 2^-126 every visible key gets 2^(c s - c m) = 1 within the
+// ex2 approximation's error for |s| < 2^100: the uniform average scale 0
+// defines; the LSE takes the caller's scale itself.
+float exp2_scale(float scale) {
+  return (float)std::max((double)scale * 1.4426950408889634, (double)FLT_MIN);
+}
+
 template <int D>
 int launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                 const FwdParams& p, int grid, cudaStream_t s) {
@@ -246,7 +257,7 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* l
   p.wl = window_left;
   p.wr = window_right;
   p.scale = scale;
-  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p.scale_log2 = exp2_scale(scale);
   p.timeout_ns = (opts && opts->wait_timeout_ns) ? opts->wait_timeout_ns : 2000000000ull;
   p.fault_inject = opts ? opts->fault_inject : 0;
 
@@ -439,7 +450,7 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
   p.wl = -1;
   p.wr = -1;
   p.scale = scale;
-  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p.scale_log2 = exp2_scale(scale);
   p.timeout_ns = 2000000000ull;
   p.fault_inject = 0;
 
@@ -542,7 +553,7 @@ extern "C" int attn_fwd_kvsplit(const void* q, const void* k, const void* v, voi
   p.wl = -1;
   p.wr = -1;
   p.scale = scale;
-  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p.scale_log2 = exp2_scale(scale);
   p.timeout_ns = 2000000000ull;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -665,11 +676,38 @@ attn::Fp8Signs pack_signs(const int8_t* signs) {
   return sg;
 }
 
+// Packed batches: validates cu_seqlens and builds the longest-first (sequence,
+// q-block) list in the stream workspace; the quantisers and the attention
+// kernel that follow on the stream read its entry count (0 when cu_seqlens
+// is invalid, with the error word set).  *ws_out: the stream workspace, [0]
+// the entry count, [1, 3) the attention kernel's unit counters, [4, ...) the
+// list.  Dense batches only get the workspace.
+int fp8_worklist(int dev, attn_stream_t stream, DeviceState* ds, const int32_t* cu_seqlens, int B,
+                 int N, int causal, int** ws_out) {
+  const int64_t max_entries = (int64_t)B * ((N + attn::kUnitRows - 1) / attn::kUnitRows);
+  int* ws = nullptr;
+  int st = stream_workspace(dev, stream, cu_seqlens ? max_entries : 0, &ws);
+  if (st != ATTN_OK) return st;
+  if (cu_seqlens) {
+    const int ncost = (int)std::min<int64_t>((N + attn::kBN - 1) / attn::kBN,
+                                             attn::kMaxCostBuckets - 1);
+    attn::build_worklist_kernel<<<1, 1024, (ncost + 1) * sizeof(int),
+                                  reinterpret_cast<cudaStream_t>(stream)>>>(
+        cu_seqlens, B, N, causal, -1, -1, ws + 4, ws, ds->err, (int)max_entries, ws + 1);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  *ws_out = ws;
+  return ATTN_OK;
+}
+
 // First stage: Q and / or K codes and block scales, and / or max |V| per
 // (sequence, head) (amax_v zeroed here first).  Null inputs are skipped.
+// Packed (cu_seqlens): num_entries is the worklist's entry count.
 int launch_quant_stage1(const void* q, const void* k, const void* v, uint8_t* q8, uint8_t* k8,
                         float* sq, float* sk, unsigned int* amax_v, int B, int H, int N,
-                        const int8_t* signs, cudaStream_t s) {
+                        const int8_t* signs, const int32_t* cu_seqlens, const int* num_entries,
+                        cudaStream_t s) {
   const int T = (N + attn::kBM - 1) / attn::kBM;
   const int nb = B * H * T;
   cudaError_t e;
@@ -681,17 +719,18 @@ int launch_quant_stage1(const void* q, const void* k, const void* v, uint8_t* q8
   attn::fp8_quant_stage1_kernel<<<(nseg - first) * nb, 32 * attn::kQuantWarps, 0, s>>>(
       reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k),
       reinterpret_cast<const __nv_bfloat16*>(v), q8, k8, sq, sk, amax_v, B, H, N, T,
-      pack_signs(signs), signs ? 1 : 0, first * nb);
+      pack_signs(signs), signs ? 1 : 0, first * nb, cu_seqlens, num_entries);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
   return ATTN_OK;
 }
 
 int launch_quant_v(const void* v, uint8_t* codes_t, float* scale, unsigned int* amax_bits, int B,
-                   int H, int N, cudaStream_t s) {
+                   int H, int N, const int32_t* cu_seqlens, const int* num_entries,
+                   cudaStream_t s) {
   const int T = (N + attn::kBN - 1) / attn::kBN;
   attn::fp8_quant_v_kernel<<<B * H * T, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(v),
                                                      amax_bits, scale, codes_t, B, H, N,
-                                                     T * attn::kBN);
+                                                     T * attn::kBN, cu_seqlens, num_entries);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
@@ -699,7 +738,8 @@ int launch_quant_v(const void* v, uint8_t* codes_t, float* scale, unsigned int* 
 }  // namespace
 
 extern "C" int attn_fp8_quantize_qk(const void* x, uint8_t* codes, float* scales, int B, int H,
-                                    int N, int d, const int8_t* signs, attn_stream_t stream) {
+                                    int N, int d, const int32_t* cu_seqlens, const int8_t* signs,
+                                    attn_stream_t stream) {
   int st = fp8_check(B, H, N, d);
   if (st != ATTN_OK) return st;
   if (B == 0 || H == 0 || N == 0) return ATTN_OK;
@@ -711,12 +751,14 @@ extern "C" int attn_fp8_quantize_qk(const void* x, uint8_t* codes, float* scales
   if (e != cudaSuccess) return cuda_fail(e);
   DeviceState* ds = nullptr;
   if ((st = device_state(dev, &ds)) != ATTN_OK) return st;
+  int* ws = nullptr;
+  if ((st = fp8_worklist(dev, stream, ds, cu_seqlens, B, N, 0, &ws)) != ATTN_OK) return st;
   return launch_quant_stage1(x, nullptr, nullptr, codes, nullptr, scales, nullptr, nullptr, B, H, N,
-                             signs, reinterpret_cast<cudaStream_t>(stream));
+                             signs, cu_seqlens, ws, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int attn_fp8_quantize_v(const void* v, uint8_t* codes_t, float* scale, int B, int H,
-                                   int N, int d, attn_stream_t stream) {
+                                   int N, int d, const int32_t* cu_seqlens, attn_stream_t stream) {
   int st = fp8_check(B, H, N, d);
   if (st != ATTN_OK) return st;
   if (B == 0 || H == 0 || N == 0) return ATTN_OK;
@@ -732,16 +774,19 @@ extern "C" int attn_fp8_quantize_v(const void* v, uint8_t* codes_t, float* scale
   if ((st = fp8_workspace(dev, stream, (size_t)B * H * sizeof(unsigned int) + 256, &ws)) != ATTN_OK)
     return st;
   unsigned int* amax = reinterpret_cast<unsigned int*>(ws);
+  int* list = nullptr;
+  if ((st = fp8_worklist(dev, stream, ds, cu_seqlens, B, N, 0, &list)) != ATTN_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if ((st = launch_quant_stage1(nullptr, nullptr, v, nullptr, nullptr, nullptr, nullptr, amax, B, H,
-                                N, nullptr, s)) != ATTN_OK)
+                                N, nullptr, cu_seqlens, list, s)) != ATTN_OK)
     return st;
-  return launch_quant_v(v, codes_t, scale, amax, B, H, N, s);
+  return launch_quant_v(v, codes_t, scale, amax, B, H, N, cu_seqlens, list, s);
 }
 
 extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
                             int B, int H, int N, int d, float scale, int causal,
-                            const int8_t* signs, attn_stream_t stream) {
+                            const int32_t* cu_seqlens, const int8_t* signs,
+                            attn_stream_t stream) {
   int st = fp8_check(B, H, N, d);
   if (st != ATTN_OK) return st;
   if (!std::isfinite(scale) || scale < 0.0f) return ATTN_ERR_SCALE;
@@ -779,17 +824,18 @@ extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o
   unsigned int* amax = reinterpret_cast<unsigned int*>(reinterpret_cast<uint8_t*>(sv) + b_v);
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if ((st = launch_quant_stage1(q, k, v, q8, k8, sq, sk, amax, B, H, N, signs, s)) != ATTN_OK)
+  int* list = nullptr;  // [0] entries, [1, 3) unit counters, [4, ...) the packed worklist
+  if ((st = fp8_worklist(dev, stream, ds, cu_seqlens, B, N, causal ? 1 : 0, &list)) != ATTN_OK)
     return st;
-  if ((st = launch_quant_v(v, vt, sv, amax, B, H, N, s)) != ATTN_OK) return st;
+  if ((st = launch_quant_stage1(q, k, v, q8, k8, sq, sk, amax, B, H, N, signs, cu_seqlens, list,
+                                s)) != ATTN_OK)
+    return st;
+  if ((st = launch_quant_v(v, vt, sv, amax, B, H, N, cu_seqlens, list, s)) != ATTN_OK) return st;
 
   CUtensorMap mq, mk, mvt;
   if ((st = make_map_fp8_rows(enc, &mq, q8, tokens, H)) != ATTN_OK) return st;
   if ((st = make_map_fp8_rows(enc, &mk, k8, tokens, H)) != ATTN_OK) return st;
   if ((st = make_map_fp8_vt(enc, &mvt, vt, bh, np)) != ATTN_OK) return st;
-  int* sched = nullptr;
-  if ((st = stream_workspace(dev, stream, 0, &sched)) != ATTN_OK) return st;
-
   attn::Fp8Params p{};
   p.o = reinterpret_cast<__nv_bfloat16*>(o);
   p.lse = lse;
@@ -797,7 +843,10 @@ extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o
   p.sk = sk;
   p.sv = sv;
   p.err = ds->err;
-  p.sched = sched + 1;
+  p.sched = list + 1;
+  p.cu_seqlens = cu_seqlens;
+  p.work = list + 4;
+  p.num_entries = list;
   p.B = B;
   p.H = H;
   p.N = N;
@@ -808,7 +857,7 @@ extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o
   p.logit_log2 = (float)((double)scale * 1.4426950408889634 / (signs ? (double)attn::kFp8D : 1.0));
   p.timeout_ns = 2000000000ull;
   const int64_t units = bh * ((N + attn::kUnitRows - 1) / attn::kUnitRows);
-  const int grid = (int)std::min<int64_t>(units, ds->sms);
+  const int grid = cu_seqlens ? ds->sms : (int)std::min<int64_t>(units, ds->sms);
   attn::attn_fp8_kernel<<<grid, attn::kThreads, attn::kFp8SmemBytes, s>>>(mq, mk, mvt, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
   return ATTN_OK;

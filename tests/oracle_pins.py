@@ -120,11 +120,13 @@ def check_zero_q_or_k(orc):
     zero = np.zeros_like(wl.q)
     rows = inputs.all_rows(wl.cu_seqlens, wl.H)
     vf = inputs.bf16_bits_to_f64(wl.v)
-    for which in ("q", "k"):
+    # Q = 0, K = 0 or scale = 0: every logit is 0
+    for which in ("q", "k", "scale"):
         q = zero if which == "q" else wl.q
         k = zero if which == "k" else wl.k
+        scale = 0.0 if which == "scale" else 0.7
         for causal in (False, True):
-            o, lse, _ = orc.attn_rows(q, k, wl.v, wl.cu_seqlens, rows, 0.7, causal, 2)
+            o, lse, _ = orc.attn_rows(q, k, wl.v, wl.cu_seqlens, rows, scale, causal, 2)
             for n, (s, h, i) in enumerate(rows):
                 base = int(wl.cu_seqlens[s]); L = int(wl.cu_seqlens[s + 1]) - base
                 nvis = i + 1 if causal else L

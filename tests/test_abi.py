@@ -126,10 +126,10 @@ def test_fp8_argument_errors(lib, args, status):
     a = dict(q=BUF, k=BUF, v=BUF, o=BUF, lse=BUF, B=2, H=4, N=256, d=128, scale=0.1, causal=1)
     a.update(args)
     st = lib.attn_fwd_fp8(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"], a["d"],
-                          a["scale"], a["causal"], None, None)
+                          a["scale"], a["causal"], None, None, None)
     assert st == status
-    assert lib.attn_fp8_quantize_qk(BUF, BUF, BUF, 1, 1, 128, 64, None, None) == -3
-    assert lib.attn_fp8_quantize_v(None, BUF, BUF, 1, 1, 128, 128, None) == -1
+    assert lib.attn_fp8_quantize_qk(BUF, BUF, BUF, 1, 1, 128, 64, None, None, None) == -3
+    assert lib.attn_fp8_quantize_v(None, BUF, BUF, 1, 1, 128, 128, None, None) == -1
 
 
 def test_backward_window_below_minus_one(lib):

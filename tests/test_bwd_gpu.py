@@ -234,6 +234,16 @@ def test_unbounded_window_is_attn_bwd(dev):
         assert np.array_equal(x, y)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_zero_scale(dev, causal):
+    # scale 0: P is uniform over the visible keys, dQ = dK = 0 exactly
+    wl = inputs.make_workload("bwd", 2501 + causal, [300] * 2, 2, 128, causal, scale=0.0)
+    dout = inputs.normal_bf16(4 * 2501 + 7, wl.q.size).reshape(wl.q.shape)
+    got = run_bwd(dev, wl, dout)
+    assert not got[0].any() and not got[1].any()
+    compare(wl, dout, got, all_pairs(wl), f"scale 0 causal={causal}")
+
+
 def test_zero_upstream_gradient(dev):
     wl, _ = make(2401, 2, 300, 2, 64, True)
     zero = np.zeros_like(wl.q)

@@ -126,13 +126,12 @@ def errors(got_o, got_lse, ref_o, ref_lse):
     return float(rel), float(np.abs(got_lse - ref_lse).max())
 
 
-def check_case(dev, B, N, H, causal, rotate, seed, outliers):
+def check_case(dev, B, N, H, causal, rotate, seed, outliers, scale=128 ** -0.5):
     q = inputs.normal_bf16(seed, B * N * H * 128).reshape(B * N, H, 128)
     k = inputs.normal_bf16(seed + 1, B * N * H * 128).reshape(B * N, H, 128)
     v = inputs.normal_bf16(seed + 2, B * N * H * 128).reshape(B * N, H, 128)
     if outliers:
         q, k = with_outliers(q, seed + 3), with_outliers(k, seed + 4)
-    scale = 128 ** -0.5
     sg = signs_of(seed + 5) if rotate else None
     got_o, got_lse = run_fp8(dev, q, k, v, B, N, H, causal, sg, scale)
     cu = np.arange(B + 1) * N
@@ -170,9 +169,164 @@ def test_fp8_short_sequence(dev):
     assert rel_e <= REL_EXACT and lse_e <= LSE_EXACT
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_zero_scale(dev, causal):
+    # every visible key weighs 1 (256 P = 256 is exact in e4m3); masked keys 0
+    (rel_d, lse_d), (rel_e, lse_e) = check_case(dev, 2, 300, 2, causal, True, 3450, False, 0.0)
+    assert rel_d <= REL_DEQ and lse_d <= LSE_DEQ
+    assert rel_e <= REL_EXACT and lse_e <= LSE_EXACT
+
+
 def test_incoherent_processing_helps_with_outliers(dev):
     # channels of Q and K 20x larger than the rest: block scales are set by
     # them, the other channels lose precision; the rotation spreads them
     (_, _), (rel_plain, _) = check_case(dev, 1, 1024, 4, False, False, 3500, True)
     (_, _), (rel_rot, _) = check_case(dev, 1, 1024, 4, False, True, 3500, True)
     assert rel_rot < rel_plain, (rel_rot, rel_plain)
+
+
+# ------------------------------------------------------------ packed batches --
+# Packed variable-length batches: every per-sequence quantity is the dense one
+# of that sequence alone (the oracle quantises each sequence on its own).
+
+PACKED_LENS = [300, 0, 1, 128, 77, 513, 256]
+
+
+def packed_inputs(seed, lens, H, scale_v=1.0, outliers=False):
+    """Packed unit-variance Q, K, V (Q with a few 20x channels when outliers)."""
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    total = int(cu[-1])
+    q = inputs.normal_bf16(seed, total * H * 128).reshape(total, H, 128)
+    if outliers:
+        q = with_outliers(q, seed + 3)
+    k = inputs.normal_bf16(seed + 1, total * H * 128).reshape(total, H, 128)
+    v = inputs.normal_bf16(seed + 2, total * H * 128, scale_v).reshape(total, H, 128)
+    return cu, q, k, v
+
+
+def cu_dev(dev, cu):
+    import torch
+    return torch.tensor(np.asarray(cu), dtype=torch.int32, device=dev)
+
+
+@pytest.mark.parametrize("rotate", [False, True])
+def test_quantize_qk_packed_bit_exact(dev, rotate):
+    import torch
+    import io_aware_exact_06_gb300 as fa
+    H, N = 3, max(PACKED_LENS)
+    cu, x, _, _ = packed_inputs(3600, PACKED_LENS, H, outliers=True)
+    sg = signs_of(3601) if rotate else None
+    B, T = len(PACKED_LENS), -(-N // 128)
+    codes = torch.zeros((int(cu[-1]), H, 128), dtype=torch.uint8, device=dev)
+    scales = torch.full((B, H, T), -1.0, dtype=torch.float32, device=dev)
+    fa.attn_fp8_quantize_qk(to_dev(dev, x), codes, scales, B, H, N, 128, sg, cu_dev(dev, cu))
+    assert fa.attn_last_device_error() == 0
+    got_c, got_s = codes.cpu().numpy(), scales.cpu().numpy()
+    for b, L in enumerate(PACKED_LENS):
+        nb = -(-L // 128)
+        assert (got_s[b, :, nb:] == -1.0).all(), "blocks past the sequence are not written"
+        if L == 0:
+            continue
+        ref_c, ref_s = oracle.fp8_quantize(x[cu[b]:cu[b + 1]], 1, L, 128, rotate, sg)
+        assert np.array_equal(got_s[b, :, :nb], ref_s[0]), b
+        assert np.array_equal(got_c[cu[b]:cu[b + 1]], ref_c), b
+
+
+def test_quantize_v_packed_bit_exact(dev):
+    import torch
+    import io_aware_exact_06_gb300 as fa
+    H, N = 3, max(PACKED_LENS)
+    cu, _, _, v = packed_inputs(3700, PACKED_LENS, H, 1.5)
+    B, Np = len(PACKED_LENS), 128 * -(-N // 128)
+    codes_t = torch.full((B, H, 128, Np), 0x55, dtype=torch.uint8, device=dev)
+    scale = torch.full((B, H), -1.0, dtype=torch.float32, device=dev)
+    fa.attn_fp8_quantize_v(to_dev(dev, v), codes_t, scale, B, H, N, 128, cu_dev(dev, cu))
+    assert fa.attn_last_device_error() == 0
+    got, got_s = codes_t.cpu().numpy(), scale.cpu().numpy()
+    for b, L in enumerate(PACKED_LENS):
+        Lp = 128 * -(-L // 128)
+        assert (got[b, :, :, Lp:] == 0x55).all(), "key tiles past the sequence are not written"
+        if L == 0:
+            assert (got_s[b] == -1.0).all()
+            continue
+        ref_c, ref_s = oracle.fp8_quantize(v[cu[b]:cu[b + 1]], 1, L, 0, False)
+        assert np.array_equal(got_s[b], ref_s[0, :, 0]), b
+        assert np.array_equal(got[b, :, :, :L].transpose(2, 0, 1), ref_c), b
+        assert not got[b, :, :, L:Lp].any(), "padding keys of the last tile are zero"
+
+
+def dequantised_packed(x, cu, block_rows, rotate, sg):
+    out = np.zeros(x.shape, dtype=np.float64)
+    for b in range(len(cu) - 1):
+        L = int(cu[b + 1] - cu[b])
+        if L:
+            out[cu[b]:cu[b + 1]] = dequantised(x[cu[b]:cu[b + 1]], 1, L, block_rows, rotate, sg)
+    return out
+
+
+def run_fp8_packed(dev, q, k, v, cu, N, H, causal, sg, scale):
+    import torch
+    import io_aware_exact_06_gb300 as fa
+    total = int(cu[-1])
+    o = torch.full((total, H, 128), 7.0, dtype=torch.bfloat16, device=dev)
+    lse = torch.full((H, total), 7.0, dtype=torch.float32, device=dev)
+    fa.attn_fwd_fp8(to_dev(dev, q), to_dev(dev, k), to_dev(dev, v), o, lse, len(cu) - 1, H, N, 128,
+                    scale, causal, sg, cu_dev(dev, cu))
+    assert fa.attn_last_device_error() == 0
+    return o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("rotate", [False, True])
+def test_fp8_attention_packed(dev, causal, rotate):
+    H, N = 2, max(PACKED_LENS)
+    cu, q, k, v = packed_inputs(3800, PACKED_LENS, H)
+    sg = signs_of(3805) if rotate else None
+    scale = 128 ** -0.5
+    got_o, got_lse = run_fp8_packed(dev, q, k, v, cu, N, H, causal, sg, scale)
+    rows = inputs.sample_rows(cu, H, 100000, seed=3806)  # every row
+    tok = cu[rows[:, 0]] + rows[:, 2]
+    go, gl = got_o[tok, rows[:, 1]], got_lse[rows[:, 1], tok]
+    qd = dequantised_packed(q, cu, 128, rotate, sg)
+    kd = dequantised_packed(k, cu, 128, rotate, sg)
+    vd = dequantised_packed(v, cu, 0, False, None)
+    ref_o, ref_l = oracle.attn_rows_f64(qd, kd, vd, cu, rows, scale / (128 if rotate else 1), causal)
+    rel_d, lse_d = errors(go, gl, ref_o, ref_l)
+    ex_o, ex_l, _ = oracle.attn_rows(q, k, v, cu, rows, scale, causal)
+    rel_e, lse_e = errors(go, gl, ex_o, ex_l)
+    log = os.environ.get("PARITY_LOG")
+    if log:
+        with open(log, "a") as f:
+            f.write(json.dumps({"test": "fp8_packed", "lens": PACKED_LENS, "H": H, "causal": causal,
+                                "rotate": rotate, "vs_dequantised": [rel_d, lse_d],
+                                "vs_exact": [rel_e, lse_e]}) + "\n")
+    assert rel_d <= REL_DEQ and lse_d <= LSE_DEQ, (rel_d, lse_d)
+    assert rel_e <= REL_EXACT and lse_e <= LSE_EXACT, (rel_e, lse_e)
+
+
+def test_fp8_packed_equal_lengths_match_dense(dev):
+    """Equal lengths: the packed call computes every unit as the dense one."""
+    H, N, B = 2, 640, 3
+    cu, q, k, v = packed_inputs(3900, [N] * B, H)
+    sg = signs_of(3901)
+    scale = 128 ** -0.5
+    o_p, lse_p = run_fp8_packed(dev, q, k, v, cu, N, H, True, sg, scale)
+    o_d, lse_d = run_fp8(dev, q, k, v, B, N, H, True, sg, scale)
+    assert np.array_equal(o_p, o_d)
+    assert np.array_equal(lse_p, lse_d.transpose(1, 0, 2).reshape(H, B * N))
+
+
+@pytest.mark.parametrize("bad", ["decreasing", "too_long", "nonzero_start"])
+def test_fp8_invalid_cu_seqlens_reported(dev, bad):
+    import torch
+    import io_aware_exact_06_gb300 as fa
+    H = 2
+    cu, q, k, v = packed_inputs(4000, [100, 100, 100], H)
+    cu_bad = {"decreasing": [0, 150, 120, 300], "too_long": [0, 100, 300, 300],
+              "nonzero_start": [8, 100, 200, 300]}[bad]
+    o = torch.full((300, H, 128), 7.0, dtype=torch.bfloat16, device=dev)
+    lse = torch.full((H, 300), 7.0, dtype=torch.float32, device=dev)
+    fa.attn_fwd_fp8(to_dev(dev, q), to_dev(dev, k), to_dev(dev, v), o, lse, 3, H, 128, 128,
+                    128 ** -0.5, True, None, cu_dev(dev, cu_bad))
+    assert fa.attn_last_device_error() == -8
+    assert (o.float() == 7.0).all() and (lse == 7.0).all(), "nothing is written"

@@ -76,9 +76,9 @@ def run_kvsplit(dev, q, k, v, scale, causal, splits):
     return o.float().cpu().numpy(), lse.cpu().numpy()
 
 
-def check(dev, q, k, v, causal, splits, what):
+def check(dev, q, k, v, causal, splits, what, scale=None):
     B, Nq, H, d = q.shape
-    scale = d ** -0.5
+    scale = d ** -0.5 if scale is None else scale
     o, lse = run_kvsplit(dev, q, k, v, scale, causal, splits)
     bb, hh, rr = np.meshgrid(np.arange(B), np.arange(H), np.arange(Nq), indexing="ij")
     rows = np.stack([bb.ravel(), hh.ravel(), rr.ravel()], axis=1).astype(np.int64)
@@ -135,3 +135,10 @@ def test_causal_needs_enough_keys(dev):
     with pytest.raises(fa.AttnError) as e:
         fa.attn_fwd_kvsplit(1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 1, 1, 200, 100, 64, 0.1, True)
     assert e.value.status == -2
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_zero_scale_is_uniform_average(dev, causal):
+    # every visible key weighs 1 in every KV range; masked keys still weigh 0
+    q, k, v = make_cross(909, 2, 2, 40, 1000, 128)
+    check(dev, q, k, v, causal, 5, "scale 0", scale=0.0)

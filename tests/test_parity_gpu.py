@@ -90,6 +90,27 @@ def test_zero_q_gives_mean_of_visible_v_at_full_size(dev):
     assert lse_err <= parity.LSE_MAX_ABS
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_zero_scale_is_uniform_average(dev, causal):
+    """scale = 0: every visible key has weight 1, O_i is the mean of the
+    visible V rows and LSE_i = log(#visible) (the masked logits must still get
+    weight 0): dense with a ragged tail, packed, and a sliding window."""
+    wl = inputs.make_workload("scale0", 4100 + causal, [300] * 2, 2, 128, causal, scale=0.0)
+    o, lse, st = parity.run_cuda(wl, dev)
+    assert st == 0
+    parity.compare(o, lse, wl, inputs.all_rows(wl.cu_seqlens, wl.H), "scale 0 dense")
+    wl = inputs.make_workload("scale0p", 4102 + causal, [300, 1, 77, 513], 2, 64, causal,
+                              varlen=True, scale=0.0)
+    o, lse, st = parity.run_cuda(wl, dev)
+    assert st == 0
+    parity.compare(o, lse, wl, inputs.all_rows(wl.cu_seqlens, wl.H), "scale 0 packed")
+    wl = inputs.make_workload("scale0w", 4104 + causal, [400] * 2, 2, 128, causal, scale=0.0)
+    o, lse, st = parity.run_cuda(wl, dev, window=(64, 32))
+    assert st == 0
+    parity.compare(o, lse, wl, inputs.all_rows(wl.cu_seqlens, wl.H), "scale 0 window",
+                   window=(64, 32))
+
+
 def test_constant_v_gives_constant_o_varlen(dev):
     wl = workload("varlen")
     c = inputs.f64_to_bf16_bits(np.array([0.8125]))[0]
