@@ -14,9 +14,9 @@
 //     tiles the tensor core multiplies), one per sequence and head for V (its
 //     scale then factors out of the P V sum); a block's max |x| maps to 448,
 //     the largest finite e4m3 value.
-// P = 2^(x - m) <= 2^0.5 is stored as e4m3 of 256 P (the normal e4m3 range then
-// reaches 2^-14), the running max moving whenever it grows by more than 0.5
-// (log2 units), so 256 P stays below 448.
+// P = 2^(x - m) <= 2^0.75 is stored as e4m3 of 256 P (the normal e4m3 range
+// then reaches 2^-14), the running max moving whenever it grows by more than
+// 0.75 (log2 units), so 256 P <= 431 stays below 448.
 //
 // Kernels:
 //   fp8_quant_stage1_kernel  rotation + block quantisation of Q and of K, one
@@ -56,8 +56,8 @@ constexpr int kFp8TileBytes = kBM * kFp8D;   // 128 rows x 128 e4m3 = one 128-by
 constexpr int kFp8Stages = 8;                // K / V ring slots
 constexpr int kFp8SmemBytes = kQTiles * kFp8TileBytes + kFp8Stages * kFp8TileBytes + 1024;
 constexpr float kFp8Max = 448.0f;
-constexpr float kFp8PScale = 256.0f;         // P is stored as e4m3(256 P)
-constexpr float kFp8RescaleLog2 = 0.5f;
+constexpr float kFp8PLog2 = 8.0f;            // P is stored as e4m3(2^8 P)
+constexpr float kFp8RescaleLog2 = 0.75f;
 
 // Instruction descriptor of tcgen05.mma kind::f8f6f4, e4m3 A and B, fp32 D,
 // both operands K-major: [4,6) D format (1 = f32), [7,10) A format (0 =
@@ -116,9 +116,12 @@ struct Fp8Signs {
 
 // ----------------------------------------------------------- quantisers --
 constexpr int kQuantWarps = 16;  // warps per quantiser CTA (one 128-row block)
-// (x * signs) H_128 of the 128 values held 4 per lane (lane l: channels
-// 4l..4l+3), fp32 butterflies over strides 1, 2 (in the lane) and 4..64
-// (across lanes): the lower element of a pair becomes a + b, the upper a - b.
+// x H_128 of the 128 values held 4 per lane (lane l: channels 4l..4l+3),
+// fp32 butterflies over strides 1, 2 (in the lane) and 4..64 (across lanes):
+// the lower element a of a pair becomes a + b, the upper b becomes a - b.
+// Across lanes both are one fma of the lane's own value with a per-lane sign
+// (+1 lower, -1 upper) and the partner's value: fma(+1, a, b) = a + b and
+// fma(-1, b, a) = a - b, each rounded once like the additions.
 __device__ __forceinline__ void fwht128_warp(float (&v)[4], int lane) {
   float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
   v[0] = a0 + a2;
@@ -127,12 +130,9 @@ __device__ __forceinline__ void fwht128_warp(float (&v)[4], int lane) {
   v[3] = a1 - a3;
 #pragma unroll
   for (int m = 1; m < 32; m <<= 1) {
-    const bool upper = lane & m;
+    const float sg = (lane & m) ? -1.0f : 1.0f;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float other = __shfl_xor_sync(0xffffffffu, v[j], m);
-      v[j] = upper ? other - v[j] : v[j] + other;
-    }
+    for (int j = 0; j < 4; ++j) v[j] = fmaf(sg, v[j], __shfl_xor_sync(0xffffffffu, v[j], m));
   }
 }
 
@@ -153,11 +153,15 @@ __device__ __forceinline__ void fp8_quant_block(const __nv_bfloat16* x, uint8_t*
                                                 float* warp_max) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int r0 = min(t * kBM, L - kBM);
-  float sgn[4];
+  // the signs of this lane's channels 4 lane .. 4 lane + 3 as bf16 sign bits
+  // of the two 32-bit words that hold them (negation is exact)
+  uint32_t flip[2] = {0u, 0u};
+  if (rotate) {
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int c = 4 * lane + j;
-    sgn[j] = rotate && ((signs.bits[c / 32] >> (c % 32)) & 1u) ? -1.0f : 1.0f;
+    for (int j = 0; j < 4; ++j) {
+      const int c = 4 * lane + j;
+      if ((signs.bits[c / 32] >> (c % 32)) & 1u) flip[j / 2] |= (j & 1) ? 0x80000000u : 0x8000u;
+    }
   }
   constexpr int kRows = kBM / kQuantWarps;  // rows per warp: warp + kQuantWarps i
   uint2 raw[kRows];
@@ -172,12 +176,11 @@ __device__ __forceinline__ void fp8_quant_block(const __nv_bfloat16* x, uint8_t*
   float amax = 0.f;
 #pragma unroll
   for (int i = 0; i < kRows; ++i) {
-    const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw[i].x);
-    const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw[i].y);
-    v[i][0] = __bfloat162float(p0.x) * sgn[0];
-    v[i][1] = __bfloat162float(p0.y) * sgn[1];
-    v[i][2] = __bfloat162float(p1.x) * sgn[2];
-    v[i][3] = __bfloat162float(p1.y) * sgn[3];
+    const uint32_t w0 = raw[i].x ^ flip[0], w1 = raw[i].y ^ flip[1];
+    v[i][0] = __uint_as_float(w0 << 16);
+    v[i][1] = __uint_as_float(w0 & 0xffff0000u);
+    v[i][2] = __uint_as_float(w1 << 16);
+    v[i][3] = __uint_as_float(w1 & 0xffff0000u);
     if (rotate) fwht128_warp(v[i], lane);
     amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[i][0]), fabsf(v[i][1])),
                              fmaxf(fabsf(v[i][2]), fabsf(v[i][3]))));
@@ -561,7 +564,7 @@ __device__ __forceinline__ void fp8_softmax_loop(const Fp8Params& p, SharedState
     const int t_last = (un.L + kBM - 1) / kBM - 1;
     const float qfac = p.logit_log2 * p.sq[(size_t)bh * p.T + min(nominal0 / kBM, t_last)];
     const int khi = p.causal ? min(row, un.L - 1) : un.L - 1;  // this row's last visible key
-    float m_used = -INFINITY;  // running max of the log2-scaled logits (moved by > 0.5 only)
+    float m_used = -INFINITY;  // running max of the log2-scaled logits (moved by > 0.75 only)
     float l = 0.f;             // sum of the fp32 probabilities (this half)
     for (int j = 0; j < un.nkv; ++j) {
       fail |= !__all_sync(0xffffffffu, fp8_wait(ss, kBarSFull + g, scount & 1, p, 220 + g));
@@ -616,7 +619,8 @@ __device__ __forceinline__ void fp8_softmax_loop(const Fp8Params& p, SharedState
         m_used = m_new;
       }
       const bool rescale_warp = __any_sync(0xffffffffu, resc);
-      const float neg = m_used == -INFINITY ? 0.f : -m_used;
+      // 2^8 P = 2^(x - m + 8): the e4m3 scale of P is folded into the exponent
+      const float neg = (m_used == -INFINITY ? 0.f : -m_used) + kFp8PLog2;
       float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
       uint32_t pw[16];
 #pragma unroll
@@ -628,7 +632,7 @@ __device__ __forceinline__ void fp8_softmax_loop(const Fp8Params& p, SharedState
         const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
         add2(sa0, sa1, p0, p1);
         add2(sb0, sb1, p2, p3);
-        pw[c / 4] = e4m3x4(p0 * kFp8PScale, p1 * kFp8PScale, p2 * kFp8PScale, p3 * kFp8PScale);
+        pw[c / 4] = e4m3x4(p0, p1, p2, p3);
       }
       l = l * alpha + ((sa0 + sa1) + (sb0 + sb1));
       if (rescale_warp) {
@@ -647,7 +651,7 @@ __device__ __forceinline__ void fp8_softmax_loop(const Fp8Params& p, SharedState
       tc_fence_before();
       mbar_arrive(bar_addr(ss, kBarPFull + g));
     }
-    // epilogue: O = O_acc * s_v / (256 l) -> bf16; LSE = ln 2 (m + log2 l)
+    // epilogue (l sums 2^8 P): O = O_acc * s_v / l -> bf16; LSE = ln 2 (m + log2 l - 8)
     ss.row_sum[g][half][0][trow] = l;
     pair_sync(g, quadrant);
     l += ss.row_sum[g][half ^ 1][0][trow];
@@ -657,7 +661,7 @@ __device__ __forceinline__ void fp8_softmax_loop(const Fp8Params& p, SharedState
     fail |= !__all_sync(0xffffffffu, fp8_wait(ss, kBarOFull + g, units_done & 1, p, 222 + g));
     tc_fence_after();
     const bool store = row >= nominal0 && row < un.L && row >= 0;
-    const float ofac = l > 0.f ? p.sv[bh] / (kFp8PScale * l) : 0.f;
+    const float ofac = l > 0.f ? p.sv[bh] / l : 0.f;
     __nv_bfloat16* orow =
         p.o + ((size_t)(store ? un.tok0 + row : 0) * p.H + un.h) * kFp8D + half * 64;
 #pragma unroll
@@ -680,7 +684,7 @@ __device__ __forceinline__ void fp8_softmax_loop(const Fp8Params& p, SharedState
     }
     if (store && half == 0)
       p.lse[p.cu_seqlens ? (size_t)un.h * p.cu_seqlens[p.B] + un.tok0 + row : (size_t)bh * p.N + row] =
-          l > 0.f ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+          l > 0.f ? (m_used + (__log2f(l) - kFp8PLog2)) * 0.69314718055994531f : -INFINITY;
     tc_fence_before();
     ++units_done;
   }

@@ -39,8 +39,11 @@ __global__ void __launch_bounds__(1024, 1) ex2_rate(float* out, long long* cycle
   if (threadIdx.x == 0) cycles[blockIdx.x] = t1 - t0;
 }
 
-// One thread per SM issues n back-to-back 128x256x16 bf16 MMAs into TMEM.
-__global__ void __launch_bounds__(128, 1) mma_rate(long long* cycles, int n, int* err) {
+// One thread per SM issues n back-to-back 128 x N x 16 bf16 MMAs into TMEM,
+// A from shared memory (ts = 0) or from TMEM (ts = 1), B from shared memory;
+// operands K-major with the 128-byte swizzle.
+__global__ void __launch_bounds__(128, 1) mma_rate(long long* cycles, int n, int N, int ts,
+                                                   int* err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -50,7 +53,7 @@ __global__ void __launch_bounds__(128, 1) mma_rate(long long* cycles, int n, int
   for (int i = tid; i < 65536 / 4; i += 128) reinterpret_cast<uint32_t*>(smem)[i] = 0;
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   if (warp == 0) {
-    tmem_alloc(smem_u32(&tmem_base), 256);
+    tmem_alloc(smem_u32(&tmem_base), 512);
     tmem_relinquish();
   }
   if (tid == 0) {
@@ -62,11 +65,15 @@ __global__ void __launch_bounds__(128, 1) mma_rate(long long* cycles, int n, int
   tc_fence_after();
   const uint32_t tmem = tmem_base;
   if (tid == 0) {
-    const uint32_t id = make_idesc_bf16(128, 256, false);
+    const uint32_t id = make_idesc_bf16(128, N, false);
     const uint64_t a = make_sdesc(smem_u32(smem), 16, 1024, kSwizzle128B);
     const uint64_t b = make_sdesc(smem_u32(smem + 16384), 16, 1024, kSwizzle128B);
     const long long t0 = clock64();
-    for (int i = 0; i < n; ++i) mma_ss(tmem, a, b, id, i > 0);
+    if (ts) {
+      for (int i = 0; i < n; ++i) mma_ts(tmem, tmem + 256, b, id, i > 0);  // A: columns 256..263
+    } else {
+      for (int i = 0; i < n; ++i) mma_ss(tmem, a, b, id, i > 0);
+    }
     mma_commit(smem_u32(&bar));
     if (!mbar_wait(smem_u32(&bar), 0, 1000000000ull)) atomicOr(err, 1);
     cycles[blockIdx.x] = clock64() - t0;
@@ -76,7 +83,7 @@ __global__ void __launch_bounds__(128, 1) mma_rate(long long* cycles, int n, int
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 512);
   }
 }
 
@@ -115,19 +122,27 @@ int main() {
   const double ex2_per_clk = 1024.0 * kChains * iters / mean;
 
   const int n = 4096;
-  const size_t smem = 65536 + 1024;
+  // 120 KB of shared memory keeps one CTA per SM (each allocates all of TMEM)
+  const size_t smem = 120 * 1024 + 1024;
   cudaFuncSetAttribute(mma_rate, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  mma_rate<<<sms, 128, smem>>>(cyc, 64, err);
-  mma_rate<<<sms, 128, smem>>>(cyc, n, err);
-  if (!check(cudaDeviceSynchronize(), "mma_rate")) return 1;
-  cudaMemcpy(h.data(), cyc, sms * sizeof(long long), cudaMemcpyDeviceToHost);
+  // flops per clock per SM of 128 x N x 16 products: {N, A from TMEM}
+  const int shapes[5][2] = {{256, 0}, {128, 0}, {64, 0}, {128, 1}, {64, 1}};
+  double rate[5];
+  for (int s = 0; s < 5; ++s) {
+    mma_rate<<<sms, 128, smem>>>(cyc, 64, shapes[s][0], shapes[s][1], err);
+    mma_rate<<<sms, 128, smem>>>(cyc, n, shapes[s][0], shapes[s][1], err);
+    if (!check(cudaDeviceSynchronize(), "mma_rate")) return 1;
+    cudaMemcpy(h.data(), cyc, sms * sizeof(long long), cudaMemcpyDeviceToHost);
+    mean = 0;
+    for (long long c : h) mean += (double)c / sms;
+    rate[s] = 2.0 * 128 * shapes[s][0] * 16 * n / mean;
+  }
   int herr = 0;
   cudaMemcpy(&herr, err, sizeof(int), cudaMemcpyDeviceToHost);
-  mean = 0;
-  for (long long c : h) mean += (double)c / sms;
-  const double mma_flop_per_clk = 2.0 * 128 * 256 * 16 * n / mean;
   printf("{\"sm_count\": %d, \"sm\": \"%d.%d\", \"max_clock_mhz\": %.0f, \"ex2_per_clk_per_sm\": %.2f, "
-         "\"mma_bf16_flop_per_clk_per_sm\": %.1f, \"mma_wait_error\": %d}\n",
-         sms, major, minor, clk_khz / 1000.0, ex2_per_clk, mma_flop_per_clk, herr);
+         "\"mma_bf16_flop_per_clk_per_sm\": %.1f, \"mma_ss_n128\": %.1f, \"mma_ss_n64\": %.1f, "
+         "\"mma_ts_n128\": %.1f, \"mma_ts_n64\": %.1f, \"mma_wait_error\": %d}\n",
+         sms, major, minor, clk_khz / 1000.0, ex2_per_clk, rate[0], rate[1], rate[2], rate[3], rate[4],
+         herr);
   return herr ? 2 : 0;
 }
