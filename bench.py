@@ -8,6 +8,8 @@ with inputs resident in device memory.  Prints one JSON line.
   python bench.py --workload decode   # split-KV decode line (attn_fwd_kvsplit)
   python bench.py --workload bwd      # backward line (attn_bwd)
   python bench.py --workload fp8      # FP8 forward line (attn_fwd_fp8)
+  python bench.py --config stress     # the forward line on another forward workload
+                                      # (tiny, gpt2_causal, long_full, stress, varlen)
 
 Metric: attention forward TFLOP/s, FLOPs = 4*B*H*N^2*d halved for causal,
 whole job (all ranks) / the slowest rank's time.  N > 1 runs one independent
@@ -44,13 +46,27 @@ FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 
 
-def workload_config(wl):
-    c = inputs.CONFIGS[WORKLOAD]
+def workload_config(wl, name=WORKLOAD):
+    c = inputs.CONFIGS[name]
     io_bytes = 4 * wl.tokens * wl.H * wl.d * 2
-    return {"workload": f"{WORKLOAD}: B={c['B']} H={c['H']} N={c['N']} d={c['d']} causal",
-            "B": c["B"], "H": c["H"], "N": c["N"], "d": c["d"], "causal": c["causal"],
-            "scale": "1/sqrt(d)", "inputs": "Q,K,V iid N(0,1) bf16, seeded (SplitMix64 + Box-Muller)",
-            "l2": f"Q,K,V,O = {io_bytes / 1e6:.0f} MB > 129 MB L2 (no flush between steps)"}
+    mask = "causal" if c["causal"] else "non-causal"
+    std = c.get("qk_std", 1.0)
+    dist = "Q,K,V iid N(0,1)" if std == 1.0 else f"Q,K iid N(0,{std:g}^2), V iid N(0,1)"
+    out = {"H": c["H"], "d": c["d"], "causal": c["causal"], "scale": "1/sqrt(d)",
+           "inputs": f"{dist} bf16, seeded (SplitMix64 + Box-Muller)",
+           "l2": (f"Q,K,V,O = {io_bytes / 1e6:.0f} MB > 129 MB L2 (no flush between steps)"
+                  if io_bytes > 129e6 else
+                  f"Q,K,V,O = {io_bytes / 1e6:.1f} MB fit in the 129 MB L2: not flushed, "
+                  f"steps after the first read them from L2")}
+    if "nseq" in c:
+        lens = wl.seqlens()
+        out.update(workload=f"{name}: {c['nseq']} packed sequences, lengths {int(lens.min())}..{int(lens.max())} "
+                            f"(uniform [{c['Lmin']}, {c['Lmax']}]), H={c['H']} d={c['d']} {mask}",
+                   nseq=c["nseq"], tokens=int(wl.tokens))
+    else:
+        out.update(workload=f"{name}: B={c['B']} H={c['H']} N={c['N']} d={c['d']} {mask}",
+                   B=c["B"], N=c["N"])
+    return out
 
 
 def peaks():
@@ -167,7 +183,7 @@ def row_flops(wl, rows) -> float:
     return float(np.sum(4.0 * wl.d * vis))
 
 
-def cpu_baseline(wl, budget_s: float = 15.0):
+def cpu_baseline(wl, budget_s: float = 15.0, name=WORKLOAD):
     import oracle
     rows = oracle_sample(wl, budget_s, seed=0xBA5E)
     t0 = time.perf_counter()
@@ -175,7 +191,7 @@ def cpu_baseline(wl, budget_s: float = 15.0):
     dt = time.perf_counter() - t0
     return {"value": row_flops(wl, rows) / dt / 1e12, "unit": UNIT, "cores": int(used),
             "kind": "oracle",
-            "sample": f"{len(rows)} seeded rows of {WORKLOAD} (fp64, materialised score rows), "
+            "sample": f"{len(rows)} seeded rows of {name} (fp64, materialised score rows), "
                       f"{dt:.1f} s; FLOPs = 4*d per visible key"}
 
 
@@ -235,20 +251,26 @@ def run_cuda(args, world, rank, local):
     __graft_entry__.build()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    wl = inputs.config_workload(WORKLOAD)
-    B, H, N, d = wl.nseq, wl.H, int(wl.seqlens()[0]), wl.d
+    name = args.config
+    wl = inputs.config_workload(name)
+    B, H, N, d = wl.nseq, wl.H, int(wl.seqlens().max()), wl.d
     host = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
     q_h, k_h, v_h = host(wl.q).pin_memory(), host(wl.k).pin_memory(), host(wl.v).pin_memory()
     q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
     o = torch.empty_like(q)
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    if wl.varlen:  # packed: lse [H, tokens], cu_seqlens on the device
+        cu = torch.from_numpy(wl.cu_seqlens.astype(np.int32)).to(dev)
+        lse = torch.empty((H, wl.tokens), dtype=torch.float32, device=dev)
+    else:
+        cu = None
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     o_h = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
     lse_h = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
     stream = torch.cuda.current_stream(dev)
     flops_step = wl.flops()
 
     def step():
-        fa.attn_fwd(q, k, v, o, lse, B, H, N, d, wl.scale, True, None, stream)
+        fa.attn_fwd(q, k, v, o, lse, B, H, N, d, wl.scale, wl.causal, cu, stream)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -312,11 +334,12 @@ def run_cuda(args, world, rank, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": workload_config(wl),
+        "config": workload_config(wl, name),
         "frac_of_dense_bf16_peak": value / world / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                      "frac": achieved / peak, "peak_source": f"{src} bf16_tflops (burst)",
-                     "kernel": "attn_fwd_kernel<128>", "traffic": args.traffic},
+                     "kernel": f"attn_fwd_kernel<{d}>" + (" + build_worklist_kernel" if wl.varlen else ""),
+                     "traffic": args.traffic if name == WORKLOAD else None},
         "clocks": clk.summary(),
         "e2e": {"value": world * flops_step * e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -324,7 +347,7 @@ def run_cuda(args, world, rank, local):
     }
     line["exp_unit_bound"] = exp_unit_bound(line["clocks"].get("sm_mhz"), d, value / world)
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl)
+        line["cpu_baseline"] = cpu_baseline(wl, name=name)
     print(json.dumps(line), flush=True)
 
 
@@ -748,6 +771,9 @@ def main():
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD, choices=[WORKLOAD, "decode", "bwd", "fp8"])
+    ap.add_argument("--config", default=WORKLOAD, choices=sorted(inputs.CONFIGS),
+                    help="forward line only: time another of the forward workloads (the default "
+                         "is the one the metric is quoted on)")
     ap.add_argument("--ref-step-s", type=float, default=0.0,
                     help="reference arm: oracle seconds per step (default: fit the run in ~2.5 min)")
     args = ap.parse_args()
