@@ -352,9 +352,9 @@ def run_cuda(args, world, rank, local):
 
 
 DECODE = {"B": 8, "H": 16, "Nq": 1, "Nk": 32768, "d": 128}
-# DRAM bytes (read + write) of one decode call (split kernel + combine), from
+# DRAM bytes (read + write) of one decode call (decode kernel + combine), from
 # the ncu capture summarised under profiles/ (None once either kernel changes).
-DECODE_TRAFFIC_BYTES = 2_217_673_728 + 875_008
+DECODE_TRAFFIC_BYTES = None
 DECODE_METRIC = "split-KV decode: algorithmic HBM GB/s on 1 GB300 (bf16 K/V cache)"
 
 
@@ -369,7 +369,7 @@ def decode_config(S):
 
 
 def run_decode(args, world, rank, local):
-    """One step = one attn_fwd_kvsplit call (split kernel + combine kernel) of a
+    """One step = one attn_fwd_kvsplit call (decode kernel + combine kernel) of a
     batch of single-token queries against a resident 32768-token K/V cache.
     Metric: algorithmic bytes (K and V read once, Q read, O and LSE written)
     per second; the path is bound by HBM bandwidth."""
@@ -451,7 +451,7 @@ def run_decode(args, world, rank, local):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": decode_config("auto"),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "peak_source": f"{src} hbm_gbs",
-                     "kernel": "attn_fwd_kernel<128, split> + attn_combine_kernel<128> (one call)",
+                     "kernel": "attn_decode_kernel<128, 1> + attn_combine_kernel<128> (one call)",
                      "traffic": DECODE_TRAFFIC_BYTES},
         "clocks": clk.summary(),
         "e2e": {"value": world * bytes_step * n_e2e / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",

@@ -15,6 +15,7 @@
 
 #include "../../include/attn_fp8.h"
 #include "../../include/attn_fwd.h"
+#include "attn_decode_kernel.cuh"
 #include "attn_fp8_kernel.cuh"
 #include "attn_fwd_kernel.cuh"
 #include "attn_host.h"
@@ -503,6 +504,56 @@ extern "C" int attn_fwd_kvsplit(const void* q, const void* k, const void* v, voi
   EncodeTiledFn enc = nullptr;
   if ((st = get_encode(&enc)) != ATTN_OK) return st;
 
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (Nq <= attn::decode::kMaxQ) {
+    // A few queries: the CUDA-core kernel, one work item per (sequence, head,
+    // key range); by default about 16 items per SM, ranges of at least 64 keys.
+    int S = num_splits;
+    if (S == 0) {
+      const int64_t bh = (int64_t)B * H;
+      const int64_t want = ((int64_t)ds->sms * 16 + bh - 1) / bh;
+      S = (int)std::max<int64_t>(1, std::min<int64_t>({want, (Nk + 63) / 64, 256}));
+    }
+    const int chunk = (Nk + S - 1) / S;
+    const int64_t items = (int64_t)B * H * S;
+    const int64_t combine_blocks = (q_tokens * H * 32 + 255) / 256;
+    if (items > INT32_MAX || combine_blocks > INT32_MAX) return ATTN_ERR_SHAPE;
+    float* part = nullptr;
+    const size_t o_floats = (size_t)S * q_tokens * H * d;
+    const size_t lse_floats = (size_t)S * B * H * Nq;
+    if ((st = partial_workspace(dev, stream, o_floats + lse_floats, &part)) != ATTN_OK) return st;
+    float* lse_part = part + o_floats;
+    const int grid = (int)std::min<int64_t>(items, (int64_t)ds->sms * 8);
+    const float c = exp2_scale(scale);
+    const int cz = causal ? 1 : 0;
+    auto q16 = reinterpret_cast<const __nv_bfloat16*>(q);
+    auto k16 = reinterpret_cast<const __nv_bfloat16*>(k);
+    auto v16 = reinterpret_cast<const __nv_bfloat16*>(v);
+    const int nq = Nq <= 1 ? 1 : (Nq <= 2 ? 2 : 4);
+#define ATTN_DECODE_LAUNCH(DD, NQ)                                                            \
+  attn::decode::attn_decode_kernel<DD, NQ><<<grid, attn::decode::kThreads, 0, s>>>(          \
+      q16, k16, v16, part, lse_part, B, H, Nq, Nk, S, chunk, cz, scale, c)
+    if (d == 64) {
+      if (nq == 1) ATTN_DECODE_LAUNCH(64, 1);
+      else if (nq == 2) ATTN_DECODE_LAUNCH(64, 2);
+      else ATTN_DECODE_LAUNCH(64, 4);
+    } else {
+      if (nq == 1) ATTN_DECODE_LAUNCH(128, 1);
+      else if (nq == 2) ATTN_DECODE_LAUNCH(128, 2);
+      else ATTN_DECODE_LAUNCH(128, 4);
+    }
+#undef ATTN_DECODE_LAUNCH
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+    if (d == 64)
+      attn::attn_combine_kernel<64><<<(int)combine_blocks, 256, 0, s>>>(
+          part, lse_part, reinterpret_cast<__nv_bfloat16*>(o), lse, B, H, Nq, S);
+    else
+      attn::attn_combine_kernel<128><<<(int)combine_blocks, 256, 0, s>>>(
+          part, lse_part, reinterpret_cast<__nv_bfloat16*>(o), lse, B, H, Nq, S);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+    return ATTN_OK;
+  }
+
   int S = num_splits;
   if (S == 0) {
     // The number of ranges with the shortest estimated makespan: units of
@@ -556,7 +607,6 @@ extern "C" int attn_fwd_kvsplit(const void* q, const void* k, const void* v, voi
   p.scale_log2 = exp2_scale(scale);
   p.timeout_ns = 2000000000ull;
 
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int grid = (int)std::min<int64_t>(units, ds->sms);
   if (d == 64)
     attn::attn_fwd_kernel<64, attn::kModeSplit><<<grid, attn::kThreads, FwdCfg<64>::kSmemBytes, s>>>(

@@ -142,3 +142,28 @@ def test_zero_scale_is_uniform_average(dev, causal):
     # every visible key weighs 1 in every KV range; masked keys still weigh 0
     q, k, v = make_cross(909, 2, 2, 40, 1000, 128)
     check(dev, q, k, v, causal, 5, "scale 0", scale=0.0)
+
+
+# A few queries (Nq <= 4) take the CUDA-core decode kernel; more take the
+# tensor-core split kernel.  Ragged key counts, more ranges than keys (empty
+# ranges), a single key, both head dimensions.
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Nq", [1, 2, 3, 4])
+def test_decode_kernel_query_counts(dev, d, causal, Nq):
+    q, k, v = make_cross(920 + Nq + d, 3, 2, Nq, 1999, d)
+    check(dev, q, k, v, causal, 0, f"Nq={Nq} Nk=1999 d={d}")
+    q, k, v = make_cross(930 + Nq + d, 1, 3, Nq, 70, d, qk_std=2.0)
+    check(dev, q, k, v, causal, 200, f"Nq={Nq} Nk=70 200 ranges d={d}")
+
+
+@pytest.mark.parametrize("Nq", [1, 4])
+def test_decode_kernel_single_key(dev, Nq):
+    q, k, v = make_cross(940 + Nq, 2, 2, Nq, Nq, 128)
+    check(dev, q, k, v, True, 0, f"Nq=Nk={Nq} causal")
+    check(dev, q, k, v, False, 3, f"Nq=Nk={Nq}")
+
+
+def test_decode_kernel_zero_scale(dev):
+    q, k, v = make_cross(950, 2, 2, 3, 777, 128)
+    check(dev, q, k, v, True, 0, "Nq=3 scale 0", scale=0.0)
