@@ -354,7 +354,7 @@ def run_cuda(args, world, rank, local):
 DECODE = {"B": 8, "H": 16, "Nq": 1, "Nk": 32768, "d": 128}
 # DRAM bytes (read + write) of one decode call (decode kernel + combine), from
 # the ncu capture summarised under profiles/ (None once either kernel changes).
-DECODE_TRAFFIC_BYTES = None
+DECODE_TRAFFIC_BYTES = 2_147_564_544 + 4_078_336 + 1_271_808  # decode + combine (profiles/attn_fwd_kvsplit_decode.md)
 DECODE_METRIC = "split-KV decode: algorithmic HBM GB/s on 1 GB300 (bf16 K/V cache)"
 
 
@@ -451,7 +451,7 @@ def run_decode(args, world, rank, local):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": decode_config("auto"),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "peak_source": f"{src} hbm_gbs",
-                     "kernel": "attn_decode_kernel<128, 1> + attn_combine_kernel<128> (one call)",
+                     "kernel": "attn_decode_kernel<128> + attn_combine_kernel<128> (one call)",
                      "traffic": DECODE_TRAFFIC_BYTES},
         "clocks": clk.summary(),
         "e2e": {"value": world * bytes_step * n_e2e / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",

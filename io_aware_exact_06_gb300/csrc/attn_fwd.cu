@@ -505,8 +505,8 @@ extern "C" int attn_fwd_kvsplit(const void* q, const void* k, const void* v, voi
   if ((st = get_encode(&enc)) != ATTN_OK) return st;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (Nq <= attn::decode::kMaxQ) {
-    // A few queries: the CUDA-core kernel, one work item per (sequence, head,
+  if (Nq == 1) {
+    // One query row: the CUDA-core kernel, one work item per (sequence, head,
     // key range); by default about 16 items per SM, ranges of at least 64 keys.
     int S = num_splits;
     if (S == 0) {
@@ -520,36 +520,27 @@ extern "C" int attn_fwd_kvsplit(const void* q, const void* k, const void* v, voi
     if (items > INT32_MAX || combine_blocks > INT32_MAX) return ATTN_ERR_SHAPE;
     float* part = nullptr;
     const size_t o_floats = (size_t)S * q_tokens * H * d;
-    const size_t lse_floats = (size_t)S * B * H * Nq;
+    const size_t lse_floats = (size_t)S * B * H;
     if ((st = partial_workspace(dev, stream, o_floats + lse_floats, &part)) != ATTN_OK) return st;
     float* lse_part = part + o_floats;
     const int grid = (int)std::min<int64_t>(items, (int64_t)ds->sms * 8);
     const float c = exp2_scale(scale);
-    const int cz = causal ? 1 : 0;
     auto q16 = reinterpret_cast<const __nv_bfloat16*>(q);
     auto k16 = reinterpret_cast<const __nv_bfloat16*>(k);
     auto v16 = reinterpret_cast<const __nv_bfloat16*>(v);
-    const int nq = Nq <= 1 ? 1 : (Nq <= 2 ? 2 : 4);
-#define ATTN_DECODE_LAUNCH(DD, NQ)                                                            \
-  attn::decode::attn_decode_kernel<DD, NQ><<<grid, attn::decode::kThreads, 0, s>>>(          \
-      q16, k16, v16, part, lse_part, B, H, Nq, Nk, S, chunk, cz, scale, c)
-    if (d == 64) {
-      if (nq == 1) ATTN_DECODE_LAUNCH(64, 1);
-      else if (nq == 2) ATTN_DECODE_LAUNCH(64, 2);
-      else ATTN_DECODE_LAUNCH(64, 4);
-    } else {
-      if (nq == 1) ATTN_DECODE_LAUNCH(128, 1);
-      else if (nq == 2) ATTN_DECODE_LAUNCH(128, 2);
-      else ATTN_DECODE_LAUNCH(128, 4);
-    }
-#undef ATTN_DECODE_LAUNCH
+    if (d == 64)
+      attn::decode::attn_decode_kernel<64><<<grid, attn::decode::kThreads, 0, s>>>(
+          q16, k16, v16, part, lse_part, B, H, Nk, S, chunk, scale, c);
+    else
+      attn::decode::attn_decode_kernel<128><<<grid, attn::decode::kThreads, 0, s>>>(
+          q16, k16, v16, part, lse_part, B, H, Nk, S, chunk, scale, c);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
     if (d == 64)
       attn::attn_combine_kernel<64><<<(int)combine_blocks, 256, 0, s>>>(
-          part, lse_part, reinterpret_cast<__nv_bfloat16*>(o), lse, B, H, Nq, S);
+          part, lse_part, reinterpret_cast<__nv_bfloat16*>(o), lse, B, H, 1, S);
     else
       attn::attn_combine_kernel<128><<<(int)combine_blocks, 256, 0, s>>>(
-          part, lse_part, reinterpret_cast<__nv_bfloat16*>(o), lse, B, H, Nq, S);
+          part, lse_part, reinterpret_cast<__nv_bfloat16*>(o), lse, B, H, 1, S);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
     return ATTN_OK;
   }

@@ -144,9 +144,9 @@ def test_zero_scale_is_uniform_average(dev, causal):
     check(dev, q, k, v, causal, 5, "scale 0", scale=0.0)
 
 
-# A few queries (Nq <= 4) take the CUDA-core decode kernel; more take the
-# tensor-core split kernel.  Ragged key counts, more ranges than keys (empty
-# ranges), a single key, both head dimensions.
+# One query row takes the CUDA-core decode kernel, more take the tensor-core
+# split kernel.  Ragged key counts, more ranges than keys (empty ranges), a
+# single key, both head dimensions.
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("Nq", [1, 2, 3, 4])
