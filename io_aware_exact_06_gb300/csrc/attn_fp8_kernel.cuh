@@ -142,41 +142,33 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
   return lo | (hi << 16);
 }
 
-// Quantises one 128-row block of Q or K (rotation, block max, codes) with one
-// CTA of 16 warps; the last block of a sequence (tokens [tok0, tok0 + L)) is
-// pulled back to end at L and leaves the rows it shares with the block before
-// it to that block; rows before the sequence count as zero.  Each warp holds
-// its 8 rotated rows in registers between the max and the codes.
-__device__ __forceinline__ void fp8_quant_block(const __nv_bfloat16* x, uint8_t* codes,
-                                                float* scale_out, int tok0, int L, int h, int t,
-                                                int H, const Fp8Signs& signs, int rotate,
+// The first quantisation stage runs in persistent CTAs of 16 warps, one
+// 128-row block at a time; a block's rows arrive by TMA in a shared-memory
+// buffer ([128 rows][128 channels] bf16), the next block's rows landing in
+// the other buffer meanwhile.  The last block of a sequence (tokens [tok0,
+// tok0 + L)) is pulled back to end at L, so no copy leaves the sequence, and
+// leaves the rows it shares with the block before it to that block; rows
+// before the sequence count as zero.
+constexpr int kQuantRowBytes = kFp8D * 2;
+constexpr int kQuantBlockBytes = kBM * kQuantRowBytes;
+constexpr int kQuantSmemBytes = 2 * kQuantBlockBytes + 1024;
+constexpr int kQuantRows = kBM / kQuantWarps;  // rows per warp: warp + kQuantWarps i
+
+// First half of a Q or K block: rotation of the warp's 8 rows (held in
+// registers) and their max |x| into warp_max[warp].  Rows r0 + i of the
+// block are at i * 256 bytes of `stage`.
+__device__ __forceinline__ void fp8_rotate_rows(const uint8_t* stage, int r0, const uint32_t (&flip)[2],
+                                                int rotate, float (&v)[kQuantRows][4],
                                                 float* warp_max) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int r0 = min(t * kBM, L - kBM);
-  // the signs of this lane's channels 4 lane .. 4 lane + 3 as bf16 sign bits
-  // of the two 32-bit words that hold them (negation is exact)
-  uint32_t flip[2] = {0u, 0u};
-  if (rotate) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int c = 4 * lane + j;
-      if ((signs.bits[c / 32] >> (c % 32)) & 1u) flip[j / 2] |= (j & 1) ? 0x80000000u : 0x8000u;
-    }
-  }
-  constexpr int kRows = kBM / kQuantWarps;  // rows per warp: warp + kQuantWarps i
-  uint2 raw[kRows];
-#pragma unroll
-  for (int i = 0; i < kRows; ++i) {
-    const int row = r0 + warp + kQuantWarps * i;
-    raw[i] = row >= 0 ? *reinterpret_cast<const uint2*>(x + ((size_t)(tok0 + row) * H + h) * kFp8D +
-                                                         4 * lane)
-                      : make_uint2(0u, 0u);
-  }
-  float v[kRows][4];
   float amax = 0.f;
 #pragma unroll
-  for (int i = 0; i < kRows; ++i) {
-    const uint32_t w0 = raw[i].x ^ flip[0], w1 = raw[i].y ^ flip[1];
+  for (int i = 0; i < kQuantRows; ++i) {
+    const int r = warp + kQuantWarps * i;
+    const uint2 raw = r0 + r >= 0
+                          ? *reinterpret_cast<const uint2*>(stage + r * kQuantRowBytes + 8 * lane)
+                          : make_uint2(0u, 0u);
+    const uint32_t w0 = raw.x ^ flip[0], w1 = raw.y ^ flip[1];
     v[i][0] = __uint_as_float(w0 << 16);
     v[i][1] = __uint_as_float(w0 & 0xffff0000u);
     v[i][2] = __uint_as_float(w1 << 16);
@@ -188,14 +180,21 @@ __device__ __forceinline__ void fp8_quant_block(const __nv_bfloat16* x, uint8_t*
 #pragma unroll
   for (int m = 16; m > 0; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
   if (lane == 0) warp_max[warp] = amax;
-  __syncthreads();
-  amax = warp_max[0];
+}
+
+// Second half: the block max from warp_max, the scale, and the codes of the
+// rows that belong to block t.
+__device__ __forceinline__ void fp8_write_codes(const float (&v)[kQuantRows][4], const float* warp_max,
+                                                uint8_t* codes, float* scale_out, int tok0, int r0,
+                                                int t, int h, int H) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  float amax = warp_max[0];
 #pragma unroll
   for (int w = 1; w < kQuantWarps; ++w) amax = fmaxf(amax, warp_max[w]);
   const float inv = amax > 0.f ? __fdiv_rn(kFp8Max, amax) : 1.0f;
   if (threadIdx.x == 0) *scale_out = amax > 0.f ? __fdiv_rn(amax, kFp8Max) : 1.0f;
 #pragma unroll
-  for (int i = 0; i < kRows; ++i) {
+  for (int i = 0; i < kQuantRows; ++i) {
     const int row = r0 + warp + kQuantWarps * i;
     if (row < t * kBM) continue;  // the previous block's row (or before the sequence)
     *reinterpret_cast<uint32_t*>(codes + ((size_t)(tok0 + row) * H + h) * kFp8D + 4 * lane) =
@@ -204,34 +203,22 @@ __device__ __forceinline__ void fp8_quant_block(const __nv_bfloat16* x, uint8_t*
   }
 }
 
-// max |V| of rows [128 t, 128 t + 128) of one (sequence, head) (tokens
-// [tok0, tok0 + L)), folded into *amax_bits (bit patterns of non-negative
-// floats order like the floats).
-__device__ __forceinline__ void fp8_amax_block(const __nv_bfloat16* v, unsigned int* amax_bits,
-                                               int tok0, int L, int h, int t, int H,
-                                               float* warp_max) {
+// max |V| over the rows of block t (rows >= 128 t of the staged rows r0 ..)
+// into warp_max[warp].
+__device__ __forceinline__ void fp8_rows_amax(const uint8_t* stage, int r0, int t, float* warp_max) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   float m = 0.f;
-#pragma unroll 4
-  for (int r = warp; r < kBM; r += kQuantWarps) {
-    const int row = t * kBM + r;
-    if (row >= L) break;
-    const uint2 w = *reinterpret_cast<const uint2*>(v + ((size_t)(tok0 + row) * H + h) * kFp8D +
-                                                    4 * lane);
-    const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&w.x);
-    const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&w.y);
-    m = fmaxf(m, fmaxf(fmaxf(fabsf(__bfloat162float(p0.x)), fabsf(__bfloat162float(p0.y))),
-                       fmaxf(fabsf(__bfloat162float(p1.x)), fabsf(__bfloat162float(p1.y)))));
+#pragma unroll
+  for (int i = 0; i < kQuantRows; ++i) {
+    const int r = warp + kQuantWarps * i;
+    if (r0 + r < t * kBM) continue;
+    const uint2 w = *reinterpret_cast<const uint2*>(stage + r * kQuantRowBytes + 8 * lane);
+    m = fmaxf(m, fmaxf(fmaxf(fabsf(__uint_as_float(w.x << 16)), fabsf(__uint_as_float(w.x & 0xffff0000u))),
+                       fmaxf(fabsf(__uint_as_float(w.y << 16)), fabsf(__uint_as_float(w.y & 0xffff0000u)))));
   }
 #pragma unroll
   for (int s = 16; s > 0; s >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
   if (lane == 0) warp_max[warp] = m;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-#pragma unroll
-    for (int w = 1; w < kQuantWarps; ++w) m = fmaxf(m, warp_max[w]);
-    atomicMax(amax_bits, __float_as_uint(m));
-  }
 }
 
 // Tokens [tok0, tok0 + L) of sequence b; false when block t lies past its end
@@ -249,28 +236,112 @@ __device__ __forceinline__ bool fp8_seq_block(const int* cu_seqlens, const int* 
   return t * kBM < L;
 }
 
-// One launch for the first quantisation stage: blocks [0, nb) quantise Q
-// (when q is given), [nb, 2 nb) quantise K (when k is given), [2 nb, 3 nb)
-// take the max |V| (when v is given); nb = B * H * T, block = (b * H + h) * T + t.
-__global__ void __launch_bounds__(32 * kQuantWarps)
-fp8_quant_stage1_kernel(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv_bfloat16* v,
-                        uint8_t* q8, uint8_t* k8, float* sq, float* sk, unsigned int* amax_v,
-                        int B, int H, int N, int T, Fp8Signs signs, int rotate, int block0,
-                        const int* cu_seqlens, const int* num_entries) {
-  __shared__ float warp_max[kQuantWarps];
+// One launch for the first quantisation stage over blocks block0 + i, i in
+// [0, n_blocks): blocks [0, nb) quantise Q, [nb, 2 nb) quantise K, [2 nb,
+// 3 nb) take the max |V| per (sequence, head) (atomic max of the
+// non-negative fp32 bit patterns); nb = B * H * T, block = (b * H + h) * T + t.
+// tm_q, tm_k, tm_v: [tokens][H][128] bf16, box 128 channels x 1 head x 128
+// rows, no swizzle (a map of an absent input is never used).
+__global__ void __launch_bounds__(32 * kQuantWarps, 2)
+fp8_quant_stage1_kernel(const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, uint8_t* q8, uint8_t* k8,
+                        float* sq, float* sk, unsigned int* amax_v, int B, int H, int N, int T,
+                        Fp8Signs signs, int rotate, int block0, int n_blocks,
+                        const int* cu_seqlens, const int* num_entries, int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* stage = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  __shared__ uint64_t full[2];
+  __shared__ float warp_max[2][kQuantWarps];
   const int nb = B * H * T;
-  const int gidx = (int)blockIdx.x + block0;  // block0 skips absent leading segments
-  const int seg = gidx / nb, idx = gidx % nb;
-  const int t = idx % T, bh = idx / T;
-  const int b = bh / H, h = bh % H;
-  int tok0, L;
-  if (!fp8_seq_block(cu_seqlens, num_entries, b, t, N, tok0, L)) return;  // uniform in the CTA
-  if (seg == 0)
-    fp8_quant_block(q, q8, sq + idx, tok0, L, h, t, H, signs, rotate, warp_max);
-  else if (seg == 1)
-    fp8_quant_block(k, k8, sk + idx, tok0, L, h, t, H, signs, rotate, warp_max);
-  else
-    fp8_amax_block(v, amax_v + bh, tok0, L, h, t, H, warp_max);
+  const int lane = threadIdx.x % 32;
+  // block i of this launch: segment, index within it, head, sequence tokens, first staged row
+  auto locate = [&](int i, int& seg, int& idx, int& h, int& tok0, int& t, int& r0) {
+    const int gidx = i + block0;
+    seg = gidx / nb;
+    idx = gidx - seg * nb;
+    t = idx % T;
+    const int bh = idx / T;
+    const int b = bh / H;
+    h = bh - b * H;
+    int L;
+    if (!fp8_seq_block(cu_seqlens, num_entries, b, t, N, tok0, L)) return false;
+    r0 = min(t * kBM, L - kBM);
+    return true;
+  };
+  auto issue = [&](int i, int buf) {  // one thread
+    int seg, idx, h, tok0, t, r0;
+    if (i >= n_blocks || !locate(i, seg, idx, h, tok0, t, r0)) return;
+    const CUtensorMap* tm = seg == 0 ? &tm_q : (seg == 1 ? &tm_k : &tm_v);
+    const uint32_t bar = smem_u32(&full[buf]);
+    mbar_arrive_expect_tx(bar, kQuantBlockBytes);
+    tma_load_3d(smem_u32(stage + buf * kQuantBlockBytes), tm, bar, 0, h, tok0 + r0);
+  };
+  // the signs of this lane's channels 4 lane .. 4 lane + 3 as bf16 sign bits
+  // of the two 32-bit words that hold them (negation is exact)
+  uint32_t flip[2] = {0u, 0u};
+  if (rotate) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = 4 * lane + j;
+      if ((signs.bits[c / 32] >> (c % 32)) & 1u) flip[j / 2] |= (j & 1) ? 0x80000000u : 0x8000u;
+    }
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&full[0]), 1);
+    mbar_init(smem_u32(&full[1]), 1);
+    fence_mbar_init();
+    issue(blockIdx.x, 0);
+    issue(blockIdx.x + gridDim.x, 1);
+  }
+  __syncthreads();
+  uint32_t used[2] = {0u, 0u};  // copies consumed per buffer
+  int k = 0;
+  bool failed = false;
+  for (int i = blockIdx.x; i < n_blocks; i += gridDim.x, ++k) {
+    const int buf = k & 1;
+    int seg, idx, h, tok0, t, r0;
+    const bool valid = locate(i, seg, idx, h, tok0, t, r0);  // the same in every thread
+    float v[kQuantRows][4];
+    if (valid) {
+      const bool ok = mbar_wait(smem_u32(&full[buf]), used[buf] & 1, 2000000000ull);
+      ++used[buf];
+      if (__syncthreads_or(!ok)) {
+        failed = true;
+        break;
+      }
+      const uint8_t* st = stage + buf * kQuantBlockBytes;
+      if (seg < 2)
+        fp8_rotate_rows(st, r0, flip, rotate, v, warp_max[k & 1]);
+      else
+        fp8_rows_amax(st, r0, t, warp_max[k & 1]);
+    }
+    __syncthreads();  // every read of this buffer is done; warp_max is complete
+    if (threadIdx.x == 0) {
+      // (the generic-proxy reads above before the copy that overwrites them)
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(i + 2 * gridDim.x, buf);
+    }
+    if (!valid) continue;
+    if (seg == 0) {
+      fp8_write_codes(v, warp_max[k & 1], q8, sq + idx, tok0, r0, t, h, H);
+    } else if (seg == 1) {
+      fp8_write_codes(v, warp_max[k & 1], k8, sk + idx, tok0, r0, t, h, H);
+    } else if (threadIdx.x == 0) {
+      float m = warp_max[k & 1][0];
+#pragma unroll
+      for (int w = 1; w < kQuantWarps; ++w) m = fmaxf(m, warp_max[k & 1][w]);
+      atomicMax(amax_v + idx / T, __float_as_uint(m));
+    }
+  }
+  if (failed) {
+    if (threadIdx.x == 0) atomicOr(err, kErrTimeout);
+    // a copy issued for a later block may still be landing
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 1000000ull) {
+    }
+  }
 }
 
 // V codes, transposed: vt[(b*H + h) * 128 + c][key] for keys padded to Np

@@ -9,6 +9,7 @@
 #include <cfloat>
 #include <cmath>
 #include <cstdint>
+#include <cstring>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -101,6 +102,10 @@ cudaError_t set_smem_attributes() {
     return e;
   if ((e = cudaFuncSetAttribute(attn::attn_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 attn::kFp8SmemBytes)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(attn::fp8_quant_stage1_kernel,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                attn::kQuantSmemBytes)) != cudaSuccess)
     return e;
   return cudaFuncSetAttribute(attn::attn_fwd_kernel<128, attn::kModeWindow>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -742,25 +747,51 @@ int fp8_worklist(int dev, attn_stream_t stream, DeviceState* ds, const int32_t* 
   return ATTN_OK;
 }
 
+// bf16 rows [tokens, H, 128] for the first quantisation stage: box 128
+// channels x 1 head x 128 rows, no swizzle (rows 256 bytes apart in shared
+// memory).
+int make_map_quant_rows(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int64_t tokens, int H) {
+  cuuint64_t dims[3] = {(cuuint64_t)attn::kFp8D, (cuuint64_t)H, (cuuint64_t)tokens};
+  cuuint64_t strides[2] = {(cuuint64_t)attn::kFp8D * 2, (cuuint64_t)H * attn::kFp8D * 2};
+  cuuint32_t box[3] = {(cuuint32_t)attn::kFp8D, 1, (cuuint32_t)attn::kBM};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : cuda_fail(cudaErrorInvalidValue);
+}
+
 // First stage: Q and / or K codes and block scales, and / or max |V| per
 // (sequence, head) (amax_v zeroed here first).  Null inputs are skipped.
-// Packed (cu_seqlens): num_entries is the worklist's entry count.
+// Packed (cu_seqlens): num_entries is the worklist's entry count.  The token
+// extent of the copies is B * N (packed: an upper bound of cu_seqlens[B]; no
+// copy leaves its sequence).
 int launch_quant_stage1(const void* q, const void* k, const void* v, uint8_t* q8, uint8_t* k8,
                         float* sq, float* sk, unsigned int* amax_v, int B, int H, int N,
                         const int8_t* signs, const int32_t* cu_seqlens, const int* num_entries,
-                        cudaStream_t s) {
+                        DeviceState* ds, cudaStream_t s) {
   const int T = (N + attn::kBM - 1) / attn::kBM;
   const int nb = B * H * T;
+  const int64_t tokens = (int64_t)B * N;
+  EncodeTiledFn enc = nullptr;
+  int st = get_encode(&enc);
+  if (st != ATTN_OK) return st;
+  CUtensorMap maps[3];
+  std::memset(maps, 0, sizeof(maps));
+  const void* src[3] = {q, k, v};
+  for (int i = 0; i < 3; ++i)
+    if (src[i] && (st = make_map_quant_rows(enc, &maps[i], src[i], tokens, H)) != ATTN_OK) return st;
   cudaError_t e;
   if (v && (e = cudaMemsetAsync(amax_v, 0, (size_t)B * H * sizeof(unsigned int), s)) != cudaSuccess)
     return cuda_fail(e);
-  // segments: Q, K, V (the grid covers the last segment that is present)
+  // segments: Q, K, V (the blocks run from the first present one to the last)
   const int nseg = v ? 3 : (k ? 2 : 1);
   const int first = q ? 0 : (k ? 1 : 2);
-  attn::fp8_quant_stage1_kernel<<<(nseg - first) * nb, 32 * attn::kQuantWarps, 0, s>>>(
-      reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k),
-      reinterpret_cast<const __nv_bfloat16*>(v), q8, k8, sq, sk, amax_v, B, H, N, T,
-      pack_signs(signs), signs ? 1 : 0, first * nb, cu_seqlens, num_entries);
+  const int n_blocks = (nseg - first) * nb;
+  const int grid = std::min(n_blocks, 2 * ds->sms);
+  attn::fp8_quant_stage1_kernel<<<grid, 32 * attn::kQuantWarps, attn::kQuantSmemBytes, s>>>(
+      maps[0], maps[1], maps[2], q8, k8, sq, sk, amax_v, B, H, N, T, pack_signs(signs),
+      signs ? 1 : 0, first * nb, n_blocks, cu_seqlens, num_entries, ds->err);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
   return ATTN_OK;
 }
@@ -795,7 +826,7 @@ extern "C" int attn_fp8_quantize_qk(const void* x, uint8_t* codes, float* scales
   int* ws = nullptr;
   if ((st = fp8_worklist(dev, stream, ds, cu_seqlens, B, N, 0, &ws)) != ATTN_OK) return st;
   return launch_quant_stage1(x, nullptr, nullptr, codes, nullptr, scales, nullptr, nullptr, B, H, N,
-                             signs, cu_seqlens, ws, reinterpret_cast<cudaStream_t>(stream));
+                             signs, cu_seqlens, ws, ds, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int attn_fp8_quantize_v(const void* v, uint8_t* codes_t, float* scale, int B, int H,
@@ -819,7 +850,7 @@ extern "C" int attn_fp8_quantize_v(const void* v, uint8_t* codes_t, float* scale
   if ((st = fp8_worklist(dev, stream, ds, cu_seqlens, B, N, 0, &list)) != ATTN_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if ((st = launch_quant_stage1(nullptr, nullptr, v, nullptr, nullptr, nullptr, nullptr, amax, B, H,
-                                N, nullptr, cu_seqlens, list, s)) != ATTN_OK)
+                                N, nullptr, cu_seqlens, list, ds, s)) != ATTN_OK)
     return st;
   return launch_quant_v(v, codes_t, scale, amax, B, H, N, cu_seqlens, list, s);
 }
@@ -869,7 +900,7 @@ extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o
   if ((st = fp8_worklist(dev, stream, ds, cu_seqlens, B, N, causal ? 1 : 0, &list)) != ATTN_OK)
     return st;
   if ((st = launch_quant_stage1(q, k, v, q8, k8, sq, sk, amax, B, H, N, signs, cu_seqlens, list,
-                                s)) != ATTN_OK)
+                                ds, s)) != ATTN_OK)
     return st;
   if ((st = launch_quant_v(v, vt, sv, amax, B, H, N, cu_seqlens, list, s)) != ATTN_OK) return st;
 
