@@ -365,23 +365,22 @@ fp8_quant_v_kernel(const __nv_bfloat16* v, const unsigned int* amax_bits, float*
   const float amax = __uint_as_float(amax_bits[bh]);
   const float inv = amax > 0.f ? __fdiv_rn(kFp8Max, amax) : 1.0f;
   if (t == 0 && threadIdx.x == 0) sv[bh] = amax > 0.f ? __fdiv_rn(amax, kFp8Max) : 1.0f;
-#pragma unroll 4
-  for (int r = warp; r < kBN; r += 8) {
-    const int key = t * kBN + r;
-    float f[4] = {0.f, 0.f, 0.f, 0.f};
-    if (key < L) {
-      const uint2 w = *reinterpret_cast<const uint2*>(v + ((size_t)(tok0 + key) * H + h) * kFp8D +
-                                                      4 * lane);
-      const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&w.x);
-      const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&w.y);
-      f[0] = __bfloat162float(p0.x);
-      f[1] = __bfloat162float(p0.y);
-      f[2] = __bfloat162float(p1.x);
-      f[3] = __bfloat162float(p1.y);
-    }
-    *reinterpret_cast<uint32_t*>(&tile[r][4 * lane]) =
-        e4m3x4(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv), __fmul_rn(f[2], inv),
-               __fmul_rn(f[3], inv));
+  // warp w: keys w, w + 8, ... of the tile, all 16 rows' loads in flight together
+  constexpr int kRowsV = kBN / 8;
+  uint2 raw[kRowsV];
+#pragma unroll
+  for (int i = 0; i < kRowsV; ++i) {
+    const int key = t * kBN + warp + 8 * i;
+    raw[i] = key < L ? *reinterpret_cast<const uint2*>(v + ((size_t)(tok0 + key) * H + h) * kFp8D +
+                                                       4 * lane)
+                     : make_uint2(0u, 0u);
+  }
+#pragma unroll
+  for (int i = 0; i < kRowsV; ++i) {
+    const float f0 = __uint_as_float(raw[i].x << 16), f1 = __uint_as_float(raw[i].x & 0xffff0000u);
+    const float f2 = __uint_as_float(raw[i].y << 16), f3 = __uint_as_float(raw[i].y & 0xffff0000u);
+    *reinterpret_cast<uint32_t*>(&tile[warp + 8 * i][4 * lane]) =
+        e4m3x4(__fmul_rn(f0, inv), __fmul_rn(f1, inv), __fmul_rn(f2, inv), __fmul_rn(f3, inv));
   }
   __syncthreads();
   // output chunk i: channel c = i % 128, keys 16 q .. 16 q + 15 with q = i / 128
