@@ -99,8 +99,12 @@ int attn_fwd_window(const void *q, const void *k, const void *v, void *o, float 
  * causal: query row r sits at key position Nk - Nq + r (the queries are the
  *   last Nq positions of the key sequence) and sees keys j <= Nk - Nq + r;
  *   requires Nq <= Nk.  Non-causal: every key is visible.
- * num_splits: 1..256 ranges, or 0 to choose (the count with the shortest
- *   estimated makespan over the SMs, at most 64).
+ * Nq == 1 (decoding one token) runs on CUDA cores: a matrix-vector product
+ *   per (sequence, head), bound by reading K and V; Nq > 1 runs on the tensor
+ *   cores in 256-row query blocks.
+ * num_splits: 1..256 ranges, or 0 to choose (Nq == 1: about 16 (sequence,
+ *   head, range) items per SM, ranges of at least 64 keys; else the count
+ *   with the shortest estimated makespan over the SMs, at most 64).
  * Ownership: like attn_fwd; in addition the library keeps a per-(device,
  *   stream) fp32 workspace for the partial results, grown on demand.
  * Errors: like attn_fwd; Nk == 0, num_splits outside [0, 256] or causal with
@@ -109,6 +113,29 @@ int attn_fwd_window(const void *q, const void *k, const void *v, void *o, float 
 int attn_fwd_kvsplit(const void *q, const void *k, const void *v, void *o, float *lse,
                      int B, int H, int Nq, int Nk, int d, float scale, int causal,
                      int num_splits, attn_stream_t stream);
+
+/*
+ * attn_fwd_decode: one query per sequence (the newest token) against the
+ * sequence's packed keys, which differ in length from sequence to sequence
+ * (a key/value cache): O_b = softmax(scale q_b K_b^T) V_b over every key of
+ * sequence b, computed as attn_fwd_kvsplit computes Nq == 1 (key ranges on
+ * CUDA cores, merged by the two-segment merge identity).
+ * Layout: q, o [B, H, d] bf16; k, v [total, H, d] bf16 with total =
+ *   cu_seqlens_k[B], sequence b's keys at tokens cu_seqlens_k[b] ..
+ *   cu_seqlens_k[b+1]-1; lse [B, H] fp32.  cu_seqlens_k: device int32[B+1].
+ * max_seqlen_k >= every key length (sizes the ranges; checked on the device).
+ * A sequence with no key gets O = 0 and LSE = -inf.
+ * num_splits: ranges per sequence, 1..256, or 0 to choose (about 16
+ *   (sequence, head, range) items per SM, ranges of at least 64 keys of the
+ *   longest sequence).
+ * Ownership: like attn_fwd_kvsplit.
+ * Errors: like attn_fwd; cu_seqlens_k not starting at 0, decreasing, or with
+ *   a length above max_seqlen_k: ATTN_ERR_SEQLENS in the error word and
+ *   nothing is read past the check or written.
+ */
+int attn_fwd_decode(const void *q, const void *k, const void *v, void *o, float *lse,
+                    int B, int H, int d, float scale, const int32_t *cu_seqlens_k,
+                    int max_seqlen_k, int num_splits, attn_stream_t stream);
 
 /* Options of attn_fwd_ex.  Zero-initialise and set what is needed. */
 typedef struct {

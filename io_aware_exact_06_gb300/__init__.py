@@ -15,12 +15,12 @@ import os
 from . import build as _build
 
 __all__ = ["attn_fwd", "attn_bwd", "attn_bwd_window", "attn_fwd_fp8", "attn_fp8_quantize_qk", "attn_fp8_quantize_v",
-           "attn_fwd_ex", "attn_fwd_noalloc", "attn_fwd_window", "attn_fwd_kvsplit", "attn_last_device_error", "attn_last_error_site",
+           "attn_fwd_ex", "attn_fwd_noalloc", "attn_fwd_window", "attn_fwd_kvsplit", "attn_fwd_decode", "attn_last_device_error", "attn_last_error_site",
            "attn_status_string", "AttnError", "AttnFwdOptions", "lib", "forward",
            "EXPORTED_SYMBOLS"]
 
 # Every symbol the headers under include/ declare.
-EXPORTED_SYMBOLS = ("attn_fwd", "attn_fwd_ex", "attn_last_device_error", "attn_last_error_site",
+EXPORTED_SYMBOLS = ("attn_fwd", "attn_fwd_ex", "attn_fwd_decode", "attn_last_device_error", "attn_last_error_site",
                     "attn_last_cuda_error", "attn_status_string", "attn_fwd_noalloc",
                     "attn_fwd_window", "attn_fwd_kvsplit", "attn_bwd", "attn_bwd_window",
                     "attn_fwd_fp8",
@@ -64,6 +64,8 @@ def lib() -> ctypes.CDLL:
         L.attn_fwd_window.restype = i
         L.attn_fwd_kvsplit.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_float, i, i, vp]
         L.attn_fwd_kvsplit.restype = i
+        L.attn_fwd_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, ctypes.c_float, vp, i, i, vp]
+        L.attn_fwd_decode.restype = i
         L.attn_bwd.argtypes = [vp] * 9 + [i, i, i, i, ctypes.c_float, i, vp, vp]
         L.attn_bwd.restype = i
         L.attn_bwd_window.argtypes = [vp] * 9 + [i, i, i, i, ctypes.c_float, i, i, i, vp, vp]
@@ -151,6 +153,17 @@ def attn_fwd_kvsplit(q, k, v, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, 
                                 int(num_splits), _stream(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_kvsplit")
+    return st
+
+
+def attn_fwd_decode(q, k, v, o, lse, B: int, H: int, d: int, scale: float, cu_seqlens_k,
+                    max_seqlen_k: int, num_splits: int = 0, stream=None) -> int:
+    """The C call ``attn_fwd_decode``: one query per sequence against its packed keys."""
+    st = lib().attn_fwd_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(d),
+                               float(scale), _ptr(cu_seqlens_k), int(max_seqlen_k), int(num_splits),
+                               _stream(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_decode")
     return st
 
 

@@ -31,6 +31,8 @@
 #include <cuda_bf16.h>
 #include <cstdint>
 
+#include "attn_fwd_kernel.cuh"
+
 namespace attn {
 namespace decode {
 
@@ -75,17 +77,22 @@ __device__ __forceinline__ void merge(float& m, float& l, float (&o)[8], float m
   m = mm;
 }
 
-// q: [B, 1, H, D], k, v: [B, Nk, H, D] bf16.  o_part [S][B][H][D] fp32,
-// lse_part [S][B][H].  Items (b, h, s), b-major; persistent CTAs stride over
-// them.  c = scale * log2(e) (at least the smallest normal float).  Causal
-// attention of the one query (at key position Nk - 1) sees every key, so
-// there is no mask.
+// q: [B, 1, H, D] bf16.  Dense keys (cu_k null): k, v [B, Nk, H, D], key
+// range s of every sequence = keys [s*chunk, min(Nk, (s+1)*chunk)).  Packed
+// keys: k, v [cu_k[B], H, D], sequence b's keys at tokens cu_k[b] ..
+// cu_k[b+1]-1, cut into S ranges of ceil(L_b / S) keys; *valid (written by
+// decode_check_kernel) is 0 when cu_k is invalid, and then nothing is read or
+// written.  o_part [S][B][H][D] fp32, lse_part [S][B][H].  Items (b, h, s),
+// b-major; persistent CTAs stride over them.  c = scale * log2(e) (at least
+// the smallest normal float).  The one query is the newest position of its
+// sequence, so causal attention sees every key: there is no mask.
 template <int D>
 __global__ void __launch_bounds__(kThreads)
 attn_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                    const __nv_bfloat16* __restrict__ v, float* __restrict__ o_part,
                    float* __restrict__ lse_part, int B, int H, int Nk, int S, int chunk,
-                   float scale, float c) {
+                   float scale, float c, const int* __restrict__ cu_k,
+                   const int* __restrict__ valid) {
   constexpr int kLpk = D / 8;        // lanes per key row
   constexpr int kKps = 32 / kLpk;    // keys per warp step
   constexpr int kStride = kWarps * kKps;
@@ -98,20 +105,27 @@ attn_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
   const int slice = lane % kLpk;     // elements 8*slice .. 8*slice+7 of the row
   const size_t row_stride = (size_t)H * D;
   const int n_items = B * H * S;
+  if (cu_k && *valid == 0) return;
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
     const int s = item % S;
     const int bh = item / S;
     const int b = bh / H, h = bh % H;
-    const int k_lo = s * chunk;
-    const int k_hi = min(Nk, k_lo + chunk);
+    int kbase = b * Nk, Lk = Nk, ch = chunk;  // first key token, keys, keys per range
+    if (cu_k) {
+      kbase = cu_k[b];
+      Lk = cu_k[b + 1] - kbase;
+      ch = (Lk + S - 1) / S;
+    }
+    const int k_lo = s * ch;
+    const int k_hi = min(Lk, k_lo + ch);
     float qf[8];
     widen(*reinterpret_cast<const uint4*>(q + (size_t)b * row_stride + (size_t)h * D + 8 * slice),
           qf);
     float m = -INFINITY, l = 0.f, acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-    const __nv_bfloat16* kb = k + (size_t)b * Nk * row_stride + (size_t)h * D + 8 * slice;
-    const __nv_bfloat16* vb = v + (size_t)b * Nk * row_stride + (size_t)h * D + 8 * slice;
+    const __nv_bfloat16* kb = k + (size_t)kbase * row_stride + (size_t)h * D + 8 * slice;
+    const __nv_bfloat16* vb = v + (size_t)kbase * row_stride + (size_t)h * D + 8 * slice;
     // keys past the range read the range's last key (in bounds) and are skipped
     auto load_group = [&](int base, uint4 (&kw)[kUnroll], uint4 (&vw)[kUnroll]) {
 #pragma unroll
@@ -202,6 +216,25 @@ attn_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
         lse_part[orow] = lsum > 0.f ? mm * scale + __log2f(lsum) * 0.69314718055994531f : -INFINITY;
     }
     __syncthreads();  // shared memory is reused by the next item
+  }
+}
+
+// Packed keys: cu_k must start at 0 and hold B lengths in [0, max_len]; then
+// every key a decode item reads lies in [0, cu_k[B]).  *valid = 1 if so, else
+// 0 with kErrSeqlens in the error word.  One CTA.
+__global__ void __launch_bounds__(256)
+decode_check_kernel(const int* cu_k, int B, int max_len, int* valid, int* err) {
+  __shared__ int bad;
+  if (threadIdx.x == 0) bad = cu_k[0] != 0;
+  __syncthreads();
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    const int L = cu_k[b + 1] - cu_k[b];
+    if (L < 0 || L > max_len) bad = 1;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    *valid = bad ? 0 : 1;
+    if (bad) atomicOr(err, kErrSeqlens);
   }
 }
 

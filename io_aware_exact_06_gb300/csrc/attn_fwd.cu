@@ -535,10 +535,10 @@ extern "C" int attn_fwd_kvsplit(const void* q, const void* k, const void* v, voi
     auto v16 = reinterpret_cast<const __nv_bfloat16*>(v);
     if (d == 64)
       attn::decode::attn_decode_kernel<64><<<grid, attn::decode::kThreads, 0, s>>>(
-          q16, k16, v16, part, lse_part, B, H, Nk, S, chunk, scale, c);
+          q16, k16, v16, part, lse_part, B, H, Nk, S, chunk, scale, c, nullptr, nullptr);
     else
       attn::decode::attn_decode_kernel<128><<<grid, attn::decode::kThreads, 0, s>>>(
-          q16, k16, v16, part, lse_part, B, H, Nk, S, chunk, scale, c);
+          q16, k16, v16, part, lse_part, B, H, Nk, S, chunk, scale, c, nullptr, nullptr);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
     if (d == 64)
       attn::attn_combine_kernel<64><<<(int)combine_blocks, 256, 0, s>>>(
@@ -620,6 +620,76 @@ extern "C" int attn_fwd_kvsplit(const void* q, const void* k, const void* v, voi
     attn::attn_combine_kernel<128><<<blocks, 256, 0, s>>>(p.o_part, p.lse_part,
                                                           reinterpret_cast<__nv_bfloat16*>(o), lse, B, H,
                                                           Nq, S);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+  return ATTN_OK;
+}
+
+// ---------------------------------------------------------------------------
+// attn_fwd_decode: one query per sequence against packed key sequences of
+// different lengths (the CUDA-core decode kernel and the combine).
+extern "C" int attn_fwd_decode(const void* q, const void* k, const void* v, void* o, float* lse,
+                               int B, int H, int d, float scale, const int32_t* cu_seqlens_k,
+                               int max_seqlen_k, int num_splits, attn_stream_t stream) {
+  if (B < 0 || H < 0 || max_seqlen_k < 0 || num_splits < 0 || num_splits > 256)
+    return ATTN_ERR_SHAPE;
+  if (d != 64 && d != 128) return ATTN_ERR_HEADDIM;
+  if (!std::isfinite(scale) || scale < 0.0f) return ATTN_ERR_SCALE;
+  if (B == 0 || H == 0) return ATTN_OK;
+  if (!q || !k || !v || !o || !lse || !cu_seqlens_k) return ATTN_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+      !aligned(cu_seqlens_k, 4))
+    return ATTN_ERR_ALIGN;
+  // key token indices (at most B * max_seqlen_k) stay within int32
+  if ((int64_t)B * max_seqlen_k > INT32_MAX - 256 || (int64_t)H * d > (1 << 20) || H > 65535)
+    return ATTN_ERR_SHAPE;
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  DeviceState* ds = nullptr;
+  int st = device_state(dev, &ds);
+  if (st != ATTN_OK) return st;
+  // key ranges: by default about 16 (sequence, head, range) items per SM,
+  // ranges of at least 64 keys of the longest sequence
+  int S = num_splits;
+  if (S == 0) {
+    const int64_t bh = (int64_t)B * H;
+    const int64_t want = ((int64_t)ds->sms * 16 + bh - 1) / bh;
+    S = (int)std::max<int64_t>(1, std::min<int64_t>({want, ((int64_t)max_seqlen_k + 63) / 64, 256}));
+  }
+  const int64_t items = (int64_t)B * H * S;
+  const int64_t combine_blocks = ((int64_t)B * H * 32 + 255) / 256;
+  if (items > INT32_MAX || combine_blocks > INT32_MAX) return ATTN_ERR_SHAPE;
+  int* ws = nullptr;  // [3]: the validity flag of cu_seqlens_k
+  if ((st = stream_workspace(dev, stream, 0, &ws)) != ATTN_OK) return st;
+  float* part = nullptr;
+  const size_t o_floats = (size_t)S * B * H * d;
+  if ((st = partial_workspace(dev, stream, o_floats + (size_t)S * B * H, &part)) != ATTN_OK)
+    return st;
+  float* lse_part = part + o_floats;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  attn::decode::decode_check_kernel<<<1, 256, 0, s>>>(cu_seqlens_k, B, max_seqlen_k, ws + 3,
+                                                       ds->err);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+  const int grid = (int)std::min<int64_t>(items, (int64_t)ds->sms * 8);
+  const float c = exp2_scale(scale);
+  auto q16 = reinterpret_cast<const __nv_bfloat16*>(q);
+  auto k16 = reinterpret_cast<const __nv_bfloat16*>(k);
+  auto v16 = reinterpret_cast<const __nv_bfloat16*>(v);
+  if (d == 64)
+    attn::decode::attn_decode_kernel<64><<<grid, attn::decode::kThreads, 0, s>>>(
+        q16, k16, v16, part, lse_part, B, H, 0, S, 0, scale, c, cu_seqlens_k, ws + 3);
+  else
+    attn::decode::attn_decode_kernel<128><<<grid, attn::decode::kThreads, 0, s>>>(
+        q16, k16, v16, part, lse_part, B, H, 0, S, 0, scale, c, cu_seqlens_k, ws + 3);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+  if (d == 64)
+    attn::attn_combine_kernel<64><<<(int)combine_blocks, 256, 0, s>>>(
+        part, lse_part, reinterpret_cast<__nv_bfloat16*>(o), lse, B, H, 1, S, ws + 3);
+  else
+    attn::attn_combine_kernel<128><<<(int)combine_blocks, 256, 0, s>>>(
+        part, lse_part, reinterpret_cast<__nv_bfloat16*>(o), lse, B, H, 1, S, ws + 3);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
   return ATTN_OK;
 }

@@ -952,15 +952,17 @@ build_worklist_kernel(const int* cu_seqlens, int nseq, int max_len, int causal, 
 //   m = max_s LSE_s,  w_s = e^{LSE_s - m},  LSE = m + ln sum_s w_s,
 //   O = sum_s w_s O_s / sum_s w_s.
 // One warp per (token, head) row; lane c holds columns c, c+32, ...
+// valid: null, or a flag that is 0 when the inputs were rejected on the
+// device (nothing is written then).
 template <int D>
 __global__ void __launch_bounds__(256)
 attn_combine_kernel(const float* o_part, const float* lse_part, __nv_bfloat16* o, float* lse,
-                    int B, int H, int Nq, int S) {
+                    int B, int H, int Nq, int S, const int* valid = nullptr) {
   constexpr int kPer = D / 32;
   const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / 32;
   const int lane = threadIdx.x % 32;
   const long long rows = (long long)B * Nq * H;
-  if (warp >= rows) return;
+  if (warp >= rows || (valid && *valid == 0)) return;
   const long long tok = warp / H;
   const int h = (int)(warp - tok * H);
   const int b = (int)(tok / Nq);

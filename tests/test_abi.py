@@ -135,3 +135,30 @@ def test_fp8_argument_errors(lib, args, status):
 def test_backward_window_below_minus_one(lib):
     assert lib.attn_bwd_window(*([BUF] * 9), 1, 1, 128, 64, 0.1, 1, -2, 0, None, None) == -2
     assert lib.attn_bwd_window(*([BUF] * 9), 1, 1, 128, 64, 0.1, 1, 0, -3, None, None) == -2
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(d=96), -3),
+    (dict(B=-1), -2),
+    (dict(max_len=-1), -2),
+    (dict(splits=257), -2),
+    (dict(splits=-1), -2),
+    (dict(scale=-1.0), -5),
+    (dict(scale=float("inf")), -5),
+    (dict(cu=None), -1),
+    (dict(k=None), -1),
+    (dict(v=BUF + 8), -4),
+    (dict(cu=BUF + 2), -4),
+    (dict(B=1 << 20, max_len=1 << 12), -2),
+])
+def test_decode_argument_errors(lib, args, status):
+    a = dict(q=BUF, k=BUF, v=BUF, o=BUF, lse=BUF, B=2, H=4, d=128, scale=0.1, cu=BUF,
+             max_len=512, splits=0)
+    a.update(args)
+    st = lib.attn_fwd_decode(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["d"],
+                             a["scale"], a["cu"], a["max_len"], a["splits"], None)
+    assert st == status
+
+
+def test_decode_empty_batch_is_a_noop(lib):
+    assert lib.attn_fwd_decode(None, None, None, None, None, 0, 4, 128, 0.1, None, 0, 0, None) == 0
