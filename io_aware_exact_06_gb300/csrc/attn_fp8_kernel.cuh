@@ -19,11 +19,13 @@
 // 0.75 (log2 units), so 256 P <= 431 stays below 448.
 //
 // Kernels:
-//   fp8_quant_stage1_kernel  rotation + block quantisation of Q and of K, one
-//                         CTA per (sequence, head, 128-row block) holding its
-//                         rotated rows in registers; and in the same launch the
-//                         max |V| per (sequence, head) (atomic max of the
-//                         non-negative fp32 bit patterns)
+//   fp8_quant_stage1_kernel  rotation + block quantisation of Q and of K, and
+//                         in the same launch the max |V| per (sequence, head)
+//                         (atomic max of the non-negative fp32 bit patterns):
+//                         persistent CTAs take one (sequence, head, 128-row
+//                         block) at a time, its rows arriving by TMA in a
+//                         shared-memory double buffer while the block before
+//                         is quantised from registers
 //   fp8_quant_v_kernel    V codes, stored transposed per (sequence, head):
 //                         [d][keys padded to 128] (keys contiguous), so both
 //                         products of the attention kernel take K-major

@@ -43,7 +43,7 @@ struct DeviceState {
 
 struct StreamWorkspace {
   int* buf = nullptr;       // [0] entry count, [1] next-unit counter, [2] finished CTAs,
-                            // [3] unused, [4..] (seq, q-block) pairs
+                            // [3] attn_fwd_decode's cu_seqlens_k check, [4..] (seq, q-block) pairs
   int64_t capacity = 0;     // entries
 };
 
