@@ -16,7 +16,7 @@ from . import build as _build
 
 __all__ = ["attn_fwd", "attn_bwd", "attn_bwd_window", "attn_fwd_fp8", "attn_fp8_quantize_qk", "attn_fp8_quantize_v",
            "attn_fwd_ex", "attn_fwd_noalloc", "attn_fwd_window", "attn_fwd_kvsplit", "attn_fwd_decode", "attn_last_device_error", "attn_last_error_site",
-           "attn_status_string", "AttnError", "AttnFwdOptions", "lib", "forward",
+           "attn_status_string", "AttnError", "AttnFwdOptions", "lib", "forward", "backward", "decode",
            "EXPORTED_SYMBOLS"]
 
 # Every symbol the headers under include/ declare.
@@ -292,3 +292,58 @@ def forward(q, k, v, causal: bool, scale: float | None = None, cu_seqlens=None,
         stream = torch.cuda.current_stream(q.device)
     attn_fwd(q, k, v, out, lse, B, H, N, d, scale, causal, cu_seqlens, stream)
     return out, lse
+
+
+def _check_bf16(*ts):
+    import torch
+    for t in ts:
+        if t.dtype != torch.bfloat16:
+            raise TypeError("tensors must be bf16")
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def backward(q, k, v, o, dout, lse, causal: bool, scale: float | None = None, cu_seqlens=None,
+             max_seqlen: int | None = None, window=(-1, -1), stream=None):
+    """Convenience call of attn_bwd / attn_bwd_window on torch CUDA tensors.
+
+    q, k, v, o, dout in the forward's layout (dense [B, N, H, d] or packed
+    [total, H, d] with cu_seqlens and max_seqlen), lse as the forward returns
+    it.  Returns (dq, dk, dv), allocated by torch.
+    """
+    import torch
+    _check_bf16(q, k, v, o, dout)
+    d = q.shape[-1]
+    if cu_seqlens is None:
+        B, N, H, _ = q.shape
+    else:
+        H = q.shape[1]
+        B = cu_seqlens.numel() - 1
+        N = int(max_seqlen)
+    if scale is None:
+        scale = d ** -0.5
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    wl, wr = window
+    attn_bwd_window(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, wl, wr,
+                    cu_seqlens, stream)
+    return dq, dk, dv
+
+
+def decode(q, k, v, cu_seqlens_k, max_seqlen_k: int, scale: float | None = None,
+           num_splits: int = 0, stream=None):
+    """Convenience call of attn_fwd_decode on torch CUDA tensors: q [B, H, d]
+    (one query per sequence), k, v [total, H, d] packed with cu_seqlens_k
+    (int32 [B+1], on the device).  Returns (o [B, H, d] bf16, lse [B, H] fp32)."""
+    import torch
+    _check_bf16(q, k, v)
+    B, H, d = q.shape
+    if scale is None:
+        scale = d ** -0.5
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    attn_fwd_decode(q, k, v, o, lse, B, H, d, scale, cu_seqlens_k, max_seqlen_k, num_splits, stream)
+    return o, lse

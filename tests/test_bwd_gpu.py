@@ -257,3 +257,20 @@ def test_deterministic(dev):
     b = run_bwd(dev, wl, dout)
     for x, y in zip(a, b):
         assert np.array_equal(x, y)
+
+
+def test_convenience_wrappers(dev):
+    """fa.forward then fa.backward give what the C calls give."""
+    import torch
+    import io_aware_exact_06_gb300 as fa
+    wl, dout = make(2601, 2, 640, 2, 128, True)
+    ref = run_bwd(dev, wl, dout)
+    tt = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+    q = tt(wl.q).view(2, 640, 2, 128)
+    k = tt(wl.k).view(2, 640, 2, 128)
+    v = tt(wl.v).view(2, 640, 2, 128)
+    o, lse = fa.forward(q, k, v, True, wl.scale)
+    dq, dk, dv = fa.backward(q, k, v, o, tt(dout).view(2, 640, 2, 128), lse, True, wl.scale)
+    assert fa.attn_last_device_error() == 0
+    for a, b in zip(ref, (dq, dk, dv)):
+        assert np.array_equal(a, b.float().cpu().numpy().astype(np.float64).reshape(a.shape))

@@ -129,3 +129,15 @@ def test_invalid_cu_seqlens_reported(dev, bad):
     o, lse, st = run(dev, cu_bad, q, k, v, 0.1, 0, max_len=128)
     assert st == -8
     assert (o.float() == 7.0).all() and (lse == 7.0).all(), "nothing is written"
+
+
+def test_convenience_wrapper(dev):
+    import torch
+    import io_aware_exact_06_gb300 as fa
+    cu, q, k, v = make(974, [900, 17, 2500], 2, 128)
+    o1, l1, st = run(dev, cu, q, k, v, 128 ** -0.5, 0)
+    assert st == 0
+    cu_d = torch.tensor(cu, dtype=torch.int32, device=dev)
+    o2, l2 = fa.decode(t(dev, q), t(dev, k), t(dev, v), cu_d, 2500)
+    assert fa.attn_last_device_error() == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
