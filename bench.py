@@ -715,7 +715,7 @@ def run_fp8(args, world, rank, local):
         "e2e": {"value": world * flops_step * n_e2e / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": 3 * q.numel() * 2,
                 "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4},
-        "gpu_launches": 5 * args.steps,
+        "gpu_launches": 3 * args.steps,  # stage-1 quantiser, V codes, attention (the V max reset is a memset)
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = fp8_cpu_baseline(wl, signs)
