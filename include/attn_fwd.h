@@ -101,10 +101,12 @@ int attn_fwd_window(const void *q, const void *k, const void *v, void *o, float 
  *   requires Nq <= Nk.  Non-causal: every key is visible.
  * Nq == 1 (decoding one token) runs on CUDA cores: a matrix-vector product
  *   per (sequence, head), bound by reading K and V; Nq > 1 runs on the tensor
- *   cores in 256-row query blocks.
+ *   cores in 256-row query blocks, and with Nq <= 128 (one 128-row query tile)
+ *   the two halves of a unit take the tile against two key ranges each.
  * num_splits: 1..256 ranges, or 0 to choose (Nq == 1: about 16 (sequence,
  *   head, range) items per SM, ranges of at least 64 keys; else the count
- *   with the shortest estimated makespan over the SMs, at most 64).
+ *   with the shortest estimated makespan over the SMs, at most 64).  With
+ *   2 <= Nq <= 128 an odd count is raised by one.
  * Ownership: like attn_fwd; in addition the library keeps a per-(device,
  *   stream) fp32 workspace for the partial results, grown on demand.
  * Errors: like attn_fwd; Nk == 0, num_splits outside [0, 256] or causal with

@@ -100,6 +100,14 @@ cudaError_t set_smem_attributes() {
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 FwdCfg<128>::kSmemBytes)) != cudaSuccess)
     return e;
+  if ((e = cudaFuncSetAttribute(attn::attn_fwd_kernel<64, attn::kModeSplitPair>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                FwdCfg<64>::kSmemBytes)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(attn::attn_fwd_kernel<128, attn::kModeSplitPair>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                FwdCfg<128>::kSmemBytes)) != cudaSuccess)
+    return e;
   if ((e = cudaFuncSetAttribute(attn::attn_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 attn::kFp8SmemBytes)) != cudaSuccess)
     return e;
@@ -550,24 +558,32 @@ extern "C" int attn_fwd_kvsplit(const void* q, const void* k, const void* v, voi
     return ATTN_OK;
   }
 
+  // At most 128 queries (one query tile per 256-row block): the two query
+  // tiles of a unit would repeat one another, so the two softmax groups take
+  // two different KV ranges of the same tile instead (an even range count).
+  const bool paired = Nq <= attn::kBM;
   int S = num_splits;
   if (S == 0) {
     // The number of ranges with the shortest estimated makespan: units of
     // equal cost run in ceil(units / SMs) rounds of ceil(tiles / S) KV tiles
-    // each; every extra range adds about a quarter tile of partial-result
-    // traffic and merge work.  At most one range per KV tile, at most 64.
+    // each (paired: two ranges per unit); every extra range adds about a
+    // quarter tile of partial-result traffic and merge work.  At most one
+    // range per KV tile (paired: two), at most 64.
     const int64_t tiles = (Nk + attn::kBN - 1) / attn::kBN;
+    const int step = paired ? 2 : 1;
     double best = 0.0;
-    for (int64_t c = 1; c <= std::min<int64_t>(tiles, 64); ++c) {
-      const int64_t rounds = (base_units * c + ds->sms - 1) / ds->sms;
+    for (int64_t c = step; c <= std::max<int64_t>(step, std::min<int64_t>(tiles, 64)); c += step) {
+      const int64_t rounds = (base_units * (c / step) + ds->sms - 1) / ds->sms;
       const double t = (double)rounds * (double)((tiles + c - 1) / c) + 0.25 * (double)(c - 1);
-      if (c == 1 || t < best) {
+      if (c == step || t < best) {
         best = t;
         S = (int)c;
       }
     }
+  } else if (paired && (S & 1)) {
+    ++S;  // paired ranges need an even count
   }
-  const int64_t units = base_units * S;
+  const int64_t units = base_units * (paired ? S / 2 : S);
   const int64_t combine_blocks = (q_tokens * H * 32 + 255) / 256;
   if (units > INT32_MAX || combine_blocks > INT32_MAX) return ATTN_ERR_SHAPE;
 
@@ -604,12 +620,20 @@ extern "C" int attn_fwd_kvsplit(const void* q, const void* k, const void* v, voi
   p.timeout_ns = 2000000000ull;
 
   const int grid = (int)std::min<int64_t>(units, ds->sms);
-  if (d == 64)
+  if (paired) {
+    if (d == 64)
+      attn::attn_fwd_kernel<64, attn::kModeSplitPair>
+          <<<grid, attn::kThreads, FwdCfg<64>::kSmemBytes, s>>>(mq, mk, mv, p);
+    else
+      attn::attn_fwd_kernel<128, attn::kModeSplitPair>
+          <<<grid, attn::kThreads, FwdCfg<128>::kSmemBytes, s>>>(mq, mk, mv, p);
+  } else if (d == 64) {
     attn::attn_fwd_kernel<64, attn::kModeSplit><<<grid, attn::kThreads, FwdCfg<64>::kSmemBytes, s>>>(
         mq, mk, mv, p);
-  else
+  } else {
     attn::attn_fwd_kernel<128, attn::kModeSplit><<<grid, attn::kThreads, FwdCfg<128>::kSmemBytes, s>>>(
         mq, mk, mv, p);
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
   const int blocks = (int)combine_blocks;
   if (d == 64)

@@ -140,7 +140,11 @@ constexpr int kUnitConsumers = 1 + kSoftmaxWarps;  // the MMA thread and every s
 
 // Kernel modes (separate instantiations): plain attention, sliding window,
 // split-KV with separate query and key lengths.
-enum : int { kModePlain = 0, kModeWindow = 1, kModeSplit = 2 };
+enum : int { kModePlain = 0, kModeWindow = 1, kModeSplit = 2, kModeSplitPair = 3 };
+// Split-KV modes.  kModeSplitPair serves query blocks with at most 128 rows
+// (one real query tile): its two softmax groups take the same query tile and
+// two different KV ranges, 2 s and 2 s + 1, of an even number of ranges.
+__host__ __device__ constexpr bool is_split_mode(int m) { return m == kModeSplit || m == kModeSplitPair; }
 
 // One work unit: rows [256 qb, 256 qb + 256) of head h of one sequence
 // (split-KV: and one range of its KV tiles).
@@ -152,7 +156,8 @@ struct Unit {
   int Lk;     // key length (split-KV; else L)
   int kv0;    // first KV tile visited
   int nkv;    // KV tiles visited
-  int split;  // KV range index (split-KV; else 0)
+  int split;  // KV range index (split-KV; else 0); kModeSplitPair: the pair of ranges
+  int kv0b, nkvb;  // kModeSplitPair: the second group's KV tiles (else 0, 0)
 };
 
 // KV tiles [kv0, kv0 + nkv) that hold a key visible to some row of q-block qb
@@ -170,10 +175,12 @@ __host__ __device__ __forceinline__ void unit_kv_range(int L, int qb, int causal
   nkv = k_hi / kBN + 1 - kv0;
 }
 
+template <int kMode>
 __device__ __forceinline__ int num_units(const FwdParams& p) {
-  if (p.cu_seqlens) return *p.num_entries * p.H;
+  if (!is_split_mode(kMode) && p.cu_seqlens) return *p.num_entries * p.H;
   const int nqb = (p.N + kUnitRows - 1) / kUnitRows;
-  return p.B * p.H * nqb * (p.num_splits > 1 ? p.num_splits : 1);
+  const int ranges = kMode == kModeSplitPair ? p.num_splits / 2 : (p.num_splits > 1 ? p.num_splits : 1);
+  return p.B * p.H * nqb * ranges;
 }
 
 // Unit u of the longest-first order.  Dense: q-blocks in decreasing cost
@@ -186,7 +193,9 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
   const int e = u / p.H;
   un.h = u - e * p.H;
   un.split = 0;
-  if (kMode != kModeSplit && p.cu_seqlens) {
+  un.kv0b = 0;
+  un.nkvb = 0;
+  if (!is_split_mode(kMode) && p.cu_seqlens) {
     un.seq = p.work[2 * e];
     un.qb = p.work[2 * e + 1];
     un.tok0 = p.cu_seqlens[un.seq];
@@ -194,9 +203,10 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
   } else {
     const int nqb = (p.N + kUnitRows - 1) / kUnitRows;
     int rank;
-    if (kMode == kModeSplit) {
-      rank = e / (p.B * p.num_splits);
-      const int rem = e - rank * p.B * p.num_splits;
+    if (is_split_mode(kMode)) {
+      const int ranges = kMode == kModeSplitPair ? p.num_splits / 2 : p.num_splits;
+      rank = e / (p.B * ranges);
+      const int rem = e - rank * p.B * ranges;
       un.split = rem / p.B;
       un.seq = rem - un.split * p.B;
     } else {
@@ -207,15 +217,20 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
     un.tok0 = un.seq * p.N;
     un.L = p.N;
   }
-  if (kMode == kModeSplit) {
+  if (is_split_mode(kMode)) {
     // visible KV tiles of the q-block, cut into num_splits near-equal ranges
     un.k_tok0 = un.seq * p.Nk;
     un.Lk = p.Nk;
     const int r_hi = min(un.qb * kUnitRows + kUnitRows, un.L) - 1;
     const int k_hi = p.causal ? min(p.Nk - 1, p.q_off + r_hi) : p.Nk - 1;
     const int n = k_hi / kBN + 1;
-    un.kv0 = (int)((long long)n * un.split / p.num_splits);
-    un.nkv = (int)((long long)n * (un.split + 1) / p.num_splits) - un.kv0;
+    const int s0 = kMode == kModeSplitPair ? 2 * un.split : un.split;
+    un.kv0 = (int)((long long)n * s0 / p.num_splits);
+    un.nkv = (int)((long long)n * (s0 + 1) / p.num_splits) - un.kv0;
+    if (kMode == kModeSplitPair) {
+      un.kv0b = (int)((long long)n * (s0 + 1) / p.num_splits);
+      un.nkvb = (int)((long long)n * (s0 + 2) / p.num_splits) - un.kv0b;
+    }
   } else {
     un.k_tok0 = un.tok0;
     un.Lk = un.L;
@@ -296,35 +311,64 @@ __device__ __forceinline__ void producer_loop(const CUtensorMap* tm_q, const CUt
     // next unit index, fetched while this unit's copies are issued
     const int next_u = (int)gridDim.x + atomicAdd(p.sched, 1);
     const Unit un = decode_unit<kMode>(p, u);
-    if (kMode == kModeSplit && un.nkv <= 0) {  // empty KV range: nothing to copy
+    if (is_split_mode(kMode) && un.nkv <= 0 && un.nkvb <= 0) {  // empty KV ranges: nothing to copy
       u = next_u;
       continue;
     }
     if (units_done > 0 && !wait_bar(ss, kBarQEmpty, (units_done - 1) & 1, p, 1)) return;
     mbar_arrive_expect_tx(bar_addr(ss, kBarQFull), kQTiles * C::kTileBytes);
     for (int g = 0; g < kQTiles; ++g) {
-      const int r0 = un.tok0 + q_tile_start(un, g);
+      // (paired ranges: both groups hold the unit's one query tile)
+      const int r0 = un.tok0 + q_tile_start(un, kMode == kModeSplitPair ? 0 : g);
       for (int c = 0; c < C::kChunks; ++c)
         tma_load_3d(smem_u32(sQ + g * C::kTileBytes + c * kChunkBytes), tm_q,
                     bar_addr(ss, kBarQFull), c * 64, un.h, r0);
     }
-    for (int j = 0; j < un.nkv; ++j) {
-      const int k0 = un.k_tok0 + kv_tile_start(un, un.kv0 + j);
-      for (int kind = 0; kind < 2; ++kind) {
+    if constexpr (kMode == kModeSplitPair) {
+      // the MMA thread's order: K_0(0), K_1(0), then per step j: V_0(j-1),
+      // K_0(j), V_1(j-1), K_1(j), each while the group's range lasts
+      const int nk[2] = {un.nkv, un.nkvb}, k0s[2] = {un.kv0, un.kv0b};
+      auto push = [&](int kind, int g, int j) -> bool {
         const int slot = ring % C::kStages;
         const uint32_t n = ring / C::kStages;
-        if (n > 0 && !wait_bar(ss, kBarKV + C::kStages + slot, (n - 1) & 1, p, 2)) return;
+        if (n > 0 && !wait_bar(ss, kBarKV + C::kStages + slot, (n - 1) & 1, p, 4)) return false;
         const uint32_t full = bar_addr(ss, kBarKV + slot);
         mbar_arrive_expect_tx(full, C::kTileBytes);
-        if (p.fault_inject == 1 && blockIdx.x == 0 && !injected && kind == 0) {
-          injected = true;  // test hook: the bytes this barrier waits for never come
-        } else {
-          const CUtensorMap* tm = kind == 0 ? tm_k : tm_v;
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_3d(smem_u32(sRing + slot * C::kTileBytes + c * kChunkBytes), tm, full,
-                        c * 64, un.h, k0);
-        }
+        const int k0 = un.k_tok0 + kv_tile_start(un, k0s[g] + j);
+        const CUtensorMap* tm = kind == 0 ? tm_k : tm_v;
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(smem_u32(sRing + slot * C::kTileBytes + c * kChunkBytes), tm, full, c * 64,
+                      un.h, k0);
         ++ring;
+        return true;
+      };
+      for (int g = 0; g < kQTiles; ++g)
+        if (nk[g] > 0 && !push(0, g, 0)) return;
+      const int steps = max(nk[0], nk[1]);
+      for (int j = 1; j <= steps; ++j)
+        for (int g = 0; g < kQTiles; ++g) {
+          if (j - 1 < nk[g] && !push(1, g, j - 1)) return;
+          if (j < nk[g] && !push(0, g, j)) return;
+        }
+    } else {
+      for (int j = 0; j < un.nkv; ++j) {
+        const int k0 = un.k_tok0 + kv_tile_start(un, un.kv0 + j);
+        for (int kind = 0; kind < 2; ++kind) {
+          const int slot = ring % C::kStages;
+          const uint32_t n = ring / C::kStages;
+          if (n > 0 && !wait_bar(ss, kBarKV + C::kStages + slot, (n - 1) & 1, p, 2)) return;
+          const uint32_t full = bar_addr(ss, kBarKV + slot);
+          mbar_arrive_expect_tx(full, C::kTileBytes);
+          if (p.fault_inject == 1 && blockIdx.x == 0 && !injected && kind == 0) {
+            injected = true;  // test hook: the bytes this barrier waits for never come
+          } else {
+            const CUtensorMap* tm = kind == 0 ? tm_k : tm_v;
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_3d(smem_u32(sRing + slot * C::kTileBytes + c * kChunkBytes), tm, full,
+                          c * 64, un.h, k0);
+          }
+          ++ring;
+        }
       }
     }
     ++units_done;
@@ -385,6 +429,62 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
            kk > 0 ? 1u : acc0);
 }
 
+// One unit of paired split-KV ranges: group g multiplies the unit's query
+// tile with the KV tiles of its own range (group 0: kv0 .., group 1: kv0b ..),
+// in the producer's order.  False when a wait gave up.
+template <int D>
+__device__ __forceinline__ bool mma_unit_pair(const FwdParams& p, SharedState& ss,
+                                              const uint32_t (&q_smem)[2], uint8_t* sRing,
+                                              uint32_t tmem, const Unit& un, int units_done,
+                                              uint32_t& ring, uint32_t (&pcount)[2]) {
+  using C = FwdCfg<D>;
+  auto slot_smem = [&](uint32_t pos) { return smem_u32(sRing + (pos % C::kStages) * C::kTileBytes); };
+  auto wait_full = [&](uint32_t pos) {
+    return wait_bar(ss, kBarKV + pos % C::kStages, (pos / C::kStages) & 1, p, 15);
+  };
+  auto release = [&](uint32_t pos) { mma_commit(bar_addr(ss, kBarKV + C::kStages + pos % C::kStages)); };
+  const int nk[2] = {un.nkv, un.nkvb};
+  int s_left = nk[0] + nk[1];  // S products still to issue (Q is free after the last)
+  if (!wait_bar(ss, kBarQFull, units_done & 1, p, 16)) return false;
+  tc_fence_after();
+  for (int g = 0; g < kQTiles; ++g) {
+    if (nk[g] <= 0) continue;
+    const uint32_t pos = ring++;
+    if (!wait_full(pos)) return false;
+    tc_fence_after();
+    issue_qk<D>(tmem + C::col_s(g), q_smem[g], slot_smem(pos));
+    mma_commit(bar_addr(ss, kBarSFull + g));
+    release(pos);
+    if (--s_left == 0) mma_commit(bar_addr(ss, kBarQEmpty));
+  }
+  const int steps = max(nk[0], nk[1]);
+  for (int j = 1; j <= steps; ++j) {
+    for (int g = 0; g < kQTiles; ++g) {
+      if (j - 1 >= nk[g]) continue;
+      const uint32_t posV = ring++;
+      if (!wait_full(posV)) return false;
+      // P_g of tile j-1 is in TMEM (and O_g rescaled if needed)
+      if (!wait_bar(ss, kBarPFull + g, pcount[g] & 1, p, 17 + g)) return false;
+      ++pcount[g];
+      tc_fence_after();
+      issue_pv<D>(tmem + C::col_o(g), tmem + C::col_s(g), slot_smem(posV), j > 1);
+      release(posV);
+      if (j < nk[g]) {
+        const uint32_t posK = ring++;
+        if (!wait_full(posK)) return false;
+        tc_fence_after();
+        issue_qk<D>(tmem + C::col_s(g), q_smem[g], slot_smem(posK));
+        mma_commit(bar_addr(ss, kBarSFull + g));
+        release(posK);
+        if (--s_left == 0) mma_commit(bar_addr(ss, kBarQEmpty));
+      } else {
+        mma_commit(bar_addr(ss, kBarOFull + g));
+      }
+    }
+  }
+  return true;
+}
+
 template <int D, int kMode>
 __device__ __forceinline__ void mma_loop(const FwdParams& p, SharedState& ss, uint8_t* sQ,
                                          uint8_t* sRing, uint32_t tmem, int n_units) {
@@ -407,6 +507,12 @@ __device__ __forceinline__ void mma_loop(const FwdParams& p, SharedState& ss, ui
     // an empty KV range (split-KV with more ranges than tiles) has no copy,
     // no MMA and no barrier traffic: the softmax warps write its empty result
     if (kMode == kModeSplit && un.nkv <= 0) continue;
+    if (kMode == kModeSplitPair) {
+      if (un.nkv <= 0 && un.nkvb <= 0) continue;
+      if (!mma_unit_pair<D>(p, ss, q_smem, sRing, tmem, un, units_done, ring, pcount)) return;
+      ++units_done;
+      continue;
+    }
     if (!wait_bar(ss, kBarQFull, units_done & 1, p, 11)) return;
     tc_fence_after();
     uint32_t posK = ring, posV = ring + 1;
@@ -548,13 +654,20 @@ __device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss
   if (pair_sync_check(g, quadrant, fail)) return;
   for (;;) {
     if (u < 0) return;
-    const Unit un = decode_unit<kMode>(p, u);
+    Unit un = decode_unit<kMode>(p, u);
+    // paired split-KV ranges: this group's range, its index, the one query tile
+    const int tg = kMode == kModeSplitPair ? 0 : g;
+    const int split_idx = kMode == kModeSplitPair ? 2 * un.split + g : un.split;
+    if (kMode == kModeSplitPair && g == 1) {
+      un.kv0 = un.kv0b;
+      un.nkv = un.nkvb;
+    }
     constexpr bool kWindow = kMode == kModeWindow;
-    const int Lk = kMode == kModeSplit ? un.Lk : un.L;
-    const int q_off = kMode == kModeSplit ? p.q_off : 0;  // key position of query row 0
-    const int a0 = q_tile_start(un, g);
+    const int Lk = is_split_mode(kMode) ? un.Lk : un.L;
+    const int q_off = is_split_mode(kMode) ? p.q_off : 0;  // key position of query row 0
+    const int a0 = q_tile_start(un, tg);
     const int row = a0 + trow;                       // sequence-relative row of this thread
-    const int nominal0 = un.qb * kUnitRows + g * kBM;
+    const int nominal0 = un.qb * kUnitRows + tg * kBM;
     float m_used = -INFINITY;
     float l = 0.f;     // sum of the fp32 probabilities (this half): the LSE
     float l_fix = 0.f; // rounding change of each tile's largest probability (this half)
@@ -691,17 +804,17 @@ __device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss
     // (an empty KV range of split-KV has no MMA work and no O-done signal;
     // after a failed wait the kernel is stopping and what is stored below is
     // not a result)
-    const bool has_o = kMode != kModeSplit || un.nkv > 0;
+    const bool has_o = !is_split_mode(kMode) || un.nkv > 0;
     if (has_o) {
       fail |= !__all_sync(0xffffffffu, wait_bar(ss, kBarOFull + g, units_done & 1, p, 22 + g));
       tc_fence_after();
     }
     const bool store = row >= nominal0 && row < un.L && row >= 0;
-    if (kMode == kModeSplit) {
+    if (is_split_mode(kMode)) {
       // partial result of this KV range: O / l_r (fp32) and its LSE; the
       // combine kernel merges the ranges
       const float inv = l_r > 0.f ? 1.0f / l_r : 0.f;
-      float* prow = p.o_part + (((size_t)un.split * p.B * p.N + (store ? un.tok0 + row : 0)) * p.H + un.h) * D +
+      float* prow = p.o_part + (((size_t)split_idx * p.B * p.N + (store ? un.tok0 + row : 0)) * p.H + un.h) * D +
                     half * kOCols;
 #pragma unroll
       for (int cc = 0; cc < kOCols; cc += 32) {
@@ -722,7 +835,7 @@ __device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss
         }
       }
       if (store && half == 0)
-        p.lse_part[(((size_t)un.split * p.B + un.seq) * p.H + un.h) * p.N + row] =
+        p.lse_part[(((size_t)split_idx * p.B + un.seq) * p.H + un.h) * p.N + row] =
             l > 0.f ? m_used * p.scale + __log2f(l) * 0.69314718055994531f : -INFINITY;
       tc_fence_before();
       if (has_o) ++units_done;
@@ -825,7 +938,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ss.tmem_base;
-  const int n_units = num_units(p);
+  const int n_units = num_units<kMode>(p);
 
   if (warp >= kSoftmaxWarps) {
     setmaxnreg_dec<kControlRegs>();
