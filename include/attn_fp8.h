@@ -1,5 +1,5 @@
 /*
- * C ABI of the GB300 (sm_103a) FP8 attention forward (e4m3, d = 128).
+ * C ABI of the GB300 (sm_103a) FP8 attention forward (e4m3, d = 64 or 128).
  *
  * The FP8 path of the pages ("flash-attention-evolution" (letsgetai),
  * FlashAttention-3 section, item 3; "FlashAttention 1-4 演进速查"
@@ -16,14 +16,14 @@
  * This is an approximation of the exact attention of attn_fwd.h.
  *
  * Layouts as in attn_fwd.h.  Dense (cu_seqlens == NULL): q, k, v, o
- * [B, N, H, 128] bf16, lse [B, H, N] fp32.  Packed (cu_seqlens int32[B+1] on
+ * [B, N, H, d] bf16, lse [B, H, N] fp32.  Packed (cu_seqlens int32[B+1] on
  * the device, lengths <= N, checked on the device like attn_fwd's): q, k, v, o
- * [total, H, 128], lse [H, total], total = cu_seqlens[B].  The per-sequence
+ * [total, H, d], lse [H, total], total = cu_seqlens[B].  The per-sequence
  * outputs of the quantisers keep their dense shapes with N as the length
  * bound: a sequence of length L has blocks [0, ceil(L / 128)) written, the
  * rest of its rows untouched.  Same conventions as attn_fwd.h (device
  * pointers, asynchronous on stream, status codes, error word); d other than
- * 128 returns ATTN_ERR_HEADDIM.
+ * 64 or 128 returns ATTN_ERR_HEADDIM.
  */
 #ifndef IO_AWARE_EXACT_06_ATTN_FP8_H
 #define IO_AWARE_EXACT_06_ATTN_FP8_H
@@ -37,21 +37,21 @@ extern "C" {
 #endif
 
 /*
- * attn_fp8_quantize_qk: the Q or K quantisation step.  x [B, N, H, 128] bf16
- * (packed: [total, H, 128]); codes e4m3 (uint8) of the same shape; scales
+ * attn_fp8_quantize_qk: the Q or K quantisation step.  x [B, N, H, d] bf16
+ * (packed: [total, H, d]); codes e4m3 (uint8) of the same shape; scales
  * [B, H, T] fp32, T = ceil(N / 128): block t holds rows [128 t, 128 t + 128)
  * of a sequence (of length L) and head, the last block pulled back to end at L
  * (the rows it shares with block t - 1 keep that block's codes; rows before
  * the sequence count as zero).  cu_seqlens: NULL (dense) or as above.  signs:
- * host array of 128 int8 (+1 / -1) for the rotation, or NULL for no rotation.
+ * host array of d int8 (+1 / -1) for the rotation, or NULL for no rotation.
  */
 int attn_fp8_quantize_qk(const void *x, uint8_t *codes, float *scales, int B, int H, int N,
                          int d, const int32_t *cu_seqlens, const int8_t *signs,
                          attn_stream_t stream);
 
 /*
- * attn_fp8_quantize_v: the V quantisation step.  v [B, N, H, 128] bf16
- * (packed: [total, H, 128]); codes_t [B, H, 128, Np] e4m3 with
+ * attn_fp8_quantize_v: the V quantisation step.  v [B, N, H, d] bf16
+ * (packed: [total, H, d]); codes_t [B, H, d, Np] e4m3 with
  * Np = 128 * ceil(N / 128): the codes transposed per sequence and head (keys
  * contiguous), keys L .. 128 ceil(L / 128) - 1 zero for a sequence of length
  * L; scale [B, H] fp32 (max |V| / 448 of the sequence and head; 1 when that

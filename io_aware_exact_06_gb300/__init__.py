@@ -203,21 +203,21 @@ def attn_bwd_window(q, k, v, o, dout, lse, dq, dk, dv, B: int, H: int, N: int, d
     return st
 
 
-def _signs(signs):
-    """A host int8[128] sign vector (kept alive by the caller) or None."""
+def _signs(signs, d: int):
+    """A host int8[d] sign vector (kept alive by the caller) or None."""
     if signs is None:
         return None, None
     import numpy as np
     arr = np.ascontiguousarray(signs, dtype=np.int8)
-    if arr.shape != (128,):
-        raise ValueError("signs must hold 128 entries of +1 / -1")
+    if arr.shape != (int(d),):
+        raise ValueError(f"signs must hold d = {int(d)} entries of +1 / -1")
     return arr, arr.ctypes.data
 
 
 def attn_fwd_fp8(q, k, v, o, lse, B: int, H: int, N: int, d: int, scale: float, causal: bool,
                  signs=None, cu_seqlens=None, stream=None) -> int:
-    """The C call ``attn_fwd_fp8`` (e4m3 path; signs: 128 x +-1 or None)."""
-    keep, sp = _signs(signs)
+    """The C call ``attn_fwd_fp8`` (e4m3 path; signs: d x +-1 or None)."""
+    keep, sp = _signs(signs, d)
     st = lib().attn_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(N),
                             int(d), float(scale), int(bool(causal)), _ptr(cu_seqlens), sp,
                             _stream(stream))
@@ -230,7 +230,7 @@ def attn_fwd_fp8(q, k, v, o, lse, B: int, H: int, N: int, d: int, scale: float, 
 def attn_fp8_quantize_qk(x, codes, scales, B: int, H: int, N: int, d: int, signs=None,
                          cu_seqlens=None, stream=None) -> int:
     """The C call ``attn_fp8_quantize_qk``."""
-    keep, sp = _signs(signs)
+    keep, sp = _signs(signs, d)
     st = lib().attn_fp8_quantize_qk(_ptr(x), _ptr(codes), _ptr(scales), int(B), int(H), int(N),
                                     int(d), _ptr(cu_seqlens), sp, _stream(stream))
     del keep

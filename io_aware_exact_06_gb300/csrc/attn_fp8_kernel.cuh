@@ -1,5 +1,7 @@
-// FP8 (e4m3) fused attention forward for sm_103a, d = 128, dense or packed
-// variable-length batches.
+// FP8 (e4m3) fused attention forward for sm_103a, d = 64 or 128, dense or
+// packed variable-length batches.  The attention kernel keeps Q and K codes
+// in rows of 128 bytes (d = 64: channels 64..127 zero), so both head
+// dimensions share the 128-byte-swizzled S product; the P V product has N = d.
 //
 // The pages name the FP8 path's two devices without formulas: block
 // quantisation and incoherent processing ("flash-attention-evolution"
@@ -53,7 +55,7 @@
 
 namespace attn {
 
-constexpr int kFp8D = 128;
+constexpr int kFp8D = 128;  // bytes of a Q / K code row in the attention kernel (channels, padded)
 constexpr int kFp8TileBytes = kBM * kFp8D;   // 128 rows x 128 e4m3 = one 128-byte swizzle span
 constexpr int kFp8Stages = 8;                // K / V ring slots
 constexpr int kFp8SmemBytes = kQTiles * kFp8TileBytes + kFp8Stages * kFp8TileBytes + 1024;
@@ -68,6 +70,10 @@ __host__ __device__ constexpr uint32_t make_idesc_e4m3(uint32_t M, uint32_t N) {
   return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 constexpr uint32_t kIdescFp8 = make_idesc_e4m3(kBM, kBN);
+// TMEM columns of the attention kernel: S_g at 128 g (P_g over its first 32
+// columns), O_g at 256 + D g.
+template <int D>
+__host__ __device__ constexpr uint32_t fp8_col_o(int g) { return 256u + (uint32_t)D * g; }
 
 __device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate) {
@@ -94,7 +100,7 @@ __device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint
 }
 
 struct Fp8Params {
-  __nv_bfloat16* o;     // [tokens, H, 128]
+  __nv_bfloat16* o;     // [tokens, H, d]
   float* lse;           // dense [B, H, N]; packed [H, cu_seqlens[B]]
   const float* sq;      // [B*H][T]: Q block scales
   const float* sk;      // [B*H][T]: K block scales
@@ -118,20 +124,22 @@ struct Fp8Signs {
 
 // ----------------------------------------------------------- quantisers --
 constexpr int kQuantWarps = 16;  // warps per quantiser CTA (one 128-row block)
-// x H_128 of the 128 values held 4 per lane (lane l: channels 4l..4l+3),
-// fp32 butterflies over strides 1, 2 (in the lane) and 4..64 (across lanes):
+// x H_D of the D values held 4 per lane (lane l: channels 4l..4l+3),
+// fp32 butterflies over strides 1, 2 (in the lane) and 4..D/2 (across lanes):
 // the lower element a of a pair becomes a + b, the upper b becomes a - b.
 // Across lanes both are one fma of the lane's own value with a per-lane sign
 // (+1 lower, -1 upper) and the partner's value: fma(+1, a, b) = a + b and
 // fma(-1, b, a) = a - b, each rounded once like the additions.
-__device__ __forceinline__ void fwht128_warp(float (&v)[4], int lane) {
+// (d = 64: the same over lanes 0..15, strides 4..32; lanes 16..31 hold zeros)
+template <int D>
+__device__ __forceinline__ void fwht_warp(float (&v)[4], int lane) {
   float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
   v[0] = a0 + a2;
   v[1] = a1 + a3;
   v[2] = a0 - a2;
   v[3] = a1 - a3;
 #pragma unroll
-  for (int m = 1; m < 32; m <<= 1) {
+  for (int m = 1; m < D / 4; m <<= 1) {
     const float sg = (lane & m) ? -1.0f : 1.0f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) v[j] = fmaf(sg, v[j], __shfl_xor_sync(0xffffffffu, v[j], m));
@@ -151,14 +159,18 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
 // tok0 + L)) is pulled back to end at L, so no copy leaves the sequence, and
 // leaves the rows it shares with the block before it to that block; rows
 // before the sequence count as zero.
-constexpr int kQuantRowBytes = kFp8D * 2;
-constexpr int kQuantBlockBytes = kBM * kQuantRowBytes;
-constexpr int kQuantSmemBytes = 2 * kQuantBlockBytes + 1024;
+template <int D>
+struct QuantCfg {
+  static constexpr int kRowBytes = D * 2;  // one bf16 input row
+  static constexpr int kBlockBytes = kBM * kRowBytes;
+  static constexpr int kSmemBytes = 2 * kBlockBytes + 1024;
+};
 constexpr int kQuantRows = kBM / kQuantWarps;  // rows per warp: warp + kQuantWarps i
 
 // First half of a Q or K block: rotation of the warp's 8 rows (held in
 // registers) and their max |x| into warp_max[warp].  Rows r0 + i of the
-// block are at i * 256 bytes of `stage`.
+// block are at i * 2 D bytes of `stage`; lanes >= D/4 hold zeros.
+template <int D>
 __device__ __forceinline__ void fp8_rotate_rows(const uint8_t* stage, int r0, const uint32_t (&flip)[2],
                                                 int rotate, float (&v)[kQuantRows][4],
                                                 float* warp_max) {
@@ -167,15 +179,15 @@ __device__ __forceinline__ void fp8_rotate_rows(const uint8_t* stage, int r0, co
 #pragma unroll
   for (int i = 0; i < kQuantRows; ++i) {
     const int r = warp + kQuantWarps * i;
-    const uint2 raw = r0 + r >= 0
-                          ? *reinterpret_cast<const uint2*>(stage + r * kQuantRowBytes + 8 * lane)
+    const uint2 raw = r0 + r >= 0 && lane < D / 4
+                          ? *reinterpret_cast<const uint2*>(stage + r * QuantCfg<D>::kRowBytes + 8 * lane)
                           : make_uint2(0u, 0u);
     const uint32_t w0 = raw.x ^ flip[0], w1 = raw.y ^ flip[1];
     v[i][0] = __uint_as_float(w0 << 16);
     v[i][1] = __uint_as_float(w0 & 0xffff0000u);
     v[i][2] = __uint_as_float(w1 << 16);
     v[i][3] = __uint_as_float(w1 & 0xffff0000u);
-    if (rotate) fwht128_warp(v[i], lane);
+    if (rotate) fwht_warp<D>(v[i], lane);
     amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[i][0]), fabsf(v[i][1])),
                              fmaxf(fabsf(v[i][2]), fabsf(v[i][3]))));
   }
@@ -185,10 +197,12 @@ __device__ __forceinline__ void fp8_rotate_rows(const uint8_t* stage, int r0, co
 }
 
 // Second half: the block max from warp_max, the scale, and the codes of the
-// rows that belong to block t.
+// rows that belong to block t, in rows of `stride` bytes (channels >= D of a
+// padded row get code 0).
+template <int D>
 __device__ __forceinline__ void fp8_write_codes(const float (&v)[kQuantRows][4], const float* warp_max,
                                                 uint8_t* codes, float* scale_out, int tok0, int r0,
-                                                int t, int h, int H) {
+                                                int t, int h, int H, int stride) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   float amax = warp_max[0];
 #pragma unroll
@@ -198,23 +212,25 @@ __device__ __forceinline__ void fp8_write_codes(const float (&v)[kQuantRows][4],
 #pragma unroll
   for (int i = 0; i < kQuantRows; ++i) {
     const int row = r0 + warp + kQuantWarps * i;
-    if (row < t * kBM) continue;  // the previous block's row (or before the sequence)
-    *reinterpret_cast<uint32_t*>(codes + ((size_t)(tok0 + row) * H + h) * kFp8D + 4 * lane) =
-        e4m3x4(__fmul_rn(v[i][0], inv), __fmul_rn(v[i][1], inv), __fmul_rn(v[i][2], inv),
-               __fmul_rn(v[i][3], inv));
+    if (row < t * kBM || 4 * lane >= stride) continue;  // the previous block's row, or past the row
+    *reinterpret_cast<uint32_t*>(codes + ((size_t)(tok0 + row) * H + h) * stride + 4 * lane) =
+        lane < D / 4 ? e4m3x4(__fmul_rn(v[i][0], inv), __fmul_rn(v[i][1], inv),
+                              __fmul_rn(v[i][2], inv), __fmul_rn(v[i][3], inv))
+                     : 0u;
   }
 }
 
 // max |V| over the rows of block t (rows >= 128 t of the staged rows r0 ..)
 // into warp_max[warp].
+template <int D>
 __device__ __forceinline__ void fp8_rows_amax(const uint8_t* stage, int r0, int t, float* warp_max) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   float m = 0.f;
 #pragma unroll
   for (int i = 0; i < kQuantRows; ++i) {
     const int r = warp + kQuantWarps * i;
-    if (r0 + r < t * kBM) continue;
-    const uint2 w = *reinterpret_cast<const uint2*>(stage + r * kQuantRowBytes + 8 * lane);
+    if (r0 + r < t * kBM || lane >= D / 4) continue;
+    const uint2 w = *reinterpret_cast<const uint2*>(stage + r * QuantCfg<D>::kRowBytes + 8 * lane);
     m = fmaxf(m, fmaxf(fmaxf(fabsf(__uint_as_float(w.x << 16)), fabsf(__uint_as_float(w.x & 0xffff0000u))),
                        fmaxf(fabsf(__uint_as_float(w.y << 16)), fabsf(__uint_as_float(w.y & 0xffff0000u)))));
   }
@@ -242,15 +258,18 @@ __device__ __forceinline__ bool fp8_seq_block(const int* cu_seqlens, const int* 
 // [0, n_blocks): blocks [0, nb) quantise Q, [nb, 2 nb) quantise K, [2 nb,
 // 3 nb) take the max |V| per (sequence, head) (atomic max of the
 // non-negative fp32 bit patterns); nb = B * H * T, block = (b * H + h) * T + t.
-// tm_q, tm_k, tm_v: [tokens][H][128] bf16, box 128 channels x 1 head x 128
-// rows, no swizzle (a map of an absent input is never used).
+// tm_q, tm_k, tm_v: [tokens][H][D] bf16, box D channels x 1 head x 128 rows,
+// no swizzle (a map of an absent input is never used).  Codes go to rows of
+// code_stride bytes (D, or 128 for the attention kernel's padded rows).
+template <int D>
 __global__ void __launch_bounds__(32 * kQuantWarps, 2)
 fp8_quant_stage1_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, uint8_t* q8, uint8_t* k8,
                         float* sq, float* sk, unsigned int* amax_v, int B, int H, int N, int T,
                         Fp8Signs signs, int rotate, int block0, int n_blocks,
-                        const int* cu_seqlens, const int* num_entries, int* err) {
+                        const int* cu_seqlens, const int* num_entries, int* err, int code_stride) {
+  using QC = QuantCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* stage = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -277,8 +296,8 @@ fp8_quant_stage1_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (i >= n_blocks || !locate(i, seg, idx, h, tok0, t, r0)) return;
     const CUtensorMap* tm = seg == 0 ? &tm_q : (seg == 1 ? &tm_k : &tm_v);
     const uint32_t bar = smem_u32(&full[buf]);
-    mbar_arrive_expect_tx(bar, kQuantBlockBytes);
-    tma_load_3d(smem_u32(stage + buf * kQuantBlockBytes), tm, bar, 0, h, tok0 + r0);
+    mbar_arrive_expect_tx(bar, QC::kBlockBytes);
+    tma_load_3d(smem_u32(stage + buf * QC::kBlockBytes), tm, bar, 0, h, tok0 + r0);
   };
   // the signs of this lane's channels 4 lane .. 4 lane + 3 as bf16 sign bits
   // of the two 32-bit words that hold them (negation is exact)
@@ -313,11 +332,11 @@ fp8_quant_stage1_kernel(const __grid_constant__ CUtensorMap tm_q,
         failed = true;
         break;
       }
-      const uint8_t* st = stage + buf * kQuantBlockBytes;
+      const uint8_t* st = stage + buf * QC::kBlockBytes;
       if (seg < 2)
-        fp8_rotate_rows(st, r0, flip, rotate, v, warp_max[k & 1]);
+        fp8_rotate_rows<D>(st, r0, flip, rotate, v, warp_max[k & 1]);
       else
-        fp8_rows_amax(st, r0, t, warp_max[k & 1]);
+        fp8_rows_amax<D>(st, r0, t, warp_max[k & 1]);
     }
     __syncthreads();  // every read of this buffer is done; warp_max is complete
     if (threadIdx.x == 0) {
@@ -327,9 +346,9 @@ fp8_quant_stage1_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     if (!valid) continue;
     if (seg == 0) {
-      fp8_write_codes(v, warp_max[k & 1], q8, sq + idx, tok0, r0, t, h, H);
+      fp8_write_codes<D>(v, warp_max[k & 1], q8, sq + idx, tok0, r0, t, h, H, code_stride);
     } else if (seg == 1) {
-      fp8_write_codes(v, warp_max[k & 1], k8, sk + idx, tok0, r0, t, h, H);
+      fp8_write_codes<D>(v, warp_max[k & 1], k8, sk + idx, tok0, r0, t, h, H, code_stride);
     } else if (threadIdx.x == 0) {
       float m = warp_max[k & 1][0];
 #pragma unroll
@@ -353,10 +372,11 @@ fp8_quant_stage1_kernel(const __grid_constant__ CUtensorMap tm_q,
 // (a warp writes one key's 128 bytes), then each thread gathers 16 keys of one
 // channel (the bytes a warp reads at once lie in 8 words: no bank conflict)
 // and writes them as one 16-byte store.
+template <int D>
 __global__ void __launch_bounds__(256)
 fp8_quant_v_kernel(const __nv_bfloat16* v, const unsigned int* amax_bits, float* sv, uint8_t* vt,
                    int B, int H, int N, int Np, const int* cu_seqlens, const int* num_entries) {
-  __shared__ __align__(16) uint8_t tile[kBN][kFp8D];
+  __shared__ __align__(16) uint8_t tile[kBN][D];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int T = Np / kBN;
   const int t = blockIdx.x % T;
@@ -373,29 +393,30 @@ fp8_quant_v_kernel(const __nv_bfloat16* v, const unsigned int* amax_bits, float*
 #pragma unroll
   for (int i = 0; i < kRowsV; ++i) {
     const int key = t * kBN + warp + 8 * i;
-    raw[i] = key < L ? *reinterpret_cast<const uint2*>(v + ((size_t)(tok0 + key) * H + h) * kFp8D +
-                                                       4 * lane)
-                     : make_uint2(0u, 0u);
+    raw[i] = key < L && lane < D / 4
+                 ? *reinterpret_cast<const uint2*>(v + ((size_t)(tok0 + key) * H + h) * D + 4 * lane)
+                 : make_uint2(0u, 0u);
   }
 #pragma unroll
   for (int i = 0; i < kRowsV; ++i) {
     const float f0 = __uint_as_float(raw[i].x << 16), f1 = __uint_as_float(raw[i].x & 0xffff0000u);
     const float f2 = __uint_as_float(raw[i].y << 16), f3 = __uint_as_float(raw[i].y & 0xffff0000u);
-    *reinterpret_cast<uint32_t*>(&tile[warp + 8 * i][4 * lane]) =
-        e4m3x4(__fmul_rn(f0, inv), __fmul_rn(f1, inv), __fmul_rn(f2, inv), __fmul_rn(f3, inv));
+    if (lane < D / 4)
+      *reinterpret_cast<uint32_t*>(&tile[warp + 8 * i][4 * lane]) =
+          e4m3x4(__fmul_rn(f0, inv), __fmul_rn(f1, inv), __fmul_rn(f2, inv), __fmul_rn(f3, inv));
   }
   __syncthreads();
   // output chunk i: channel c = i % 128, keys 16 q .. 16 q + 15 with q = i / 128
 #pragma unroll
-  for (int i = threadIdx.x; i < kFp8D * (kBN / 16); i += 256) {
-    const int c = i % kFp8D, q = i / kFp8D;
+  for (int i = threadIdx.x; i < D * (kBN / 16); i += 256) {
+    const int c = i % D, q = i / D;
     uint32_t w[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j)
       w[j] = (uint32_t)tile[16 * q + 4 * j][c] | ((uint32_t)tile[16 * q + 4 * j + 1][c] << 8) |
              ((uint32_t)tile[16 * q + 4 * j + 2][c] << 16) |
              ((uint32_t)tile[16 * q + 4 * j + 3][c] << 24);
-    *reinterpret_cast<uint4*>(vt + ((size_t)bh * kFp8D + c) * Np + t * kBN + q * 16) =
+    *reinterpret_cast<uint4*>(vt + ((size_t)bh * D + c) * Np + t * kBN + q * 16) =
         make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
@@ -412,14 +433,16 @@ __device__ __forceinline__ void issue_qk_fp8(uint32_t d_tmem, uint32_t q_smem, u
 }
 
 // O (+)= P V over 4 k-steps of 32 keys: P (e4m3, four per TMEM column, keys
-// 32 kk.. in columns 8 kk..) and V^T (128 channels x 128 keys, K-major).
+// 32 kk.. in columns 8 kk..) and V^T (D channels x 128 keys, K-major).
+template <int D>
 __device__ __forceinline__ void issue_pv_fp8(uint32_t d_tmem, uint32_t p_tmem, uint32_t vt_smem,
                                              bool accumulate) {
+  constexpr uint32_t kIdescPV = make_idesc_e4m3(kBM, D);
   const uint64_t b0 = make_sdesc(vt_smem, 16, 1024, kSwizzle128B);
   const uint32_t acc0 = accumulate ? 1u : 0u;
 #pragma unroll
   for (int kk = 0; kk < kBN / 32; ++kk)
-    mma_f8_ts(d_tmem, p_tmem + 8 * kk, b0 + (uint64_t)(kk * 2), kIdescFp8, kk > 0 ? 1u : acc0);
+    mma_f8_ts(d_tmem, p_tmem + 8 * kk, b0 + (uint64_t)(kk * 2), kIdescPV, kk > 0 ? 1u : acc0);
 }
 
 __device__ __forceinline__ bool fp8_wait(SharedState& ss, int bar, uint32_t parity,
@@ -481,6 +504,7 @@ __device__ __forceinline__ int fp8_q_start(const Fp8Unit& un, int g) {
   return min(un.qb * kUnitRows + g * kBM, un.L - kBM);
 }
 
+template <int D>
 __device__ __forceinline__ void fp8_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                              const CUtensorMap* tm_vt, const Fp8Params& p,
                                              SharedState& ss, uint8_t* sQ, uint8_t* sRing,
@@ -512,7 +536,8 @@ __device__ __forceinline__ void fp8_producer(const CUtensorMap* tm_q, const CUte
         const uint32_t n = ring / kFp8Stages;
         if (n > 0 && !fp8_wait(ss, kBarKV + kFp8Stages + slot, (n - 1) & 1, p, 202)) return;
         const uint32_t full = bar_addr(ss, kBarKV + slot);
-        mbar_arrive_expect_tx(full, kFp8TileBytes);
+        // K: 128 keys x 128 code bytes; V^T: D channels x 128 keys
+        mbar_arrive_expect_tx(full, kind == 0 ? kFp8TileBytes : D * kBN);
         const uint32_t dst = smem_u32(sRing + slot * kFp8TileBytes);
         if (kind == 0)
           tma_load_3d(dst, tm_k, full, 0, un.h, un.tok0 + j * kBN);
@@ -543,6 +568,7 @@ __device__ __forceinline__ bool fp8_next_unit(SharedState& ss, const Fp8Params& 
   return true;
 }
 
+template <int D>
 __device__ __forceinline__ void fp8_mma_loop(const Fp8Params& p, SharedState& ss, uint8_t* sQ,
                                              uint8_t* sRing, uint32_t tmem) {
   uint32_t ring = 0;
@@ -585,7 +611,7 @@ __device__ __forceinline__ void fp8_mma_loop(const Fp8Params& p, SharedState& ss
         if (!fp8_wait(ss, kBarPFull + g, pcount[g] & 1, p, 212 + g)) return;
         ++pcount[g];
         tc_fence_after();
-        issue_pv_fp8(tmem + 256u + 128u * g, tmem + 128u * g, slot_smem(posV), j > 1);
+        issue_pv_fp8<D>(tmem + fp8_col_o<D>(g), tmem + 128u * g, slot_smem(posV), j > 1);
         if (g == kQTiles - 1) release(posV);
         if (more) {
           if (g == 0) {
@@ -608,6 +634,7 @@ __device__ __forceinline__ void fp8_mma_loop(const Fp8Params& p, SharedState& ss
   }
 }
 
+template <int D>
 __device__ __forceinline__ void fp8_softmax_loop(const Fp8Params& p, SharedState& ss,
                                                  uint32_t tmem, int g) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -617,7 +644,8 @@ __device__ __forceinline__ void fp8_softmax_loop(const Fp8Params& p, SharedState
   const uint32_t lane_addr = tmem + ((uint32_t)(quadrant * 32) << 16);
   const uint32_t colS = 128u * g + half * kHalfCols;
   const uint32_t colP = 128u * g + half * 16u;        // 64 e4m3 = 16 columns
-  const uint32_t colO = 256u + 128u * g + half * 64u; // this thread's 64 O columns
+  constexpr int kOCols = D / 2;                       // O columns of this thread
+  const uint32_t colO = fp8_col_o<D>(g) + half * kOCols;
   uint32_t scount = 0, uslot = 0;
   int units_done = 0;
   int u = -1;
@@ -709,7 +737,7 @@ __device__ __forceinline__ void fp8_softmax_loop(const Fp8Params& p, SharedState
       l = l * alpha + ((sa0 + sa1) + (sb0 + sb1));
       if (rescale_warp) {
 #pragma unroll
-        for (int cc = 0; cc < 64; cc += 32) {
+        for (int cc = 0; cc < kOCols; cc += 32) {
           uint32_t r[32];
           tmem_ld_x32(lane_addr + colO + cc, r);
           tmem_ld_wait_x32(r);
@@ -735,9 +763,9 @@ __device__ __forceinline__ void fp8_softmax_loop(const Fp8Params& p, SharedState
     const bool store = row >= nominal0 && row < un.L && row >= 0;
     const float ofac = l > 0.f ? p.sv[bh] / l : 0.f;
     __nv_bfloat16* orow =
-        p.o + ((size_t)(store ? un.tok0 + row : 0) * p.H + un.h) * kFp8D + half * 64;
+        p.o + ((size_t)(store ? un.tok0 + row : 0) * p.H + un.h) * D + half * kOCols;
 #pragma unroll
-    for (int cc = 0; cc < 64; cc += 32) {
+    for (int cc = 0; cc < kOCols; cc += 32) {
       uint32_t r[32];
       tmem_ld_x32(lane_addr + colO + cc, r);
       tmem_ld_wait_x32(r);
@@ -762,6 +790,7 @@ __device__ __forceinline__ void fp8_softmax_loop(const Fp8Params& p, SharedState
   }
 }
 
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_vt, const Fp8Params p) {
@@ -811,10 +840,10 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   if (warp >= kSoftmaxWarps) {
     setmaxnreg_dec<kControlRegs>();
     if (warp == kProducerWarp) {
-      if (lane == 0) fp8_producer(&tm_q, &tm_k, &tm_vt, p, ss, sQ, sRing, n_units);
+      if (lane == 0) fp8_producer<D>(&tm_q, &tm_k, &tm_vt, p, ss, sQ, sRing, n_units);
     } else if (warp == kMmaWarp) {
       if (lane == 0) {
-        fp8_mma_loop(p, ss, sQ, sRing, tmem);
+        fp8_mma_loop<D>(p, ss, sQ, sRing, tmem);
         mma_commit(bar_addr(ss, kBarDrain));
         mbar_wait(bar_addr(ss, kBarDrain), 0, 100000000ull);
       }
@@ -822,7 +851,7 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __syncwarp();
   } else {
     setmaxnreg_inc<kSoftmaxRegs>();
-    fp8_softmax_loop(p, ss, tmem, warp / kGroupWarps);
+    fp8_softmax_loop<D>(p, ss, tmem, warp / kGroupWarps);
     __syncwarp();
   }
 

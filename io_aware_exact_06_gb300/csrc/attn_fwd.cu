@@ -108,12 +108,21 @@ cudaError_t set_smem_attributes() {
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 FwdCfg<128>::kSmemBytes)) != cudaSuccess)
     return e;
-  if ((e = cudaFuncSetAttribute(attn::attn_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if ((e = cudaFuncSetAttribute(attn::attn_fp8_kernel<64>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 attn::kFp8SmemBytes)) != cudaSuccess)
     return e;
-  if ((e = cudaFuncSetAttribute(attn::fp8_quant_stage1_kernel,
+  if ((e = cudaFuncSetAttribute(attn::attn_fp8_kernel<128>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                attn::kQuantSmemBytes)) != cudaSuccess)
+                                attn::kFp8SmemBytes)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(attn::fp8_quant_stage1_kernel<64>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                attn::QuantCfg<64>::kSmemBytes)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(attn::fp8_quant_stage1_kernel<128>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                attn::QuantCfg<128>::kSmemBytes)) != cudaSuccess)
     return e;
   return cudaFuncSetAttribute(attn::attn_fwd_kernel<128, attn::kModeWindow>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -786,11 +795,12 @@ int make_map_fp8_rows(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int6
   return r == CUDA_SUCCESS ? ATTN_OK : cuda_fail(cudaErrorInvalidValue);
 }
 
-// transposed e4m3 V [B*H][128][Np]: box 128 keys x 128 channels x 1.
-int make_map_fp8_vt(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int64_t bh, int64_t np) {
-  cuuint64_t dims[3] = {(cuuint64_t)np, (cuuint64_t)attn::kFp8D, (cuuint64_t)bh};
-  cuuint64_t strides[2] = {(cuuint64_t)np, (cuuint64_t)np * attn::kFp8D};
-  cuuint32_t box[3] = {(cuuint32_t)attn::kBN, (cuuint32_t)attn::kFp8D, 1};
+// transposed e4m3 V [B*H][d][Np]: box 128 keys x d channels x 1.
+int make_map_fp8_vt(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int64_t bh, int64_t np,
+                    int d) {
+  cuuint64_t dims[3] = {(cuuint64_t)np, (cuuint64_t)d, (cuuint64_t)bh};
+  cuuint64_t strides[2] = {(cuuint64_t)np, (cuuint64_t)np * d};
+  cuuint32_t box[3] = {(cuuint32_t)attn::kBN, (cuuint32_t)d, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box,
                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -800,7 +810,7 @@ int make_map_fp8_vt(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int64_
 
 int fp8_check(int B, int H, int N, int d) {
   if (B < 0 || H < 0 || N < 0) return ATTN_ERR_SHAPE;
-  if (d != attn::kFp8D) return ATTN_ERR_HEADDIM;
+  if (d != 64 && d != 128) return ATTN_ERR_HEADDIM;
   const int64_t tokens = (int64_t)B * N;
   if (tokens > INT32_MAX - 2 * attn::kBN || H > 65535 ||
       (int64_t)B * H * ((N + attn::kBN - 1) / attn::kBN) > INT32_MAX / 2)
@@ -808,10 +818,10 @@ int fp8_check(int B, int H, int N, int d) {
   return ATTN_OK;
 }
 
-attn::Fp8Signs pack_signs(const int8_t* signs) {
+attn::Fp8Signs pack_signs(const int8_t* signs, int d) {
   attn::Fp8Signs sg{};
   if (signs)
-    for (int c = 0; c < attn::kFp8D; ++c)
+    for (int c = 0; c < d; ++c)
       if (signs[c] < 0) sg.bits[c / 32] |= 1u << (c % 32);
   return sg;
 }
@@ -841,13 +851,13 @@ int fp8_worklist(int dev, attn_stream_t stream, DeviceState* ds, const int32_t* 
   return ATTN_OK;
 }
 
-// bf16 rows [tokens, H, 128] for the first quantisation stage: box 128
-// channels x 1 head x 128 rows, no swizzle (rows 256 bytes apart in shared
-// memory).
-int make_map_quant_rows(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int64_t tokens, int H) {
-  cuuint64_t dims[3] = {(cuuint64_t)attn::kFp8D, (cuuint64_t)H, (cuuint64_t)tokens};
-  cuuint64_t strides[2] = {(cuuint64_t)attn::kFp8D * 2, (cuuint64_t)H * attn::kFp8D * 2};
-  cuuint32_t box[3] = {(cuuint32_t)attn::kFp8D, 1, (cuuint32_t)attn::kBM};
+// bf16 rows [tokens, H, d] for the first quantisation stage: box d channels
+// x 1 head x 128 rows, no swizzle (rows 2 d bytes apart in shared memory).
+int make_map_quant_rows(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int64_t tokens, int H,
+                        int d) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)tokens};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
+  cuuint32_t box[3] = {(cuuint32_t)d, 1, (cuuint32_t)attn::kBM};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -861,9 +871,9 @@ int make_map_quant_rows(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, in
 // extent of the copies is B * N (packed: an upper bound of cu_seqlens[B]; no
 // copy leaves its sequence).
 int launch_quant_stage1(const void* q, const void* k, const void* v, uint8_t* q8, uint8_t* k8,
-                        float* sq, float* sk, unsigned int* amax_v, int B, int H, int N,
-                        const int8_t* signs, const int32_t* cu_seqlens, const int* num_entries,
-                        DeviceState* ds, cudaStream_t s) {
+                        float* sq, float* sk, unsigned int* amax_v, int B, int H, int N, int d,
+                        int code_stride, const int8_t* signs, const int32_t* cu_seqlens,
+                        const int* num_entries, DeviceState* ds, cudaStream_t s) {
   const int T = (N + attn::kBM - 1) / attn::kBM;
   const int nb = B * H * T;
   const int64_t tokens = (int64_t)B * N;
@@ -874,7 +884,7 @@ int launch_quant_stage1(const void* q, const void* k, const void* v, uint8_t* q8
   std::memset(maps, 0, sizeof(maps));
   const void* src[3] = {q, k, v};
   for (int i = 0; i < 3; ++i)
-    if (src[i] && (st = make_map_quant_rows(enc, &maps[i], src[i], tokens, H)) != ATTN_OK) return st;
+    if (src[i] && (st = make_map_quant_rows(enc, &maps[i], src[i], tokens, H, d)) != ATTN_OK) return st;
   cudaError_t e;
   if (v && (e = cudaMemsetAsync(amax_v, 0, (size_t)B * H * sizeof(unsigned int), s)) != cudaSuccess)
     return cuda_fail(e);
@@ -883,20 +893,29 @@ int launch_quant_stage1(const void* q, const void* k, const void* v, uint8_t* q8
   const int first = q ? 0 : (k ? 1 : 2);
   const int n_blocks = (nseg - first) * nb;
   const int grid = std::min(n_blocks, 2 * ds->sms);
-  attn::fp8_quant_stage1_kernel<<<grid, 32 * attn::kQuantWarps, attn::kQuantSmemBytes, s>>>(
-      maps[0], maps[1], maps[2], q8, k8, sq, sk, amax_v, B, H, N, T, pack_signs(signs),
-      signs ? 1 : 0, first * nb, n_blocks, cu_seqlens, num_entries, ds->err);
+  if (d == 64)
+    attn::fp8_quant_stage1_kernel<64><<<grid, 32 * attn::kQuantWarps, attn::QuantCfg<64>::kSmemBytes, s>>>(
+        maps[0], maps[1], maps[2], q8, k8, sq, sk, amax_v, B, H, N, T, pack_signs(signs, d),
+        signs ? 1 : 0, first * nb, n_blocks, cu_seqlens, num_entries, ds->err, code_stride);
+  else
+    attn::fp8_quant_stage1_kernel<128><<<grid, 32 * attn::kQuantWarps, attn::QuantCfg<128>::kSmemBytes, s>>>(
+        maps[0], maps[1], maps[2], q8, k8, sq, sk, amax_v, B, H, N, T, pack_signs(signs, d),
+        signs ? 1 : 0, first * nb, n_blocks, cu_seqlens, num_entries, ds->err, code_stride);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
   return ATTN_OK;
 }
 
 int launch_quant_v(const void* v, uint8_t* codes_t, float* scale, unsigned int* amax_bits, int B,
-                   int H, int N, const int32_t* cu_seqlens, const int* num_entries,
+                   int H, int N, int d, const int32_t* cu_seqlens, const int* num_entries,
                    cudaStream_t s) {
   const int T = (N + attn::kBN - 1) / attn::kBN;
-  attn::fp8_quant_v_kernel<<<B * H * T, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(v),
-                                                     amax_bits, scale, codes_t, B, H, N,
-                                                     T * attn::kBN, cu_seqlens, num_entries);
+  auto v16 = reinterpret_cast<const __nv_bfloat16*>(v);
+  if (d == 64)
+    attn::fp8_quant_v_kernel<64><<<B * H * T, 256, 0, s>>>(v16, amax_bits, scale, codes_t, B, H, N,
+                                                           T * attn::kBN, cu_seqlens, num_entries);
+  else
+    attn::fp8_quant_v_kernel<128><<<B * H * T, 256, 0, s>>>(v16, amax_bits, scale, codes_t, B, H, N,
+                                                            T * attn::kBN, cu_seqlens, num_entries);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
@@ -920,7 +939,7 @@ extern "C" int attn_fp8_quantize_qk(const void* x, uint8_t* codes, float* scales
   int* ws = nullptr;
   if ((st = fp8_worklist(dev, stream, ds, cu_seqlens, B, N, 0, &ws)) != ATTN_OK) return st;
   return launch_quant_stage1(x, nullptr, nullptr, codes, nullptr, scales, nullptr, nullptr, B, H, N,
-                             signs, cu_seqlens, ws, ds, reinterpret_cast<cudaStream_t>(stream));
+                             d, d, signs, cu_seqlens, ws, ds, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int attn_fp8_quantize_v(const void* v, uint8_t* codes_t, float* scale, int B, int H,
@@ -944,9 +963,9 @@ extern "C" int attn_fp8_quantize_v(const void* v, uint8_t* codes_t, float* scale
   if ((st = fp8_worklist(dev, stream, ds, cu_seqlens, B, N, 0, &list)) != ATTN_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if ((st = launch_quant_stage1(nullptr, nullptr, v, nullptr, nullptr, nullptr, nullptr, amax, B, H,
-                                N, nullptr, cu_seqlens, list, ds, s)) != ATTN_OK)
+                                N, d, d, nullptr, cu_seqlens, list, ds, s)) != ATTN_OK)
     return st;
-  return launch_quant_v(v, codes_t, scale, amax, B, H, N, cu_seqlens, list, s);
+  return launch_quant_v(v, codes_t, scale, amax, B, H, N, d, cu_seqlens, list, s);
 }
 
 extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -976,7 +995,7 @@ extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o
   // workspace: Q codes, K codes, V codes (transposed, padded), Q and K block
   // scales, V scales, V max bits; each part 256-byte aligned
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  const size_t b_q = up((size_t)tokens * H * attn::kFp8D), b_vt = up((size_t)bh * attn::kFp8D * np);
+  const size_t b_q = up((size_t)tokens * H * attn::kFp8D), b_vt = up((size_t)bh * d * np);
   const size_t b_s = up((size_t)bh * T * sizeof(float)), b_v = up((size_t)bh * sizeof(float));
   uint8_t* ws = nullptr;
   if ((st = fp8_workspace(dev, stream, 2 * b_q + b_vt + 2 * b_s + 2 * b_v + 256, &ws)) != ATTN_OK)
@@ -993,15 +1012,16 @@ extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o
   int* list = nullptr;  // [0] entries, [1, 3) unit counters, [4, ...) the packed worklist
   if ((st = fp8_worklist(dev, stream, ds, cu_seqlens, B, N, causal ? 1 : 0, &list)) != ATTN_OK)
     return st;
-  if ((st = launch_quant_stage1(q, k, v, q8, k8, sq, sk, amax, B, H, N, signs, cu_seqlens, list,
-                                ds, s)) != ATTN_OK)
+  // Q and K codes in rows of 128 bytes (d = 64: zero-padded), V codes [B*H][d][Np]
+  if ((st = launch_quant_stage1(q, k, v, q8, k8, sq, sk, amax, B, H, N, d, attn::kFp8D, signs,
+                                cu_seqlens, list, ds, s)) != ATTN_OK)
     return st;
-  if ((st = launch_quant_v(v, vt, sv, amax, B, H, N, cu_seqlens, list, s)) != ATTN_OK) return st;
+  if ((st = launch_quant_v(v, vt, sv, amax, B, H, N, d, cu_seqlens, list, s)) != ATTN_OK) return st;
 
   CUtensorMap mq, mk, mvt;
   if ((st = make_map_fp8_rows(enc, &mq, q8, tokens, H)) != ATTN_OK) return st;
   if ((st = make_map_fp8_rows(enc, &mk, k8, tokens, H)) != ATTN_OK) return st;
-  if ((st = make_map_fp8_vt(enc, &mvt, vt, bh, np)) != ATTN_OK) return st;
+  if ((st = make_map_fp8_vt(enc, &mvt, vt, bh, np, d)) != ATTN_OK) return st;
   attn::Fp8Params p{};
   p.o = reinterpret_cast<__nv_bfloat16*>(o);
   p.lse = lse;
@@ -1020,11 +1040,14 @@ extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o
   p.causal = causal ? 1 : 0;
   p.scale = scale;
   // the unnormalised rotation multiplies Q K^T by d
-  p.logit_log2 = (float)((double)scale * 1.4426950408889634 / (signs ? (double)attn::kFp8D : 1.0));
+  p.logit_log2 = (float)((double)scale * 1.4426950408889634 / (signs ? (double)d : 1.0));
   p.timeout_ns = 2000000000ull;
   const int64_t units = bh * ((N + attn::kUnitRows - 1) / attn::kUnitRows);
   const int grid = cu_seqlens ? ds->sms : (int)std::min<int64_t>(units, ds->sms);
-  attn::attn_fp8_kernel<<<grid, attn::kThreads, attn::kFp8SmemBytes, s>>>(mq, mk, mvt, p);
+  if (d == 64)
+    attn::attn_fp8_kernel<64><<<grid, attn::kThreads, attn::kFp8SmemBytes, s>>>(mq, mk, mvt, p);
+  else
+    attn::attn_fp8_kernel<128><<<grid, attn::kThreads, attn::kFp8SmemBytes, s>>>(mq, mk, mvt, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
   return ATTN_OK;
 }

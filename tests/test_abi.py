@@ -115,7 +115,8 @@ def test_backward_empty_problem_is_a_noop(lib):
 
 
 @pytest.mark.parametrize("args,status", [
-    (dict(d=64), -3),
+    (dict(d=96), -3),
+    (dict(d=256), -3),
     (dict(B=-1), -2),
     (dict(scale=-1.0), -5),
     (dict(scale=float("nan")), -5),
@@ -128,7 +129,7 @@ def test_fp8_argument_errors(lib, args, status):
     st = lib.attn_fwd_fp8(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"], a["d"],
                           a["scale"], a["causal"], None, None, None)
     assert st == status
-    assert lib.attn_fp8_quantize_qk(BUF, BUF, BUF, 1, 1, 128, 64, None, None, None) == -3
+    assert lib.attn_fp8_quantize_qk(BUF, BUF, BUF, 1, 1, 128, 32, None, None, None) == -3
     assert lib.attn_fp8_quantize_v(None, BUF, BUF, 1, 1, 128, 128, None, None) == -1
 
 

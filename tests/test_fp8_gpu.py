@@ -45,8 +45,8 @@ def dev():
     return torch.device("cuda:0")
 
 
-def signs_of(seed):
-    return np.where(inputs.splitmix64(seed, 0, 128) & np.uint64(1), -1, 1).astype(np.int8)
+def signs_of(seed, d=128):
+    return np.where(inputs.splitmix64(seed, 0, d) & np.uint64(1), -1, 1).astype(np.int8)
 
 
 def with_outliers(bits, seed, factor=20.0, nch=3):
@@ -62,39 +62,41 @@ def to_dev(dev, bits):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("N", [1, 300, 1024])
 @pytest.mark.parametrize("rotate", [False, True])
-def test_quantize_qk_bit_exact(dev, N, rotate):
+def test_quantize_qk_bit_exact(dev, N, rotate, d):
     import torch
     import io_aware_exact_06_gb300 as fa
     B, H = 2, 3
-    x = with_outliers(inputs.normal_bf16(3100 + N, B * N * H * 128).reshape(B * N, H, 128), 3101)
-    sg = signs_of(3102) if rotate else None
+    x = with_outliers(inputs.normal_bf16(3100 + N + d, B * N * H * d).reshape(B * N, H, d), 3101)
+    sg = signs_of(3102, d) if rotate else None
     T = -(-N // 128)
-    codes = torch.zeros((B * N, H, 128), dtype=torch.uint8, device=dev)
+    codes = torch.zeros((B * N, H, d), dtype=torch.uint8, device=dev)
     scales = torch.zeros((B, H, T), dtype=torch.float32, device=dev)
-    fa.attn_fp8_quantize_qk(to_dev(dev, x), codes, scales, B, H, N, 128, sg)
+    fa.attn_fp8_quantize_qk(to_dev(dev, x), codes, scales, B, H, N, d, sg)
     assert fa.attn_last_device_error() == 0
     ref_codes, ref_scales = oracle.fp8_quantize(x, B, N, 128, rotate, sg)
     assert np.array_equal(scales.cpu().numpy(), ref_scales)
     assert np.array_equal(codes.cpu().numpy(), ref_codes)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("N", [1, 300, 1024])
-def test_quantize_v_bit_exact(dev, N):
+def test_quantize_v_bit_exact(dev, N, d):
     import torch
     import io_aware_exact_06_gb300 as fa
     B, H = 2, 3
-    v = inputs.normal_bf16(3200 + N, B * N * H * 128, 1.5).reshape(B * N, H, 128)
+    v = inputs.normal_bf16(3200 + N + d, B * N * H * d, 1.5).reshape(B * N, H, d)
     Np = 128 * (-(-N // 128))
-    codes_t = torch.full((B, H, 128, Np), 0x55, dtype=torch.uint8, device=dev)
+    codes_t = torch.full((B, H, d, Np), 0x55, dtype=torch.uint8, device=dev)
     scale = torch.zeros((B, H), dtype=torch.float32, device=dev)
-    fa.attn_fp8_quantize_v(to_dev(dev, v), codes_t, scale, B, H, N, 128)
+    fa.attn_fp8_quantize_v(to_dev(dev, v), codes_t, scale, B, H, N, d)
     assert fa.attn_last_device_error() == 0
     ref_codes, ref_scale = oracle.fp8_quantize(v, B, N, 0, False)
     got = codes_t.cpu().numpy()
     assert np.array_equal(scale.cpu().numpy(), ref_scale[:, :, 0])
-    back = got[:, :, :, :N].transpose(0, 3, 1, 2).reshape(B * N, H, 128)
+    back = got[:, :, :, :N].transpose(0, 3, 1, 2).reshape(B * N, H, d)
     assert np.array_equal(back, ref_codes)
     assert not got[:, :, :, N:].any(), "padding keys are zero"
 
@@ -113,9 +115,10 @@ def dequantised(x, B, N, block_rows, rotate, sg):
 def run_fp8(dev, q, k, v, B, N, H, causal, sg, scale):
     import torch
     import io_aware_exact_06_gb300 as fa
-    o = torch.empty((B * N, H, 128), dtype=torch.bfloat16, device=dev)
+    d = q.shape[-1]
+    o = torch.empty((B * N, H, d), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    fa.attn_fwd_fp8(to_dev(dev, q), to_dev(dev, k), to_dev(dev, v), o, lse, B, H, N, 128, scale,
+    fa.attn_fwd_fp8(to_dev(dev, q), to_dev(dev, k), to_dev(dev, v), o, lse, B, H, N, d, scale,
                     causal, sg)
     assert fa.attn_last_device_error() == 0
     return o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
@@ -126,13 +129,15 @@ def errors(got_o, got_lse, ref_o, ref_lse):
     return float(rel), float(np.abs(got_lse - ref_lse).max())
 
 
-def check_case(dev, B, N, H, causal, rotate, seed, outliers, scale=128 ** -0.5):
-    q = inputs.normal_bf16(seed, B * N * H * 128).reshape(B * N, H, 128)
-    k = inputs.normal_bf16(seed + 1, B * N * H * 128).reshape(B * N, H, 128)
-    v = inputs.normal_bf16(seed + 2, B * N * H * 128).reshape(B * N, H, 128)
+def check_case(dev, B, N, H, causal, rotate, seed, outliers, scale=None, d=128):
+    if scale is None:
+        scale = d ** -0.5
+    q = inputs.normal_bf16(seed, B * N * H * d).reshape(B * N, H, d)
+    k = inputs.normal_bf16(seed + 1, B * N * H * d).reshape(B * N, H, d)
+    v = inputs.normal_bf16(seed + 2, B * N * H * d).reshape(B * N, H, d)
     if outliers:
         q, k = with_outliers(q, seed + 3), with_outliers(k, seed + 4)
-    sg = signs_of(seed + 5) if rotate else None
+    sg = signs_of(seed + 5, d) if rotate else None
     got_o, got_lse = run_fp8(dev, q, k, v, B, N, H, causal, sg, scale)
     cu = np.arange(B + 1) * N
     rows = inputs.sample_rows(cu, H, 512, seed=seed + 6)
@@ -141,24 +146,26 @@ def check_case(dev, B, N, H, causal, rotate, seed, outliers, scale=128 ** -0.5):
     qd = dequantised(q, B, N, 128, rotate, sg)
     kd = dequantised(k, B, N, 128, rotate, sg)
     vd = dequantised(v, B, N, 0, False, None)
-    ref_o, ref_l = oracle.attn_rows_f64(qd, kd, vd, cu, rows, scale / (128 if rotate else 1), causal)
+    ref_o, ref_l = oracle.attn_rows_f64(qd, kd, vd, cu, rows, scale / (d if rotate else 1), causal)
     deq = errors(go, gl, ref_o, ref_l)
     ex_o, ex_l, _ = oracle.attn_rows(q, k, v, cu, rows, scale, causal)
     exact = errors(go, gl, ex_o, ex_l)
     log = os.environ.get("PARITY_LOG")
     if log:
         with open(log, "a") as f:
-            f.write(json.dumps({"test": "fp8", "B": B, "N": N, "H": H, "causal": causal,
+            f.write(json.dumps({"test": "fp8", "B": B, "N": N, "H": H, "d": d, "causal": causal,
                                 "rotate": rotate, "outliers": outliers, "vs_dequantised": deq,
                                 "vs_exact": exact}) + "\n")
     return deq, exact
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("rotate", [False, True])
-def test_fp8_attention(dev, causal, rotate):
+def test_fp8_attention(dev, causal, rotate, d):
     for (B, N, H) in [(1, 256, 2), (2, 1000, 3)]:
-        (rel_d, lse_d), (rel_e, lse_e) = check_case(dev, B, N, H, causal, rotate, 3300 + N, False)
+        (rel_d, lse_d), (rel_e, lse_e) = check_case(dev, B, N, H, causal, rotate, 3300 + N + d,
+                                                    False, d=d)
         assert rel_d <= REL_DEQ and lse_d <= LSE_DEQ, (N, causal, rotate, rel_d, lse_d)
         assert rel_e <= REL_EXACT and lse_e <= LSE_EXACT, (N, causal, rotate, rel_e, lse_e)
 
@@ -172,7 +179,7 @@ def test_fp8_short_sequence(dev):
 @pytest.mark.parametrize("causal", [False, True])
 def test_fp8_zero_scale(dev, causal):
     # every visible key weighs 1 (256 P = 256 is exact in e4m3); masked keys 0
-    (rel_d, lse_d), (rel_e, lse_e) = check_case(dev, 2, 300, 2, causal, True, 3450, False, 0.0)
+    (rel_d, lse_d), (rel_e, lse_e) = check_case(dev, 2, 300, 2, causal, True, 3450, False, scale=0.0)
     assert rel_d <= REL_DEQ and lse_d <= LSE_DEQ
     assert rel_e <= REL_EXACT and lse_e <= LSE_EXACT
 
@@ -192,15 +199,15 @@ def test_incoherent_processing_helps_with_outliers(dev):
 PACKED_LENS = [300, 0, 1, 128, 77, 513, 256]
 
 
-def packed_inputs(seed, lens, H, scale_v=1.0, outliers=False):
+def packed_inputs(seed, lens, H, scale_v=1.0, outliers=False, d=128):
     """Packed unit-variance Q, K, V (Q with a few 20x channels when outliers)."""
     cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
     total = int(cu[-1])
-    q = inputs.normal_bf16(seed, total * H * 128).reshape(total, H, 128)
+    q = inputs.normal_bf16(seed, total * H * d).reshape(total, H, d)
     if outliers:
         q = with_outliers(q, seed + 3)
-    k = inputs.normal_bf16(seed + 1, total * H * 128).reshape(total, H, 128)
-    v = inputs.normal_bf16(seed + 2, total * H * 128, scale_v).reshape(total, H, 128)
+    k = inputs.normal_bf16(seed + 1, total * H * d).reshape(total, H, d)
+    v = inputs.normal_bf16(seed + 2, total * H * d, scale_v).reshape(total, H, d)
     return cu, q, k, v
 
 
@@ -267,22 +274,23 @@ def dequantised_packed(x, cu, block_rows, rotate, sg):
 def run_fp8_packed(dev, q, k, v, cu, N, H, causal, sg, scale):
     import torch
     import io_aware_exact_06_gb300 as fa
-    total = int(cu[-1])
-    o = torch.full((total, H, 128), 7.0, dtype=torch.bfloat16, device=dev)
+    total, d = int(cu[-1]), q.shape[-1]
+    o = torch.full((total, H, d), 7.0, dtype=torch.bfloat16, device=dev)
     lse = torch.full((H, total), 7.0, dtype=torch.float32, device=dev)
-    fa.attn_fwd_fp8(to_dev(dev, q), to_dev(dev, k), to_dev(dev, v), o, lse, len(cu) - 1, H, N, 128,
+    fa.attn_fwd_fp8(to_dev(dev, q), to_dev(dev, k), to_dev(dev, v), o, lse, len(cu) - 1, H, N, d,
                     scale, causal, sg, cu_dev(dev, cu))
     assert fa.attn_last_device_error() == 0
     return o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("rotate", [False, True])
-def test_fp8_attention_packed(dev, causal, rotate):
+def test_fp8_attention_packed(dev, causal, rotate, d):
     H, N = 2, max(PACKED_LENS)
-    cu, q, k, v = packed_inputs(3800, PACKED_LENS, H)
-    sg = signs_of(3805) if rotate else None
-    scale = 128 ** -0.5
+    cu, q, k, v = packed_inputs(3800 + d, PACKED_LENS, H, d=d)
+    sg = signs_of(3805, d) if rotate else None
+    scale = d ** -0.5
     got_o, got_lse = run_fp8_packed(dev, q, k, v, cu, N, H, causal, sg, scale)
     rows = inputs.sample_rows(cu, H, 100000, seed=3806)  # every row
     tok = cu[rows[:, 0]] + rows[:, 2]
@@ -290,14 +298,14 @@ def test_fp8_attention_packed(dev, causal, rotate):
     qd = dequantised_packed(q, cu, 128, rotate, sg)
     kd = dequantised_packed(k, cu, 128, rotate, sg)
     vd = dequantised_packed(v, cu, 0, False, None)
-    ref_o, ref_l = oracle.attn_rows_f64(qd, kd, vd, cu, rows, scale / (128 if rotate else 1), causal)
+    ref_o, ref_l = oracle.attn_rows_f64(qd, kd, vd, cu, rows, scale / (d if rotate else 1), causal)
     rel_d, lse_d = errors(go, gl, ref_o, ref_l)
     ex_o, ex_l, _ = oracle.attn_rows(q, k, v, cu, rows, scale, causal)
     rel_e, lse_e = errors(go, gl, ex_o, ex_l)
     log = os.environ.get("PARITY_LOG")
     if log:
         with open(log, "a") as f:
-            f.write(json.dumps({"test": "fp8_packed", "lens": PACKED_LENS, "H": H, "causal": causal,
+            f.write(json.dumps({"test": "fp8_packed", "lens": PACKED_LENS, "H": H, "d": d, "causal": causal,
                                 "rotate": rotate, "vs_dequantised": [rel_d, lse_d],
                                 "vs_exact": [rel_e, lse_e]}) + "\n")
     assert rel_d <= REL_DEQ and lse_d <= LSE_DEQ, (rel_d, lse_d)
