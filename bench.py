@@ -354,7 +354,7 @@ def run_cuda(args, world, rank, local):
 DECODE = {"B": 8, "H": 16, "Nq": 1, "Nk": 32768, "d": 128}
 # DRAM bytes (read + write) of one decode call (decode kernel + combine), from
 # the ncu capture summarised under profiles/ (None once either kernel changes).
-DECODE_TRAFFIC_BYTES = 2_147_573_504 + 4_097_792 + 1_271_296  # decode + combine (profiles/attn_fwd_kvsplit_decode.md)
+DECODE_TRAFFIC_BYTES = 2_147_573_504 + 4_097_792 + 1_271_296  # decode kernel read + write, combine read
 DECODE_METRIC = "split-KV decode: algorithmic HBM GB/s on 1 GB300 (bf16 K/V cache)"
 
 
@@ -760,7 +760,7 @@ BWD_TRAFFIC_BYTES = None
 # DRAM bytes (read + write) of one attn_fwd_kernel<128> launch of this
 # workload, from the ncu capture summarised under profiles/ (None until taken
 # for the current kernel).
-TRAFFIC_BYTES = 609_281_024  # 550.83 MB read + 58.45 MB written (profiles/attn_fwd_kernel_long_causal.md)
+TRAFFIC_BYTES = 609_281_024  # 550.83 MB read + 58.45 MB written
 
 
 def main():
