@@ -353,7 +353,7 @@ def run_cuda(args, world, rank, local):
 
 DECODE = {"B": 8, "H": 16, "Nq": 1, "Nk": 32768, "d": 128}
 # DRAM bytes (read + write) of one decode call (decode kernel + combine), from
-# the ncu capture summarised under profiles/ (None once either kernel changes).
+# one ncu capture of the current kernels (None once either kernel changes).
 DECODE_TRAFFIC_BYTES = 2_147_573_504 + 4_097_792 + 1_271_296  # decode kernel read + write, combine read
 DECODE_METRIC = "split-KV decode: algorithmic HBM GB/s on 1 GB300 (bf16 K/V cache)"
 
@@ -753,13 +753,14 @@ def fp8_cpu_baseline(wl, signs, budget_s: float = 10.0):
 
 
 # DRAM bytes (read + write) of one backward call on this workload (all three
-# kernels), from the ncu capture summarised under profiles/ (None until taken).
-BWD_TRAFFIC_BYTES = None
+# kernels), from one ncu capture of the current kernels (None once one of them
+# changes): prep 135.27 + 3.88 MB, dK/dV 930.22 + 102.11 MB, dQ 954.44 +
+# 46.93 MB.
+BWD_TRAFFIC_BYTES = 135_274_496 + 3_879_168 + 930_220_544 + 102_106_624 + 954_436_096 + 46_928_384
 
 
 # DRAM bytes (read + write) of one attn_fwd_kernel<128> launch of this
-# workload, from the ncu capture summarised under profiles/ (None until taken
-# for the current kernel).
+# workload, from one ncu capture of the current kernel (None once it changes).
 TRAFFIC_BYTES = 609_281_024  # 550.83 MB read + 58.45 MB written
 
 
