@@ -198,8 +198,10 @@ def cpu_baseline(wl, budget_s: float = 15.0, name=WORKLOAD):
 def exp_unit_bound(sm_mhz, d: int, per_gpu_tflops: float):
     """The exp-unit roofline: each score element costs 4*d flops of the metric
     and one exp2, so the bound is SMs * f_SM * (ex2 per clock per SM) * 4d.
-    Also the clock-based tensor peak SMs * f_SM * (MMA flop per clock per SM).
-    Rates are measured on this GPU; f_SM is the median clock of the run."""
+    Also the clock-based tensor peak SMs * f_SM * (MMA flop per clock per SM),
+    and (d = 128) the bound set by the rate at which one SM's shared memory
+    and TMEM feed its tensor core in the kernel's operand forms.  Rates are
+    measured on this GPU; f_SM is the median clock of the run."""
     try:
         from io_aware_exact_06_gb300 import unit_rates
         r = unit_rates.measure()
@@ -208,12 +210,27 @@ def exp_unit_bound(sm_mhz, d: int, per_gpu_tflops: float):
     f = (sm_mhz or r["max_clock_mhz"]) * 1e6
     exp_tf = r["sm_count"] * f * r["ex2_per_clk_per_sm"] * 4 * d / 1e12
     mma_tf = r["sm_count"] * f * r["mma_bf16_flop_per_clk_per_sm"] / 1e12
-    return {"ex2_per_clk_per_sm": r["ex2_per_clk_per_sm"],
-            "mma_flop_per_clk_per_sm": r["mma_bf16_flop_per_clk_per_sm"],
-            "sm_count": r["sm_count"], "sm_mhz": f / 1e6,
-            "exp_bound_tflops": exp_tf, "frac_of_exp_bound": per_gpu_tflops / exp_tf,
-            "tensor_peak_at_clock_tflops": mma_tf,
-            "frac_of_tensor_peak_at_clock": per_gpu_tflops / mma_tf}
+    out = {"ex2_per_clk_per_sm": r["ex2_per_clk_per_sm"],
+           "mma_flop_per_clk_per_sm": r["mma_bf16_flop_per_clk_per_sm"],
+           "sm_count": r["sm_count"], "sm_mhz": f / 1e6,
+           "exp_bound_tflops": exp_tf, "frac_of_exp_bound": per_gpu_tflops / exp_tf,
+           "tensor_peak_at_clock_tflops": mma_tf,
+           "frac_of_tensor_peak_at_clock": per_gpu_tflops / mma_tf}
+    if d == 128 and "ksteps_ss_kmajor" in r:
+        # The tensor core fed by one SM's shared memory: a 128x128 tile pair
+        # costs S = Q K^T (both operands from shared memory) plus O += P V (P
+        # from TMEM while the softmax warps use TMEM too), each at the rate the
+        # probe measures for products stepping through a tile's k-slices.
+        # Flops of the products issued (diagonal tiles in full), so for causal
+        # the fraction understates the kernel's share of this bound.
+        tile = 2.0 * 128 * 128 * d
+        cyc = tile / r["ksteps_ss_kmajor"] + tile / r["ksteps_ts_b_mnmajor_tmem_traffic"]
+        op_tf = r["sm_count"] * f * 2 * tile / cyc / 1e12
+        out.update({"ksteps_ss_flop_per_clk_per_sm": r["ksteps_ss_kmajor"],
+                    "ksteps_ts_tmem_traffic_flop_per_clk_per_sm": r["ksteps_ts_b_mnmajor_tmem_traffic"],
+                    "operand_rate_bound_tflops": op_tf,
+                    "frac_of_operand_rate_bound": per_gpu_tflops / op_tf})
+    return out
 
 
 def run_reference(args, world, rank):
@@ -754,9 +771,8 @@ def fp8_cpu_baseline(wl, signs, budget_s: float = 10.0):
 
 # DRAM bytes (read + write) of one backward call on this workload (all three
 # kernels), from one ncu capture of the current kernels (None once one of them
-# changes): prep 135.27 + 3.88 MB, dK/dV 930.22 + 102.11 MB, dQ 954.44 +
-# 46.93 MB.
-BWD_TRAFFIC_BYTES = 135_274_496 + 3_879_168 + 930_220_544 + 102_106_624 + 954_436_096 + 46_928_384
+# changes).
+BWD_TRAFFIC_BYTES = None
 
 
 # DRAM bytes (read + write) of one attn_fwd_kernel<128> launch of this

@@ -118,13 +118,25 @@ template <int D>
 struct BwdCfg {
   static_assert(D == 64 || D == 128, "head dim 64 or 128");
   static constexpr int kTileBytes = (D / 64) * kChunkBytes;  // one 128 x D bf16 tile
-  static constexpr int kStages = D == 128 ? 2 : 4;
-  // dK/dV kernel: K, V resident; stages of (Q, dO, LSE*log2e, D)
-  static constexpr int kKvStageBytes = 2 * kTileBytes + 1024;
-  static constexpr int kKvSmemBytes = 2 * kTileBytes + kStages * kKvStageBytes + 1024;
-  // dQ kernel: Q, dO resident; stages of (K, V)
-  static constexpr int kQStageBytes = 2 * kTileBytes;
-  static constexpr int kQSmemBytes = 2 * kTileBytes + kStages * kQStageBytes + 1024;
+  // Each kernel streams two rings with their own full / empty barriers, so
+  // that a slot is refilled as soon as its own last product is done:
+  //   dK/dV kernel: ring A = (Q, LSE*log2e, D) slots, last read by dK += dS^T Q;
+  //                 ring B = dO slots, last read by dV += P^T dO (earlier);
+  //   dQ kernel:    ring A = K slots, last read by dQ += dS K;
+  //                 ring B = V slots, last read by dP = dO V^T (earlier).
+  // Ring A feeds the first product of a tile (S^T or S), so its refill
+  // latency is on the critical path; the dQ kernel gets a third K slot at
+  // D = 128 (225 KB in all, within the 227 KB a CTA may have).
+  static constexpr int kKvASlots = D == 128 ? 2 : 4;
+  static constexpr int kKvBSlots = D == 128 ? 2 : 4;
+  static constexpr int kKvASlotBytes = kTileBytes + 1024;
+  static constexpr int kKvSmemBytes =
+      2 * kTileBytes + kKvASlots * kKvASlotBytes + kKvBSlots * kTileBytes + 1024;
+  static constexpr int kQASlots = D == 128 ? 3 : 4;
+  static constexpr int kQBSlots = D == 128 ? 2 : 4;
+  static constexpr int kQSmemBytes = 2 * kTileBytes + (kQASlots + kQBSlots) * kTileBytes + 1024;
+  static_assert(kKvASlots <= 4 && kKvBSlots <= 4 && kQASlots <= 4 && kQBSlots <= 4, "barrier slots");
+  static_assert(kKvSmemBytes <= 232448 && kQSmemBytes <= 232448, "shared memory per CTA");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kIdescS = make_idesc_bf16(kTile, kTile, false);
   static constexpr uint32_t kIdescAcc = make_idesc_bf16(kTile, D, true);
@@ -231,10 +243,13 @@ enum : int {
   kBarAccFull = 11,   // the unit's accumulators are complete
   kBarAccEmpty = 12,  // the compute warps have read them
   kBarDrain = 13,
-  kBarStage = 14,     // full[s] = kBarStage + s, empty[s] = kBarStage + 4 + s
-  kBarQTmemFull = 22, // dQ kernel: the unit's Q and dO are in TMEM
-  kBarQTmemEmpty = 23,// dQ kernel: the unit's products no longer read them
-  kMaxBars = 24,
+  kBarAFull = 14,     // ring A slot s loaded: kBarAFull + s
+  kBarAEmpty = 18,    // ring A slot s free: kBarAEmpty + s
+  kBarBFull = 22,     // ring B likewise
+  kBarBEmpty = 26,
+  kBarQTmemFull = 30, // dQ kernel: the unit's Q and dO are in TMEM
+  kBarQTmemEmpty = 31,// dQ kernel: the unit's products no longer read them
+  kMaxBars = 32,
 };
 
 struct Shared {
@@ -544,9 +559,9 @@ template <int D>
 __device__ __forceinline__ void kv_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                             const CUtensorMap* tm_v, const CUtensorMap* tm_do,
                                             const BwdParams& p, Shared& ss, uint8_t* sK,
-                                            uint8_t* sV, uint8_t* sStage, int n_units) {
+                                            uint8_t* sV, uint8_t* sA, uint8_t* sB, int n_units) {
   using C = BwdCfg<D>;
-  uint32_t ring = 0, uslot = 0;
+  uint32_t ringA = 0, ringB = 0, uslot = 0;
   int units_done = 0;
   int u = blockIdx.x;
   for (;;) {
@@ -562,21 +577,32 @@ __device__ __forceinline__ void kv_producer(const CUtensorMap* tm_q, const CUten
       tma_load_3d(smem_u32(sV + c * kChunkBytes), tm_v, bar_addr(ss, kBarResFull), c * 64, un.h, k0);
     }
     for (int i = un.o0; i < un.o0 + un.n; ++i) {
-      const int slot = ring % C::kStages;
-      const uint32_t n = ring / C::kStages;
-      if (n > 0 && !wait_bar(ss, kBarStage + 4 + slot, (n - 1) & 1, p, 103)) return;
-      const uint32_t full = bar_addr(ss, kBarStage + slot);
-      uint8_t* st = sStage + slot * C::kKvStageBytes;
-      mbar_arrive_expect_tx(full, C::kKvStageBytes);
       const int q0 = un.tok0 + tile_start(i, un.L);
-      for (int c = 0; c < D / 64; ++c) {
-        tma_load_3d(smem_u32(st + c * kChunkBytes), tm_q, full, c * 64, un.h, q0);
-        tma_load_3d(smem_u32(st + C::kTileBytes + c * kChunkBytes), tm_do, full, c * 64, un.h, q0);
+      {  // dO (ring B: its slot is free first, after the dV product)
+        const int slot = ringB % C::kKvBSlots;
+        const uint32_t n = ringB / C::kKvBSlots;
+        if (n > 0 && !wait_bar(ss, kBarBEmpty + slot, (n - 1) & 1, p, 106)) return;
+        const uint32_t full = bar_addr(ss, kBarBFull + slot);
+        uint8_t* st = sB + slot * C::kTileBytes;
+        mbar_arrive_expect_tx(full, C::kTileBytes);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem_u32(st + c * kChunkBytes), tm_do, full, c * 64, un.h, q0);
+        ++ringB;
       }
-      const size_t vec = vec_index(p, un, i);
-      bulk_load(smem_u32(st + 2 * C::kTileBytes), p.lse2 + vec, 512, full);
-      bulk_load(smem_u32(st + 2 * C::kTileBytes + 512), p.dd + vec, 512, full);
-      ++ring;
+      {  // Q, LSE*log2e, D (ring A: free after the dK product)
+        const int slot = ringA % C::kKvASlots;
+        const uint32_t n = ringA / C::kKvASlots;
+        if (n > 0 && !wait_bar(ss, kBarAEmpty + slot, (n - 1) & 1, p, 103)) return;
+        const uint32_t full = bar_addr(ss, kBarAFull + slot);
+        uint8_t* st = sA + slot * C::kKvASlotBytes;
+        mbar_arrive_expect_tx(full, C::kKvASlotBytes);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem_u32(st + c * kChunkBytes), tm_q, full, c * 64, un.h, q0);
+        const size_t vec = vec_index(p, un, i);
+        bulk_load(smem_u32(st + C::kTileBytes), p.lse2 + vec, 512, full);
+        bulk_load(smem_u32(st + C::kTileBytes + 512), p.dd + vec, 512, full);
+        ++ringA;
+      }
     }
     ++units_done;
     u = next_u;
@@ -585,14 +611,17 @@ __device__ __forceinline__ void kv_producer(const CUtensorMap* tm_q, const CUten
 
 template <int D>
 __device__ __forceinline__ void kv_mma(const BwdParams& p, Shared& ss, uint8_t* sK, uint8_t* sV,
-                                       uint8_t* sStage, uint32_t tmem) {
+                                       uint8_t* sA, uint8_t* sB, uint32_t tmem) {
   using C = BwdCfg<D>;
   constexpr uint32_t kColDV = 0, kColDK = D, kColS = 2 * D, kColDP = 2 * D + 128;
   const uint32_t k_smem = smem_u32(sK), v_smem = smem_u32(sV);
-  auto q_smem = [&](uint32_t pos) { return smem_u32(sStage + (pos % C::kStages) * C::kKvStageBytes); };
-  auto do_smem = [&](uint32_t pos) { return q_smem(pos) + C::kTileBytes; };
-  auto stage_full = [&](uint32_t pos) {
-    return wait_bar(ss, kBarStage + pos % C::kStages, (pos / C::kStages) & 1, p, 110);
+  auto q_smem = [&](uint32_t pos) { return smem_u32(sA + (pos % C::kKvASlots) * C::kKvASlotBytes); };
+  auto do_smem = [&](uint32_t pos) { return smem_u32(sB + (pos % C::kKvBSlots) * C::kTileBytes); };
+  auto a_full = [&](uint32_t pos) {
+    return wait_bar(ss, kBarAFull + pos % C::kKvASlots, (pos / C::kKvASlots) & 1, p, 110);
+  };
+  auto b_full = [&](uint32_t pos) {
+    return wait_bar(ss, kBarBFull + pos % C::kKvBSlots, (pos / C::kKvBSlots) & 1, p, 115);
   };
   uint32_t ring = 0, uslot = 0, pcount = 0, dscount = 0;
   int units_done = 0;
@@ -601,10 +630,12 @@ __device__ __forceinline__ void kv_mma(const BwdParams& p, Shared& ss, uint8_t* 
     if (!next_unit(ss, p, uslot, false, u) || u < 0) return;
     const Unit un = kv_unit(p, u);
     if (!wait_bar(ss, kBarResFull, units_done & 1, p, 111)) return;
-    if (!stage_full(ring)) return;
+    if (!a_full(ring)) return;
     tc_fence_after();
     mma_rows_rows<D>(tmem + kColS, k_smem, q_smem(ring));     // S^T = K Q^T
     mma_commit(bar_addr(ss, kBarSFull));
+    if (!b_full(ring)) return;
+    tc_fence_after();
     mma_rows_rows<D>(tmem + kColDP, v_smem, do_smem(ring));   // dP^T = V dO^T
     mma_commit(bar_addr(ss, kBarDPFull));
     for (int i = 0; i < un.n; ++i) {
@@ -615,8 +646,9 @@ __device__ __forceinline__ void kv_mma(const BwdParams& p, Shared& ss, uint8_t* 
         return;
       tc_fence_after();
       mma_tmem_rows<D>(tmem + kColDV, tmem + kColS, do_smem(pos), i > 0);   // dV += P^T dO
+      mma_commit(bar_addr(ss, kBarBEmpty + pos % C::kKvBSlots));            // dO slot free
       if (more) {
-        if (!stage_full(pos + 1)) return;
+        if (!a_full(pos + 1)) return;
         tc_fence_after();
         mma_rows_rows<D>(tmem + kColS, k_smem, q_smem(pos + 1));
         mma_commit(bar_addr(ss, kBarSFull));
@@ -624,8 +656,10 @@ __device__ __forceinline__ void kv_mma(const BwdParams& p, Shared& ss, uint8_t* 
       if (!wait_bar(ss, kBarDSFull, dscount++ & 1, p, 114)) return;
       tc_fence_after();
       mma_tmem_rows<D>(tmem + kColDK, tmem + kColDP, q_smem(pos), i > 0);   // dK += dS^T Q
-      mma_commit(bar_addr(ss, kBarStage + 4 + pos % C::kStages));           // stage free
+      mma_commit(bar_addr(ss, kBarAEmpty + pos % C::kKvASlots));            // Q slot free
       if (more) {
+        if (!b_full(pos + 1)) return;
+        tc_fence_after();
         mma_rows_rows<D>(tmem + kColDP, v_smem, do_smem(pos + 1));
         mma_commit(bar_addr(ss, kBarDPFull));
       }
@@ -638,7 +672,7 @@ __device__ __forceinline__ void kv_mma(const BwdParams& p, Shared& ss, uint8_t* 
 }
 
 template <int D>
-__device__ __forceinline__ void kv_compute(const BwdParams& p, Shared& ss, uint8_t* sStage,
+__device__ __forceinline__ void kv_compute(const BwdParams& p, Shared& ss, uint8_t* sA,
                                            uint32_t tmem) {
   using C = BwdCfg<D>;
   constexpr uint32_t kColDV = 0, kColDK = D, kColS = 2 * D, kColDP = 2 * D + 128;
@@ -658,12 +692,12 @@ __device__ __forceinline__ void kv_compute(const BwdParams& p, Shared& ss, uint8
     const int key = ks + kr;
     for (int i = 0; i < un.n; ++i) {
       const uint32_t pos = ring + i;
-      const float* sl = reinterpret_cast<const float*>(sStage + (pos % C::kStages) * C::kKvStageBytes +
-                                                       2 * C::kTileBytes);
+      const float* sl = reinterpret_cast<const float*>(sA + (pos % C::kKvASlots) * C::kKvASlotBytes +
+                                                       C::kTileBytes);
       const int q0 = tile_start(un.o0 + i, un.L) + 32 * cg;  // query of this warp's column 0
-      // the stage's LSE and D vectors are read below: wait for its copies too
-      if (!__all_sync(0xffffffffu, wait_bar(ss, kBarStage + pos % C::kStages,
-                                            (pos / C::kStages) & 1, p, 123)))
+      // the slot's LSE and D vectors are read below: wait for its copies too
+      if (!__all_sync(0xffffffffu, wait_bar(ss, kBarAFull + pos % C::kKvASlots,
+                                            (pos / C::kKvASlots) & 1, p, 123)))
         return;
       if (!__all_sync(0xffffffffu, wait_bar(ss, kBarSFull, scount & 1, p, 120))) return;
       tc_fence_after();
@@ -763,9 +797,9 @@ template <int D>
 __device__ __forceinline__ void q_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                            const CUtensorMap* tm_v, const CUtensorMap* tm_do,
                                            const BwdParams& p, Shared& ss, uint8_t* sQ,
-                                           uint8_t* sDO, uint8_t* sStage, int n_units) {
+                                           uint8_t* sDO, uint8_t* sA, uint8_t* sB, int n_units) {
   using C = BwdCfg<D>;
-  uint32_t ring = 0, uslot = 0;
+  uint32_t ringA = 0, ringB = 0, uslot = 0;
   int units_done = 0;
   int u = blockIdx.x;
   for (;;) {
@@ -781,18 +815,29 @@ __device__ __forceinline__ void q_producer(const CUtensorMap* tm_q, const CUtens
       tma_load_3d(smem_u32(sDO + c * kChunkBytes), tm_do, bar_addr(ss, kBarResFull), c * 64, un.h, q0);
     }
     for (int j = un.o0; j < un.o0 + un.n; ++j) {
-      const int slot = ring % C::kStages;
-      const uint32_t n = ring / C::kStages;
-      if (n > 0 && !wait_bar(ss, kBarStage + 4 + slot, (n - 1) & 1, p, 105)) return;
-      const uint32_t full = bar_addr(ss, kBarStage + slot);
-      uint8_t* st = sStage + slot * C::kQStageBytes;
-      mbar_arrive_expect_tx(full, C::kQStageBytes);
       const int k0 = un.tok0 + tile_start(j, un.L);
-      for (int c = 0; c < D / 64; ++c) {
-        tma_load_3d(smem_u32(st + c * kChunkBytes), tm_k, full, c * 64, un.h, k0);
-        tma_load_3d(smem_u32(st + C::kTileBytes + c * kChunkBytes), tm_v, full, c * 64, un.h, k0);
+      {  // K (ring A)
+        const int slot = ringA % C::kQASlots;
+        const uint32_t n = ringA / C::kQASlots;
+        if (n > 0 && !wait_bar(ss, kBarAEmpty + slot, (n - 1) & 1, p, 105)) return;
+        const uint32_t full = bar_addr(ss, kBarAFull + slot);
+        uint8_t* st = sA + slot * C::kTileBytes;
+        mbar_arrive_expect_tx(full, C::kTileBytes);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem_u32(st + c * kChunkBytes), tm_k, full, c * 64, un.h, k0);
+        ++ringA;
       }
-      ++ring;
+      {  // V (ring B)
+        const int slot = ringB % C::kQBSlots;
+        const uint32_t n = ringB / C::kQBSlots;
+        if (n > 0 && !wait_bar(ss, kBarBEmpty + slot, (n - 1) & 1, p, 107)) return;
+        const uint32_t full = bar_addr(ss, kBarBFull + slot);
+        uint8_t* st = sB + slot * C::kTileBytes;
+        mbar_arrive_expect_tx(full, C::kTileBytes);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem_u32(st + c * kChunkBytes), tm_v, full, c * 64, un.h, k0);
+        ++ringB;
+      }
     }
     ++units_done;
     u = next_u;
@@ -800,14 +845,33 @@ __device__ __forceinline__ void q_producer(const CUtensorMap* tm_q, const CUtens
 }
 
 template <int D>
-__device__ __forceinline__ void q_mma(const BwdParams& p, Shared& ss, uint8_t* sQ, uint8_t* sDO,
-                                      uint8_t* sStage, uint32_t tmem) {
+__device__ __forceinline__ void q_mma(const BwdParams& p, Shared& ss, uint8_t* sA, uint8_t* sB,
+                                      uint32_t tmem) {
   using C = BwdCfg<D>;
   constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColQ = 256 + D, kColDO = 256 + D + D / 2;
-  auto k_smem = [&](uint32_t pos) { return smem_u32(sStage + (pos % C::kStages) * C::kQStageBytes); };
-  auto v_smem = [&](uint32_t pos) { return k_smem(pos) + C::kTileBytes; };
-  auto stage_full = [&](uint32_t pos) {
-    return wait_bar(ss, kBarStage + pos % C::kStages, (pos / C::kStages) & 1, p, 140);
+  auto k_smem = [&](uint32_t pos) { return smem_u32(sA + (pos % C::kQASlots) * C::kTileBytes); };
+  auto v_smem = [&](uint32_t pos) { return smem_u32(sB + (pos % C::kQBSlots) * C::kTileBytes); };
+  auto a_full = [&](uint32_t pos) {
+    return wait_bar(ss, kBarAFull + pos % C::kQASlots, (pos / C::kQASlots) & 1, p, 140);
+  };
+  auto b_full = [&](uint32_t pos) {
+    return wait_bar(ss, kBarBFull + pos % C::kQBSlots, (pos / C::kQBSlots) & 1, p, 145);
+  };
+  // dP of tile j (V's slot is free once it is done)
+  auto issue_dp = [&](uint32_t pos) {
+    if (!b_full(pos)) return false;
+    tc_fence_after();
+    mma_cols_rows<D>(tmem + kColDP, tmem + kColDO, v_smem(pos));   // dP = dO V^T
+    mma_commit(bar_addr(ss, kBarDPFull));
+    mma_commit(bar_addr(ss, kBarBEmpty + pos % C::kQBSlots));
+    return true;
+  };
+  auto issue_s = [&](uint32_t pos) {
+    if (!a_full(pos)) return false;
+    tc_fence_after();
+    mma_cols_rows<D>(tmem + kColS, tmem + kColQ, k_smem(pos));     // S = Q K^T
+    mma_commit(bar_addr(ss, kBarSFull));
+    return true;
   };
   uint32_t ring = 0, uslot = 0, scons = 0, dscount = 0;
   int units_done = 0;
@@ -817,32 +881,25 @@ __device__ __forceinline__ void q_mma(const BwdParams& p, Shared& ss, uint8_t* s
     const Unit un = q_unit(p, u);
     // Q and dO of the unit, copied into TMEM by the compute warps
     if (!wait_bar(ss, kBarQTmemFull, units_done & 1, p, 141)) return;
-    if (!stage_full(ring)) return;
-    tc_fence_after();
-    mma_cols_rows<D>(tmem + kColS, tmem + kColQ, k_smem(ring));     // S = Q K^T
-    mma_commit(bar_addr(ss, kBarSFull));
-    mma_cols_rows<D>(tmem + kColDP, tmem + kColDO, v_smem(ring));   // dP = dO V^T
-    mma_commit(bar_addr(ss, kBarDPFull));
+    // Product order per tile j: dQ(j), dP(j+1), then S(j+2) (S(j+1) was
+    // issued one tile earlier), so the compute warps find S and dP of the next
+    // tile ready and the K slot of tile j+2 has had a whole tile to arrive.
+    // S is overwritten only after every compute warp has read it (SCons).
+    if (!issue_s(ring) || !issue_dp(ring)) return;
+    if (!wait_bar(ss, kBarSCons, scons++ & 1, p, 142)) return;
+    if (un.n > 1 && !issue_s(ring + 1)) return;
     for (int j = 0; j < un.n; ++j) {
       const uint32_t pos = ring + j;
-      const bool more = j + 1 < un.n;
-      // S may be overwritten once every compute warp has read it
-      if (!wait_bar(ss, kBarSCons, scons++ & 1, p, 142)) return;
-      if (more) {
-        if (!stage_full(pos + 1)) return;
-        tc_fence_after();
-        mma_cols_rows<D>(tmem + kColS, tmem + kColQ, k_smem(pos + 1));
-        mma_commit(bar_addr(ss, kBarSFull));
-      }
       if (!wait_bar(ss, kBarDSFull, dscount++ & 1, p, 143)) return;
       if (j == 0 && units_done > 0 && !wait_bar(ss, kBarAccEmpty, (units_done - 1) & 1, p, 144))
         return;
       tc_fence_after();
       mma_tmem_rows<D>(tmem + kColDQ, tmem + kColDP, k_smem(pos), j > 0);   // dQ += dS K
-      mma_commit(bar_addr(ss, kBarStage + 4 + pos % C::kStages));
-      if (more) {
-        mma_cols_rows<D>(tmem + kColDP, tmem + kColDO, v_smem(pos + 1));
-        mma_commit(bar_addr(ss, kBarDPFull));
+      mma_commit(bar_addr(ss, kBarAEmpty + pos % C::kQASlots));               // K slot free
+      if (j + 1 < un.n) {
+        if (!issue_dp(pos + 1)) return;
+        if (!wait_bar(ss, kBarSCons, scons++ & 1, p, 146)) return;
+        if (j + 2 < un.n && !issue_s(pos + 2)) return;
       }
     }
     ring += un.n;
@@ -976,7 +1033,8 @@ bwd_tile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sRes0 = smem;                     // K (dK/dV kernel) or Q (dQ kernel)
   uint8_t* sRes1 = smem + C::kTileBytes;     // V or dO
-  uint8_t* sStage = smem + 2 * C::kTileBytes;
+  uint8_t* sA = smem + 2 * C::kTileBytes;    // ring A, then ring B
+  uint8_t* sB = sA + (kKv ? C::kKvASlots * C::kKvASlotBytes : C::kQASlots * C::kTileBytes);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int n_units = total_tiles(p) * p.H;
 
@@ -1000,8 +1058,10 @@ bwd_tile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     mbar_init(bar_addr(ss, kBarAccEmpty), kComputeWarps);
     mbar_init(bar_addr(ss, kBarDrain), 1);
     for (int s = 0; s < 4; ++s) {
-      mbar_init(bar_addr(ss, kBarStage + s), 1);
-      mbar_init(bar_addr(ss, kBarStage + 4 + s), 1);
+      mbar_init(bar_addr(ss, kBarAFull + s), 1);
+      mbar_init(bar_addr(ss, kBarAEmpty + s), 1);
+      mbar_init(bar_addr(ss, kBarBFull + s), 1);
+      mbar_init(bar_addr(ss, kBarBEmpty + s), 1);
     }
     ss.abort_flag = 0;
     attn::fence_mbar_init();
@@ -1026,16 +1086,16 @@ bwd_tile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (warp == kProducerWarp) {
       if (lane == 0) {
         if (kKv)
-          kv_producer<D>(&tm_q, &tm_k, &tm_v, &tm_do, p, ss, sRes0, sRes1, sStage, n_units);
+          kv_producer<D>(&tm_q, &tm_k, &tm_v, &tm_do, p, ss, sRes0, sRes1, sA, sB, n_units);
         else
-          q_producer<D>(&tm_q, &tm_k, &tm_v, &tm_do, p, ss, sRes0, sRes1, sStage, n_units);
+          q_producer<D>(&tm_q, &tm_k, &tm_v, &tm_do, p, ss, sRes0, sRes1, sA, sB, n_units);
       }
     } else if (warp == kMmaWarp) {
       if (lane == 0) {
         if (kKv)
-          kv_mma<D>(p, ss, sRes0, sRes1, sStage, tmem);
+          kv_mma<D>(p, ss, sRes0, sRes1, sA, sB, tmem);
         else
-          q_mma<D>(p, ss, sRes0, sRes1, sStage, tmem);
+          q_mma<D>(p, ss, sA, sB, tmem);
         // every MMA issued by this thread has finished before TMEM is freed
         mma_commit(bar_addr(ss, kBarDrain));
         mbar_wait(bar_addr(ss, kBarDrain), 0, 100000000ull);
@@ -1045,7 +1105,7 @@ bwd_tile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   } else {
     setmaxnreg_inc<kComputeRegs>();
     if (kKv)
-      kv_compute<D>(p, ss, sStage, tmem);
+      kv_compute<D>(p, ss, sA, tmem);
     else
       q_compute<D>(p, ss, sRes0, sRes1, tmem);
     __syncwarp();

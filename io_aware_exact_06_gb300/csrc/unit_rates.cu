@@ -87,6 +87,74 @@ __global__ void __launch_bounds__(128, 1) mma_rate(long long* cycles, int n, int
   }
 }
 
+// The operand forms of the attention kernels, 128 x 128 x 16 products cycling
+// through the eight k-steps of a 128 x 128 tile as those kernels do: A from
+// shared memory (ts = 0, K-major) or from TMEM (ts = 1); B K-major (bmn = 0:
+// S = Q K^T) or MN-major (bmn = 1: P V, dS K, P^T dO, dS^T Q).  With
+// contend = 1, warps 4-7 load and store TMEM columns the products do not use,
+// back to back, while warp 0 issues (the softmax and gradient warps' traffic).
+__global__ void __launch_bounds__(256, 1) mma_form_rate(long long* cycles, int n, int ts, int bmn,
+                                                        int contend, int* err) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tmem_base;
+  const int tid = threadIdx.x, warp = tid / 32;
+  for (int i = tid; i < 65536 / 4; i += 256) reinterpret_cast<uint32_t*>(smem)[i] = 0;
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&tmem_base), 512);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  if (tid == 0) {
+    const uint32_t id = make_idesc_bf16(128, 128, bmn != 0);
+    const uint64_t a0 = make_sdesc(smem_u32(smem), 16, 1024, kSwizzle128B);
+    const uint64_t b0 = bmn ? make_sdesc(smem_u32(smem + 32768), 16384, 1024, kSwizzle128B)
+                            : make_sdesc(smem_u32(smem + 32768), 16, 1024, kSwizzle128B);
+    const long long t0 = clock64();
+    for (int i = 0; i < n; ++i) {
+      const int kk = i % 8;
+      const uint64_t koff = (uint64_t)(((kk / 4) * 16384 + (kk % 4) * 32) >> 4);
+      const uint64_t boff = bmn ? (uint64_t)((kk * 2048) >> 4) : koff;
+      if (ts)
+        mma_ts(tmem, tmem + 256 + 8 * kk, b0 + boff, id, i > 0);
+      else
+        mma_ss(tmem, a0 + koff, b0 + boff, id, i > 0);
+    }
+    mma_commit(smem_u32(&bar));
+    if (!mbar_wait(smem_u32(&bar), 0, 1000000000ull)) atomicOr(err, 1);
+    cycles[blockIdx.x] = clock64() - t0;
+  } else if (contend && warp >= 4) {
+    // bounded: a fixed number of load / store pairs (longer than the products)
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp % 4)) << 16);
+    uint32_t r[32];
+    for (int it = 0; it < 4 * n; ++it) {
+      tmem_ld_x32(lane_addr + 384, r);
+      tmem_ld_wait_x32(r);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) r[i] += 1u;
+      tmem_st_x32(lane_addr + 416, r);
+      tmem_st_wait();
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 bool check(cudaError_t e, const char* what) {
   if (e != cudaSuccess) {
     printf("{\"error\": \"%s: %s\"}\n", what, cudaGetErrorString(e));
@@ -137,12 +205,28 @@ int main() {
     for (long long c : h) mean += (double)c / sms;
     rate[s] = 2.0 * 128 * shapes[s][0] * 16 * n / mean;
   }
+  // the attention kernels' operand forms: {ts, bmn, contend}
+  cudaFuncSetAttribute(mma_form_rate, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const int forms[6][3] = {{0, 0, 0}, {1, 0, 0}, {0, 1, 0}, {1, 1, 0}, {1, 0, 1}, {1, 1, 1}};
+  double form_rate[6];
+  for (int s = 0; s < 6; ++s) {
+    mma_form_rate<<<sms, 256, smem>>>(cyc, 64, forms[s][0], forms[s][1], forms[s][2], err);
+    mma_form_rate<<<sms, 256, smem>>>(cyc, n, forms[s][0], forms[s][1], forms[s][2], err);
+    if (!check(cudaDeviceSynchronize(), "mma_form_rate")) return 1;
+    cudaMemcpy(h.data(), cyc, sms * sizeof(long long), cudaMemcpyDeviceToHost);
+    mean = 0;
+    for (long long c : h) mean += (double)c / sms;
+    form_rate[s] = 2.0 * 128 * 128 * 16 * n / mean;
+  }
   int herr = 0;
   cudaMemcpy(&herr, err, sizeof(int), cudaMemcpyDeviceToHost);
   printf("{\"sm_count\": %d, \"sm\": \"%d.%d\", \"max_clock_mhz\": %.0f, \"ex2_per_clk_per_sm\": %.2f, "
          "\"mma_bf16_flop_per_clk_per_sm\": %.1f, \"mma_ss_n128\": %.1f, \"mma_ss_n64\": %.1f, "
-         "\"mma_ts_n128\": %.1f, \"mma_ts_n64\": %.1f, \"mma_wait_error\": %d}\n",
+         "\"mma_ts_n128\": %.1f, \"mma_ts_n64\": %.1f, \"ksteps_ss_kmajor\": %.1f, "
+         "\"ksteps_ts_kmajor\": %.1f, \"ksteps_ss_b_mnmajor\": %.1f, \"ksteps_ts_b_mnmajor\": %.1f, "
+         "\"ksteps_ts_kmajor_tmem_traffic\": %.1f, \"ksteps_ts_b_mnmajor_tmem_traffic\": %.1f, "
+         "\"mma_wait_error\": %d}\n",
          sms, major, minor, clk_khz / 1000.0, ex2_per_clk, rate[0], rate[1], rate[2], rate[3], rate[4],
-         herr);
+         form_rate[0], form_rate[1], form_rate[2], form_rate[3], form_rate[4], form_rate[5], herr);
   return herr ? 2 : 0;
 }

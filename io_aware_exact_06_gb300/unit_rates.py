@@ -2,7 +2,9 @@
 
 Builds ``csrc/unit_rates.cu`` (a standalone sm_103a program) into _build/ and
 runs it; returns its JSON: SM count, ex2 results per clock per SM, bf16 MMA
-flops per clock per SM.  Used for the exp-unit roofline of the forward pass.
+flops per clock per SM at a fixed operand address and (``ksteps_*``) for
+products stepping through a tile's k-slices in the attention kernels' operand
+forms.  Used for the exp-unit and operand-rate rooflines of the forward pass.
 
     python -m io_aware_exact_06_gb300.unit_rates
 """
