@@ -118,24 +118,21 @@ template <int D>
 struct BwdCfg {
   static_assert(D == 64 || D == 128, "head dim 64 or 128");
   static constexpr int kTileBytes = (D / 64) * kChunkBytes;  // one 128 x D bf16 tile
-  // Each kernel streams two rings with their own full / empty barriers, so
-  // that a slot is refilled as soon as its own last product is done:
-  //   dK/dV kernel: ring A = (Q, LSE*log2e, D) slots, last read by dK += dS^T Q;
-  //                 ring B = dO slots, last read by dV += P^T dO (earlier);
-  //   dQ kernel:    ring A = K slots, last read by dQ += dS K;
-  //                 ring B = V slots, last read by dP = dO V^T (earlier).
-  // Ring A feeds the first product of a tile (S^T or S), so its refill
-  // latency is on the critical path; the dQ kernel gets a third K slot at
-  // D = 128 (225 KB in all, within the 227 KB a CTA may have).
-  static constexpr int kKvASlots = D == 128 ? 2 : 4;
-  static constexpr int kKvBSlots = D == 128 ? 2 : 4;
-  static constexpr int kKvASlotBytes = kTileBytes + 1024;
-  static constexpr int kKvSmemBytes =
-      2 * kTileBytes + kKvASlots * kKvASlotBytes + kKvBSlots * kTileBytes + 1024;
+  // dK/dV kernel: K, V resident; one ring of stages (Q, dO, LSE*log2e, D).
+  // (Q and dO in rings of their own, dO's slot refilled after the dV product,
+  // measured 3.5 % slower: one more commit and wait per tile.)
+  static constexpr int kKvStages = D == 128 ? 2 : 4;
+  static constexpr int kKvStageBytes = 2 * kTileBytes + 1024;
+  static constexpr int kKvSmemBytes = 2 * kTileBytes + kKvStages * kKvStageBytes + 1024;
+  // dQ kernel: Q, dO staged for their copy into TMEM; ring A = K slots, last
+  // read by dQ += dS K, ring B = V slots, last read by dP = dO V^T, each with
+  // its own full / empty barriers.  K feeds the first product of a tile (S),
+  // so it gets a third slot at D = 128 (225 KB in all, within the 227 KB a
+  // CTA may have) and its slot is refilled a whole tile ahead.
   static constexpr int kQASlots = D == 128 ? 3 : 4;
   static constexpr int kQBSlots = D == 128 ? 2 : 4;
   static constexpr int kQSmemBytes = 2 * kTileBytes + (kQASlots + kQBSlots) * kTileBytes + 1024;
-  static_assert(kKvASlots <= 4 && kKvBSlots <= 4 && kQASlots <= 4 && kQBSlots <= 4, "barrier slots");
+  static_assert(kKvStages <= 4 && kQASlots <= 4 && kQBSlots <= 4, "barrier slots");
   static_assert(kKvSmemBytes <= 232448 && kQSmemBytes <= 232448, "shared memory per CTA");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kIdescS = make_idesc_bf16(kTile, kTile, false);
@@ -243,9 +240,9 @@ enum : int {
   kBarAccFull = 11,   // the unit's accumulators are complete
   kBarAccEmpty = 12,  // the compute warps have read them
   kBarDrain = 13,
-  kBarAFull = 14,     // ring A slot s loaded: kBarAFull + s
-  kBarAEmpty = 18,    // ring A slot s free: kBarAEmpty + s
-  kBarBFull = 22,     // ring B likewise
+  kBarAFull = 14,     // slot s of the (first) streamed ring loaded: kBarAFull + s
+  kBarAEmpty = 18,    // and free again: kBarAEmpty + s
+  kBarBFull = 22,     // dQ kernel's second ring (V) likewise
   kBarBEmpty = 26,
   kBarQTmemFull = 30, // dQ kernel: the unit's Q and dO are in TMEM
   kBarQTmemEmpty = 31,// dQ kernel: the unit's products no longer read them
@@ -559,9 +556,9 @@ template <int D>
 __device__ __forceinline__ void kv_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                             const CUtensorMap* tm_v, const CUtensorMap* tm_do,
                                             const BwdParams& p, Shared& ss, uint8_t* sK,
-                                            uint8_t* sV, uint8_t* sA, uint8_t* sB, int n_units) {
+                                            uint8_t* sV, uint8_t* sStage, int n_units) {
   using C = BwdCfg<D>;
-  uint32_t ringA = 0, ringB = 0, uslot = 0;
+  uint32_t ring = 0, uslot = 0;
   int units_done = 0;
   int u = blockIdx.x;
   for (;;) {
@@ -577,32 +574,21 @@ __device__ __forceinline__ void kv_producer(const CUtensorMap* tm_q, const CUten
       tma_load_3d(smem_u32(sV + c * kChunkBytes), tm_v, bar_addr(ss, kBarResFull), c * 64, un.h, k0);
     }
     for (int i = un.o0; i < un.o0 + un.n; ++i) {
+      const int slot = ring % C::kKvStages;
+      const uint32_t n = ring / C::kKvStages;
+      if (n > 0 && !wait_bar(ss, kBarAEmpty + slot, (n - 1) & 1, p, 103)) return;
+      const uint32_t full = bar_addr(ss, kBarAFull + slot);
+      uint8_t* st = sStage + slot * C::kKvStageBytes;
+      mbar_arrive_expect_tx(full, C::kKvStageBytes);
       const int q0 = un.tok0 + tile_start(i, un.L);
-      {  // dO (ring B: its slot is free first, after the dV product)
-        const int slot = ringB % C::kKvBSlots;
-        const uint32_t n = ringB / C::kKvBSlots;
-        if (n > 0 && !wait_bar(ss, kBarBEmpty + slot, (n - 1) & 1, p, 106)) return;
-        const uint32_t full = bar_addr(ss, kBarBFull + slot);
-        uint8_t* st = sB + slot * C::kTileBytes;
-        mbar_arrive_expect_tx(full, C::kTileBytes);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem_u32(st + c * kChunkBytes), tm_do, full, c * 64, un.h, q0);
-        ++ringB;
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_3d(smem_u32(st + c * kChunkBytes), tm_q, full, c * 64, un.h, q0);
+        tma_load_3d(smem_u32(st + C::kTileBytes + c * kChunkBytes), tm_do, full, c * 64, un.h, q0);
       }
-      {  // Q, LSE*log2e, D (ring A: free after the dK product)
-        const int slot = ringA % C::kKvASlots;
-        const uint32_t n = ringA / C::kKvASlots;
-        if (n > 0 && !wait_bar(ss, kBarAEmpty + slot, (n - 1) & 1, p, 103)) return;
-        const uint32_t full = bar_addr(ss, kBarAFull + slot);
-        uint8_t* st = sA + slot * C::kKvASlotBytes;
-        mbar_arrive_expect_tx(full, C::kKvASlotBytes);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem_u32(st + c * kChunkBytes), tm_q, full, c * 64, un.h, q0);
-        const size_t vec = vec_index(p, un, i);
-        bulk_load(smem_u32(st + C::kTileBytes), p.lse2 + vec, 512, full);
-        bulk_load(smem_u32(st + C::kTileBytes + 512), p.dd + vec, 512, full);
-        ++ringA;
-      }
+      const size_t vec = vec_index(p, un, i);
+      bulk_load(smem_u32(st + 2 * C::kTileBytes), p.lse2 + vec, 512, full);
+      bulk_load(smem_u32(st + 2 * C::kTileBytes + 512), p.dd + vec, 512, full);
+      ++ring;
     }
     ++units_done;
     u = next_u;
@@ -611,17 +597,14 @@ __device__ __forceinline__ void kv_producer(const CUtensorMap* tm_q, const CUten
 
 template <int D>
 __device__ __forceinline__ void kv_mma(const BwdParams& p, Shared& ss, uint8_t* sK, uint8_t* sV,
-                                       uint8_t* sA, uint8_t* sB, uint32_t tmem) {
+                                       uint8_t* sStage, uint32_t tmem) {
   using C = BwdCfg<D>;
   constexpr uint32_t kColDV = 0, kColDK = D, kColS = 2 * D, kColDP = 2 * D + 128;
   const uint32_t k_smem = smem_u32(sK), v_smem = smem_u32(sV);
-  auto q_smem = [&](uint32_t pos) { return smem_u32(sA + (pos % C::kKvASlots) * C::kKvASlotBytes); };
-  auto do_smem = [&](uint32_t pos) { return smem_u32(sB + (pos % C::kKvBSlots) * C::kTileBytes); };
-  auto a_full = [&](uint32_t pos) {
-    return wait_bar(ss, kBarAFull + pos % C::kKvASlots, (pos / C::kKvASlots) & 1, p, 110);
-  };
-  auto b_full = [&](uint32_t pos) {
-    return wait_bar(ss, kBarBFull + pos % C::kKvBSlots, (pos / C::kKvBSlots) & 1, p, 115);
+  auto q_smem = [&](uint32_t pos) { return smem_u32(sStage + (pos % C::kKvStages) * C::kKvStageBytes); };
+  auto do_smem = [&](uint32_t pos) { return q_smem(pos) + C::kTileBytes; };
+  auto stage_full = [&](uint32_t pos) {
+    return wait_bar(ss, kBarAFull + pos % C::kKvStages, (pos / C::kKvStages) & 1, p, 110);
   };
   uint32_t ring = 0, uslot = 0, pcount = 0, dscount = 0;
   int units_done = 0;
@@ -630,12 +613,10 @@ __device__ __forceinline__ void kv_mma(const BwdParams& p, Shared& ss, uint8_t* 
     if (!next_unit(ss, p, uslot, false, u) || u < 0) return;
     const Unit un = kv_unit(p, u);
     if (!wait_bar(ss, kBarResFull, units_done & 1, p, 111)) return;
-    if (!a_full(ring)) return;
+    if (!stage_full(ring)) return;
     tc_fence_after();
     mma_rows_rows<D>(tmem + kColS, k_smem, q_smem(ring));     // S^T = K Q^T
     mma_commit(bar_addr(ss, kBarSFull));
-    if (!b_full(ring)) return;
-    tc_fence_after();
     mma_rows_rows<D>(tmem + kColDP, v_smem, do_smem(ring));   // dP^T = V dO^T
     mma_commit(bar_addr(ss, kBarDPFull));
     for (int i = 0; i < un.n; ++i) {
@@ -646,9 +627,8 @@ __device__ __forceinline__ void kv_mma(const BwdParams& p, Shared& ss, uint8_t* 
         return;
       tc_fence_after();
       mma_tmem_rows<D>(tmem + kColDV, tmem + kColS, do_smem(pos), i > 0);   // dV += P^T dO
-      mma_commit(bar_addr(ss, kBarBEmpty + pos % C::kKvBSlots));            // dO slot free
       if (more) {
-        if (!a_full(pos + 1)) return;
+        if (!stage_full(pos + 1)) return;
         tc_fence_after();
         mma_rows_rows<D>(tmem + kColS, k_smem, q_smem(pos + 1));
         mma_commit(bar_addr(ss, kBarSFull));
@@ -656,10 +636,8 @@ __device__ __forceinline__ void kv_mma(const BwdParams& p, Shared& ss, uint8_t* 
       if (!wait_bar(ss, kBarDSFull, dscount++ & 1, p, 114)) return;
       tc_fence_after();
       mma_tmem_rows<D>(tmem + kColDK, tmem + kColDP, q_smem(pos), i > 0);   // dK += dS^T Q
-      mma_commit(bar_addr(ss, kBarAEmpty + pos % C::kKvASlots));            // Q slot free
+      mma_commit(bar_addr(ss, kBarAEmpty + pos % C::kKvStages));           // stage free
       if (more) {
-        if (!b_full(pos + 1)) return;
-        tc_fence_after();
         mma_rows_rows<D>(tmem + kColDP, v_smem, do_smem(pos + 1));
         mma_commit(bar_addr(ss, kBarDPFull));
       }
@@ -672,7 +650,7 @@ __device__ __forceinline__ void kv_mma(const BwdParams& p, Shared& ss, uint8_t* 
 }
 
 template <int D>
-__device__ __forceinline__ void kv_compute(const BwdParams& p, Shared& ss, uint8_t* sA,
+__device__ __forceinline__ void kv_compute(const BwdParams& p, Shared& ss, uint8_t* sStage,
                                            uint32_t tmem) {
   using C = BwdCfg<D>;
   constexpr uint32_t kColDV = 0, kColDK = D, kColS = 2 * D, kColDP = 2 * D + 128;
@@ -692,12 +670,12 @@ __device__ __forceinline__ void kv_compute(const BwdParams& p, Shared& ss, uint8
     const int key = ks + kr;
     for (int i = 0; i < un.n; ++i) {
       const uint32_t pos = ring + i;
-      const float* sl = reinterpret_cast<const float*>(sA + (pos % C::kKvASlots) * C::kKvASlotBytes +
-                                                       C::kTileBytes);
+      const float* sl = reinterpret_cast<const float*>(sStage + (pos % C::kKvStages) * C::kKvStageBytes +
+                                                       2 * C::kTileBytes);
       const int q0 = tile_start(un.o0 + i, un.L) + 32 * cg;  // query of this warp's column 0
-      // the slot's LSE and D vectors are read below: wait for its copies too
-      if (!__all_sync(0xffffffffu, wait_bar(ss, kBarAFull + pos % C::kKvASlots,
-                                            (pos / C::kKvASlots) & 1, p, 123)))
+      // the stage's LSE and D vectors are read below: wait for its copies too
+      if (!__all_sync(0xffffffffu, wait_bar(ss, kBarAFull + pos % C::kKvStages,
+                                            (pos / C::kKvStages) & 1, p, 123)))
         return;
       if (!__all_sync(0xffffffffu, wait_bar(ss, kBarSFull, scount & 1, p, 120))) return;
       tc_fence_after();
@@ -1033,8 +1011,8 @@ bwd_tile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sRes0 = smem;                     // K (dK/dV kernel) or Q (dQ kernel)
   uint8_t* sRes1 = smem + C::kTileBytes;     // V or dO
-  uint8_t* sA = smem + 2 * C::kTileBytes;    // ring A, then ring B
-  uint8_t* sB = sA + (kKv ? C::kKvASlots * C::kKvASlotBytes : C::kQASlots * C::kTileBytes);
+  uint8_t* sA = smem + 2 * C::kTileBytes;    // the stage ring (dK/dV) or ring A, then B (dQ)
+  uint8_t* sB = sA + C::kQASlots * C::kTileBytes;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int n_units = total_tiles(p) * p.H;
 
@@ -1086,14 +1064,14 @@ bwd_tile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (warp == kProducerWarp) {
       if (lane == 0) {
         if (kKv)
-          kv_producer<D>(&tm_q, &tm_k, &tm_v, &tm_do, p, ss, sRes0, sRes1, sA, sB, n_units);
+          kv_producer<D>(&tm_q, &tm_k, &tm_v, &tm_do, p, ss, sRes0, sRes1, sA, n_units);
         else
           q_producer<D>(&tm_q, &tm_k, &tm_v, &tm_do, p, ss, sRes0, sRes1, sA, sB, n_units);
       }
     } else if (warp == kMmaWarp) {
       if (lane == 0) {
         if (kKv)
-          kv_mma<D>(p, ss, sRes0, sRes1, sA, sB, tmem);
+          kv_mma<D>(p, ss, sRes0, sRes1, sA, tmem);
         else
           q_mma<D>(p, ss, sA, sB, tmem);
         // every MMA issued by this thread has finished before TMEM is freed
