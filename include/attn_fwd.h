@@ -139,6 +139,35 @@ int attn_fwd_decode(const void *q, const void *k, const void *v, void *o, float 
                     int B, int H, int d, float scale, const int32_t *cu_seqlens_k,
                     int max_seqlen_k, int num_splits, attn_stream_t stream);
 
+/*
+ * attn_fwd_host: attn_fwd on HOST buffers (dense batches).  The call copies
+ * Q, K, V to the device, computes O and the LSE with attn_fwd's kernels, and
+ * copies them back, in groups of heads so that the copies of one group
+ * overlap the attention of the next: group g + 1 is copied in on one
+ * internal stream while group g is computed on `stream` and group g - 1 is
+ * copied out on another.  Every row is computed exactly as by attn_fwd, so O
+ * and the LSE are bit-identical to attn_fwd's on the same inputs.  This is
+ * plumbing around the pages' kernel, which assumes its inputs already sit in
+ * HBM ("flash-attention-evolution" (letsgetai), FlashAttention "核心机制").
+ * Layout: q, k, v, o [B, N, H, d] bf16 and lse [B, H, N] fp32, in host (or
+ *   any) memory; page-locked host memory lets the copies run asynchronously
+ *   and overlap; with pageable memory the call still works, its copies
+ *   serialise with the host.
+ * Ordering: the call is asynchronous like attn_fwd.  Its work starts after
+ *   the work queued on `stream` before it, and the work queued on `stream`
+ *   after it starts once o and lse are written; synchronise `stream` before
+ *   reading them.  The caller keeps the host buffers alive and unchanged
+ *   until then.
+ * Ownership: the library keeps, per (device, stream), two internal copy
+ *   streams, their events and a device workspace for two head groups (four
+ *   [B, N, hg, d] tiles and a [B, hg, N] LSE block each), grown on demand.
+ * Errors: like attn_fwd (no alignment requirement on the host buffers); a
+ *   failed copy returns ATTN_ERR_CUDA.  Device-side errors are read with
+ *   attn_last_device_error(stream).
+ */
+int attn_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse,
+                  int B, int H, int N, int d, float scale, int causal, attn_stream_t stream);
+
 /* Options of attn_fwd_ex.  Zero-initialise and set what is needed. */
 typedef struct {
     uint64_t wait_timeout_ns; /* bound on each device-side wait; 0 = 2 s */

@@ -15,12 +15,12 @@ import os
 from . import build as _build
 
 __all__ = ["attn_fwd", "attn_bwd", "attn_bwd_window", "attn_fwd_fp8", "attn_fp8_quantize_qk", "attn_fp8_quantize_v",
-           "attn_fwd_ex", "attn_fwd_noalloc", "attn_fwd_window", "attn_fwd_kvsplit", "attn_fwd_decode", "attn_last_device_error", "attn_last_error_site",
+           "attn_fwd_ex", "attn_fwd_host", "attn_fwd_noalloc", "attn_fwd_window", "attn_fwd_kvsplit", "attn_fwd_decode", "attn_last_device_error", "attn_last_error_site",
            "attn_status_string", "AttnError", "AttnFwdOptions", "lib", "forward", "backward", "decode",
            "EXPORTED_SYMBOLS"]
 
 # Every symbol the headers under include/ declare.
-EXPORTED_SYMBOLS = ("attn_fwd", "attn_fwd_ex", "attn_fwd_decode", "attn_last_device_error", "attn_last_error_site",
+EXPORTED_SYMBOLS = ("attn_fwd", "attn_fwd_ex", "attn_fwd_host", "attn_fwd_decode", "attn_last_device_error", "attn_last_error_site",
                     "attn_last_cuda_error", "attn_status_string", "attn_fwd_noalloc",
                     "attn_fwd_window", "attn_fwd_kvsplit", "attn_bwd", "attn_bwd_window",
                     "attn_fwd_fp8",
@@ -78,6 +78,8 @@ def lib() -> ctypes.CDLL:
         L.attn_fp8_quantize_v.restype = i
         L.attn_fwd_noalloc.argtypes = sig
         L.attn_fwd_noalloc.restype = i
+        L.attn_fwd_host.argtypes = sig[:11] + [vp]
+        L.attn_fwd_host.restype = i
         L.attn_last_device_error.argtypes = [vp]
         L.attn_last_device_error.restype = i
         L.attn_last_error_site.restype = i
@@ -89,7 +91,7 @@ def lib() -> ctypes.CDLL:
 
 
 def _ptr(x) -> int | None:
-    """A device pointer from a torch tensor, an int address or None."""
+    """A buffer address from a torch tensor, an int address or None."""
     if x is None:
         return None
     if isinstance(x, int):
@@ -114,6 +116,17 @@ def attn_fwd(q, k, v, o, lse, B: int, H: int, N: int, d: int, scale: float, caus
     Raises AttnError on a non-zero status; returns 0."""
     st = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(N),
                         int(d), float(scale), int(bool(causal)), _ptr(cu_seqlens), _stream(stream))
+    if st != ATTN_OK:
+        raise AttnError(st)
+    return st
+
+
+def attn_fwd_host(q, k, v, o, lse, B: int, H: int, N: int, d: int, scale: float, causal: bool,
+                  stream=None) -> int:
+    """The C call ``attn_fwd_host``: attn_fwd on host buffers (CPU tensors,
+    page-locked for overlapped copies, or addresses); dense [B, N, H, d]."""
+    st = lib().attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(N),
+                             int(d), float(scale), int(bool(causal)), _stream(stream))
     if st != ATTN_OK:
         raise AttnError(st)
     return st

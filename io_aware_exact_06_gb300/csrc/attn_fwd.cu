@@ -322,6 +322,141 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
                        nullptr);
 }
 
+namespace {
+
+// attn_fwd_host's pipeline state for one (device, stream): two copy streams,
+// the events that order them against the caller's stream, and a device
+// workspace of two slots, each holding one head group's Q, K, V, O tiles and
+// LSE block.
+struct HostPipe {
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, done = nullptr;
+  cudaEvent_t in_done[2] = {}, comp_done[2] = {}, out_done[2] = {};
+  uint8_t* slot[2] = {nullptr, nullptr};
+  size_t slot_bytes = 0;
+};
+
+std::mutex g_host_mu;  // attn_fwd_host's state; attn_fwd_impl takes g_mu itself
+std::map<std::pair<int, attn_stream_t>, HostPipe> g_host;
+
+size_t round_up_256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+int host_pipe(int dev, attn_stream_t stream, size_t slot_bytes, HostPipe** out) {
+  HostPipe& hp = g_host[std::make_pair(dev, stream)];
+  cudaError_t e;
+  if (!hp.in) {
+    if ((e = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking)) != cudaSuccess) return cuda_fail(e);
+    cudaEvent_t* evs[] = {&hp.start, &hp.done, &hp.in_done[0], &hp.in_done[1], &hp.comp_done[0],
+                          &hp.comp_done[1], &hp.out_done[0], &hp.out_done[1]};
+    for (cudaEvent_t* ev : evs)
+      if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess) return cuda_fail(e);
+  }
+  if (hp.slot_bytes < slot_bytes) {
+    // the slots may still be read or written by the previous call's work
+    if ((e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream))) != cudaSuccess)
+      return cuda_fail(e);
+    for (auto& p : hp.slot) {
+      if (p) cudaFree(p);
+      p = nullptr;
+    }
+    hp.slot_bytes = 0;
+    for (auto& p : hp.slot)
+      if ((e = cudaMalloc(&p, slot_bytes)) != cudaSuccess) return cuda_fail(e);
+    hp.slot_bytes = slot_bytes;
+  }
+  *out = &hp;
+  return ATTN_OK;
+}
+
+// Heads per group: about 32 MB of Q, K, V per group, and at least two groups
+// when there are two heads (so that copies and attention overlap); groups as
+// even as the head count allows.
+int host_head_group(int B, int H, int N, int d) {
+  const size_t head_bytes = 3 * (size_t)B * N * d * 2;
+  int64_t hg = std::max<int64_t>(1, (int64_t)((32ull << 20) / std::max<size_t>(head_bytes, 1)));
+  if (H >= 2) hg = std::min<int64_t>(hg, (H + 1) / 2);
+  hg = std::min<int64_t>(hg, H);
+  const int64_t groups = (H + hg - 1) / hg;
+  return (int)((H + groups - 1) / groups);
+}
+
+}  // namespace
+
+extern "C" int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int B, int H, int N, int d, float scale, int causal,
+                             attn_stream_t stream) {
+  if (B < 0 || H < 0 || N < 0) return ATTN_ERR_SHAPE;
+  if (d != 64 && d != 128) return ATTN_ERR_HEADDIM;
+  if (!std::isfinite(scale) || scale < 0.0f) return ATTN_ERR_SCALE;
+  if (B == 0 || H == 0 || N == 0) return ATTN_OK;
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL;
+  if ((int64_t)B * N > INT32_MAX - 2 * attn::kBN || (int64_t)H * d > (1 << 20) || H > 65535)
+    return ATTN_ERR_SHAPE;
+  const int hg = host_head_group(B, H, N, d);
+  const size_t tile = round_up_256((size_t)B * N * hg * d * 2);  // one [B, N, hg, d] bf16 tile
+  const size_t lse_bytes = round_up_256((size_t)B * hg * N * sizeof(float));
+
+  std::lock_guard<std::mutex> lock(g_host_mu);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  HostPipe* hp = nullptr;
+  int st = host_pipe(dev, stream, 4 * tile + lse_bytes, &hp);
+  if (st != ATTN_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t row = (size_t)H * d * 2;  // bytes of one token's heads
+  const auto* qh = static_cast<const uint8_t*>(q);
+  const auto* kh = static_cast<const uint8_t*>(k);
+  const auto* vh = static_cast<const uint8_t*>(v);
+  auto* oh = static_cast<uint8_t*>(o);
+  // the copies start after the caller's earlier work (and this stream's
+  // previous call, which used the same slots)
+  if ((e = cudaEventRecord(hp->start, s)) != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaStreamWaitEvent(hp->in, hp->start, 0)) != cudaSuccess) return cuda_fail(e);
+  const int groups = (H + hg - 1) / hg;
+  for (int g = 0; g < groups; ++g) {
+    const int j = g & 1;
+    const int h0 = g * hg, hn = std::min(hg, H - h0);
+    const size_t w = (size_t)hn * d * 2;  // bytes of one token's heads of this group
+    uint8_t* base = hp->slot[j];
+    uint8_t *dq = base, *dk = base + tile, *dv = base + 2 * tile, *dout = base + 3 * tile;
+    float* dlse = reinterpret_cast<float*>(base + 4 * tile);
+    // Q, K, V of the group into slot j, once group g - 2's attention has read it
+    if (g >= 2 && (e = cudaStreamWaitEvent(hp->in, hp->comp_done[j], 0)) != cudaSuccess)
+      return cuda_fail(e);
+    const uint8_t* srcs[3] = {qh, kh, vh};
+    uint8_t* dsts[3] = {dq, dk, dv};
+    for (int t = 0; t < 3; ++t)
+      if ((e = cudaMemcpy2DAsync(dsts[t], w, srcs[t] + (size_t)h0 * d * 2, row, w, (size_t)B * N,
+                                 cudaMemcpyDefault, hp->in)) != cudaSuccess)
+        return cuda_fail(e);
+    if ((e = cudaEventRecord(hp->in_done[j], hp->in)) != cudaSuccess) return cuda_fail(e);
+    // attention of the group on the caller's stream, once its inputs are in
+    // and group g - 2's outputs have left slot j
+    if ((e = cudaStreamWaitEvent(s, hp->in_done[j], 0)) != cudaSuccess) return cuda_fail(e);
+    if (g >= 2 && (e = cudaStreamWaitEvent(s, hp->out_done[j], 0)) != cudaSuccess) return cuda_fail(e);
+    st = attn_fwd_impl(dq, dk, dv, dout, dlse, B, hn, N, d, scale, causal, -1, -1, nullptr, stream,
+                       nullptr);
+    if (st != ATTN_OK) return st;
+    if ((e = cudaEventRecord(hp->comp_done[j], s)) != cudaSuccess) return cuda_fail(e);
+    // O and the LSE of the group back to the host buffers
+    if ((e = cudaStreamWaitEvent(hp->out, hp->comp_done[j], 0)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaMemcpy2DAsync(oh + (size_t)h0 * d * 2, row, dout, w, w, (size_t)B * N,
+                               cudaMemcpyDefault, hp->out)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((e = cudaMemcpy2DAsync(lse + (size_t)h0 * N, (size_t)H * N * sizeof(float), dlse,
+                               (size_t)hn * N * sizeof(float), (size_t)hn * N * sizeof(float), B,
+                               cudaMemcpyDefault, hp->out)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((e = cudaEventRecord(hp->out_done[j], hp->out)) != cudaSuccess) return cuda_fail(e);
+  }
+  // later work on the caller's stream sees O and the LSE in the host buffers
+  if ((e = cudaEventRecord(hp->done, hp->out)) != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaStreamWaitEvent(s, hp->done, 0)) != cudaSuccess) return cuda_fail(e);
+  return ATTN_OK;
+}
+
 extern "C" int attn_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse,
                                int B, int H, int N, int d, float scale, int causal,
                                int window_left, int window_right, const int32_t* cu_seqlens,

@@ -81,6 +81,35 @@ def test_empty_problem_is_a_noop(lib, zero):
                         None, None) == 0
 
 
+@pytest.mark.parametrize("args,status", [
+    (dict(B=-1), -2),
+    (dict(N=-5), -2),
+    (dict(d=96), -3),
+    (dict(scale=float("nan")), -5),
+    (dict(scale=-0.5), -5),
+    (dict(q=None), -1),
+    (dict(o=None), -1),
+    (dict(lse=None), -1),
+    (dict(B=70000, N=1 << 16), -2),
+    (dict(H=70000), -2),
+])
+def test_host_argument_errors(lib, args, status):
+    a = dict(q=BUF, k=BUF, v=BUF, o=BUF, lse=BUF, B=2, H=4, N=256, d=128, scale=0.1,
+             causal=1, stream=None)
+    a.update(args)
+    st = lib.attn_fwd_host(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"],
+                           a["d"], a["scale"], a["causal"], a["stream"])
+    assert st == status
+
+
+@pytest.mark.parametrize("zero", ["B", "H", "N"])
+def test_host_empty_problem_is_a_noop(lib, zero):
+    a = dict(B=2, H=4, N=256)
+    a[zero] = 0
+    assert lib.attn_fwd_host(None, None, None, None, None, a["B"], a["H"], a["N"], 128, 0.125, 1,
+                             None) == 0
+
+
 def test_binding_raises_on_error(lib):
     with pytest.raises(fa.AttnError) as e:
         fa.attn_fwd(BUF, BUF, BUF, BUF, BUF, 1, 1, 128, 80, 0.1, False)
