@@ -86,9 +86,11 @@ template <int D>
 int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                const CUtensorMap& mdo, const void* o, const void* dout, const float* lse,
                BwdParams p, int* counters, int64_t max_tiles, int grid, cudaStream_t s) {
-  // one warp per row slot of every tile and head (packed: an upper bound of the tiles)
+  // every row slot of every tile and head (packed: an upper bound of the
+  // tiles), PrepCfg<D>::kRowsPerWarp slots per warp
   const long long slots = (long long)p.H * max_tiles * bwd::kTile;
-  const long long blocks = (slots * 32 + 255) / 256;
+  const long long warps = slots / bwd::PrepCfg<D>::kRowsPerWarp;
+  const long long blocks = (warps * 32 + 255) / 256;
   bwd::bwd_prep_kernel<D><<<(unsigned)blocks, 256, 0, s>>>(
       reinterpret_cast<const __nv_bfloat16*>(o), reinterpret_cast<const __nv_bfloat16*>(dout), lse,
       p, slots);

@@ -403,18 +403,32 @@ __device__ __forceinline__ size_t vec_index(const BwdParams& p, const Unit& un, 
 
 // ------------------------------------------------------------ prologue --
 // D_i = <dO_i, O_i> (fp32 sum of bf16 products) and LSE_i log2(e), written
-// for every row slot of every query tile.  One warp per row slot.
+// for every row slot of every query tile.  A row of D bf16 is read by D/8
+// lanes, 16 bytes each; a warp covers kRowsPerLoad rows per load and takes
+// kIters such groups, all its loads of O and dO issued before the first is
+// used (the kernel moves 2 x 33.5 MB on the long workloads: bandwidth, not
+// arithmetic).
+template <int D>
+struct PrepCfg {
+  static constexpr int kLanesPerRow = D / 8;
+  static constexpr int kRowsPerLoad = 32 / kLanesPerRow;
+  static constexpr int kIters = 2;
+  static constexpr int kRowsPerWarp = kRowsPerLoad * kIters;
+  static_assert(kTile % kRowsPerWarp == 0, "the rows of a warp lie in one tile");
+};
+
 template <int D>
 __global__ void __launch_bounds__(256)
 bwd_prep_kernel(const __nv_bfloat16* o, const __nv_bfloat16* dout, const float* lse, BwdParams p,
                 long long slots) {
+  using C = PrepCfg<D>;
   const long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / 32;
   const int lane = threadIdx.x % 32;
-  if (w >= slots) return;
+  const long long s0 = w * C::kRowsPerWarp;  // first row slot of this warp
+  if (s0 >= slots) return;
   const int tiles = total_tiles(p);
   if (tiles <= 0) return;
-  const int r = (int)(w % kTile);
-  const long long gt = w / kTile;
+  const long long gt = s0 / kTile;
   const int g = (int)(gt % tiles);
   const int h = (int)(gt / tiles);
   if (h >= p.H) return;  // (packed: the grid covers an upper bound of the tiles)
@@ -429,32 +443,47 @@ bwd_prep_kernel(const __nv_bfloat16* o, const __nv_bfloat16* dout, const float* 
     t = g - un.b * p.T;
   }
   place(p, un);
-  const int row = tile_start(t, un.L) + r;
-  const bool valid = row >= t * kTile;  // (and row < L: the tile ends at L)
-  float acc = 0.f;
-  if (valid) {
-    constexpr int kPer = D / 32;
-    const size_t base = ((size_t)(un.tok0 + row) * p.H + h) * D + lane * kPer;
+  const int chunk = lane % C::kLanesPerRow;  // elements 8 chunk .. 8 chunk + 7 of the row
+  int r[C::kIters], row[C::kIters];
+  bool valid[C::kIters];
+  uint4 xo[C::kIters], xd[C::kIters];
 #pragma unroll
-    for (int c = 0; c < kPer; c += 2) {
-      const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(o + base + c);
-      const __nv_bfloat162 y = *reinterpret_cast<const __nv_bfloat162*>(dout + base + c);
-      acc = fmaf(__bfloat162float(x.x), __bfloat162float(y.x), acc);
-      acc = fmaf(__bfloat162float(x.y), __bfloat162float(y.y), acc);
+  for (int it = 0; it < C::kIters; ++it) {
+    r[it] = (int)(s0 % kTile) + it * C::kRowsPerLoad + lane / C::kLanesPerRow;
+    row[it] = tile_start(t, un.L) + r[it];
+    valid[it] = row[it] >= t * kTile;  // (and row < L: the tile ends at L)
+    xo[it] = make_uint4(0u, 0u, 0u, 0u);
+    xd[it] = xo[it];
+    if (valid[it]) {
+      const size_t base = ((size_t)(un.tok0 + row[it]) * p.H + h) * D + 8 * chunk;
+      xo[it] = *reinterpret_cast<const uint4*>(o + base);
+      xd[it] = *reinterpret_cast<const uint4*>(dout + base);
     }
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) {
-    const size_t idx = vec_index(p, un, t) + r;
-    float* dd = const_cast<float*>(p.dd);
-    float* lse2 = const_cast<float*>(p.lse2);
-    dd[idx] = acc;
-    size_t li = 0;
-    if (valid)
-      li = p.cu_seqlens ? (size_t)h * p.cu_seqlens[p.B] + un.tok0 + row
-                        : ((size_t)un.b * p.H + h) * p.N + row;
-    lse2[idx] = valid ? lse[li] * 1.4426950408889634f : INFINITY;
+  for (int it = 0; it < C::kIters; ++it) {
+    const uint32_t a[4] = {xo[it].x, xo[it].y, xo[it].z, xo[it].w};
+    const uint32_t b[4] = {xd[it].x, xd[it].y, xd[it].z, xd[it].w};
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc = fmaf(__uint_as_float(a[i] << 16), __uint_as_float(b[i] << 16), acc);
+      acc = fmaf(__uint_as_float(a[i] & 0xffff0000u), __uint_as_float(b[i] & 0xffff0000u), acc);
+    }
+#pragma unroll
+    for (int off = C::kLanesPerRow / 2; off > 0; off >>= 1)
+      acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (chunk == 0) {
+      const size_t idx = vec_index(p, un, t) + r[it];
+      float* dd = const_cast<float*>(p.dd);
+      float* lse2 = const_cast<float*>(p.lse2);
+      dd[idx] = acc;
+      size_t li = 0;
+      if (valid[it])
+        li = p.cu_seqlens ? (size_t)h * p.cu_seqlens[p.B] + un.tok0 + row[it]
+                          : ((size_t)un.b * p.H + h) * p.N + row[it];
+      lse2[idx] = valid[it] ? lse[li] * 1.4426950408889634f : INFINITY;
+    }
   }
 }
 
