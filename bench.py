@@ -781,9 +781,9 @@ def fp8_cpu_baseline(wl, signs, budget_s: float = 10.0):
 
 # DRAM bytes (read + write) of one backward call on this workload (all three
 # kernels), from one ncu capture of the current kernels (None once one of them
-# changes): prep 135.28 + 4.01 MB, dK/dV 924.74 + 102.22 MB, dQ 957.09 +
-# 46.58 MB.
-BWD_TRAFFIC_BYTES = 135_275_776 + 4_005_632 + 924_736_768 + 102_221_312 + 957_086_976 + 46_578_688
+# changes): prep 135.28 + 3.91 MB, dK/dV 928.37 + 101.98 MB, dQ 954.79 +
+# 46.44 MB.
+BWD_TRAFFIC_BYTES = 135_278_592 + 3_907_072 + 928_369_664 + 101_978_368 + 954_793_472 + 46_435_584
 
 
 # DRAM bytes (read + write) of one attn_fwd_kernel<128> launch of this
