@@ -318,24 +318,14 @@ def run_cuda(args, world, rank, local):
     kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
 
     # end to end through the C ABI with host buffers, every step: H2D of Q,
-    # K, V from pinned memory, the forward, D2H of O and LSE.  Dense batches
-    # call attn_fwd_host (the copies of one head group overlap the attention
-    # of the next); packed batches copy around attn_fwd on one stream.
-    if cu is None:
-        e2e_api = "attn_fwd_host"
+    # K, V from pinned memory, the forward, D2H of O and LSE, by
+    # attn_fwd_host (the copies of one head group overlap the attention of
+    # the next)
+    cu_h = torch.from_numpy(wl.cu_seqlens.astype(np.int32)).pin_memory() if cu is not None else None
+    e2e_api = "attn_fwd_host"
 
-        def e2e_step():
-            fa.attn_fwd_host(q_h, k_h, v_h, o_h, lse_h, B, H, N, d, wl.scale, wl.causal, stream)
-    else:
-        e2e_api = "torch copies + attn_fwd"
-
-        def e2e_step():
-            q.copy_(q_h, non_blocking=True)
-            k.copy_(k_h, non_blocking=True)
-            v.copy_(v_h, non_blocking=True)
-            step()
-            o_h.copy_(o, non_blocking=True)
-            lse_h.copy_(lse, non_blocking=True)
+    def e2e_step():
+        fa.attn_fwd_host(q_h, k_h, v_h, o_h, lse_h, B, H, N, d, wl.scale, wl.causal, cu_h, stream)
 
     e2e_steps = max(3, min(args.steps, 10))
     for _ in range(2):

@@ -140,19 +140,21 @@ int attn_fwd_decode(const void *q, const void *k, const void *v, void *o, float 
                     int max_seqlen_k, int num_splits, attn_stream_t stream);
 
 /*
- * attn_fwd_host: attn_fwd on HOST buffers (dense batches).  The call copies
- * Q, K, V to the device, computes O and the LSE with attn_fwd's kernels, and
- * copies them back, in groups of heads so that the copies of one group
- * overlap the attention of the next: group g + 1 is copied in on one
- * internal stream while group g is computed on `stream` and group g - 1 is
- * copied out on another.  Every row is computed exactly as by attn_fwd, so O
- * and the LSE are bit-identical to attn_fwd's on the same inputs.  This is
- * plumbing around the pages' kernel, which assumes its inputs already sit in
- * HBM ("flash-attention-evolution" (letsgetai), FlashAttention "核心机制").
- * Layout: q, k, v, o [B, N, H, d] bf16 and lse [B, H, N] fp32, in host (or
- *   any) memory; page-locked host memory lets the copies run asynchronously
- *   and overlap; with pageable memory the call still works, its copies
- *   serialise with the host.
+ * attn_fwd_host: attn_fwd on HOST buffers.  The call copies Q, K, V to the
+ * device, computes O and the LSE with attn_fwd's kernels, and copies them
+ * back, in groups of heads so that the copies of one group overlap the
+ * attention of the next: group g + 1 is copied in on one internal stream
+ * while group g is computed on `stream` and group g - 1 is copied out on
+ * another.  Every row is computed exactly as by attn_fwd, so O and the LSE
+ * are bit-identical to attn_fwd's on the same inputs.  This is plumbing
+ * around the pages' kernel, which assumes its inputs already sit in HBM
+ * ("flash-attention-evolution" (letsgetai), FlashAttention "核心机制").
+ * Arguments and layouts: those of attn_fwd, with every buffer (cu_seqlens
+ *   included) in host (or any) memory: dense q, k, v, o [B, N, H, d] bf16 and
+ *   lse [B, H, N] fp32; packed [total, H, d] and lse [H, total] with total =
+ *   cu_seqlens[B].  Page-locked host memory lets the copies run
+ *   asynchronously and overlap; with pageable memory the call still works,
+ *   its copies serialise with the host.
  * Ordering: the call is asynchronous like attn_fwd.  Its work starts after
  *   the work queued on `stream` before it, and the work queued on `stream`
  *   after it starts once o and lse are written; synchronise `stream` before
@@ -160,13 +162,17 @@ int attn_fwd_decode(const void *q, const void *k, const void *v, void *o, float 
  *   until then.
  * Ownership: the library keeps, per (device, stream), two internal copy
  *   streams, their events and a device workspace for two head groups (four
- *   [B, N, hg, d] tiles and a [B, hg, N] LSE block each), grown on demand.
- * Errors: like attn_fwd (no alignment requirement on the host buffers); a
- *   failed copy returns ATTN_ERR_CUDA.  Device-side errors are read with
- *   attn_last_device_error(stream).
+ *   [tokens, hg, d] tiles, the group's LSE and a copy of cu_seqlens each),
+ *   grown on demand.
+ * Errors: like attn_fwd (no alignment requirement on the host buffers).
+ *   cu_seqlens is checked on the host before anything is copied: not
+ *   starting at 0, decreasing, or with a length above N returns
+ *   ATTN_ERR_SEQLENS.  A failed copy returns ATTN_ERR_CUDA; device-side
+ *   errors are read with attn_last_device_error(stream).
  */
 int attn_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse,
-                  int B, int H, int N, int d, float scale, int causal, attn_stream_t stream);
+                  int B, int H, int N, int d, float scale, int causal,
+                  const int32_t *cu_seqlens, attn_stream_t stream);
 
 /* Options of attn_fwd_ex.  Zero-initialise and set what is needed. */
 typedef struct {

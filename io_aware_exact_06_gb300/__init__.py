@@ -78,7 +78,7 @@ def lib() -> ctypes.CDLL:
         L.attn_fp8_quantize_v.restype = i
         L.attn_fwd_noalloc.argtypes = sig
         L.attn_fwd_noalloc.restype = i
-        L.attn_fwd_host.argtypes = sig[:11] + [vp]
+        L.attn_fwd_host.argtypes = sig
         L.attn_fwd_host.restype = i
         L.attn_last_device_error.argtypes = [vp]
         L.attn_last_device_error.restype = i
@@ -122,11 +122,12 @@ def attn_fwd(q, k, v, o, lse, B: int, H: int, N: int, d: int, scale: float, caus
 
 
 def attn_fwd_host(q, k, v, o, lse, B: int, H: int, N: int, d: int, scale: float, causal: bool,
-                  stream=None) -> int:
+                  cu_seqlens=None, stream=None) -> int:
     """The C call ``attn_fwd_host``: attn_fwd on host buffers (CPU tensors,
-    page-locked for overlapped copies, or addresses); dense [B, N, H, d]."""
+    page-locked for overlapped copies, or addresses), cu_seqlens included."""
     st = lib().attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(N),
-                             int(d), float(scale), int(bool(causal)), _stream(stream))
+                             int(d), float(scale), int(bool(causal)), _ptr(cu_seqlens),
+                             _stream(stream))
     if st != ATTN_OK:
         raise AttnError(st)
     return st

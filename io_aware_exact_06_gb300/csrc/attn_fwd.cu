@@ -369,12 +369,15 @@ int host_pipe(int dev, attn_stream_t stream, size_t slot_bytes, HostPipe** out) 
   return ATTN_OK;
 }
 
-// Heads per group: about 32 MB of Q, K, V per group, and at least two groups
-// when there are two heads (so that copies and attention overlap); groups as
-// even as the head count allows.
-int host_head_group(int B, int H, int N, int d) {
-  const size_t head_bytes = 3 * (size_t)B * N * d * 2;
-  int64_t hg = std::max<int64_t>(1, (int64_t)((32ull << 20) / std::max<size_t>(head_bytes, 1)));
+// Heads per group: about 32 MB of Q, K, V per group but at least two heads
+// (groups of one head measured 1.3-1.9x slower end to end on the long causal,
+// stress and packed workloads: a launch of one head holds too few work units
+// for the SMs, and every group adds launches and hand-offs), and at least two
+// groups when there are two heads (so that copies and attention overlap);
+// groups as even as the head count allows.
+int host_head_group(int64_t tokens, int H, int d) {
+  const size_t head_bytes = 3 * (size_t)tokens * d * 2;
+  int64_t hg = std::max<int64_t>(2, (int64_t)((32ull << 20) / std::max<size_t>(head_bytes, 1)));
   if (H >= 2) hg = std::min<int64_t>(hg, (H + 1) / 2);
   hg = std::min<int64_t>(hg, H);
   const int64_t groups = (H + hg - 1) / hg;
@@ -385,7 +388,7 @@ int host_head_group(int B, int H, int N, int d) {
 
 extern "C" int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
                              int B, int H, int N, int d, float scale, int causal,
-                             attn_stream_t stream) {
+                             const int32_t* cu_seqlens, attn_stream_t stream) {
   if (B < 0 || H < 0 || N < 0) return ATTN_ERR_SHAPE;
   if (d != 64 && d != 128) return ATTN_ERR_HEADDIM;
   if (!std::isfinite(scale) || scale < 0.0f) return ATTN_ERR_SCALE;
@@ -393,16 +396,29 @@ extern "C" int attn_fwd_host(const void* q, const void* k, const void* v, void* 
   if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL;
   if ((int64_t)B * N > INT32_MAX - 2 * attn::kBN || (int64_t)H * d > (1 << 20) || H > 65535)
     return ATTN_ERR_SHAPE;
-  const int hg = host_head_group(B, H, N, d);
-  const size_t tile = round_up_256((size_t)B * N * hg * d * 2);  // one [B, N, hg, d] bf16 tile
-  const size_t lse_bytes = round_up_256((size_t)B * hg * N * sizeof(float));
+  // packed batches: the offsets are host memory, so they are checked here,
+  // before any copy reads cu_seqlens[B] tokens of the caller's buffers
+  int64_t tokens = (int64_t)B * N;
+  if (cu_seqlens) {
+    if (cu_seqlens[0] != 0) return ATTN_ERR_SEQLENS;
+    for (int b = 0; b < B; ++b) {
+      const int64_t len = (int64_t)cu_seqlens[b + 1] - cu_seqlens[b];
+      if (len < 0 || len > N) return ATTN_ERR_SEQLENS;
+    }
+    tokens = cu_seqlens[B];
+    if (tokens == 0) return ATTN_OK;
+  }
+  const int hg = host_head_group(tokens, H, d);
+  const size_t tile = round_up_256((size_t)tokens * hg * d * 2);  // [tokens, hg, d] bf16
+  const size_t lse_bytes = round_up_256((size_t)tokens * hg * sizeof(float));
+  const size_t cu_bytes = cu_seqlens ? round_up_256((size_t)(B + 1) * sizeof(int32_t)) : 0;
 
   std::lock_guard<std::mutex> lock(g_host_mu);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
   HostPipe* hp = nullptr;
-  int st = host_pipe(dev, stream, 4 * tile + lse_bytes, &hp);
+  int st = host_pipe(dev, stream, 4 * tile + lse_bytes + cu_bytes, &hp);
   if (st != ATTN_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const size_t row = (size_t)H * d * 2;  // bytes of one token's heads
@@ -422,33 +438,42 @@ extern "C" int attn_fwd_host(const void* q, const void* k, const void* v, void* 
     uint8_t* base = hp->slot[j];
     uint8_t *dq = base, *dk = base + tile, *dv = base + 2 * tile, *dout = base + 3 * tile;
     float* dlse = reinterpret_cast<float*>(base + 4 * tile);
+    int32_t* dcu = cu_seqlens ? reinterpret_cast<int32_t*>(base + 4 * tile + lse_bytes) : nullptr;
     // Q, K, V of the group into slot j, once group g - 2's attention has read it
     if (g >= 2 && (e = cudaStreamWaitEvent(hp->in, hp->comp_done[j], 0)) != cudaSuccess)
       return cuda_fail(e);
     const uint8_t* srcs[3] = {qh, kh, vh};
     uint8_t* dsts[3] = {dq, dk, dv};
     for (int t = 0; t < 3; ++t)
-      if ((e = cudaMemcpy2DAsync(dsts[t], w, srcs[t] + (size_t)h0 * d * 2, row, w, (size_t)B * N,
+      if ((e = cudaMemcpy2DAsync(dsts[t], w, srcs[t] + (size_t)h0 * d * 2, row, w, (size_t)tokens,
                                  cudaMemcpyDefault, hp->in)) != cudaSuccess)
         return cuda_fail(e);
+    if (dcu && (e = cudaMemcpyAsync(dcu, cu_seqlens, (size_t)(B + 1) * sizeof(int32_t),
+                                    cudaMemcpyDefault, hp->in)) != cudaSuccess)
+      return cuda_fail(e);
     if ((e = cudaEventRecord(hp->in_done[j], hp->in)) != cudaSuccess) return cuda_fail(e);
     // attention of the group on the caller's stream, once its inputs are in
     // and group g - 2's outputs have left slot j
     if ((e = cudaStreamWaitEvent(s, hp->in_done[j], 0)) != cudaSuccess) return cuda_fail(e);
     if (g >= 2 && (e = cudaStreamWaitEvent(s, hp->out_done[j], 0)) != cudaSuccess) return cuda_fail(e);
-    st = attn_fwd_impl(dq, dk, dv, dout, dlse, B, hn, N, d, scale, causal, -1, -1, nullptr, stream,
+    st = attn_fwd_impl(dq, dk, dv, dout, dlse, B, hn, N, d, scale, causal, -1, -1, dcu, stream,
                        nullptr);
     if (st != ATTN_OK) return st;
     if ((e = cudaEventRecord(hp->comp_done[j], s)) != cudaSuccess) return cuda_fail(e);
-    // O and the LSE of the group back to the host buffers
+    // O and the LSE of the group back to the host buffers (LSE: dense [B, H,
+    // N], the group's [B, hn, N] block; packed [H, tokens], its rows h0 ..)
     if ((e = cudaStreamWaitEvent(hp->out, hp->comp_done[j], 0)) != cudaSuccess) return cuda_fail(e);
-    if ((e = cudaMemcpy2DAsync(oh + (size_t)h0 * d * 2, row, dout, w, w, (size_t)B * N,
+    if ((e = cudaMemcpy2DAsync(oh + (size_t)h0 * d * 2, row, dout, w, w, (size_t)tokens,
                                cudaMemcpyDefault, hp->out)) != cudaSuccess)
       return cuda_fail(e);
-    if ((e = cudaMemcpy2DAsync(lse + (size_t)h0 * N, (size_t)H * N * sizeof(float), dlse,
-                               (size_t)hn * N * sizeof(float), (size_t)hn * N * sizeof(float), B,
-                               cudaMemcpyDefault, hp->out)) != cudaSuccess)
-      return cuda_fail(e);
+    if (cu_seqlens)
+      e = cudaMemcpyAsync(lse + (size_t)h0 * tokens, dlse, (size_t)hn * tokens * sizeof(float),
+                          cudaMemcpyDefault, hp->out);
+    else
+      e = cudaMemcpy2DAsync(lse + (size_t)h0 * N, (size_t)H * N * sizeof(float), dlse,
+                            (size_t)hn * N * sizeof(float), (size_t)hn * N * sizeof(float), B,
+                            cudaMemcpyDefault, hp->out);
+    if (e != cudaSuccess) return cuda_fail(e);
     if ((e = cudaEventRecord(hp->out_done[j], hp->out)) != cudaSuccess) return cuda_fail(e);
   }
   // later work on the caller's stream sees O and the LSE in the host buffers

@@ -95,10 +95,10 @@ def test_empty_problem_is_a_noop(lib, zero):
 ])
 def test_host_argument_errors(lib, args, status):
     a = dict(q=BUF, k=BUF, v=BUF, o=BUF, lse=BUF, B=2, H=4, N=256, d=128, scale=0.1,
-             causal=1, stream=None)
+             causal=1, cu=None, stream=None)
     a.update(args)
     st = lib.attn_fwd_host(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"],
-                           a["d"], a["scale"], a["causal"], a["stream"])
+                           a["d"], a["scale"], a["causal"], a["cu"], a["stream"])
     assert st == status
 
 
@@ -107,7 +107,22 @@ def test_host_empty_problem_is_a_noop(lib, zero):
     a = dict(B=2, H=4, N=256)
     a[zero] = 0
     assert lib.attn_fwd_host(None, None, None, None, None, a["B"], a["H"], a["N"], 128, 0.125, 1,
-                             None) == 0
+                             None, None) == 0
+
+
+# host cu_seqlens is checked on the host before anything is copied
+@pytest.mark.parametrize("cu,status", [
+    ([1, 100, 200], -8),    # does not start at 0
+    ([0, 100, 50], -8),     # decreasing
+    ([0, 300, 400], -8),    # a length above N = 256
+    ([0, 0, 0], 0),         # no tokens: nothing to do
+])
+def test_host_cu_seqlens_checked_on_the_host(lib, cu, status):
+    import numpy as np
+    arr = np.asarray(cu, dtype=np.int32)
+    st = lib.attn_fwd_host(BUF, BUF, BUF, BUF, BUF, 2, 4, 256, 128, 0.1, 1,
+                           arr.ctypes.data, None)
+    assert st == status
 
 
 def test_binding_raises_on_error(lib):

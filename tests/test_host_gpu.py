@@ -5,9 +5,9 @@ oracle.
 Every row is computed by the same kernel with the same arithmetic whatever
 the number of heads in a launch, so O and the LSE must equal attn_fwd's bit
 for bit.  The cases give one group (H = 1), two groups, uneven groups (H = 7)
-and more groups than the two workspace slots (H = 12 at B = 4, N = 4096,
-d = 128: three heads per group), pinned and pageable host memory, the default
-and a created stream."""
+and more groups than the two workspace slots (H = 12: six groups of two
+heads), dense and packed batches, pinned and pageable host memory, the
+default and a created stream."""
 import numpy as np
 import pytest
 
@@ -51,7 +51,7 @@ def run_both(dev, B, N, H, d, causal, pinned, seed, stream=None):
     lse_h = torch.full((B, H, N), float("nan"), dtype=torch.float32)
     if pinned:
         o_h, lse_h = o_h.pin_memory(), lse_h.pin_memory()
-    fa.attn_fwd_host(q_h, k_h, v_h, o_h, lse_h, B, H, N, d, scale, causal, stream)
+    fa.attn_fwd_host(q_h, k_h, v_h, o_h, lse_h, B, H, N, d, scale, causal, stream=stream)
     assert fa.attn_last_device_error(stream) == 0
     return o.cpu(), lse.cpu(), o_h, lse_h
 
@@ -67,6 +67,33 @@ def test_bit_identical_to_attn_fwd(dev, B, N, H, d, causal, pinned):
     o, lse, o_h, lse_h = run_both(dev, B, N, H, d, causal, pinned, seed=B * 100 + H)
     assert bool((o_h.view(torch.int16) == o.view(torch.int16)).all())
     assert bool((lse_h == lse).all())
+
+
+@pytest.mark.parametrize("lens,H,d,causal", [([300, 0, 1000, 129, 640], 5, 128, True),
+                                             ([64, 2048, 1], 12, 64, False)])
+@pytest.mark.parametrize("pinned", [True, False])
+def test_packed_bit_identical_to_attn_fwd(dev, lens, H, d, causal, pinned):
+    import torch
+    import io_aware_exact_06_gb300 as fa
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    total, B, N = int(cu[-1]), len(lens), max(lens)
+    q_h, k_h, v_h = host_inputs(len(lens) * 10 + H, 1, total, H, d, pinned)
+    q_h, k_h, v_h = (x.reshape(total, H, d) for x in (q_h, k_h, v_h))
+    scale = d ** -0.5
+    q, k, v = (x.to(dev) for x in (q_h, k_h, v_h))
+    o = torch.empty_like(q)
+    lse = torch.empty((H, total), dtype=torch.float32, device=dev)
+    fa.attn_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, torch.from_numpy(cu).to(dev))
+    assert fa.attn_last_device_error() == 0
+    o_h = torch.full((total, H, d), float("nan"), dtype=torch.bfloat16)
+    lse_h = torch.full((H, total), float("nan"), dtype=torch.float32)
+    cu_h = torch.from_numpy(cu)
+    if pinned:
+        o_h, lse_h, cu_h = o_h.pin_memory(), lse_h.pin_memory(), cu_h.pin_memory()
+    fa.attn_fwd_host(q_h, k_h, v_h, o_h, lse_h, B, H, N, d, scale, causal, cu_h)
+    assert fa.attn_last_device_error() == 0
+    assert bool((o_h.view(torch.int16) == o.cpu().view(torch.int16)).all())
+    assert bool((lse_h == lse.cpu()).all())
 
 
 def test_created_stream_and_repeated_calls(dev):
