@@ -72,6 +72,27 @@ int attn_fwd_fp8(const void *q, const void *k, const void *v, void *o, float *ls
                  int N, int d, float scale, int causal, const int32_t *cu_seqlens,
                  const int8_t *signs, attn_stream_t stream);
 
+/*
+ * attn_fwd_fp8_codes: the FP8 attention step of attn_fwd_fp8 alone, on codes
+ * and scales the caller made with attn_fp8_quantize_qk and
+ * attn_fp8_quantize_v, so that keys and values quantised once (a key/value
+ * cache) serve many query batches.  d must be 128 (the quantisers' code rows
+ * are then the 128-byte rows the attention kernel reads; d = 64 returns
+ * ATTN_ERR_HEADDIM).  q8, k8: [B, N, H, 128] e4m3 (packed [total, H, 128]);
+ * sq, sk: [B, H, T] fp32; vt: [B, H, 128, Np] e4m3; sv: [B, H] fp32 (the
+ * quantisers' layouts).  rotated: nonzero when Q and K were quantised with
+ * the same signs (the rotated logits carry the factor d of the unnormalised
+ * rotation, divided out here); zero when both were quantised without.
+ * o, lse, scale, causal, cu_seqlens: as for attn_fwd_fp8.  Alignment: q8,
+ * k8, vt, o 16 bytes; the scales and lse 4 bytes.  Same ordering, errors
+ * and worklist workspace as attn_fwd_fp8; O and the LSE equal attn_fwd_fp8's
+ * on the same inputs bit for bit.
+ */
+int attn_fwd_fp8_codes(const uint8_t *q8, const float *sq, const uint8_t *k8, const float *sk,
+                       const uint8_t *vt, const float *sv, void *o, float *lse, int B, int H,
+                       int N, int d, float scale, int causal, int rotated,
+                       const int32_t *cu_seqlens, attn_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -14,7 +14,7 @@ import os
 
 from . import build as _build
 
-__all__ = ["attn_fwd", "attn_bwd", "attn_bwd_window", "attn_fwd_fp8", "attn_fp8_quantize_qk", "attn_fp8_quantize_v",
+__all__ = ["attn_fwd", "attn_bwd", "attn_bwd_window", "attn_fwd_fp8", "attn_fwd_fp8_codes", "attn_fp8_quantize_qk", "attn_fp8_quantize_v",
            "attn_fwd_ex", "attn_fwd_host", "attn_fwd_noalloc", "attn_fwd_window", "attn_fwd_kvsplit", "attn_fwd_decode", "attn_last_device_error", "attn_last_error_site",
            "attn_status_string", "AttnError", "AttnFwdOptions", "lib", "forward", "backward", "decode",
            "EXPORTED_SYMBOLS"]
@@ -23,7 +23,7 @@ __all__ = ["attn_fwd", "attn_bwd", "attn_bwd_window", "attn_fwd_fp8", "attn_fp8_
 EXPORTED_SYMBOLS = ("attn_fwd", "attn_fwd_ex", "attn_fwd_host", "attn_fwd_decode", "attn_last_device_error", "attn_last_error_site",
                     "attn_last_cuda_error", "attn_status_string", "attn_fwd_noalloc",
                     "attn_fwd_window", "attn_fwd_kvsplit", "attn_bwd", "attn_bwd_window",
-                    "attn_fwd_fp8",
+                    "attn_fwd_fp8", "attn_fwd_fp8_codes",
                     "attn_fp8_quantize_qk", "attn_fp8_quantize_v")
 
 ATTN_OK = 0
@@ -72,6 +72,8 @@ def lib() -> ctypes.CDLL:
         L.attn_bwd_window.restype = i
         L.attn_fwd_fp8.argtypes = sig[:11] + [vp, vp, vp]
         L.attn_fwd_fp8.restype = i
+        L.attn_fwd_fp8_codes.argtypes = [vp] * 8 + [i, i, i, i, ctypes.c_float, i, i, vp, vp]
+        L.attn_fwd_fp8_codes.restype = i
         L.attn_fp8_quantize_qk.argtypes = [vp, vp, vp, i, i, i, i, vp, vp, vp]
         L.attn_fp8_quantize_qk.restype = i
         L.attn_fp8_quantize_v.argtypes = [vp, vp, vp, i, i, i, i, vp, vp]
@@ -240,6 +242,19 @@ def attn_fwd_fp8(q, k, v, o, lse, B: int, H: int, N: int, d: int, scale: float, 
         raise AttnError(st, "attn_fwd_fp8")
     return st
 
+
+def attn_fwd_fp8_codes(q8, sq, k8, sk, vt, sv, o, lse, B: int, H: int, N: int, d: int,
+                       scale: float, causal: bool, rotated: bool, cu_seqlens=None,
+                       stream=None) -> int:
+    """The C call ``attn_fwd_fp8_codes``: the FP8 attention on codes and scales
+    from attn_fp8_quantize_qk / attn_fp8_quantize_v (d = 128)."""
+    st = lib().attn_fwd_fp8_codes(_ptr(q8), _ptr(sq), _ptr(k8), _ptr(sk), _ptr(vt), _ptr(sv),
+                                  _ptr(o), _ptr(lse), int(B), int(H), int(N), int(d),
+                                  float(scale), int(bool(causal)), int(bool(rotated)),
+                                  _ptr(cu_seqlens), _stream(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_fp8_codes")
+    return st
 
 def attn_fp8_quantize_qk(x, codes, scales, B: int, H: int, N: int, d: int, signs=None,
                          cu_seqlens=None, stream=None) -> int:

@@ -1128,6 +1128,57 @@ extern "C" int attn_fp8_quantize_v(const void* v, uint8_t* codes_t, float* scale
   return launch_quant_v(v, codes_t, scale, amax, B, H, N, d, cu_seqlens, list, s);
 }
 
+namespace {
+
+// The FP8 attention kernel on codes and scales already in device memory: Q
+// and K codes in rows of 128 bytes, V codes [B*H][d][Np]; list: the FP8
+// worklist (packed batches) and unit counters.
+int launch_fp8_attention(EncodeTiledFn enc, DeviceState* ds, int* list, const uint8_t* q8,
+                         const float* sq, const uint8_t* k8, const float* sk, const uint8_t* vt,
+                         const float* sv, void* o, float* lse, int B, int H, int N, int d,
+                         float scale, int causal, bool rotated, const int32_t* cu_seqlens,
+                         cudaStream_t s) {
+  const int64_t tokens = (int64_t)B * N;
+  const int64_t T = (N + attn::kBM - 1) / attn::kBM;
+  const int64_t np = T * attn::kBN;
+  const int64_t bh = (int64_t)B * H;
+  int st;
+  CUtensorMap mq, mk, mvt;
+  if ((st = make_map_fp8_rows(enc, &mq, q8, tokens, H)) != ATTN_OK) return st;
+  if ((st = make_map_fp8_rows(enc, &mk, k8, tokens, H)) != ATTN_OK) return st;
+  if ((st = make_map_fp8_vt(enc, &mvt, vt, bh, np, d)) != ATTN_OK) return st;
+  attn::Fp8Params p{};
+  p.o = reinterpret_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.sq = sq;
+  p.sk = sk;
+  p.sv = sv;
+  p.err = ds->err;
+  p.sched = list + 1;
+  p.cu_seqlens = cu_seqlens;
+  p.work = list + 4;
+  p.num_entries = list;
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.T = (int)T;
+  p.causal = causal ? 1 : 0;
+  p.scale = scale;
+  // the unnormalised rotation multiplies Q K^T by d
+  p.logit_log2 = (float)((double)scale * 1.4426950408889634 / (rotated ? (double)d : 1.0));
+  p.timeout_ns = 2000000000ull;
+  const int64_t units = bh * ((N + attn::kUnitRows - 1) / attn::kUnitRows);
+  const int grid = cu_seqlens ? ds->sms : (int)std::min<int64_t>(units, ds->sms);
+  if (d == 64)
+    attn::attn_fp8_kernel<64><<<grid, attn::kThreads, attn::kFp8SmemBytes, s>>>(mq, mk, mvt, p);
+  else
+    attn::attn_fp8_kernel<128><<<grid, attn::kThreads, attn::kFp8SmemBytes, s>>>(mq, mk, mvt, p);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+}  // namespace
+
 extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
                             int B, int H, int N, int d, float scale, int causal,
                             const int32_t* cu_seqlens, const int8_t* signs,
@@ -1178,36 +1229,36 @@ extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o
     return st;
   if ((st = launch_quant_v(v, vt, sv, amax, B, H, N, d, cu_seqlens, list, s)) != ATTN_OK) return st;
 
-  CUtensorMap mq, mk, mvt;
-  if ((st = make_map_fp8_rows(enc, &mq, q8, tokens, H)) != ATTN_OK) return st;
-  if ((st = make_map_fp8_rows(enc, &mk, k8, tokens, H)) != ATTN_OK) return st;
-  if ((st = make_map_fp8_vt(enc, &mvt, vt, bh, np, d)) != ATTN_OK) return st;
-  attn::Fp8Params p{};
-  p.o = reinterpret_cast<__nv_bfloat16*>(o);
-  p.lse = lse;
-  p.sq = sq;
-  p.sk = sk;
-  p.sv = sv;
-  p.err = ds->err;
-  p.sched = list + 1;
-  p.cu_seqlens = cu_seqlens;
-  p.work = list + 4;
-  p.num_entries = list;
-  p.B = B;
-  p.H = H;
-  p.N = N;
-  p.T = (int)T;
-  p.causal = causal ? 1 : 0;
-  p.scale = scale;
-  // the unnormalised rotation multiplies Q K^T by d
-  p.logit_log2 = (float)((double)scale * 1.4426950408889634 / (signs ? (double)d : 1.0));
-  p.timeout_ns = 2000000000ull;
-  const int64_t units = bh * ((N + attn::kUnitRows - 1) / attn::kUnitRows);
-  const int grid = cu_seqlens ? ds->sms : (int)std::min<int64_t>(units, ds->sms);
-  if (d == 64)
-    attn::attn_fp8_kernel<64><<<grid, attn::kThreads, attn::kFp8SmemBytes, s>>>(mq, mk, mvt, p);
-  else
-    attn::attn_fp8_kernel<128><<<grid, attn::kThreads, attn::kFp8SmemBytes, s>>>(mq, mk, mvt, p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
-  return ATTN_OK;
+  return launch_fp8_attention(enc, ds, list, q8, sq, k8, sk, vt, sv, o, lse, B, H, N, d, scale,
+                              causal, signs != nullptr, cu_seqlens, s);
+}
+
+extern "C" int attn_fwd_fp8_codes(const uint8_t* q8, const float* sq, const uint8_t* k8,
+                                  const float* sk, const uint8_t* vt, const float* sv, void* o,
+                                  float* lse, int B, int H, int N, int d, float scale, int causal,
+                                  int rotated, const int32_t* cu_seqlens, attn_stream_t stream) {
+  int st = fp8_check(B, H, N, d);
+  if (st != ATTN_OK) return st;
+  // (d = 64: the quantisers' code rows are 64 bytes, the kernel reads 128)
+  if (d != attn::kFp8D) return ATTN_ERR_HEADDIM;
+  if (!std::isfinite(scale) || scale < 0.0f) return ATTN_ERR_SCALE;
+  if (B == 0 || H == 0 || N == 0) return ATTN_OK;
+  if (!q8 || !sq || !k8 || !sk || !vt || !sv || !o || !lse) return ATTN_ERR_NULL;
+  if (!aligned(q8, 16) || !aligned(k8, 16) || !aligned(vt, 16) || !aligned(o, 16) ||
+      !aligned(sq, 4) || !aligned(sk, 4) || !aligned(sv, 4) || !aligned(lse, 4))
+    return ATTN_ERR_ALIGN;
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  DeviceState* ds = nullptr;
+  if ((st = device_state(dev, &ds)) != ATTN_OK) return st;
+  EncodeTiledFn enc = nullptr;
+  if ((st = get_encode(&enc)) != ATTN_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int* list = nullptr;
+  if ((st = fp8_worklist(dev, stream, ds, cu_seqlens, B, N, causal ? 1 : 0, &list)) != ATTN_OK)
+    return st;
+  return launch_fp8_attention(enc, ds, list, q8, sq, k8, sk, vt, sv, o, lse, B, H, N, d, scale,
+                              causal, rotated != 0, cu_seqlens, s);
 }

@@ -125,6 +125,26 @@ def test_host_cu_seqlens_checked_on_the_host(lib, cu, status):
     assert st == status
 
 
+@pytest.mark.parametrize("args,status", [
+    (dict(d=64), -3),
+    (dict(d=96), -3),
+    (dict(B=-1), -2),
+    (dict(scale=float("nan")), -5),
+    (dict(q8=None), -1),
+    (dict(sv=None), -1),
+    (dict(vt=BUF + 8), -4),
+    (dict(sk=BUF + 2), -4),
+])
+def test_fp8_codes_argument_errors(lib, args, status):
+    a = dict(q8=BUF, sq=BUF, k8=BUF, sk=BUF, vt=BUF, sv=BUF, o=BUF, lse=BUF, B=2, H=4, N=256,
+             d=128, scale=0.1, causal=1, rotated=1, cu=None, stream=None)
+    a.update(args)
+    st = lib.attn_fwd_fp8_codes(a["q8"], a["sq"], a["k8"], a["sk"], a["vt"], a["sv"], a["o"],
+                                a["lse"], a["B"], a["H"], a["N"], a["d"], a["scale"], a["causal"],
+                                a["rotated"], a["cu"], a["stream"])
+    assert st == status
+
+
 def test_binding_raises_on_error(lib):
     with pytest.raises(fa.AttnError) as e:
         fa.attn_fwd(BUF, BUF, BUF, BUF, BUF, 1, 1, 128, 80, 0.1, False)

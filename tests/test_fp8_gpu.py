@@ -338,3 +338,49 @@ def test_fp8_invalid_cu_seqlens_reported(dev, bad):
                     128 ** -0.5, True, None, cu_dev(dev, cu_bad))
     assert fa.attn_last_device_error() == -8
     assert (o.float() == 7.0).all() and (lse == 7.0).all(), "nothing is written"
+
+
+# attn_fwd_fp8_codes: the attention step alone on the quantisers' outputs
+# (d = 128) gives attn_fwd_fp8's O and LSE bit for bit: the quantisers are
+# the same arithmetic (their codes are bit-exact against the oracle above)
+# and the attention kernel is the same launch.
+@pytest.mark.parametrize("packed", [False, True])
+@pytest.mark.parametrize("rotate", [False, True])
+@pytest.mark.parametrize("causal", [False, True])
+def test_codes_entry_matches_full_call(dev, packed, rotate, causal):
+    import torch
+    import io_aware_exact_06_gb300 as fa
+    d, H = 128, 3
+    lens = [300, 129, 1024, 1] if packed else [700, 700]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    B, N, total = len(lens), max(lens), int(cu[-1])
+    seed = 3700 + 10 * packed + 2 * rotate + causal
+    q = inputs.normal_bf16(seed, total * H * d).reshape(total, H, d)
+    k = inputs.normal_bf16(seed + 1, total * H * d).reshape(total, H, d)
+    v = inputs.normal_bf16(seed + 2, total * H * d).reshape(total, H, d)
+    sg = signs_of(seed + 3, d) if rotate else None
+    cu_d = torch.from_numpy(cu).to(dev) if packed else None
+    qd, kd, vd = to_dev(dev, q), to_dev(dev, k), to_dev(dev, v)
+    scale = d ** -0.5
+    lse_shape = (H, total) if packed else (B, H, N)
+    o1 = torch.empty((total, H, d), dtype=torch.bfloat16, device=dev)
+    l1 = torch.empty(lse_shape, dtype=torch.float32, device=dev)
+    fa.attn_fwd_fp8(qd, kd, vd, o1, l1, B, H, N, d, scale, causal, sg, cu_seqlens=cu_d)
+    T = -(-N // 128)
+    tok_rows = total if packed else B * N
+    q8 = torch.zeros((tok_rows, H, d), dtype=torch.uint8, device=dev)
+    k8 = torch.zeros_like(q8)
+    sq = torch.zeros((B, H, T), dtype=torch.float32, device=dev)
+    sk = torch.zeros_like(sq)
+    vt = torch.zeros((B, H, d, 128 * T), dtype=torch.uint8, device=dev)
+    sv = torch.zeros((B, H), dtype=torch.float32, device=dev)
+    fa.attn_fp8_quantize_qk(qd, q8, sq, B, H, N, d, sg, cu_seqlens=cu_d)
+    fa.attn_fp8_quantize_qk(kd, k8, sk, B, H, N, d, sg, cu_seqlens=cu_d)
+    fa.attn_fp8_quantize_v(vd, vt, sv, B, H, N, d, cu_seqlens=cu_d)
+    o2 = torch.full((total, H, d), float("nan"), dtype=torch.bfloat16, device=dev)
+    l2 = torch.full(lse_shape, float("nan"), dtype=torch.float32, device=dev)
+    fa.attn_fwd_fp8_codes(q8, sq, k8, sk, vt, sv, o2, l2, B, H, N, d, scale, causal, rotate,
+                          cu_seqlens=cu_d)
+    assert fa.attn_last_device_error() == 0
+    assert bool((o1.view(torch.int16) == o2.view(torch.int16)).all())
+    assert bool((l1 == l2).all())
