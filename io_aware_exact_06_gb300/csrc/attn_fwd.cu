@@ -430,6 +430,14 @@ extern "C" int attn_fwd_host(const void* q, const void* k, const void* v, void* 
   // previous call, which used the same slots)
   if ((e = cudaEventRecord(hp->start, s)) != cudaSuccess) return cuda_fail(e);
   if ((e = cudaStreamWaitEvent(hp->in, hp->start, 0)) != cudaSuccess) return cuda_fail(e);
+  // On an error past this point, later work on the caller's stream still
+  // waits for every copy already queued, so that the caller may release its
+  // buffers once the stream is idle; the error is returned.
+  auto fail_joined = [&](int status) {
+    if (cudaEventRecord(hp->done, hp->in) == cudaSuccess) cudaStreamWaitEvent(s, hp->done, 0);
+    if (cudaEventRecord(hp->done, hp->out) == cudaSuccess) cudaStreamWaitEvent(s, hp->done, 0);
+    return status;
+  };
   const int groups = (H + hg - 1) / hg;
   for (int g = 0; g < groups; ++g) {
     const int j = g & 1;
@@ -441,31 +449,36 @@ extern "C" int attn_fwd_host(const void* q, const void* k, const void* v, void* 
     int32_t* dcu = cu_seqlens ? reinterpret_cast<int32_t*>(base + 4 * tile + lse_bytes) : nullptr;
     // Q, K, V of the group into slot j, once group g - 2's attention has read it
     if (g >= 2 && (e = cudaStreamWaitEvent(hp->in, hp->comp_done[j], 0)) != cudaSuccess)
-      return cuda_fail(e);
+      return fail_joined(cuda_fail(e));
     const uint8_t* srcs[3] = {qh, kh, vh};
     uint8_t* dsts[3] = {dq, dk, dv};
     for (int t = 0; t < 3; ++t)
       if ((e = cudaMemcpy2DAsync(dsts[t], w, srcs[t] + (size_t)h0 * d * 2, row, w, (size_t)tokens,
                                  cudaMemcpyDefault, hp->in)) != cudaSuccess)
-        return cuda_fail(e);
+        return fail_joined(cuda_fail(e));
     if (dcu && (e = cudaMemcpyAsync(dcu, cu_seqlens, (size_t)(B + 1) * sizeof(int32_t),
                                     cudaMemcpyDefault, hp->in)) != cudaSuccess)
-      return cuda_fail(e);
-    if ((e = cudaEventRecord(hp->in_done[j], hp->in)) != cudaSuccess) return cuda_fail(e);
+      return fail_joined(cuda_fail(e));
+    if ((e = cudaEventRecord(hp->in_done[j], hp->in)) != cudaSuccess)
+      return fail_joined(cuda_fail(e));
     // attention of the group on the caller's stream, once its inputs are in
     // and group g - 2's outputs have left slot j
-    if ((e = cudaStreamWaitEvent(s, hp->in_done[j], 0)) != cudaSuccess) return cuda_fail(e);
-    if (g >= 2 && (e = cudaStreamWaitEvent(s, hp->out_done[j], 0)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaStreamWaitEvent(s, hp->in_done[j], 0)) != cudaSuccess)
+      return fail_joined(cuda_fail(e));
+    if (g >= 2 && (e = cudaStreamWaitEvent(s, hp->out_done[j], 0)) != cudaSuccess)
+      return fail_joined(cuda_fail(e));
     st = attn_fwd_impl(dq, dk, dv, dout, dlse, B, hn, N, d, scale, causal, -1, -1, dcu, stream,
                        nullptr);
-    if (st != ATTN_OK) return st;
-    if ((e = cudaEventRecord(hp->comp_done[j], s)) != cudaSuccess) return cuda_fail(e);
+    if (st != ATTN_OK) return fail_joined(st);
+    if ((e = cudaEventRecord(hp->comp_done[j], s)) != cudaSuccess)
+      return fail_joined(cuda_fail(e));
     // O and the LSE of the group back to the host buffers (LSE: dense [B, H,
     // N], the group's [B, hn, N] block; packed [H, tokens], its rows h0 ..)
-    if ((e = cudaStreamWaitEvent(hp->out, hp->comp_done[j], 0)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaStreamWaitEvent(hp->out, hp->comp_done[j], 0)) != cudaSuccess)
+      return fail_joined(cuda_fail(e));
     if ((e = cudaMemcpy2DAsync(oh + (size_t)h0 * d * 2, row, dout, w, w, (size_t)tokens,
                                cudaMemcpyDefault, hp->out)) != cudaSuccess)
-      return cuda_fail(e);
+      return fail_joined(cuda_fail(e));
     if (cu_seqlens)
       e = cudaMemcpyAsync(lse + (size_t)h0 * tokens, dlse, (size_t)hn * tokens * sizeof(float),
                           cudaMemcpyDefault, hp->out);
@@ -473,11 +486,12 @@ extern "C" int attn_fwd_host(const void* q, const void* k, const void* v, void* 
       e = cudaMemcpy2DAsync(lse + (size_t)h0 * N, (size_t)H * N * sizeof(float), dlse,
                             (size_t)hn * N * sizeof(float), (size_t)hn * N * sizeof(float), B,
                             cudaMemcpyDefault, hp->out);
-    if (e != cudaSuccess) return cuda_fail(e);
-    if ((e = cudaEventRecord(hp->out_done[j], hp->out)) != cudaSuccess) return cuda_fail(e);
+    if (e != cudaSuccess) return fail_joined(cuda_fail(e));
+    if ((e = cudaEventRecord(hp->out_done[j], hp->out)) != cudaSuccess)
+      return fail_joined(cuda_fail(e));
   }
   // later work on the caller's stream sees O and the LSE in the host buffers
-  if ((e = cudaEventRecord(hp->done, hp->out)) != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaEventRecord(hp->done, hp->out)) != cudaSuccess) return fail_joined(cuda_fail(e));
   if ((e = cudaStreamWaitEvent(s, hp->done, 0)) != cudaSuccess) return cuda_fail(e);
   return ATTN_OK;
 }
