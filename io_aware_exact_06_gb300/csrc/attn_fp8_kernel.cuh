@@ -580,7 +580,7 @@ __device__ __forceinline__ void fp8_mma_loop(const Fp8Params& p, SharedState& ss
     return fp8_wait(ss, kBarKV + pos % kFp8Stages, (pos / kFp8Stages) & 1, p, 210);
   };
   auto release = [&](uint32_t pos) { mma_commit(bar_addr(ss, kBarKV + kFp8Stages + pos % kFp8Stages)); };
-  // TMEM: S_g at 128 g (P_g over its first 32 columns), O_g at 256 + 128 g
+  // TMEM: S_g at 128 g (P_g over its first 32 columns), O_g at 256 + D g
   uint32_t uslot = 0;
   for (;;) {
     int u;
