@@ -732,7 +732,7 @@ __device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss
       pair_sync(g, quadrant);
       const float mx = fmaxf(mine, ss.row_max[j & 1][g][half ^ 1][trow]);
       const float m_new = fmaxf(m_used, mx);
-      // O correction decision: only when the row max grew by more than 2^8
+      // O correction decision: only when the row max grew by more than 2^16
       // (warp-uniform; the partner warp holds the same rows and decides alike)
       // (a row whose keys so far were all hidden has O = 0 and l = 0: its
       // first visible key sets the reference without a rescale)
