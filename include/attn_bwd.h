@@ -15,7 +15,11 @@
  * taken to carry no gradient of its own.
  *
  * Numerics: bf16 inputs, fp32 accumulation; P and dS rounded to bf16 before
- * their products; dQ, dK, dV written as bf16 (round to nearest even).
+ * their products; dQ, dK, dV written as bf16 (round to nearest even).  D_i =
+ * dO_i.O_i uses the forward's bf16 O, so on a row where one key carries
+ * nearly all of P, dS = P (dP - D) is a difference of nearly equal terms and
+ * keeps the bf16 rounding of O (about 2^-9 |dO_i| |v_j|): dQ_i and dK_j of
+ * such rows have that absolute error where their exact values are near 0.
  *
  * Only sm_103 devices; device pointers; asynchronous on `stream`; argument
  * errors are reported synchronously before anything is launched.  Status
