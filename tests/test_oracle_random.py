@@ -88,3 +88,75 @@ def test_oracle_gradients_match_autograd(lens, H, d, causal, wl, wr, scale, seed
             ref = ref.numpy()
             err = np.max(np.abs(got - ref) / np.maximum(1.0, np.abs(ref)))
             assert err <= 1e-11, (s, h, name, err)
+
+
+def _e4m3_grid():
+    """(value, code) of every non-negative finite e4m3 code, from the bit fields."""
+    out = []
+    for c in range(128):
+        e, m = (c >> 3) & 15, c & 7
+        if e == 15 and m == 7:
+            continue
+        out.append((m * 2.0 ** -9 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7), c))
+    return sorted(out)
+
+
+_GRID = _e4m3_grid()
+
+
+def _nearest_e4m3(y):
+    """Nearest e4m3 code by exhaustive search, ties to the even code, beyond
+    448 saturating at 448 (y fp32)."""
+    vals = np.array([v for v, _ in _GRID])
+    codes = np.array([c for _, c in _GRID], dtype=np.uint8)
+    a = np.minimum(np.abs(y.astype(np.float64)), 448.0)
+    dist = np.abs(a[..., None] - vals)
+    best = dist.min(axis=-1, keepdims=True)
+    cand = dist == best
+    # among equally near codes the even one
+    even = cand & ((codes & 1) == 0)
+    idx = np.where(even.any(axis=-1), even.argmax(axis=-1), cand.argmax(axis=-1))
+    c = codes[idx]
+    return np.where((y < 0) & (c != 0), c | 0x80, c).astype(np.uint8)
+
+
+@settings(max_examples=30, deadline=None)
+@given(B=st.integers(1, 2), N=st.integers(1, 300), H=st.integers(1, 2),
+       d=st.sampled_from([8, 64]), rotate=st.booleans(),
+       std=st.sampled_from([0.01, 1.0, 60.0]), zero_block=st.booleans(),
+       outlier=st.booleans(), seed=st.integers(0, 1 << 20))
+def test_fp8_quantize_matches_exhaustive_encoder(B, N, H, d, rotate, std, zero_block, outlier,
+                                                seed):
+    """Block scales and codes of the quantisation step against the definition:
+    scale = max|x| / 448 (1 for an all-zero block), codes = nearest e4m3 of
+    x * (448 / max|x|) in fp32, the last block pulled back to end at N; with
+    rotation the block is that of the Hadamard-rotated rows."""
+    rows = 128
+    xf = inputs.bf16_bits_to_f64(inputs.normal_bf16(seed, B * N * H * d, std)).reshape(B * N, H, d)
+    if outlier:
+        xf[:, :, seed % d] *= 30.0
+    if zero_block:
+        xf[:min(N, rows)] = 0.0
+    x = inputs.f64_to_bf16_bits(xf)
+    xf = inputs.bf16_bits_to_f64(x).astype(np.float32)
+    signs = np.where(inputs.splitmix64(seed + 5, 0, d) & np.uint64(1), -1, 1).astype(np.int8)
+    codes, scales = oracle.fp8_quantize(x, B, N, rows, rotate, signs if rotate else None)
+    nblk = -(-N // rows)
+    assert scales.shape == (B, H, nblk)
+    for b in range(B):
+        for h in range(H):
+            for t in range(nblk):
+                r0 = max(0, min(t * rows, N - rows))
+                blk = xf[b * N + r0:b * N + min(r0 + rows, N), h]
+                if rotate:
+                    blk = oracle.fwht_f32(blk, signs)
+                amax = np.float32(np.max(np.abs(blk)))
+                want_scale = np.float32(amax / np.float32(448.0)) if amax > 0 else np.float32(1.0)
+                assert scales[b, h, t] == want_scale, (b, h, t)
+                inv = np.float32(np.float32(448.0) / amax) if amax > 0 else np.float32(1.0)
+                want = _nearest_e4m3((blk * inv).astype(np.float32))
+                keep = np.arange(r0, r0 + len(blk)) >= t * rows
+                got = codes[b * N + r0:b * N + r0 + len(blk), h][keep]
+                assert np.array_equal(got & 0x7f, want[keep] & 0x7f), (b, h, t, rotate)
+                nz = (want[keep] & 0x7f) != 0
+                assert np.array_equal(got[nz], want[keep][nz]), (b, h, t, "sign")
