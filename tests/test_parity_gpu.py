@@ -90,6 +90,23 @@ def test_dense_lengths_not_multiple_of_tile(dev, N, causal):
     parity.compare(o, lse, wl, inputs.all_rows(wl.cu_seqlens, wl.H), f"dense N={N}")
 
 
+def test_causal_last_row_equals_full_row_at_full_size(dev):
+    # row L-1 sees every key under both masks: on the long workloads (same
+    # inputs, every sequence and head, full size) its causal and non-causal
+    # O and LSE agree bit for bit (same tiles, same order, nothing masked)
+    import torch
+    wc, wf = workload("long_causal"), workload("long_full")
+    assert wc.q is not None and np.array_equal(wc.q, wf.q) and np.array_equal(wc.v, wf.v)
+    oc, lc, st = parity.run_cuda(wc, dev)
+    assert st == 0
+    of, lf, st = parity.run_cuda(wf, dev)
+    assert st == 0
+    N = int(wc.seqlens()[0])
+    last = torch.tensor([b * N + N - 1 for b in range(wc.nseq)], device=oc.device)
+    assert torch.equal(oc[last].view(torch.int16), of[last].view(torch.int16))
+    assert torch.equal(lc[:, last], lf[:, last])
+
+
 def test_zero_q_gives_mean_of_visible_v_at_full_size(dev):
     """Q = 0: every logit is 0, so O_i is the mean of the visible V rows and
     LSE_i = log(#visible).  Checked on every row of the long causal workload."""
