@@ -251,6 +251,21 @@ __device__ __forceinline__ int kv_tile_start(const Unit& un, int j) {
   return min(j * kBN, un.Lk - kBN);
 }
 
+// KV tiles the lower query tile (group 0) of a unit visits: the unit's nkv,
+// except that under a causal mask (or a right window) the unit's last tile is
+// skipped when none of its keys not visited before is visible to any row of
+// the lower tile (its first new key lies past the tile's last row): its S
+// product, softmax and P V product would all be of masked keys.  The upper
+// tile (group 1) visits every tile of the unit.
+template <int kMode>
+__device__ __forceinline__ int lower_tiles(const FwdParams& p, const Unit& un) {
+  if (is_split_mode(kMode) || un.nkv < 2) return un.nkv;
+  const int last_row = q_tile_start(un, 0) + kBM - 1;
+  int k_hi = p.causal ? last_row : un.L - 1;
+  if (kMode == kModeWindow && p.wr >= 0) k_hi = min(k_hi, last_row + p.wr);
+  return k_hi < (un.kv0 + un.nkv - 1) * kBN ? un.nkv - 1 : un.nkv;
+}
+
 struct SharedState {
   uint64_t bars[kMaxBars];
   uint32_t tmem_base;
@@ -515,6 +530,8 @@ __device__ __forceinline__ void mma_loop(const FwdParams& p, SharedState& ss, ui
     }
     if (!wait_bar(ss, kBarQFull, units_done & 1, p, 11)) return;
     tc_fence_after();
+    // group 0 may skip the unit's last tile (lower_tiles); group 1 visits all
+    const int n0 = lower_tiles<kMode>(p, un);
     uint32_t posK = ring, posV = ring + 1;
     ring += 2;
     if (!wait_full(posK)) return;
@@ -535,21 +552,27 @@ __device__ __forceinline__ void mma_loop(const FwdParams& p, SharedState& ss, ui
         ring += 2;
       }
       if (!wait_full(posV)) return;
+      bool k_ready = false;
+#pragma unroll
       for (int g = 0; g < kQTiles; ++g) {
-        // P_g of tile j-1 is in TMEM (and O_g rescaled if needed)
-        if (!wait_bar(ss, kBarPFull + g, pcount[g] & 1, p, 12 + g)) return;
-        ++pcount[g];
-        tc_fence_after();
-        issue_pv<D>(tmem + C::col_o(g), tmem + C::col_s(g), slot_smem(posV), j > 1);
+        const int ng = g == 0 ? n0 : un.nkv;
+        if (j <= ng) {
+          // P_g of tile j-1 is in TMEM (and O_g rescaled if needed)
+          if (!wait_bar(ss, kBarPFull + g, pcount[g] & 1, p, 12 + g)) return;
+          ++pcount[g];
+          tc_fence_after();
+          issue_pv<D>(tmem + C::col_o(g), tmem + C::col_s(g), slot_smem(posV), j > 1);
+        }
         if (g == kQTiles - 1) release(posV);
-        if (more) {
-          if (g == 0) {
+        if (more && j < ng) {
+          if (!k_ready) {
             if (!wait_full(nextK)) return;
             tc_fence_after();
+            k_ready = true;
           }
           issue_qk<D>(tmem + C::col_s(g), q_smem[g], slot_smem(nextK));
           mma_commit(bar_addr(ss, kBarSFull + g));
-        } else {
+        } else if (j == ng) {
           mma_commit(bar_addr(ss, kBarOFull + g));
         }
       }
@@ -668,10 +691,11 @@ __device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss
     const int a0 = q_tile_start(un, tg);
     const int row = a0 + trow;                       // sequence-relative row of this thread
     const int nominal0 = un.qb * kUnitRows + tg * kBM;
+    const int n_tiles = g == 0 ? lower_tiles<kMode>(p, un) : un.nkv;
     float m_used = -INFINITY;
     float l = 0.f;     // sum of the fp32 probabilities (this half): the LSE
     float l_fix = 0.f; // rounding change of each tile's largest probability (this half)
-    for (int j = 0; j < un.nkv; ++j) {
+    for (int j = 0; j < n_tiles; ++j) {
       fail |= !__all_sync(0xffffffffu, wait_bar(ss, kBarSFull + g, scount & 1, p, 20 + g));
       ++scount;
       tc_fence_after();
@@ -711,9 +735,17 @@ __device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss
         klo = max(klo, jt * kBN);
         const int lo = klo - b0 - half * kHalfCols;
         const int hi = min(khi - b0, kBN - 1) - half * kHalfCols;
+        // The visible columns [lo, hi] of a row are one range: each 32-column
+        // chunk is masked from a bit mask of its visible columns.
 #pragma unroll
-        for (int c = 0; c < kHalfCols; ++c)
-          if (c < lo || c > hi) s[c] = -INFINITY;
+        for (int k = 0; k < kHalfCols / 32; ++k) {
+          const int lo_k = lo - 32 * k, hi_k = hi - 32 * k;
+          const bool none = hi_k < 0 || lo_k > 31 || hi_k < lo_k;
+          const uint32_t vis =
+              none ? 0u : (0xffffffffu >> (31 - min(hi_k, 31))) & (0xffffffffu << max(lo_k, 0));
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[32 * k + i] = (vis >> i) & 1u ? s[32 * k + i] : -INFINITY;
+        }
       }
       // row max: partial over this half (four 3-input max chains), then the
       // partner's half through shared memory

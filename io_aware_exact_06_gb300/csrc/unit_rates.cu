@@ -155,6 +155,83 @@ __global__ void __launch_bounds__(256, 1) mma_form_rate(long long* cycles, int n
   }
 }
 
+// A pair of SMs (a cluster of two CTAs) sharing each product: the even CTA
+// issues n products of 256 x 128 x 16 (cta_group::2) stepping through the
+// k-slices of a 128-deep tile as a paired attention kernel does.  A is each
+// CTA's own 128 rows, from shared memory (ts = 0, K-major) or from TMEM
+// (ts = 1); B is 64 of the 128 columns from each CTA's shared memory, K-major
+// (bmn = 0: S = Q K^T with 64 keys per CTA) or MN-major (bmn = 1: P V with 64
+// of the d columns per CTA).  contend = 1: warps 4-7 of both CTAs load and
+// store TMEM columns the products do not use.  256 TMEM columns per CTA:
+// D [0, 128), A [128, 192), traffic [192, 256).
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
+    mma_pair_rate(long long* cycles, int n, int ts, int bmn, int contend, int* err) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tmem_base;
+  const int tid = threadIdx.x, warp = tid / 32;
+  const uint32_t rank = cluster_ctarank();
+  for (int i = tid; i < 65536 / 4; i += 256) reinterpret_cast<uint32_t*>(smem)[i] = 0;
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  if (warp == 0) {
+    tmem_alloc_pair(smem_u32(&tmem_base), 256);
+    tmem_relinquish_pair();
+  }
+  if (tid == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  if (tid == 0) {
+    const long long t0 = clock64();
+    if (rank == 0) {
+      const uint32_t id = make_idesc_bf16(256, 128, bmn != 0);
+      const uint64_t a0 = make_sdesc(smem_u32(smem), 16, 1024, kSwizzle128B);
+      const uint64_t b0 = bmn ? make_sdesc(smem_u32(smem + 32768), 16384, 1024, kSwizzle128B)
+                              : make_sdesc(smem_u32(smem + 32768), 16, 1024, kSwizzle128B);
+      for (int i = 0; i < n; ++i) {
+        const int kk = i % 8;
+        const uint64_t aoff = (uint64_t)(((kk / 4) * 16384 + (kk % 4) * 32) >> 4);
+        // B: 64 rows per 64-column chunk when K-major (8 KB chunks), 16 keys
+        // (2048 bytes) per k-step when MN-major
+        const uint64_t boff = bmn ? (uint64_t)((kk * 2048) >> 4)
+                                  : (uint64_t)(((kk / 4) * 8192 + (kk % 4) * 32) >> 4);
+        if (ts)
+          mma_ts_pair(tmem, tmem + 128 + 8 * kk, b0 + boff, id, i > 0);
+        else
+          mma_ss_pair(tmem, a0 + aoff, b0 + boff, id, i > 0);
+      }
+      mma_commit_pair(smem_u32(&bar), 3);
+    }
+    // both CTAs: every product has finished writing this CTA's TMEM
+    if (!mbar_wait(smem_u32(&bar), 0, 1000000000ull)) atomicOr(err, 1);
+    cycles[blockIdx.x] = clock64() - t0;
+  } else if (contend && warp >= 4) {
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp % 4)) << 16);
+    uint32_t r[32];
+    for (int it = 0; it < 2 * n; ++it) {
+      tmem_ld_x32(lane_addr + 192, r);
+      tmem_ld_wait_x32(r);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) r[i] += 1u;
+      tmem_st_x32(lane_addr + 224, r);
+      tmem_st_wait();
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc_pair(tmem, 256);
+}
+
 bool check(cudaError_t e, const char* what) {
   if (e != cudaSuccess) {
     printf("{\"error\": \"%s: %s\"}\n", what, cudaGetErrorString(e));
@@ -218,6 +295,21 @@ int main() {
     for (long long c : h) mean += (double)c / sms;
     form_rate[s] = 2.0 * 128 * 128 * 16 * n / mean;
   }
+  // the pair of SMs: {ts, bmn, contend}; flops per clock per SM (half of a
+  // 256-row product per SM), cycles of the even CTA
+  cudaFuncSetAttribute(mma_pair_rate, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const int pforms[5][3] = {{0, 0, 0}, {1, 0, 0}, {1, 1, 0}, {1, 0, 1}, {1, 1, 1}};
+  double pair_rate[5];
+  const int pgrid = sms & ~1;
+  for (int s = 0; s < 5; ++s) {
+    mma_pair_rate<<<pgrid, 256, smem>>>(cyc, 64, pforms[s][0], pforms[s][1], pforms[s][2], err);
+    mma_pair_rate<<<pgrid, 256, smem>>>(cyc, n, pforms[s][0], pforms[s][1], pforms[s][2], err);
+    if (!check(cudaDeviceSynchronize(), "mma_pair_rate")) return 1;
+    cudaMemcpy(h.data(), cyc, sms * sizeof(long long), cudaMemcpyDeviceToHost);
+    mean = 0;
+    for (int b = 0; b < pgrid; b += 2) mean += (double)h[b] / (pgrid / 2);
+    pair_rate[s] = 2.0 * 256 * 128 * 16 * n / 2 / mean;
+  }
   int herr = 0;
   cudaMemcpy(&herr, err, sizeof(int), cudaMemcpyDeviceToHost);
   printf("{\"sm_count\": %d, \"sm\": \"%d.%d\", \"max_clock_mhz\": %.0f, \"ex2_per_clk_per_sm\": %.2f, "
@@ -225,8 +317,12 @@ int main() {
          "\"mma_ts_n128\": %.1f, \"mma_ts_n64\": %.1f, \"ksteps_ss_kmajor\": %.1f, "
          "\"ksteps_ts_kmajor\": %.1f, \"ksteps_ss_b_mnmajor\": %.1f, \"ksteps_ts_b_mnmajor\": %.1f, "
          "\"ksteps_ts_kmajor_tmem_traffic\": %.1f, \"ksteps_ts_b_mnmajor_tmem_traffic\": %.1f, "
+         "\"pair_ksteps_ss_kmajor\": %.1f, \"pair_ksteps_ts_kmajor\": %.1f, "
+         "\"pair_ksteps_ts_b_mnmajor\": %.1f, \"pair_ksteps_ts_kmajor_tmem_traffic\": %.1f, "
+         "\"pair_ksteps_ts_b_mnmajor_tmem_traffic\": %.1f, "
          "\"mma_wait_error\": %d}\n",
          sms, major, minor, clk_khz / 1000.0, ex2_per_clk, rate[0], rate[1], rate[2], rate[3], rate[4],
-         form_rate[0], form_rate[1], form_rate[2], form_rate[3], form_rate[4], form_rate[5], herr);
+         form_rate[0], form_rate[1], form_rate[2], form_rate[3], form_rate[4], form_rate[5],
+         pair_rate[0], pair_rate[1], pair_rate[2], pair_rate[3], pair_rate[4], herr);
   return herr ? 2 : 0;
 }
