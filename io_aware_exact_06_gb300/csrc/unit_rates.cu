@@ -87,21 +87,24 @@ __global__ void __launch_bounds__(128, 1) mma_rate(long long* cycles, int n, int
   }
 }
 
-// The operand forms of the attention kernels, 128 x 128 x 16 products cycling
-// through the eight k-steps of a 128 x 128 tile as those kernels do: A from
-// shared memory (ts = 0, K-major) or from TMEM (ts = 1); B K-major (bmn = 0:
-// S = Q K^T) or MN-major (bmn = 1: P V, dS K, P^T dO, dS^T Q).  With
-// contend = 1, warps 4-7 load and store TMEM columns the products do not use,
-// back to back, while warp 0 issues (the softmax and gradient warps' traffic).
-__global__ void __launch_bounds__(256, 1) mma_form_rate(long long* cycles, int n, int ts, int bmn,
-                                                        int contend, int* err) {
+// The operand forms of the attention kernels: products of 128 x N x 16
+// cycling through the eight k-steps of a 128-deep tile, issued as the kernels
+// issue them (eight products with compile-time descriptor offsets per loop
+// step): A from shared memory (TS = 0, K-major) or from TMEM (TS = 1); B
+// K-major (BMN = 0: S = Q K^T) or MN-major (BMN = 1: P V, dS K, P^T dO, dS^T
+// Q).  With contend = 1, warps 4-7 load and store TMEM columns the products do
+// not use, back to back, while warp 0 issues (the softmax and gradient warps'
+// traffic).  N = 256: TMEM D [0, 256), A [256, 320), traffic [384, 448).
+template <int TS, int BMN, int N>
+__global__ void __launch_bounds__(256, 1) mma_form_rate(long long* cycles, int n, int contend,
+                                                        int* err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   __shared__ uint64_t bar;
   __shared__ uint32_t tmem_base;
   const int tid = threadIdx.x, warp = tid / 32;
-  for (int i = tid; i < 65536 / 4; i += 256) reinterpret_cast<uint32_t*>(smem)[i] = 0;
+  for (int i = tid; i < 98304 / 4; i += 256) reinterpret_cast<uint32_t*>(smem)[i] = 0;
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   if (warp == 0) {
     tmem_alloc(smem_u32(&tmem_base), 512);
@@ -115,20 +118,27 @@ __global__ void __launch_bounds__(256, 1) mma_form_rate(long long* cycles, int n
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
+  // B K-major: 64-column chunks of N rows (N * 128 bytes apart); MN-major: N/64
+  // chunks of 128 keys (16 KB apart), 16 keys per k-step (2048 bytes)
+  constexpr uint32_t kBChunk = BMN ? 16384u : (uint32_t)N * 128u;
   if (tid == 0) {
-    const uint32_t id = make_idesc_bf16(128, 128, bmn != 0);
+    const uint32_t id = make_idesc_bf16(128, N, BMN != 0);
     const uint64_t a0 = make_sdesc(smem_u32(smem), 16, 1024, kSwizzle128B);
-    const uint64_t b0 = bmn ? make_sdesc(smem_u32(smem + 32768), 16384, 1024, kSwizzle128B)
+    const uint64_t b0 = BMN ? make_sdesc(smem_u32(smem + 32768), 16384, 1024, kSwizzle128B)
                             : make_sdesc(smem_u32(smem + 32768), 16, 1024, kSwizzle128B);
     const long long t0 = clock64();
-    for (int i = 0; i < n; ++i) {
-      const int kk = i % 8;
-      const uint64_t koff = (uint64_t)(((kk / 4) * 16384 + (kk % 4) * 32) >> 4);
-      const uint64_t boff = bmn ? (uint64_t)((kk * 2048) >> 4) : koff;
-      if (ts)
-        mma_ts(tmem, tmem + 256 + 8 * kk, b0 + boff, id, i > 0);
-      else
-        mma_ss(tmem, a0 + koff, b0 + boff, id, i > 0);
+    for (int i = 0; i < n; i += 8) {
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint64_t aoff = (uint64_t)(((kk / 4) * 16384 + (kk % 4) * 32) >> 4);
+        const uint64_t boff = BMN ? (uint64_t)((kk * 2048) >> 4)
+                                  : (uint64_t)(((kk / 4) * kBChunk + (kk % 4) * 32) >> 4);
+        const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+        if (TS)
+          mma_ts(tmem, tmem + 256 + 8 * kk, b0 + boff, id, acc);
+        else
+          mma_ss(tmem, a0 + aoff, b0 + boff, id, acc);
+      }
     }
     mma_commit(smem_u32(&bar));
     if (!mbar_wait(smem_u32(&bar), 0, 1000000000ull)) atomicOr(err, 1);
@@ -157,15 +167,17 @@ __global__ void __launch_bounds__(256, 1) mma_form_rate(long long* cycles, int n
 
 // A pair of SMs (a cluster of two CTAs) sharing each product: the even CTA
 // issues n products of 256 x 128 x 16 (cta_group::2) stepping through the
-// k-slices of a 128-deep tile as a paired attention kernel does.  A is each
-// CTA's own 128 rows, from shared memory (ts = 0, K-major) or from TMEM
-// (ts = 1); B is 64 of the 128 columns from each CTA's shared memory, K-major
-// (bmn = 0: S = Q K^T with 64 keys per CTA) or MN-major (bmn = 1: P V with 64
-// of the d columns per CTA).  contend = 1: warps 4-7 of both CTAs load and
+// k-slices of a 128-deep tile as a paired attention kernel does (eight
+// products with compile-time offsets per loop step).  A is each
+// CTA's own 128 rows, from shared memory (TS = 0, K-major) or from TMEM
+// (TS = 1); B is 64 of the 128 columns from each CTA's shared memory, K-major
+// (BMN = 0: S = Q K^T with 64 keys per CTA) or MN-major (bmn = 1: P V with 64
+// of the d columns per CTA; BMN = 1).  contend = 1: warps 4-7 of both CTAs load and
 // store TMEM columns the products do not use.  256 TMEM columns per CTA:
 // D [0, 128), A [128, 192), traffic [192, 256).
+template <int TS, int BMN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
-    mma_pair_rate(long long* cycles, int n, int ts, int bmn, int contend, int* err) {
+    mma_pair_rate(long long* cycles, int n, int contend, int* err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -191,21 +203,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
   if (tid == 0) {
     const long long t0 = clock64();
     if (rank == 0) {
-      const uint32_t id = make_idesc_bf16(256, 128, bmn != 0);
+      const uint32_t id = make_idesc_bf16(256, 128, BMN != 0);
       const uint64_t a0 = make_sdesc(smem_u32(smem), 16, 1024, kSwizzle128B);
-      const uint64_t b0 = bmn ? make_sdesc(smem_u32(smem + 32768), 16384, 1024, kSwizzle128B)
+      const uint64_t b0 = BMN ? make_sdesc(smem_u32(smem + 32768), 16384, 1024, kSwizzle128B)
                               : make_sdesc(smem_u32(smem + 32768), 16, 1024, kSwizzle128B);
-      for (int i = 0; i < n; ++i) {
-        const int kk = i % 8;
-        const uint64_t aoff = (uint64_t)(((kk / 4) * 16384 + (kk % 4) * 32) >> 4);
-        // B: 64 rows per 64-column chunk when K-major (8 KB chunks), 16 keys
-        // (2048 bytes) per k-step when MN-major
-        const uint64_t boff = bmn ? (uint64_t)((kk * 2048) >> 4)
-                                  : (uint64_t)(((kk / 4) * 8192 + (kk % 4) * 32) >> 4);
-        if (ts)
-          mma_ts_pair(tmem, tmem + 128 + 8 * kk, b0 + boff, id, i > 0);
-        else
-          mma_ss_pair(tmem, a0 + aoff, b0 + boff, id, i > 0);
+      for (int i = 0; i < n; i += 8) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t aoff = (uint64_t)(((kk / 4) * 16384 + (kk % 4) * 32) >> 4);
+          // B: 64 rows per 64-column chunk when K-major (8 KB chunks), 16 keys
+          // (2048 bytes) per k-step when MN-major
+          const uint64_t boff = BMN ? (uint64_t)((kk * 2048) >> 4)
+                                    : (uint64_t)(((kk / 4) * 8192 + (kk % 4) * 32) >> 4);
+          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+          if (TS)
+            mma_ts_pair(tmem, tmem + 128 + 8 * kk, b0 + boff, id, acc);
+          else
+            mma_ss_pair(tmem, a0 + aoff, b0 + boff, id, acc);
+        }
       }
       mma_commit_pair(smem_u32(&bar), 3);
     }
@@ -282,28 +297,37 @@ int main() {
     for (long long c : h) mean += (double)c / sms;
     rate[s] = 2.0 * 128 * shapes[s][0] * 16 * n / mean;
   }
-  // the attention kernels' operand forms: {ts, bmn, contend}
-  cudaFuncSetAttribute(mma_form_rate, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  const int forms[6][3] = {{0, 0, 0}, {1, 0, 0}, {0, 1, 0}, {1, 1, 0}, {1, 0, 1}, {1, 1, 1}};
-  double form_rate[6];
-  for (int s = 0; s < 6; ++s) {
-    mma_form_rate<<<sms, 256, smem>>>(cyc, 64, forms[s][0], forms[s][1], forms[s][2], err);
-    mma_form_rate<<<sms, 256, smem>>>(cyc, n, forms[s][0], forms[s][1], forms[s][2], err);
+  // the attention kernels' operand forms, issued unrolled
+  const size_t smem_f = 96 * 1024 + 1024;
+  typedef void (*FormFn)(long long*, int, int, int*);
+  struct Form { FormFn fn; int N, contend; };
+  const Form forms[8] = {{mma_form_rate<0, 0, 128>, 128, 0}, {mma_form_rate<1, 0, 128>, 128, 0},
+                         {mma_form_rate<0, 1, 128>, 128, 0}, {mma_form_rate<1, 1, 128>, 128, 0},
+                         {mma_form_rate<1, 0, 128>, 128, 1}, {mma_form_rate<1, 1, 128>, 128, 1},
+                         {mma_form_rate<0, 0, 256>, 256, 0}, {mma_form_rate<1, 0, 256>, 256, 0}};
+  double form_rate[8];
+  for (int s = 0; s < 8; ++s) {
+    cudaFuncSetAttribute(forms[s].fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_f);
+    forms[s].fn<<<sms, 256, smem_f>>>(cyc, 64, forms[s].contend, err);
+    forms[s].fn<<<sms, 256, smem_f>>>(cyc, n, forms[s].contend, err);
     if (!check(cudaDeviceSynchronize(), "mma_form_rate")) return 1;
     cudaMemcpy(h.data(), cyc, sms * sizeof(long long), cudaMemcpyDeviceToHost);
     mean = 0;
     for (long long c : h) mean += (double)c / sms;
-    form_rate[s] = 2.0 * 128 * 128 * 16 * n / mean;
+    form_rate[s] = 2.0 * 128 * forms[s].N * 16 * n / mean;
   }
-  // the pair of SMs: {ts, bmn, contend}; flops per clock per SM (half of a
-  // 256-row product per SM), cycles of the even CTA
-  cudaFuncSetAttribute(mma_pair_rate, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  const int pforms[5][3] = {{0, 0, 0}, {1, 0, 0}, {1, 1, 0}, {1, 0, 1}, {1, 1, 1}};
+  // the pair of SMs: flops per clock per SM (half of a 256-row product per
+  // SM), cycles of the even CTA
+  typedef void (*PairFn)(long long*, int, int, int*);
+  struct PForm { PairFn fn; int contend; };
+  const PForm pforms[5] = {{mma_pair_rate<0, 0>, 0}, {mma_pair_rate<1, 0>, 0}, {mma_pair_rate<1, 1>, 0},
+                           {mma_pair_rate<1, 0>, 1}, {mma_pair_rate<1, 1>, 1}};
   double pair_rate[5];
   const int pgrid = sms & ~1;
   for (int s = 0; s < 5; ++s) {
-    mma_pair_rate<<<pgrid, 256, smem>>>(cyc, 64, pforms[s][0], pforms[s][1], pforms[s][2], err);
-    mma_pair_rate<<<pgrid, 256, smem>>>(cyc, n, pforms[s][0], pforms[s][1], pforms[s][2], err);
+    cudaFuncSetAttribute(pforms[s].fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    pforms[s].fn<<<pgrid, 256, smem>>>(cyc, 64, pforms[s].contend, err);
+    pforms[s].fn<<<pgrid, 256, smem>>>(cyc, n, pforms[s].contend, err);
     if (!check(cudaDeviceSynchronize(), "mma_pair_rate")) return 1;
     cudaMemcpy(h.data(), cyc, sms * sizeof(long long), cudaMemcpyDeviceToHost);
     mean = 0;
@@ -317,12 +341,14 @@ int main() {
          "\"mma_ts_n128\": %.1f, \"mma_ts_n64\": %.1f, \"ksteps_ss_kmajor\": %.1f, "
          "\"ksteps_ts_kmajor\": %.1f, \"ksteps_ss_b_mnmajor\": %.1f, \"ksteps_ts_b_mnmajor\": %.1f, "
          "\"ksteps_ts_kmajor_tmem_traffic\": %.1f, \"ksteps_ts_b_mnmajor_tmem_traffic\": %.1f, "
+         "\"ksteps_ss_n256\": %.1f, \"ksteps_ts_n256\": %.1f, "
          "\"pair_ksteps_ss_kmajor\": %.1f, \"pair_ksteps_ts_kmajor\": %.1f, "
          "\"pair_ksteps_ts_b_mnmajor\": %.1f, \"pair_ksteps_ts_kmajor_tmem_traffic\": %.1f, "
          "\"pair_ksteps_ts_b_mnmajor_tmem_traffic\": %.1f, "
          "\"mma_wait_error\": %d}\n",
          sms, major, minor, clk_khz / 1000.0, ex2_per_clk, rate[0], rate[1], rate[2], rate[3], rate[4],
          form_rate[0], form_rate[1], form_rate[2], form_rate[3], form_rate[4], form_rate[5],
+         form_rate[6], form_rate[7],
          pair_rate[0], pair_rate[1], pair_rate[2], pair_rate[3], pair_rate[4], herr);
   return herr ? 2 : 0;
 }
