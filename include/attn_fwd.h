@@ -21,6 +21,7 @@
 #ifndef IO_AWARE_EXACT_06_ATTN_FWD_H
 #define IO_AWARE_EXACT_06_ATTN_FWD_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -180,6 +181,9 @@ typedef struct {
     int fault_inject;         /* 0 = none; 1 = CTA 0 never issues its first K copy,
                                  so a bounded wait must expire (tests only) */
     int max_ctas;             /* 0 = one persistent CTA per SM; else at most this many */
+    int kernel;               /* d = 128 without a window: 0 = the library's choice
+                                 (the one-CTA kernel), 1 = the one-CTA kernel,
+                                 2 = the pair-of-SMs kernel (two SMs share each product) */
 } attn_fwd_options;
 
 /* attn_fwd with options (opts may be NULL).  Same arguments and errors. */
@@ -219,9 +223,10 @@ int attn_last_cuda_error(void);
  * that loads the library holds until the process exits.
  *
  * Same arguments, layouts and results as attn_fwd.  Differences:
- *   - B * ceil(N / 256) must not exceed 65536 (the number of (sequence,
- *     256-row block) pairs the scratch holds); larger problems return
- *     ATTN_ERR_SCRATCH before anything is launched.
+ *   - Packed batches (cu_seqlens given): B * ceil(N / 256) must not exceed
+ *     65536 (the number of (sequence, 256-row block) pairs the scratch
+ *     holds); larger ones return ATTN_ERR_SCRATCH before anything is
+ *     launched.  Dense batches keep no list there and have no such limit.
  *   - The first call on a device does the set-up for that device (kernel
  *     attributes and the device address of the scratch array); make that
  *     first call before any stream capture.  No call allocates device memory.
@@ -232,11 +237,41 @@ int attn_last_cuda_error(void);
  *     the caller.  The array keeps the last call's contents.
  *   - Device-side errors of this variant (an expired bounded wait, invalid
  *     cu_seqlens) are recorded in its scratch, not in the error word read by
- *     attn_last_device_error; the outputs of such a call are incomplete.
+ *     attn_last_device_error; read them with
+ *     attn_fwd_noalloc_last_device_error.  The outputs of such a call are
+ *     incomplete (with invalid cu_seqlens nothing is written).
  */
 int attn_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
                      int B, int H, int N, int d, float scale, int causal,
                      const int32_t *cu_seqlens, attn_stream_t stream);
+
+/* attn_fwd_noalloc with the options of attn_fwd_ex (opts may be NULL): the
+ * bound on each device-side wait, the test hook that makes one wait expire,
+ * a cap on the CTAs.  Allocates nothing either; same arguments and errors. */
+int attn_fwd_noalloc_ex(const void *q, const void *k, const void *v, void *o, float *lse,
+                        int B, int H, int N, int d, float scale, int causal,
+                        const int32_t *cu_seqlens, attn_stream_t stream,
+                        const attn_fwd_options *opts);
+
+/*
+ * The device-side error status of the attn_fwd_noalloc calls on the current
+ * device since the last one started (each call clears it when it starts):
+ * synchronises `stream`, reads the error words of the fixed scratch with
+ * plain copies (no allocation), clears them and returns ATTN_OK,
+ * ATTN_ERR_DEVICE_TIMEOUT (a bounded wait expired; that call's outputs are
+ * incomplete), ATTN_ERR_SEQLENS (invalid cu_seqlens; nothing was computed)
+ * or ATTN_ERR_SHAPE; ATTN_ERR_CUDA if the synchronisation or a copy fails.
+ * The site of an expired wait is then read with attn_last_error_site.  Like
+ * the calls it reports on, it races with attn_fwd_noalloc work of another
+ * stream that overlaps it on the GPU.  The pages have no counterpart to it.
+ */
+int attn_fwd_noalloc_last_device_error(attn_stream_t stream);
+
+/* Bytes of device memory the library currently holds in its own workspaces
+ * (error words, scheduling lists, split-KV partial results, attn_fwd_host's
+ * slots, the backward's and the FP8 path's buffers), over all devices.
+ * attn_fwd_noalloc adds nothing to it.  For diagnostics; not on the pages. */
+size_t attn_device_bytes(void);
 
 /* A static, human-readable name of a status code. */
 const char *attn_status_string(int status);

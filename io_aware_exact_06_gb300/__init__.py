@@ -15,13 +15,15 @@ import os
 from . import build as _build
 
 __all__ = ["attn_fwd", "attn_bwd", "attn_bwd_window", "attn_fwd_fp8", "attn_fwd_fp8_codes", "attn_fp8_quantize_qk", "attn_fp8_quantize_v",
-           "attn_fwd_ex", "attn_fwd_host", "attn_fwd_noalloc", "attn_fwd_window", "attn_fwd_kvsplit", "attn_fwd_decode", "attn_last_device_error", "attn_last_error_site",
+           "attn_fwd_ex", "attn_fwd_host", "attn_fwd_noalloc", "attn_fwd_noalloc_ex",
+           "attn_fwd_noalloc_last_device_error", "attn_device_bytes", "attn_fwd_window", "attn_fwd_kvsplit", "attn_fwd_decode", "attn_last_device_error", "attn_last_error_site",
            "attn_status_string", "AttnError", "AttnFwdOptions", "lib", "forward", "backward", "decode",
            "EXPORTED_SYMBOLS"]
 
 # Every symbol the headers under include/ declare.
 EXPORTED_SYMBOLS = ("attn_fwd", "attn_fwd_ex", "attn_fwd_host", "attn_fwd_decode", "attn_last_device_error", "attn_last_error_site",
                     "attn_last_cuda_error", "attn_status_string", "attn_fwd_noalloc",
+                    "attn_fwd_noalloc_ex", "attn_fwd_noalloc_last_device_error", "attn_device_bytes",
                     "attn_fwd_window", "attn_fwd_kvsplit", "attn_bwd", "attn_bwd_window",
                     "attn_fwd_fp8", "attn_fwd_fp8_codes",
                     "attn_fp8_quantize_qk", "attn_fp8_quantize_v")
@@ -39,7 +41,8 @@ class AttnError(RuntimeError):
 class AttnFwdOptions(ctypes.Structure):
     _fields_ = [("wait_timeout_ns", ctypes.c_uint64),
                 ("fault_inject", ctypes.c_int),
-                ("max_ctas", ctypes.c_int)]
+                ("max_ctas", ctypes.c_int),
+                ("kernel", ctypes.c_int)]
 
 
 _lib = None
@@ -80,6 +83,12 @@ def lib() -> ctypes.CDLL:
         L.attn_fp8_quantize_v.restype = i
         L.attn_fwd_noalloc.argtypes = sig
         L.attn_fwd_noalloc.restype = i
+        L.attn_fwd_noalloc_ex.argtypes = sig + [ctypes.POINTER(AttnFwdOptions)]
+        L.attn_fwd_noalloc_ex.restype = i
+        L.attn_fwd_noalloc_last_device_error.argtypes = [vp]
+        L.attn_fwd_noalloc_last_device_error.restype = i
+        L.attn_device_bytes.argtypes = []
+        L.attn_device_bytes.restype = ctypes.c_size_t
         L.attn_fwd_host.argtypes = sig
         L.attn_fwd_host.restype = i
         L.attn_last_device_error.argtypes = [vp]
@@ -137,9 +146,10 @@ def attn_fwd_host(q, k, v, o, lse, B: int, H: int, N: int, d: int, scale: float,
 
 def attn_fwd_ex(q, k, v, o, lse, B: int, H: int, N: int, d: int, scale: float, causal: bool,
                 cu_seqlens=None, stream=None, wait_timeout_ns: int = 0, fault_inject: int = 0,
-                max_ctas: int = 0) -> int:
-    """The C call ``attn_fwd_ex``; options as keyword arguments."""
-    opts = AttnFwdOptions(int(wait_timeout_ns), int(fault_inject), int(max_ctas))
+                max_ctas: int = 0, kernel: int = 0) -> int:
+    """The C call ``attn_fwd_ex``; options as keyword arguments (kernel: 0 the
+    library's choice, 1 one CTA per unit, 2 a pair of SMs, for d = 128)."""
+    opts = AttnFwdOptions(int(wait_timeout_ns), int(fault_inject), int(max_ctas), int(kernel))
     st = lib().attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(N),
                            int(d), float(scale), int(bool(causal)), _ptr(cu_seqlens),
                            _stream(stream), ctypes.byref(opts))
@@ -193,6 +203,30 @@ def attn_fwd_noalloc(q, k, v, o, lse, B: int, H: int, N: int, d: int, scale: flo
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_noalloc")
     return st
+
+
+def attn_fwd_noalloc_ex(q, k, v, o, lse, B: int, H: int, N: int, d: int, scale: float,
+                        causal: bool, cu_seqlens=None, stream=None, wait_timeout_ns: int = 0,
+                        fault_inject: int = 0, max_ctas: int = 0) -> int:
+    """The C call ``attn_fwd_noalloc_ex``: attn_fwd_noalloc with attn_fwd_ex's options."""
+    opts = AttnFwdOptions(int(wait_timeout_ns), int(fault_inject), int(max_ctas), 0)
+    st = lib().attn_fwd_noalloc_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H),
+                                   int(N), int(d), float(scale), int(bool(causal)),
+                                   _ptr(cu_seqlens), _stream(stream), ctypes.byref(opts))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_noalloc_ex")
+    return st
+
+
+def attn_fwd_noalloc_last_device_error(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device error status
+    of attn_fwd_noalloc's scratch."""
+    return lib().attn_fwd_noalloc_last_device_error(_stream(stream))
+
+
+def attn_device_bytes() -> int:
+    """Bytes of device memory the library holds in its own workspaces."""
+    return int(lib().attn_device_bytes())
 
 
 def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B: int, H: int, N: int, d: int, scale: float,

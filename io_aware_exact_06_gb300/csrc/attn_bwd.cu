@@ -60,13 +60,13 @@ int bwd_workspace(int dev, attn_stream_t stream, size_t floats, size_t ints, int
       // the old buffers may still be read by work queued on this stream
       if ((e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream))) != cudaSuccess)
         return attn_host::lib_cuda_fail(e);
-      cudaFree(ws.buf);
+      attn_host::lib_free(ws.buf);
       ws.buf = nullptr;
       ws.floats = 0;
     }
     const size_t cap = std::max<size_t>(floats, 1 << 16);
     const size_t icap = std::max<size_t>(ints, 1024);
-    if ((e = cudaMalloc(&ws.buf, kCounterBytes + 2 * cap * sizeof(float) + icap * sizeof(int))) !=
+    if ((e = attn_host::lib_malloc(&ws.buf, kCounterBytes + 2 * cap * sizeof(float) + icap * sizeof(int))) !=
         cudaSuccess)
       return attn_host::lib_cuda_fail(e);
     if ((e = cudaMemset(ws.buf, 0, kCounterBytes)) != cudaSuccess) return attn_host::lib_cuda_fail(e);

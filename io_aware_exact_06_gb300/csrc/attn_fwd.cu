@@ -19,6 +19,7 @@
 #include "attn_decode_kernel.cuh"
 #include "attn_fp8_kernel.cuh"
 #include "attn_fwd_kernel.cuh"
+#include "attn_fwd_pair_kernel.cuh"
 #include "attn_host.h"
 
 namespace {
@@ -37,6 +38,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 struct DeviceState {
   bool ready = false;
   int sms = 0;
+  int pair_clusters = 0;  // co-resident clusters of the pair kernel
   int major = 0, minor = 0;
   int* err = nullptr;  // [0] error bits, [1] site of an expired wait
 };
@@ -124,9 +126,27 @@ cudaError_t set_smem_attributes() {
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 attn::QuantCfg<128>::kSmemBytes)) != cudaSuccess)
     return e;
+  if ((e = cudaFuncSetAttribute(attn::attn_fwd_pair_kernel,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                attn::kPairSmemBytes)) != cudaSuccess)
+    return e;
   return cudaFuncSetAttribute(attn::attn_fwd_kernel<128, attn::kModeWindow>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               FwdCfg<128>::kSmemBytes);
+}
+
+// Clusters of the pair kernel that fit on the device at once (its persistent
+// grid is twice this).
+cudaError_t pair_cluster_count(int sms, int* out) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(sms & ~1), 1, 1);
+  cfg.blockDim = dim3(attn::kPairThreads, 1, 1);
+  cfg.dynamicSmemBytes = attn::kPairSmemBytes;
+  int n = 0;
+  cudaError_t e = cudaOccupancyMaxActiveClusters(&n, attn::attn_fwd_pair_kernel, &cfg);
+  if (e != cudaSuccess) return e;
+  *out = n;
+  return cudaSuccess;
 }
 
 int device_state(int dev, DeviceState** out) {
@@ -141,7 +161,8 @@ int device_state(int dev, DeviceState** out) {
       return cuda_fail(e);
     if (st.major != 10 || st.minor != 3) return ATTN_ERR_ARCH;
     if ((e = set_smem_attributes()) != cudaSuccess) return cuda_fail(e);
-    if ((e = cudaMalloc(&st.err, 4 * sizeof(int))) != cudaSuccess) return cuda_fail(e);
+    if ((e = pair_cluster_count(st.sms, &st.pair_clusters)) != cudaSuccess) return cuda_fail(e);
+    if ((e = attn_host::lib_malloc(&st.err, 4 * sizeof(int))) != cudaSuccess) return cuda_fail(e);
     if ((e = cudaMemset(st.err, 0, 4 * sizeof(int))) != cudaSuccess) return cuda_fail(e);
     st.ready = true;
   }
@@ -157,12 +178,12 @@ int stream_workspace(int dev, attn_stream_t stream, int64_t entries, int** out) 
       // the old list may still be read by work queued on this stream
       if ((e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream))) != cudaSuccess)
         return cuda_fail(e);
-      cudaFree(ws.buf);
+      attn_host::lib_free(ws.buf);
       ws.buf = nullptr;
       ws.capacity = 0;
     }
     const int64_t cap = entries < 1024 ? 1024 : entries;
-    if ((e = cudaMalloc(&ws.buf, (size_t)(4 + 2 * cap) * sizeof(int))) != cudaSuccess)
+    if ((e = attn_host::lib_malloc(&ws.buf, (size_t)(4 + 2 * cap) * sizeof(int))) != cudaSuccess)
       return cuda_fail(e);
     if ((e = cudaMemset(ws.buf, 0, 4 * sizeof(int))) != cudaSuccess) return cuda_fail(e);
     ws.capacity = cap;
@@ -178,23 +199,24 @@ int partial_workspace(int dev, attn_stream_t stream, size_t floats, float** out)
     if (ws.buf) {
       if ((e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream))) != cudaSuccess)
         return cuda_fail(e);
-      cudaFree(ws.buf);
+      attn_host::lib_free(ws.buf);
       ws.buf = nullptr;
       ws.capacity = 0;
     }
-    if ((e = cudaMalloc(&ws.buf, floats * sizeof(float))) != cudaSuccess) return cuda_fail(e);
+    if ((e = attn_host::lib_malloc(&ws.buf, floats * sizeof(float))) != cudaSuccess) return cuda_fail(e);
     ws.capacity = floats;
   }
   *out = ws.buf;
   return ATTN_OK;
 }
 
-// 3-D view [tokens, H, d] of a bf16 tensor; box = 128 tokens x 1 head x 64
-// elements (128 bytes, the 128-byte swizzle span).
-int make_map(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int64_t tokens, int H, int d) {
+// 3-D view [tokens, H, d] of a bf16 tensor; box = box_rows tokens (128 unless
+// given) x 1 head x 64 elements (128 bytes, the 128-byte swizzle span).
+int make_map(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int64_t tokens, int H, int d,
+             int box_rows = attn::kBM) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)tokens};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
-  cuuint32_t box[3] = {64, 1, (cuuint32_t)attn::kBM};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -301,6 +323,20 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* l
   } else if (units < grid) {
     grid = (int)units;
   }
+  // d = 128 without a window: the pair-of-SMs kernel when asked for; clusters
+  // take the units round robin
+  if (d == 128 && window_left < 0 && window_right < 0 && opts && opts->kernel == 2 &&
+      ds->pair_clusters > 0) {
+    CUtensorMap mk64;
+    if ((st = make_map(enc, &mk64, k, tokens_bound, H, d, 64)) != ATTN_OK) return st;
+    int64_t clusters = ds->pair_clusters;
+    if (!cu_seqlens) clusters = std::min<int64_t>(clusters, units);
+    if (opts && opts->max_ctas > 0) clusters = std::min<int64_t>(clusters, std::max(1, opts->max_ctas / 2));
+    attn::attn_fwd_pair_kernel<<<(unsigned)(2 * clusters), attn::kPairThreads, attn::kPairSmemBytes, s>>>(
+        mq, mk64, mv, p);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+  }
   if (opts && opts->max_ctas > 0 && opts->max_ctas < grid) grid = opts->max_ctas;
   return d == 64 ? launch_attn<64>(mq, mk, mv, p, grid, s) : launch_attn<128>(mq, mk, mv, p, grid, s);
 }
@@ -357,12 +393,12 @@ int host_pipe(int dev, attn_stream_t stream, size_t slot_bytes, HostPipe** out) 
     if ((e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream))) != cudaSuccess)
       return cuda_fail(e);
     for (auto& p : hp.slot) {
-      if (p) cudaFree(p);
+      attn_host::lib_free(p);
       p = nullptr;
     }
     hp.slot_bytes = 0;
     for (auto& p : hp.slot)
-      if ((e = cudaMalloc(&p, slot_bytes)) != cudaSuccess) return cuda_fail(e);
+      if ((e = attn_host::lib_malloc(&p, slot_bytes)) != cudaSuccess) return cuda_fail(e);
     hp.slot_bytes = slot_bytes;
   }
   *out = &hp;
@@ -595,9 +631,11 @@ int noalloc_setup(int dev, NoAllocDevice** out) {
 
 }  // namespace
 
-extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
-                                int B, int H, int N, int d, float scale, int causal,
-                                const int32_t* cu_seqlens, attn_stream_t stream) {
+namespace {
+
+int attn_fwd_noalloc_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                          int H, int N, int d, float scale, int causal, const int32_t* cu_seqlens,
+                          attn_stream_t stream, const attn_fwd_options* opts) {
   if (B < 0 || H < 0 || N < 0) return ATTN_ERR_SHAPE;
   if (d != 64 && d != 128) return ATTN_ERR_HEADDIM;
   if (!std::isfinite(scale) || scale < 0.0f) return ATTN_ERR_SCALE;
@@ -610,7 +648,8 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
     return ATTN_ERR_SHAPE;
   const int64_t nqb = (N + attn::kUnitRows - 1) / attn::kUnitRows;
   const int64_t entries = (int64_t)B * nqb;
-  if (entries > kNoAllocMaxEntries) return ATTN_ERR_SCRATCH;
+  // only packed batches keep a scheduling list in the scratch
+  if (cu_seqlens && entries > kNoAllocMaxEntries) return ATTN_ERR_SCRATCH;
   const int64_t units = entries * H;
   if (units > INT32_MAX) return ATTN_ERR_SHAPE;
 
@@ -648,8 +687,8 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
   p.wr = -1;
   p.scale = scale;
   p.scale_log2 = exp2_scale(scale);
-  p.timeout_ns = 2000000000ull;
-  p.fault_inject = 0;
+  p.timeout_ns = (opts && opts->wait_timeout_ns) ? opts->wait_timeout_ns : 2000000000ull;
+  p.fault_inject = opts ? opts->fault_inject : 0;
 
   int grid = nd->sms;
   if (cu_seqlens) {
@@ -664,8 +703,52 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
   } else if (units < grid) {
     grid = (int)units;
   }
+  if (opts && opts->max_ctas > 0 && opts->max_ctas < grid) grid = opts->max_ctas;
   return d == 64 ? launch_attn<64>(mq, mk, mv, p, grid, s) : launch_attn<128>(mq, mk, mv, p, grid, s);
 }
+
+}  // namespace
+
+extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                                int B, int H, int N, int d, float scale, int causal,
+                                const int32_t* cu_seqlens, attn_stream_t stream) {
+  return attn_fwd_noalloc_impl(q, k, v, o, lse, B, H, N, d, scale, causal, cu_seqlens, stream,
+                               nullptr);
+}
+
+extern "C" int attn_fwd_noalloc_ex(const void* q, const void* k, const void* v, void* o,
+                                   float* lse, int B, int H, int N, int d, float scale,
+                                   int causal, const int32_t* cu_seqlens, attn_stream_t stream,
+                                   const attn_fwd_options* opts) {
+  return attn_fwd_noalloc_impl(q, k, v, o, lse, B, H, N, d, scale, causal, cu_seqlens, stream,
+                               opts);
+}
+
+// Reads the error words of attn_fwd_noalloc's scratch with plain copies
+// (no allocation) and clears them.
+extern "C" int attn_fwd_noalloc_last_device_error(attn_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e);
+  auto it = g_noalloc_dev.find(dev);
+  if (it == g_noalloc_dev.end() || !it->second.ready) {
+    g_last_error_site = 0;
+    return ATTN_OK;
+  }
+  int h[2] = {0, 0};
+  if ((e = cudaMemcpy(h, it->second.scratch, sizeof h, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e);
+  if ((e = cudaMemset(it->second.scratch, 0, sizeof h)) != cudaSuccess) return cuda_fail(e);
+  g_last_error_site = h[1];
+  if (h[0] & attn::kErrTimeout) return ATTN_ERR_DEVICE_TIMEOUT;
+  if (h[0] & attn::kErrSeqlens) return ATTN_ERR_SEQLENS;
+  if (h[0] & attn::kErrWorklist) return ATTN_ERR_SHAPE;
+  return ATTN_OK;
+}
+
+extern "C" size_t attn_device_bytes(void) { return attn_host::lib_device_bytes(); }
 
 // ---------------------------------------------------------------------------
 // attn_fwd_kvsplit: queries and keys of different lengths (bottom-right
@@ -909,6 +992,40 @@ std::mutex& lib_mutex() { return g_mu; }
 
 int lib_cuda_fail(cudaError_t e) { return cuda_fail(e); }
 
+namespace {
+std::mutex g_alloc_mu;                 // the allocation record (own lock: attn_fwd_host
+std::map<void*, size_t> g_alloc;       // allocates under its own lock, not the library's)
+size_t g_alloc_bytes = 0;
+}  // namespace
+
+cudaError_t lib_malloc_raw(void** p, size_t bytes) {
+  cudaError_t e = cudaMalloc(p, bytes);
+  if (e == cudaSuccess) {
+    std::lock_guard<std::mutex> lock(g_alloc_mu);
+    g_alloc[*p] = bytes;
+    g_alloc_bytes += bytes;
+  }
+  return e;
+}
+
+size_t lib_device_bytes() {
+  std::lock_guard<std::mutex> lock(g_alloc_mu);
+  return g_alloc_bytes;
+}
+
+void lib_free(void* p) {
+  if (!p) return;
+  {
+    std::lock_guard<std::mutex> lock(g_alloc_mu);
+    auto it = g_alloc.find(p);
+    if (it != g_alloc.end()) {
+      g_alloc_bytes -= it->second;
+      g_alloc.erase(it);
+    }
+  }
+  cudaFree(p);
+}
+
 int lib_device(int* dev, int* sms, int** err) {
   cudaError_t e = cudaGetDevice(dev);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -946,11 +1063,11 @@ int fp8_workspace(int dev, attn_stream_t stream, size_t bytes, uint8_t** out) {
     if (ws.buf) {
       if ((e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream))) != cudaSuccess)
         return cuda_fail(e);
-      cudaFree(ws.buf);
+      attn_host::lib_free(ws.buf);
       ws.buf = nullptr;
       ws.bytes = 0;
     }
-    if ((e = cudaMalloc(&ws.buf, bytes)) != cudaSuccess) return cuda_fail(e);
+    if ((e = attn_host::lib_malloc(&ws.buf, bytes)) != cudaSuccess) return cuda_fail(e);
     ws.bytes = bytes;
   }
   *out = static_cast<uint8_t*>(ws.buf);

@@ -18,6 +18,17 @@ std::mutex& lib_mutex();
 // Records e as the thread's last CUDA error and returns ATTN_ERR_CUDA.
 int lib_cuda_fail(cudaError_t e);
 
+// Device allocations of the library's workspaces, counted for
+// attn_device_bytes: every workspace is allocated and released through these.
+cudaError_t lib_malloc_raw(void** p, size_t bytes);
+void lib_free(void* p);
+// Bytes the library holds through lib_malloc (all devices).
+size_t lib_device_bytes();
+template <class T>
+cudaError_t lib_malloc(T** p, size_t bytes) {
+  return lib_malloc_raw(reinterpret_cast<void**>(p), bytes);
+}
+
 // The current device (checked to be sm_103), its SM count and its error word
 // (read by attn_last_device_error).  Call with the lock held.
 int lib_device(int* dev, int* sms, int** err);
