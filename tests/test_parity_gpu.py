@@ -40,24 +40,55 @@ def test_small_configs_every_row(dev, name):
     parity.compare(o, lse, wl, inputs.all_rows(wl.cu_seqlens, wl.H), name)
 
 
+# d = 128 without a window runs on one CTA per unit by default; kernel=2 asks
+# for the pair-of-SMs kernel, so both stay covered.
+KERNELS = {"pair": {"kernel": 2}, "one_cta": {}}
+
+
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
 @pytest.mark.parametrize("name", ["long_causal", "long_full", "stress", "varlen"])
-def test_large_configs_sampled_rows(dev, name):
+def test_large_configs_sampled_rows(dev, name, kernel):
     wl = workload(name)
-    o, lse, st = parity.run_cuda(wl, dev)
+    o, lse, st = parity.run_cuda(wl, dev, **KERNELS[kernel])
     assert st == 0
     rows = inputs.sample_rows(wl.cu_seqlens, wl.H, 4096, seed=inputs.CONFIG_SEED_BASE + 7)
     assert len(rows) >= 4096
-    parity.compare(o, lse, wl, rows, name)
+    parity.compare(o, lse, wl, rows, f"{name} {kernel}")
 
 
-@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-def test_ragged_packed_lengths(dev, d, causal):
+def test_pair_kernel_one_cluster_many_units(dev, causal):
+    """One cluster (max_ctas = 2) walks every unit of a dense batch in turn:
+    Q buffers, S buffers and ring phases carried across many units."""
+    wl = inputs.make_workload("pair1", 4300 + causal, [700] * 3, 5, 128, causal)
+    o, lse, st = parity.run_cuda(wl, dev, max_ctas=2, kernel=2)
+    assert st == 0
+    parity.compare(o, lse, wl, inputs.all_rows(wl.cu_seqlens, wl.H), "pair one cluster")
+
+
+def test_pair_kernel_bounded_wait_expires(dev):
+    """The test hook makes CTA 0 (the even CTA of cluster 0) skip one K copy,
+    so the MMA thread's bounded wait on the pair's full barrier expires: both
+    CTAs of the pair stop, the call reports ATTN_ERR_DEVICE_TIMEOUT and the
+    next call is correct."""
+    import io_aware_exact_06_gb300 as fa
+    wl = inputs.make_workload("pairto", 4310, [512] * 2, 4, 128, True)
+    _, _, st = parity.run_cuda(wl, dev, wait_timeout_ns=50_000_000, fault_inject=1, kernel=2)
+    assert st == -7
+    assert fa.attn_last_error_site() != 0
+    o, lse, st = parity.run_cuda(wl, dev, kernel=2)
+    assert st == 0
+    parity.compare(o, lse, wl, inputs.all_rows(wl.cu_seqlens, wl.H), "pair after timeout")
+
+
+@pytest.mark.parametrize("d,kernel", [(64, "one_cta"), (128, "pair"), (128, "one_cta")])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ragged_packed_lengths(dev, d, causal, kernel):
     lens = [1, 127, 128, 129, 0, 255, 256, 257, 300, 2, 513]
     wl = inputs.make_workload("ragged", 4242 + d, lens, 3, d, causal, qk_std=1.5, varlen=True)
-    o, lse, st = parity.run_cuda(wl, dev, packed=True)
+    o, lse, st = parity.run_cuda(wl, dev, packed=True, **KERNELS[kernel])
     assert st == 0
-    parity.compare(o, lse, wl, inputs.all_rows(wl.cu_seqlens, wl.H), "ragged")
+    parity.compare(o, lse, wl, inputs.all_rows(wl.cu_seqlens, wl.H), f"ragged {kernel}")
 
 
 # scale 2 on unit-variance Q and K: logit standard deviation 2 sqrt(d) (16 at
@@ -107,25 +138,44 @@ def test_causal_last_row_equals_full_row_at_full_size(dev):
     assert torch.equal(lc[:, last], lf[:, last])
 
 
-def test_zero_q_gives_mean_of_visible_v_at_full_size(dev):
-    """Q = 0: every logit is 0, so O_i is the mean of the visible V rows and
-    LSE_i = log(#visible).  Checked on every row of the long causal workload."""
+def _visible_means(wl, v, dev):
+    """Mean of the visible V rows of every query row (fp64, [tokens, H, d])
+    and the number of visible keys ([tokens]): the prefix 0..i of its
+    sequence when causal, the whole sequence otherwise."""
     import torch
-    wl = workload("long_causal")
+    cu = torch.from_numpy(wl.cu_seqlens.astype(np.int64)).to(dev)
+    lens = cu[1:] - cu[:-1]
+    seq = torch.repeat_interleave(torch.arange(wl.nseq, device=dev), lens)
+    start = cu[:-1][seq]
+    pos = torch.arange(wl.tokens, device=dev) - start
+    cs = torch.cat([torch.zeros_like(v[:1]), torch.cumsum(v, dim=0)])
+    if wl.causal:
+        count = pos + 1
+        total = cs[start + count] - cs[start]
+    else:
+        count = lens[seq]
+        total = cs[start + count] - cs[start]
+    return total / count.view(-1, 1, 1).double(), count
+
+
+@pytest.mark.parametrize("name", ["long_causal", "long_full", "stress", "varlen"])
+def test_zero_q_gives_mean_of_visible_v_at_full_size(dev, name):
+    """Q = 0: every logit is 0, so O_i is the mean of the visible V rows and
+    LSE_i = log(#visible) (closed forms of the definition, computed in fp64
+    with prefix sums).  Checked on every row and head of the workload."""
+    wl = workload(name)
     wl0 = inputs.Workload("zeroq", np.zeros_like(wl.q), wl.k, wl.v, wl.cu_seqlens, wl.H, wl.d,
-                          wl.scale, True, False, wl.max_seqlen)
+                          wl.scale, wl.causal, wl.varlen, wl.max_seqlen)
     o, lse, st = parity.run_cuda(wl0, dev)
     assert st == 0
-    B, N = wl.nseq, int(wl.seqlens()[0])
-    v = parity.to_device(wl, dev)[2].double().reshape(B, N, wl.H, wl.d)
-    prefix = torch.cumsum(v, dim=1) / torch.arange(1, N + 1, device=dev, dtype=torch.float64).view(1, N, 1, 1)
-    got = o.double().reshape(B, N, wl.H, wl.d)
-    err = (got - prefix).abs().max().item()
-    rel = ((got - prefix).norm() / prefix.norm()).item()
-    assert err <= parity.O_MAX_ABS and rel <= parity.O_REL_L2, (err, rel)
-    ref_lse = torch.log(torch.arange(1, N + 1, device=dev, dtype=torch.float64))
-    lse_err = (lse.double().reshape(wl.H, B, N) - ref_lse).abs().max().item()
-    assert lse_err <= parity.LSE_MAX_ABS
+    v = parity.to_device(wl, dev)[2].double()
+    ref, count = _visible_means(wl, v, dev)
+    got = o.double()
+    err = (got - ref).abs().max().item()
+    rel = ((got - ref).norm() / ref.norm()).item()
+    assert err <= parity.O_MAX_ABS and rel <= parity.O_REL_L2, (name, err, rel)
+    lse_err = (lse.double() - count.double().log().view(1, -1)).abs().max().item()
+    assert lse_err <= parity.LSE_MAX_ABS, (name, lse_err)
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -149,14 +199,26 @@ def test_zero_scale_is_uniform_average(dev, causal):
                    window=(64, 32))
 
 
-def test_constant_v_gives_constant_o_varlen(dev):
-    wl = workload("varlen")
-    c = inputs.f64_to_bf16_bits(np.array([0.8125]))[0]
-    wlc = inputs.Workload("constv", wl.q, wl.k, np.full_like(wl.v, c), wl.cu_seqlens, wl.H, wl.d,
-                          wl.scale, True, True, wl.max_seqlen)
+@pytest.mark.parametrize("name", ["long_causal", "long_full", "stress", "varlen"])
+def test_constant_v_gives_constant_o(dev, name):
+    """V = c on every row: O_i = c exactly in the definition (the weights of a
+    row sum to 1).  The kernel's weights are bf16-rounded probabilities over
+    their fp32 sum (reading 5): each rounding changes a probability by at
+    most 2^-8 of itself, so the fp32 O lies within c * 2^-8 of c and rounds
+    to c or a neighbouring bf16 value.  Bound: one bf16 ulp of c (2^-8 for
+    c = 0.8125), on every row and head, with O = c exactly on most."""
+    import torch
+    wl = workload(name)
+    c = 0.8125
+    cb = inputs.f64_to_bf16_bits(np.array([c]))[0]
+    wlc = inputs.Workload("constv", wl.q, wl.k, np.full_like(wl.v, cb), wl.cu_seqlens, wl.H, wl.d,
+                          wl.scale, wl.causal, wl.varlen, wl.max_seqlen)
     o, lse, st = parity.run_cuda(wlc, dev)
     assert st == 0
-    assert (o.float() - 0.8125).abs().max().item() <= 4e-3
+    ulp = 2.0 ** -8  # bf16 spacing in [0.5, 1)
+    dev_o = (o.float() - c).abs()
+    assert dev_o.max().item() <= ulp, (name, dev_o.max().item())
+    assert (dev_o == 0).float().mean().item() >= 0.5, name
 
 
 def test_deterministic(dev):
