@@ -84,6 +84,10 @@ class Oracle:
                                           ctypes.POINTER(ctypes.c_int8),
                                           ctypes.POINTER(ctypes.c_uint8),
                                           ctypes.POINTER(ctypes.c_float)]
+        L.oracle_fp8_quantize_tensor.restype = ctypes.c_int
+        L.oracle_fp8_quantize_tensor.argtypes = [_c_u16p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                                 ctypes.POINTER(ctypes.c_uint8),
+                                                 ctypes.POINTER(ctypes.c_float)]
         L.oracle_attn_rows_f64.restype = ctypes.c_int
         L.oracle_attn_rows_f64.argtypes = [_c_dp, _c_dp, _c_dp, _c_i64p, ctypes.c_int64,
                                            ctypes.c_int, ctypes.c_int, ctypes.c_double,
@@ -191,6 +195,21 @@ class Oracle:
                                           _ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_float))
         if st != 0:
             raise ValueError(f"oracle_fp8_quantize failed with status {st}")
+        return codes, scales
+
+    def fp8_quantize_tensor(self, x):
+        """Per-tensor e4m3 quantisation (one scale per head) of bf16 bits x
+        [tokens, H, d] (see oracle.c).  Returns (codes uint8 [tokens, H, d],
+        scales fp32 [H])."""
+        x = _u16(x)
+        tokens, H, d = x.shape
+        codes = np.zeros(x.shape, dtype=np.uint8)
+        scales = np.zeros(H, dtype=np.float32)
+        st = self.lib.oracle_fp8_quantize_tensor(_ptr(x, ctypes.c_uint16), int(tokens), H, d,
+                                                 _ptr(codes, ctypes.c_uint8),
+                                                 _ptr(scales, ctypes.c_float))
+        if st != 0:
+            raise ValueError(f"oracle_fp8_quantize_tensor failed with status {st}")
         return codes, scales
 
     def attn_rows_f64(self, q, k, v, cu_seqlens, rows, scale: float, causal: bool):
@@ -304,6 +323,10 @@ def fwht_f32(*a, **kw):
 
 def fp8_quantize(*a, **kw):
     return default().fp8_quantize(*a, **kw)
+
+
+def fp8_quantize_tensor(*a, **kw):
+    return default().fp8_quantize_tensor(*a, **kw)
 
 
 def attn_rows_f64(*a, **kw):

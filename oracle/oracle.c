@@ -812,6 +812,40 @@ int oracle_fp8_quantize(const uint16_t *x, int64_t B, int64_t N, int H, int d, i
 }
 
 /*
+ * Per-tensor e4m3 quantisation, the baseline the pages measure the FP8 path
+ * against ("flash-attention-evolution" (letsgetai), FlashAttention-3
+ * section, results: block quantisation with incoherent processing gives 2.6x
+ * lower error than per-tensor FP8 attention).  Reading: one scale per tensor
+ * and head (the largest |x| of head h over every token of x maps to 448), no
+ * rotation, and the block quantiser's fp32 steps (448 / amax, x * (448 /
+ * amax), e4m3 rounding).  x: [tokens, H, d] bf16; codes: [tokens, H, d];
+ * scales: [H] = amax / 448 (1 when the head is all zero).
+ */
+int oracle_fp8_quantize_tensor(const uint16_t *x, int64_t tokens, int H, int d, uint8_t *codes,
+                               float *scales)
+{
+    if (!x || !codes || !scales || tokens <= 0 || H <= 0 || d <= 0)
+        return ORACLE_EINVAL;
+    for (int h = 0; h < H; ++h) {
+        float amax = 0.0f;
+        for (int64_t t = 0; t < tokens; ++t)
+            for (int c = 0; c < d; ++c) {
+                const float y = (float)widen_bf16(x[(t * H + h) * (int64_t)d + c]);
+                if (fabsf(y) > amax)
+                    amax = fabsf(y);
+            }
+        const float inv_t = amax > 0.0f ? 448.0f / amax : 1.0f;
+        scales[h] = amax > 0.0f ? amax / 448.0f : 1.0f;
+        for (int64_t t = 0; t < tokens; ++t)
+            for (int c = 0; c < d; ++c) {
+                const int64_t at = (t * H + h) * (int64_t)d + c;
+                codes[at] = oracle_e4m3_encode((float)widen_bf16(x[at]) * inv_t);
+            }
+    }
+    return ORACLE_OK;
+}
+
+/*
  * O and LSE of the requested rows, by the plain definition, for fp64 inputs
  * in the packed layout [tokens, H, d] (e.g. dequantised FP8 values).
  * Single-threaded.

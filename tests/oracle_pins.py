@@ -605,6 +605,44 @@ def check_fp8_block_quantize(orc):
                     assert np.array_equal(got, want[keep]), f"codes b={b} h={h} t={t} rotate={rotate}"
 
 
+def check_fp8_tensor_quantize(orc):
+    """Per-tensor quantisation: one scale per head = max|x| over every token of
+    the head / 448, codes = nearest e4m3 of x * (448 / max|x|) (fp32), by
+    exhaustive search; an all-zero head gets scale 1 and zero codes."""
+    table = _e4m3_table()
+    pos = sorted((v, c) for c, v in table.items() if v >= 0 and c != 0x80)
+    grid = np.array([v for v, _ in pos])
+    codes_of = np.array([c for _, c in pos], dtype=np.uint8)
+    tokens, H, d = 301, 3, 8
+    x = inputs.normal_bf16(1719, tokens * H * d, 1.5).reshape(tokens, H, d)
+    xf = inputs.bf16_bits_to_f64(x).astype(np.float32)
+    # head 1 carries one large entry late in the tensor (the scale must see it);
+    # head 2 is all zero
+    x[250, 1, 5] = inputs.f64_to_bf16_bits(np.array([37.0]))[0]
+    xf[250, 1, 5] = 37.0
+    x[:, 2] = 0
+    xf[:, 2] = 0
+    codes, scales = orc.fp8_quantize_tensor(x)
+    assert scales.shape == (H,) and codes.shape == (tokens, H, d)
+    for h in range(H):
+        amax = np.float32(np.max(np.abs(xf[:, h])))
+        if amax == 0:
+            assert scales[h] == 1.0 and not codes[:, h].any(), "all-zero head"
+            continue
+        assert scales[h] == np.float32(amax / np.float32(448.0)), f"tensor scale h={h}"
+        y = (xf[:, h] * np.float32(np.float32(448.0) / amax)).astype(np.float32)
+        a = np.abs(y.astype(np.float64))
+        dist = np.abs(a[..., None] - grid[None, :])
+        best = dist.min(axis=-1, keepdims=True)
+        # nearest value; among two equally near, the even code
+        cand = np.where(dist == best, codes_of[None, None, :].astype(np.int32) | 0x100, 0)
+        even = np.where((cand & 1) == 0, cand, 0).max(axis=-1)
+        want = np.where(even > 0, even, cand.max(axis=-1)) & 0xff
+        want = np.where((y < 0) & (want != 0), want | 0x80, want).astype(np.uint8)
+        assert np.array_equal(codes[:, h], want), f"tensor codes h={h}"
+    assert codes[250, 1, 5] == 0x7e, "the head's largest value maps to 448"
+
+
 def check_attn_rows_f64(orc):
     """The fp64-input definition equals the bf16-input one on bf16 values."""
     wl = _rand_workload(1818, [37, 5], H=2, d=8, std=1.5)
@@ -645,5 +683,6 @@ ALL_CHECKS = [
     check_e4m3_brute_force,
     check_fwht,
     check_fp8_block_quantize,
+    check_fp8_tensor_quantize,
     check_attn_rows_f64,
 ]

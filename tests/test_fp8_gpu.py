@@ -13,12 +13,15 @@ Tolerances, from the e4m3 format (3 mantissa bits: a rounded value is within
     P-weighted sum of V rows, so its relative L2 error is about 0.036 (the
     errors of different keys have independent signs): bound 0.08, twice that;
     the LSE comes from the unquantised fp32 row sum: bound 2e-3;
-  - against the exact attention, Q, K and V add their own e4m3 rounding.  A
-    logit scale * sum_c q_c k_c then carries an error of standard deviation
-    sqrt(2) * 0.036 * (logit standard deviation) ~ 0.05 for unit-variance
-    inputs; a row with one visible key has that error in its LSE, and the
-    largest of a few hundred compared rows reaches about 5 sigma: bound 0.3 on
-    the LSE; O adds V's 0.036 to P's: bound 0.15 on its relative L2.
+  - against the exact attention, V adds its own 0.036 to P's, in quadrature:
+    O's relative L2 error is about 0.036 * sqrt(2) ~ 0.051 (measured 0.044 to
+    0.055 over every case here): bound 0.11, about twice the worst measured.
+    Q and K add theirs to each logit scale * sum_c q_c k_c: a standard
+    deviation of about 0.036 * sqrt(2) ~ 0.05 for unit-variance inputs (the
+    d products' errors add in quadrature and the scale 1/sqrt(d) divides
+    them out); a row with one visible key has that whole error in its LSE,
+    and the largest over the compared rows reached 0.086: bound 0.18, about
+    twice that (3.5 sigma).
 """
 import json
 import os
@@ -32,7 +35,7 @@ from io_aware_exact_06_gb300 import inputs
 pytestmark = pytest.mark.gpu
 
 REL_DEQ, LSE_DEQ = 0.08, 2e-3
-REL_EXACT, LSE_EXACT = 0.15, 0.3
+REL_EXACT, LSE_EXACT = 0.11, 0.18
 
 
 @pytest.fixture(scope="module")
@@ -190,6 +193,80 @@ def test_incoherent_processing_helps_with_outliers(dev):
     (_, _), (rel_plain, _) = check_case(dev, 1, 1024, 4, False, False, 3500, True)
     (_, _), (rel_rot, _) = check_case(dev, 1, 1024, 4, False, True, 3500, True)
     assert rel_rot < rel_plain, (rel_rot, rel_plain)
+
+
+def sparse_outliers(bits, seed, prob=1e-3, factor=10.0):
+    """bf16 bits with each entry, independently with probability prob, made
+    factor times larger (rare large activations)."""
+    x = inputs.bf16_bits_to_f64(bits).copy()
+    u = (inputs.splitmix64(seed, 0, x.size) >> np.uint64(11)).astype(np.float64) / 2.0 ** 53
+    x.reshape(-1)[u < prob] *= factor
+    return inputs.f64_to_bf16_bits(x)
+
+
+def per_tensor_fp8(dev, q, k, v, B, N, H, d, scale):
+    """FP8 attention with per-tensor quantisation: one e4m3 scale per tensor and
+    head for Q and K (oracle codes, no rotation), V per head, through the same
+    attention kernel as attn_fwd_fp8 (attn_fwd_fp8_codes)."""
+    import torch
+    import io_aware_exact_06_gb300 as fa
+    T = -(-N // 128)
+    Np = 128 * T
+    q8, sq = oracle.fp8_quantize_tensor(q)
+    k8, sk = oracle.fp8_quantize_tensor(k)
+    v8, sv = oracle.fp8_quantize(v, B, N, 0, False)
+    vt = np.zeros((B, H, d, Np), dtype=np.uint8)
+    vt[:, :, :, :N] = v8.reshape(B, N, H, d).transpose(0, 2, 3, 1)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    o = torch.empty((B * N, H, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    fa.attn_fwd_fp8_codes(t(q8), t(np.broadcast_to(sq.reshape(1, H, 1), (B, H, T))), t(k8),
+                          t(np.broadcast_to(sk.reshape(1, H, 1), (B, H, T))), t(vt), t(sv[:, :, 0]),
+                          o, lse, B, H, N, d, scale, False, False)
+    assert fa.attn_last_device_error() == 0
+    return o.float().cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("case", ["sparse_outliers", "plain"])
+def test_block_and_rotation_against_per_tensor_fp8(dev, case):
+    """The pages' claim for the FP8 path: block quantisation with incoherent
+    processing has 2.6x lower error than FP8 attention with per-tensor
+    quantisation ("flash-attention-evolution" (letsgetai), FlashAttention-3
+    section, results).  The pages give no workload; this reads "outliers" as
+    rare large entries: each entry of Q and K, with probability 1/1000, ten
+    times larger, V unit normal (B1 N2048 H4 d128, non-causal).  Both
+    quantisations run through the same attention kernel, and both errors are
+    the relative L2 of O against the exact attention of the bf16 inputs.
+    Measured ratios (per-tensor over block + rotation) 2.21 and 1.72 on two
+    seeds; asserted > 1.5.  Without outliers the e4m3 rounding is relative
+    (a floating-point format) and the rotation changes nothing: ratio 1.00,
+    asserted within 5 %.  (With whole channels of Q and K 20x larger the
+    rotation mixes them into every channel and is worse: ratio 0.61.)"""
+    B, N, H, d, seed = 1, 2048, 4, 128, 3700
+    scale = d ** -0.5
+    q = inputs.normal_bf16(seed, B * N * H * d).reshape(B * N, H, d)
+    k = inputs.normal_bf16(seed + 1, B * N * H * d).reshape(B * N, H, d)
+    v = inputs.normal_bf16(seed + 2, B * N * H * d).reshape(B * N, H, d)
+    if case == "sparse_outliers":
+        q, k = sparse_outliers(q, seed + 10), sparse_outliers(k, seed + 11)
+    cu = np.arange(B + 1) * N
+    rows = inputs.sample_rows(cu, H, 1024, seed=seed + 6)
+    tok = cu[rows[:, 0]] + rows[:, 2]
+    ex_o, _, _ = oracle.attn_rows(q, k, v, cu, rows, scale, False)
+    rel = lambda got: float(np.linalg.norm(got[tok, rows[:, 1]] - ex_o) / np.linalg.norm(ex_o))
+    e_block = rel(run_fp8(dev, q, k, v, B, N, H, False, signs_of(seed + 5), scale)[0])
+    e_tensor = rel(per_tensor_fp8(dev, q, k, v, B, N, H, d, scale))
+    ratio = e_tensor / e_block
+    log = os.environ.get("PARITY_LOG")
+    if log:
+        with open(log, "a") as f:
+            f.write(json.dumps({"test": "fp8_vs_per_tensor", "case": case,
+                                "rel_l2_block_rotated": e_block, "rel_l2_per_tensor": e_tensor,
+                                "ratio": ratio}) + "\n")
+    if case == "sparse_outliers":
+        assert ratio > 1.5, (e_block, e_tensor, ratio)
+    else:
+        assert 0.95 < ratio < 1.05, (e_block, e_tensor, ratio)
 
 
 # ------------------------------------------------------------ packed batches --

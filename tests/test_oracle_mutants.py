@@ -66,6 +66,12 @@ MUTANTS = {
     "quant_scale_inverted": [("const float inv = amax > 0.0f ? 448.0f / amax : 1.0f;",
                               "const float inv = amax > 0.0f ? amax / 448.0f : 1.0f;")],
     "quant_tail_overwrites_shared_rows": [("if (row < nominal || row < 0)", "if (row < 0)")],
+    "tensor_scale_from_first_token": [("        for (int64_t t = 0; t < tokens; ++t)\n            for (int c = 0; c < d; ++c) {\n                const float y",
+                                       "        for (int64_t t = 0; t < 1; ++t)\n            for (int c = 0; c < d; ++c) {\n                const float y")],
+    "tensor_scale_inverted": [("const float inv_t = amax > 0.0f ? 448.0f / amax : 1.0f;",
+                               "const float inv_t = amax > 0.0f ? amax / 448.0f : 1.0f;")],
+    "tensor_reads_next_column": [("codes[at] = oracle_e4m3_encode((float)widen_bf16(x[at]) * inv_t);",
+                           "codes[at] = oracle_e4m3_encode((float)widen_bf16(x[at - c + (c ^ 1)]) * inv_t);")],
     "attn_f64_no_max": [("            if (sc[j] > mx)\n                mx = sc[j];\n        }\n        double z",
                          "            if (j == 0)\n                mx = sc[j];\n        }\n        double z")],
 }
