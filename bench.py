@@ -189,19 +189,25 @@ def cpu_baseline(wl, budget_s: float = 15.0, name=WORKLOAD):
     t0 = time.perf_counter()
     _, _, used = oracle.attn_rows(wl.q, wl.k, wl.v, wl.cu_seqlens, rows, wl.scale, wl.causal)
     dt = time.perf_counter() - t0
-    return {"value": row_flops(wl, rows) / dt / 1e12, "unit": UNIT, "cores": int(used),
+    fl = row_flops(wl, rows)
+    # the oracle's cost per row is proportional to its visible keys, so the
+    # whole workload takes dt scaled by its FLOPs over the sample's
+    return {"value": fl / dt / 1e12, "unit": UNIT, "cores": int(used),
             "kind": "oracle",
             "sample": f"{len(rows)} seeded rows of {name} (fp64, materialised score rows), "
-                      f"{dt:.1f} s; FLOPs = 4*d per visible key"}
+                      f"{dt:.1f} s; FLOPs = 4*d per visible key",
+            "rows_per_s": len(rows) / dt, "fp64_gflops": fl / dt / 1e9,
+            "full_config_s": dt * wl.flops() / fl}
 
 
 def exp_unit_bound(sm_mhz, d: int, per_gpu_tflops: float):
     """The exp-unit roofline: each score element costs 4*d flops of the metric
     and one exp2, so the bound is SMs * f_SM * (ex2 per clock per SM) * 4d.
-    Also the clock-based tensor peak SMs * f_SM * (MMA flop per clock per SM),
-    and (d = 128) the bound set by the rate at which one SM's shared memory
-    and TMEM feed its tensor core in the kernel's operand forms.  Rates are
-    measured on this GPU; f_SM is the median clock of the run."""
+    Also the clock-based tensor peak SMs * f_SM * (MMA flop per clock per SM);
+    the probe measures every operand form the kernels issue (A and B from
+    shared memory, A from TMEM, MN-major B, 256-row products of a pair of
+    SMs) at that same rate.  Rates are measured on this GPU; f_SM is the
+    median clock of the run."""
     try:
         from io_aware_exact_06_gb300 import unit_rates
         r = unit_rates.measure()
@@ -216,20 +222,6 @@ def exp_unit_bound(sm_mhz, d: int, per_gpu_tflops: float):
            "exp_bound_tflops": exp_tf, "frac_of_exp_bound": per_gpu_tflops / exp_tf,
            "tensor_peak_at_clock_tflops": mma_tf,
            "frac_of_tensor_peak_at_clock": per_gpu_tflops / mma_tf}
-    if d == 128 and "ksteps_ss_kmajor" in r:
-        # The tensor core fed by one SM's shared memory: a 128x128 tile pair
-        # costs S = Q K^T (both operands from shared memory) plus O += P V (P
-        # from TMEM while the softmax warps use TMEM too), each at the rate the
-        # probe measures for products stepping through a tile's k-slices.
-        # Flops of the products issued (diagonal tiles in full), so for causal
-        # the fraction understates the kernel's share of this bound.
-        tile = 2.0 * 128 * 128 * d
-        cyc = tile / r["ksteps_ss_kmajor"] + tile / r["ksteps_ts_b_mnmajor_tmem_traffic"]
-        op_tf = r["sm_count"] * f * 2 * tile / cyc / 1e12
-        out.update({"ksteps_ss_flop_per_clk_per_sm": r["ksteps_ss_kmajor"],
-                    "ksteps_ts_tmem_traffic_flop_per_clk_per_sm": r["ksteps_ts_b_mnmajor_tmem_traffic"],
-                    "operand_rate_bound_tflops": op_tf,
-                    "frac_of_operand_rate_bound": per_gpu_tflops / op_tf})
     return out
 
 
@@ -819,7 +811,7 @@ BWD_TRAFFIC_BYTES = 135_278_592 + 3_907_072 + 928_369_664 + 101_978_368 + 954_79
 
 # DRAM bytes (read + write) of one attn_fwd_kernel<128> launch of this
 # workload, from one ncu capture of the current kernel (None once it changes).
-TRAFFIC_BYTES = 609_281_024  # 550.83 MB read + 58.45 MB written
+TRAFFIC_BYTES = None
 
 
 def main():
