@@ -259,6 +259,9 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* l
   if (window_left < -1 || window_right < -1) return ATTN_ERR_SHAPE;
   if (d != 64 && d != 128) return ATTN_ERR_HEADDIM;
   if (!std::isfinite(scale) || scale < 0.0f) return ATTN_ERR_SCALE;
+  // the pair-of-SMs kernel takes d = 128 without a window only
+  const bool use_pair = opts && opts->kernel == 2;
+  if (use_pair && (d != 128 || window_left >= 0 || window_right >= 0)) return ATTN_ERR_SHAPE;
   if (B == 0 || H == 0 || N == 0) return ATTN_OK;
   if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
@@ -278,6 +281,8 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* l
   DeviceState* ds = nullptr;
   int st = device_state(dev, &ds);
   if (st != ATTN_OK) return st;
+  // asked for, the pair kernel runs or the call fails (no other kernel instead)
+  if (use_pair && ds->pair_clusters <= 0) return cuda_fail(cudaErrorLaunchOutOfResources);
   EncodeTiledFn enc = nullptr;
   if ((st = get_encode(&enc)) != ATTN_OK) return st;
 
@@ -324,9 +329,9 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* l
     grid = (int)units;
   }
   // d = 128 without a window: the pair-of-SMs kernel when asked for; clusters
-  // take the units round robin
-  if (d == 128 && window_left < 0 && window_right < 0 && opts && opts->kernel == 2 &&
-      ds->pair_clusters > 0) {
+  // take the units round robin.  Asked for where it cannot run, the call fails
+  // instead of running another kernel.
+  if (use_pair) {
     CUtensorMap mk64;
     if ((st = make_map(enc, &mk64, k, tokens_bound, H, d, 64)) != ATTN_OK) return st;
     int64_t clusters = ds->pair_clusters;

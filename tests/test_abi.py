@@ -227,3 +227,12 @@ def test_decode_argument_errors(lib, args, status):
 
 def test_decode_empty_batch_is_a_noop(lib):
     assert lib.attn_fwd_decode(None, None, None, None, None, 0, 4, 128, 0.1, None, 0, 0, None) == 0
+
+
+def test_pair_kernel_request_checked_before_the_device(lib):
+    """Asking for the pair-of-SMs kernel with a shape it does not take (d = 64,
+    or a sliding window) fails with ATTN_ERR_SHAPE before any device work."""
+    opts = fa.AttnFwdOptions(0, 0, 0, 2)
+    st = lib.attn_fwd_ex(BUF, BUF, BUF, BUF, BUF, 1, 1, 256, 64, 0.125, 1, None, None,
+                         ctypes.byref(opts))
+    assert st == -2
