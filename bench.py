@@ -347,7 +347,7 @@ def run_cuda(args, world, rank, local):
         "frac_of_dense_bf16_peak": value / world / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                      "frac": achieved / peak, "peak_source": f"{src} bf16_tflops (burst)",
-                     "kernel": f"attn_fwd_kernel<{d}>" + (" + build_worklist_kernel" if wl.varlen else ""),
+                     "kernel": f"attn_fwd_row_kernel<{d}>" + (" + build_worklist_kernel" if wl.varlen else ""),
                      "traffic": args.traffic if name == WORKLOAD else None},
         "clocks": clk.summary(),
         "e2e": {"value": world * flops_step * e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
@@ -809,9 +809,9 @@ FP8_TRAFFIC_BYTES = (159_129_600 + 29_851_648 + 158_655_232 + 27_379_968) // 2
 BWD_TRAFFIC_BYTES = 135_278_592 + 3_907_072 + 928_369_664 + 101_978_368 + 954_793_472 + 46_435_584
 
 
-# DRAM bytes (read + write) of one attn_fwd_kernel<128> launch of this
+# DRAM bytes (read + write) of one attn_fwd_row_kernel<128> launch of this
 # workload, from one ncu capture of the current kernel (None once it changes).
-TRAFFIC_BYTES = None
+TRAFFIC_BYTES = 586_072_320  # 540.07 MB read + 46.00 MB written
 
 
 def main():

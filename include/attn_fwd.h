@@ -181,11 +181,12 @@ typedef struct {
     int fault_inject;         /* 0 = none; 1 = CTA 0 never issues its first K copy,
                                  so a bounded wait must expire (tests only) */
     int max_ctas;             /* 0 = one persistent CTA per SM; else at most this many */
-    int kernel;               /* 0 = the library's choice (the one-CTA kernel),
-                                 1 = the one-CTA kernel, 2 = the pair-of-SMs kernel
-                                 (two SMs share each product; d = 128 without a
-                                 window only, else ATTN_ERR_SHAPE; ATTN_ERR_CUDA if
-                                 the device cannot run it) */
+    int kernel;               /* 0 = the library's choice (3); 1 = one CTA per unit,
+                                 two softmax threads per query row; 3 = one CTA per
+                                 unit, one softmax thread per row; 2 = the pair-of-SMs
+                                 kernel (two SMs share each product; d = 128 without a
+                                 window only, else ATTN_ERR_SHAPE; ATTN_ERR_CUDA if the
+                                 device cannot run it) */
 } attn_fwd_options;
 
 /* attn_fwd with options (opts may be NULL).  Same arguments and errors. */

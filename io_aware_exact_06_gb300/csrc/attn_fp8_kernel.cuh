@@ -635,7 +635,7 @@ __device__ __forceinline__ void fp8_mma_loop(const Fp8Params& p, SharedState& ss
 }
 
 template <int D>
-__device__ __forceinline__ void fp8_softmax_loop(const Fp8Params& p, SharedState& ss,
+__device__ __forceinline__ void fp8_softmax_loop(const Fp8Params& p, SharedState& ss, RowExchange& xs,
                                                  uint32_t tmem, int g) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int quadrant = warp % 4;
@@ -701,13 +701,13 @@ __device__ __forceinline__ void fp8_softmax_loop(const Fp8Params& p, SharedState
         mx3 = max3(mx3, s[c + 6], s[c + 7]);
       }
       const float mine = fmaxf(max3(mx0, mx1, mx2), mx3);
-      ss.row_max[j & 1][g][half][trow] = mine;
+      xs.row_max[j & 1][g][half][trow] = mine;
       pair_sync(g, quadrant);  // (also orders both halves' S loads before any P store)
       // log2 units per raw S unit, at least the smallest normal float so that a
       // masked (-inf) logit stays -inf (a zero scale, or tiny block scales,
       // would give -inf * 0 = NaN)
       const float c2t = fmaxf(qfac * p.sk[(size_t)bh * p.T + j], FLT_MIN);
-      const float raw = fmaxf(mine, ss.row_max[j & 1][g][half ^ 1][trow]);
+      const float raw = fmaxf(mine, xs.row_max[j & 1][g][half ^ 1][trow]);
       const float m_new = fmaxf(m_used, raw == -INFINITY ? -INFINITY : raw * c2t);
       float alpha = 1.0f;
       bool resc = false;
@@ -752,9 +752,9 @@ __device__ __forceinline__ void fp8_softmax_loop(const Fp8Params& p, SharedState
       mbar_arrive(bar_addr(ss, kBarPFull + g));
     }
     // epilogue (l sums 2^8 P): O = O_acc * s_v / l -> bf16; LSE = ln 2 (m + log2 l - 8)
-    ss.row_sum[g][half][0][trow] = l;
+    xs.row_sum[g][half][0][trow] = l;
     pair_sync(g, quadrant);
-    l += ss.row_sum[g][half ^ 1][0][trow];
+    l += xs.row_sum[g][half ^ 1][0][trow];
     u = -1;
     if (!fail) fail = !fp8_next_unit(ss, p, uslot, true, u);
     if (pair_sync_check(g, quadrant, fail)) return;
@@ -796,6 +796,7 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const __grid_constant__ CUtensorMap tm_vt, const Fp8Params p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ SharedState ss;
+  __shared__ RowExchange xs;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
@@ -851,7 +852,7 @@ attn_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __syncwarp();
   } else {
     setmaxnreg_inc<kSoftmaxRegs>();
-    fp8_softmax_loop<D>(p, ss, tmem, warp / kGroupWarps);
+    fp8_softmax_loop<D>(p, ss, xs, tmem, warp / kGroupWarps);
     __syncwarp();
   }
 

@@ -20,6 +20,7 @@
 #include "attn_fp8_kernel.cuh"
 #include "attn_fwd_kernel.cuh"
 #include "attn_fwd_pair_kernel.cuh"
+#include "attn_fwd_row_kernel.cuh"
 #include "attn_host.h"
 
 namespace {
@@ -125,6 +126,22 @@ cudaError_t set_smem_attributes() {
   if ((e = cudaFuncSetAttribute(attn::fp8_quant_stage1_kernel<128>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 attn::QuantCfg<128>::kSmemBytes)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(attn::attn_fwd_row_kernel<64, attn::kModePlain>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                FwdCfg<64>::kSmemBytes)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(attn::attn_fwd_row_kernel<128, attn::kModePlain>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                FwdCfg<128>::kSmemBytes)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(attn::attn_fwd_row_kernel<64, attn::kModeWindow>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                FwdCfg<64>::kSmemBytes)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(attn::attn_fwd_row_kernel<128, attn::kModeWindow>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                FwdCfg<128>::kSmemBytes)) != cudaSuccess)
     return e;
   if ((e = cudaFuncSetAttribute(attn::attn_fwd_pair_kernel,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -237,10 +254,25 @@ float exp2_scale(float scale) {
   return (float)std::max((double)scale * 1.4426950408889634, (double)FLT_MIN);
 }
 
+// The library's choice of softmax layout for the one-CTA kernels (attn_fwd_options.kernel
+// 0): one thread per query row, which measured faster at both head dims (same-process,
+// TFLOP/s: GPT-2 shaped causal 377 against 347, long causal 1457 against 1327, long
+// non-causal 1520 against 1408, stress 1525 against 1363); kernel 1 keeps two.
+bool one_thread_per_row(int d, int kernel) {
+  (void)d;
+  return kernel != 1;
+}
+
+// rows: one softmax thread per query row (attn_fwd_row_kernel) instead of two
 template <int D>
 int launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                const FwdParams& p, int grid, cudaStream_t s) {
-  if (p.wl >= 0 || p.wr >= 0)
+                const FwdParams& p, int grid, cudaStream_t s, bool rows = false) {
+  const bool window = p.wl >= 0 || p.wr >= 0;
+  if (rows && window)
+    attn::attn_fwd_row_kernel<D, attn::kModeWindow><<<grid, attn::kRowThreads, FwdCfg<D>::kSmemBytes, s>>>(mq, mk, mv, p);
+  else if (rows)
+    attn::attn_fwd_row_kernel<D, attn::kModePlain><<<grid, attn::kRowThreads, FwdCfg<D>::kSmemBytes, s>>>(mq, mk, mv, p);
+  else if (window)
     attn::attn_fwd_kernel<D, attn::kModeWindow><<<grid, attn::kThreads, FwdCfg<D>::kSmemBytes, s>>>(mq, mk, mv, p);
   else
     attn::attn_fwd_kernel<D, attn::kModePlain><<<grid, attn::kThreads, FwdCfg<D>::kSmemBytes, s>>>(mq, mk, mv, p);
@@ -343,7 +375,9 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* l
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
   }
   if (opts && opts->max_ctas > 0 && opts->max_ctas < grid) grid = opts->max_ctas;
-  return d == 64 ? launch_attn<64>(mq, mk, mv, p, grid, s) : launch_attn<128>(mq, mk, mv, p, grid, s);
+  const bool rows = one_thread_per_row(d, opts ? opts->kernel : 0);
+  return d == 64 ? launch_attn<64>(mq, mk, mv, p, grid, s, rows)
+                 : launch_attn<128>(mq, mk, mv, p, grid, s, rows);
 }
 
 }  // namespace
@@ -709,7 +743,9 @@ int attn_fwd_noalloc_impl(const void* q, const void* k, const void* v, void* o, 
     grid = (int)units;
   }
   if (opts && opts->max_ctas > 0 && opts->max_ctas < grid) grid = opts->max_ctas;
-  return d == 64 ? launch_attn<64>(mq, mk, mv, p, grid, s) : launch_attn<128>(mq, mk, mv, p, grid, s);
+  const bool rows = one_thread_per_row(d, opts ? opts->kernel : 0);
+  return d == 64 ? launch_attn<64>(mq, mk, mv, p, grid, s, rows)
+                 : launch_attn<128>(mq, mk, mv, p, grid, s, rows);
 }
 
 }  // namespace

@@ -271,6 +271,10 @@ struct SharedState {
   uint32_t tmem_base;
   volatile int abort_flag;
   volatile int unit_ring[kUnitSlots];
+};
+
+// Row maxima and sums exchanged by the two softmax warps that share rows.
+struct RowExchange {
   float row_max[2][kQTiles][2][kBM];   // [tile parity][group][column half][row]
   float row_sum[kQTiles][2][2][kBM];   // [group][column half][l, l_fix][row]
 };
@@ -301,7 +305,8 @@ __device__ __forceinline__ uint32_t bar_addr(SharedState& ss, int bar) {
 }
 
 // ------------------------------------------------------------ producer --
-template <int D, int kMode>
+// kStages: slots of the K/V ring (the kernel's shared-memory layout decides)
+template <int D, int kMode, int kStages = FwdCfg<D>::kStages>
 __device__ __forceinline__ void producer_loop(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                               const CUtensorMap* tm_v, const FwdParams& p,
                                               SharedState& ss, uint8_t* sQ, uint8_t* sRing,
@@ -344,9 +349,9 @@ __device__ __forceinline__ void producer_loop(const CUtensorMap* tm_q, const CUt
       // K_0(j), V_1(j-1), K_1(j), each while the group's range lasts
       const int nk[2] = {un.nkv, un.nkvb}, k0s[2] = {un.kv0, un.kv0b};
       auto push = [&](int kind, int g, int j) -> bool {
-        const int slot = ring % C::kStages;
-        const uint32_t n = ring / C::kStages;
-        if (n > 0 && !wait_bar(ss, kBarKV + C::kStages + slot, (n - 1) & 1, p, 4)) return false;
+        const int slot = ring % kStages;
+        const uint32_t n = ring / kStages;
+        if (n > 0 && !wait_bar(ss, kBarKV + kStages + slot, (n - 1) & 1, p, 4)) return false;
         const uint32_t full = bar_addr(ss, kBarKV + slot);
         mbar_arrive_expect_tx(full, C::kTileBytes);
         const int k0 = un.k_tok0 + kv_tile_start(un, k0s[g] + j);
@@ -369,9 +374,9 @@ __device__ __forceinline__ void producer_loop(const CUtensorMap* tm_q, const CUt
       for (int j = 0; j < un.nkv; ++j) {
         const int k0 = un.k_tok0 + kv_tile_start(un, un.kv0 + j);
         for (int kind = 0; kind < 2; ++kind) {
-          const int slot = ring % C::kStages;
-          const uint32_t n = ring / C::kStages;
-          if (n > 0 && !wait_bar(ss, kBarKV + C::kStages + slot, (n - 1) & 1, p, 2)) return;
+          const int slot = ring % kStages;
+          const uint32_t n = ring / kStages;
+          if (n > 0 && !wait_bar(ss, kBarKV + kStages + slot, (n - 1) & 1, p, 2)) return;
           const uint32_t full = bar_addr(ss, kBarKV + slot);
           mbar_arrive_expect_tx(full, C::kTileBytes);
           if (p.fault_inject == 1 && blockIdx.x == 0 && !injected && kind == 0) {
@@ -649,8 +654,8 @@ __device__ __forceinline__ bool pair_sync_check(int g, int quadrant, bool fail) 
 }
 
 template <int D, int kMode>
-__device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss, uint32_t tmem,
-                                             int g, int n_units) {
+__device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss, RowExchange& xs,
+                                             uint32_t tmem, int g, int n_units) {
   using C = FwdCfg<D>;
   constexpr int kOCols = D / 2;             // O columns rescaled / stored by this thread
   const int warp = threadIdx.x / 32;
@@ -759,10 +764,10 @@ __device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss
         mx3 = max3(mx3, s[c + 6], s[c + 7]);
       }
       const float mine = fmaxf(max3(mx0, mx1, mx2), mx3);
-      ss.row_max[j & 1][g][half][trow] = mine;
+      xs.row_max[j & 1][g][half][trow] = mine;
       // (also orders both halves' S loads before any P store)
       pair_sync(g, quadrant);
-      const float mx = fmaxf(mine, ss.row_max[j & 1][g][half ^ 1][trow]);
+      const float mx = fmaxf(mine, xs.row_max[j & 1][g][half ^ 1][trow]);
       const float m_new = fmaxf(m_used, mx);
       // O correction decision: only when the row max grew by more than 2^16
       // (warp-uniform; the partner warp holds the same rows and decides alike)
@@ -824,11 +829,11 @@ __device__ __forceinline__ void softmax_loop(const FwdParams& p, SharedState& ss
     // Epilogue: the two halves' sums are combined; O / l_r -> bf16 (each
     // thread its D/2 columns), LSE = scale * m + ln(l).  Rows before the
     // nominal tile start (recomputed) and rows past the sequence are skipped.
-    ss.row_sum[g][half][0][trow] = l;
-    ss.row_sum[g][half][1][trow] = l_fix;
+    xs.row_sum[g][half][0][trow] = l;
+    xs.row_sum[g][half][1][trow] = l_fix;
     pair_sync(g, quadrant);
-    l += ss.row_sum[g][half ^ 1][0][trow];
-    const float l_r = l + l_fix + ss.row_sum[g][half ^ 1][1][trow];
+    l += xs.row_sum[g][half ^ 1][0][trow];
+    const float l_r = l + l_fix + xs.row_sum[g][half ^ 1][1][trow];
     u = -1;
     if (!fail) fail = !next_unit(ss, p, uslot, true, u);
     // (also: both halves have read row_sum before the next unit writes it)
@@ -930,6 +935,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ SharedState ss;
+  __shared__ RowExchange xs;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
@@ -987,7 +993,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __syncwarp();
   } else {
     setmaxnreg_inc<kSoftmaxRegs>();
-    softmax_loop<D, kMode>(p, ss, tmem, warp / kGroupWarps, n_units);
+    softmax_loop<D, kMode>(p, ss, xs, tmem, warp / kGroupWarps, n_units);
     __syncwarp();
   }
 

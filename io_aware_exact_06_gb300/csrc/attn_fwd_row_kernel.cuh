@@ -1,0 +1,332 @@
+// Fused exact softmax-attention forward for sm_103a with one softmax thread
+// per query row (plain and sliding-window masks, d = 64 or 128, dense or
+// packed batches).
+//
+// The work units, the TMA producer, the MMA issuer, the TMEM layout and the
+// ping-pong of two query tiles are those of attn_fwd_kernel (see there); the
+// softmax differs.  Each query tile has four softmax warps, one per TMEM
+// row quadrant, and each thread owns one row and all 128 key columns of the
+// tile: the row maximum, the exponentials, the row sums and the O epilogue
+// of a row stay in one thread, with no exchange between warps (the layout of
+// the FA-4 softmax: "FlashAttention 1-4 演进速查" (argus-lessons),
+// FlashAttention-4 items).  The scores of a row take 128 registers, so the
+// softmax warps get 184 registers each and the control warps 120 (setmaxnreg).
+//
+// CTA layout (384 threads = 3 warpgroups, one CTA per SM, persistent):
+//   warps 0-3   softmax group 0 (query tile 0 of the unit), warps 4-7 group
+//               1: warp w reads TMEM lanes 32 (w % 4) .. (its 32 rows)
+//   warp  8     TMA producer (lane 0)
+//   warp  9     MMA issuer (lane 0) and TMEM owner
+//   warps 10-11 idle
+#pragma once
+
+#include "attn_fwd_kernel.cuh"
+
+namespace attn {
+
+constexpr int kRowGroupWarps = 4;
+constexpr int kRowSoftmaxWarps = kQTiles * kRowGroupWarps;
+constexpr int kRowProducerWarp = kRowSoftmaxWarps;
+constexpr int kRowMmaWarp = kRowSoftmaxWarps + 1;
+constexpr int kRowThreads = 32 * (kRowSoftmaxWarps + 4);
+constexpr int kRowLaunchRegs = 168;   // 65536 / 384, rounded down to 8
+constexpr int kRowSoftmaxRegs = 184;
+constexpr int kRowControlRegs = 120;
+constexpr int kRowUnitConsumers = 1 + kRowSoftmaxWarps;  // the MMA thread and every softmax warp
+static_assert(kRowThreads == 384, "three warpgroups");
+static_assert(kRowSoftmaxWarps * 32 * kRowSoftmaxRegs + 128 * kRowControlRegs <= kRowThreads * kRowLaunchRegs,
+              "register split exceeds the launch allotment");
+// each of the SM's four register-file quarters holds two softmax warps and
+// one control warp
+static_assert(2 * 32 * kRowSoftmaxRegs + 32 * kRowControlRegs <= 16384, "register-file quarter");
+
+// The softmax of query tile g of every unit, one thread per row.
+template <int D, int kMode>
+__device__ __forceinline__ void softmax_rows(const FwdParams& p, SharedState& ss, uint32_t tmem,
+                                             int g, int n_units) {
+  using C = FwdCfg<D>;
+  static_assert(kMode == kModePlain || kMode == kModeWindow, "plain and window masks");
+  constexpr bool kWindow = kMode == kModeWindow;
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int quadrant = warp % 4;
+  const int trow = quadrant * 32 + lane;       // row within the tile = TMEM lane
+  const uint32_t lane_addr = tmem + ((uint32_t)(quadrant * 32) << 16);
+  const uint32_t colS = C::col_s(g);
+  const uint32_t colO = C::col_o(g);
+  const float c2 = p.scale_log2;
+  uint32_t scount = 0;
+  int units_done = 0;
+  int tokens_total = 0;
+  if (p.cu_seqlens) tokens_total = p.cu_seqlens[p.B];
+
+  uint32_t uslot = 0;
+  int u = -1;
+  if (!next_unit(ss, p, uslot, true, u)) return;
+  while (u >= 0) {
+    const Unit un = decode_unit<kMode>(p, u);
+    const int a0 = q_tile_start(un, g);
+    const int row = a0 + trow;                       // sequence-relative row of this thread
+    const int nominal0 = un.qb * kUnitRows + g * kBM;
+    const int n_tiles = g == 0 ? lower_tiles<kMode>(p, un) : un.nkv;
+    float m_used = -INFINITY;
+    float l = 0.f;     // sum of the fp32 probabilities: the LSE
+    float l_fix = 0.f; // rounding change of each half tile's largest probability
+    for (int j = 0; j < n_tiles; ++j) {
+      if (!__all_sync(0xffffffffu, wait_bar(ss, kBarSFull + g, scount & 1, p, 60 + g))) return;
+      ++scount;
+      tc_fence_after();
+      float s[kBN];
+#pragma unroll
+      for (int k = 0; k < kBN / 32; ++k) {
+        uint32_t r[32];
+        tmem_ld_x32(lane_addr + colS + 32 * k, r);
+        tmem_ld_wait_x32(r);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) s[32 * k + c] = __uint_as_float(r[c]);
+      }
+      // Mask: keys already visited by the previous tile (pulled-back last
+      // tile), keys after this row when causal, keys outside the sliding
+      // window.  Decided per group, applied per row: this row's visible
+      // columns [lo, hi] form one range, masked from a bit mask per 32 columns.
+      const int jt = un.kv0 + j;
+      const int b0 = kv_tile_start(un, jt);
+      const int max_klo = (kWindow && p.wl >= 0) ? max(0, a0 + kBM - 1 - p.wl) : 0;
+      int min_khi = p.causal ? a0 : un.L - 1;
+      if (kWindow && p.wr >= 0) min_khi = min(min_khi, a0 + p.wr);
+      if (jt * kBN > b0 || b0 < max_klo || b0 + kBN - 1 > min_khi) {
+        int klo = (kWindow && p.wl >= 0) ? max(0, row - p.wl) : 0;
+        int khi = p.causal ? row : un.L - 1;
+        if (kWindow && p.wr >= 0) khi = min(khi, row + p.wr);
+        klo = max(klo, jt * kBN);
+        const int lo = klo - b0;
+        const int hi = min(khi - b0, kBN - 1);
+#pragma unroll
+        for (int k = 0; k < kBN / 32; ++k) {
+          const int lo_k = lo - 32 * k, hi_k = hi - 32 * k;
+          const bool none = hi_k < 0 || lo_k > 31 || hi_k < lo_k;
+          const uint32_t vis =
+              none ? 0u : (0xffffffffu >> (31 - min(hi_k, 31))) & (0xffffffffu << max(lo_k, 0));
+#pragma unroll
+          for (int c = 0; c < 32; ++c) s[32 * k + c] = (vis >> c) & 1u ? s[32 * k + c] : -INFINITY;
+        }
+      }
+      // row maximum of each 64-key half (four 3-input max chains each)
+      float mine[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float* sh = s + 64 * h;
+        float mx0 = fmaxf(sh[0], sh[1]), mx1 = fmaxf(sh[2], sh[3]);
+        float mx2 = fmaxf(sh[4], sh[5]), mx3 = fmaxf(sh[6], sh[7]);
+#pragma unroll
+        for (int c = 8; c < 64; c += 8) {
+          mx0 = max3(mx0, sh[c], sh[c + 1]);
+          mx1 = max3(mx1, sh[c + 2], sh[c + 3]);
+          mx2 = max3(mx2, sh[c + 4], sh[c + 5]);
+          mx3 = max3(mx3, sh[c + 6], sh[c + 7]);
+        }
+        mine[h] = fmaxf(max3(mx0, mx1, mx2), mx3);
+      }
+      const float m_new = fmaxf(m_used, fmaxf(mine[0], mine[1]));
+      // O correction decision: only when the row max grew by more than 2^16
+      // (a row whose keys so far were all hidden has O = 0 and l = 0: its
+      // first visible key sets the reference without a rescale)
+      float alpha = 1.0f;
+      bool resc = false;
+      if (m_used == -INFINITY) {
+        m_used = m_new;
+      } else if ((m_new - m_used) * c2 > kRescaleLog2) {
+        resc = true;
+        alpha = ex2_approx((m_used - m_new) * c2);
+        m_used = m_new;
+      }
+      const bool rescale_warp = __any_sync(0xffffffffu, resc);
+      const float neg = m_used == -INFINITY ? 0.f : -m_used * c2;
+      // O is divided by l plus the bf16 rounding change of the largest
+      // probability of each 64-key half tile (same arithmetic as below, so
+      // each p_max is bit-identical to the value written to P)
+      float fix = 0.f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float p_max = ex2_approx(fmaf(mine[h], c2, neg));
+        fix += bf16_round_f32(p_max) - p_max;
+      }
+      // p = 2^(c2 s - c2 m): packed fp32x2 FMA, MUFU ex2, packed sums; P goes
+      // to TMEM 32 keys at a time (bf16 pairs over the first 64 columns of
+      // S_g, whose scores this thread already holds)
+      float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
+#pragma unroll
+      for (int k = 0; k < kBN / 32; ++k) {
+        uint32_t pw[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+          float x0, x1, x2, x3;
+          fma2(x0, x1, s[32 * k + c], s[32 * k + c + 1], c2, neg);
+          fma2(x2, x3, s[32 * k + c + 2], s[32 * k + c + 3], c2, neg);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+          add2(sa0, sa1, p0, p1);
+          add2(sb0, sb1, p2, p3);
+          pw[c / 2] = pack_bf16x2(p0, p1);
+          pw[c / 2 + 1] = pack_bf16x2(p2, p3);
+        }
+        tmem_st_x16(lane_addr + colS + 16 * k, pw);
+      }
+      l = l * alpha + ((sa0 + sa1) + (sb0 + sb1));
+      l_fix = l_fix * alpha + fix;
+      // O *= alpha before this tile's P V product (the previous one has
+      // finished: S of this tile was issued after it)
+      if (rescale_warp) {
+#pragma unroll
+        for (int cc = 0; cc < D; cc += 32) {
+          uint32_t r[32];
+          tmem_ld_x32(lane_addr + colO + cc, r);
+          tmem_ld_wait_x32(r);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
+          tmem_st_x32(lane_addr + colO + cc, r);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar_addr(ss, kBarPFull + g));
+    }
+    // Epilogue: O / l_r -> bf16 (this thread: its row, all D columns), LSE =
+    // scale * m + ln(l).  Rows before the nominal tile start (recomputed) and
+    // rows past the sequence are not stored.  The next unit's index is taken
+    // first (the producer published it long ago).
+    const int cur_seq = un.seq, cur_h = un.h, cur_tok0 = un.tok0, cur_L = un.L;
+    int u_next = -1;
+    if (!next_unit(ss, p, uslot, true, u_next)) return;
+    if (!__all_sync(0xffffffffu, wait_bar(ss, kBarOFull + g, units_done & 1, p, 62 + g))) return;
+    tc_fence_after();
+    const float l_r = l + l_fix;
+    const bool store = row >= nominal0 && row < cur_L && row >= 0;
+    const float inv_l = l_r > 0.f ? 1.0f / l_r : 0.f;
+    __nv_bfloat16* orow = p.o + ((size_t)(store ? cur_tok0 + row : 0) * p.H + cur_h) * D;
+#pragma unroll
+    for (int cc = 0; cc < D; cc += 32) {
+      uint32_t r[32];
+      tmem_ld_x32(lane_addr + colO + cc, r);
+      tmem_ld_wait_x32(r);
+      if (store) {
+        uint4* dst = reinterpret_cast<uint4*>(orow + cc);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(r[8 * i + 0]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l);
+          w.y = pack_bf16x2(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l);
+          w.z = pack_bf16x2(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l);
+          w.w = pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l);
+          dst[i] = w;
+        }
+      }
+    }
+    if (store) {
+      const float lse = l > 0.f ? m_used * p.scale + __log2f(l) * 0.69314718055994531f : -INFINITY;
+      size_t idx;
+      if (p.cu_seqlens)
+        idx = (size_t)cur_h * tokens_total + cur_tok0 + row;
+      else
+        idx = ((size_t)cur_seq * p.H + cur_h) * p.N + row;
+      p.lse[idx] = lse;
+    }
+    tc_fence_before();
+    ++units_done;
+    u = u_next;
+  }
+}
+
+template <int D, int kMode>
+__global__ void __launch_bounds__(kRowThreads, 1)
+attn_fwd_row_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ SharedState ss;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sRing = smem + C::kSmemQ;
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_addr(ss, kBarQFull), 1);
+    mbar_init(bar_addr(ss, kBarQEmpty), 1);
+    for (int g = 0; g < kQTiles; ++g) {
+      mbar_init(bar_addr(ss, kBarSFull + g), 1);
+      mbar_init(bar_addr(ss, kBarPFull + g), 32 * kRowGroupWarps);
+      mbar_init(bar_addr(ss, kBarOFull + g), 1);
+    }
+    mbar_init(bar_addr(ss, kBarDrain), 1);
+    for (int i = 0; i < kUnitSlots; ++i) {
+      mbar_init(bar_addr(ss, kBarUnitFull + i), 1);
+      mbar_init(bar_addr(ss, kBarUnitEmpty + i), kRowUnitConsumers);
+    }
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar_addr(ss, kBarKV + s), 1);
+      mbar_init(bar_addr(ss, kBarKV + C::kStages + s), 1);
+    }
+    ss.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kRowProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  if (warp == kRowMmaWarp) {
+    tmem_alloc(smem_u32(&ss.tmem_base), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ss.tmem_base;
+  const int n_units = num_units<kMode>(p);
+
+  if (warp >= kRowSoftmaxWarps) {
+    setmaxnreg_dec<kRowControlRegs>();
+    if (warp == kRowProducerWarp) {
+      if (lane == 0) producer_loop<D, kMode>(&tm_q, &tm_k, &tm_v, p, ss, sQ, sRing, n_units);
+    } else if (warp == kRowMmaWarp) {
+      if (lane == 0) {
+        mma_loop<D, kMode>(p, ss, sQ, sRing, tmem, n_units);
+        // every MMA issued by this thread has finished before TMEM is freed
+        mma_commit(bar_addr(ss, kBarDrain));
+        mbar_wait(bar_addr(ss, kBarDrain), 0, 100000000ull);
+      }
+    }
+    __syncwarp();
+  } else {
+    setmaxnreg_inc<kRowSoftmaxRegs>();
+    softmax_rows<D, kMode>(p, ss, tmem, warp / kRowGroupWarps, n_units);
+    __syncwarp();
+  }
+
+  if (ss.abort_flag) {
+    // copies issued before the abort may still be landing: give them 1 ms
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 1000000ull) {
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kRowMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+  if (threadIdx.x == 0) {
+    // every CTA has taken its last unit once all have arrived here: the last
+    // one leaves the counters at zero for the next launch on this workspace
+    __threadfence();
+    if (atomicAdd(p.sched + 1, 1) == (int)gridDim.x - 1) {
+      atomicExch(p.sched, 0);
+      atomicExch(p.sched + 1, 0);
+      __threadfence();
+    }
+  }
+}
+
+}  // namespace attn

@@ -32,17 +32,19 @@ def workload(name):
     return _cache[name]
 
 
+@pytest.mark.parametrize("kernel", ["one_cta", "rows"])
 @pytest.mark.parametrize("name", ["tiny", "gpt2_causal"])
-def test_small_configs_every_row(dev, name):
+def test_small_configs_every_row(dev, name, kernel):
     wl = workload(name)
-    o, lse, st = parity.run_cuda(wl, dev)
+    o, lse, st = parity.run_cuda(wl, dev, **KERNELS[kernel])
     assert st == 0
-    parity.compare(o, lse, wl, inputs.all_rows(wl.cu_seqlens, wl.H), name)
+    parity.compare(o, lse, wl, inputs.all_rows(wl.cu_seqlens, wl.H), f"{name} {kernel}")
 
 
-# d = 128 without a window runs on one CTA per unit by default; kernel=2 asks
-# for the pair-of-SMs kernel, so both stay covered.
-KERNELS = {"pair": {"kernel": 2}, "one_cta": {}}
+# The forward's kernels: one CTA per unit with one softmax thread per query
+# row (kernel=3, the default) or two (kernel=1), and at d = 128 without a
+# window the pair of SMs (kernel=2); every one stays covered.
+KERNELS = {"pair": {"kernel": 2}, "one_cta": {"kernel": 1}, "rows": {"kernel": 3}}
 
 
 @pytest.mark.parametrize("kernel", sorted(KERNELS))
@@ -81,7 +83,8 @@ def test_pair_kernel_bounded_wait_expires(dev):
     parity.compare(o, lse, wl, inputs.all_rows(wl.cu_seqlens, wl.H), "pair after timeout")
 
 
-@pytest.mark.parametrize("d,kernel", [(64, "one_cta"), (128, "pair"), (128, "one_cta")])
+@pytest.mark.parametrize("d,kernel", [(64, "one_cta"), (64, "rows"), (128, "pair"), (128, "one_cta"),
+                                      (128, "rows")])
 @pytest.mark.parametrize("causal", [False, True])
 def test_ragged_packed_lengths(dev, d, causal, kernel):
     lens = [1, 127, 128, 129, 0, 255, 256, 257, 300, 2, 513]
