@@ -129,19 +129,19 @@ cudaError_t set_smem_attributes() {
     return e;
   if ((e = cudaFuncSetAttribute(attn::attn_fwd_row_kernel<64, attn::kModePlain>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                FwdCfg<64>::kSmemBytes)) != cudaSuccess)
+                                attn::RowCfg<64>::kSmemBytes)) != cudaSuccess)
     return e;
   if ((e = cudaFuncSetAttribute(attn::attn_fwd_row_kernel<128, attn::kModePlain>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                FwdCfg<128>::kSmemBytes)) != cudaSuccess)
+                                attn::RowCfg<128>::kSmemBytes)) != cudaSuccess)
     return e;
   if ((e = cudaFuncSetAttribute(attn::attn_fwd_row_kernel<64, attn::kModeWindow>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                FwdCfg<64>::kSmemBytes)) != cudaSuccess)
+                                attn::RowCfg<64>::kSmemBytes)) != cudaSuccess)
     return e;
   if ((e = cudaFuncSetAttribute(attn::attn_fwd_row_kernel<128, attn::kModeWindow>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                FwdCfg<128>::kSmemBytes)) != cudaSuccess)
+                                attn::RowCfg<128>::kSmemBytes)) != cudaSuccess)
     return e;
   if ((e = cudaFuncSetAttribute(attn::attn_fwd_pair_kernel,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -269,9 +269,9 @@ int launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap&
                 const FwdParams& p, int grid, cudaStream_t s, bool rows = false) {
   const bool window = p.wl >= 0 || p.wr >= 0;
   if (rows && window)
-    attn::attn_fwd_row_kernel<D, attn::kModeWindow><<<grid, attn::kRowThreads, FwdCfg<D>::kSmemBytes, s>>>(mq, mk, mv, p);
+    attn::attn_fwd_row_kernel<D, attn::kModeWindow><<<grid, attn::kRowThreads, attn::RowCfg<D>::kSmemBytes, s>>>(mq, mk, mv, p);
   else if (rows)
-    attn::attn_fwd_row_kernel<D, attn::kModePlain><<<grid, attn::kRowThreads, FwdCfg<D>::kSmemBytes, s>>>(mq, mk, mv, p);
+    attn::attn_fwd_row_kernel<D, attn::kModePlain><<<grid, attn::kRowThreads, attn::RowCfg<D>::kSmemBytes, s>>>(mq, mk, mv, p);
   else if (window)
     attn::attn_fwd_kernel<D, attn::kModeWindow><<<grid, attn::kThreads, FwdCfg<D>::kSmemBytes, s>>>(mq, mk, mv, p);
   else

@@ -133,8 +133,17 @@ enum : int {
   kBarUnitFull = 9,    // +slot
   kBarUnitEmpty = 11,  // +slot
   kBarKV = 13,     // kv_full[s] = kBarKV + s, kv_empty[s] = kBarKV + kStages + s
+  kBarQFull1 = 29,   // second Q buffer (kernels that double-buffer Q by unit)
+  kBarQEmpty1 = 30,
+  kBarSFree = 31,    // +g: the softmax of group g has read S_g (kernels with P apart from S)
+  kBarPFree = 33,    // +g: the P V product of group g finished (same kernels)
+  kBarDrain1 = 35,   // a second MMA-issuing thread's products all finished
 };
-constexpr int kMaxBars = kBarKV + 2 * 8;
+constexpr int kMaxBars = kBarDrain1 + 1;
+static_assert(kBarKV + 2 * 8 <= kBarQFull1, "K/V ring barriers");
+// Barriers of Q buffer b.
+__device__ __forceinline__ int bar_qfull(int b) { return b == 0 ? kBarQFull : kBarQFull1; }
+__device__ __forceinline__ int bar_qempty(int b) { return b == 0 ? kBarQEmpty : kBarQEmpty1; }
 constexpr int kUnitSlots = 2;            // unit indices published by the producer
 constexpr int kUnitConsumers = 1 + kSoftmaxWarps;  // the MMA thread and every softmax warp
 
@@ -305,8 +314,10 @@ __device__ __forceinline__ uint32_t bar_addr(SharedState& ss, int bar) {
 }
 
 // ------------------------------------------------------------ producer --
-// kStages: slots of the K/V ring (the kernel's shared-memory layout decides)
-template <int D, int kMode, int kStages = FwdCfg<D>::kStages>
+// kStages: slots of the K/V ring (the kernel's shared-memory layout decides);
+// kQBufs: Q buffers, 1 or 2 (with 2 the Q tiles of unit n go to buffer n % 2,
+// so they load while unit n - 1 still runs).
+template <int D, int kMode, int kStages = FwdCfg<D>::kStages, int kQBufs = 1>
 __device__ __forceinline__ void producer_loop(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                               const CUtensorMap* tm_v, const FwdParams& p,
                                               SharedState& ss, uint8_t* sQ, uint8_t* sRing,
@@ -335,14 +346,20 @@ __device__ __forceinline__ void producer_loop(const CUtensorMap* tm_q, const CUt
       u = next_u;
       continue;
     }
-    if (units_done > 0 && !wait_bar(ss, kBarQEmpty, (units_done - 1) & 1, p, 1)) return;
-    mbar_arrive_expect_tx(bar_addr(ss, kBarQFull), kQTiles * C::kTileBytes);
-    for (int g = 0; g < kQTiles; ++g) {
-      // (paired ranges: both groups hold the unit's one query tile)
-      const int r0 = un.tok0 + q_tile_start(un, kMode == kModeSplitPair ? 0 : g);
-      for (int c = 0; c < C::kChunks; ++c)
-        tma_load_3d(smem_u32(sQ + g * C::kTileBytes + c * kChunkBytes), tm_q,
-                    bar_addr(ss, kBarQFull), c * 64, un.h, r0);
+    {
+      const int qb = units_done % kQBufs;
+      const int qn = units_done / kQBufs;
+      if (qn > 0 && !wait_bar(ss, bar_qempty(qb), (qn - 1) & 1, p, 1)) return;
+      const uint32_t qfull = bar_addr(ss, bar_qfull(qb));
+      uint8_t* sQb = sQ + qb * C::kSmemQ;
+      mbar_arrive_expect_tx(qfull, kQTiles * C::kTileBytes);
+      for (int g = 0; g < kQTiles; ++g) {
+        // (paired ranges: both groups hold the unit's one query tile)
+        const int r0 = un.tok0 + q_tile_start(un, kMode == kModeSplitPair ? 0 : g);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(smem_u32(sQb + g * C::kTileBytes + c * kChunkBytes), tm_q, qfull, c * 64,
+                      un.h, r0);
+      }
     }
     if constexpr (kMode == kModeSplitPair) {
       // the MMA thread's order: K_0(0), K_1(0), then per step j: V_0(j-1),
@@ -505,14 +522,14 @@ __device__ __forceinline__ bool mma_unit_pair(const FwdParams& p, SharedState& s
   return true;
 }
 
-template <int D, int kMode>
+// kQBufs: as for producer_loop.
+template <int D, int kMode, int kQBufs = 1>
 __device__ __forceinline__ void mma_loop(const FwdParams& p, SharedState& ss, uint8_t* sQ,
                                          uint8_t* sRing, uint32_t tmem, int n_units) {
   using C = FwdCfg<D>;
   uint32_t ring = 0;
   uint32_t pcount[2] = {0, 0};
   int units_done = 0;
-  const uint32_t q_smem[2] = {smem_u32(sQ), smem_u32(sQ + C::kTileBytes)};
   auto slot_smem = [&](uint32_t pos) { return smem_u32(sRing + (pos % C::kStages) * C::kTileBytes); };
   auto wait_full = [&](uint32_t pos) {
     return wait_bar(ss, kBarKV + pos % C::kStages, (pos / C::kStages) & 1, p, 10);
@@ -529,11 +546,15 @@ __device__ __forceinline__ void mma_loop(const FwdParams& p, SharedState& ss, ui
     if (kMode == kModeSplit && un.nkv <= 0) continue;
     if (kMode == kModeSplitPair) {
       if (un.nkv <= 0 && un.nkvb <= 0) continue;
+      const uint32_t q_smem[2] = {smem_u32(sQ), smem_u32(sQ + C::kTileBytes)};
       if (!mma_unit_pair<D>(p, ss, q_smem, sRing, tmem, un, units_done, ring, pcount)) return;
       ++units_done;
       continue;
     }
-    if (!wait_bar(ss, kBarQFull, units_done & 1, p, 11)) return;
+    const int qb = units_done % kQBufs;
+    const uint32_t q_smem[2] = {smem_u32(sQ + qb * C::kSmemQ),
+                                smem_u32(sQ + qb * C::kSmemQ + C::kTileBytes)};
+    if (!wait_bar(ss, bar_qfull(qb), (units_done / kQBufs) & 1, p, 11)) return;
     tc_fence_after();
     // group 0 may skip the unit's last tile (lower_tiles); group 1 visits all
     const int n0 = lower_tiles<kMode>(p, un);
@@ -546,8 +567,8 @@ __device__ __forceinline__ void mma_loop(const FwdParams& p, SharedState& ss, ui
       mma_commit(bar_addr(ss, kBarSFull + g));
     }
     release(posK);
-    // Q is free for the next unit's copy once the unit's last S product is done
-    if (un.nkv == 1) mma_commit(bar_addr(ss, kBarQEmpty));
+    // Q is free for a later unit's copy once the unit's last S product is done
+    if (un.nkv == 1) mma_commit(bar_addr(ss, bar_qempty(qb)));
     for (int j = 1; j <= un.nkv; ++j) {
       const bool more = j < un.nkv;
       uint32_t nextK = 0, nextV = 0;
@@ -583,7 +604,7 @@ __device__ __forceinline__ void mma_loop(const FwdParams& p, SharedState& ss, ui
       }
       if (more) {
         release(nextK);
-        if (j == un.nkv - 1) mma_commit(bar_addr(ss, kBarQEmpty));
+        if (j == un.nkv - 1) mma_commit(bar_addr(ss, bar_qempty(qb)));
         posV = nextV;
       }
     }

@@ -16,8 +16,9 @@
 //   warps 0-3   softmax group 0 (query tile 0 of the unit), warps 4-7 group
 //               1: warp w reads TMEM lanes 32 (w % 4) .. (its 32 rows)
 //   warp  8     TMA producer (lane 0)
-//   warp  9     MMA issuer (lane 0) and TMEM owner
-//   warps 10-11 idle
+//   warp  9     MMA issuer (lane 0; at d = 64 of the S products) and TMEM owner
+//   warp  10    at d = 64: issuer of the P V products (lane 0); else idle
+//   warp  11    idle
 #pragma once
 
 #include "attn_fwd_kernel.cuh"
@@ -28,11 +29,11 @@ constexpr int kRowGroupWarps = 4;
 constexpr int kRowSoftmaxWarps = kQTiles * kRowGroupWarps;
 constexpr int kRowProducerWarp = kRowSoftmaxWarps;
 constexpr int kRowMmaWarp = kRowSoftmaxWarps + 1;
+constexpr int kRowPvWarp = kRowSoftmaxWarps + 2;
 constexpr int kRowThreads = 32 * (kRowSoftmaxWarps + 4);
 constexpr int kRowLaunchRegs = 168;   // 65536 / 384, rounded down to 8
 constexpr int kRowSoftmaxRegs = 184;
 constexpr int kRowControlRegs = 120;
-constexpr int kRowUnitConsumers = 1 + kRowSoftmaxWarps;  // the MMA thread and every softmax warp
 static_assert(kRowThreads == 384, "three warpgroups");
 static_assert(kRowSoftmaxWarps * 32 * kRowSoftmaxRegs + 128 * kRowControlRegs <= kRowThreads * kRowLaunchRegs,
               "register split exceeds the launch allotment");
@@ -40,13 +41,127 @@ static_assert(kRowSoftmaxWarps * 32 * kRowSoftmaxRegs + 128 * kRowControlRegs <=
 // one control warp
 static_assert(2 * 32 * kRowSoftmaxRegs + 32 * kRowControlRegs <= 16384, "register-file quarter");
 
+// Shared memory of the kernel: Q tiles, the K/V ring and, at d = 64, where
+// they fit, a second Q buffer (the next unit's Q tiles load while the
+// current unit runs) and an O staging tile per query tile (the epilogue
+// writes each warp's 32 rows there and stores them to global memory four
+// whole rows per instruction).
+//
+// At d = 64 TMEM also has room for P apart from S (S_g [128 g, +128), O_g
+// [256 + 64 g, +64), P_g [384 + 64 g, +64)), so a group's next S product is
+// issued as soon as its softmax has read S and runs during that softmax
+// (mma_s_loop, mma_pv_loop); at d = 128 P takes the first 64 columns of S_g.
+template <int D>
+struct RowCfg {
+  using C = FwdCfg<D>;
+  static constexpr int kQBufs = D == 64 ? 2 : 1;
+  static constexpr bool kStageO = D == 64;
+  static constexpr bool kSPre = D == 64;
+  __host__ __device__ static constexpr uint32_t col_p(int g) {
+    return kSPre ? 384u + 64u * (uint32_t)g : C::col_s(g);
+  }
+  static constexpr int kSmemStage = kStageO ? kQTiles * C::kTileBytes : 0;
+  static constexpr int kSmemBytes = kQBufs * C::kSmemQ + C::kSmemRing + kSmemStage + 1024;
+};
+static_assert(RowCfg<64>::kSmemBytes + 1024 <= 227 * 1024, "shared memory of the d = 64 kernel");
+// Readers of each published unit index: the MMA thread(s) and every softmax warp.
+template <int D>
+__host__ __device__ constexpr int row_unit_consumers() {
+  return (RowCfg<D>::kSPre ? 2 : 1) + kRowSoftmaxWarps;
+}
+static_assert(RowCfg<128>::kSmemBytes + 1024 <= 227 * 1024, "shared memory of the d = 128 kernel");
+
+// MMA issuers of the d = 64 layout (P apart from S): two threads, so that
+// neither stream of products waits behind the other's issue (an issuing
+// thread returns from tcgen05.mma only as the tensor pipe takes it).
+//   mma_s_loop   S_g of every tile: after the group's softmax has read its
+//                previous S (SFree); K slots released here; runs on into the
+//                next unit (its Q tiles in the other Q buffer).
+//   mma_pv_loop  O_g += P_g V of every tile: after P_g (PFull); each product
+//                signals PFree, the unit's last one OFull; V slots released here.
+// Ring positions follow the producer's order, K_0, V_0, K_1, V_1, ... per unit.
+template <int D, int kMode>
+__device__ __forceinline__ void mma_s_loop(const FwdParams& p, SharedState& ss, uint8_t* sQ,
+                                           uint8_t* sRing, uint32_t tmem) {
+  using C = FwdCfg<D>;
+  using R = RowCfg<D>;
+  static_assert(R::kSPre && R::kQBufs == 2, "layout with P apart from S and two Q buffers");
+  uint32_t sfree[2] = {0, 0};
+  bool first[2] = {true, true};
+  uint32_t uslot = 0, base = 0;
+  for (int ux = 0;; ++ux) {
+    int u;
+    if (!next_unit(ss, p, uslot, false, u) || u < 0) return;
+    const Unit un = decode_unit<kMode>(p, u);
+    // group 0 may skip the unit's last tile (lower_tiles); group 1 visits all
+    const int n[2] = {lower_tiles<kMode>(p, un), un.nkv};
+    const int qb = ux % R::kQBufs;
+    if (!wait_bar(ss, bar_qfull(qb), (ux / R::kQBufs) & 1, p, 11)) return;
+    for (int j = 0; j < un.nkv; ++j) {
+      const uint32_t posK = base + 2 * j;
+      if (!wait_bar(ss, kBarKV + posK % C::kStages, (posK / C::kStages) & 1, p, 10)) return;
+      tc_fence_after();
+      for (int g = 0; g < kQTiles; ++g) {
+        if (j >= n[g]) continue;
+        if (!first[g]) {
+          if (!wait_bar(ss, kBarSFree + g, sfree[g] & 1, p, 18 + g)) return;
+          ++sfree[g];
+          tc_fence_after();
+        }
+        first[g] = false;
+        issue_qk<D>(tmem + C::col_s(g), smem_u32(sQ + qb * C::kSmemQ + g * C::kTileBytes),
+                    smem_u32(sRing + (posK % C::kStages) * C::kTileBytes));
+        mma_commit(bar_addr(ss, kBarSFull + g));
+      }
+      mma_commit(bar_addr(ss, kBarKV + C::kStages + posK % C::kStages));
+      // Q is free for a later unit's copy once the unit's last S product is done
+      if (j == un.nkv - 1) mma_commit(bar_addr(ss, bar_qempty(qb)));
+    }
+    base += 2 * un.nkv;
+  }
+}
+
+template <int D, int kMode>
+__device__ __forceinline__ void mma_pv_loop(const FwdParams& p, SharedState& ss, uint8_t* sRing,
+                                            uint32_t tmem) {
+  using C = FwdCfg<D>;
+  using R = RowCfg<D>;
+  uint32_t pfull[2] = {0, 0};
+  uint32_t uslot = 0, base = 0;
+  for (;;) {
+    int u;
+    if (!next_unit(ss, p, uslot, false, u) || u < 0) return;
+    const Unit un = decode_unit<kMode>(p, u);
+    const int n[2] = {lower_tiles<kMode>(p, un), un.nkv};
+    for (int j = 0; j < un.nkv; ++j) {
+      const uint32_t posV = base + 2 * j + 1;
+      if (!wait_bar(ss, kBarKV + posV % C::kStages, (posV / C::kStages) & 1, p, 10)) return;
+      tc_fence_after();
+      for (int g = 0; g < kQTiles; ++g) {
+        if (j >= n[g]) continue;
+        if (!wait_bar(ss, kBarPFull + g, pfull[g] & 1, p, 12 + g)) return;
+        ++pfull[g];
+        tc_fence_after();
+        issue_pv<D>(tmem + C::col_o(g), tmem + R::col_p(g),
+                    smem_u32(sRing + (posV % C::kStages) * C::kTileBytes), j > 0);
+        mma_commit(bar_addr(ss, kBarPFree + g));
+        if (j == n[g] - 1) mma_commit(bar_addr(ss, kBarOFull + g));
+      }
+      mma_commit(bar_addr(ss, kBarKV + C::kStages + posV % C::kStages));
+    }
+    base += 2 * un.nkv;
+  }
+}
+
 // The softmax of query tile g of every unit, one thread per row.
 template <int D, int kMode>
 __device__ __forceinline__ void softmax_rows(const FwdParams& p, SharedState& ss, uint32_t tmem,
-                                             int g, int n_units) {
+                                             int g, int n_units, uint8_t* sStage) {
   using C = FwdCfg<D>;
+  using R = RowCfg<D>;
   static_assert(kMode == kModePlain || kMode == kModeWindow, "plain and window masks");
   constexpr bool kWindow = kMode == kModeWindow;
+  constexpr bool kSPre = R::kSPre;
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const int quadrant = warp % 4;
@@ -54,8 +169,11 @@ __device__ __forceinline__ void softmax_rows(const FwdParams& p, SharedState& ss
   const uint32_t lane_addr = tmem + ((uint32_t)(quadrant * 32) << 16);
   const uint32_t colS = C::col_s(g);
   const uint32_t colO = C::col_o(g);
+  const uint32_t colP = R::col_p(g);
   const float c2 = p.scale_log2;
   uint32_t scount = 0;
+  uint32_t pfree = 0;     // P V products of this group waited for (P apart from S)
+  bool first_tile = true; // no P V product of this group before this tile
   int units_done = 0;
   int tokens_total = 0;
   if (p.cu_seqlens) tokens_total = p.cu_seqlens[p.B];
@@ -84,6 +202,12 @@ __device__ __forceinline__ void softmax_rows(const FwdParams& p, SharedState& ss
         tmem_ld_wait_x32(r);
 #pragma unroll
         for (int c = 0; c < 32; ++c) s[32 * k + c] = __uint_as_float(r[c]);
+      }
+      if constexpr (kSPre) {
+        // S_g is read: the group's next S product may overwrite it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_addr(ss, kBarSFree + g));
       }
       // Mask: keys already visited by the previous tile (pulled-back last
       // tile), keys after this row when causal, keys outside the sliding
@@ -154,10 +278,12 @@ __device__ __forceinline__ void softmax_rows(const FwdParams& p, SharedState& ss
       // p = 2^(c2 s - c2 m): packed fp32x2 FMA, MUFU ex2, packed sums; P goes
       // to TMEM 32 keys at a time (bf16 pairs over the first 64 columns of
       // S_g, whose scores this thread already holds)
+      // (P apart from S: all of P in registers first; its TMEM columns are
+      // written once the group's previous P V product has finished)
       float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
+      uint32_t pw[kBN / 32][16];
 #pragma unroll
       for (int k = 0; k < kBN / 32; ++k) {
-        uint32_t pw[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 4) {
           float x0, x1, x2, x3;
@@ -167,15 +293,26 @@ __device__ __forceinline__ void softmax_rows(const FwdParams& p, SharedState& ss
           const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
           add2(sa0, sa1, p0, p1);
           add2(sb0, sb1, p2, p3);
-          pw[c / 2] = pack_bf16x2(p0, p1);
-          pw[c / 2 + 1] = pack_bf16x2(p2, p3);
+          pw[k][c / 2] = pack_bf16x2(p0, p1);
+          pw[k][c / 2 + 1] = pack_bf16x2(p2, p3);
         }
-        tmem_st_x16(lane_addr + colS + 16 * k, pw);
+        if (!kSPre) tmem_st_x16(lane_addr + colP + 16 * k, pw[k]);
       }
+      if constexpr (kSPre) {
+        if (!first_tile) {
+          if (!__all_sync(0xffffffffu, wait_bar(ss, kBarPFree + g, pfree & 1, p, 64 + g))) return;
+          ++pfree;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int k = 0; k < kBN / 32; ++k) tmem_st_x16(lane_addr + colP + 16 * k, pw[k]);
+      }
+      first_tile = false;
       l = l * alpha + ((sa0 + sa1) + (sb0 + sb1));
       l_fix = l_fix * alpha + fix;
       // O *= alpha before this tile's P V product (the previous one has
-      // finished: S of this tile was issued after it)
+      // finished: S of this tile was issued after it, or, with P apart from
+      // S, PFree was waited for above)
       if (rescale_warp) {
 #pragma unroll
         for (int cc = 0; cc < D; cc += 32) {
@@ -203,14 +340,18 @@ __device__ __forceinline__ void softmax_rows(const FwdParams& p, SharedState& ss
     const float l_r = l + l_fix;
     const bool store = row >= nominal0 && row < cur_L && row >= 0;
     const float inv_l = l_r > 0.f ? 1.0f / l_r : 0.f;
-    __nv_bfloat16* orow = p.o + ((size_t)(store ? cur_tok0 + row : 0) * p.H + cur_h) * D;
+    if constexpr (RowCfg<D>::kStageO) {
+      // This warp's 32 rows through its staging tile: the thread writes its
+      // row (16-byte chunk c of row r at r * 128 + 16 (c ^ (r % 8)), no bank
+      // conflicts), then lane l stores chunk l % 8 of rows 4 i + l / 8: four
+      // whole rows per store instruction.
+      static_assert(D == 64, "one 128-byte row per thread");
+      uint8_t* stage = sStage + g * FwdCfg<D>::kTileBytes + quadrant * 32 * 128;
 #pragma unroll
-    for (int cc = 0; cc < D; cc += 32) {
-      uint32_t r[32];
-      tmem_ld_x32(lane_addr + colO + cc, r);
-      tmem_ld_wait_x32(r);
-      if (store) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + cc);
+      for (int cc = 0; cc < D; cc += 32) {
+        uint32_t r[32];
+        tmem_ld_x32(lane_addr + colO + cc, r);
+        tmem_ld_wait_x32(r);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           uint4 w;
@@ -218,7 +359,39 @@ __device__ __forceinline__ void softmax_rows(const FwdParams& p, SharedState& ss
           w.y = pack_bf16x2(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l);
           w.z = pack_bf16x2(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l);
           w.w = pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l);
-          dst[i] = w;
+          const int c = cc / 8 + i;
+          *reinterpret_cast<uint4*>(stage + lane * 128 + ((c ^ (lane & 7)) << 4)) = w;
+        }
+      }
+      __syncwarp();
+      const int c = lane & 7;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int rr = 4 * i + (lane >> 3);
+        const uint4 w = *reinterpret_cast<const uint4*>(stage + rr * 128 + ((c ^ (rr & 7)) << 4));
+        const int row_r = a0 + quadrant * 32 + rr;
+        if (row_r >= nominal0 && row_r < cur_L && row_r >= 0)
+          *reinterpret_cast<uint4*>(p.o + ((size_t)(cur_tok0 + row_r) * p.H + cur_h) * D + 8 * c) = w;
+      }
+      __syncwarp();   // every lane has read the tile before the next unit writes it
+    } else {
+      __nv_bfloat16* orow = p.o + ((size_t)(store ? cur_tok0 + row : 0) * p.H + cur_h) * D;
+#pragma unroll
+      for (int cc = 0; cc < D; cc += 32) {
+        uint32_t r[32];
+        tmem_ld_x32(lane_addr + colO + cc, r);
+        tmem_ld_wait_x32(r);
+        if (store) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + cc);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(r[8 * i + 0]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l);
+            w.y = pack_bf16x2(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l);
+            w.z = pack_bf16x2(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l);
+            w.w = pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l);
+            dst[i] = w;
+          }
         }
       }
     }
@@ -242,27 +415,34 @@ __global__ void __launch_bounds__(kRowThreads, 1)
 attn_fwd_row_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using C = FwdCfg<D>;
+  using R = RowCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ SharedState ss;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
-  uint8_t* sRing = smem + C::kSmemQ;
+  uint8_t* sRing = smem + R::kQBufs * C::kSmemQ;
+  uint8_t* sStage = sRing + C::kSmemRing;
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar_addr(ss, kBarQFull), 1);
-    mbar_init(bar_addr(ss, kBarQEmpty), 1);
+    for (int b = 0; b < R::kQBufs; ++b) {
+      mbar_init(bar_addr(ss, bar_qfull(b)), 1);
+      mbar_init(bar_addr(ss, bar_qempty(b)), 1);
+    }
     for (int g = 0; g < kQTiles; ++g) {
       mbar_init(bar_addr(ss, kBarSFull + g), 1);
       mbar_init(bar_addr(ss, kBarPFull + g), 32 * kRowGroupWarps);
+      mbar_init(bar_addr(ss, kBarSFree + g), kRowGroupWarps);
+      mbar_init(bar_addr(ss, kBarPFree + g), 1);
       mbar_init(bar_addr(ss, kBarOFull + g), 1);
     }
     mbar_init(bar_addr(ss, kBarDrain), 1);
+    mbar_init(bar_addr(ss, kBarDrain1), 1);
     for (int i = 0; i < kUnitSlots; ++i) {
       mbar_init(bar_addr(ss, kBarUnitFull + i), 1);
-      mbar_init(bar_addr(ss, kBarUnitEmpty + i), kRowUnitConsumers);
+      mbar_init(bar_addr(ss, kBarUnitEmpty + i), row_unit_consumers<D>());
     }
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(bar_addr(ss, kBarKV + s), 1);
@@ -289,19 +469,29 @@ attn_fwd_row_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   if (warp >= kRowSoftmaxWarps) {
     setmaxnreg_dec<kRowControlRegs>();
     if (warp == kRowProducerWarp) {
-      if (lane == 0) producer_loop<D, kMode>(&tm_q, &tm_k, &tm_v, p, ss, sQ, sRing, n_units);
+      if (lane == 0)
+        producer_loop<D, kMode, C::kStages, R::kQBufs>(&tm_q, &tm_k, &tm_v, p, ss, sQ, sRing, n_units);
     } else if (warp == kRowMmaWarp) {
       if (lane == 0) {
-        mma_loop<D, kMode>(p, ss, sQ, sRing, tmem, n_units);
+        if constexpr (R::kSPre)
+          mma_s_loop<D, kMode>(p, ss, sQ, sRing, tmem);
+        else
+          mma_loop<D, kMode, R::kQBufs>(p, ss, sQ, sRing, tmem, n_units);
         // every MMA issued by this thread has finished before TMEM is freed
         mma_commit(bar_addr(ss, kBarDrain));
         mbar_wait(bar_addr(ss, kBarDrain), 0, 100000000ull);
+      }
+    } else if (R::kSPre && warp == kRowPvWarp) {
+      if (lane == 0) {
+        mma_pv_loop<D, kMode>(p, ss, sRing, tmem);
+        mma_commit(bar_addr(ss, kBarDrain1));
+        mbar_wait(bar_addr(ss, kBarDrain1), 0, 100000000ull);
       }
     }
     __syncwarp();
   } else {
     setmaxnreg_inc<kRowSoftmaxRegs>();
-    softmax_rows<D, kMode>(p, ss, tmem, warp / kRowGroupWarps, n_units);
+    softmax_rows<D, kMode>(p, ss, tmem, warp / kRowGroupWarps, n_units, sStage);
     __syncwarp();
   }
 
