@@ -103,6 +103,8 @@ struct FwdParams {
   float scale_log2;        // scale * log2(e)
   unsigned long long timeout_ns;
   int fault_inject;        // 1: CTA 0 never issues its first K copy (test hook)
+  int pair_group;          // dense, not split: (batch, head) pairs per group of the
+                           // unit order (0: one group of all pairs)
 };
 
 template <int D>
@@ -192,8 +194,11 @@ __device__ __forceinline__ int num_units(const FwdParams& p) {
   return p.B * p.H * nqb * ranges;
 }
 
-// Unit u of the longest-first order.  Dense: q-blocks in decreasing cost
-// (causal cost grows with the q-block index), then batch, then head.  Varlen:
+// Unit u of the longest-first order.  Dense: the (batch, head) pairs in
+// groups of p.pair_group, one group after the other; within a group
+// q-blocks in decreasing cost (causal cost grows with the q-block index),
+// then batch, then head.  A group's keys and values fit in a part of L2, so
+// the units running at one time re-read them from L2 rather than HBM.  Varlen:
 // the scheduler kernel's sorted (seq, q-block) list, then head.  Split-KV:
 // q-blocks in decreasing cost, then KV range, then batch, then head.
 template <int kMode>
@@ -219,8 +224,23 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
       un.split = rem / p.B;
       un.seq = rem - un.split * p.B;
     } else {
-      rank = e / p.B;
-      un.seq = e - rank * p.B;
+      const int P = p.B * p.H;
+      const int G = (p.pair_group > 0 && p.pair_group < P) ? p.pair_group : P;
+      const int full = P / G;
+      int gi, r, npg;
+      if (u < full * G * nqb) {
+        gi = u / (G * nqb);
+        r = u - gi * G * nqb;
+        npg = G;
+      } else {
+        gi = full;
+        r = u - full * G * nqb;
+        npg = P - full * G;
+      }
+      rank = r / npg;
+      const int pair = gi * G + (r - rank * npg);
+      un.seq = pair / p.H;
+      un.h = pair - un.seq * p.H;
     }
     un.qb = nqb - 1 - rank;
     un.tok0 = un.seq * p.N;
@@ -280,6 +300,7 @@ struct SharedState {
   uint32_t tmem_base;
   volatile int abort_flag;
   volatile int unit_ring[kUnitSlots];
+  Unit unit_dec[kUnitSlots];   // the published units, decoded by the producer
 };
 
 // Row maxima and sums exchanged by the two softmax warps that share rows.
@@ -330,10 +351,15 @@ __device__ __forceinline__ void producer_loop(const CUtensorMap* tm_q, const CUt
   int u = blockIdx.x;  // first unit static, then longest-first order by atomic pop
   for (;;) {
     if (u >= n_units) u = -1;
+    // the unit is decoded once, here, and published with its index (the
+    // producer runs ahead of its consumers, so the divisions are off their path)
+    Unit un{};
+    if (u >= 0) un = decode_unit<kMode>(p, u);
     {
       const int slot = uslot % kUnitSlots;
       const uint32_t n = uslot / kUnitSlots;
       if (n > 0 && !wait_bar(ss, kBarUnitEmpty + slot, (n - 1) & 1, p, 3)) return;
+      ss.unit_dec[slot] = un;
       ss.unit_ring[slot] = u;
       mbar_arrive(bar_addr(ss, kBarUnitFull + slot));
       ++uslot;
@@ -341,7 +367,6 @@ __device__ __forceinline__ void producer_loop(const CUtensorMap* tm_q, const CUt
     if (u < 0) return;
     // next unit index, fetched while this unit's copies are issued
     const int next_u = (int)gridDim.x + atomicAdd(p.sched, 1);
-    const Unit un = decode_unit<kMode>(p, u);
     if (is_split_mode(kMode) && un.nkv <= 0 && un.nkvb <= 0) {  // empty KV ranges: nothing to copy
       u = next_u;
       continue;
@@ -414,15 +439,17 @@ __device__ __forceinline__ void producer_loop(const CUtensorMap* tm_q, const CUt
 }
 
 // Unit index published by the producer for the consumer's next unit
-// (-1: no more work).  `lane0_arrives`: the arrive on the slot's empty
-// barrier comes from lane 0 of a warp after every lane has read it.
+// (-1: no more work), and with `un` the unit decoded.  `whole_warp`: the
+// arrive on the slot's empty barrier comes from lane 0 of a warp after every
+// lane has read it.
 __device__ __forceinline__ bool next_unit(SharedState& ss, const FwdParams& p, uint32_t& uslot,
-                                          bool whole_warp, int& u) {
+                                          bool whole_warp, int& u, Unit* un = nullptr) {
   const int slot = uslot % kUnitSlots;
   bool ok = wait_bar(ss, kBarUnitFull + slot, (uslot / kUnitSlots) & 1, p, 30);
   if (whole_warp) ok = __all_sync(0xffffffffu, ok);
   if (!ok) return false;
   u = ss.unit_ring[slot];
+  if (un) *un = ss.unit_dec[slot];
   if (whole_warp) {
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(bar_addr(ss, kBarUnitEmpty + slot));

@@ -91,8 +91,8 @@ __device__ __forceinline__ void mma_s_loop(const FwdParams& p, SharedState& ss, 
   uint32_t uslot = 0, base = 0;
   for (int ux = 0;; ++ux) {
     int u;
-    if (!next_unit(ss, p, uslot, false, u) || u < 0) return;
-    const Unit un = decode_unit<kMode>(p, u);
+    Unit un;
+    if (!next_unit(ss, p, uslot, false, u, &un) || u < 0) return;
     // group 0 may skip the unit's last tile (lower_tiles); group 1 visits all
     const int n[2] = {lower_tiles<kMode>(p, un), un.nkv};
     const int qb = ux % R::kQBufs;
@@ -130,8 +130,8 @@ __device__ __forceinline__ void mma_pv_loop(const FwdParams& p, SharedState& ss,
   uint32_t uslot = 0, base = 0;
   for (;;) {
     int u;
-    if (!next_unit(ss, p, uslot, false, u) || u < 0) return;
-    const Unit un = decode_unit<kMode>(p, u);
+    Unit un;
+    if (!next_unit(ss, p, uslot, false, u, &un) || u < 0) return;
     const int n[2] = {lower_tiles<kMode>(p, un), un.nkv};
     for (int j = 0; j < un.nkv; ++j) {
       const uint32_t posV = base + 2 * j + 1;
@@ -156,7 +156,8 @@ __device__ __forceinline__ void mma_pv_loop(const FwdParams& p, SharedState& ss,
 // The softmax of query tile g of every unit, one thread per row.
 template <int D, int kMode>
 __device__ __forceinline__ void softmax_rows(const FwdParams& p, SharedState& ss, uint32_t tmem,
-                                             int g, int n_units, uint8_t* sStage) {
+                                             int g, int n_units, uint8_t* sStage,
+                                             const CUtensorMap* tm_o) {
   using C = FwdCfg<D>;
   using R = RowCfg<D>;
   static_assert(kMode == kModePlain || kMode == kModeWindow, "plain and window masks");
@@ -180,9 +181,10 @@ __device__ __forceinline__ void softmax_rows(const FwdParams& p, SharedState& ss
 
   uint32_t uslot = 0;
   int u = -1;
-  if (!next_unit(ss, p, uslot, true, u)) return;
+  Unit un_cur{};
+  if (!next_unit(ss, p, uslot, true, u, &un_cur)) return;
   while (u >= 0) {
-    const Unit un = decode_unit<kMode>(p, u);
+    const Unit un = un_cur;
     const int a0 = q_tile_start(un, g);
     const int row = a0 + trow;                       // sequence-relative row of this thread
     const int nominal0 = un.qb * kUnitRows + g * kBM;
@@ -334,7 +336,7 @@ __device__ __forceinline__ void softmax_rows(const FwdParams& p, SharedState& ss
     // first (the producer published it long ago).
     const int cur_seq = un.seq, cur_h = un.h, cur_tok0 = un.tok0, cur_L = un.L;
     int u_next = -1;
-    if (!next_unit(ss, p, uslot, true, u_next)) return;
+    if (!next_unit(ss, p, uslot, true, u_next, &un_cur)) return;
     if (!__all_sync(0xffffffffu, wait_bar(ss, kBarOFull + g, units_done & 1, p, 62 + g))) return;
     tc_fence_after();
     const float l_r = l + l_fix;
@@ -343,10 +345,15 @@ __device__ __forceinline__ void softmax_rows(const FwdParams& p, SharedState& ss
     if constexpr (RowCfg<D>::kStageO) {
       // This warp's 32 rows through its staging tile: the thread writes its
       // row (16-byte chunk c of row r at r * 128 + 16 (c ^ (r % 8)), no bank
-      // conflicts), then lane l stores chunk l % 8 of rows 4 i + l / 8: four
-      // whole rows per store instruction.
+      // conflicts; the 128-byte swizzle of the tensor map), then one TMA store
+      // of the 32 rows; where the tile starts before its nominal rows (pulled
+      // back at the sequence end) or before the buffer, lane l stores chunk
+      // l % 8 of rows 4 i + l / 8 instead, four whole rows per instruction.
       static_assert(D == 64, "one 128-byte row per thread");
       uint8_t* stage = sStage + g * FwdCfg<D>::kTileBytes + quadrant * 32 * 128;
+      // the previous TMA store from this tile has read it
+      if (lane == 0) bulk_wait_read_all();
+      __syncwarp();
 #pragma unroll
       for (int cc = 0; cc < D; cc += 32) {
         uint32_t r[32];
@@ -363,17 +370,26 @@ __device__ __forceinline__ void softmax_rows(const FwdParams& p, SharedState& ss
           *reinterpret_cast<uint4*>(stage + lane * 128 + ((c ^ (lane & 7)) << 4)) = w;
         }
       }
-      __syncwarp();
-      const int c = lane & 7;
+      if (a0 == nominal0 && a0 >= 0) {
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(tm_o, smem_u32(stage), 0, cur_h, cur_tok0 + a0 + quadrant * 32);
+          bulk_commit();
+        }
+      } else {
+        __syncwarp();
+        const int c = lane & 7;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int rr = 4 * i + (lane >> 3);
-        const uint4 w = *reinterpret_cast<const uint4*>(stage + rr * 128 + ((c ^ (rr & 7)) << 4));
-        const int row_r = a0 + quadrant * 32 + rr;
-        if (row_r >= nominal0 && row_r < cur_L && row_r >= 0)
-          *reinterpret_cast<uint4*>(p.o + ((size_t)(cur_tok0 + row_r) * p.H + cur_h) * D + 8 * c) = w;
+        for (int i = 0; i < 8; ++i) {
+          const int rr = 4 * i + (lane >> 3);
+          const uint4 w = *reinterpret_cast<const uint4*>(stage + rr * 128 + ((c ^ (rr & 7)) << 4));
+          const int row_r = a0 + quadrant * 32 + rr;
+          if (row_r >= nominal0 && row_r < cur_L && row_r >= 0)
+            *reinterpret_cast<uint4*>(p.o + ((size_t)(cur_tok0 + row_r) * p.H + cur_h) * D + 8 * c) = w;
+        }
+        __syncwarp();   // every lane has read the tile before the next unit writes it
       }
-      __syncwarp();   // every lane has read the tile before the next unit writes it
     } else {
       __nv_bfloat16* orow = p.o + ((size_t)(store ? cur_tok0 + row : 0) * p.H + cur_h) * D;
 #pragma unroll
@@ -408,12 +424,15 @@ __device__ __forceinline__ void softmax_rows(const FwdParams& p, SharedState& ss
     ++units_done;
     u = u_next;
   }
+  // the TMA stores of O have completed before the kernel's shared memory goes
+  if (RowCfg<D>::kStageO && (threadIdx.x & 31) == 0) bulk_wait_all();
 }
 
 template <int D, int kMode>
 __global__ void __launch_bounds__(kRowThreads, 1)
 attn_fwd_row_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                    const FwdParams p) {
   using C = FwdCfg<D>;
   using R = RowCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -491,7 +510,7 @@ attn_fwd_row_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     __syncwarp();
   } else {
     setmaxnreg_inc<kRowSoftmaxRegs>();
-    softmax_rows<D, kMode>(p, ss, tmem, warp / kRowGroupWarps, n_units, sStage);
+    softmax_rows<D, kMode>(p, ss, tmem, warp / kRowGroupWarps, n_units, sStage, &tm_o);
     __syncwarp();
   }
 
