@@ -288,8 +288,6 @@ def run_cuda(args, world, rank, local):
         raise RuntimeError("device error during warm-up")
 
     # device-timed region: inputs resident in HBM
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
@@ -297,9 +295,7 @@ def run_cuda(args, world, rank, local):
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
         for i in range(args.steps):
-            ev[i][0].record(stream)
             step()
-            ev[i][1].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize(dev)
     barrier(world)
@@ -307,7 +303,9 @@ def run_cuda(args, world, rank, local):
     if status != 0:
         raise RuntimeError(f"device error status {status}")
     total_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
-    kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    # the calls run back to back (no event between them, as an application
+    # issues them); one call per step, so its mean duration is total / steps
+    kernel_ms = total_ms / args.steps
 
     # end to end through the C ABI with host buffers, every step: H2D of Q,
     # K, V from pinned memory, the forward, D2H of O and LSE, by
@@ -412,24 +410,22 @@ def run_decode(args, world, rank, local):
     torch.cuda.synchronize(dev)
     if fa.attn_last_device_error(stream) != 0:
         raise RuntimeError("device error during warm-up")
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0.record(stream)
         for i in range(args.steps):
-            ev[i][0].record(stream)
             step()
-            ev[i][1].record(stream)
         t1.record(stream)
         torch.cuda.synchronize(dev)
     barrier(world)
     if fa.attn_last_device_error(stream) != 0:
         raise RuntimeError("device error in the timed region")
     total_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
-    call_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    # the calls run back to back (no event between them, as an application
+    # issues them); one call per step, so its mean duration is total / steps
+    call_ms = total_ms / args.steps
 
     def e2e_step():  # a new query batch from the host, the result back
         q.copy_(q_h, non_blocking=True)
@@ -543,24 +539,22 @@ def run_bwd(args, world, rank, local):
     torch.cuda.synchronize(dev)
     if fa.attn_last_device_error(stream) != 0:
         raise RuntimeError("device error during warm-up")
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0.record(stream)
         for i in range(args.steps):
-            ev[i][0].record(stream)
             step()
-            ev[i][1].record(stream)
         t1.record(stream)
         torch.cuda.synchronize(dev)
     barrier(world)
     if fa.attn_last_device_error(stream) != 0:
         raise RuntimeError("device error in the timed region")
     total_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
-    call_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    # the calls run back to back (no event between them, as an application
+    # issues them); one call per step, so its mean duration is total / steps
+    call_ms = total_ms / args.steps
 
     def e2e_step():  # Q, K, V, O, dO and LSE from the host, the three gradients back
         for dst, src in zip((q, k, v, do), host):
@@ -667,26 +661,24 @@ def run_fp8(args, world, rank, local):
     torch.cuda.synchronize(dev)
     if fa.attn_last_device_error(stream) != 0:
         raise RuntimeError("device error during warm-up")
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0.record(stream)
         for i in range(args.steps):
-            ev[i][0].record(stream)
             step()
-            ev[i][1].record(stream)
         t1.record(stream)
         torch.cuda.synchronize(dev)
     barrier(world)
     if fa.attn_last_device_error(stream) != 0:
         raise RuntimeError("device error in the timed region")
     total_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
-    call_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    # the calls run back to back (no event between them, as an application
+    # issues them); one call per step, so its mean duration is total / steps
+    call_ms = total_ms / args.steps
 
-    # the dominant kernel alone (attn_fp8_kernel, about three quarters of a
+    # the dominant kernel alone (attn_fp8_row_kernel, about three quarters of a
     # call): the same attention launch through attn_fwd_fp8_codes, on codes
     # and scales made once by the quantiser entry points
     T = -(-N // 128)
@@ -707,16 +699,15 @@ def run_fp8(args, world, rank, local):
     for _ in range(3):
         attention()
     torch.cuda.synchronize(dev)
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
+    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    k0.record(stream)
     for i in range(args.steps):
-        kev[i][0].record(stream)
         attention()
-        kev[i][1].record(stream)
+    k1.record(stream)
     torch.cuda.synchronize(dev)
     if fa.attn_last_device_error(stream) != 0:
         raise RuntimeError("device error in the attention-kernel timing")
-    kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
+    kernel_ms = k0.elapsed_time(k1) / args.steps
 
     def e2e_step():
         for dst, src in zip((q, k, v), host):
@@ -752,7 +743,7 @@ def run_fp8(args, world, rank, local):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                      "frac": achieved / peak,
                      "peak_source": f"{src} bf16_tflops (burst) x 2, the nominal FP8:BF16 dense ratio",
-                     "kernel": "attn_fp8_kernel<128> (through attn_fwd_fp8_codes)",
+                     "kernel": "attn_fp8_row_kernel<128> (through attn_fwd_fp8_codes)",
                      "call_tflops": flops_step / (call_ms * 1e-3) / 1e12,
                      "call_frac": flops_step / (call_ms * 1e-3) / 1e12 / peak,
                      "traffic": FP8_TRAFFIC_BYTES},
@@ -797,10 +788,10 @@ def fp8_cpu_baseline(wl, signs, budget_s: float = 10.0):
                       f"dequantised rows, {dt:.1f} s (single-threaded)"}
 
 
-# DRAM bytes (read + write) of one attn_fp8_kernel<128> launch of this
+# DRAM bytes (read + write) of one attn_fp8_row_kernel<128> launch of this
 # workload, from one ncu capture of the current kernel (None once it
-# changes): the mean of two launches, 159.13 + 29.85 and 158.66 + 27.38 MB.
-FP8_TRAFFIC_BYTES = (159_129_600 + 29_851_648 + 158_655_232 + 27_379_968) // 2
+# changes).
+FP8_TRAFFIC_BYTES = None
 
 # DRAM bytes (read + write) of one backward call on this workload (all three
 # kernels), from one ncu capture of the current kernels (None once one of them
@@ -811,7 +802,7 @@ BWD_TRAFFIC_BYTES = 135_278_592 + 3_907_072 + 928_369_664 + 101_978_368 + 954_79
 
 # DRAM bytes (read + write) of one attn_fwd_row_kernel<128> launch of this
 # workload, from one ncu capture of the current kernel (None once it changes).
-TRAFFIC_BYTES = 586_072_320  # 540.07 MB read + 46.00 MB written
+TRAFFIC_BYTES = None  # until the capture of the current kernel
 
 
 def main():

@@ -32,12 +32,13 @@
 //                         [d][keys padded to 128] (keys contiguous), so both
 //                         products of the attention kernel take K-major
 //                         operands
-//   attn_fp8_kernel       the forward pass: the bf16 kernel's schedule and warp
-//                         roles (persistent CTAs, longest-first units of two
-//                         128-row query tiles, producer / MMA / 16 softmax
-//                         warps, P in TMEM over its S), tcgen05.mma of
-//                         kind::f8f6f4, K tiles not pulled back (keys past the
-//                         sequence are masked).
+//   attn_fp8_row_kernel   the forward pass (attn_fp8_row_kernel.cuh): the
+//                         bf16 kernel's schedule and warp roles (persistent
+//                         CTAs, longest-first units of two 128-row query
+//                         tiles, producer / MMA / one softmax thread per query
+//                         row, P in TMEM over its S), with this file's producer
+//                         and MMA issuer: tcgen05.mma of kind::f8f6f4, K tiles
+//                         not pulled back (keys past the sequence are masked).
 // Packed batches (cu_seqlens, every length <= N) keep the dense layouts of the
 // scales and of the transposed V codes, indexed by sequence with N the length
 // bound: blocks and key tiles past a sequence's end are neither written nor
@@ -631,249 +632,6 @@ __device__ __forceinline__ void fp8_mma_loop(const Fp8Params& p, SharedState& ss
       }
     }
     ++units_done;
-  }
-}
-
-template <int D>
-__device__ __forceinline__ void fp8_softmax_loop(const Fp8Params& p, SharedState& ss, RowExchange& xs,
-                                                 uint32_t tmem, int g) {
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int quadrant = warp % 4;
-  const int half = (warp % kGroupWarps) / 4;         // which 64 key columns
-  const int trow = quadrant * 32 + lane;              // row of the tile = TMEM lane
-  const uint32_t lane_addr = tmem + ((uint32_t)(quadrant * 32) << 16);
-  const uint32_t colS = 128u * g + half * kHalfCols;
-  const uint32_t colP = 128u * g + half * 16u;        // 64 e4m3 = 16 columns
-  constexpr int kOCols = D / 2;                       // O columns of this thread
-  const uint32_t colO = fp8_col_o<D>(g) + half * kOCols;
-  uint32_t scount = 0, uslot = 0;
-  int units_done = 0;
-  int u = -1;
-  bool fail = !fp8_next_unit(ss, p, uslot, true, u);
-  if (pair_sync_check(g, quadrant, fail)) return;
-  for (;;) {
-    if (u < 0) return;
-    const Fp8Unit un = fp8_unit(p, u);
-    const int bh = un.b * p.H + un.h;
-    const int a0 = fp8_q_start(un, g);
-    const int row = a0 + trow;
-    const int nominal0 = un.qb * kUnitRows + g * kBM;
-    // the quantisation block of this query tile (the pulled-back last block
-    // when the tile is pulled back; rows it shares with the block before it
-    // are recomputed with the wrong scale here but never stored)
-    const int t_last = (un.L + kBM - 1) / kBM - 1;
-    const float qfac = p.logit_log2 * p.sq[(size_t)bh * p.T + min(nominal0 / kBM, t_last)];
-    const int khi = p.causal ? min(row, un.L - 1) : un.L - 1;  // this row's last visible key
-    float m_used = -INFINITY;  // running max of the log2-scaled logits (moved by > 0.75 only)
-    float l = 0.f;             // sum of the fp32 probabilities (this half)
-    for (int j = 0; j < un.nkv; ++j) {
-      fail |= !__all_sync(0xffffffffu, fp8_wait(ss, kBarSFull + g, scount & 1, p, 220 + g));
-      ++scount;
-      tc_fence_after();
-      float s[kHalfCols];
-      {
-        uint32_t r0[32], r1[32];
-        tmem_ld_x32(lane_addr + colS, r0);
-        tmem_ld_x32(lane_addr + colS + 32, r1);
-        tmem_ld_wait_x32(r0);
-        tmem_ld_wait_x32(r1);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          s[i] = __uint_as_float(r0[i]);
-          s[32 + i] = __uint_as_float(r1[i]);
-        }
-      }
-      // keys past the sequence (the tile is not pulled back) and, when
-      // causal, after the row
-      const int hi = khi - (j * kBN + half * kHalfCols);  // last visible column of this thread
-      if (__any_sync(0xffffffffu, hi < kHalfCols - 1)) {
-#pragma unroll
-        for (int c = 0; c < kHalfCols; ++c)
-          if (c > hi) s[c] = -INFINITY;
-      }
-      float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]);
-      float mx2 = fmaxf(s[4], s[5]), mx3 = fmaxf(s[6], s[7]);
-#pragma unroll
-      for (int c = 8; c < kHalfCols; c += 8) {
-        mx0 = max3(mx0, s[c], s[c + 1]);
-        mx1 = max3(mx1, s[c + 2], s[c + 3]);
-        mx2 = max3(mx2, s[c + 4], s[c + 5]);
-        mx3 = max3(mx3, s[c + 6], s[c + 7]);
-      }
-      const float mine = fmaxf(max3(mx0, mx1, mx2), mx3);
-      xs.row_max[j & 1][g][half][trow] = mine;
-      pair_sync(g, quadrant);  // (also orders both halves' S loads before any P store)
-      // log2 units per raw S unit, at least the smallest normal float so that a
-      // masked (-inf) logit stays -inf (a zero scale, or tiny block scales,
-      // would give -inf * 0 = NaN)
-      const float c2t = fmaxf(qfac * p.sk[(size_t)bh * p.T + j], FLT_MIN);
-      const float raw = fmaxf(mine, xs.row_max[j & 1][g][half ^ 1][trow]);
-      const float m_new = fmaxf(m_used, raw == -INFINITY ? -INFINITY : raw * c2t);
-      float alpha = 1.0f;
-      bool resc = false;
-      if (m_used == -INFINITY) {
-        m_used = m_new;
-      } else if (m_new - m_used > kFp8RescaleLog2) {
-        resc = true;
-        alpha = ex2_approx(m_used - m_new);
-        m_used = m_new;
-      }
-      const bool rescale_warp = __any_sync(0xffffffffu, resc);
-      // 2^8 P = 2^(x - m + 8): the e4m3 scale of P is folded into the exponent
-      const float neg = (m_used == -INFINITY ? 0.f : -m_used) + kFp8PLog2;
-      float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
-      uint32_t pw[16];
-#pragma unroll
-      for (int c = 0; c < kHalfCols; c += 4) {
-        float x0, x1, x2, x3;
-        fma2(x0, x1, s[c], s[c + 1], c2t, neg);
-        fma2(x2, x3, s[c + 2], s[c + 3], c2t, neg);
-        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-        const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
-        add2(sa0, sa1, p0, p1);
-        add2(sb0, sb1, p2, p3);
-        pw[c / 4] = e4m3x4(p0, p1, p2, p3);
-      }
-      l = l * alpha + ((sa0 + sa1) + (sb0 + sb1));
-      if (rescale_warp) {
-#pragma unroll
-        for (int cc = 0; cc < kOCols; cc += 32) {
-          uint32_t r[32];
-          tmem_ld_x32(lane_addr + colO + cc, r);
-          tmem_ld_wait_x32(r);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-          tmem_st_x32(lane_addr + colO + cc, r);
-        }
-      }
-      tmem_st_x16(lane_addr + colP, pw);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar_addr(ss, kBarPFull + g));
-    }
-    // epilogue (l sums 2^8 P): O = O_acc * s_v / l -> bf16; LSE = ln 2 (m + log2 l - 8)
-    xs.row_sum[g][half][0][trow] = l;
-    pair_sync(g, quadrant);
-    l += xs.row_sum[g][half ^ 1][0][trow];
-    u = -1;
-    if (!fail) fail = !fp8_next_unit(ss, p, uslot, true, u);
-    if (pair_sync_check(g, quadrant, fail)) return;
-    fail |= !__all_sync(0xffffffffu, fp8_wait(ss, kBarOFull + g, units_done & 1, p, 222 + g));
-    tc_fence_after();
-    const bool store = row >= nominal0 && row < un.L && row >= 0;
-    const float ofac = l > 0.f ? p.sv[bh] / l : 0.f;
-    __nv_bfloat16* orow =
-        p.o + ((size_t)(store ? un.tok0 + row : 0) * p.H + un.h) * D + half * kOCols;
-#pragma unroll
-    for (int cc = 0; cc < kOCols; cc += 32) {
-      uint32_t r[32];
-      tmem_ld_x32(lane_addr + colO + cc, r);
-      tmem_ld_wait_x32(r);
-      if (store) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + cc);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(r[8 * i + 0]) * ofac, __uint_as_float(r[8 * i + 1]) * ofac);
-          w.y = pack_bf16x2(__uint_as_float(r[8 * i + 2]) * ofac, __uint_as_float(r[8 * i + 3]) * ofac);
-          w.z = pack_bf16x2(__uint_as_float(r[8 * i + 4]) * ofac, __uint_as_float(r[8 * i + 5]) * ofac);
-          w.w = pack_bf16x2(__uint_as_float(r[8 * i + 6]) * ofac, __uint_as_float(r[8 * i + 7]) * ofac);
-          dst[i] = w;
-        }
-      }
-    }
-    if (store && half == 0)
-      p.lse[p.cu_seqlens ? (size_t)un.h * p.cu_seqlens[p.B] + un.tok0 + row : (size_t)bh * p.N + row] =
-          l > 0.f ? (m_used + (__log2f(l) - kFp8PLog2)) * 0.69314718055994531f : -INFINITY;
-    tc_fence_before();
-    ++units_done;
-  }
-}
-
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
-attn_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_vt, const Fp8Params p) {
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ SharedState ss;
-  __shared__ RowExchange xs;
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  uint8_t* sQ = smem;
-  uint8_t* sRing = smem + kQTiles * kFp8TileBytes;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int n_units = fp8_num_units(p);
-
-  if (threadIdx.x == 0) {
-    mbar_init(bar_addr(ss, kBarQFull), 1);
-    mbar_init(bar_addr(ss, kBarQEmpty), 1);
-    for (int g = 0; g < kQTiles; ++g) {
-      mbar_init(bar_addr(ss, kBarSFull + g), 1);
-      mbar_init(bar_addr(ss, kBarPFull + g), kGroupThreads);
-      mbar_init(bar_addr(ss, kBarOFull + g), 1);
-    }
-    mbar_init(bar_addr(ss, kBarDrain), 1);
-    for (int i = 0; i < kUnitSlots; ++i) {
-      mbar_init(bar_addr(ss, kBarUnitFull + i), 1);
-      mbar_init(bar_addr(ss, kBarUnitEmpty + i), kUnitConsumers);
-    }
-    for (int s = 0; s < kFp8Stages; ++s) {
-      mbar_init(bar_addr(ss, kBarKV + s), 1);
-      mbar_init(bar_addr(ss, kBarKV + kFp8Stages + s), 1);
-    }
-    ss.abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (warp == kProducerWarp && lane == 0) {
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_vt);
-  }
-  if (warp == kMmaWarp) {
-    tmem_alloc(smem_u32(&ss.tmem_base), 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = ss.tmem_base;
-
-  if (warp >= kSoftmaxWarps) {
-    setmaxnreg_dec<kControlRegs>();
-    if (warp == kProducerWarp) {
-      if (lane == 0) fp8_producer<D>(&tm_q, &tm_k, &tm_vt, p, ss, sQ, sRing, n_units);
-    } else if (warp == kMmaWarp) {
-      if (lane == 0) {
-        fp8_mma_loop<D>(p, ss, sQ, sRing, tmem);
-        mma_commit(bar_addr(ss, kBarDrain));
-        mbar_wait(bar_addr(ss, kBarDrain), 0, 100000000ull);
-      }
-    }
-    __syncwarp();
-  } else {
-    setmaxnreg_inc<kSoftmaxRegs>();
-    fp8_softmax_loop<D>(p, ss, xs, tmem, warp / kGroupWarps);
-    __syncwarp();
-  }
-
-  if (ss.abort_flag) {
-    const uint64_t t0 = globaltimer_ns();
-    while (globaltimer_ns() - t0 < 1000000ull) {
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == kMmaWarp) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
-  if (threadIdx.x == 0) {
-    __threadfence();
-    if (atomicAdd(p.sched + 1, 1) == (int)gridDim.x - 1) {
-      atomicExch(p.sched, 0);
-      atomicExch(p.sched + 1, 0);
-      __threadfence();
-    }
   }
 }
 

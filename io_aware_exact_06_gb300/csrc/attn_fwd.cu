@@ -21,6 +21,7 @@
 #include "attn_fwd_kernel.cuh"
 #include "attn_fwd_pair_kernel.cuh"
 #include "attn_fwd_row_kernel.cuh"
+#include "attn_fp8_row_kernel.cuh"
 #include "attn_host.h"
 
 namespace {
@@ -111,11 +112,11 @@ cudaError_t set_smem_attributes() {
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 FwdCfg<128>::kSmemBytes)) != cudaSuccess)
     return e;
-  if ((e = cudaFuncSetAttribute(attn::attn_fp8_kernel<64>,
+  if ((e = cudaFuncSetAttribute(attn::attn_fp8_row_kernel<64>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 attn::kFp8SmemBytes)) != cudaSuccess)
     return e;
-  if ((e = cudaFuncSetAttribute(attn::attn_fp8_kernel<128>,
+  if ((e = cudaFuncSetAttribute(attn::attn_fp8_row_kernel<128>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 attn::kFp8SmemBytes)) != cudaSuccess)
     return e;
@@ -1369,9 +1370,9 @@ int launch_fp8_attention(EncodeTiledFn enc, DeviceState* ds, int* list, const ui
   const int64_t units = bh * ((N + attn::kUnitRows - 1) / attn::kUnitRows);
   const int grid = cu_seqlens ? ds->sms : (int)std::min<int64_t>(units, ds->sms);
   if (d == 64)
-    attn::attn_fp8_kernel<64><<<grid, attn::kThreads, attn::kFp8SmemBytes, s>>>(mq, mk, mvt, p);
+    attn::attn_fp8_row_kernel<64><<<grid, attn::kRowThreads, attn::kFp8SmemBytes, s>>>(mq, mk, mvt, p);
   else
-    attn::attn_fp8_kernel<128><<<grid, attn::kThreads, attn::kFp8SmemBytes, s>>>(mq, mk, mvt, p);
+    attn::attn_fp8_row_kernel<128><<<grid, attn::kRowThreads, attn::kFp8SmemBytes, s>>>(mq, mk, mvt, p);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
