@@ -2,9 +2,11 @@
 // per query row (plain and sliding-window masks, d = 64 or 128, dense or
 // packed batches).
 //
-// The work units, the TMA producer, the MMA issuer, the TMEM layout and the
-// ping-pong of two query tiles are those of attn_fwd_kernel (see there); the
-// softmax differs.  Each query tile has four softmax warps, one per TMEM
+// The work units and the TMA producer are those of attn_fwd_kernel (see
+// there), and so, at d = 128, are the MMA issuer, the TMEM layout and the
+// ping-pong of two query tiles; at d = 64 P has TMEM columns of its own and
+// two threads issue the products (RowCfg, mma_s_loop, mma_pv_loop).  The
+// softmax differs throughout.  Each query tile has four softmax warps, one per TMEM
 // row quadrant, and each thread owns one row and all 128 key columns of the
 // tile: the row maximum, the exponentials, the row sums and the O epilogue
 // of a row stay in one thread, with no exchange between warps (the layout of
