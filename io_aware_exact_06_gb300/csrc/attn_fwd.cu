@@ -279,6 +279,26 @@ bool one_thread_per_row(int d, int kernel) {
 }
 
 // rows: one softmax thread per query row (attn_fwd_row_kernel) instead of two
+// Launch with programmatic stream serialisation: the kernel may start on the
+// SMs the previous kernel of the stream has left (its set-up overlapping that
+// kernel's last CTAs); it waits for that kernel's completion (griddepcontrol)
+// before its first global access, so the order of the stream holds.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), int grid, int threads, size_t smem,
+                             cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // mo: O through 32-row boxes, for the d = 64 one-thread-per-row kernel's TMA
 // stores (unused by the other kernels).
 template <int D>
@@ -286,11 +306,15 @@ int launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap&
                 const CUtensorMap& mo, const FwdParams& p, int grid, cudaStream_t s,
                 bool rows = false) {
   const bool window = p.wl >= 0 || p.wr >= 0;
-  if (rows && window)
-    attn::attn_fwd_row_kernel<D, attn::kModeWindow><<<grid, attn::kRowThreads, attn::RowCfg<D>::kSmemBytes, s>>>(mq, mk, mv, mo, p);
-  else if (rows)
-    attn::attn_fwd_row_kernel<D, attn::kModePlain><<<grid, attn::kRowThreads, attn::RowCfg<D>::kSmemBytes, s>>>(mq, mk, mv, mo, p);
-  else if (window)
+  if (rows) {
+    cudaError_t e = window ? launch_dependent(attn::attn_fwd_row_kernel<D, attn::kModeWindow>, grid,
+                                              attn::kRowThreads, attn::RowCfg<D>::kSmemBytes, s, mq, mk, mv, mo, p)
+                           : launch_dependent(attn::attn_fwd_row_kernel<D, attn::kModePlain>, grid,
+                                              attn::kRowThreads, attn::RowCfg<D>::kSmemBytes, s, mq, mk, mv, mo, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+  }
+  if (window)
     attn::attn_fwd_kernel<D, attn::kModeWindow><<<grid, attn::kThreads, FwdCfg<D>::kSmemBytes, s>>>(mq, mk, mv, p);
   else
     attn::attn_fwd_kernel<D, attn::kModePlain><<<grid, attn::kThreads, FwdCfg<D>::kSmemBytes, s>>>(mq, mk, mv, p);

@@ -446,6 +446,9 @@ attn_fwd_row_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   uint8_t* sStage = sRing + C::kSmemRing;
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
+  // the next call on the stream may start its CTAs (and their set-up) on the
+  // SMs this grid leaves; it reads nothing before this grid has completed
+  if (threadIdx.x == 0) grid_dep_launch();
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < R::kQBufs; ++b) {
@@ -485,6 +488,9 @@ attn_fwd_row_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ss.tmem_base;
+  // every global access below waits for the grids this one depends on (the
+  // previous call on the stream, when launched as its dependent)
+  grid_dep_wait();
   const int n_units = num_units<kMode>(p);
 
   if (warp >= kRowSoftmaxWarps) {
