@@ -101,9 +101,23 @@ int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
       mq, mk, mv, mdo, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return attn_host::lib_cuda_fail(e);
   p.sched = counters + 4;
-  bwd::bwd_tile_kernel<D, false><<<grid, bwd::kThreads, BwdCfg<D>::kQSmemBytes, s>>>(
-      mq, mk, mv, mdo, p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return attn_host::lib_cuda_fail(e);
+  // the dQ kernel as the dK/dV kernel's programmatic dependent (it may start
+  // on the SMs that kernel leaves; see bwd_tile_kernel)
+  {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(bwd::kThreads);
+    cfg.dynamicSmemBytes = BwdCfg<D>::kQSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, bwd::bwd_tile_kernel<D, false>, mq, mk, mv, mdo, p);
+  }
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) return attn_host::lib_cuda_fail(e);
   return ATTN_OK;
 }
 

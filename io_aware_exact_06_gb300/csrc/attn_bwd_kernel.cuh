@@ -1042,6 +1042,11 @@ bwd_tile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   uint8_t* sRes1 = smem + C::kTileBytes;     // V or dO
   uint8_t* sA = smem + 2 * C::kTileBytes;    // the stage ring (dK/dV) or ring A, then B (dQ)
   uint8_t* sB = sA + C::kQASlots * C::kTileBytes;
+  // The dQ kernel reads nothing the dK/dV kernel writes (only the inputs and
+  // the prologue's vectors, complete before the dK/dV kernel starts), so it is
+  // launched as the dK/dV kernel's dependent and may take the SMs that kernel
+  // leaves while its last units run.
+  if (kKv && threadIdx.x == 0) attn::grid_dep_launch();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int n_units = total_tiles(p) * p.H;
 
@@ -1138,6 +1143,9 @@ bwd_tile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       __threadfence();
     }
   }
+  // the dQ kernel ends only after the dK/dV kernel: the call completes with
+  // both, for whatever the stream runs next
+  if (!kKv) attn::grid_dep_wait();
 }
 
 }  // namespace bwd
