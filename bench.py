@@ -346,7 +346,7 @@ def run_cuda(args, world, rank, local):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                      "frac": achieved / peak, "peak_source": f"{src} bf16_tflops (burst)",
                      "kernel": f"attn_fwd_row_kernel<{d}>" + (" + build_worklist_kernel" if wl.varlen else ""),
-                     "traffic": args.traffic if name == WORKLOAD else None},
+                     "traffic": args.traffic if name == WORKLOAD else CONFIG_TRAFFIC_BYTES.get(name)},
         "clocks": clk.summary(),
         "e2e": {"value": world * flops_step * e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "api": e2e_api},
@@ -790,19 +790,22 @@ def fp8_cpu_baseline(wl, signs, budget_s: float = 10.0):
 
 # DRAM bytes (read + write) of one attn_fp8_row_kernel<128> launch of this
 # workload, from one ncu capture of the current kernel (None once it
-# changes): 161.28 MB read + 30.86 MB written.
-FP8_TRAFFIC_BYTES = 161_275_136 + 30_858_496
+# changes): 163.25 MB read + 30.99 MB written.
+FP8_TRAFFIC_BYTES = 163_252_480 + 30_993_152
 
 # DRAM bytes (read + write) of one backward call on this workload (all three
 # kernels), from one ncu capture of the current kernels (None once one of them
-# changes): prep 135.28 + 3.91 MB, dK/dV 928.37 + 101.98 MB, dQ 954.79 +
+# changes): prep 135.28 + 3.56 MB, dK/dV 926.19 + 101.86 MB, dQ 955.66 +
 # 46.44 MB.
-BWD_TRAFFIC_BYTES = 135_278_592 + 3_907_072 + 928_369_664 + 101_978_368 + 954_793_472 + 46_435_584
+BWD_TRAFFIC_BYTES = 135_279_104 + 3_557_376 + 926_191_872 + 101_856_768 + 955_664_640 + 46_438_400
 
 
 # DRAM bytes (read + write) of one attn_fwd_row_kernel<128> launch of this
 # workload, from one ncu capture of the current kernel (None once it changes).
-TRAFFIC_BYTES = 577_595_392  # 531.69 MB read + 45.90 MB written
+TRAFFIC_BYTES = 538_326_528 + 45_424_128  # 538.33 MB read + 45.42 MB written
+# The same for attn_fwd_row_kernel<64> on the GPT-2 shaped workload: 37.82 MB
+# read + 1.5 KB written (O, 12.6 MB, is still in L2 when the kernel ends).
+CONFIG_TRAFFIC_BYTES = {"gpt2_causal": 37_816_576 + 1_536}
 
 
 def main():
