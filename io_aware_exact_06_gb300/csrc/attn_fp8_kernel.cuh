@@ -608,6 +608,9 @@ __device__ __forceinline__ void fp8_mma_loop(const Fp8Params& p, SharedState& ss
         ring += 2;
       }
       if (!wait_full(posV)) return;
+      // the next K tile before the first P: no wait between a group's P V
+      // product and its next S product
+      if (more && !wait_full(nextK)) return;
       for (int g = 0; g < kQTiles; ++g) {
         if (!fp8_wait(ss, kBarPFull + g, pcount[g] & 1, p, 212 + g)) return;
         ++pcount[g];
@@ -615,10 +618,6 @@ __device__ __forceinline__ void fp8_mma_loop(const Fp8Params& p, SharedState& ss
         issue_pv_fp8<D>(tmem + fp8_col_o<D>(g), tmem + 128u * g, slot_smem(posV), j > 1);
         if (g == kQTiles - 1) release(posV);
         if (more) {
-          if (g == 0) {
-            if (!wait_full(nextK)) return;
-            tc_fence_after();
-          }
           issue_qk_fp8(tmem + 128u * g, q_smem[g], slot_smem(nextK));
           mma_commit(bar_addr(ss, kBarSFull + g));
         } else {

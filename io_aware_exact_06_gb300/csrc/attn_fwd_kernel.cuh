@@ -605,7 +605,9 @@ __device__ __forceinline__ void mma_loop(const FwdParams& p, SharedState& ss, ui
         ring += 2;
       }
       if (!wait_full(posV)) return;
-      bool k_ready = false;
+      // the next K tile before the first P: no wait between a group's P V
+      // product and its next S product
+      if (more && !wait_full(nextK)) return;
 #pragma unroll
       for (int g = 0; g < kQTiles; ++g) {
         const int ng = g == 0 ? n0 : un.nkv;
@@ -618,11 +620,6 @@ __device__ __forceinline__ void mma_loop(const FwdParams& p, SharedState& ss, ui
         }
         if (g == kQTiles - 1) release(posV);
         if (more && j < ng) {
-          if (!k_ready) {
-            if (!wait_full(nextK)) return;
-            tc_fence_after();
-            k_ready = true;
-          }
           issue_qk<D>(tmem + C::col_s(g), q_smem[g], slot_smem(nextK));
           mma_commit(bar_addr(ss, kBarSFull + g));
         } else if (j == ng) {
