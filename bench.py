@@ -790,8 +790,8 @@ def fp8_cpu_baseline(wl, signs, budget_s: float = 10.0):
 
 # DRAM bytes (read + write) of one attn_fp8_row_kernel<128> launch of this
 # workload, from one ncu capture of the current kernel (None once it
-# changes): 163.25 MB read + 30.99 MB written.
-FP8_TRAFFIC_BYTES = 163_252_480 + 30_993_152
+# changes): 162.61 MB read + 30.54 MB written.
+FP8_TRAFFIC_BYTES = 162_609_920 + 30_540_288
 
 # DRAM bytes (read + write) of one backward call on this workload (all three
 # kernels), from one ncu capture of the current kernels (None once one of them
@@ -802,10 +802,11 @@ BWD_TRAFFIC_BYTES = 135_279_104 + 3_557_376 + 926_191_872 + 101_856_768 + 955_66
 
 # DRAM bytes (read + write) of one attn_fwd_row_kernel<128> launch of this
 # workload, from one ncu capture of the current kernel (None once it changes).
-TRAFFIC_BYTES = 538_326_528 + 45_424_128  # 538.33 MB read + 45.42 MB written
-# The same for attn_fwd_row_kernel<64> on the GPT-2 shaped workload: 37.82 MB
-# read + 1.5 KB written (O, 12.6 MB, is still in L2 when the kernel ends).
-CONFIG_TRAFFIC_BYTES = {"gpt2_causal": 37_816_576 + 1_536}
+TRAFFIC_BYTES = 537_853_440 + 45_941_248  # 537.85 MB read + 45.94 MB written
+# The same for other forward workloads: attn_fwd_row_kernel<64> on the GPT-2
+# shaped one (37.82 MB read + 1.5 KB written: O, 12.6 MB, is still in L2
+# when the kernel ends) and attn_fwd_row_kernel<128> on the stress one.
+CONFIG_TRAFFIC_BYTES = {"gpt2_causal": 37_816_576 + 1_536, "stress": 248_950_016 + 50_955_008}
 
 
 def main():
