@@ -124,120 +124,76 @@ struct Fp8Signs {
 };
 
 // ----------------------------------------------------------- quantisers --
-constexpr int kQuantWarps = 16;  // warps per quantiser CTA (one 128-row block)
-// x H_D of the D values held 4 per lane (lane l: channels 4l..4l+3),
-// fp32 butterflies over strides 1, 2 (in the lane) and 4..D/2 (across lanes):
-// the lower element a of a pair becomes a + b, the upper b becomes a - b.
-// Across lanes both are one fma of the lane's own value with a per-lane sign
-// (+1 lower, -1 upper) and the partner's value: fma(+1, a, b) = a + b and
-// fma(-1, b, a) = a - b, each rounded once like the additions.
-// (d = 64: the same over lanes 0..15, strides 4..32; lanes 16..31 hold zeros)
-template <int D>
-__device__ __forceinline__ void fwht_warp(float (&v)[4], int lane) {
-  float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
-  v[0] = a0 + a2;
-  v[1] = a1 + a3;
-  v[2] = a0 - a2;
-  v[3] = a1 - a3;
-#pragma unroll
-  for (int m = 1; m < D / 4; m <<= 1) {
-    const float sg = (lane & m) ? -1.0f : 1.0f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) v[j] = fmaf(sg, v[j], __shfl_xor_sync(0xffffffffu, v[j], m));
-  }
-}
-
 __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
   const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
   const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
   return lo | (hi << 16);
 }
 
-// The first quantisation stage runs in persistent CTAs of 16 warps, one
-// 128-row block at a time; a block's rows arrive by TMA in a shared-memory
-// buffer ([128 rows][128 channels] bf16), the next block's rows landing in
-// the other buffer meanwhile.  The last block of a sequence (tokens [tok0,
-// tok0 + L)) is pulled back to end at L, so no copy leaves the sequence, and
-// leaves the rows it shares with the block before it to that block; rows
-// before the sequence count as zero.
+// The first quantisation stage: one thread per row of a 128-row block, the
+// row's D channels in registers.  A block's rows arrive by TMA in a
+// shared-memory buffer (64-channel chunks of [128 rows][128 bytes], 128-byte
+// swizzle: row r's 16-byte unit u at (u ^ (r mod 8)) * 16, so the 32 rows a
+// warp reads at once spread over all banks), the next block's rows landing
+// in the other buffer meanwhile.  The last block of a sequence (tokens
+// [tok0, tok0 + L)) is pulled back to end at L, so no copy leaves the
+// sequence, and leaves the rows it shares with the block before it to that
+// block; rows before the sequence count as zero.
 template <int D>
 struct QuantCfg {
-  static constexpr int kRowBytes = D * 2;  // one bf16 input row
-  static constexpr int kBlockBytes = kBM * kRowBytes;
+  static constexpr int kChunks = D / 64;
+  static constexpr int kBlockBytes = kBM * D * 2;
   static constexpr int kSmemBytes = 2 * kBlockBytes + 1024;
 };
-constexpr int kQuantRows = kBM / kQuantWarps;  // rows per warp: warp + kQuantWarps i
+constexpr int kQuantThreads = kBM;  // one per row of a block
 
-// First half of a Q or K block: rotation of the warp's 8 rows (held in
-// registers) and their max |x| into warp_max[warp].  Rows r0 + i of the
-// block are at i * 2 D bytes of `stage`; lanes >= D/4 hold zeros.
+// x H_D of one row held by one thread, unnormalised, fp32: butterflies over
+// strides 1, 2, 4, ..., D/2, each pair (i, i + s) with bit s of i clear
+// becoming (a + b, a - b), each rounded once.
 template <int D>
-__device__ __forceinline__ void fp8_rotate_rows(const uint8_t* stage, int r0, const uint32_t (&flip)[2],
-                                                int rotate, float (&v)[kQuantRows][4],
-                                                float* warp_max) {
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  float amax = 0.f;
+__device__ __forceinline__ void fwht_row(float (&v)[D]) {
 #pragma unroll
-  for (int i = 0; i < kQuantRows; ++i) {
-    const int r = warp + kQuantWarps * i;
-    const uint2 raw = r0 + r >= 0 && lane < D / 4
-                          ? *reinterpret_cast<const uint2*>(stage + r * QuantCfg<D>::kRowBytes + 8 * lane)
-                          : make_uint2(0u, 0u);
-    const uint32_t w0 = raw.x ^ flip[0], w1 = raw.y ^ flip[1];
-    v[i][0] = __uint_as_float(w0 << 16);
-    v[i][1] = __uint_as_float(w0 & 0xffff0000u);
-    v[i][2] = __uint_as_float(w1 << 16);
-    v[i][3] = __uint_as_float(w1 & 0xffff0000u);
-    if (rotate) fwht_warp<D>(v[i], lane);
-    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[i][0]), fabsf(v[i][1])),
-                             fmaxf(fabsf(v[i][2]), fabsf(v[i][3]))));
-  }
+  for (int s = 1; s < D; s <<= 1) {
 #pragma unroll
-  for (int m = 16; m > 0; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
-  if (lane == 0) warp_max[warp] = amax;
-}
-
-// Second half: the block max from warp_max, the scale, and the codes of the
-// rows that belong to block t, in rows of `stride` bytes (channels >= D of a
-// padded row get code 0).
-template <int D>
-__device__ __forceinline__ void fp8_write_codes(const float (&v)[kQuantRows][4], const float* warp_max,
-                                                uint8_t* codes, float* scale_out, int tok0, int r0,
-                                                int t, int h, int H, int stride) {
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  float amax = warp_max[0];
-#pragma unroll
-  for (int w = 1; w < kQuantWarps; ++w) amax = fmaxf(amax, warp_max[w]);
-  const float inv = amax > 0.f ? __fdiv_rn(kFp8Max, amax) : 1.0f;
-  if (threadIdx.x == 0) *scale_out = amax > 0.f ? __fdiv_rn(amax, kFp8Max) : 1.0f;
-#pragma unroll
-  for (int i = 0; i < kQuantRows; ++i) {
-    const int row = r0 + warp + kQuantWarps * i;
-    if (row < t * kBM || 4 * lane >= stride) continue;  // the previous block's row, or past the row
-    *reinterpret_cast<uint32_t*>(codes + ((size_t)(tok0 + row) * H + h) * stride + 4 * lane) =
-        lane < D / 4 ? e4m3x4(__fmul_rn(v[i][0], inv), __fmul_rn(v[i][1], inv),
-                              __fmul_rn(v[i][2], inv), __fmul_rn(v[i][3], inv))
-                     : 0u;
+    for (int i = 0; i < D; ++i) {
+      if (i & s) continue;
+      const float a = v[i], b = v[i + s];
+      v[i] = a + b;
+      v[i + s] = a - b;
+    }
   }
 }
 
-// max |V| over the rows of block t (rows >= 128 t of the staged rows r0 ..)
-// into warp_max[warp].
+// Row r of the staged block (bf16) as fp32, the sign bits of the channels
+// whose sign is -1 flipped first (exact); flips: one 32-bit mask per pair of
+// channels (bit 15: the even channel, bit 31: the odd one).
 template <int D>
-__device__ __forceinline__ void fp8_rows_amax(const uint8_t* stage, int r0, int t, float* warp_max) {
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  float m = 0.f;
+__device__ __forceinline__ void fp8_load_row(const uint8_t* stage, int r, const uint32_t* flips,
+                                             float (&v)[D]) {
 #pragma unroll
-  for (int i = 0; i < kQuantRows; ++i) {
-    const int r = warp + kQuantWarps * i;
-    if (r0 + r < t * kBM || lane >= D / 4) continue;
-    const uint2 w = *reinterpret_cast<const uint2*>(stage + r * QuantCfg<D>::kRowBytes + 8 * lane);
-    m = fmaxf(m, fmaxf(fmaxf(fabsf(__uint_as_float(w.x << 16)), fabsf(__uint_as_float(w.x & 0xffff0000u))),
-                       fmaxf(fabsf(__uint_as_float(w.y << 16)), fabsf(__uint_as_float(w.y & 0xffff0000u)))));
+  for (int c = 0; c < D / 64; ++c) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint4 w = *reinterpret_cast<const uint4*>(stage + c * kBM * 128 + r * 128 + ((u ^ (r & 7)) << 4));
+      const uint4 f = *reinterpret_cast<const uint4*>(flips + 32 * c + 4 * u);
+      const uint32_t x[4] = {w.x ^ f.x, w.y ^ f.y, w.z ^ f.z, w.w ^ f.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        v[64 * c + 8 * u + 2 * q] = __uint_as_float(x[q] << 16);
+        v[64 * c + 8 * u + 2 * q + 1] = __uint_as_float(x[q] & 0xffff0000u);
+      }
+    }
   }
+}
+
+// max over the 128 threads of m (every thread gets it); red: 4 floats of
+// shared memory, free on entry
+__device__ __forceinline__ float block_max128(float m, float* red) {
 #pragma unroll
   for (int s = 16; s > 0; s >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
-  if (lane == 0) warp_max[warp] = m;
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x / 32] = m;
+  __syncthreads();
+  return fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
 }
 
 // Tokens [tok0, tok0 + L) of sequence b; false when block t lies past its end
@@ -255,15 +211,17 @@ __device__ __forceinline__ bool fp8_seq_block(const int* cu_seqlens, const int* 
   return t * kBM < L;
 }
 
+
 // One launch for the first quantisation stage over blocks block0 + i, i in
 // [0, n_blocks): blocks [0, nb) quantise Q, [nb, 2 nb) quantise K, [2 nb,
 // 3 nb) take the max |V| per (sequence, head) (atomic max of the
 // non-negative fp32 bit patterns); nb = B * H * T, block = (b * H + h) * T + t.
-// tm_q, tm_k, tm_v: [tokens][H][D] bf16, box D channels x 1 head x 128 rows,
-// no swizzle (a map of an absent input is never used).  Codes go to rows of
-// code_stride bytes (D, or 128 for the attention kernel's padded rows).
+// tm_q, tm_k, tm_v: [tokens][H][D] bf16, box 64 channels x 1 head x 128 rows,
+// 128-byte swizzle (a map of an absent input is never used).  Codes go to
+// rows of code_stride bytes (D, or 128 for the attention kernel's padded
+// rows).  Persistent CTAs of 128 threads.
 template <int D>
-__global__ void __launch_bounds__(32 * kQuantWarps, 2)
+__global__ void __launch_bounds__(kQuantThreads, 3)
 fp8_quant_stage1_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, uint8_t* q8, uint8_t* k8,
@@ -275,9 +233,10 @@ fp8_quant_stage1_kernel(const __grid_constant__ CUtensorMap tm_q,
   uint8_t* stage = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   __shared__ uint64_t full[2];
-  __shared__ float warp_max[2][kQuantWarps];
+  __shared__ __align__(16) uint32_t flips[D / 2];
+  __shared__ float red[2][kQuantThreads / 32];
   const int nb = B * H * T;
-  const int lane = threadIdx.x % 32;
+  const int r = threadIdx.x;  // the row of the block this thread takes
   // block i of this launch: segment, index within it, head, sequence tokens, first staged row
   auto locate = [&](int i, int& seg, int& idx, int& h, int& tok0, int& t, int& r0) {
     const int gidx = i + block0;
@@ -298,17 +257,19 @@ fp8_quant_stage1_kernel(const __grid_constant__ CUtensorMap tm_q,
     const CUtensorMap* tm = seg == 0 ? &tm_q : (seg == 1 ? &tm_k : &tm_v);
     const uint32_t bar = smem_u32(&full[buf]);
     mbar_arrive_expect_tx(bar, QC::kBlockBytes);
-    tma_load_3d(smem_u32(stage + buf * QC::kBlockBytes), tm, bar, 0, h, tok0 + r0);
-  };
-  // the signs of this lane's channels 4 lane .. 4 lane + 3 as bf16 sign bits
-  // of the two 32-bit words that hold them (negation is exact)
-  uint32_t flip[2] = {0u, 0u};
-  if (rotate) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int c = 4 * lane + j;
-      if ((signs.bits[c / 32] >> (c % 32)) & 1u) flip[j / 2] |= (j & 1) ? 0x80000000u : 0x8000u;
+    for (int c = 0; c < QC::kChunks; ++c)
+      tma_load_3d(smem_u32(stage + buf * QC::kBlockBytes + c * kBM * 128), tm, bar, 64 * c, h, tok0 + r0);
+  };
+  // sign masks of the channel pairs (negation is exact)
+  if (threadIdx.x < D / 2) {
+    const int c0 = 2 * threadIdx.x;
+    uint32_t f = 0u;
+    if (rotate) {
+      if ((signs.bits[c0 / 32] >> (c0 % 32)) & 1u) f |= 0x8000u;
+      if ((signs.bits[(c0 + 1) / 32] >> ((c0 + 1) % 32)) & 1u) f |= 0x80000000u;
     }
+    flips[threadIdx.x] = f;
   }
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&full[0]), 1);
@@ -318,43 +279,83 @@ fp8_quant_stage1_kernel(const __grid_constant__ CUtensorMap tm_q,
     issue(blockIdx.x + gridDim.x, 1);
   }
   __syncthreads();
-  uint32_t used[2] = {0u, 0u};  // copies consumed per buffer
+  uint32_t used0 = 0u, used1 = 0u;  // copies consumed per buffer
   int k = 0;
   bool failed = false;
   for (int i = blockIdx.x; i < n_blocks; i += gridDim.x, ++k) {
     const int buf = k & 1;
     int seg, idx, h, tok0, t, r0;
     const bool valid = locate(i, seg, idx, h, tok0, t, r0);  // the same in every thread
-    float v[kQuantRows][4];
+    float v[D];
+    float m = 0.f;
     if (valid) {
-      const bool ok = mbar_wait(smem_u32(&full[buf]), used[buf] & 1, 2000000000ull);
-      ++used[buf];
+      const bool ok = mbar_wait(smem_u32(&full[buf]), (buf ? used1 : used0) & 1, 2000000000ull);
+      if (buf)
+        ++used1;
+      else
+        ++used0;
       if (__syncthreads_or(!ok)) {
         failed = true;
         break;
       }
       const uint8_t* st = stage + buf * QC::kBlockBytes;
-      if (seg < 2)
-        fp8_rotate_rows<D>(st, r0, flip, rotate, v, warp_max[k & 1]);
-      else
-        fp8_rows_amax<D>(st, r0, t, warp_max[k & 1]);
+      if (seg < 2) {
+        if (r0 + r >= 0) {
+          fp8_load_row<D>(st, r, flips, v);
+          if (rotate) fwht_row<D>(v);
+        } else {
+#pragma unroll
+          for (int c = 0; c < D; ++c) v[c] = 0.f;
+        }
+#pragma unroll
+        for (int c = 0; c < D; c += 2) m = max3(m, fabsf(v[c]), fabsf(v[c + 1]));
+      } else if (r0 + r >= t * kBM) {  // V: the rows of this block only
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint4 w = *reinterpret_cast<const uint4*>(st + c * kBM * 128 + r * 128 + ((u ^ (r & 7)) << 4));
+            const uint32_t x[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              m = max3(m, fabsf(__uint_as_float(x[q] << 16)), fabsf(__uint_as_float(x[q] & 0xffff0000u)));
+          }
+        }
+      }
     }
-    __syncthreads();  // every read of this buffer is done; warp_max is complete
+    // every read of this buffer is done once all threads have the block max
+    const float amax = block_max128(m, red[k & 1]);
     if (threadIdx.x == 0) {
       // (the generic-proxy reads above before the copy that overwrites them)
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       issue(i + 2 * gridDim.x, buf);
     }
     if (!valid) continue;
-    if (seg == 0) {
-      fp8_write_codes<D>(v, warp_max[k & 1], q8, sq + idx, tok0, r0, t, h, H, code_stride);
-    } else if (seg == 1) {
-      fp8_write_codes<D>(v, warp_max[k & 1], k8, sk + idx, tok0, r0, t, h, H, code_stride);
-    } else if (threadIdx.x == 0) {
-      float m = warp_max[k & 1][0];
+    if (seg < 2) {
+      uint8_t* codes = seg == 0 ? q8 : k8;
+      float* scale_out = (seg == 0 ? sq : sk) + idx;
+      const float inv = amax > 0.f ? __fdiv_rn(kFp8Max, amax) : 1.0f;
+      if (threadIdx.x == 0) *scale_out = amax > 0.f ? __fdiv_rn(amax, kFp8Max) : 1.0f;
+      const int row = r0 + r;
+      if (row >= t * kBM) {  // (rows before it are the previous block's)
+        uint4* dst = reinterpret_cast<uint4*>(codes + ((size_t)(tok0 + row) * H + h) * code_stride);
 #pragma unroll
-      for (int w = 1; w < kQuantWarps; ++w) m = fmaxf(m, warp_max[k & 1][w]);
-      atomicMax(amax_v + idx / T, __float_as_uint(m));
+        for (int q = 0; q < D / 16; ++q) {
+          uint4 w;
+          w.x = e4m3x4(__fmul_rn(v[16 * q + 0], inv), __fmul_rn(v[16 * q + 1], inv),
+                       __fmul_rn(v[16 * q + 2], inv), __fmul_rn(v[16 * q + 3], inv));
+          w.y = e4m3x4(__fmul_rn(v[16 * q + 4], inv), __fmul_rn(v[16 * q + 5], inv),
+                       __fmul_rn(v[16 * q + 6], inv), __fmul_rn(v[16 * q + 7], inv));
+          w.z = e4m3x4(__fmul_rn(v[16 * q + 8], inv), __fmul_rn(v[16 * q + 9], inv),
+                       __fmul_rn(v[16 * q + 10], inv), __fmul_rn(v[16 * q + 11], inv));
+          w.w = e4m3x4(__fmul_rn(v[16 * q + 12], inv), __fmul_rn(v[16 * q + 13], inv),
+                       __fmul_rn(v[16 * q + 14], inv), __fmul_rn(v[16 * q + 15], inv));
+          dst[q] = w;
+        }
+        for (int q = D / 16; q < code_stride / 16; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    } else if (threadIdx.x == 0) {
+      atomicMax(amax_v + idx / T, __float_as_uint(amax));
     }
   }
   if (failed) {

@@ -1235,16 +1235,16 @@ int fp8_worklist(int dev, attn_stream_t stream, DeviceState* ds, const int32_t* 
   return ATTN_OK;
 }
 
-// bf16 rows [tokens, H, d] for the first quantisation stage: box d channels
-// x 1 head x 128 rows, no swizzle (rows 2 d bytes apart in shared memory).
+// bf16 rows [tokens, H, d] for the first quantisation stage: box 64 channels
+// x 1 head x 128 rows, 128-byte swizzle (one copy per 64-channel chunk).
 int make_map_quant_rows(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int64_t tokens, int H,
                         int d) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)tokens};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
-  cuuint32_t box[3] = {(cuuint32_t)d, 1, (cuuint32_t)attn::kBM};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)attn::kBM};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? ATTN_OK : cuda_fail(cudaErrorInvalidValue);
 }
@@ -1276,13 +1276,13 @@ int launch_quant_stage1(const void* q, const void* k, const void* v, uint8_t* q8
   const int nseg = v ? 3 : (k ? 2 : 1);
   const int first = q ? 0 : (k ? 1 : 2);
   const int n_blocks = (nseg - first) * nb;
-  const int grid = std::min(n_blocks, 2 * ds->sms);
+  const int grid = std::min(n_blocks, 3 * ds->sms);
   if (d == 64)
-    attn::fp8_quant_stage1_kernel<64><<<grid, 32 * attn::kQuantWarps, attn::QuantCfg<64>::kSmemBytes, s>>>(
+    attn::fp8_quant_stage1_kernel<64><<<grid, attn::kQuantThreads, attn::QuantCfg<64>::kSmemBytes, s>>>(
         maps[0], maps[1], maps[2], q8, k8, sq, sk, amax_v, B, H, N, T, pack_signs(signs, d),
         signs ? 1 : 0, first * nb, n_blocks, cu_seqlens, num_entries, ds->err, code_stride);
   else
-    attn::fp8_quant_stage1_kernel<128><<<grid, 32 * attn::kQuantWarps, attn::QuantCfg<128>::kSmemBytes, s>>>(
+    attn::fp8_quant_stage1_kernel<128><<<grid, attn::kQuantThreads, attn::QuantCfg<128>::kSmemBytes, s>>>(
         maps[0], maps[1], maps[2], q8, k8, sq, sk, amax_v, B, H, N, T, pack_signs(signs, d),
         signs ? 1 : 0, first * nb, n_blocks, cu_seqlens, num_entries, ds->err, code_stride);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
