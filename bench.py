@@ -805,8 +805,10 @@ BWD_TRAFFIC_BYTES = 135_279_104 + 3_557_376 + 926_191_872 + 101_856_768 + 955_66
 TRAFFIC_BYTES = 537_853_440 + 45_941_248  # 537.85 MB read + 45.94 MB written
 # The same for other forward workloads: attn_fwd_row_kernel<64> on the GPT-2
 # shaped one (37.82 MB read + 1.5 KB written: O, 12.6 MB, is still in L2
-# when the kernel ends) and attn_fwd_row_kernel<128> on the stress one.
-CONFIG_TRAFFIC_BYTES = {"gpt2_causal": 37_816_576 + 1_536, "stress": 248_950_016 + 50_955_008}
+# when the kernel ends) and attn_fwd_row_kernel<128> on the stress and the
+# packed ones.
+CONFIG_TRAFFIC_BYTES = {"gpt2_causal": 37_816_576 + 1_536, "stress": 248_950_016 + 50_955_008,
+                        "varlen": 1_910_574_080 + 463_506_688}
 
 
 def main():

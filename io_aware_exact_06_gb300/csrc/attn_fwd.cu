@@ -269,6 +269,15 @@ int pair_group(int N, int d, bool causal, int64_t units, int sms) {
   return (int)std::max<int64_t>(1, std::min<int64_t>(1 << 20, (int64_t(32) << 20) / kv));
 }
 
+// Heads per group of the packed unit order (0: one group): as many heads as
+// have the keys and values of all sequences (at most B N tokens) in about
+// 32 MB, under the same rule as pair_group.
+int head_group(int B, int N, int d, int H, bool causal, int64_t units, int sms) {
+  if (causal && units < 64 * (int64_t)sms) return 0;
+  const int64_t kv = 2 * (int64_t)B * N * d * 2;
+  return (int)std::max<int64_t>(1, std::min<int64_t>(H, (int64_t(32) << 20) / kv));
+}
+
 // The library's choice of softmax layout for the one-CTA kernels (attn_fwd_options.kernel
 // 0): one thread per query row, which measured faster at both head dims (same-process,
 // TFLOP/s: GPT-2 shaped causal 377 against 347, long causal 1457 against 1327, long
@@ -384,7 +393,8 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* l
   p.scale_log2 = exp2_scale(scale);
   p.timeout_ns = (opts && opts->wait_timeout_ns) ? opts->wait_timeout_ns : 2000000000ull;
   p.fault_inject = opts ? opts->fault_inject : 0;
-  p.pair_group = cu_seqlens ? 0 : pair_group(N, d, p.causal, units, ds->sms);
+  p.pair_group = cu_seqlens ? head_group(B, N, d, H, p.causal, units, ds->sms)
+                            : pair_group(N, d, p.causal, units, ds->sms);
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int grid = ds->sms;
@@ -775,7 +785,8 @@ int attn_fwd_noalloc_impl(const void* q, const void* k, const void* v, void* o, 
   p.scale_log2 = exp2_scale(scale);
   p.timeout_ns = (opts && opts->wait_timeout_ns) ? opts->wait_timeout_ns : 2000000000ull;
   p.fault_inject = opts ? opts->fault_inject : 0;
-  p.pair_group = cu_seqlens ? 0 : pair_group(N, d, p.causal, units, nd->sms);
+  p.pair_group = cu_seqlens ? head_group(B, N, d, H, p.causal, units, nd->sms)
+                            : pair_group(N, d, p.causal, units, nd->sms);
 
   int grid = nd->sms;
   if (cu_seqlens) {

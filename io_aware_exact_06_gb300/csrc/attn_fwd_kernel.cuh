@@ -103,8 +103,8 @@ struct FwdParams {
   float scale_log2;        // scale * log2(e)
   unsigned long long timeout_ns;
   int fault_inject;        // 1: CTA 0 never issues its first K copy (test hook)
-  int pair_group;          // dense, not split: (batch, head) pairs per group of the
-                           // unit order (0: one group of all pairs)
+  int pair_group;          // not split: dense, (batch, head) pairs per group of the
+                           // unit order; packed, heads per group (0: one group)
 };
 
 template <int D>
@@ -210,8 +210,30 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
   un.kv0b = 0;
   un.nkvb = 0;
   if (!is_split_mode(kMode) && p.cu_seqlens) {
-    un.seq = p.work[2 * e];
-    un.qb = p.work[2 * e + 1];
+    if (p.pair_group > 0 && p.pair_group < p.H) {
+      // heads in groups of p.pair_group, one group after the other; within
+      // a group the sorted list, then head
+      const int E = *p.num_entries;
+      const int G = p.pair_group;
+      const int full = p.H / G;
+      int gi, r, ng;
+      if (u < full * G * E) {
+        gi = u / (G * E);
+        r = u - gi * G * E;
+        ng = G;
+      } else {
+        gi = full;
+        r = u - full * G * E;
+        ng = p.H - full * G;
+      }
+      const int ee = r / ng;
+      un.h = gi * G + (r - ee * ng);
+      un.seq = p.work[2 * ee];
+      un.qb = p.work[2 * ee + 1];
+    } else {
+      un.seq = p.work[2 * e];
+      un.qb = p.work[2 * e + 1];
+    }
     un.tok0 = p.cu_seqlens[un.seq];
     un.L = p.cu_seqlens[un.seq + 1] - un.tok0;
   } else {
