@@ -116,6 +116,7 @@ struct Fp8Params {
   float logit_log2;     // scale * log2(e) / d (the transform's 1/d folded in)
   float scale;
   unsigned long long timeout_ns;
+  int head_group;       // packed: heads per group of the unit order (0: one group)
 };
 
 // Sign vector of the transform, one bit per channel (1: negate).
@@ -480,8 +481,27 @@ __device__ __forceinline__ int fp8_num_units(const Fp8Params& p) {
 
 __device__ __forceinline__ Fp8Unit fp8_unit(const Fp8Params& p, int u) {
   Fp8Unit un;
-  const int e = u / p.H;
+  int e = u / p.H;
   un.h = u - e * p.H;
+  if (p.cu_seqlens && p.head_group > 0 && p.head_group < p.H) {
+    // heads in groups of p.head_group, one group after the other; within a
+    // group the sorted list, then head (their codes stay in L2 meanwhile)
+    const int E = *p.num_entries;
+    const int G = p.head_group;
+    const int full = p.H / G;
+    int gi, r, ng;
+    if (u < full * G * E) {
+      gi = u / (G * E);
+      r = u - gi * G * E;
+      ng = G;
+    } else {
+      gi = full;
+      r = u - full * G * E;
+      ng = p.H - full * G;
+    }
+    e = r / ng;
+    un.h = gi * G + (r - e * ng);
+  }
   if (p.cu_seqlens) {
     un.b = p.work[2 * e];
     un.qb = p.work[2 * e + 1];

@@ -1403,6 +1403,9 @@ int launch_fp8_attention(EncodeTiledFn enc, DeviceState* ds, int* list, const ui
   p.logit_log2 = (float)((double)scale * 1.4426950408889634 / (rotated ? (double)d : 1.0));
   p.timeout_ns = 2000000000ull;
   const int64_t units = bh * ((N + attn::kUnitRows - 1) / attn::kUnitRows);
+  // packed: heads in groups whose codes (one byte per channel) fit in about
+  // 32 MB, as for the bf16 path
+  p.head_group = cu_seqlens ? head_group(B, N, d / 2, H, causal != 0, units, ds->sms) : 0;
   const int grid = cu_seqlens ? ds->sms : (int)std::min<int64_t>(units, ds->sms);
   if (d == 64)
     attn::attn_fp8_row_kernel<64><<<grid, attn::kRowThreads, attn::kFp8SmemBytes, s>>>(mq, mk, mvt, p);

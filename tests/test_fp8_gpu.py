@@ -461,3 +461,29 @@ def test_codes_entry_matches_full_call(dev, packed, rotate, causal):
     assert fa.attn_last_device_error() == 0
     assert bool((o1.view(torch.int16) == o2.view(torch.int16)).all())
     assert bool((l1 == l2).all())
+
+
+def test_fp8_packed_head_group_order_same_result(dev):
+    """Packed FP8 calls with at least 64 units per SM (counted from the length
+    bound N) take their units in head groups; the result may not depend on the
+    order.  The same sequences with N = their longest length (one group) and
+    with N = 8192 (16 x 20 x 32 = 10240 units on 152 SMs, one head per group)
+    give bit-identical O and LSE, within the bounds against the dequantised
+    reference on sampled rows."""
+    H, d = 20, 128
+    lens = inputs.uniform_ints(3950, 16, 1, 1500).tolist()
+    cu, q, k, v = packed_inputs(3951, lens, H)
+    sg = signs_of(3952)
+    scale = d ** -0.5
+    o1, l1 = run_fp8_packed(dev, q, k, v, cu, max(lens), H, True, sg, scale)
+    o2, l2 = run_fp8_packed(dev, q, k, v, cu, 8192, H, True, sg, scale)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    rows = inputs.sample_rows(cu, H, 1024, seed=3953)
+    tok = cu[rows[:, 0]] + rows[:, 2]
+    go, gl = o2[tok, rows[:, 1]], l2[rows[:, 1], tok]
+    qd = dequantised_packed(q, cu, 128, True, sg)
+    kd = dequantised_packed(k, cu, 128, True, sg)
+    vd = dequantised_packed(v, cu, 0, False, None)
+    ref_o, ref_l = oracle.attn_rows_f64(qd, kd, vd, cu, rows, scale / d, True)
+    rel_d, lse_d = errors(go, gl, ref_o, ref_l)
+    assert rel_d <= REL_DEQ and lse_d <= LSE_DEQ, (rel_d, lse_d)
