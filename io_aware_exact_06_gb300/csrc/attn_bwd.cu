@@ -208,6 +208,14 @@ int attn_bwd_impl(const void* q, const void* k, const void* v, const void* o, co
   p.scale = scale;
   p.scale_log2 = (float)((double)scale * 1.4426950408889634);
   p.timeout_ns = 2000000000ull;
+  // packed causal calls with at least 64 units per SM (units counted from the
+  // length bound): heads in groups whose streamed operands (two [tokens, d]
+  // bf16 tensors of all sequences, at most B N tokens) fit in about 32 MB of
+  // L2, the forward's rule
+  if (cu_seqlens && (!causal || units >= 64 * (int64_t)sms)) {
+    const int64_t bytes = 2 * (int64_t)B * N * d * 2;
+    p.head_group = (int)std::max<int64_t>(1, std::min<int64_t>(H, (int64_t(32) << 20) / bytes));
+  }
   const int grid = (int)std::min<int64_t>(units, sms);
   return d == 64 ? launch_bwd<64>(mq, mk, mv, mdo, o, dout, lse, p, counters, max_tiles, grid, s)
                  : launch_bwd<128>(mq, mk, mv, mdo, o, dout, lse, p, counters, max_tiles, grid, s);

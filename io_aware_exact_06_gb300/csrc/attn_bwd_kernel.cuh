@@ -107,6 +107,7 @@ struct BwdParams {
   float scale;         // softmax scale on the logits
   float scale_log2;    // scale * log2(e)
   unsigned long long timeout_ns;
+  int head_group;        // packed: heads per group of the unit order (0: one group)
 };
 
 // Start (sequence-relative) of the 128-row tile t, pulled back so the tile
@@ -363,10 +364,32 @@ __device__ __forceinline__ void place(const BwdParams& p, Unit& un) {
   }
 }
 
+// Packed batches with p.head_group set: heads in groups of that many, one
+// group after the other; within a group the sorted list, then head (the
+// streamed tiles of a group stay in L2).  e: the list entry, h: the head.
+__device__ __forceinline__ void packed_entry(const BwdParams& p, int u, int& e, int& h) {
+  const int E = *p.num_tiles;
+  const int G = p.head_group;
+  const int full = p.H / G;
+  int gi, r, ng;
+  if (u < full * G * E) {
+    gi = u / (G * E);
+    r = u - gi * G * E;
+    ng = G;
+  } else {
+    gi = full;
+    r = u - full * G * E;
+    ng = p.H - full * G;
+  }
+  e = r / ng;
+  h = gi * G + (r - e * ng);
+}
+
 __device__ __forceinline__ Unit kv_unit(const BwdParams& p, int u) {
   Unit un;
-  const int e = u / p.H;
+  int e = u / p.H;
   un.h = u - e * p.H;
+  if (p.cu_seqlens && p.head_group > 0 && p.head_group < p.H) packed_entry(p, u, e, un.h);
   if (p.cu_seqlens) {
     un.b = p.kv_list[2 * e];
     un.t = p.kv_list[2 * e + 1];
@@ -381,8 +404,9 @@ __device__ __forceinline__ Unit kv_unit(const BwdParams& p, int u) {
 
 __device__ __forceinline__ Unit q_unit(const BwdParams& p, int u) {
   Unit un;
-  const int e = u / p.H;
+  int e = u / p.H;
   un.h = u - e * p.H;
+  if (p.cu_seqlens && p.head_group > 0 && p.head_group < p.H) packed_entry(p, u, e, un.h);
   if (p.cu_seqlens) {
     un.b = p.q_list[2 * e];
     un.t = p.q_list[2 * e + 1];

@@ -132,13 +132,15 @@ def test_long_causal_sampled(dev):
     compare(wl, dout, run_bwd(dev, wl, dout), [(0, 3), (1, 14)], "long causal sampled")
 
 
-def run_bwd_packed(dev, wl, dout_bits):
-    """CUDA forward then backward on a packed batch (cu_seqlens on the device)."""
+def run_bwd_packed(dev, wl, dout_bits, N=None):
+    """CUDA forward then backward on a packed batch (cu_seqlens on the device;
+    N: the length bound, by default the longest length)."""
     import torch
     import io_aware_exact_06_gb300 as fa
     H, d = wl.H, wl.d
     lens = wl.seqlens()
-    N = int(lens.max()) if len(lens) else 0
+    if N is None:
+        N = int(lens.max()) if len(lens) else 0
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
     q, k, v, do = t(wl.q), t(wl.k), t(wl.v), t(dout_bits)
     cu = torch.from_numpy(wl.cu_seqlens.astype(np.int32)).to(dev)
@@ -274,3 +276,22 @@ def test_convenience_wrappers(dev):
     assert fa.attn_last_device_error() == 0
     for a, b in zip(ref, (dq, dk, dv)):
         assert np.array_equal(a, b.float().cpu().numpy().astype(np.float64).reshape(a.shape))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_packed_head_group_order_same_result(dev, causal):
+    """Packed calls with a large length bound take their units in head groups
+    (causal: at least 64 units per SM counted from the bound); the result may
+    not depend on the order.  The same sequences with N = their longest length
+    and with N = 8192 (16 sequences x 20 heads x 64 tiles = 20480 units, one
+    head per group on 152 SMs) give bit-identical gradients, and sampled
+    (sequence, head) pairs match the oracle."""
+    lens = inputs.uniform_ints(2750 + causal, 16, 1, 1200).tolist()
+    wl = inputs.make_workload("bwd_groups", 2760 + causal, lens, 20, 128, causal, varlen=True)
+    dout = inputs.normal_bf16(2770 + causal, wl.q.size).reshape(wl.q.shape)
+    a = run_bwd_packed(dev, wl, dout)
+    b = run_bwd_packed(dev, wl, dout, N=8192)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+    pairs = [(s, h) for s, h in ((0, 0), (3, 7), (9, 19), (15, 11)) if lens[s] > 0]
+    compare(wl, dout, b, pairs, f"packed head groups causal={causal}")

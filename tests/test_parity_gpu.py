@@ -357,23 +357,24 @@ def test_grouped_causal_unit_order_every_row(dev, d):
 
 
 @pytest.mark.parametrize("d", [64, 128])
-def test_packed_head_group_order_same_result(dev, d):
-    """Packed causal calls with at least 64 units per SM (counted from the
-    length bound N) take their units in head groups; the result may not
-    depend on the order.  The same sequences with N = their longest length
-    (one group) and with N = 8192 (16 sequences x 20 heads x 32 q-blocks =
-    10240 units, one head per group on 152 SMs) give bit-identical O and
-    LSE, and sampled rows match the oracle."""
+@pytest.mark.parametrize("causal", [False, True])
+def test_packed_head_group_order_same_result(dev, d, causal):
+    """Packed calls take their units in head groups (causal ones with at
+    least 64 units per SM counted from the length bound N); the result may
+    not depend on the order.  The same sequences with N = their longest
+    length and with N = 8192 (16 sequences x 20 heads x 32 q-blocks = 10240
+    units, one head per group on 152 SMs) give bit-identical O and LSE, and
+    sampled rows match the oracle."""
     import io_aware_exact_06_gb300 as fa
     import torch
     lens = inputs.uniform_ints(4545 + d, 16, 1, 1500).tolist()
-    wl = inputs.make_workload("packed_groups", 4546 + d, lens, 20, d, True, varlen=True)
+    wl = inputs.make_workload("packed_groups", 4546 + d, lens, 20, d, causal, varlen=True)
     q, k, v, cu = parity.to_device(wl, dev)
     outs = []
     for N in (int(max(lens)), 8192):
         o = torch.full_like(q, float("nan"))
         lse = torch.full((wl.H, wl.tokens), float("nan"), dtype=torch.float32, device=dev)
-        fa.attn_fwd(q, k, v, o, lse, wl.nseq, wl.H, N, d, wl.scale, True, cu)
+        fa.attn_fwd(q, k, v, o, lse, wl.nseq, wl.H, N, d, wl.scale, causal, cu)
         assert fa.attn_last_device_error() == 0
         outs.append((o, lse))
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
