@@ -108,7 +108,30 @@ struct BwdParams {
   float scale_log2;    // scale * log2(e)
   unsigned long long timeout_ns;
   int head_group;        // packed: heads per group of the unit order (0: one group)
+  int pair_group;        // dense: (sequence, head) pairs per group of the unit order (0: one)
 };
+
+// Dense unit u in pair groups of p.pair_group: within a group, rank (the
+// position in the longest-first tile order) first, then pair.
+__device__ __forceinline__ void dense_grouped(const BwdParams& p, int u, int& rank, int& b, int& h) {
+  const int P = p.B * p.H;
+  const int G = p.pair_group;
+  const int full = P / G;
+  int gi, r, np_;
+  if (u < full * G * p.T) {
+    gi = u / (G * p.T);
+    r = u - gi * G * p.T;
+    np_ = G;
+  } else {
+    gi = full;
+    r = u - full * G * p.T;
+    np_ = P - full * G;
+  }
+  rank = r / np_;
+  const int pair = gi * G + (r - rank * np_);
+  b = pair / p.H;
+  h = pair - b * p.H;
+}
 
 // Start (sequence-relative) of the 128-row tile t, pulled back so the tile
 // ends at the sequence end at the latest; rows before 128 t are the previous
@@ -393,6 +416,8 @@ __device__ __forceinline__ Unit kv_unit(const BwdParams& p, int u) {
   if (p.cu_seqlens) {
     un.b = p.kv_list[2 * e];
     un.t = p.kv_list[2 * e + 1];
+  } else if (p.pair_group > 0 && p.pair_group < p.B * p.H) {
+    dense_grouped(p, u, un.t, un.b, un.h);
   } else {
     un.t = e / p.B;
     un.b = e - un.t * p.B;
@@ -410,6 +435,10 @@ __device__ __forceinline__ Unit q_unit(const BwdParams& p, int u) {
   if (p.cu_seqlens) {
     un.b = p.q_list[2 * e];
     un.t = p.q_list[2 * e + 1];
+  } else if (p.pair_group > 0 && p.pair_group < p.B * p.H) {
+    int rank;
+    dense_grouped(p, u, rank, un.b, un.h);
+    un.t = p.T - 1 - rank;
   } else {
     const int rank = e / p.B;
     un.b = e - rank * p.B;
