@@ -790,14 +790,14 @@ def fp8_cpu_baseline(wl, signs, budget_s: float = 10.0):
 
 # DRAM bytes (read + write) of one attn_fp8_row_kernel<128> launch of this
 # workload, from one ncu capture of the current kernel (None once it
-# changes): 162.61 MB read + 30.54 MB written.
-FP8_TRAFFIC_BYTES = 162_609_920 + 30_540_288
+# changes): 161.60 MB read + 30.78 MB written.
+FP8_TRAFFIC_BYTES = 161_597_184 + 30_781_440
 
 # DRAM bytes (read + write) of one backward call on this workload (all three
 # kernels), from one ncu capture of the current kernels (None once one of them
-# changes): prep 135.28 + 3.56 MB, dK/dV 926.19 + 101.86 MB, dQ 955.66 +
-# 46.44 MB.
-BWD_TRAFFIC_BYTES = 135_279_104 + 3_557_376 + 926_191_872 + 101_856_768 + 955_664_640 + 46_438_400
+# changes): prep 135.28 + 3.50 MB, dK/dV 329.99 + 101.39 MB, dQ 392.99 +
+# 47.84 MB.
+BWD_TRAFFIC_BYTES = 135_279_104 + 3_500_032 + 329_993_472 + 101_385_728 + 392_993_024 + 47_838_720
 
 
 # DRAM bytes (read + write) of one attn_fwd_row_kernel<128> launch of this
