@@ -151,16 +151,29 @@ constexpr int kQuantThreads = kBM;  // one per row of a block
 // x H_D of one row held by one thread, unnormalised, fp32: butterflies over
 // strides 1, 2, 4, ..., D/2, each pair (i, i + s) with bit s of i clear
 // becoming (a + b, a - b), each rounded once.
+// From stride 2 on, the butterflies of channels i and i + 1 (both with bit
+// s clear) run as one packed fp32x2 addition and one subtraction, each lane
+// rounded once like the scalar operations.
+__device__ __forceinline__ void butterfly2(float& a0, float& a1, float& b0, float& b1) {
+  asm("{\n .reg .b64 a, b, s, d;\n mov.b64 a, {%0, %1};\n mov.b64 b, {%2, %3};\n"
+      " add.rn.f32x2 s, a, b;\n sub.rn.f32x2 d, a, b;\n mov.b64 {%0, %1}, s;\n mov.b64 {%2, %3}, d;\n}"
+      : "+f"(a0), "+f"(a1), "+f"(b0), "+f"(b1));
+}
+
 template <int D>
 __device__ __forceinline__ void fwht_row(float (&v)[D]) {
 #pragma unroll
-  for (int s = 1; s < D; s <<= 1) {
+  for (int i = 0; i < D; i += 2) {
+    const float a = v[i], b = v[i + 1];
+    v[i] = a + b;
+    v[i + 1] = a - b;
+  }
 #pragma unroll
-    for (int i = 0; i < D; ++i) {
+  for (int s = 2; s < D; s <<= 1) {
+#pragma unroll
+    for (int i = 0; i < D; i += 2) {
       if (i & s) continue;
-      const float a = v[i], b = v[i + s];
-      v[i] = a + b;
-      v[i + s] = a - b;
+      butterfly2(v[i], v[i + 1], v[i + s], v[i + s + 1]);
     }
   }
 }
