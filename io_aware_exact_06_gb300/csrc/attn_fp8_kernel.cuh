@@ -251,6 +251,9 @@ fp8_quant_stage1_kernel(const __grid_constant__ CUtensorMap tm_q,
   __shared__ float red[2][kQuantThreads / 32];
   const int nb = B * H * T;
   const int r = threadIdx.x;  // the row of the block this thread takes
+  // the V quantiser, launched as this grid's dependent, may take the SM
+  // resources left free meanwhile (it waits for this grid's completion)
+  if (r == 0) grid_dep_launch();
   // block i of this launch: segment, index within it, head, sequence tokens, first staged row
   auto locate = [&](int i, int& seg, int& idx, int& h, int& tok0, int& t, int& r0) {
     const int gidx = i + block0;
@@ -394,6 +397,11 @@ fp8_quant_v_kernel(const __nv_bfloat16* v, const unsigned int* amax_bits, float*
                    int B, int H, int N, int Np, const int* cu_seqlens, const int* num_entries) {
   __shared__ __align__(16) uint8_t tile[kBN][D];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // launched as a dependent of the first stage: nothing global is read before
+  // that grid (the maxima of |V|) has completed; the attention kernel, this
+  // grid's dependent, waits in turn for this one
+  grid_dep_wait();
+  if (threadIdx.x == 0) grid_dep_launch();
   const int T = Np / kBN;
   const int t = blockIdx.x % T;
   const int bh = blockIdx.x / T;

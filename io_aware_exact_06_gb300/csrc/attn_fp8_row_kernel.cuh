@@ -197,7 +197,6 @@ attn_fp8_row_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   uint8_t* sQ = smem;
   uint8_t* sRing = smem + kQTiles * kFp8TileBytes;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int n_units = fp8_num_units(p);
 
   if (threadIdx.x == 0) {
     mbar_init(bar_addr(ss, kBarQFull), 1);
@@ -232,6 +231,10 @@ attn_fp8_row_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ss.tmem_base;
+  // launched as a dependent of the V quantiser: every global access below
+  // waits for that grid (and so for the whole quantisation) to complete
+  grid_dep_wait();
+  const int n_units = fp8_num_units(p);
 
   if (warp >= kRowSoftmaxWarps) {
     setmaxnreg_dec<kRowControlRegs>();

@@ -1305,13 +1305,14 @@ int launch_quant_v(const void* v, uint8_t* codes_t, float* scale, unsigned int* 
                    cudaStream_t s) {
   const int T = (N + attn::kBN - 1) / attn::kBN;
   auto v16 = reinterpret_cast<const __nv_bfloat16*>(v);
-  if (d == 64)
-    attn::fp8_quant_v_kernel<64><<<B * H * T, 256, 0, s>>>(v16, amax_bits, scale, codes_t, B, H, N,
-                                                           T * attn::kBN, cu_seqlens, num_entries);
-  else
-    attn::fp8_quant_v_kernel<128><<<B * H * T, 256, 0, s>>>(v16, amax_bits, scale, codes_t, B, H, N,
-                                                            T * attn::kBN, cu_seqlens, num_entries);
-  cudaError_t e = cudaGetLastError();
+  // a programmatic dependent of the first stage (the kernel waits for it)
+  const int Np = T * attn::kBN;
+  cudaError_t e =
+      d == 64 ? launch_dependent(attn::fp8_quant_v_kernel<64>, B * H * T, 256, 0, s, v16, amax_bits,
+                                 scale, codes_t, B, H, N, Np, cu_seqlens, num_entries)
+              : launch_dependent(attn::fp8_quant_v_kernel<128>, B * H * T, 256, 0, s, v16, amax_bits,
+                                 scale, codes_t, B, H, N, Np, cu_seqlens, num_entries);
+  if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 
@@ -1407,11 +1408,13 @@ int launch_fp8_attention(EncodeTiledFn enc, DeviceState* ds, int* list, const ui
   // 32 MB, as for the bf16 path
   p.head_group = cu_seqlens ? head_group(B, N, d / 2, H, causal != 0, units, ds->sms) : 0;
   const int grid = cu_seqlens ? ds->sms : (int)std::min<int64_t>(units, ds->sms);
-  if (d == 64)
-    attn::attn_fp8_row_kernel<64><<<grid, attn::kRowThreads, attn::kFp8SmemBytes, s>>>(mq, mk, mvt, p);
-  else
-    attn::attn_fp8_row_kernel<128><<<grid, attn::kRowThreads, attn::kFp8SmemBytes, s>>>(mq, mk, mvt, p);
-  cudaError_t e = cudaGetLastError();
+  // a programmatic dependent of the stream's previous kernel (the V
+  // quantiser in attn_fwd_fp8): its set-up overlaps that kernel's last CTAs
+  cudaError_t e = d == 64 ? launch_dependent(attn::attn_fp8_row_kernel<64>, grid, attn::kRowThreads,
+                                             attn::kFp8SmemBytes, s, mq, mk, mvt, p)
+                          : launch_dependent(attn::attn_fp8_row_kernel<128>, grid, attn::kRowThreads,
+                                             attn::kFp8SmemBytes, s, mq, mk, mvt, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 
