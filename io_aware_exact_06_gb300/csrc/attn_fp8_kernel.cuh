@@ -22,13 +22,15 @@
 //
 // Kernels:
 //   fp8_quant_stage1_kernel  rotation + block quantisation of Q and of K, and
-//                         in the same launch the max |V| per (sequence, head)
-//                         (atomic max of the non-negative fp32 bit patterns):
+//                         in the same launch the max |V| of every 128-row
+//                         block of V (its fp32 bit pattern, one word a block):
 //                         persistent CTAs take one (sequence, head, 128-row
 //                         block) at a time, its rows arriving by TMA in a
 //                         shared-memory double buffer while the block before
 //                         is quantised from registers
-//   fp8_quant_v_kernel    V codes, stored transposed per (sequence, head):
+//   fp8_quant_v_kernel    the max |V| per (sequence, head) over its blocks'
+//                         maxima, then V codes, stored transposed per
+//                         (sequence, head):
 //                         [d][keys padded to 128] (keys contiguous), so both
 //                         products of the attention kernel take K-major
 //                         operands
@@ -251,8 +253,11 @@ fp8_quant_stage1_kernel(const __grid_constant__ CUtensorMap tm_q,
   __shared__ float red[2][kQuantThreads / 32];
   const int nb = B * H * T;
   const int r = threadIdx.x;  // the row of the block this thread takes
-  // the V quantiser, launched as this grid's dependent, may take the SM
-  // resources left free meanwhile (it waits for this grid's completion)
+  // launched as a programmatic dependent of the stream's previous kernel:
+  // nothing global is touched before that grid has completed; the V
+  // quantiser, this grid's dependent, may take the SM resources left free
+  // meanwhile (it waits in turn for this grid's completion)
+  grid_dep_wait();
   if (r == 0) grid_dep_launch();
   // block i of this launch: segment, index within it, head, sequence tokens, first staged row
   auto locate = [&](int i, int& seg, int& idx, int& h, int& tok0, int& t, int& r0) {
@@ -372,7 +377,7 @@ fp8_quant_stage1_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int q = D / 16; q < code_stride / 16; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
       }
     } else if (threadIdx.x == 0) {
-      atomicMax(amax_v + idx / T, __float_as_uint(amax));
+      amax_v[idx] = __float_as_uint(amax);
     }
   }
   if (failed) {
@@ -386,7 +391,9 @@ fp8_quant_stage1_kernel(const __grid_constant__ CUtensorMap tm_q,
 
 // V codes, transposed: vt[(b*H + h) * 128 + c][key] for keys padded to Np
 // (a multiple of 128; padding keys of the sequence's last tile get code 0,
-// tiles past its end are not written).  Also writes the V scale.
+// tiles past its end are not written).  The scale is max |V| over the
+// sequence's blocks (amax_bits[(b*H + h) * T + t], the first stage's block
+// maxima); the first tile's CTA writes it to sv.
 // One CTA per (sequence, head, 128 keys): codes go to shared memory key-major
 // (a warp writes one key's 128 bytes), then each thread gathers 16 keys of one
 // channel (the bytes a warp reads at once lie in 8 words: no bank conflict)
@@ -408,7 +415,20 @@ fp8_quant_v_kernel(const __nv_bfloat16* v, const unsigned int* amax_bits, float*
   const int b = bh / H, h = bh % H;
   int tok0, L;
   if (!fp8_seq_block(cu_seqlens, num_entries, b, t, N, tok0, L)) return;  // uniform in the CTA
-  const float amax = __uint_as_float(amax_bits[bh]);
+  // max |V| of the sequence: the bit patterns of non-negative floats order
+  // as the floats do
+  __shared__ unsigned int red_v[8];
+  unsigned int mb = 0u;
+  const int nblk = (L + kBM - 1) / kBM;
+  for (int i = threadIdx.x; i < nblk; i += 256) mb = max(mb, amax_bits[(size_t)bh * T + i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+  if (lane == 0) red_v[warp] = mb;
+  __syncthreads();
+  mb = red_v[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) mb = max(mb, red_v[w]);
+  const float amax = __uint_as_float(mb);
   const float inv = amax > 0.f ? __fdiv_rn(kFp8Max, amax) : 1.0f;
   if (t == 0 && threadIdx.x == 0) sv[bh] = amax > 0.f ? __fdiv_rn(amax, kFp8Max) : 1.0f;
   // warp w: keys w, w + 8, ... of the tile, all 16 rows' loads in flight together

@@ -197,6 +197,9 @@ attn_fp8_row_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   uint8_t* sQ = smem;
   uint8_t* sRing = smem + kQTiles * kFp8TileBytes;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // the next call on the stream may start its CTAs (and their set-up) on the
+  // SMs this grid leaves; it reads nothing before this grid has completed
+  if (threadIdx.x == 0) grid_dep_launch();
 
   if (threadIdx.x == 0) {
     mbar_init(bar_addr(ss, kBarQFull), 1);

@@ -1261,7 +1261,7 @@ int make_map_quant_rows(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, in
 }
 
 // First stage: Q and / or K codes and block scales, and / or max |V| per
-// (sequence, head) (amax_v zeroed here first).  Null inputs are skipped.
+// 128-row block of V (amax_v: B * H * T words).  Null inputs are skipped.
 // Packed (cu_seqlens): num_entries is the worklist's entry count.  The token
 // extent of the copies is B * N (packed: an upper bound of cu_seqlens[B]; no
 // copy leaves its sequence).
@@ -1280,23 +1280,26 @@ int launch_quant_stage1(const void* q, const void* k, const void* v, uint8_t* q8
   const void* src[3] = {q, k, v};
   for (int i = 0; i < 3; ++i)
     if (src[i] && (st = make_map_quant_rows(enc, &maps[i], src[i], tokens, H, d)) != ATTN_OK) return st;
-  cudaError_t e;
-  if (v && (e = cudaMemsetAsync(amax_v, 0, (size_t)B * H * sizeof(unsigned int), s)) != cudaSuccess)
-    return cuda_fail(e);
   // segments: Q, K, V (the blocks run from the first present one to the last)
   const int nseg = v ? 3 : (k ? 2 : 1);
   const int first = q ? 0 : (k ? 1 : 2);
   const int n_blocks = (nseg - first) * nb;
   const int grid = std::min(n_blocks, 3 * ds->sms);
-  if (d == 64)
-    attn::fp8_quant_stage1_kernel<64><<<grid, attn::kQuantThreads, attn::QuantCfg<64>::kSmemBytes, s>>>(
-        maps[0], maps[1], maps[2], q8, k8, sq, sk, amax_v, B, H, N, T, pack_signs(signs, d),
-        signs ? 1 : 0, first * nb, n_blocks, cu_seqlens, num_entries, ds->err, code_stride);
-  else
-    attn::fp8_quant_stage1_kernel<128><<<grid, attn::kQuantThreads, attn::QuantCfg<128>::kSmemBytes, s>>>(
-        maps[0], maps[1], maps[2], q8, k8, sq, sk, amax_v, B, H, N, T, pack_signs(signs, d),
-        signs ? 1 : 0, first * nb, n_blocks, cu_seqlens, num_entries, ds->err, code_stride);
-  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+  // a programmatic dependent of the stream's previous kernel (the kernel
+  // waits for it before its first global access)
+  const attn::Fp8Signs sg = pack_signs(signs, d);
+  const int rotate = signs ? 1 : 0, block0 = first * nb;
+  cudaError_t e =
+      d == 64 ? launch_dependent(attn::fp8_quant_stage1_kernel<64>, grid, attn::kQuantThreads,
+                                 attn::QuantCfg<64>::kSmemBytes, s, maps[0], maps[1], maps[2], q8, k8,
+                                 sq, sk, amax_v, B, H, N, T, sg, rotate, block0, n_blocks,
+                                 cu_seqlens, num_entries, ds->err, code_stride)
+              : launch_dependent(attn::fp8_quant_stage1_kernel<128>, grid, attn::kQuantThreads,
+                                 attn::QuantCfg<128>::kSmemBytes, s, maps[0], maps[1], maps[2], q8, k8,
+                                 sq, sk, amax_v, B, H, N, T, sg, rotate, block0, n_blocks,
+                                 cu_seqlens, num_entries, ds->err, code_stride);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
   return ATTN_OK;
 }
 
@@ -1352,9 +1355,10 @@ extern "C" int attn_fp8_quantize_v(const void* v, uint8_t* codes_t, float* scale
   DeviceState* ds = nullptr;
   if ((st = device_state(dev, &ds)) != ATTN_OK) return st;
   uint8_t* ws = nullptr;
-  if ((st = fp8_workspace(dev, stream, (size_t)B * H * sizeof(unsigned int) + 256, &ws)) != ATTN_OK)
+  const size_t n_blk = (size_t)B * H * ((N + attn::kBM - 1) / attn::kBM);
+  if ((st = fp8_workspace(dev, stream, n_blk * sizeof(unsigned int) + 256, &ws)) != ATTN_OK)
     return st;
-  unsigned int* amax = reinterpret_cast<unsigned int*>(ws);
+  unsigned int* amax = reinterpret_cast<unsigned int*>(ws);  // max |V| per 128-row block
   int* list = nullptr;
   if ((st = fp8_worklist(dev, stream, ds, cu_seqlens, B, N, 0, &list)) != ATTN_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -1445,12 +1449,12 @@ extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o
   const int64_t np = T * attn::kBN;
   const int64_t bh = (int64_t)B * H;
   // workspace: Q codes, K codes, V codes (transposed, padded), Q and K block
-  // scales, V scales, V max bits; each part 256-byte aligned
+  // scales, V scales, V block maxima (bits); each part 256-byte aligned
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
   const size_t b_q = up((size_t)tokens * H * attn::kFp8D), b_vt = up((size_t)bh * d * np);
   const size_t b_s = up((size_t)bh * T * sizeof(float)), b_v = up((size_t)bh * sizeof(float));
   uint8_t* ws = nullptr;
-  if ((st = fp8_workspace(dev, stream, 2 * b_q + b_vt + 2 * b_s + 2 * b_v + 256, &ws)) != ATTN_OK)
+  if ((st = fp8_workspace(dev, stream, 2 * b_q + b_vt + 3 * b_s + b_v + 256, &ws)) != ATTN_OK)
     return st;
   uint8_t* q8 = ws;
   uint8_t* k8 = q8 + b_q;
