@@ -394,15 +394,16 @@ fp8_quant_stage1_kernel(const __grid_constant__ CUtensorMap tm_q,
 // tiles past its end are not written).  The scale is max |V| over the
 // sequence's blocks (amax_bits[(b*H + h) * T + t], the first stage's block
 // maxima); the first tile's CTA writes it to sv.
-// One CTA per (sequence, head, 128 keys): codes go to shared memory key-major
-// (a warp writes one key's 128 bytes), then each thread gathers 16 keys of one
-// channel (the bytes a warp reads at once lie in 8 words: no bank conflict)
-// and writes them as one 16-byte store.
+// One CTA per (sequence, head, 128 keys); warp w takes keys 16 w .. 16 w + 15
+// and lane l channels 4 l .. 4 l + 3 (one 8-byte load per key, a warp reading
+// whole rows), so a thread holds a 16-key x 4-channel block of codes: four
+// 4 x 4 byte transposes (byte permutes) turn it into 16 keys of each of its
+// channels, one 16-byte store per channel.
 template <int D>
 __global__ void __launch_bounds__(256)
 fp8_quant_v_kernel(const __nv_bfloat16* v, const unsigned int* amax_bits, float* sv, uint8_t* vt,
                    int B, int H, int N, int Np, const int* cu_seqlens, const int* num_entries) {
-  __shared__ __align__(16) uint8_t tile[kBN][D];
+  static_assert(kBN == 8 * 16, "8 warps of 16 keys");
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   // launched as a dependent of the first stage: nothing global is read before
   // that grid (the maxima of |V|) has completed; the attention kernel, this
@@ -415,6 +416,16 @@ fp8_quant_v_kernel(const __nv_bfloat16* v, const unsigned int* amax_bits, float*
   const int b = bh / H, h = bh % H;
   int tok0, L;
   if (!fp8_seq_block(cu_seqlens, num_entries, b, t, N, tok0, L)) return;  // uniform in the CTA
+  // this thread's 16 keys, all loads in flight together (issued before the
+  // scale is known: they overlap its reduction)
+  const bool active = lane < D / 4;
+  const int key0 = t * kBN + 16 * warp;
+  uint2 raw[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    raw[i] = active && key0 + i < L
+                 ? *reinterpret_cast<const uint2*>(v + ((size_t)(tok0 + key0 + i) * H + h) * D + 4 * lane)
+                 : make_uint2(0u, 0u);
   // max |V| of the sequence: the bit patterns of non-negative floats order
   // as the floats do
   __shared__ unsigned int red_v[8];
@@ -431,38 +442,31 @@ fp8_quant_v_kernel(const __nv_bfloat16* v, const unsigned int* amax_bits, float*
   const float amax = __uint_as_float(mb);
   const float inv = amax > 0.f ? __fdiv_rn(kFp8Max, amax) : 1.0f;
   if (t == 0 && threadIdx.x == 0) sv[bh] = amax > 0.f ? __fdiv_rn(amax, kFp8Max) : 1.0f;
-  // warp w: keys w, w + 8, ... of the tile, all 16 rows' loads in flight together
-  constexpr int kRowsV = kBN / 8;
-  uint2 raw[kRowsV];
+  if (!active) return;
+  // codes of key i, channels 4 l + j in byte j
+  uint32_t cw[16];
 #pragma unroll
-  for (int i = 0; i < kRowsV; ++i) {
-    const int key = t * kBN + warp + 8 * i;
-    raw[i] = key < L && lane < D / 4
-                 ? *reinterpret_cast<const uint2*>(v + ((size_t)(tok0 + key) * H + h) * D + 4 * lane)
-                 : make_uint2(0u, 0u);
-  }
-#pragma unroll
-  for (int i = 0; i < kRowsV; ++i) {
+  for (int i = 0; i < 16; ++i) {
     const float f0 = __uint_as_float(raw[i].x << 16), f1 = __uint_as_float(raw[i].x & 0xffff0000u);
     const float f2 = __uint_as_float(raw[i].y << 16), f3 = __uint_as_float(raw[i].y & 0xffff0000u);
-    if (lane < D / 4)
-      *reinterpret_cast<uint32_t*>(&tile[warp + 8 * i][4 * lane]) =
-          e4m3x4(__fmul_rn(f0, inv), __fmul_rn(f1, inv), __fmul_rn(f2, inv), __fmul_rn(f3, inv));
+    cw[i] = e4m3x4(__fmul_rn(f0, inv), __fmul_rn(f1, inv), __fmul_rn(f2, inv), __fmul_rn(f3, inv));
   }
-  __syncthreads();
-  // output chunk i: channel c = i % 128, keys 16 q .. 16 q + 15 with q = i / 128
+  // out[j][m]: channel 4 l + j, keys 4 m .. 4 m + 3 (key 4 m + i in byte i)
+  uint32_t out[4][4];
 #pragma unroll
-  for (int i = threadIdx.x; i < D * (kBN / 16); i += 256) {
-    const int c = i % D, q = i / D;
-    uint32_t w[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      w[j] = (uint32_t)tile[16 * q + 4 * j][c] | ((uint32_t)tile[16 * q + 4 * j + 1][c] << 8) |
-             ((uint32_t)tile[16 * q + 4 * j + 2][c] << 16) |
-             ((uint32_t)tile[16 * q + 4 * j + 3][c] << 24);
-    *reinterpret_cast<uint4*>(vt + ((size_t)bh * D + c) * Np + t * kBN + q * 16) =
-        make_uint4(w[0], w[1], w[2], w[3]);
+  for (int m = 0; m < 4; ++m) {
+    const uint32_t a0 = cw[4 * m], a1 = cw[4 * m + 1], a2 = cw[4 * m + 2], a3 = cw[4 * m + 3];
+    const uint32_t lo01 = __byte_perm(a0, a1, 0x5140), lo23 = __byte_perm(a2, a3, 0x5140);
+    const uint32_t hi01 = __byte_perm(a0, a1, 0x7362), hi23 = __byte_perm(a2, a3, 0x7362);
+    out[0][m] = __byte_perm(lo01, lo23, 0x5410);
+    out[1][m] = __byte_perm(lo01, lo23, 0x7632);
+    out[2][m] = __byte_perm(hi01, hi23, 0x5410);
+    out[3][m] = __byte_perm(hi01, hi23, 0x7632);
   }
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    *reinterpret_cast<uint4*>(vt + ((size_t)bh * D + 4 * lane + j) * Np + key0) =
+        make_uint4(out[j][0], out[j][1], out[j][2], out[j][3]);
 }
 
 // ------------------------------------------------------------ attention --
