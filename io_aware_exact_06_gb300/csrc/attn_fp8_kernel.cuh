@@ -202,14 +202,14 @@ __device__ __forceinline__ void fp8_load_row(const uint8_t* stage, int r, const 
   }
 }
 
-// max over the 128 threads of m (every thread gets it); red: 4 floats of
-// shared memory, free on entry
-__device__ __forceinline__ float block_max128(float m, float* red) {
-#pragma unroll
-  for (int s = 16; s > 0; s >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x / 32] = m;
+// max over the 128 threads of the words b (every thread gets it); red: 4
+// words of shared memory, free on entry.  For the bit patterns of
+// non-negative floats this is the float maximum.
+__device__ __forceinline__ uint32_t block_max128_bits(uint32_t b, uint32_t* red) {
+  b = __reduce_max_sync(0xffffffffu, b);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x / 32] = b;
   __syncthreads();
-  return fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  return max(max(red[0], red[1]), max(red[2], red[3]));
 }
 
 // Tokens [tok0, tok0 + L) of sequence b; false when block t lies past its end
@@ -250,7 +250,7 @@ fp8_quant_stage1_kernel(const __grid_constant__ CUtensorMap tm_q,
                                               ~static_cast<uintptr_t>(1023));
   __shared__ uint64_t full[2];
   __shared__ __align__(16) uint32_t flips[D / 2];
-  __shared__ float red[2][kQuantThreads / 32];
+  __shared__ uint32_t red[2][kQuantThreads / 32];
   const int nb = B * H * T;
   const int r = threadIdx.x;  // the row of the block this thread takes
   // launched as a programmatic dependent of the stream's previous kernel:
@@ -309,17 +309,16 @@ fp8_quant_stage1_kernel(const __grid_constant__ CUtensorMap tm_q,
     int seg, idx, h, tok0, t, r0;
     const bool valid = locate(i, seg, idx, h, tok0, t, r0);  // the same in every thread
     float v[D];
-    float m = 0.f;
+    float m = 0.f;  // max |x| of this thread's row: never NaN (max.f32 drops NaN inputs)
+    bool ok = true;
     if (valid) {
-      const bool ok = mbar_wait(smem_u32(&full[buf]), (buf ? used1 : used0) & 1, 2000000000ull);
+      ok = mbar_wait(smem_u32(&full[buf]), (buf ? used1 : used0) & 1, 2000000000ull);
       if (buf)
         ++used1;
       else
         ++used0;
-      if (__syncthreads_or(!ok)) {
-        failed = true;
-        break;
-      }
+    }
+    if (valid && ok) {
       const uint8_t* st = stage + buf * QC::kBlockBytes;
       if (seg < 2) {
         if (r0 + r >= 0) {
@@ -345,8 +344,15 @@ fp8_quant_stage1_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
       }
     }
-    // every read of this buffer is done once all threads have the block max
-    const float amax = block_max128(m, red[k & 1]);
+    // every read of this buffer is done once all threads have the block max;
+    // a thread whose copy wait gave up contributes all-ones, above the bits
+    // of every non-negative float, so that all threads leave together
+    const uint32_t mbits = block_max128_bits(ok ? __float_as_uint(m) : 0xffffffffu, red[k & 1]);
+    if (mbits == 0xffffffffu) {
+      failed = true;
+      break;
+    }
+    const float amax = __uint_as_float(mbits);
     if (threadIdx.x == 0) {
       // (the generic-proxy reads above before the copy that overwrites them)
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
