@@ -147,6 +147,10 @@ struct QuantCfg {
   static constexpr int kChunks = D / 64;
   static constexpr int kBlockBytes = kBM * D * 2;
   static constexpr int kSmemBytes = 2 * kBlockBytes + 1024;
+  // resident CTAs per SM: at d = 128 a row's 128 channels and the butterflies
+  // need about 225 registers (two CTAs: no spills; three spilled 24 bytes and
+  // were slower); at d = 64, three
+  static constexpr int kCtasPerSm = D == 128 ? 2 : 3;
 };
 constexpr int kQuantThreads = kBM;  // one per row of a block
 
@@ -235,9 +239,9 @@ __device__ __forceinline__ bool fp8_seq_block(const int* cu_seqlens, const int* 
 // tm_q, tm_k, tm_v: [tokens][H][D] bf16, box 64 channels x 1 head x 128 rows,
 // 128-byte swizzle (a map of an absent input is never used).  Codes go to
 // rows of code_stride bytes (D, or 128 for the attention kernel's padded
-// rows).  Persistent CTAs of 128 threads.
+// rows).  Persistent CTAs of 128 threads, QuantCfg<D>::kCtasPerSm per SM.
 template <int D>
-__global__ void __launch_bounds__(kQuantThreads, 3)
+__global__ void __launch_bounds__(kQuantThreads, QuantCfg<D>::kCtasPerSm)
 fp8_quant_stage1_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, uint8_t* q8, uint8_t* k8,

@@ -1284,7 +1284,8 @@ int launch_quant_stage1(const void* q, const void* k, const void* v, uint8_t* q8
   const int nseg = v ? 3 : (k ? 2 : 1);
   const int first = q ? 0 : (k ? 1 : 2);
   const int n_blocks = (nseg - first) * nb;
-  const int grid = std::min(n_blocks, 3 * ds->sms);
+  const int grid = std::min(n_blocks, (d == 64 ? attn::QuantCfg<64>::kCtasPerSm
+                                                : attn::QuantCfg<128>::kCtasPerSm) * ds->sms);
   // a programmatic dependent of the stream's previous kernel (the kernel
   // waits for it before its first global access)
   const attn::Fp8Signs sg = pack_signs(signs, d);
