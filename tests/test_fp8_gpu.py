@@ -104,6 +104,30 @@ def test_quantize_v_bit_exact(dev, N, d):
     assert not got[:, :, :, N:].any(), "padding keys are zero"
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_quantize_v_many_blocks_bit_exact(dev, d):
+    """More than 256 blocks of 128 keys per sequence: the V quantiser's
+    reduction of the block maxima loops over them; one outlier in the last
+    block sets the scale."""
+    import torch
+    import io_aware_exact_06_gb300 as fa
+    B, H, N = 1, 2, 33000
+    v = inputs.normal_bf16(3250 + d, B * N * H * d).reshape(B * N, H, d)
+    v[N - 5, 1, d - 1] = inputs.f64_to_bf16_bits(np.array([40.0]))[0]
+    Np = 128 * (-(-N // 128))
+    codes_t = torch.full((B, H, d, Np), 0x55, dtype=torch.uint8, device=dev)
+    scale = torch.zeros((B, H), dtype=torch.float32, device=dev)
+    fa.attn_fp8_quantize_v(to_dev(dev, v), codes_t, scale, B, H, N, d)
+    assert fa.attn_last_device_error() == 0
+    ref_codes, ref_scale = oracle.fp8_quantize(v, B, N, 0, False)
+    assert ref_scale[0, 1, 0] == np.float32(40.0 / 448.0)
+    got = codes_t.cpu().numpy()
+    assert np.array_equal(scale.cpu().numpy(), ref_scale[:, :, 0])
+    back = got[:, :, :, :N].transpose(0, 3, 1, 2).reshape(B * N, H, d)
+    assert np.array_equal(back, ref_codes)
+    assert not got[:, :, :, N:].any(), "padding keys are zero"
+
+
 def dequantised(x, B, N, block_rows, rotate, sg):
     """fp64 values of the oracle's codes times their block scales."""
     codes, scales = oracle.fp8_quantize(x, B, N, block_rows, rotate, sg)
@@ -316,15 +340,16 @@ def test_quantize_qk_packed_bit_exact(dev, rotate):
         assert np.array_equal(got_c[cu[b]:cu[b + 1]], ref_c), b
 
 
-def test_quantize_v_packed_bit_exact(dev):
+@pytest.mark.parametrize("d", [64, 128])
+def test_quantize_v_packed_bit_exact(dev, d):
     import torch
     import io_aware_exact_06_gb300 as fa
     H, N = 3, max(PACKED_LENS)
-    cu, _, _, v = packed_inputs(3700, PACKED_LENS, H, 1.5)
+    cu, _, _, v = packed_inputs(3700 + d, PACKED_LENS, H, 1.5, d=d)
     B, Np = len(PACKED_LENS), 128 * -(-N // 128)
-    codes_t = torch.full((B, H, 128, Np), 0x55, dtype=torch.uint8, device=dev)
+    codes_t = torch.full((B, H, d, Np), 0x55, dtype=torch.uint8, device=dev)
     scale = torch.full((B, H), -1.0, dtype=torch.float32, device=dev)
-    fa.attn_fp8_quantize_v(to_dev(dev, v), codes_t, scale, B, H, N, 128, cu_dev(dev, cu))
+    fa.attn_fp8_quantize_v(to_dev(dev, v), codes_t, scale, B, H, N, d, cu_dev(dev, cu))
     assert fa.attn_last_device_error() == 0
     got, got_s = codes_t.cpu().numpy(), scale.cpu().numpy()
     for b, L in enumerate(PACKED_LENS):
