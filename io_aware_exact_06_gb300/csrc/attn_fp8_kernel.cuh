@@ -234,8 +234,8 @@ __device__ __forceinline__ bool fp8_seq_block(const int* cu_seqlens, const int* 
 
 // One launch for the first quantisation stage over blocks block0 + i, i in
 // [0, n_blocks): blocks [0, nb) quantise Q, [nb, 2 nb) quantise K, [2 nb,
-// 3 nb) take the max |V| per (sequence, head) (atomic max of the
-// non-negative fp32 bit patterns); nb = B * H * T, block = (b * H + h) * T + t.
+// 3 nb) write the max |V| of each 128-row block of V (its fp32 bit pattern,
+// amax_v[block]); nb = B * H * T, block = (b * H + h) * T + t.
 // tm_q, tm_k, tm_v: [tokens][H][D] bf16, box 64 channels x 1 head x 128 rows,
 // 128-byte swizzle (a map of an absent input is never used).  Codes go to
 // rows of code_stride bytes (D, or 128 for the attention kernel's padded
