@@ -308,8 +308,8 @@ cudaError_t launch_dependent(void (*kernel)(KArgs...), int grid, int threads, si
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-// mo: O through 32-row boxes, for the d = 64 one-thread-per-row kernel's TMA
-// stores (unused by the other kernels).
+// mo: O through 32-row x 64-column boxes, for the one-thread-per-row kernel's
+// TMA stores (unused by the other kernels).
 template <int D>
 int launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                 const CUtensorMap& mo, const FwdParams& p, int grid, cudaStream_t s,
@@ -430,7 +430,7 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* l
   if (opts && opts->max_ctas > 0 && opts->max_ctas < grid) grid = opts->max_ctas;
   const bool rows = one_thread_per_row(d, opts ? opts->kernel : 0);
   CUtensorMap mo = mq;
-  if (rows && attn::RowCfg<64>::kStageO && d == 64 &&
+  if (rows && (d == 64 ? attn::RowCfg<64>::kStageO : attn::RowCfg<128>::kStageO) &&
       (st = make_map(enc, &mo, o, tokens_bound, H, d, 32)) != ATTN_OK)
     return st;
   return d == 64 ? launch_attn<64>(mq, mk, mv, mo, p, grid, s, rows)
@@ -804,7 +804,7 @@ int attn_fwd_noalloc_impl(const void* q, const void* k, const void* v, void* o, 
   if (opts && opts->max_ctas > 0 && opts->max_ctas < grid) grid = opts->max_ctas;
   const bool rows = one_thread_per_row(d, opts ? opts->kernel : 0);
   CUtensorMap mo = mq;
-  if (rows && attn::RowCfg<64>::kStageO && d == 64 &&
+  if (rows && (d == 64 ? attn::RowCfg<64>::kStageO : attn::RowCfg<128>::kStageO) &&
       (st = make_map(enc, &mo, o, tokens_bound, H, d, 32)) != ATTN_OK)
     return st;
   return d == 64 ? launch_attn<64>(mq, mk, mv, mo, p, grid, s, rows)

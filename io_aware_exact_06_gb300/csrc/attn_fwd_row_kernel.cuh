@@ -43,11 +43,11 @@ static_assert(kRowSoftmaxWarps * 32 * kRowSoftmaxRegs + 128 * kRowControlRegs <=
 // one control warp
 static_assert(2 * 32 * kRowSoftmaxRegs + 32 * kRowControlRegs <= 16384, "register-file quarter");
 
-// Shared memory of the kernel: Q tiles, the K/V ring and, at d = 64, where
-// they fit, a second Q buffer (the next unit's Q tiles load while the
-// current unit runs) and an O staging tile per query tile (the epilogue
-// writes each warp's 32 rows there and stores them to global memory four
-// whole rows per instruction).
+// Shared memory of the kernel: Q tiles, the K/V ring, an O staging tile of
+// 32 rows x 64 columns per softmax warp (the epilogue writes 64 columns of
+// the warp's 32 rows there and stores them with one TMA store, two rounds at
+// d = 128), and, at d = 64, where it fits, a second Q buffer (the next
+// unit's Q tiles load while the current unit runs).
 //
 // At d = 64 TMEM also has room for P apart from S (S_g [128 g, +128), O_g
 // [256 + 64 g, +64), P_g [384 + 64 g, +64)), so a group's next S product is
@@ -57,12 +57,14 @@ template <int D>
 struct RowCfg {
   using C = FwdCfg<D>;
   static constexpr int kQBufs = D == 64 ? 2 : 1;
-  static constexpr bool kStageO = D == 64;
+  static constexpr bool kStageO = true;
+  static constexpr int kStageWarpBytes = 32 * 128;               // 32 rows x 64 bf16
+  static constexpr int kStageGroupBytes = 4 * kStageWarpBytes;   // a query tile's 4 warps
   static constexpr bool kSPre = D == 64;
   __host__ __device__ static constexpr uint32_t col_p(int g) {
     return kSPre ? 384u + 64u * (uint32_t)g : C::col_s(g);
   }
-  static constexpr int kSmemStage = kStageO ? kQTiles * C::kTileBytes : 0;
+  static constexpr int kSmemStage = kStageO ? kQTiles * kStageGroupBytes : 0;
   static constexpr int kSmemBytes = kQBufs * C::kSmemQ + C::kSmemRing + kSmemStage + 1024;
 };
 static_assert(RowCfg<64>::kSmemBytes + 1024 <= 227 * 1024, "shared memory of the d = 64 kernel");
@@ -345,52 +347,57 @@ __device__ __forceinline__ void softmax_rows(const FwdParams& p, SharedState& ss
     const bool store = row >= nominal0 && row < cur_L && row >= 0;
     const float inv_l = l_r > 0.f ? 1.0f / l_r : 0.f;
     if constexpr (RowCfg<D>::kStageO) {
-      // This warp's 32 rows through its staging tile: the thread writes its
-      // row (16-byte chunk c of row r at r * 128 + 16 (c ^ (r % 8)), no bank
-      // conflicts; the 128-byte swizzle of the tensor map), then one TMA store
-      // of the 32 rows; where the tile starts before its nominal rows (pulled
-      // back at the sequence end) or before the buffer, lane l stores chunk
-      // l % 8 of rows 4 i + l / 8 instead, four whole rows per instruction.
-      static_assert(D == 64, "one 128-byte row per thread");
-      uint8_t* stage = sStage + g * FwdCfg<D>::kTileBytes + quadrant * 32 * 128;
-      // the previous TMA store from this tile has read it
-      if (lane == 0) bulk_wait_read_all();
-      __syncwarp();
+      // This warp's 32 rows through its staging tile, 64 columns at a time:
+      // the thread writes its row's 64 columns (16-byte chunk c of row r at
+      // r * 128 + 16 (c ^ (r % 8)), no bank conflicts; the 128-byte swizzle
+      // of the tensor map), then one TMA store of the 32 rows x 64 columns;
+      // where the tile starts before its nominal rows (pulled back at the
+      // sequence end) or before the buffer, lane l stores chunk l % 8 of rows
+      // 4 i + l / 8 instead, four 128-byte row pieces per instruction.
+      uint8_t* stage = sStage + g * RowCfg<D>::kStageGroupBytes + quadrant * RowCfg<D>::kStageWarpBytes;
+      const bool whole = a0 == nominal0 && a0 >= 0;
 #pragma unroll
-      for (int cc = 0; cc < D; cc += 32) {
-        uint32_t r[32];
-        tmem_ld_x32(lane_addr + colO + cc, r);
-        tmem_ld_wait_x32(r);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(r[8 * i + 0]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l);
-          w.y = pack_bf16x2(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l);
-          w.z = pack_bf16x2(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l);
-          w.w = pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l);
-          const int c = cc / 8 + i;
-          *reinterpret_cast<uint4*>(stage + lane * 128 + ((c ^ (lane & 7)) << 4)) = w;
-        }
-      }
-      if (a0 == nominal0 && a0 >= 0) {
-        fence_async_smem();
+      for (int hh = 0; hh < D / 64; ++hh) {
+        // the previous TMA store from this tile has read it
+        if (lane == 0) bulk_wait_read_all();
         __syncwarp();
-        if (lane == 0) {
-          tma_store_3d(tm_o, smem_u32(stage), 0, cur_h, cur_tok0 + a0 + quadrant * 32);
-          bulk_commit();
-        }
-      } else {
-        __syncwarp();
-        const int c = lane & 7;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int rr = 4 * i + (lane >> 3);
-          const uint4 w = *reinterpret_cast<const uint4*>(stage + rr * 128 + ((c ^ (rr & 7)) << 4));
-          const int row_r = a0 + quadrant * 32 + rr;
-          if (row_r >= nominal0 && row_r < cur_L && row_r >= 0)
-            *reinterpret_cast<uint4*>(p.o + ((size_t)(cur_tok0 + row_r) * p.H + cur_h) * D + 8 * c) = w;
+        for (int cc = 0; cc < 64; cc += 32) {
+          uint32_t r[32];
+          tmem_ld_x32(lane_addr + colO + 64 * hh + cc, r);
+          tmem_ld_wait_x32(r);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(r[8 * i + 0]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l);
+            w.y = pack_bf16x2(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l);
+            w.z = pack_bf16x2(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l);
+            w.w = pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l);
+            const int c = cc / 8 + i;
+            *reinterpret_cast<uint4*>(stage + lane * 128 + ((c ^ (lane & 7)) << 4)) = w;
+          }
         }
-        __syncwarp();   // every lane has read the tile before the next unit writes it
+        if (whole) {
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(tm_o, smem_u32(stage), 64 * hh, cur_h, cur_tok0 + a0 + quadrant * 32);
+            bulk_commit();
+          }
+        } else {
+          __syncwarp();
+          const int c = lane & 7;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = 4 * i + (lane >> 3);
+            const uint4 w = *reinterpret_cast<const uint4*>(stage + rr * 128 + ((c ^ (rr & 7)) << 4));
+            const int row_r = a0 + quadrant * 32 + rr;
+            if (row_r >= nominal0 && row_r < cur_L && row_r >= 0)
+              *reinterpret_cast<uint4*>(p.o + ((size_t)(cur_tok0 + row_r) * p.H + cur_h) * D + 64 * hh +
+                                        8 * c) = w;
+          }
+          __syncwarp();   // every lane has read the tile before it is written again
+        }
       }
     } else {
       __nv_bfloat16* orow = p.o + ((size_t)(store ? cur_tok0 + row : 0) * p.H + cur_h) * D;
