@@ -803,13 +803,13 @@ BWD_TRAFFIC_BYTES = 135_279_104 + 3_500_032 + 329_993_472 + 101_385_728 + 392_99
 
 # DRAM bytes (read + write) of one attn_fwd_row_kernel<128> launch of this
 # workload, from one ncu capture of the current kernel (None once it changes).
-TRAFFIC_BYTES = 537_853_440 + 45_941_248  # 537.85 MB read + 45.94 MB written
+TRAFFIC_BYTES = 542_989_056 + 47_214_592  # 542.99 MB read + 47.21 MB written
 # The same for other forward workloads: attn_fwd_row_kernel<64> on the GPT-2
-# shaped one (37.82 MB read + 1.5 KB written: O, 12.6 MB, is still in L2
+# shaped one (37.82 MB read + 2 KB written: O, 12.6 MB, is still in L2
 # when the kernel ends) and attn_fwd_row_kernel<128> on the stress and the
 # packed ones.
-CONFIG_TRAFFIC_BYTES = {"gpt2_causal": 37_816_576 + 1_536, "stress": 248_950_016 + 50_955_008,
-                        "varlen": 1_910_574_080 + 463_506_688}
+CONFIG_TRAFFIC_BYTES = {"gpt2_causal": 37_817_856 + 2_048, "stress": 262_001_408 + 52_552_448,
+                        "varlen": 1_985_222_400 + 464_122_880}
 
 
 def main():
