@@ -61,7 +61,13 @@ namespace attn {
 constexpr int kFp8D = 128;  // bytes of a Q / K code row in the attention kernel (channels, padded)
 constexpr int kFp8TileBytes = kBM * kFp8D;   // 128 rows x 128 e4m3 = one 128-byte swizzle span
 constexpr int kFp8Stages = 8;                // K / V ring slots
-constexpr int kFp8SmemBytes = kQTiles * kFp8TileBytes + kFp8Stages * kFp8TileBytes + 1024;
+// O staging: per softmax warp its 32 rows of bf16 O, one 32 x 64 tile (4 KB,
+// 128-byte swizzle) per 64 channels, stored by TMA
+constexpr int kFp8StageWarpBytes = 2 * 32 * 128;
+constexpr int kFp8SmemStage = kQTiles * 4 * kFp8StageWarpBytes;
+constexpr int kFp8SmemBytes =
+    kQTiles * kFp8TileBytes + kFp8Stages * kFp8TileBytes + kFp8SmemStage + 1024;
+static_assert(kFp8SmemBytes + 1024 <= 227 * 1024, "shared memory of the FP8 kernel");
 constexpr float kFp8Max = 448.0f;
 constexpr float kFp8PLog2 = 8.0f;            // P is stored as e4m3(2^8 P)
 constexpr float kFp8RescaleLog2 = 0.75f;

@@ -26,7 +26,7 @@ constexpr int kFp8RowUnitConsumers = 1 + kRowSoftmaxWarps;  // the MMA thread an
 
 template <int D>
 __device__ __forceinline__ void fp8_softmax_rows(const Fp8Params& p, SharedState& ss, uint32_t tmem,
-                                                 int g) {
+                                                 int g, uint8_t* sStage, const CUtensorMap* tm_o) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int quadrant = warp % 4;
   const int trow = quadrant * 32 + lane;              // row of the tile = TMEM lane
@@ -158,24 +158,60 @@ __device__ __forceinline__ void fp8_softmax_rows(const Fp8Params& p, SharedState
     tc_fence_after();
     const bool store = row >= nominal0 && row < un.L && row >= 0;
     const float ofac = l > 0.f ? p.sv[bh] / l : 0.f;
-    __nv_bfloat16* orow = p.o + ((size_t)(store ? un.tok0 + row : 0) * p.H + un.h) * D;
+    // O of the warp's 32 rows through its staging tiles (64 channels each:
+    // 16-byte chunk c of row r at r * 128 + 16 (c ^ (r % 8)), the 128-byte
+    // swizzle of the tensor map), then one TMA store per 64 channels; where
+    // the tile starts before its nominal rows (pulled back at the sequence
+    // end) or before the buffer, lane l stores chunk l % 8 of rows 4 i + l / 8
+    // instead, four 128-byte row pieces per instruction
+    uint8_t* stage = sStage + (g * 4 + quadrant) * kFp8StageWarpBytes;
+    // the previous unit's TMA stores from these tiles have read them
+    if (lane == 0) bulk_wait_read_all();
+    __syncwarp();
 #pragma unroll
     for (int cc = 0; cc < D; cc += 32) {
       uint32_t r[32];
       tmem_ld_x32(lane_addr + colO + cc, r);
       tmem_ld_wait_x32(r);
-      if (store) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + cc);
+      uint8_t* st = stage + (cc / 64) * (32 * 128);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(r[8 * i + 0]) * ofac, __uint_as_float(r[8 * i + 1]) * ofac);
-          w.y = pack_bf16x2(__uint_as_float(r[8 * i + 2]) * ofac, __uint_as_float(r[8 * i + 3]) * ofac);
-          w.z = pack_bf16x2(__uint_as_float(r[8 * i + 4]) * ofac, __uint_as_float(r[8 * i + 5]) * ofac);
-          w.w = pack_bf16x2(__uint_as_float(r[8 * i + 6]) * ofac, __uint_as_float(r[8 * i + 7]) * ofac);
-          dst[i] = w;
+      for (int i = 0; i < 4; ++i) {
+        uint4 w;
+        w.x = pack_bf16x2(__uint_as_float(r[8 * i + 0]) * ofac, __uint_as_float(r[8 * i + 1]) * ofac);
+        w.y = pack_bf16x2(__uint_as_float(r[8 * i + 2]) * ofac, __uint_as_float(r[8 * i + 3]) * ofac);
+        w.z = pack_bf16x2(__uint_as_float(r[8 * i + 4]) * ofac, __uint_as_float(r[8 * i + 5]) * ofac);
+        w.w = pack_bf16x2(__uint_as_float(r[8 * i + 6]) * ofac, __uint_as_float(r[8 * i + 7]) * ofac);
+        const int c = (cc % 64) / 8 + i;
+        *reinterpret_cast<uint4*>(st + lane * 128 + ((c ^ (lane & 7)) << 4)) = w;
+      }
+    }
+    if (a0 == nominal0 && a0 >= 0) {
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+#pragma unroll
+        for (int hh = 0; hh < D / 64; ++hh)
+          tma_store_3d(tm_o, smem_u32(stage + hh * (32 * 128)), 64 * hh, un.h,
+                       un.tok0 + a0 + quadrant * 32);
+        bulk_commit();
+      }
+    } else {
+      __syncwarp();
+      const int c = lane & 7;
+#pragma unroll
+      for (int hh = 0; hh < D / 64; ++hh) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rr = 4 * i + (lane >> 3);
+          const uint4 w =
+              *reinterpret_cast<const uint4*>(stage + hh * (32 * 128) + rr * 128 + ((c ^ (rr & 7)) << 4));
+          const int row_r = a0 + quadrant * 32 + rr;
+          if (row_r >= nominal0 && row_r < un.L && row_r >= 0)
+            *reinterpret_cast<uint4*>(p.o + ((size_t)(un.tok0 + row_r) * p.H + un.h) * D + 64 * hh +
+                                      8 * c) = w;
         }
       }
+      __syncwarp();   // every lane has read the tiles before they are written again
     }
     if (store)
       p.lse[p.cu_seqlens ? (size_t)un.h * p.cu_seqlens[p.B] + un.tok0 + row : (size_t)bh * p.N + row] =
@@ -184,18 +220,22 @@ __device__ __forceinline__ void fp8_softmax_rows(const Fp8Params& p, SharedState
     ++units_done;
     u = u_next;
   }
+  // the TMA stores of O have completed before the kernel's shared memory goes
+  if (lane == 0) bulk_wait_all();
 }
 
 template <int D>
 __global__ void __launch_bounds__(kRowThreads, 1)
 attn_fp8_row_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_vt, const Fp8Params p) {
+                    const __grid_constant__ CUtensorMap tm_vt, const __grid_constant__ CUtensorMap tm_o,
+                    const Fp8Params p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ SharedState ss;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
   uint8_t* sRing = smem + kQTiles * kFp8TileBytes;
+  uint8_t* sStage = sRing + kFp8Stages * kFp8TileBytes;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   // the next call on the stream may start its CTAs (and their set-up) on the
   // SMs this grid leaves; it reads nothing before this grid has completed
@@ -254,7 +294,7 @@ attn_fp8_row_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     __syncwarp();
   } else {
     setmaxnreg_inc<kRowSoftmaxRegs>();
-    fp8_softmax_rows<D>(p, ss, tmem, warp / kRowGroupWarps);
+    fp8_softmax_rows<D>(p, ss, tmem, warp / kRowGroupWarps, sStage, &tm_o);
     __syncwarp();
   }
 

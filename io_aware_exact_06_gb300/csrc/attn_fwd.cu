@@ -1384,10 +1384,12 @@ int launch_fp8_attention(EncodeTiledFn enc, DeviceState* ds, int* list, const ui
   const int64_t np = T * attn::kBN;
   const int64_t bh = (int64_t)B * H;
   int st;
-  CUtensorMap mq, mk, mvt;
+  CUtensorMap mq, mk, mvt, mo;
   if ((st = make_map_fp8_rows(enc, &mq, q8, tokens, H)) != ATTN_OK) return st;
   if ((st = make_map_fp8_rows(enc, &mk, k8, tokens, H)) != ATTN_OK) return st;
   if ((st = make_map_fp8_vt(enc, &mvt, vt, bh, np, d)) != ATTN_OK) return st;
+  // O (bf16 [tokens, H, d]) through 32-row x 64-channel boxes: the epilogue's TMA stores
+  if ((st = make_map(enc, &mo, o, tokens, H, d, 32)) != ATTN_OK) return st;
   attn::Fp8Params p{};
   p.o = reinterpret_cast<__nv_bfloat16*>(o);
   p.lse = lse;
@@ -1416,9 +1418,9 @@ int launch_fp8_attention(EncodeTiledFn enc, DeviceState* ds, int* list, const ui
   // a programmatic dependent of the stream's previous kernel (the V
   // quantiser in attn_fwd_fp8): its set-up overlaps that kernel's last CTAs
   cudaError_t e = d == 64 ? launch_dependent(attn::attn_fp8_row_kernel<64>, grid, attn::kRowThreads,
-                                             attn::kFp8SmemBytes, s, mq, mk, mvt, p)
+                                             attn::kFp8SmemBytes, s, mq, mk, mvt, mo, p)
                           : launch_dependent(attn::attn_fp8_row_kernel<128>, grid, attn::kRowThreads,
-                                             attn::kFp8SmemBytes, s, mq, mk, mvt, p);
+                                             attn::kFp8SmemBytes, s, mq, mk, mvt, mo, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
