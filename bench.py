@@ -790,9 +790,8 @@ def fp8_cpu_baseline(wl, signs, budget_s: float = 10.0):
 
 # DRAM bytes (read + write) of one attn_fp8_row_kernel<128> launch of this
 # workload, from one ncu capture of the current kernel (None once it
-# changes): 160.61 MB read + 27.60 MB written (mean of the 15 launches of
-# the launch list).
-FP8_TRAFFIC_BYTES = 160_613_325 + 27_598_507
+# changes): 169.59 MB read + 33.15 MB written.
+FP8_TRAFFIC_BYTES = 169_592_320 + 33_148_672
 
 # DRAM bytes (read + write) of one backward call on this workload (all three
 # kernels), from one ncu capture of the current kernels (None once one of them
