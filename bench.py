@@ -90,6 +90,8 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.out = ""
+        self.settle_steps = 0
+        self.t_start = time.perf_counter()
 
     def __enter__(self):
         try:
@@ -97,10 +99,28 @@ class ClockSampler:
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            time.sleep(0.3)
         except OSError:
             self.proc = None
+        self.t_start = time.perf_counter()
         return self
+
+    def settle(self, step, dev, seconds: float = 0.3, busy: float = 0.02):
+        """Lets the sampler start (`seconds` after __enter__), the GPU idle
+        but for the last `busy` seconds, which run untimed steps: a GPU left
+        idle runs its next calls slower (a timed region of a few hundred µs
+        would see that), and a long busy stretch can bring the power cap into
+        a short timed region.  The steps' count is reported with the clocks."""
+        import torch
+        time.sleep(max(0.0, self.t_start + seconds - busy - time.perf_counter()))
+        t0 = time.perf_counter()
+        n = 0
+        while n < 3 or time.perf_counter() - t0 < busy:
+            step()
+            n += 1
+            if n % 8 == 0:
+                torch.cuda.synchronize(dev)  # a bounded queue of calls
+        torch.cuda.synchronize(dev)
+        self.settle_steps = n
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -129,9 +149,10 @@ class ClockSampler:
                 if val.lower() == "active":
                     reasons.add(name)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"],
+                    "settle_steps": self.settle_steps}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "settle_steps": self.settle_steps}
 
 
 def dist_setup():
@@ -288,9 +309,10 @@ def run_cuda(args, world, rank, local):
         raise RuntimeError("device error during warm-up")
 
     # device-timed region: inputs resident in HBM
-    barrier(world)
-    torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
+        clk.settle(step, dev)
+        barrier(world)
+        torch.cuda.synchronize(dev)
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
@@ -410,9 +432,10 @@ def run_decode(args, world, rank, local):
     torch.cuda.synchronize(dev)
     if fa.attn_last_device_error(stream) != 0:
         raise RuntimeError("device error during warm-up")
-    barrier(world)
-    torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
+        clk.settle(step, dev)
+        barrier(world)
+        torch.cuda.synchronize(dev)
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0.record(stream)
         for i in range(args.steps):
@@ -539,9 +562,10 @@ def run_bwd(args, world, rank, local):
     torch.cuda.synchronize(dev)
     if fa.attn_last_device_error(stream) != 0:
         raise RuntimeError("device error during warm-up")
-    barrier(world)
-    torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
+        clk.settle(step, dev)
+        barrier(world)
+        torch.cuda.synchronize(dev)
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0.record(stream)
         for i in range(args.steps):
@@ -661,9 +685,10 @@ def run_fp8(args, world, rank, local):
     torch.cuda.synchronize(dev)
     if fa.attn_last_device_error(stream) != 0:
         raise RuntimeError("device error during warm-up")
-    barrier(world)
-    torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
+        clk.settle(step, dev)
+        barrier(world)
+        torch.cuda.synchronize(dev)
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0.record(stream)
         for i in range(args.steps):
