@@ -430,8 +430,7 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* l
   if (opts && opts->max_ctas > 0 && opts->max_ctas < grid) grid = opts->max_ctas;
   const bool rows = one_thread_per_row(d, opts ? opts->kernel : 0);
   CUtensorMap mo = mq;
-  if (rows && (d == 64 ? attn::RowCfg<64>::kStageO : attn::RowCfg<128>::kStageO) &&
-      (st = make_map(enc, &mo, o, tokens_bound, H, d, 32)) != ATTN_OK)
+  if (rows && (st = make_map(enc, &mo, o, tokens_bound, H, d, 32)) != ATTN_OK)
     return st;
   return d == 64 ? launch_attn<64>(mq, mk, mv, mo, p, grid, s, rows)
                  : launch_attn<128>(mq, mk, mv, mo, p, grid, s, rows);
@@ -804,8 +803,7 @@ int attn_fwd_noalloc_impl(const void* q, const void* k, const void* v, void* o, 
   if (opts && opts->max_ctas > 0 && opts->max_ctas < grid) grid = opts->max_ctas;
   const bool rows = one_thread_per_row(d, opts ? opts->kernel : 0);
   CUtensorMap mo = mq;
-  if (rows && (d == 64 ? attn::RowCfg<64>::kStageO : attn::RowCfg<128>::kStageO) &&
-      (st = make_map(enc, &mo, o, tokens_bound, H, d, 32)) != ATTN_OK)
+  if (rows && (st = make_map(enc, &mo, o, tokens_bound, H, d, 32)) != ATTN_OK)
     return st;
   return d == 64 ? launch_attn<64>(mq, mk, mv, mo, p, grid, s, rows)
                  : launch_attn<128>(mq, mk, mv, mo, p, grid, s, rows);

@@ -57,14 +57,13 @@ template <int D>
 struct RowCfg {
   using C = FwdCfg<D>;
   static constexpr int kQBufs = D == 64 ? 2 : 1;
-  static constexpr bool kStageO = true;
   static constexpr int kStageWarpBytes = 32 * 128;               // 32 rows x 64 bf16
   static constexpr int kStageGroupBytes = 4 * kStageWarpBytes;   // a query tile's 4 warps
   static constexpr bool kSPre = D == 64;
   __host__ __device__ static constexpr uint32_t col_p(int g) {
     return kSPre ? 384u + 64u * (uint32_t)g : C::col_s(g);
   }
-  static constexpr int kSmemStage = kStageO ? kQTiles * kStageGroupBytes : 0;
+  static constexpr int kSmemStage = kQTiles * kStageGroupBytes;
   static constexpr int kSmemBytes = kQBufs * C::kSmemQ + C::kSmemRing + kSmemStage + 1024;
 };
 static_assert(RowCfg<64>::kSmemBytes + 1024 <= 227 * 1024, "shared memory of the d = 64 kernel");
@@ -346,7 +345,7 @@ __device__ __forceinline__ void softmax_rows(const FwdParams& p, SharedState& ss
     const float l_r = l + l_fix;
     const bool store = row >= nominal0 && row < cur_L && row >= 0;
     const float inv_l = l_r > 0.f ? 1.0f / l_r : 0.f;
-    if constexpr (RowCfg<D>::kStageO) {
+    {
       // This warp's 32 rows through its staging tile, 64 columns at a time:
       // the thread writes its row's 64 columns (16-byte chunk c of row r at
       // r * 128 + 16 (c ^ (r % 8)), no bank conflicts; the 128-byte swizzle
@@ -399,26 +398,6 @@ __device__ __forceinline__ void softmax_rows(const FwdParams& p, SharedState& ss
           __syncwarp();   // every lane has read the tile before it is written again
         }
       }
-    } else {
-      __nv_bfloat16* orow = p.o + ((size_t)(store ? cur_tok0 + row : 0) * p.H + cur_h) * D;
-#pragma unroll
-      for (int cc = 0; cc < D; cc += 32) {
-        uint32_t r[32];
-        tmem_ld_x32(lane_addr + colO + cc, r);
-        tmem_ld_wait_x32(r);
-        if (store) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + cc);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(r[8 * i + 0]) * inv_l, __uint_as_float(r[8 * i + 1]) * inv_l);
-            w.y = pack_bf16x2(__uint_as_float(r[8 * i + 2]) * inv_l, __uint_as_float(r[8 * i + 3]) * inv_l);
-            w.z = pack_bf16x2(__uint_as_float(r[8 * i + 4]) * inv_l, __uint_as_float(r[8 * i + 5]) * inv_l);
-            w.w = pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv_l, __uint_as_float(r[8 * i + 7]) * inv_l);
-            dst[i] = w;
-          }
-        }
-      }
     }
     if (store) {
       const float lse = l > 0.f ? m_used * p.scale + __log2f(l) * 0.69314718055994531f : -INFINITY;
@@ -434,7 +413,7 @@ __device__ __forceinline__ void softmax_rows(const FwdParams& p, SharedState& ss
     u = u_next;
   }
   // the TMA stores of O have completed before the kernel's shared memory goes
-  if (RowCfg<D>::kStageO && (threadIdx.x & 31) == 0) bulk_wait_all();
+  if ((threadIdx.x & 31) == 0) bulk_wait_all();
 }
 
 template <int D, int kMode>
