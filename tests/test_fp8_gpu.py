@@ -512,3 +512,31 @@ def test_fp8_packed_head_group_order_same_result(dev):
     ref_o, ref_l = oracle.attn_rows_f64(qd, kd, vd, cu, rows, scale / d, True)
     rel_d, lse_d = errors(go, gl, ref_o, ref_l)
     assert rel_d <= REL_DEQ and lse_d <= LSE_DEQ, (rel_d, lse_d)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_fp8_packed_outputs_stay_inside_their_rows(dev, d):
+    """As for the bf16 forward: O a view at the start of a larger buffer whose
+    tail holds a sentinel; the FP8 call's TMA stores and row-wise stores leave
+    the tail untouched, and O matches the unguarded call bit for bit."""
+    import torch
+    import io_aware_exact_06_gb300 as fa
+    lens = [129, 0, 256, 77, 384, 1, 200]
+    H, N = 2, max(lens)
+    cu, q, k, v = packed_inputs(3900 + d, lens, H, d=d)
+    total = int(cu[-1])
+    guard = 384
+    sentinel = 0x7F81
+    big = torch.full((total + guard, H, d), sentinel, dtype=torch.int16, device=dev)
+    o = big[:total].view(torch.bfloat16)
+    lse = torch.empty((H, total), dtype=torch.float32, device=dev)
+    qd, kd, vd, cud = to_dev(dev, q), to_dev(dev, k), to_dev(dev, v), cu_dev(dev, cu)
+    fa.attn_fwd_fp8(qd, kd, vd, o, lse, len(lens), H, N, d, d ** -0.5, True, None, cu_seqlens=cud)
+    assert fa.attn_last_device_error() == 0
+    assert bool((big[total:] == sentinel).all()), "rows past the packed tokens were written"
+    o2 = torch.empty_like(o)
+    lse2 = torch.empty_like(lse)
+    fa.attn_fwd_fp8(qd, kd, vd, o2, lse2, len(lens), H, N, d, d ** -0.5, True, None, cu_seqlens=cud)
+    assert fa.attn_last_device_error() == 0
+    assert torch.equal(o.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(lse, lse2)

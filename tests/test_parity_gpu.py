@@ -380,3 +380,28 @@ def test_packed_head_group_order_same_result(dev, d, causal):
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
     rows = inputs.sample_rows(wl.cu_seqlens, wl.H, 2048, seed=4547 + d)
     parity.compare(outs[1][0], outs[1][1], wl, rows, "packed head groups")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_packed_outputs_stay_inside_their_rows(dev, d, causal):
+    """O goes out through whole-tile TMA stores where a query tile lies
+    inside its sequence and row by row elsewhere: with O a view at the start
+    of a larger buffer whose tail holds a sentinel, every row of the packed
+    tokens matches the oracle and the tail is untouched (lengths whose last
+    tile is pulled back, shorter than a tile, or exactly whole)."""
+    import torch
+    import io_aware_exact_06_gb300 as fa
+    lens = [129, 0, 256, 77, 384, 1, 200]
+    wl = inputs.make_workload("guard", 5151 + d, lens, 2, d, causal, varlen=True)
+    q, k, v, cu = parity.to_device(wl, dev)
+    guard = 384
+    sentinel = 0x7F81  # a signalling-NaN bf16 bit pattern no kernel writes
+    big = torch.full((wl.tokens + guard, wl.H, d), sentinel, dtype=torch.int16, device=dev)
+    o = big[:wl.tokens].view(torch.bfloat16)
+    lse = torch.empty((wl.H, wl.tokens), dtype=torch.float32, device=dev)
+    N = max(lens)
+    fa.attn_fwd(q, k, v, o, lse, wl.nseq, wl.H, N, d, wl.scale, causal, cu)
+    assert fa.attn_last_device_error() == 0
+    assert bool((big[wl.tokens:] == sentinel).all()), "rows past the packed tokens were written"
+    parity.compare(o, lse, wl, inputs.all_rows(wl.cu_seqlens, wl.H), f"guard d={d}")
