@@ -442,19 +442,13 @@ fp8_quant_v_kernel(const __nv_bfloat16* v, const unsigned int* amax_bits, float*
     raw[i] = active && key0 + i < L
                  ? *reinterpret_cast<const uint2*>(v + ((size_t)(tok0 + key0 + i) * H + h) * D + 4 * lane)
                  : make_uint2(0u, 0u);
-  // max |V| of the sequence: the bit patterns of non-negative floats order
-  // as the floats do
-  __shared__ unsigned int red_v[8];
+  // max |V| of the sequence, by every warp on its own (a few words, in L2;
+  // no block barrier): the bit patterns of non-negative floats order as the
+  // floats do
   unsigned int mb = 0u;
   const int nblk = (L + kBM - 1) / kBM;
-  for (int i = threadIdx.x; i < nblk; i += 256) mb = max(mb, amax_bits[(size_t)bh * T + i]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, o));
-  if (lane == 0) red_v[warp] = mb;
-  __syncthreads();
-  mb = red_v[0];
-#pragma unroll
-  for (int w = 1; w < 8; ++w) mb = max(mb, red_v[w]);
+  for (int i = lane; i < nblk; i += 32) mb = max(mb, amax_bits[(size_t)bh * T + i]);
+  mb = __reduce_max_sync(0xffffffffu, mb);
   const float amax = __uint_as_float(mb);
   const float inv = amax > 0.f ? __fdiv_rn(kFp8Max, amax) : 1.0f;
   if (t == 0 && threadIdx.x == 0) sv[bh] = amax > 0.f ? __fdiv_rn(amax, kFp8Max) : 1.0f;
