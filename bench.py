@@ -827,13 +827,13 @@ BWD_TRAFFIC_BYTES = 135_279_104 + 3_500_032 + 329_993_472 + 101_385_728 + 392_99
 
 # DRAM bytes (read + write) of one attn_fwd_row_kernel<128> launch of this
 # workload, from one ncu capture of the current kernel (None once it changes).
-TRAFFIC_BYTES = 542_989_056 + 47_214_592  # 542.99 MB read + 47.21 MB written
+TRAFFIC_BYTES = 542_067_456 + 46_948_864  # 542.07 MB read + 46.95 MB written
 # The same for other forward workloads: attn_fwd_row_kernel<64> on the GPT-2
-# shaped one (37.82 MB read + 2 KB written: O, 12.6 MB, is still in L2
+# shaped one (37.82 MB read + 1.8 KB written: O, 12.6 MB, is still in L2
 # when the kernel ends) and attn_fwd_row_kernel<128> on the stress and the
 # packed ones.
-CONFIG_TRAFFIC_BYTES = {"gpt2_causal": 37_817_856 + 2_048, "stress": 262_001_408 + 52_552_448,
-                        "varlen": 1_985_222_400 + 464_122_880}
+CONFIG_TRAFFIC_BYTES = {"gpt2_causal": 37_819_648 + 1_792, "stress": 258_630_400 + 51_655_680,
+                        "varlen": 2_000_659_200 + 464_386_816}
 
 
 def main():
